@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Benchmark of the NHA layer operator (forward + backward) on GB300.
+
+One step = nha_forward + nha_backward over one batch of the chosen workload
+(default: the 1.3B-like layer, B4 H16 T2048 d128 m64 w512 C64, bf16), inputs
+resident in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl nha|reference]
+
+Multi-GPU: one process per GPU under torchrun; every rank runs the same
+per-GPU workload (heads are independent, so the work partitions over B x H
+with no collective); value = tokens of all ranks / the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle (the method's plain definition) on
+this machine's host cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NHA layer fwd and fwd+bwd tokens/s on 1 GB300; fraction of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def workloads():
+    from sliding_window_softmax_gb300 import synthetic as s
+
+    out = {"1.3B": s.LAYER_1P3B, "340M": s.LAYER_340M, "tiny": s.TINY_F32,
+           "1.3B-w0": s.LAYER_1P3B.with_(name="1.3B-like w=0", w=0),
+           "1.3B-wT": s.LAYER_1P3B.with_(name="1.3B-like w=T", w=2048)}
+    for T in s.LONG_CONTEXT_T:
+        out[f"long{T}"] = s.long_context(T)
+    for w in s.GRID_W:
+        for m in s.GRID_M:
+            out[f"grid-w{w}-m{m}"] = s.grid_point(w, m)
+    return out
+
+
+# ----------------------------------------------------------------------------------------
+# Algorithmic work model (per launch).
+def work_model(wl):
+    T, d, m = wl.T, wl.d, wl.m
+    w = min(wl.w, T)
+    R = max(0, T - w)
+    e = 2 if wl.dtype == "bf16" else 4
+    n_sum = sum(min(t + 1, w) for t in range(T)) if w > 0 else 0  # window keys per head
+    BH = wl.B * wl.H
+    fwd_flops = BH * (4 * d * n_sum + 8 * m * d * R)
+    fwd_bytes = BH * T * (4 * d * e + 4 * m + 4)
+    bwd_bytes = BH * T * (8 * d * e + 8 * m + 4)
+    k = {
+        # name: (flops, bytes) per launch
+        "fwd_main": (BH * (4 * d * n_sum + 4 * m * d * R), fwd_bytes),
+        "state_chunk": (BH * 4 * m * d * R, BH * R * (2 * d * e + 4 * m)),
+        "bwd_window_dq": (BH * 6 * d * n_sum, BH * T * (5 * d * e + 8)),
+        "bwd_window_dkdv": (BH * 8 * d * n_sum, BH * T * (6 * d * e + 8)),
+        "bwd_slot_query": (BH * 12 * m * d * R, BH * T * (3 * d * e + 4 * m + 8)),
+        "bwd_slot_key": (BH * 12 * m * d * R, BH * T * (6 * d * e + 8 * m)),
+    }
+    return dict(fwd_flops=fwd_flops, fwd_bytes=fwd_bytes, step_flops=3.5 * fwd_flops,
+                step_bytes=fwd_bytes + bwd_bytes, kernels=k, n_sum=n_sum, R=R)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sliding_window_softmax_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (lines `traffic <kernel> <workload> <hash> <bytes>`)."""
+    p = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(p):
+        return None
+    cur = source_hash()
+    with open(p) as f:
+        for line in f:
+            mm = re.match(r"\s*traffic\s+(\S+)\s+(\S+)\s+(\S+)\s+([0-9.eE+]+)", line)
+            if mm and mm.group(1) == kernel and mm.group(2) == workload_key and mm.group(3) == cur:
+                return float(mm.group(4))
+    return None
+
+
+# ----------------------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------
+def oracle_sample(wl, heads, nthreads):
+    """fwd + bwd of the fp64 oracle on `heads` heads (batch-major order); returns seconds."""
+    import torch
+
+    import oracle
+    from sliding_window_softmax_gb300.synthetic import make_inputs
+
+    x = make_inputs(wl)
+    idx = [(i // wl.H, i % wl.H) for i in range(heads)]
+    sel = {n: torch.stack([t[b, h] for b, h in idx])[None] for n, t in x.items()}
+    t0 = time.perf_counter()
+    oracle.forward(sel["q"], sel["k"], sel["v"], sel["log_alpha"], wl.w, nthreads=nthreads)
+    if wl.backward:
+        oracle.backward(sel["q"], sel["k"], sel["v"], sel["log_alpha"], sel["dout"], wl.w,
+                        nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, budget_s=20.0):
+    import oracle
+
+    cores = os.cpu_count() or 1
+    oracle.build()
+    t1 = oracle_sample(wl, 1, 1)
+    heads = int(min(wl.B * wl.H, cores * max(1, math.floor(budget_s / max(t1, 1e-3)))))
+    heads = max(1, min(heads, cores))
+    sec = oracle_sample(wl, heads, min(cores, heads))
+    tokens = heads * wl.T / wl.H  # a token is one position across all H heads
+    return {"value": tokens / sec, "unit": "tokens/s", "cores": min(cores, heads), "kind": "oracle",
+            "sample": f"{heads} of {wl.B * wl.H} heads of {wl.name}, "
+                      f"{'fwd+bwd' if wl.backward else 'fwd'}, fp64, {sec:.2f} s wall"}
+
+
+def run_reference(args, wl):
+    """The reference arm: the oracle on the host cores, bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    cores = os.cpu_count() or 1
+    oracle.build()
+    t1 = oracle_sample(wl, 1, 1)
+    per_step = 150.0 / max(1, args.steps + args.warmup + 1)
+    heads = max(1, min(cores, wl.B * wl.H, int(per_step / max(t1, 1e-3)) * cores))
+    nth = min(cores, heads)
+    for _ in range(args.warmup):
+        oracle_sample(wl, heads, nth)
+    times = [oracle_sample(wl, heads, nth) for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(times)
+    tokens = heads * wl.T / wl.H
+    val = tokens / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "T": wl.T, "d": wl.d,
+                       "m": wl.m, "w": wl.w, "C": wl.C, "pass": "fwd+bwd" if wl.backward else "fwd",
+                       "sample_heads": heads},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": nth, "kind": "oracle",
+                             "sample": f"{heads} of {wl.B * wl.H} heads per step"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------
+def run_nha(args, wl, wl_key):
+    import torch
+    import torch.distributed as dist
+
+    import sliding_window_softmax_gb300 as nha
+    from sliding_window_softmax_gb300.synthetic import make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    x = make_inputs(wl)
+    d = {n: t.to(dev) for n, t in x.items()}
+    B, H, T, D = d["q"].shape
+    o, lse = torch.empty_like(d["q"]), torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(d["q"]) for _ in range(3))
+    dla = torch.empty_like(d["log_alpha"])
+    wsf = torch.empty(max(1, nha.nha_workspace_bytes(B, H, T, D, wl.m, wl.w, wl.C, d["q"].dtype)),
+                      dtype=torch.uint8, device=dev)
+    wsb = torch.empty(max(1, nha.nha_workspace_bytes(B, H, T, D, wl.m, wl.w, wl.C, d["q"].dtype,
+                                                     backward=True)), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(fwd_evt=None):
+        nha.nha_forward(d["q"], d["k"], d["v"], d["log_alpha"], wl.w, wl.C, o=o, lse=lse,
+                        workspace=wsf, stream=stream)
+        if fwd_evt is not None:
+            fwd_evt.record(stream)
+        if wl.backward:
+            nha.nha_backward(d["q"], d["k"], d["v"], d["log_alpha"], o, lse, d["dout"], wl.w,
+                             wl.C, dq=dq, dk=dk, dv=dv, dlog_alpha=dla, workspace=wsb,
+                             stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with ClockSampler(local) as clk:
+        n0 = nha.launch_count()
+        nha.profile_begin()
+        for i in range(K):
+            flush.zero_()  # L2 flush between timed steps, outside the step's events
+            ev[i][0].record(stream)
+            step(ev[i][1])
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        prof = nha.profile_end()
+        launches = nha.launch_count() - n0
+    wall = time.perf_counter() - wall0
+    barrier()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    ms = statistics.mean(step_ms)
+    ms_fwd = statistics.mean(fwd_ms)
+    if world > 1:
+        t = torch.tensor([ms, ms_fwd], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_fwd = float(t[0]), float(t[1])
+
+    # ---- end to end through the public API with pinned host buffers
+    hin = {n: t.pin_memory() for n, t in x.items()}
+    hout = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+            for n, t in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv, dlog_alpha=dla).items()}
+    h2d = sum(t.numel() * t.element_size() for n, t in hin.items()
+              if wl.backward or n != "dout")
+    d2h = sum(t.numel() * t.element_size() for n, t in hout.items()
+              if wl.backward or n in ("o", "lse"))
+    outs = dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv, dlog_alpha=dla)
+
+    def e2e_step():
+        for n, t in hin.items():
+            if wl.backward or n != "dout":
+                d[n].copy_(t, non_blocking=True)
+        step()
+        for n, t in hout.items():
+            if wl.backward or n in ("o", "lse"):
+                t.copy_(outs[n], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    E = max(3, min(K, 10))
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(E)]
+    barrier()
+    for i in range(E):
+        flush.zero_()
+        e_ev[i][0].record(stream)
+        e2e_step()
+        e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e_ev)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+
+    if rank == 0:
+        model = work_model(wl)
+        peaks = load_peaks()
+        tokens = world * B * T
+        value = tokens / (ms / 1e3)
+        # dominant kernel by measured time share
+        name, (cnt, tot) = max(prof.items(), key=lambda kv: kv[1][1])
+        per_launch_ms = tot / cnt
+        flops, nbytes = model["kernels"].get(name, (model["step_flops"], model["step_bytes"]))
+        t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+        t_bw = nbytes / (peaks["hbm_gbs"] * 1e9)
+        if t_tc > t_bw:
+            roof = {"bound": "tensor", "achieved": flops / (per_launch_ms / 1e3) / 1e12,
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+        else:
+            roof = {"bound": "hbm", "achieved": nbytes / (per_launch_ms / 1e3) / 1e9,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["traffic"] = ncu_traffic(name, wl_key)
+        roof["kernel"] = name
+        roof["kernel_ms"] = per_launch_ms
+        roof["peak_source"] = peaks["source"]
+        total_prof = sum(v[1] for v in prof.values())
+        t_roof_step = max(model["step_flops"] / (peaks["bf16_tflops"] * 1e12),
+                          model["step_bytes"] / (peaks["hbm_gbs"] * 1e9)) if wl.backward else \
+            max(model["fwd_flops"] / (peaks["bf16_tflops"] * 1e12),
+                model["fwd_bytes"] / (peaks["hbm_gbs"] * 1e9))
+        t_roof_fwd = max(model["fwd_flops"] / (peaks["bf16_tflops"] * 1e12),
+                         model["fwd_bytes"] / (peaks["hbm_gbs"] * 1e9))
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "B": B, "H": H, "T": T, "d": D, "m": wl.m, "w": wl.w,
+                       "C": wl.C, "pass": "fwd+bwd" if wl.backward else "fwd",
+                       "l2": "flushed between timed steps (512 MB write)",
+                       "parallelism": f"replicas x{world} over B*H (no collective)"},
+            "fwd": {"ms": ms_fwd, "tokens_per_s": tokens / (ms_fwd / 1e3),
+                    "roofline_frac": t_roof_fwd / (ms_fwd / 1e3)},
+            "step_roofline_frac": t_roof_step / (ms / 1e3),
+            "roofline": roof,
+            "kernels": {k: {"launches": c, "ms_per_launch": t / c, "share": t / total_prof}
+                        for k, (c, t) in sorted(prof.items(), key=lambda kv: -kv[1][1])},
+            "gpu_launches": int(launches),
+            "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "ms_per_step": e2e_ms},
+            "clocks": clk.summary(),
+            "wall_s_timed_region": wall,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="1.3B")
+    ap.add_argument("--impl", default="nha", choices=["nha", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    wls = workloads()
+    if args.workload not in wls:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(wls)}")
+    wl = wls[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_nha(args, wl, args.workload)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,128 @@
+/*
+ * libnha -- Native Hybrid Attention (NHA) layer operator, forward and backward,
+ * for NVIDIA GB300 (sm_103a).  C ABI: plain pointers and sizes only.
+ *
+ * The operator ("Native Hybrid Attention for Efficient Sequence Modeling",
+ * Paper-Notes page, section 关键设计/层内混合, the K^long_t recurrence and the
+ * o_t = softmax(q_t K^H_t^T / sqrt(d)) V^H_t equation; "整体框架" for the
+ * memory shapes; the chunkwise form in section "Chunkwise 并行计算"):
+ *
+ *   per (b,h), tokens t = 0..T-1, slots i = 0..m-1,
+ *     alpha_t = exp(log_alpha_t),  u_t = 1 - alpha_t   (computed as -expm1)
+ *     long memory after token j:
+ *        K^long_j = Diag(alpha_j) K^long_{j-1} + u_j (x) k_j,  V^long likewise,
+ *        zero before token 0;
+ *     query t reads the long memory after token j = t - w (token shift: only
+ *     tokens that have left the window are absorbed); when t < w no token has
+ *     left yet and all m slot logits are masked;
+ *     slot logits   L_{t,i} = q_t . K^long_{t-w}[i] / sqrt(d)   (no position code)
+ *     window logits S_{t,s} = rope(q_t, t) . rope(k_s, s) / sqrt(d),
+ *                   s in [max(0, t-w+1), t]
+ *     p = one softmax over [L_t | S_t];  lse_t = log of its partition
+ *     o_t = sum_i p_{t,i} V^long_{t-w}[i] + sum_s p_{t,s} v_s
+ *   RoPE: rotate-half pairing (i, i + d/2), theta_i = rope_base^(-2i/d),
+ *   absolute 0-based positions.  w = 0 is a pure gated-slot RNN; w >= T is
+ *   causal softmax attention (w > T is treated as T).
+ *
+ * Layout: q, k, v, o, dout, dq, dk, dv are contiguous row-major [B, H, T, d]
+ * in the element type `dtype`; log_alpha and dlog_alpha are [B, H, T, m] fp32;
+ * lse is [B, H, T] fp32.  Every pointer is a DEVICE pointer, 16-byte aligned.
+ *
+ * Supported: d in {64, 128}; m in {16, 32, 64}; C == 64 (the chunk length of
+ * the chunkwise-parallel form; results depend on C only through rounding);
+ * 0 <= T <= 262144; w >= 0; B*H*T*max(d,m) < 2^31.
+ * Numerical range: within any chunk of C consecutive tokens, the per-slot sum
+ * of log_alpha must be >= -160 (the intra-chunk gate factorisation is exact in
+ * fp32 only inside that range).
+ *
+ * Ownership: the caller allocates every buffer, including the workspace
+ * (size from nha_workspace_bytes).  The library never allocates or frees
+ * device memory and never synchronises; all work is enqueued on `stream`
+ * (a cudaStream_t; NULL means the legacy default stream).  Outputs are fully
+ * overwritten, never accumulated.
+ *
+ * Errors: every entry point returns a status and never throws.  Arguments are
+ * validated before anything is enqueued; a failed launch maps to
+ * NHA_ERR_CUDA.  Faults inside kernels surface at the caller's next
+ * synchronisation.  nha_last_error() gives a thread-local message for the
+ * last failing call on this thread.
+ *
+ * Re-entrancy: reentrant; the only process-wide state is lazily set kernel
+ * attributes.  Calls on different streams with different workspaces may run
+ * concurrently.
+ */
+#ifndef NHA_H_
+#define NHA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NHA_OK = 0,
+    NHA_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, negative size, bad enum */
+    NHA_ERR_UNSUPPORTED = 2,      /* valid but outside the supported d, m, C, T set */
+    NHA_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required */
+    NHA_ERR_CUDA = 4,             /* a CUDA runtime call or kernel launch failed */
+    NHA_ERR_INTERNAL = 5          /* host-side fault injection or an internal check */
+} nha_status_t;
+
+typedef enum { NHA_DTYPE_F32 = 0, NHA_DTYPE_BF16 = 1 } nha_dtype_t;
+
+/* Bytes of device workspace nha_forward (backward = 0) or nha_backward
+ * (backward = 1) needs for this shape.  Returns 0 for an invalid or
+ * unsupported shape (nha_forward / nha_backward then report why). */
+size_t nha_workspace_bytes(int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dtype,
+                           int backward);
+
+/* Forward.  Writes o [B,H,T,d] (dtype) and lse [B,H,T] (fp32, natural log of
+ * the softmax partition, kept for nha_backward). */
+nha_status_t nha_forward(const void* q, const void* k, const void* v, const float* log_alpha,
+                         void* o, float* lse, int B, int H, int T, int d, int m, int w, int C,
+                         nha_dtype_t dtype, float rope_base, void* workspace, size_t ws_bytes,
+                         void* stream);
+
+/* Backward of loss = <o, dout>.  Takes the forward's o and lse.  Writes
+ * dq, dk, dv [B,H,T,d] (dtype; gradients w.r.t. the un-rotated q and k) and
+ * dlog_alpha [B,H,T,m] (fp32). */
+nha_status_t nha_backward(const void* q, const void* k, const void* v, const float* log_alpha,
+                          const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                          void* dv, float* dlog_alpha, int B, int H, int T, int d, int m, int w,
+                          int C, nha_dtype_t dtype, float rope_base, void* workspace,
+                          size_t ws_bytes, void* stream);
+
+/* ---- Instrumentation (the pages have no counterpart; used by the benchmark) ---- */
+
+/* Number of kernels this library has launched in this process so far. */
+unsigned long long nha_launch_count(void);
+
+typedef struct {
+    char name[64];    /* kernel name */
+    int launches;     /* launches recorded in the session */
+    double total_ms;  /* sum of their CUDA-event durations */
+} nha_profile_record_t;
+
+/* Opens a profiling session: until nha_profile_end, every kernel launch is
+ * bracketed by CUDA events recorded on its own stream (this adds two event
+ * records per launch).  Process-wide; not for concurrent sessions. */
+nha_status_t nha_profile_begin(void);
+
+/* Closes the session, waits for its events and writes up to `cap`
+ * per-kernel records to `out`.  Returns the number of distinct kernels seen,
+ * or -1 if an event could not be read. */
+int nha_profile_end(nha_profile_record_t* out, int cap);
+
+/* Static description of a status code. */
+const char* nha_status_string(nha_status_t status);
+
+/* Message of the last failing call on the calling thread ("" if none). */
+const char* nha_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NHA_H_ */

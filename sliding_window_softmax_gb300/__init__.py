@@ -1,0 +1,21 @@
+"""Native Hybrid Attention (NHA) layer operator for NVIDIA GB300 (sm_103a).
+
+The operator ("Native Hybrid Attention for Efficient Sequence Modeling",
+Paper-Notes page, section 关键设计/层内混合): m gated linear-RNN key/value
+slots fed only by tokens that have left a causal sliding window of w tokens,
+the window itself with RoPE, and one 1/sqrt(d) softmax over all m + w keys.
+Forward and backward run in the hand-written CUDA kernels of ``libnha.so``
+behind the C ABI of ``include/nha.h``; this package is the thin binding.
+"""
+from ._binding import (  # noqa: F401
+    EXPORTS,
+    LIB_PATH,
+    NHAError,
+    launch_count,
+    load_library,
+    nha_backward,
+    nha_forward,
+    nha_workspace_bytes,
+    profile_begin,
+    profile_end,
+)

@@ -1,0 +1,191 @@
+"""ctypes binding of libnha.so (argument marshalling only: every step of the
+operator runs in the library's CUDA kernels).
+
+The names mirror the C ABI in ``include/nha.h``: :func:`nha_forward`,
+:func:`nha_backward`, :func:`nha_workspace_bytes`.  Tensors are PyTorch CUDA
+tensors (PyTorch supplies device memory and the stream); nothing here computes
+any part of the operator, and there is no fallback: if the library is missing
+or the call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libnha.so")
+
+NHA_OK = 0
+STATUS = {0: "NHA_OK", 1: "NHA_ERR_INVALID_ARGUMENT", 2: "NHA_ERR_UNSUPPORTED",
+          3: "NHA_ERR_WORKSPACE", 4: "NHA_ERR_CUDA", 5: "NHA_ERR_INTERNAL"}
+DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+
+# Every symbol include/nha.h declares (checked by the tests).
+EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward", "nha_launch_count",
+           "nha_profile_begin", "nha_profile_end", "nha_status_string", "nha_last_error")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ProfileRecord(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 64), ("launches", ctypes.c_int),
+                ("total_ms", ctypes.c_double)]
+
+
+def launch_count() -> int:
+    """Kernels libnha has launched in this process."""
+    return int(load_library().nha_launch_count())
+
+
+def profile_begin() -> None:
+    """Start bracketing every libnha kernel launch with CUDA events."""
+    _raise(load_library(), load_library().nha_profile_begin())
+
+
+def profile_end() -> dict:
+    """End the session: {kernel name: (launches, total ms)}."""
+    lib = load_library()
+    recs = (ProfileRecord * 64)()
+    n = lib.nha_profile_end(recs, 64)
+    if n < 0:
+        raise RuntimeError("nha_profile_end could not read its CUDA events")
+    return {recs[i].name.decode(): (recs[i].launches, recs[i].total_ms) for i in range(min(n, 64))}
+
+
+class NHAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libnha.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"libnha.so not found at {p}: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(there is no CPU fallback)")
+        lib = ctypes.CDLL(p)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.nha_workspace_bytes.restype = sz
+        lib.nha_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i]
+        lib.nha_forward.restype = i
+        lib.nha_forward.argtypes = [vp] * 6 + [i] * 8 + [f, vp, sz, vp]
+        lib.nha_backward.restype = i
+        lib.nha_backward.argtypes = [vp] * 11 + [i] * 8 + [f, vp, sz, vp]
+        lib.nha_status_string.restype = ctypes.c_char_p
+        lib.nha_status_string.argtypes = [i]
+        lib.nha_last_error.restype = ctypes.c_char_p
+        lib.nha_last_error.argtypes = []
+        lib.nha_launch_count.restype = ctypes.c_ulonglong
+        lib.nha_launch_count.argtypes = []
+        lib.nha_profile_begin.restype = i
+        lib.nha_profile_begin.argtypes = []
+        lib.nha_profile_end.restype = i
+        lib.nha_profile_end.argtypes = [ctypes.POINTER(ProfileRecord), i]
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _raise(lib, rc):
+    if rc != NHA_OK:
+        raise NHAError(rc, lib.nha_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(name, t, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def nha_workspace_bytes(B, H, T, d, m, w, C=64, dtype=torch.bfloat16, backward=False) -> int:
+    lib = load_library()
+    return int(lib.nha_workspace_bytes(B, H, T, d, m, w, C, DTYPE[dtype], int(bool(backward))))
+
+
+def nha_forward(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 10000.0,
+                o=None, lse=None, workspace=None, stream=None):
+    """o, lse = nha_forward(q, k, v, log_alpha, w).  q, k, v [B,H,T,d]; log_alpha [B,H,T,m] fp32."""
+    lib = load_library()
+    B, H, T, d = q.shape
+    m = log_alpha.shape[-1]
+    dt = q.dtype
+    if dt not in DTYPE:
+        raise TypeError(f"unsupported dtype {dt}")
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check(n, t, dt, (B, H, T, d))
+    _check("log_alpha", log_alpha, torch.float32, (B, H, T, m))
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    _check("o", o, dt, (B, H, T, d))
+    _check("lse", lse, torch.float32, (B, H, T))
+    need = int(lib.nha_workspace_bytes(B, H, T, d, m, w, C, DTYPE[dt], 0))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.nha_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(lse),
+                         B, H, T, d, m, int(w), int(C), DTYPE[dt], float(rope_base),
+                         _ptr(workspace), ws_bytes, _stream_handle(stream))
+    _raise(lib, rc)
+    return o, lse
+
+
+def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
+                 rope_base: float = 10000.0, dq=None, dk=None, dv=None, dlog_alpha=None,
+                 workspace=None, stream=None):
+    """dq, dk, dv, dlog_alpha = nha_backward(q, k, v, log_alpha, o, lse, dout, w)."""
+    lib = load_library()
+    B, H, T, d = q.shape
+    m = log_alpha.shape[-1]
+    dt = q.dtype
+    if dt not in DTYPE:
+        raise TypeError(f"unsupported dtype {dt}")
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check(n, t, dt, (B, H, T, d))
+    _check("log_alpha", log_alpha, torch.float32, (B, H, T, m))
+    _check("lse", lse, torch.float32, (B, H, T))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    dlog_alpha = torch.empty_like(log_alpha) if dlog_alpha is None else dlog_alpha
+    for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check(n, t, dt, (B, H, T, d))
+    _check("dlog_alpha", dlog_alpha, torch.float32, (B, H, T, m))
+    need = int(lib.nha_workspace_bytes(B, H, T, d, m, w, C, DTYPE[dt], 1))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.nha_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(lse),
+                          _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dlog_alpha),
+                          B, H, T, d, m, int(w), int(C), DTYPE[dt], float(rope_base),
+                          _ptr(workspace), ws_bytes, _stream_handle(stream))
+    _raise(lib, rc)
+    return dq, dk, dv, dlog_alpha

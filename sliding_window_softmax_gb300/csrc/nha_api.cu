@@ -1,0 +1,244 @@
+// C-ABI layer of libnha: argument validation, workspace planning, RoPE
+// frequency tables and the launch sequence on the caller's stream.
+// Declarations and the full contract are in include/nha.h.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "nha.h"
+#include "nha_kernels.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+nha_status_t fail(nha_status_t s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+nha_status_t ok() {
+    g_err[0] = '\0';
+    return NHA_OK;
+}
+
+// Host-side fault injection for tests: NHA_FAULT_INJECT=<site> makes the call
+// fail with NHA_ERR_INTERNAL at that step, before anything is enqueued there.
+bool inject(const char* site) {
+    const char* e = getenv("NHA_FAULT_INJECT");
+    return e != nullptr && strcmp(e, site) == 0;
+}
+
+constexpr int kMaxT = 1 << 18;
+
+struct Plan {
+    nha::Shape sh;
+    int d, m;
+    // workspace offsets, in floats
+    size_t SK, SV, G, Dv, dqw, dkw, dvw, DL, PL, DB1, RK, RV, TOT, total;
+};
+
+nha_status_t check_shape(int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dt) {
+    if (B < 0 || H < 0 || T < 0 || w < 0 || d <= 0 || m <= 0 || C <= 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "negative or zero size (B=%d H=%d T=%d d=%d m=%d w=%d C=%d)",
+                    B, H, T, d, m, w, C);
+    if (dt != NHA_DTYPE_F32 && dt != NHA_DTYPE_BF16)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "unknown dtype %d", (int)dt);
+    if (d != 64 && d != 128) return fail(NHA_ERR_UNSUPPORTED, "head dim d=%d not in {64, 128}", d);
+    if (m != 16 && m != 32 && m != 64) return fail(NHA_ERR_UNSUPPORTED, "slots m=%d not in {16, 32, 64}", m);
+    if (C != nha::kChunk) return fail(NHA_ERR_UNSUPPORTED, "chunk C=%d unsupported (only %d)", C, nha::kChunk);
+    if (T > kMaxT) return fail(NHA_ERR_UNSUPPORTED, "T=%d above the supported %d", T, kMaxT);
+    long long elems = (long long)B * H * T * (d > m ? d : m);
+    if (elems >= (1LL << 31)) return fail(NHA_ERR_UNSUPPORTED, "B*H*T*max(d,m)=%lld >= 2^31", elems);
+    return NHA_OK;
+}
+
+Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward) {
+    Plan p;
+    memset(&p, 0, sizeof(p));
+    p.d = d;
+    p.m = m;
+    nha::Shape& sh = p.sh;
+    sh.BH = B * H;
+    sh.T = T;
+    sh.w = w < T ? w : T;
+    sh.R = T - sh.w;
+    sh.NC = (sh.R + nha::kChunk - 1) / nha::kChunk;
+    sh.NL = (sh.w + nha::kChunk - 1) / nha::kChunk;
+    sh.NKT = (T + nha::kChunk - 1) / nha::kChunk;
+    sh.sigma = (float)(1.0 / sqrt((double)d));
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        size_t o = off;
+        off += (n + 63) & ~(size_t)63;  // keep every sub-buffer 256-byte aligned
+        return o;
+    };
+    const size_t BH = (size_t)sh.BH, NC = (size_t)sh.NC, Tz = (size_t)T;
+    p.SK = take(BH * NC * m * d);
+    p.SV = take(BH * NC * m * d);
+    p.G = take(BH * NC * m);
+    if (backward) {
+        p.Dv = take(BH * Tz);
+        p.dqw = take(BH * Tz * d);
+        p.dkw = take(BH * Tz * d);
+        p.dvw = take(BH * Tz * d);
+        p.DL = take(BH * NC * nha::kChunk * m);
+        p.PL = take(BH * NC * nha::kChunk * m);
+        p.DB1 = take(BH * NC * nha::kChunk * m);
+        p.RK = take(BH * NC * m * d);
+        p.RV = take(BH * NC * m * d);
+        p.TOT = take(BH * NC * m);
+    }
+    p.total = off;
+    return p;
+}
+
+void make_rope(nha::RopeTab& rt, int d, float base) {
+    memset(&rt, 0, sizeof(rt));
+    for (int i = 0; i < d / 2; i++) {
+        double f = pow((double)base, -2.0 * i / d) / M_PI;  // theta_i / pi
+        int e;
+        double mant = frexp(f, &e);                            // f = mant * 2^e, mant in [0.5, 1)
+        double hi = ldexp(nearbyint(mant * 64.0) / 64.0, e);   // 6 significant bits
+        rt.f_hi[i] = (float)hi;
+        rt.f_lo[i] = (float)(f - hi);
+    }
+}
+
+bool misaligned(const void* p) { return ((uintptr_t)p & 15u) != 0; }
+
+template <typename Tin>
+cudaError_t run_forward(const Plan& p, const nha::FwdArgs& a, cudaStream_t s) {
+    switch (p.d * 1000 + p.m) {
+        case 64016: return nha::simt_forward<Tin, 64, 16>(a, s);
+        case 64032: return nha::simt_forward<Tin, 64, 32>(a, s);
+        case 64064: return nha::simt_forward<Tin, 64, 64>(a, s);
+        case 128016: return nha::simt_forward<Tin, 128, 16>(a, s);
+        case 128032: return nha::simt_forward<Tin, 128, 32>(a, s);
+        case 128064: return nha::simt_forward<Tin, 128, 64>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename Tin>
+cudaError_t run_backward(const Plan& p, const nha::BwdArgs& a, cudaStream_t s) {
+    switch (p.d * 1000 + p.m) {
+        case 64016: return nha::simt_backward<Tin, 64, 16>(a, s);
+        case 64032: return nha::simt_backward<Tin, 64, 32>(a, s);
+        case 64064: return nha::simt_backward<Tin, 64, 64>(a, s);
+        case 128016: return nha::simt_backward<Tin, 128, 16>(a, s);
+        case 128032: return nha::simt_backward<Tin, 128, 32>(a, s);
+        case 128064: return nha::simt_backward<Tin, 128, 64>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t nha_workspace_bytes(int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dtype,
+                           int backward) {
+    if (check_shape(B, H, T, d, m, w, C, dtype) != NHA_OK) return 0;
+    Plan p = make_plan(B, H, T, d, m, w, backward != 0);
+    return p.total * sizeof(float);
+}
+
+nha_status_t nha_forward(const void* q, const void* k, const void* v, const float* log_alpha,
+                         void* o, float* lse, int B, int H, int T, int d, int m, int w, int C,
+                         nha_dtype_t dtype, float rope_base, void* workspace, size_t ws_bytes,
+                         void* stream) {
+    if (inject("validate")) return fail(NHA_ERR_INTERNAL, "fault injected at validate");
+    nha_status_t st = check_shape(B, H, T, d, m, w, C, dtype);
+    if (st != NHA_OK) return st;
+    if (!(rope_base > 1.0f) || !isfinite(rope_base))
+        return fail(NHA_ERR_INVALID_ARGUMENT, "rope_base must be a finite value > 1");
+    if ((long long)B * H * T == 0) return ok();
+    const void* ptrs[] = {q, k, v, log_alpha, o, lse};
+    const char* names[] = {"q", "k", "v", "log_alpha", "o", "lse"};
+    for (int i = 0; i < 6; i++) {
+        if (ptrs[i] == nullptr) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is NULL", names[i]);
+        if (misaligned(ptrs[i])) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", names[i]);
+    }
+    Plan p = make_plan(B, H, T, d, m, w, false);
+    const size_t need = p.total * sizeof(float);
+    if (need > 0 && (workspace == nullptr || ws_bytes < need))
+        return fail(NHA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? ws_bytes : (size_t)0);
+    if (need > 0 && misaligned(workspace))
+        return fail(NHA_ERR_INVALID_ARGUMENT, "workspace is not 16-byte aligned");
+    if (inject("forward_launch")) return fail(NHA_ERR_INTERNAL, "fault injected at forward_launch");
+    float* ws = (float*)workspace;
+    nha::FwdArgs a;
+    a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.o = o; a.lse = lse;
+    a.SK = ws + p.SK; a.SV = ws + p.SV; a.G = ws + p.G;
+    a.sh = p.sh;
+    make_rope(a.rope, d, rope_base);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = dtype == NHA_DTYPE_F32 ? run_forward<float>(p, a, s)
+                                           : run_forward<__nv_bfloat16>(p, a, s);
+    if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "forward launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+nha_status_t nha_backward(const void* q, const void* k, const void* v, const float* log_alpha,
+                          const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                          void* dv, float* dlog_alpha, int B, int H, int T, int d, int m, int w,
+                          int C, nha_dtype_t dtype, float rope_base, void* workspace,
+                          size_t ws_bytes, void* stream) {
+    if (inject("validate")) return fail(NHA_ERR_INTERNAL, "fault injected at validate");
+    nha_status_t st = check_shape(B, H, T, d, m, w, C, dtype);
+    if (st != NHA_OK) return st;
+    if (!(rope_base > 1.0f) || !isfinite(rope_base))
+        return fail(NHA_ERR_INVALID_ARGUMENT, "rope_base must be a finite value > 1");
+    if ((long long)B * H * T == 0) return ok();
+    const void* ptrs[] = {q, k, v, log_alpha, o, lse, dout, dq, dk, dv, dlog_alpha};
+    const char* names[] = {"q", "k", "v", "log_alpha", "o", "lse", "dout", "dq", "dk", "dv", "dlog_alpha"};
+    for (int i = 0; i < 11; i++) {
+        if (ptrs[i] == nullptr) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is NULL", names[i]);
+        if (misaligned(ptrs[i])) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", names[i]);
+    }
+    Plan p = make_plan(B, H, T, d, m, w, true);
+    const size_t need = p.total * sizeof(float);
+    if (workspace == nullptr || ws_bytes < need)
+        return fail(NHA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? ws_bytes : (size_t)0);
+    if (misaligned(workspace)) return fail(NHA_ERR_INVALID_ARGUMENT, "workspace is not 16-byte aligned");
+    if (inject("backward_launch")) return fail(NHA_ERR_INTERNAL, "fault injected at backward_launch");
+    float* ws = (float*)workspace;
+    nha::BwdArgs a;
+    a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.o = o; a.lse = lse; a.dout = dout;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dla = dlog_alpha;
+    a.SK = ws + p.SK; a.SV = ws + p.SV; a.G = ws + p.G; a.Dv = ws + p.Dv;
+    a.dqw = ws + p.dqw; a.dkw = ws + p.dkw; a.dvw = ws + p.dvw;
+    a.wsDL = ws + p.DL; a.wsPL = ws + p.PL; a.wsDB1 = ws + p.DB1;
+    a.RK = ws + p.RK; a.RV = ws + p.RV; a.TOT = ws + p.TOT;
+    a.sh = p.sh;
+    make_rope(a.rope, d, rope_base);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = dtype == NHA_DTYPE_F32 ? run_backward<float>(p, a, s)
+                                           : run_backward<__nv_bfloat16>(p, a, s);
+    if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "backward launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+const char* nha_status_string(nha_status_t status) {
+    switch (status) {
+        case NHA_OK: return "NHA_OK";
+        case NHA_ERR_INVALID_ARGUMENT: return "NHA_ERR_INVALID_ARGUMENT";
+        case NHA_ERR_UNSUPPORTED: return "NHA_ERR_UNSUPPORTED";
+        case NHA_ERR_WORKSPACE: return "NHA_ERR_WORKSPACE";
+        case NHA_ERR_CUDA: return "NHA_ERR_CUDA";
+        case NHA_ERR_INTERNAL: return "NHA_ERR_INTERNAL";
+    }
+    return "NHA_ERR_UNKNOWN";
+}
+
+const char* nha_last_error(void) { return g_err; }
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// Internal interface between the C-ABI layer (nha_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "nha_common.cuh"
+
+namespace nha {
+
+// Forward arguments.  q, k, v, o are [BH, T, D] in the element type; la is
+// [BH, T, M]; lse [BH, T].  Workspace: SK, SV [BH, NC, M, D] and G [BH, NC, M].
+struct FwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* la;
+    void* o;
+    float* lse;
+    float* SK;
+    float* SV;
+    float* G;
+    Shape sh;
+    RopeTab rope;
+};
+
+// Backward arguments.  Workspace beyond the forward's: Dv [BH, T];
+// dqw, dkw, dvw [BH, T, D] (window-branch partial gradients, fp32);
+// wsDL, wsPL, wsDB1 [BH, NC * C, M]; RK, RV [BH, NC, M, D]; TOT [BH, NC, M].
+struct BwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* la;
+    const void* o;
+    const float* lse;
+    const void* dout;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* dla;
+    float* SK;
+    float* SV;
+    float* G;
+    float* Dv;
+    float* dqw;
+    float* dkw;
+    float* dvw;
+    float* wsDL;
+    float* wsPL;
+    float* wsDB1;
+    float* RK;
+    float* RV;
+    float* TOT;
+    Shape sh;
+    RopeTab rope;
+};
+
+template <typename Tin, int D, int M>
+cudaError_t simt_forward(const FwdArgs& a, cudaStream_t st);
+template <typename Tin, int D, int M>
+cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st);
+
+}  // namespace nha

@@ -1,0 +1,129 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every symbol include/nha.h declares, and validates arguments before it
+enqueues anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sliding_window_softmax_gb300 as nha
+from sliding_window_softmax_gb300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    __graft_entry__.build_library()
+    return nha.load_library()
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "nha.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b(nha_[a-z_]+)\s*\(", src))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_symbols()
+    assert declared == set(_binding.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_workspace_bytes(lib):
+    f = lib.nha_workspace_bytes
+    assert f(1, 2, 256, 64, 16, 32, 64, 0, 0) > 0
+    assert f(1, 2, 256, 64, 16, 32, 64, 0, 1) > f(1, 2, 256, 64, 16, 32, 64, 0, 0)
+    assert f(1, 2, 256, 64, 16, 256, 64, 0, 0) == 0  # w >= T: no slot states
+    assert f(1, 2, 256, 96, 16, 32, 64, 0, 0) == 0  # unsupported d
+    assert f(1, 2, 256, 64, 16, 32, 32, 0, 0) == 0  # unsupported C
+    assert f(-1, 2, 256, 64, 16, 32, 64, 0, 0) == 0
+    # grows linearly in T (chunked states, no T^2 term)
+    a = f(1, 1, 4096, 128, 64, 512, 64, 1, 1)
+    b = f(1, 1, 8192, 128, 64, 512, 64, 1, 1)
+    assert 1.9 < b / a < 2.2
+
+
+def _fwd(lib, q=1, **kw):
+    args = dict(B=1, H=1, T=16, d=64, m=16, w=4, C=64, dt=1, base=10000.0, ws=None, ws_bytes=0)
+    args.update(kw)
+    p = ctypes.c_void_p(q * 4096) if q else None  # never dereferenced: validation fails first
+    return lib.nha_forward(p, p, p, p, p, p, args["B"], args["H"], args["T"], args["d"], args["m"],
+                           args["w"], args["C"], args["dt"], args["base"], args["ws"],
+                           args["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=96), 2), (dict(m=8), 2), (dict(C=128), 2), (dict(T=(1 << 18) + 1), 2),
+    (dict(w=-1), 1), (dict(B=-2), 1), (dict(dt=7), 1), (dict(base=0.0), 1),
+    (dict(base=float("nan")), 1), (dict(m=0), 1),
+])
+def test_forward_rejects_bad_arguments(lib, kw, status):
+    assert _fwd(lib, **kw) == status
+    assert lib.nha_last_error()
+
+
+def test_forward_null_and_misaligned_and_workspace(lib):
+    assert _fwd(lib, q=0) == 1 and b"NULL" in lib.nha_last_error()
+    p = ctypes.c_void_p(4096 + 4)
+    rc = lib.nha_forward(p, p, p, p, p, p, 1, 1, 16, 64, 16, 4, 64, 1, 10000.0, None, 0, None)
+    assert rc == 1 and b"aligned" in lib.nha_last_error()
+    # valid pointers but no workspace where one is needed (w < T)
+    assert _fwd(lib) == 3 and b"workspace" in lib.nha_last_error()
+    # the library only checks the size: too small by one byte is rejected too
+    need = lib.nha_workspace_bytes(1, 1, 16, 64, 16, 4, 64, 1, 0)
+    assert _fwd(lib, ws=ctypes.c_void_p(1 << 20), ws_bytes=need - 1) == 3
+
+
+def test_empty_inputs_are_a_no_op(lib):
+    # B*H*T == 0: nothing to do, NULL pointers allowed, no CUDA call made
+    assert _fwd(lib, q=0, T=0) == 0
+    assert _fwd(lib, q=0, B=0) == 0
+    assert lib.nha_backward(*([None] * 11), 1, 1, 0, 64, 16, 4, 64, 1, 10000.0, None, 0, None) == 0
+
+
+def test_backward_validation(lib):
+    p = ctypes.c_void_p(4096)
+    ptrs = [p] * 11
+    assert lib.nha_backward(*ptrs, 1, 1, 16, 64, 16, 4, 64, 1, 10000.0, None, 0, None) == 3
+    ptrs[6] = None
+    assert lib.nha_backward(*ptrs, 1, 1, 16, 64, 16, 4, 64, 1, 10000.0, None, 0, None) == 1
+    assert b"dout" in lib.nha_last_error()
+
+
+def test_status_strings(lib):
+    for code, name in _binding.STATUS.items():
+        assert lib.nha_status_string(code).decode() == name
+
+
+def test_fault_injection_on_host(lib, monkeypatch):
+    monkeypatch.setenv("NHA_FAULT_INJECT", "validate")
+    assert _fwd(lib) == 5 and b"injected" in lib.nha_last_error()
+    monkeypatch.setenv("NHA_FAULT_INJECT", "forward_launch")
+    need = lib.nha_workspace_bytes(1, 1, 16, 64, 16, 4, 64, 1, 0)
+    # validation passes, the injected failure stops the call before any launch
+    assert _fwd(lib, ws=ctypes.c_void_p(1 << 20), ws_bytes=need) == 5
+    monkeypatch.delenv("NHA_FAULT_INJECT")
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    import torch
+
+    x = torch.zeros(1, 1, 8, 64)
+    with pytest.raises(TypeError):
+        nha.nha_forward(x, x, x, torch.zeros(1, 1, 8, 16), w=2)
+
+
+def test_product_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "sliding_window_softmax_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if not f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                continue
+            src = open(os.path.join(dirpath, f), errors="ignore").read()
+            assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
+            assert "nha_oracle" not in src, f
