@@ -40,7 +40,7 @@ struct Plan {
     nha::Shape sh;
     int d, m;
     // workspace offsets, in floats
-    size_t SK, SV, G, Dv, dqw, dkw, dvw, DL, PL, DB1, RK, RV, TOT, total;
+    size_t SK, SV, G, TAB, STATUS, Dv, dqw, dkw, dvw, DL, PL, DB1, RK, RV, TOT, total;
 };
 
 nha_status_t check_shape(int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dt) {
@@ -82,6 +82,8 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward) {
     p.SK = take(BH * NC * m * d);
     p.SV = take(BH * NC * m * d);
     p.G = take(BH * NC * m);
+    p.TAB = take(Tz * (size_t)d);  // RoPE (cos, sin) per position and frequency
+    p.STATUS = take(16);
     if (backward) {
         p.Dv = take(BH * Tz);
         p.dqw = take(BH * Tz * d);
@@ -111,6 +113,20 @@ void make_rope(nha::RopeTab& rt, int d, float base) {
 }
 
 bool misaligned(const void* p) { return ((uintptr_t)p & 15u) != 0; }
+
+cudaError_t run_forward_tc(const Plan& p, const nha::FwdArgs& a, float* ws, cudaStream_t s) {
+    float2* tab = (float2*)(ws + p.TAB);
+    int* status = (int*)(ws + p.STATUS);
+    switch (p.d * 1000 + p.m) {
+        case 64016: return nha::tc_forward<64, 16>(a, tab, status, s);
+        case 64032: return nha::tc_forward<64, 32>(a, tab, status, s);
+        case 64064: return nha::tc_forward<64, 64>(a, tab, status, s);
+        case 128016: return nha::tc_forward<128, 16>(a, tab, status, s);
+        case 128032: return nha::tc_forward<128, 32>(a, tab, status, s);
+        case 128064: return nha::tc_forward<128, 64>(a, tab, status, s);
+    }
+    return cudaErrorInvalidValue;
+}
 
 template <typename Tin>
 cudaError_t run_forward(const Plan& p, const nha::FwdArgs& a, cudaStream_t s) {
@@ -180,8 +196,7 @@ nha_status_t nha_forward(const void* q, const void* k, const void* v, const floa
     a.sh = p.sh;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = dtype == NHA_DTYPE_F32 ? run_forward<float>(p, a, s)
-                                           : run_forward<__nv_bfloat16>(p, a, s);
+    cudaError_t e = dtype == NHA_DTYPE_F32 ? run_forward<float>(p, a, s) : run_forward_tc(p, a, ws, s);
     if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "forward launch failed: %s", cudaGetErrorString(e));
     return ok();
 }

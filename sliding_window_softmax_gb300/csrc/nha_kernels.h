@@ -57,7 +57,14 @@ struct BwdArgs {
 };
 
 template <typename Tin, int D, int M>
+cudaError_t simt_states(const Tin* k, const Tin* v, const float* la, float* SK, float* SV, float* G,
+                        const Shape& sh, cudaStream_t st);
+template <typename Tin, int D, int M>
 cudaError_t simt_forward(const FwdArgs& a, cudaStream_t st);
+// bf16 tensor-core forward; tab: RoPE (cos, sin) table [T][D/2] in the workspace,
+// status: device word set non-zero if a kernel gave up waiting on its tensor core.
+template <int D, int M>
+cudaError_t tc_forward(const FwdArgs& a, float2* tab, int* status, cudaStream_t st);
 template <typename Tin, int D, int M>
 cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st);
 

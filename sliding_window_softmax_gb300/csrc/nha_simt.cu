@@ -729,7 +729,7 @@ static cudaError_t set_smem(K kernel, size_t bytes) {
     } while (0)
 
 template <typename Tin, int D, int M>
-static cudaError_t simt_states(const Tin* k, const Tin* v, const float* la, float* SK, float* SV,
+cudaError_t simt_states(const Tin* k, const Tin* v, const float* la, float* SK, float* SV,
                                float* G, const Shape& sh, cudaStream_t st) {
     if (sh.NC == 0) return cudaSuccess;
     constexpr int LX = D + 1, LG = M + 1;
@@ -810,6 +810,8 @@ cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st) {
 }
 
 #define NHA_INST(Tin, D, M)                                                          \
+    template cudaError_t simt_states<Tin, D, M>(const Tin*, const Tin*, const float*, float*, \
+                                                float*, float*, const Shape&, cudaStream_t); \
     template cudaError_t simt_forward<Tin, D, M>(const FwdArgs&, cudaStream_t);      \
     template cudaError_t simt_backward<Tin, D, M>(const BwdArgs&, cudaStream_t);
 
