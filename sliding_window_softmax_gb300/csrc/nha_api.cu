@@ -141,6 +141,20 @@ cudaError_t run_forward(const Plan& p, const nha::FwdArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
 }
 
+cudaError_t run_backward_tc(const Plan& p, const nha::BwdArgs& a, float* ws, cudaStream_t s) {
+    float2* tab = (float2*)(ws + p.TAB);
+    int* status = (int*)(ws + p.STATUS);
+    switch (p.d * 1000 + p.m) {
+        case 64016: return nha::tc_backward<64, 16>(a, tab, status, s);
+        case 64032: return nha::tc_backward<64, 32>(a, tab, status, s);
+        case 64064: return nha::tc_backward<64, 64>(a, tab, status, s);
+        case 128016: return nha::tc_backward<128, 16>(a, tab, status, s);
+        case 128032: return nha::tc_backward<128, 32>(a, tab, status, s);
+        case 128064: return nha::tc_backward<128, 64>(a, tab, status, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 template <typename Tin>
 cudaError_t run_backward(const Plan& p, const nha::BwdArgs& a, cudaStream_t s) {
     switch (p.d * 1000 + p.m) {
@@ -236,8 +250,7 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
     a.sh = p.sh;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = dtype == NHA_DTYPE_F32 ? run_backward<float>(p, a, s)
-                                           : run_backward<__nv_bfloat16>(p, a, s);
+    cudaError_t e = dtype == NHA_DTYPE_F32 ? run_backward<float>(p, a, s) : run_backward_tc(p, a, ws, s);
     if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "backward launch failed: %s", cudaGetErrorString(e));
     return ok();
 }

@@ -21,15 +21,10 @@
 #include "nha_kernels.h"
 #include "nha_prof.h"
 #include "nha_tc.cuh"
+#include "nha_tc_tiles.cuh"
 
 namespace nha {
 using namespace tc;
-
-constexpr int kTcThreads = 256;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr long long kWaitCycles = 1LL << 32;  // about 2 s at 2 GHz
-constexpr int kStatusTimeout = 1;
 
 __global__ void rope_table_kernel(float2* __restrict__ tab, int T, int H2, RopeTab rt) {
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -37,146 +32,6 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, int T, int H2, RopeT
     float c, s;
     rope_cs(rt, e / H2, e % H2, c, s);
     tab[e] = make_float2(c, s);
-}
-
-__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        float2 t = __bfloat1622float2(h[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
-}
-
-__device__ __forceinline__ uint4 pack8(const float* f) {
-    uint4 u;
-    u.x = pack_bf16(f[0], f[1]);
-    u.y = pack_bf16(f[2], f[3]);
-    u.z = pack_bf16(f[4], f[5]);
-    u.w = pack_bf16(f[6], f[7]);
-    return u;
-}
-
-// Rotate 8 (x, y) pairs by the angles whose (cos, sin) are at cs[0..7].
-__device__ __forceinline__ void rotate8(float* x, float* y, const float2* __restrict__ cs) {
-    const float4* c4 = reinterpret_cast<const float4*>(cs);
-#pragma unroll
-    for (int q = 0; q < 4; q++) {
-        const float4 t = c4[q];
-        float a = x[2 * q], b = y[2 * q];
-        x[2 * q] = a * t.x - b * t.y;
-        y[2 * q] = b * t.x + a * t.y;
-        a = x[2 * q + 1];
-        b = y[2 * q + 1];
-        x[2 * q + 1] = a * t.z - b * t.w;
-        y[2 * q + 1] = b * t.z + a * t.w;
-    }
-}
-
-// Rows [row0, row0 + n) of a [T][D] bf16 tensor into a 128-row swizzled tile;
-// rows >= n are zero.  With tab != nullptr the rows are rotated by RoPE at
-// absolute positions row0 + r.
-template <int D>
-__device__ void load_tile(const __nv_bfloat16* __restrict__ src, int row0, int n, unsigned char* tile,
-                          const float2* __restrict__ tab) {
-    constexpr int CH = D / 8, H = D / 2, CHH = CH / 2;
-    if (tab == nullptr) {
-        for (int e = threadIdx.x; e < 128 * CH; e += kTcThreads) {
-            const int r = e / CH, ch = e % CH;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < n) v = __ldg(reinterpret_cast<const uint4*>(src + (size_t)(row0 + r) * D + ch * 8));
-            *reinterpret_cast<uint4*>(tile + sw_chunk(r, ch, 128)) = v;
-        }
-    } else {
-        for (int e = threadIdx.x; e < 128 * CHH; e += kTcThreads) {
-            const int r = e / CHH, ch = e % CHH;
-            uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-            if (r < n) {
-                const __nv_bfloat16* row = src + (size_t)(row0 + r) * D;
-                float x[8], y[8];
-                unpack8(__ldg(reinterpret_cast<const uint4*>(row + ch * 8)), x);
-                unpack8(__ldg(reinterpret_cast<const uint4*>(row + H + ch * 8)), y);
-                rotate8(x, y, tab + (size_t)(row0 + r) * H + ch * 8);
-                lo = pack8(x);
-                hi = pack8(y);
-            }
-            *reinterpret_cast<uint4*>(tile + sw_chunk(r, ch, 128)) = lo;
-            *reinterpret_cast<uint4*>(tile + sw_chunk(r, ch + CHH, 128)) = hi;
-        }
-    }
-}
-
-// Rotate rows [0, n) of a 128-row tile in place (positions row0 + r).
-template <int D>
-__device__ void rotate_tile(unsigned char* tile, int row0, int n, const float2* __restrict__ tab) {
-    constexpr int H = D / 2, CHH = D / 16;
-    for (int e = threadIdx.x; e < 128 * CHH; e += kTcThreads) {
-        const int r = e / CHH, ch = e % CHH;
-        if (r >= n) continue;
-        uint4* plo = reinterpret_cast<uint4*>(tile + sw_chunk(r, ch, 128));
-        uint4* phi = reinterpret_cast<uint4*>(tile + sw_chunk(r, ch + CHH, 128));
-        float x[8], y[8];
-        unpack8(*plo, x);
-        unpack8(*phi, y);
-        rotate8(x, y, tab + (size_t)(row0 + r) * H + ch * 8);
-        *plo = pack8(x);
-        *phi = pack8(y);
-    }
-}
-
-// [S1; S2] (fp32 [M][D] each, S2 may be null = zeros) into a 2M-row bf16 tile.
-template <int D, int M>
-__device__ void load_state_pair(const float* __restrict__ S1, const float* __restrict__ S2,
-                                unsigned char* tile) {
-    constexpr int CH = D / 8;
-    for (int e = threadIdx.x; e < 2 * M * CH; e += kTcThreads) {
-        const int r = e / CH, ch = e % CH;
-        const float* src = r < M ? S1 + (size_t)r * D : (S2 ? S2 + (size_t)(r - M) * D : nullptr);
-        float f[8];
-        if (src) {
-            const float4 a = __ldg(reinterpret_cast<const float4*>(src + ch * 8));
-            const float4 b = __ldg(reinterpret_cast<const float4*>(src + ch * 8 + 4));
-            f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-            f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; i++) f[i] = 0.0f;
-        }
-        *reinterpret_cast<uint4*>(tile + sw_chunk(r, ch, 2 * M)) = pack8(f);
-    }
-}
-
-// Store n (multiple of 8) fp32 values as bf16 into row `row` of a 128-row tile
-// starting at column col0 (multiple of 8).
-__device__ __forceinline__ void store_row(unsigned char* tile, int row, int col0, const float* v, int n) {
-    for (int c = 0; c < n; c += 8)
-        *reinterpret_cast<uint4*>(tile + sw_chunk(row, (col0 + c) >> 3, 128)) = pack8(v + c);
-}
-
-struct TcCtl {
-    uint64_t* bar;
-    uint32_t phase;
-    int* s_abort;
-    int* status;
-    // Wait for the MMAs committed last; uniform across the CTA; false on timeout.
-    __device__ bool wait() {
-        const bool ok = mbar_wait(bar, phase, kWaitCycles);
-        phase ^= 1u;
-        fence_after_sync();
-        if (__syncthreads_or(!ok)) {
-            if (threadIdx.x == 0) atomicExch(status, kStatusTimeout);
-            return false;
-        }
-        return true;
-    }
-};
-
-__device__ __forceinline__ void sync_for_mma() {
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
 }
 
 template <int D, int M>
@@ -483,6 +338,12 @@ fwd_tc_kernel(const FwdArgs a, const float2* __restrict__ tab, int* __restrict__
     if (warp == 0) tmem_dealloc(tm, 256);
 }
 
+cudaError_t launch_rope_table(float2* tab, int T, int H2, const RopeTab& rt, cudaStream_t st) {
+    const int n = T * H2;
+    NHA_LAUNCH("rope_table", st, rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(tab, T, H2, rt));
+    return cudaGetLastError();
+}
+
 template <int D, int M>
 size_t tc_fwd_smem() {
     return 1024 + 128 * D * 2 + 32768 + 32768 + 2 * M * D * 2 + sizeof(float) * (2 * 128 * M + 2 * M + 512);
@@ -494,9 +355,7 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, int* status, cudaStream_t 
     cudaError_t e = simt_states<__nv_bfloat16, D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
                                                      a.la, a.SK, a.SV, a.G, sh, st);
     if (e != cudaSuccess) return e;
-    const int n = sh.T * (D / 2);
-    NHA_LAUNCH("rope_table", st, rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(tab, sh.T, D / 2, a.rope));
-    e = cudaGetLastError();
+    e = launch_rope_table(tab, sh.T, D / 2, a.rope, st);
     if (e != cudaSuccess) return e;
     const int W0 = sh.T - sh.R;
     const int tiles = (W0 + 127) / 128 + (sh.R + 127) / 128;

@@ -67,5 +67,14 @@ template <int D, int M>
 cudaError_t tc_forward(const FwdArgs& a, float2* tab, int* status, cudaStream_t st);
 template <typename Tin, int D, int M>
 cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st);
+// Slot-branch backward (query side, reverse adjoint scan, key side, dlog_alpha
+// carry); expects the window-branch partials dqw, dkw, dvw and Dv in place.
+template <typename Tin, int D, int M>
+cudaError_t simt_bwd_slot(const BwdArgs& a, cudaStream_t st);
+// bf16 backward: window branch on the tensor core, then the slot branch.
+template <int D, int M>
+cudaError_t tc_backward(const BwdArgs& a, float2* tab, int* status, cudaStream_t st);
+// RoPE (cos, sin) table [T][H2] of the absolute positions.
+cudaError_t launch_rope_table(float2* tab, int T, int H2, const RopeTab& rt, cudaStream_t st);
 
 }  // namespace nha

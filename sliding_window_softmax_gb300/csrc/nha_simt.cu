@@ -758,29 +758,9 @@ cudaError_t simt_forward(const FwdArgs& a, cudaStream_t st) {
 }
 
 template <typename Tin, int D, int M>
-cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st) {
+cudaError_t simt_bwd_slot(const BwdArgs& a, cudaStream_t st) {
     const Shape& sh = a.sh;
     constexpr int LX = D + 1, LP = kChunk + 1, LG = M + 1;
-    NHA_CHECK(simt_states<Tin, D, M>((const Tin*)a.k, (const Tin*)a.v, a.la, a.SK, a.SV, a.G, sh, st));
-    const long rows = (long)sh.BH * sh.T;
-    NHA_LAUNCH("bwd_rowdot", st,
-               bwd_rowdot_kernel<Tin, D><<<(unsigned)((rows + 7) / 8), kThreads, 0, st>>>(
-                   (const Tin*)a.o, (const Tin*)a.dout, a.Dv, rows));
-    NHA_CHECK(cudaGetLastError());
-    {
-        size_t sm = sizeof(float) * (size_t)(4 * kChunk * LX + kChunk * LP);
-        auto kern = bwd_window_dq_kernel<Tin, D, M>;
-        NHA_CHECK(set_smem(kern, sm));
-        NHA_LAUNCH("bwd_window_dq", st, kern<<<dim3(sh.NKT, sh.BH), kThreads, sm, st>>>(a));
-        NHA_CHECK(cudaGetLastError());
-    }
-    {
-        size_t sm = sizeof(float) * (size_t)(4 * kChunk * LX + 2 * kChunk * LP + 2 * kChunk);
-        auto kern = bwd_window_dkdv_kernel<Tin, D, M>;
-        NHA_CHECK(set_smem(kern, sm));
-        NHA_LAUNCH("bwd_window_dkdv", st, kern<<<dim3(sh.NKT, sh.BH), kThreads, sm, st>>>(a));
-        NHA_CHECK(cudaGetLastError());
-    }
     {
         size_t sm = sizeof(float) * (size_t)(4 * kChunk * LX + kChunk * LP + 4 * kChunk * LG + 2 * M);
         auto kern = bwd_slot_query_kernel<Tin, D, M>;
@@ -809,11 +789,39 @@ cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st) {
     return cudaSuccess;
 }
 
+template <typename Tin, int D, int M>
+cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st) {
+    const Shape& sh = a.sh;
+    constexpr int LX = D + 1, LP = kChunk + 1;
+    NHA_CHECK(simt_states<Tin, D, M>((const Tin*)a.k, (const Tin*)a.v, a.la, a.SK, a.SV, a.G, sh, st));
+    const long rows = (long)sh.BH * sh.T;
+    NHA_LAUNCH("bwd_rowdot", st,
+               bwd_rowdot_kernel<Tin, D><<<(unsigned)((rows + 7) / 8), kThreads, 0, st>>>(
+                   (const Tin*)a.o, (const Tin*)a.dout, a.Dv, rows));
+    NHA_CHECK(cudaGetLastError());
+    {
+        size_t sm = sizeof(float) * (size_t)(4 * kChunk * LX + kChunk * LP);
+        auto kern = bwd_window_dq_kernel<Tin, D, M>;
+        NHA_CHECK(set_smem(kern, sm));
+        NHA_LAUNCH("bwd_window_dq", st, kern<<<dim3(sh.NKT, sh.BH), kThreads, sm, st>>>(a));
+        NHA_CHECK(cudaGetLastError());
+    }
+    {
+        size_t sm = sizeof(float) * (size_t)(4 * kChunk * LX + 2 * kChunk * LP + 2 * kChunk);
+        auto kern = bwd_window_dkdv_kernel<Tin, D, M>;
+        NHA_CHECK(set_smem(kern, sm));
+        NHA_LAUNCH("bwd_window_dkdv", st, kern<<<dim3(sh.NKT, sh.BH), kThreads, sm, st>>>(a));
+        NHA_CHECK(cudaGetLastError());
+    }
+    return simt_bwd_slot<Tin, D, M>(a, st);
+}
+
 #define NHA_INST(Tin, D, M)                                                          \
     template cudaError_t simt_states<Tin, D, M>(const Tin*, const Tin*, const float*, float*, \
                                                 float*, float*, const Shape&, cudaStream_t); \
     template cudaError_t simt_forward<Tin, D, M>(const FwdArgs&, cudaStream_t);      \
-    template cudaError_t simt_backward<Tin, D, M>(const BwdArgs&, cudaStream_t);
+    template cudaError_t simt_backward<Tin, D, M>(const BwdArgs&, cudaStream_t);    \
+    template cudaError_t simt_bwd_slot<Tin, D, M>(const BwdArgs&, cudaStream_t);
 
 #define NHA_INST_D(Tin, D) NHA_INST(Tin, D, 16) NHA_INST(Tin, D, 32) NHA_INST(Tin, D, 64)
 NHA_INST_D(float, 64)

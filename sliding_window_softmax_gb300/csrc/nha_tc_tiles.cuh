@@ -1,0 +1,188 @@
+// Shared-memory tile movers and synchronisation helpers of the tcgen05
+// kernels (bf16 operands in the 128B-swizzled layout of nha_tc.cuh).
+#pragma once
+
+#include "nha_common.cuh"
+#include "nha_tc.cuh"
+
+namespace nha {
+using namespace tc;
+
+constexpr int kTcThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr long long kWaitCycles = 1LL << 32;  // about 2 s at 2 GHz
+constexpr int kStatusTimeout = 1;
+
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+    uint4 u;
+    u.x = pack_bf16(f[0], f[1]);
+    u.y = pack_bf16(f[2], f[3]);
+    u.z = pack_bf16(f[4], f[5]);
+    u.w = pack_bf16(f[6], f[7]);
+    return u;
+}
+
+// Rotate 8 (x, y) pairs; c[q] holds (cos, sin) of pairs 2q and 2q + 1.
+__device__ __forceinline__ void rotate8v(float* x, float* y, const float4 (&c)[4]) {
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const float4 t = c[q];
+        float a = x[2 * q], b = y[2 * q];
+        x[2 * q] = a * t.x - b * t.y;
+        y[2 * q] = b * t.x + a * t.y;
+        a = x[2 * q + 1];
+        b = y[2 * q + 1];
+        x[2 * q + 1] = a * t.z - b * t.w;
+        y[2 * q + 1] = b * t.z + a * t.w;
+    }
+}
+
+// Rotate 8 (x, y) pairs by the angles whose (cos, sin) are at cs[0..7].
+__device__ __forceinline__ void rotate8(float* x, float* y, const float2* __restrict__ cs) {
+    const float4* c4 = reinterpret_cast<const float4*>(cs);
+    float4 c[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) c[q] = __ldg(c4 + q);
+    rotate8v(x, y, c);
+}
+
+// Rows [row0, row0 + n) of a [T][D] bf16 tensor into a 128-row swizzled tile;
+// rows >= n are zero.  With tab != nullptr the rows are rotated by RoPE at
+// absolute positions row0 + r.  Every thread issues all of its global loads
+// before it stores anything, so the load latency is paid once per tile.
+template <int D>
+__device__ void load_tile(const __nv_bfloat16* __restrict__ src, int row0, int n, unsigned char* tile,
+                          const float2* __restrict__ tab) {
+    constexpr int CH = D / 8, H = D / 2, CHH = CH / 2;
+    if (tab == nullptr) {
+        constexpr int IT = 128 * CH / kTcThreads;
+        uint4 buf[IT];
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            const int e = threadIdx.x + it * kTcThreads, r = e / CH, ch = e % CH;
+            buf[it] = r < n ? __ldg(reinterpret_cast<const uint4*>(src + (size_t)(row0 + r) * D + ch * 8))
+                            : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            const int e = threadIdx.x + it * kTcThreads, r = e / CH, ch = e % CH;
+            *reinterpret_cast<uint4*>(tile + sw_chunk(r, ch, 128)) = buf[it];
+        }
+    } else {
+        constexpr int IT = 128 * CHH / kTcThreads;
+        uint4 bx[IT], by[IT];
+        float4 cs[IT][4];
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            const int e = threadIdx.x + it * kTcThreads, r = e / CHH, ch = e % CHH;
+            if (r < n) {
+                const __nv_bfloat16* row = src + (size_t)(row0 + r) * D;
+                bx[it] = __ldg(reinterpret_cast<const uint4*>(row + ch * 8));
+                by[it] = __ldg(reinterpret_cast<const uint4*>(row + H + ch * 8));
+                const float4* c4 = reinterpret_cast<const float4*>(tab + (size_t)(row0 + r) * H + ch * 8);
+#pragma unroll
+                for (int qq = 0; qq < 4; qq++) cs[it][qq] = __ldg(c4 + qq);
+            } else {
+                bx[it] = by[it] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int qq = 0; qq < 4; qq++) cs[it][qq] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            const int e = threadIdx.x + it * kTcThreads, r = e / CHH, ch = e % CHH;
+            float x[8], y[8];
+            unpack8(bx[it], x);
+            unpack8(by[it], y);
+            rotate8v(x, y, cs[it]);
+            *reinterpret_cast<uint4*>(tile + sw_chunk(r, ch, 128)) = pack8(x);
+            *reinterpret_cast<uint4*>(tile + sw_chunk(r, ch + CHH, 128)) = pack8(y);
+        }
+    }
+}
+
+// Rotate rows [0, n) of a 128-row tile in place (positions row0 + r).
+template <int D>
+__device__ void rotate_tile(unsigned char* tile, int row0, int n, const float2* __restrict__ tab) {
+    constexpr int H = D / 2, CHH = D / 16;
+    for (int e = threadIdx.x; e < 128 * CHH; e += kTcThreads) {
+        const int r = e / CHH, ch = e % CHH;
+        if (r >= n) continue;
+        uint4* plo = reinterpret_cast<uint4*>(tile + sw_chunk(r, ch, 128));
+        uint4* phi = reinterpret_cast<uint4*>(tile + sw_chunk(r, ch + CHH, 128));
+        float x[8], y[8];
+        unpack8(*plo, x);
+        unpack8(*phi, y);
+        rotate8(x, y, tab + (size_t)(row0 + r) * H + ch * 8);
+        *plo = pack8(x);
+        *phi = pack8(y);
+    }
+}
+
+// [S1; S2] (fp32 [M][D] each, S2 may be null = zeros) into a 2M-row bf16 tile.
+template <int D, int M>
+__device__ void load_state_pair(const float* __restrict__ S1, const float* __restrict__ S2,
+                                unsigned char* tile) {
+    constexpr int CH = D / 8;
+    for (int e = threadIdx.x; e < 2 * M * CH; e += kTcThreads) {
+        const int r = e / CH, ch = e % CH;
+        const float* src = r < M ? S1 + (size_t)r * D : (S2 ? S2 + (size_t)(r - M) * D : nullptr);
+        float f[8];
+        if (src) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(src + ch * 8));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(src + ch * 8 + 4));
+            f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+            f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) f[i] = 0.0f;
+        }
+        *reinterpret_cast<uint4*>(tile + sw_chunk(r, ch, 2 * M)) = pack8(f);
+    }
+}
+
+// Store n (multiple of 8) fp32 values as bf16 into row `row` of a 128-row tile
+// starting at column col0 (multiple of 8).
+__device__ __forceinline__ void store_row(unsigned char* tile, int row, int col0, const float* v, int n) {
+    for (int c = 0; c < n; c += 8)
+        *reinterpret_cast<uint4*>(tile + sw_chunk(row, (col0 + c) >> 3, 128)) = pack8(v + c);
+}
+
+struct TcCtl {
+    uint64_t* bar;
+    uint32_t phase;
+    int* s_abort;
+    int* status;
+    // Wait for the MMAs committed last; uniform across the CTA; false on timeout.
+    __device__ bool wait() {
+        const bool ok = mbar_wait(bar, phase, kWaitCycles);
+        phase ^= 1u;
+        fence_after_sync();
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) atomicExch(status, kStatusTimeout);
+            return false;
+        }
+        return true;
+    }
+};
+
+__device__ __forceinline__ void sync_for_mma() {
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+}
+
+
+}  // namespace nha
