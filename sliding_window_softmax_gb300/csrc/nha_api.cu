@@ -40,7 +40,7 @@ struct Plan {
     nha::Shape sh;
     int d, m;
     // workspace offsets, in floats
-    size_t SK, SV, G, TAB, STATUS, Dv, dqw, dkw, dvw, DL, PL, DB1, RK, RV, TOT, total;
+    size_t SK, SV, G, TAB, STATUS, Dv, Dhat, Dwin, dqwV, dqw, dkw, dvw, DL, PL, DB1, RK, RV, total;
 };
 
 nha_status_t check_shape(int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dt) {
@@ -86,6 +86,9 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward) {
     p.STATUS = take(16);
     if (backward) {
         p.Dv = take(BH * Tz);
+        p.Dhat = take(BH * Tz);
+        p.Dwin = take(BH * Tz);
+        p.dqwV = take(BH * Tz * d);
         p.dqw = take(BH * Tz * d);
         p.dkw = take(BH * Tz * d);
         p.dvw = take(BH * Tz * d);
@@ -94,7 +97,6 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward) {
         p.DB1 = take(BH * NC * nha::kChunk * m);
         p.RK = take(BH * NC * m * d);
         p.RV = take(BH * NC * m * d);
-        p.TOT = take(BH * NC * m);
     }
     p.total = off;
     return p;
@@ -244,9 +246,10 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
     a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.o = o; a.lse = lse; a.dout = dout;
     a.dq = dq; a.dk = dk; a.dv = dv; a.dla = dlog_alpha;
     a.SK = ws + p.SK; a.SV = ws + p.SV; a.G = ws + p.G; a.Dv = ws + p.Dv;
+    a.Dhat = ws + p.Dhat; a.Dwin = ws + p.Dwin; a.dqwV = ws + p.dqwV;
     a.dqw = ws + p.dqw; a.dkw = ws + p.dkw; a.dvw = ws + p.dvw;
     a.wsDL = ws + p.DL; a.wsPL = ws + p.PL; a.wsDB1 = ws + p.DB1;
-    a.RK = ws + p.RK; a.RV = ws + p.RV; a.TOT = ws + p.TOT;
+    a.RK = ws + p.RK; a.RV = ws + p.RV;
     a.sh = p.sh;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;

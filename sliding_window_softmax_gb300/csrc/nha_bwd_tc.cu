@@ -5,10 +5,17 @@
 // dS = P o (dout V^T - D):
 //   dq~ = sigma dS K~,   dk~ = sigma dS^T Q~,   dv = P^T dout
 // in rotated coordinates, then dq = R_t^T dq~ and dk = R_s^T dk~.
-// Two kernels, no atomics: a query-major one (dq, and D_t for the other) and
-// a key-major one (dk, dv), each recomputing S and dP on the tensor core.
-// Results are the window branch's fp32 partial gradients; the slot branch
-// adds its own parts and writes the final outputs.
+// Two kernels, no atomics: a query-major one (dq) and a key-major one
+// (dk, dv), each recomputing S and dP on the tensor core.
+// D_t is needed exactly: the dlog_alpha reverse cumsum sums terms whose total
+// is zero (the loss sees the cumulative gates only through differences), so
+// an error in D from the bf16-rounded o accumulates along the sequence.  The
+// query-major kernel therefore forms dS with D^ = dout . o_bf16, and also
+// accumulates sum_s P dP (the window part of the exact D) and sum_s P k~; the
+// slot-branch query kernel adds the slot part of D and corrects
+// dq += sigma (D^ - D) R^T sum_s P k~.  The key-major kernel runs afterwards
+// with the exact D.  Results are the window branch's fp32 partial gradients;
+// the slot branch adds its own parts and writes the final outputs.
 #include "nha_common.cuh"
 #include "nha_kernels.h"
 #include "nha_prof.h"
@@ -81,8 +88,9 @@ bwd_wdq_tc_kernel(const BwdArgs a, const float2* __restrict__ tab, int* __restri
     unsigned char* X1 = X0 + TB;  // K~ block
     unsigned char* X2 = X1 + TB;  // V block
     unsigned char* X3 = X2 + TB;  // dout tile
-    unsigned char* X4 = X3 + TB;  // dS [128 q][128 keys]
-    float* red = reinterpret_cast<float*>(X4 + 32768);  // [2][128]
+    unsigned char* X4 = X3 + TB;      // dS [128 q][128 keys]
+    unsigned char* X5 = X4 + 32768;   // P  [128 q][128 keys]
+    float* red = reinterpret_cast<float*>(X5 + 32768);  // [2][128]
     __shared__ uint64_t bar;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -114,9 +122,10 @@ bwd_wdq_tc_kernel(const BwdArgs a, const float2* __restrict__ tab, int* __restri
     fence_after_sync();
     const uint32_t tm = s_tmem;
     const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t tS = 0, tP = 128, tQ = 256;
-    const float Dr = red[r] + red[128 + r];
-    if (h == 0 && row_ok) a.Dv[hoff + t] = Dr;
+    const uint32_t tS = 0, tP = 128, tQ = 256, tV = 384;
+    const float Dr = red[r] + red[128 + r];  // from the bf16 o
+    if (h == 0 && row_ok) a.Dhat[hoff + t] = Dr;
+    float dwin = 0.0f;
     const float lse2 = row_ok ? a.lse[hoff + t] * kLog2e : 0.0f;
     TcCtl ctl{&bar, 0u, &s_abort, status};
     bool ok = true, acc = false;
@@ -146,14 +155,20 @@ bwd_wdq_tc_kernel(const BwdArgs a, const float2* __restrict__ tab, int* __restri
                 const int c = 64 * h + jj, key = kb + c;
                 const bool valid = row_ok && c < nk && key <= t && key > t - sh.w;
                 const float p = valid ? ex2(sv[jj] * sig2 - lse2) : 0.0f;
+                dwin += p * dp[jj];
                 sv[jj] = p * (dp[jj] - Dr);
+                dp[jj] = p;
             }
             store_row(X4, r, 64 * h, sv, 64);
+            store_row(X5, r, 64 * h, dp, 64);
             sync_for_mma();
             if (tid == 0) {
-                const uint32_t s1 = smem_u32(X1), s4 = smem_u32(X4);
+                const uint32_t s1 = smem_u32(X1), s4 = smem_u32(X4), s5 = smem_u32(X5);
                 for (int kk = 0; kk < 8; kk++)
                     mma_bf16(tm + tQ, desc_k(s4, 128, kk), desc_mn(s1, 128, kk), idesc_bf16(128, D, true),
+                             (acc || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 8; kk++)
+                    mma_bf16(tm + tV, desc_k(s5, 128, kk), desc_mn(s1, 128, kk), idesc_bf16(128, D, true),
                              (acc || kk > 0) ? 1u : 0u);
                 mma_commit(&bar);
             }
@@ -161,8 +176,12 @@ bwd_wdq_tc_kernel(const BwdArgs a, const float2* __restrict__ tab, int* __restri
             ok = ctl.wait();
         }
     }
+    red[h * 128 + r] = dwin;
+    __syncthreads();
+    if (h == 0 && row_ok) a.Dwin[hoff + t] = red[r] + red[128 + r];
     if (ok) {
         store_unrotated<D>(tl + tQ, acc, sh.sigma, t, row_ok, h, tab, a.dqw + (hoff + t) * D);
+        store_unrotated<D>(tl + tV, acc, sh.sigma, t, row_ok, h, tab, a.dqwV + (hoff + t) * D);
     } else if (row_ok) {
         a.dqw[(hoff + t) * D + h] = __int_as_float(0x7fc00000);
     }
@@ -296,7 +315,7 @@ bwd_wkv_tc_kernel(const BwdArgs a, const float2* __restrict__ tab, int* __restri
 }
 
 template <int D>
-size_t wdq_smem() { return 1024 + 4 * 128 * D * 2 + 32768 + 256 * sizeof(float); }
+size_t wdq_smem() { return 1024 + 4 * 128 * D * 2 + 2 * 32768 + 256 * sizeof(float); }
 template <int D>
 size_t wkv_smem() { return 1024 + 4 * 128 * D * 2 + 2 * 32768 + 256 * sizeof(float); }
 
@@ -315,15 +334,20 @@ cudaError_t tc_backward(const BwdArgs& a, float2* tab, int* status, cudaStream_t
         NHA_LAUNCH("bwd_wdq_tc", st, kern<<<grid, kTcThreads, wdq_smem<D>(), st>>>(a, tab, status));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    {
-        auto kern = bwd_wkv_tc_kernel<D>;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wkv_smem<D>())) != cudaSuccess)
-            return e;
-        NHA_LAUNCH("bwd_wkv_tc", st, kern<<<grid, kTcThreads, wkv_smem<D>(), st>>>(a, tab, status));
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    return simt_bwd_slot<__nv_bfloat16, D, M>(a, st);
+    return tc_bwd_slot<D, M>(a, tab, status, st);
 }
+
+template <int D>
+cudaError_t launch_wkv(const BwdArgs& a, const float2* tab, int* status, cudaStream_t st) {
+    const dim3 grid((a.sh.T + 127) / 128, a.sh.BH);
+    auto kern = bwd_wkv_tc_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wkv_smem<D>());
+    if (e != cudaSuccess) return e;
+    NHA_LAUNCH("bwd_wkv_tc", st, kern<<<grid, kTcThreads, wkv_smem<D>(), st>>>(a, tab, status));
+    return cudaGetLastError();
+}
+template cudaError_t launch_wkv<64>(const BwdArgs&, const float2*, int*, cudaStream_t);
+template cudaError_t launch_wkv<128>(const BwdArgs&, const float2*, int*, cudaStream_t);
 
 #define NHA_TCB_INST(D, M) template cudaError_t tc_backward<D, M>(const BwdArgs&, float2*, int*, cudaStream_t);
 NHA_TCB_INST(64, 16)

@@ -26,7 +26,7 @@ struct FwdArgs {
 
 // Backward arguments.  Workspace beyond the forward's: Dv [BH, T];
 // dqw, dkw, dvw [BH, T, D] (window-branch partial gradients, fp32);
-// wsDL, wsPL, wsDB1 [BH, NC * C, M]; RK, RV [BH, NC, M, D]; TOT [BH, NC, M].
+// wsDL, wsPL, wsDB1 [BH, NC * C, M]; RK, RV [BH, NC, M, D].
 struct BwdArgs {
     const void* q;
     const void* k;
@@ -42,7 +42,10 @@ struct BwdArgs {
     float* SK;
     float* SV;
     float* G;
-    float* Dv;
+    float* Dv;     // D_t = dout_t . o_t
+    float* Dhat;   // D from the rounded o (bf16 path)
+    float* Dwin;   // window part of sum_s P dP (bf16 path)
+    float* dqwV;   // sigma R^T sum_s P k~ (bf16 path: dq correction for D - Dhat)
     float* dqw;
     float* dkw;
     float* dvw;
@@ -51,7 +54,6 @@ struct BwdArgs {
     float* wsDB1;
     float* RK;
     float* RV;
-    float* TOT;
     Shape sh;
     RopeTab rope;
 };
@@ -74,6 +76,14 @@ cudaError_t simt_bwd_slot(const BwdArgs& a, cudaStream_t st);
 // bf16 backward: window branch on the tensor core, then the slot branch.
 template <int D, int M>
 cudaError_t tc_backward(const BwdArgs& a, float2* tab, int* status, cudaStream_t st);
+// bf16 slot-branch backward on the tensor core (same contract as simt_bwd_slot).
+template <int D, int M>
+cudaError_t tc_bwd_slot(const BwdArgs& a, const float2* tab, int* status, cudaStream_t st);
+// Key-major window dk / dv (needs the exact D_t in a.Dv).
+template <int D>
+cudaError_t launch_wkv(const BwdArgs& a, const float2* tab, int* status, cudaStream_t st);
+cudaError_t launch_state_scan_rev(const BwdArgs& a, int M, int D, cudaStream_t st);
+cudaError_t launch_dla_carry(const BwdArgs& a, int M, int D, cudaStream_t st);
 // RoPE (cos, sin) table [T][H2] of the absolute positions.
 cudaError_t launch_rope_table(float2* tab, int T, int H2, const RopeTab& rt, cudaStream_t st);
 

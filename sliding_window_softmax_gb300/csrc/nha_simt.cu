@@ -674,7 +674,6 @@ __global__ void __launch_bounds__(kThreads) bwd_slot_key_kernel(const BwdArgs a)
                 acc += sDB[rr * LG + tid];
                 sDB[rr * LG + tid] = acc;
             }
-            a.TOT[((size_t)bh * sh.NC + x) * M + tid] = acc;
         }
         __syncthreads();
     }
@@ -697,22 +696,39 @@ __global__ void __launch_bounds__(kThreads) bwd_slot_key_kernel(const BwdArgs a)
     }
 }
 
-// dlog_alpha rows of chunk c += sum of db over all later chunks.  Grid (NC, BH).
+// dlog_alpha rows of chunk c += sum of db over all later chunks.  That sum
+// telescopes: with F_r = sum_{j >= r} db_j = d loss / d log_alpha_r through
+// alpha_r alone = alpha_r (R_r . S_{r-1}) (R_r the adjoint of the state after
+// token r), and j' the first token of chunk c + 1,
+//   sum_{c' > c} (db summed over chunk c') = F_{j'} = Rc(c) . S_prev(c + 1)
+// per slot, where Rc(c) = alpha_{j'} R_{j'} is the adjoint carried into the end
+// of chunk c (reverse scan) and S_prev(c + 1) = S_{j'-1} the state before
+// chunk c + 1 (forward scan).  Computing it at the boundary avoids summing
+// thousands of terms whose total is zero.  Grid (NC, BH); one warp per slot.
 template <int M>
-__global__ void __launch_bounds__(kThreads) bwd_dla_carry_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kThreads) bwd_dla_carry_kernel(const BwdArgs a, int D) {
     const Shape sh = a.sh;
     const int c = blockIdx.x, bh = blockIdx.y;
     const int j0 = c * kChunk, nc = min(kChunk, sh.R - j0);
     __shared__ float carry[64];
-    if (threadIdx.x < M) {
-        float acc = 0.0f;
-        for (int cc = c + 1; cc < sh.NC; cc++) acc += a.TOT[((size_t)bh * sh.NC + cc) * M + threadIdx.x];
-        carry[threadIdx.x] = acc;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (c + 1 < sh.NC) {
+        const size_t cur = ((size_t)bh * sh.NC + c) * M * D, nxt = ((size_t)bh * sh.NC + c + 1) * M * D;
+        for (int i = warp; i < M; i += kThreads / 32) {
+            float acc = 0.0f;
+            for (int d = lane; d < D; d += 32) {
+                const size_t o = (size_t)i * D + d;
+                acc += a.RK[cur + o] * a.SK[nxt + o] + a.RV[cur + o] * a.SV[nxt + o];
+            }
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (lane == 0) carry[i] = acc;
+        }
+    } else if (threadIdx.x < M) {
+        carry[threadIdx.x] = 0.0f;
     }
     __syncthreads();
     const size_t hoff = (size_t)bh * sh.T;
-    for (int e = threadIdx.x; e < nc * M; e += kThreads)
-        a.dla[(hoff + j0) * M + e] += carry[e % M];
+    for (int e = threadIdx.x; e < nc * M; e += kThreads) a.dla[(hoff + j0) * M + e] += carry[e % M];
 }
 
 // ---------------------------------------------------------------------------------------
@@ -783,7 +799,7 @@ cudaError_t simt_bwd_slot(const BwdArgs& a, cudaStream_t st) {
         NHA_CHECK(cudaGetLastError());
     }
     if (sh.NC > 1) {
-        NHA_LAUNCH("bwd_dla_carry", st, bwd_dla_carry_kernel<M><<<dim3(sh.NC, sh.BH), kThreads, 0, st>>>(a));
+        NHA_LAUNCH("bwd_dla_carry", st, bwd_dla_carry_kernel<M><<<dim3(sh.NC, sh.BH), kThreads, 0, st>>>(a, D));
         NHA_CHECK(cudaGetLastError());
     }
     return cudaSuccess;
@@ -814,6 +830,24 @@ cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st) {
         NHA_CHECK(cudaGetLastError());
     }
     return simt_bwd_slot<Tin, D, M>(a, st);
+}
+
+cudaError_t launch_state_scan_rev(const BwdArgs& a, int M, int D, cudaStream_t st) {
+    NHA_LAUNCH("state_scan_rev", st,
+               state_scan_kernel<<<dim3((M * D + kThreads - 1) / kThreads, a.sh.BH, 2), kThreads, 0, st>>>(
+                   a.RK, a.RV, a.G, a.sh.NC, M, D, -1));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dla_carry(const BwdArgs& a, int M, int D, cudaStream_t st) {
+    const dim3 grid(a.sh.NC, a.sh.BH);
+    switch (M) {
+        case 16: NHA_LAUNCH("bwd_dla_carry", st, bwd_dla_carry_kernel<16><<<grid, kThreads, 0, st>>>(a, D)); break;
+        case 32: NHA_LAUNCH("bwd_dla_carry", st, bwd_dla_carry_kernel<32><<<grid, kThreads, 0, st>>>(a, D)); break;
+        case 64: NHA_LAUNCH("bwd_dla_carry", st, bwd_dla_carry_kernel<64><<<grid, kThreads, 0, st>>>(a, D)); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
 }
 
 #define NHA_INST(Tin, D, M)                                                          \

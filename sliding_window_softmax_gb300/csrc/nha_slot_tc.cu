@@ -1,0 +1,635 @@
+// Tensor-core (tcgen05) backward of the NHA slot branch for bf16 inputs.
+//
+// Per tile of 128 rows = two C = 64 gate chunks.  With b the chunk-local
+// cumsum of log_alpha, rho = G / 2 (G = b at the chunk's end), Eq = exp(b - rho),
+// Ek = exp(rho - b) u, Fk = exp(rho - b), Eb = exp(b), eG = exp(G - rho), M the
+// within-chunk causal mask, and S_prev the slot states carried into the chunk:
+//
+// query side (rows = queries t = j + w of state indices j):
+//   L    = sigma [Eb o (Q S^K_prev^T) + Eq o ((Q K_c^T o M) Ek)]       P_L = exp(L - lse)
+//   dP_L = Eb o (dout S^V_prev^T) + Eq o ((dout V_c^T o M) Ek)        dL = P_L o (dP_L - D)
+//   dq  += (sigma dL o Eb) S^K_prev + (((sigma dL o Eq) Ek^T) o M) K_c
+//   dR^K_c = (Eb o sigma dL)^T Q,  dR^V_c = (Eb o P_L)^T dout          (adjoint contributions)
+//   db1  = dL o L + P_L o dP_L
+// key side (rows = tokens s; Rc = adjoint carried in from later chunks):
+//   dk  += ((Ek (sigma dL o Eq)^T) o M^T) Q_t + (Ek o eG) Rc^K
+//   dv  += ((Ek (P_L o Eq)^T) o M^T) dout_t + (Ek o eG) Rc^V
+//   du   = Fk o [((K_c Q_t^T o M^T)(sigma dL o Eq)) + eG o (K_c Rc^K^T)] + (same with V, dout, P_L, Rc^V)
+//   db   = db1 - u o du;  dlog_alpha = suffix-sum of db in the chunk - alpha o du
+//          (+ the totals of all later chunks, added by the carry kernel)
+// ("Native Hybrid Attention for Efficient Sequence Modeling", Paper-Notes page,
+// 关键设计/层内混合 recurrence and Chunkwise 并行计算; the backward is the
+// derivative of that chunked form.)
+#include "nha_common.cuh"
+#include "nha_kernels.h"
+#include "nha_prof.h"
+#include "nha_tc.cuh"
+#include "nha_tc_tiles.cuh"
+
+namespace nha {
+
+__host__ __device__ constexpr uint32_t idesc_am(int M, int N, bool a_mn, bool b_mn) {
+    return idesc_bf16(M, N, b_mn) | ((a_mn ? 1u : 0u) << 15);
+}
+
+// Inclusive cumsum of x over the 64 rows of this thread's chunk (tile rows
+// 0-63 or 64-127), for the HM slots i = h HM + jj.  s_tot: [4][M] scratch.
+template <int M>
+__device__ __forceinline__ void chunk_prefix(float (&x)[M / 2], float* s_tot, int warp, int lane, int h) {
+    constexpr int HM = M / 2;
+    const int wq = warp & 3;
+#pragma unroll
+    for (int jj = 0; jj < HM; jj++) {
+        float v = x[jj];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += y;
+        }
+        x[jj] = v;
+        if (lane == 31) s_tot[wq * M + h * HM + jj] = v;
+    }
+    __syncthreads();
+    if (wq & 1)
+#pragma unroll
+        for (int jj = 0; jj < HM; jj++) x[jj] += s_tot[(wq - 1) * M + h * HM + jj];
+    __syncthreads();
+}
+
+// Inclusive suffix sum of x over the 64 rows of this thread's chunk.
+template <int M>
+__device__ __forceinline__ void chunk_suffix(float (&x)[M / 2], float* s_tot, int warp, int lane, int h) {
+    constexpr int HM = M / 2;
+    const int wq = warp & 3;
+#pragma unroll
+    for (int jj = 0; jj < HM; jj++) {
+        float v = x[jj];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_down_sync(0xffffffffu, v, off);
+            if (lane + off < 32) v += y;
+        }
+        x[jj] = v;
+        if (lane == 0) s_tot[wq * M + h * HM + jj] = v;
+    }
+    __syncthreads();
+    if (!(wq & 1))
+#pragma unroll
+        for (int jj = 0; jj < HM; jj++) x[jj] += s_tot[(wq + 1) * M + h * HM + jj];
+    __syncthreads();
+}
+
+// Gates of this thread's row: loads log_alpha (0 past the valid rows), the
+// chunk-local cumsum b and the chunk totals sG[2][M] (zero for an empty chunk).
+template <int M>
+__device__ __forceinline__ void row_gates(const float* __restrict__ la_row, bool valid, float (&l)[M / 2],
+                                          float (&b)[M / 2], float* s_tot, float* sG, int warp, int lane,
+                                          int h, int r, int nrows) {
+    constexpr int HM = M / 2;
+#pragma unroll
+    for (int jj = 0; jj < HM; jj += 4) {
+        const float4 v = valid ? __ldg(reinterpret_cast<const float4*>(la_row + h * HM + jj))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        l[jj] = v.x; l[jj + 1] = v.y; l[jj + 2] = v.z; l[jj + 3] = v.w;
+    }
+#pragma unroll
+    for (int jj = 0; jj < HM; jj++) b[jj] = l[jj];
+    chunk_prefix<M>(b, s_tot, warp, lane, h);
+    const int cc = r >> 6, last = min(nrows, 64 * (cc + 1)) - 1;
+    if (r == last)
+#pragma unroll
+        for (int jj = 0; jj < HM; jj++) sG[cc * M + h * HM + jj] = b[jj];
+    __syncthreads();
+}
+
+__device__ __forceinline__ void zero_cols(unsigned char* tile, int row, int c0, int c1) {
+    for (int c = c0; c < c1; c += 8)
+        *reinterpret_cast<uint4*>(tile + sw_chunk(row, c >> 3, 128)) = make_uint4(0, 0, 0, 0);
+}
+
+// Masked copy of 64 TMEM columns (this half's) into a bf16 tile row:
+// keep (row, col) iff h == own chunk and (upper ? col >= row : col <= row).
+__device__ __forceinline__ void mask_to_tile(uint32_t taddr, unsigned char* tile, int r, int h, int cr,
+                                             bool row_ok, bool upper) {
+    float vv[64];
+    tmem_ld(taddr + 64 * h, vv, 64);
+#pragma unroll
+    for (int jj = 0; jj < 64; jj++) {
+        const int col = 64 * h + jj;
+        const bool keep = row_ok && h == cr && (upper ? col >= r : col <= r);
+        if (!keep) vv[jj] = 0.0f;
+    }
+    store_row(tile, r, 64 * h, vv, 64);
+}
+
+// ---------------------------------------------------------------------------------------
+template <int D, int M>
+__global__ void __launch_bounds__(kTcThreads, 1)
+bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
+    constexpr int HM = M / 2, HD = D / 2, TB = 128 * D * 2;
+    constexpr int SSZ = ((2 * M * D * 2) + 1023) / 1024 * 1024;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* XE = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char* XdO = XE + 16384;  // dout rows of the tile's queries
+    unsigned char* XKV = XdO + TB;    // V_c, then K_c
+    unsigned char* XS = XKV + TB;     // [S^V pair], then [S^K pair]   (2M rows)
+    unsigned char* XM = XS + SSZ;     // masked products / G2
+    unsigned char* XQ = XM + 32768;   // Q, then sigma dL o Eq
+    unsigned char* XG = XQ + TB;      // G1 = sigma dL o Eb, chunk-blocked [128][2M]
+    float* s_tot = reinterpret_cast<float*>(XG + 32768);  // [4][M]
+    float* sG = s_tot + 4 * M;                             // [2][M]
+    float* red = sG + 2 * M;                               // [2][128]
+    __shared__ uint64_t bar;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    const Shape sh = a.sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
+    const int W0 = sh.T - sh.R, NLT = (W0 + 127) / 128;
+    const int x = blockIdx.x, bh = blockIdx.y;
+    const size_t hoff = (size_t)bh * sh.T;
+    if (x < NLT) {  // window-only queries: D = its window part; dq = window branch only
+        const int tb = x * 128, n = min(128, W0 - tb);
+        for (int e = tid; e < n * D / 8; e += kTcThreads) {
+            const int row = e / (D / 8);
+            const size_t tt = hoff + tb + row;
+            const float corr = a.Dhat[tt] - a.Dwin[tt];
+            const float* src = a.dqw + (hoff + tb) * D + e * 8;
+            const float* cv = a.dqwV + (hoff + tb) * D + e * 8;
+            float f[8];
+#pragma unroll
+            for (int q = 0; q < 8; q++) f[q] = src[q] + corr * cv[q];
+            *reinterpret_cast<uint4*>((__nv_bfloat16*)a.dq + (hoff + tb) * D + e * 8) = pack8(f);
+        }
+        for (int e = tid; e < n; e += kTcThreads) a.Dv[hoff + tb + e] = a.Dwin[hoff + tb + e];
+        return;
+    }
+    const int j0 = (x - NLT) * 128, nq = min(128, sh.R - j0), tbase = j0 + sh.w;
+    const int c1 = j0 / kChunk;
+    const bool has2 = nq > kChunk, row_ok = r < nq;
+    const int t = tbase + r, j = j0 + r;
+    const size_t jrow = (size_t)bh * sh.NC * kChunk + j;
+    const __nv_bfloat16* q = (const __nv_bfloat16*)a.q + hoff * D;
+    const __nv_bfloat16* k = (const __nv_bfloat16*)a.k + hoff * D;
+    const __nv_bfloat16* v = (const __nv_bfloat16*)a.v + hoff * D;
+    const __nv_bfloat16* dout = (const __nv_bfloat16*)a.dout + hoff * D;
+    const float sig = sh.sigma;
+
+    if (tid < 2 * M) sG[tid] = 0.0f;
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+        s_abort = 0;
+    }
+    if (warp == 0) tmem_alloc(&s_tmem, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tm = s_tmem;
+    const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t R0 = 0, R1 = 128, R2 = 256, R3 = 384;
+    TcCtl ctl{&bar, 0u, &s_abort, status};
+    bool ok = true;
+
+    float l[HM], b[HM];
+    row_gates<M>(a.la + (hoff + j) * M, row_ok, l, b, s_tot, sG, warp, lane, h, r, nq);
+    float rho[HM];
+#pragma unroll
+    for (int jj = 0; jj < HM; jj++) rho[jj] = 0.5f * sG[cr * M + h * HM + jj];
+    {  // Ek tile
+        float ek[HM];
+#pragma unroll
+        for (int jj = 0; jj < HM; jj++) ek[jj] = row_ok ? expf(rho[jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
+        store_row(XE, r, h * HM, ek, HM);
+    }
+    const float lse_r = row_ok ? a.lse[hoff + t] : 0.0f;
+    const float Dwin_r = row_ok ? a.Dwin[hoff + t] : 0.0f;
+    const float Dhat_r = row_ok ? a.Dhat[hoff + t] : 0.0f;
+    float D_r = 0.0f;  // exact D = window part + slot part, set below
+    const float* SV1 = a.SV + ((size_t)bh * sh.NC + c1) * M * D;
+    const float* SK1 = a.SK + ((size_t)bh * sh.NC + c1) * M * D;
+
+    // ---- value side: dP_L
+    load_tile<D>(dout, tbase, nq, XdO, nullptr);
+    load_tile<D>(v, j0, nq, XKV, nullptr);
+    load_state_pair<D, M>(SV1, has2 ? SV1 + M * D : nullptr, XS);
+    sync_for_mma();
+    if (tid == 0) {
+        const uint32_t sd = smem_u32(XdO), sk = smem_u32(XKV), ss = smem_u32(XS);
+        for (int kk = 0; kk < D / 16; kk++)
+            mma_bf16(tm + R0, desc_k(sd, 128, kk), desc_k(sk, 128, kk), idesc_bf16(128, 128, false), kk > 0);
+        for (int kk = 0; kk < D / 16; kk++)
+            mma_bf16(tm + R1, desc_k(sd, 128, kk), desc_k(ss, 2 * M, kk), idesc_bf16(128, 2 * M, false), kk > 0);
+        mma_commit(&bar);
+    }
+    float dpl[HM];
+    if ((ok = ctl.wait())) {
+        mask_to_tile(tl + R0, XM, r, h, cr, row_ok, false);
+        sync_for_mma();
+        if (tid == 0) {
+            const uint32_t sm = smem_u32(XM), se = smem_u32(XE);
+            for (int kk = 0; kk < 8; kk++)
+                mma_bf16(tm + R0, desc_k(sm, 128, kk), desc_mn(se, 128, kk), idesc_bf16(128, M, true), kk > 0);
+            mma_commit(&bar);
+        }
+        ok = ctl.wait();
+    }
+    if (ok) {
+        float so[HM], pin[HM];
+        tmem_ld(tl + R1 + cr * M + h * HM, so, HM);
+        tmem_ld(tl + R0 + h * HM, pin, HM);
+#pragma unroll
+        for (int jj = 0; jj < HM; jj++) dpl[jj] = expf(b[jj]) * so[jj] + expf(b[jj] - rho[jj]) * pin[jj];
+        // ---- key side: slot logits
+        load_tile<D>(q, tbase, nq, XQ, nullptr);
+        load_tile<D>(k, j0, nq, XKV, nullptr);
+        load_state_pair<D, M>(SK1, has2 ? SK1 + M * D : nullptr, XS);
+        sync_for_mma();
+        if (tid == 0) {
+            const uint32_t sq = smem_u32(XQ), sk = smem_u32(XKV), ss = smem_u32(XS);
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_bf16(tm + R0, desc_k(sq, 128, kk), desc_k(sk, 128, kk), idesc_bf16(128, 128, false), kk > 0);
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_bf16(tm + R1, desc_k(sq, 128, kk), desc_k(ss, 2 * M, kk), idesc_bf16(128, 2 * M, false), kk > 0);
+            mma_commit(&bar);
+        }
+        ok = ctl.wait();
+    }
+    if (ok) {
+        mask_to_tile(tl + R0, XM, r, h, cr, row_ok, false);
+        sync_for_mma();
+        if (tid == 0) {
+            const uint32_t sm = smem_u32(XM), se = smem_u32(XE);
+            for (int kk = 0; kk < 8; kk++)
+                mma_bf16(tm + R0, desc_k(sm, 128, kk), desc_mn(se, 128, kk), idesc_bf16(128, M, true), kk > 0);
+            mma_commit(&bar);
+        }
+        ok = ctl.wait();
+    }
+    float weq[HM];
+    if (ok) {
+        float si[HM], lin[HM], g1[HM], g2[HM], z[HM];
+        tmem_ld(tl + R1 + cr * M + h * HM, si, HM);
+        tmem_ld(tl + R0 + h * HM, lin, HM);
+        float* wsDL = a.wsDL + jrow * M + h * HM;
+        float* wsPL = a.wsPL + jrow * M + h * HM;
+        float* wsDB = a.wsDB1 + jrow * M + h * HM;
+        float Lv[HM], pl[HM];
+        float sp = 0.0f;
+#pragma unroll
+        for (int jj = 0; jj < HM; jj++) {
+            const float eb = expf(b[jj]), eq = expf(b[jj] - rho[jj]);
+            Lv[jj] = sig * (eb * si[jj] + eq * lin[jj]);
+            pl[jj] = row_ok ? expf(Lv[jj] - lse_r) : 0.0f;
+            sp += pl[jj] * dpl[jj];
+        }
+        red[h * 128 + r] = sp;
+        __syncthreads();
+        D_r = Dwin_r + red[r] + red[128 + r];
+        if (h == 0 && row_ok) a.Dv[hoff + t] = D_r;
+#pragma unroll
+        for (int jj = 0; jj < HM; jj++) {
+            const float eb = expf(b[jj]), eq = expf(b[jj] - rho[jj]);
+            const float dl = pl[jj] * (dpl[jj] - D_r);
+            const float db1 = dl * Lv[jj] + pl[jj] * dpl[jj];
+            if (row_ok) {
+                wsDL[jj] = sig * dl;
+                wsPL[jj] = pl[jj];
+                wsDB[jj] = db1;
+            }
+            g1[jj] = sig * dl * eb;
+            g2[jj] = pl[jj] * eb;
+            weq[jj] = sig * dl * eq;
+            z[jj] = 0.0f;
+        }
+        // chunk-blocked [128][2M] tiles; columns >= 2M are zero
+        store_row(XG, r, cr * M + h * HM, g1, HM);
+        store_row(XG, r, (1 - cr) * M + h * HM, z, HM);
+        store_row(XM, r, cr * M + h * HM, g2, HM);
+        store_row(XM, r, (1 - cr) * M + h * HM, z, HM);
+        if (2 * M < 128) {
+            const int span = (128 - 2 * M) / 2;
+            zero_cols(XG, r, 2 * M + h * span, 2 * M + (h + 1) * span);
+            zero_cols(XM, r, 2 * M + h * span, 2 * M + (h + 1) * span);
+        }
+        sync_for_mma();
+        if (tid == 0) {  // dR^K = G1^T Q, dR^V = G2^T dout (A read MN-major: rows = slots)
+            const uint32_t sg = smem_u32(XG), sq = smem_u32(XQ), sm = smem_u32(XM), sd = smem_u32(XdO);
+            for (int kk = 0; kk < 8; kk++)
+                mma_bf16(tm + R1, desc_mn(sg, 128, kk), desc_mn(sq, 128, kk), idesc_am(128, D, true, true), kk > 0);
+            for (int kk = 0; kk < 8; kk++)
+                mma_bf16(tm + R2, desc_mn(sm, 128, kk), desc_mn(sd, 128, kk), idesc_am(128, D, true, true), kk > 0);
+            mma_commit(&bar);
+        }
+        ok = ctl.wait();
+    }
+    if (ok) {
+        // row r of the result = slot n = r of chunk r / M
+        const int cc = r / M, i = r % M;
+        const bool keep = r < 2 * M && (cc == 0 || has2);
+        float* RK = a.RK + (((size_t)bh * sh.NC + c1 + cc) * M + i) * D + h * HD;
+        float* RV = a.RV + (((size_t)bh * sh.NC + c1 + cc) * M + i) * D + h * HD;
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+            float vk[32], vv[32];
+            tmem_ld32(tl + R1 + h * HD + c0, vk);
+            tmem_ld32(tl + R2 + h * HD + c0, vv);
+            if (keep)
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    *reinterpret_cast<float4*>(RK + c0 + e) = make_float4(vk[e], vk[e + 1], vk[e + 2], vk[e + 3]);
+                    *reinterpret_cast<float4*>(RV + c0 + e) = make_float4(vv[e], vv[e + 1], vv[e + 2], vv[e + 3]);
+                }
+        }
+        // ---- dq_slot = G1 [S^K pair] + ((sigma dL o Eq) Ek^T o M) K_c
+        store_row(XQ, r, h * HM, weq, HM);
+        sync_for_mma();
+        if (tid == 0) {
+            const uint32_t sg = smem_u32(XG), ss = smem_u32(XS), sq = smem_u32(XQ), se = smem_u32(XE);
+            for (int kk = 0; kk < 2 * M / 16; kk++)
+                mma_bf16(tm + R3, desc_k(sg, 128, kk), desc_mn(ss, 2 * M, kk), idesc_bf16(128, D, true), kk > 0);
+            for (int kk = 0; kk < M / 16; kk++)
+                mma_bf16(tm + R0, desc_k(sq, 128, kk), desc_k(se, 128, kk), idesc_bf16(128, 128, false), kk > 0);
+            mma_commit(&bar);
+        }
+        ok = ctl.wait();
+    }
+    if (ok) {
+        mask_to_tile(tl + R0, XM, r, h, cr, row_ok, false);
+        sync_for_mma();
+        if (tid == 0) {
+            const uint32_t sm = smem_u32(XM), sk = smem_u32(XKV);
+            for (int kk = 0; kk < 8; kk++)
+                mma_bf16(tm + R3, desc_k(sm, 128, kk), desc_mn(sk, 128, kk), idesc_bf16(128, D, true), 1u);
+            mma_commit(&bar);
+        }
+        ok = ctl.wait();
+    }
+    if (ok) {
+        const float* dqw = a.dqw + (hoff + t) * D + h * HD;
+        const float* cv = a.dqwV + (hoff + t) * D + h * HD;
+        const float corr = Dhat_r - D_r;
+        __nv_bfloat16* dq = (__nv_bfloat16*)a.dq + (hoff + t) * D + h * HD;
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+            float g[32];
+            tmem_ld32(tl + R3 + h * HD + c0, g);
+            if (row_ok) {
+#pragma unroll
+                for (int e = 0; e < 32; e++) g[e] += corr * cv[c0 + e];
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                    const float4 u0 = *reinterpret_cast<const float4*>(dqw + c0 + e);
+                    const float4 u1 = *reinterpret_cast<const float4*>(dqw + c0 + e + 4);
+                    const float f[8] = {u0.x + g[e], u0.y + g[e + 1], u0.z + g[e + 2], u0.w + g[e + 3],
+                                        u1.x + g[e + 4], u1.y + g[e + 5], u1.z + g[e + 6], u1.w + g[e + 7]};
+                    *reinterpret_cast<uint4*>(dq + c0 + e) = pack8(f);
+                }
+            }
+        }
+    } else if (row_ok && h == 0) {
+        ((__nv_bfloat16*)a.dq)[(hoff + t) * D] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
+    }
+    if (!ok && tid == 0) mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+// ---------------------------------------------------------------------------------------
+template <int D, int M>
+__global__ void __launch_bounds__(kTcThreads, 1)
+bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
+    constexpr int HM = M / 2, HD = D / 2, TB = 128 * D * 2;
+    constexpr int SSZ = ((2 * M * D * 2) + 1023) / 1024 * 1024;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* XE = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char* XW = XE + 16384;   // W o Eq  [128 j][M]
+    unsigned char* XEG = XW + 16384;  // Ek o eG chunk-blocked [128][2M]
+    unsigned char* XA = XEG + 32768;  // q_t or dout_t rows
+    unsigned char* XB = XA + TB;      // k_c or v_c rows
+    unsigned char* XR = XB + TB;      // [Rc pair]  (2M rows)
+    unsigned char* XM1 = XR + SSZ;
+    unsigned char* XM2 = XM1 + 32768;
+    float* s_tot = reinterpret_cast<float*>(XM2 + 32768);  // [4][M]
+    float* sG = s_tot + 4 * M;                              // [2][M]
+    __shared__ uint64_t bar;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    const Shape sh = a.sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
+    const int x = blockIdx.x, bh = blockIdx.y;
+    const size_t hoff = (size_t)bh * sh.T;
+    const int sbase = x * 128, nk = min(128, sh.T - sbase);
+    const int nc = max(0, min(128, sh.R - sbase));
+    const int s = sbase + r;
+    const bool row_ok = r < nk, slot_ok = r < nc;
+    if (nc == 0) {  // tokens that never enter a state read by a query
+        if (row_ok) {
+            const float* gk = a.dkw + (hoff + s) * D + h * HD;
+            const float* gv = a.dvw + (hoff + s) * D + h * HD;
+            __nv_bfloat16* ok_ = (__nv_bfloat16*)a.dk + (hoff + s) * D + h * HD;
+            __nv_bfloat16* ov_ = (__nv_bfloat16*)a.dv + (hoff + s) * D + h * HD;
+            for (int c = 0; c < HD; c += 8) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) f[e] = gk[c + e];
+                *reinterpret_cast<uint4*>(ok_ + c) = pack8(f);
+#pragma unroll
+                for (int e = 0; e < 8; e++) f[e] = gv[c + e];
+                *reinterpret_cast<uint4*>(ov_ + c) = pack8(f);
+            }
+            float* dla = a.dla + (hoff + s) * M + h * HM;
+#pragma unroll
+            for (int jj = 0; jj < HM; jj++) dla[jj] = 0.0f;
+        }
+        return;
+    }
+    const int c1 = sbase / kChunk;
+    const bool has2 = nc > kChunk;
+    const size_t jrow = (size_t)bh * sh.NC * kChunk + s;
+
+    if (tid < 2 * M) sG[tid] = 0.0f;
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+        s_abort = 0;
+    }
+    if (warp == 0) tmem_alloc(&s_tmem, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tm = s_tmem;
+    const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t R0 = 0, R1 = 128, R2 = 256, R3 = 384;
+    TcCtl ctl{&bar, 0u, &s_abort, status};
+    bool ok = true;
+
+    float l[HM], b[HM];
+    row_gates<M>(a.la + (hoff + s) * M, slot_ok, l, b, s_tot, sG, warp, lane, h, r, nc);
+    float rho[HM], eG[HM];
+#pragma unroll
+    for (int jj = 0; jj < HM; jj++) {
+        const float G = sG[cr * M + h * HM + jj];
+        rho[jj] = 0.5f * G;
+        eG[jj] = expf(0.5f * G);
+    }
+    {
+        float ek[HM], eke[HM], z[HM];
+#pragma unroll
+        for (int jj = 0; jj < HM; jj++) {
+            ek[jj] = slot_ok ? expf(rho[jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
+            eke[jj] = ek[jj] * eG[jj];
+            z[jj] = 0.0f;
+        }
+        store_row(XE, r, h * HM, ek, HM);
+        store_row(XEG, r, cr * M + h * HM, eke, HM);
+        store_row(XEG, r, (1 - cr) * M + h * HM, z, HM);
+    }
+    float du[HM];
+#pragma unroll
+    for (int jj = 0; jj < HM; jj++) du[jj] = 0.0f;
+
+    for (int pass = 0; pass < 2 && ok; pass++) {
+        const __nv_bfloat16* X = (const __nv_bfloat16*)(pass == 0 ? a.q : a.dout) + hoff * D;
+        const __nv_bfloat16* Y = (const __nv_bfloat16*)(pass == 0 ? a.k : a.v) + hoff * D;
+        const float* W = (pass == 0 ? a.wsDL : a.wsPL) + jrow * M + h * HM;
+        const float* Rc = (pass == 0 ? a.RK : a.RV) + ((size_t)bh * sh.NC + c1) * M * D;
+        load_tile<D>(X, sbase + sh.w, nc, XA, nullptr);
+        load_tile<D>(Y, sbase, nc, XB, nullptr);
+        load_state_pair<D, M>(Rc, has2 ? Rc + M * D : nullptr, XR);
+        {
+            float weq[HM];
+#pragma unroll
+            for (int jj = 0; jj < HM; jj++) weq[jj] = slot_ok ? W[jj] * expf(b[jj] - rho[jj]) : 0.0f;
+            store_row(XW, r, h * HM, weq, HM);
+        }
+        sync_for_mma();
+        if (tid == 0) {
+            const uint32_t se = smem_u32(XE), sw = smem_u32(XW), sa = smem_u32(XA), sb = smem_u32(XB),
+                           sr = smem_u32(XR);
+            for (int kk = 0; kk < M / 16; kk++)
+                mma_bf16(tm + R0, desc_k(se, 128, kk), desc_k(sw, 128, kk), idesc_bf16(128, 128, false), kk > 0);
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_bf16(tm + R1, desc_k(sb, 128, kk), desc_k(sa, 128, kk), idesc_bf16(128, 128, false), kk > 0);
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_bf16(tm + R2, desc_k(sb, 128, kk), desc_k(sr, 2 * M, kk), idesc_bf16(128, 2 * M, false), kk > 0);
+            mma_commit(&bar);
+        }
+        if (!(ok = ctl.wait())) break;
+        mask_to_tile(tl + R0, XM1, r, h, cr, slot_ok, true);
+        mask_to_tile(tl + R1, XM2, r, h, cr, slot_ok, true);
+        float inter[HM];
+        tmem_ld(tl + R2 + cr * M + h * HM, inter, HM);
+        sync_for_mma();
+        if (tid == 0) {
+            const uint32_t s1 = smem_u32(XM1), s2 = smem_u32(XM2), sa = smem_u32(XA), sg = smem_u32(XEG),
+                           sr = smem_u32(XR), sw = smem_u32(XW);
+            for (int kk = 0; kk < 8; kk++)
+                mma_bf16(tm + R3, desc_k(s1, 128, kk), desc_mn(sa, 128, kk), idesc_bf16(128, D, true), kk > 0);
+            for (int kk = 0; kk < 2 * M / 16; kk++)
+                mma_bf16(tm + R3, desc_k(sg, 128, kk), desc_mn(sr, 2 * M, kk), idesc_bf16(128, D, true), 1u);
+            for (int kk = 0; kk < 8; kk++)
+                mma_bf16(tm + R0, desc_k(s2, 128, kk), desc_mn(sw, 128, kk), idesc_bf16(128, M, true), kk > 0);
+            mma_commit(&bar);
+        }
+        if (!(ok = ctl.wait())) break;
+        {
+            float intra[HM];
+            tmem_ld(tl + R0 + h * HM, intra, HM);
+#pragma unroll
+            for (int jj = 0; jj < HM; jj++) du[jj] += expf(rho[jj] - b[jj]) * (intra[jj] + eG[jj] * inter[jj]);
+        }
+        const float* gw = (pass == 0 ? a.dkw : a.dvw) + (hoff + s) * D + h * HD;
+        __nv_bfloat16* go = (__nv_bfloat16*)(pass == 0 ? a.dk : a.dv) + (hoff + s) * D + h * HD;
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+            float g[32];
+            tmem_ld32(tl + R3 + h * HD + c0, g);
+            if (row_ok) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                    const float4 u0 = *reinterpret_cast<const float4*>(gw + c0 + e);
+                    const float4 u1 = *reinterpret_cast<const float4*>(gw + c0 + e + 4);
+                    const float f[8] = {u0.x + g[e], u0.y + g[e + 1], u0.z + g[e + 2], u0.w + g[e + 3],
+                                        u1.x + g[e + 4], u1.y + g[e + 5], u1.z + g[e + 6], u1.w + g[e + 7]};
+                    *reinterpret_cast<uint4*>(go + c0 + e) = pack8(f);
+                }
+            }
+        }
+        fence_before_sync();
+        __syncthreads();
+    }
+    if (ok) {
+        // db = db1 - u du;  dlog_alpha = (suffix sum of db in the chunk) - alpha du
+        float db[HM];
+        const float* db1 = a.wsDB1 + jrow * M + h * HM;
+#pragma unroll
+        for (int jj = 0; jj < HM; jj++) db[jj] = slot_ok ? db1[jj] - (-expm1f(l[jj])) * du[jj] : 0.0f;
+        chunk_suffix<M>(db, s_tot, warp, lane, h);
+        if (row_ok) {
+            float* dla = a.dla + (hoff + s) * M + h * HM;
+#pragma unroll
+            for (int jj = 0; jj < HM; jj++) dla[jj] = slot_ok ? db[jj] - expf(l[jj]) * du[jj] : 0.0f;
+        }
+    } else if (row_ok && h == 0) {
+        a.dla[(hoff + s) * M] = __int_as_float(0x7fc00000);
+    }
+    if (!ok && tid == 0) mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+template <int D, int M>
+size_t sq_smem() {
+    return 1024 + 16384 + 3 * 128 * D * 2 + ((2 * M * D * 2) + 1023) / 1024 * 1024 + 2 * 32768 + 6 * M * 4 +
+           256 * 4;
+}
+template <int D, int M>
+size_t sk_smem() {
+    return 1024 + 2 * 16384 + 32768 + 2 * 128 * D * 2 + ((2 * M * D * 2) + 1023) / 1024 * 1024 + 2 * 32768 +
+           6 * M * 4;
+}
+
+template <int D, int M>
+cudaError_t tc_bwd_slot(const BwdArgs& a, const float2* tab, int* status, cudaStream_t st) {
+    const Shape& sh = a.sh;
+    cudaError_t e;
+    const int W0 = sh.T - sh.R;
+    const int qtiles = (W0 + 127) / 128 + (sh.R + 127) / 128;
+    {
+        auto kern = bwd_sq_tc_kernel<D, M>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sq_smem<D, M>())) != cudaSuccess)
+            return e;
+        if (qtiles > 0)
+            NHA_LAUNCH("bwd_sq_tc", st, kern<<<dim3(qtiles, sh.BH), kTcThreads, sq_smem<D, M>(), st>>>(a, status));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if ((e = launch_wkv<D>(a, tab, status, st)) != cudaSuccess) return e;
+    if (sh.NC > 0) {
+        if ((e = launch_state_scan_rev(a, M, D, st)) != cudaSuccess) return e;
+    }
+    {
+        auto kern = bwd_sk_tc_kernel<D, M>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk_smem<D, M>())) != cudaSuccess)
+            return e;
+        NHA_LAUNCH("bwd_sk_tc", st,
+                   kern<<<dim3((sh.T + 127) / 128, sh.BH), kTcThreads, sk_smem<D, M>(), st>>>(a, status));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (sh.NC > 1) {
+        if ((e = launch_dla_carry(a, M, D, st)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+#define NHA_TCS_INST(D, M) template cudaError_t tc_bwd_slot<D, M>(const BwdArgs&, const float2*, int*, cudaStream_t);
+NHA_TCS_INST(64, 16)
+NHA_TCS_INST(64, 32)
+NHA_TCS_INST(64, 64)
+NHA_TCS_INST(128, 16)
+NHA_TCS_INST(128, 32)
+NHA_TCS_INST(128, 64)
+
+}  // namespace nha
