@@ -40,7 +40,7 @@ struct Plan {
     nha::Shape sh;
     int d, m;
     // workspace offsets, in floats
-    size_t SK, SV, G, TAB, STATUS, Dv, Dhat, Dwin, dqwV, dqw, dkw, dvw, DL, PL, DB1, RK, RV, total;
+    size_t SK, SV, G, TAB, STATUS, QR, KR, Dv, Dhat, Dwin, dqwV, dqw, dkw, dvw, DL, PL, DB1, RK, RV, total;
 };
 
 nha_status_t check_shape(int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dt) {
@@ -84,6 +84,8 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward) {
     p.G = take(BH * NC * m);
     p.TAB = take(Tz * (size_t)d);  // RoPE (cos, sin) per position and frequency
     p.STATUS = take(16);
+    p.QR = take(BH * Tz * d / 2);  // RoPE(q), bf16
+    p.KR = take(BH * Tz * d / 2);  // RoPE(k), bf16
     if (backward) {
         p.Dv = take(BH * Tz);
         p.Dhat = take(BH * Tz);
@@ -119,13 +121,15 @@ bool misaligned(const void* p) { return ((uintptr_t)p & 15u) != 0; }
 cudaError_t run_forward_tc(const Plan& p, const nha::FwdArgs& a, float* ws, cudaStream_t s) {
     float2* tab = (float2*)(ws + p.TAB);
     int* status = (int*)(ws + p.STATUS);
+    __nv_bfloat16* qr = (__nv_bfloat16*)(ws + p.QR);
+    __nv_bfloat16* kr = (__nv_bfloat16*)(ws + p.KR);
     switch (p.d * 1000 + p.m) {
-        case 64016: return nha::tc_forward<64, 16>(a, tab, status, s);
-        case 64032: return nha::tc_forward<64, 32>(a, tab, status, s);
-        case 64064: return nha::tc_forward<64, 64>(a, tab, status, s);
-        case 128016: return nha::tc_forward<128, 16>(a, tab, status, s);
-        case 128032: return nha::tc_forward<128, 32>(a, tab, status, s);
-        case 128064: return nha::tc_forward<128, 64>(a, tab, status, s);
+        case 64016: return nha::tc_forward<64, 16>(a, tab, qr, kr, status, s);
+        case 64032: return nha::tc_forward<64, 32>(a, tab, qr, kr, status, s);
+        case 64064: return nha::tc_forward<64, 64>(a, tab, qr, kr, status, s);
+        case 128016: return nha::tc_forward<128, 16>(a, tab, qr, kr, status, s);
+        case 128032: return nha::tc_forward<128, 32>(a, tab, qr, kr, status, s);
+        case 128064: return nha::tc_forward<128, 64>(a, tab, qr, kr, status, s);
     }
     return cudaErrorInvalidValue;
 }

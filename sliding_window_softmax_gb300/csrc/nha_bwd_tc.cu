@@ -322,8 +322,8 @@ size_t wkv_smem() { return 1024 + 4 * 128 * D * 2 + 2 * 32768 + 256 * sizeof(flo
 template <int D, int M>
 cudaError_t tc_backward(const BwdArgs& a, float2* tab, int* status, cudaStream_t st) {
     const Shape& sh = a.sh;
-    cudaError_t e = simt_states<__nv_bfloat16, D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
-                                                     a.la, a.SK, a.SV, a.G, sh, st);
+    cudaError_t e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV, a.G,
+                                    sh, status, st);
     if (e != cudaSuccess) return e;
     if ((e = launch_rope_table(tab, sh.T, D / 2, a.rope, st)) != cudaSuccess) return e;
     const dim3 grid((sh.T + 127) / 128, sh.BH);

@@ -36,25 +36,28 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, int T, int H2, RopeT
 
 template <int D, int M>
 __global__ void __launch_bounds__(kTcThreads, 1)
-fwd_tc_kernel(const FwdArgs a, const float2* __restrict__ tab, int* __restrict__ status) {
-    constexpr int HM = M / 2, HD = D / 2;
+fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_bfloat16* __restrict__ kr,
+              int* __restrict__ status) {
+    constexpr int HM = M / 2, HD = D / 2, TB = 128 * D * 2;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* X0 = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char* X1 = X0 + 128 * D * 2;  // 32 KB
-    unsigned char* X2 = X1 + 32768;        // 32 KB
-    unsigned char* X3 = X2 + 32768;        // [2M][D]
-    float* sB = reinterpret_cast<float*>(X3 + 2 * M * D * 2);  // [128][M]
-    float* sU = sB + 128 * M;                                   // [128][M]
-    float* sRho = sU + 128 * M;                                 // [2][M]
-    float* redm = sRho + 2 * M;                                 // [2][128]
-    float* reds = redm + 256;                                   // [2][128]
+    unsigned char* KB[2];
+    unsigned char* VB[2];
+    KB[0] = X0 + TB;        // K~ block / P      (slot phase: K_c, masks, A_inter)
+    VB[0] = KB[0] + 32768;  // V block           (slot phase: V_c)
+    KB[1] = VB[0] + 32768;  //                   (slot phase: [S^K] then [S^V] pair)
+    VB[1] = KB[1] + 32768;  //                   (slot phase: Ek, then pEq at +16 KB)
+    float* s_tot = reinterpret_cast<float*>(VB[1] + 32768);  // [4][M]
+    float* sG = s_tot + 4 * M;                                // [2][M]
+    float* redm = sG + 2 * M;                                 // [2][128]
+    float* reds = redm + 256;                                 // [2][128]
     __shared__ uint64_t bar;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
     const Shape sh = a.sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = ((warp & 3) << 5) | lane, h = warp >> 2;
+    const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
     const int W0 = sh.T - sh.R;
     const int NLT = (W0 + 127) / 128;
     const int x = blockIdx.x, bh = blockIdx.y;
@@ -68,12 +71,16 @@ fwd_tc_kernel(const FwdArgs a, const float2* __restrict__ tab, int* __restrict__
         nq = min(128, sh.R - j0);
         tbase = j0 + sh.w;
     }
+    const bool row_ok = r < nq;
     const size_t hoff = (size_t)bh * sh.T;
     const __nv_bfloat16* q = (const __nv_bfloat16*)a.q + hoff * D;
     const __nv_bfloat16* k = (const __nv_bfloat16*)a.k + hoff * D;
     const __nv_bfloat16* v = (const __nv_bfloat16*)a.v + hoff * D;
+    qr += hoff * D;
+    kr += hoff * D;
     const float sig2 = sh.sigma * kLog2e;
 
+    if (tid < 2 * M) sG[tid] = 0.0f;
     if (tid == 0) {
         mbar_init(&bar, 1);
         mbar_fence_init();
@@ -91,72 +98,46 @@ fwd_tc_kernel(const FwdArgs a, const float2* __restrict__ tab, int* __restrict__
 
     float m = -INFINITY, l = 0.0f;  // running max (log2 domain) and sum of the row
     bool o_valid = false;
-    const int cr = r >> 6;  // chunk of this row inside a slot tile (uniform per warp)
 
     if (slot) {
         const int c1 = j0 / kChunk;
         const bool has2 = nq > kChunk;
-        load_tile<D>(q, tbase, nq, X0, nullptr);
-        load_tile<D>(k, j0, nq, X1, nullptr);
-        load_state_pair<D, M>(a.SK + ((size_t)bh * sh.NC + c1) * M * D,
-                              has2 ? a.SK + ((size_t)bh * sh.NC + c1 + 1) * M * D : nullptr, X3);
-        for (int e = tid; e < 128 * M; e += kTcThreads) {
-            const int rr = e / M;
-            const float lg = rr < nq ? a.la[(hoff + j0 + rr) * M + (e % M)] : 0.0f;
-            sB[e] = lg;
-            sU[e] = -expm1f(lg);
+        load_tile_async<D>(q, tbase, nq, X0);
+        load_tile_async<D>(k, j0, nq, KB[0]);
+        load_tile_async<D>(v, j0, nq, VB[0]);
+        cp_async_commit();
+        const float* SK1 = a.SK + ((size_t)bh * sh.NC + c1) * M * D;
+        const float* SV1 = a.SV + ((size_t)bh * sh.NC + c1) * M * D;
+        load_state_pair<D, M>(SK1, has2 ? SK1 + M * D : nullptr, KB[1]);
+        float lg[HM], b[HM], rho[HM];
+        row_gates<M>(a.la + (hoff + j0 + r) * M, row_ok, lg, b, s_tot, sG, warp, lane, h, r, nq);
+        {
+            float ek[HM];
+#pragma unroll
+            for (int jj = 0; jj < HM; jj++) {
+                rho[jj] = 0.5f * sG[cr * M + h * HM + jj];
+                ek[jj] = row_ok ? expf(rho[jj] - b[jj]) * (-expm1f(lg[jj])) : 0.0f;
+            }
+            store_row(VB[1], r, h * HM, ek, HM);
         }
+        cp_async_wait<0>();
         sync_for_mma();
         if (tid == 0) {
-            const uint32_t s0 = smem_u32(X0), s1 = smem_u32(X1), s3 = smem_u32(X3);
+            const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[0]), s3 = smem_u32(KB[1]);
             for (int kk = 0; kk < D / 16; kk++)
                 mma_bf16(tm + tA, desc_k(s0, 128, kk), desc_k(s1, 128, kk), idesc_bf16(128, 128, false), kk > 0);
             for (int kk = 0; kk < D / 16; kk++)
                 mma_bf16(tm + tO, desc_k(s0, 128, kk), desc_k(s3, 2 * M, kk), idesc_bf16(128, 2 * M, false), kk > 0);
             mma_commit(&bar);
         }
-        // chunk-local inclusive cumsum of log_alpha, per slot (overlaps the MMAs)
-        if (tid < 2 * M) {
-            const int i = tid % M, cc = tid / M;
-            const int r0 = cc * kChunk, r1 = min(nq, r0 + kChunk);
-            float b = 0.0f;
-            for (int rr = r0; rr < r1; rr++) {
-                b += sB[rr * M + i];
-                sB[rr * M + i] = b;
-            }
-            sRho[cc * M + i] = 0.5f * b;
-        }
-        __syncthreads();
-        // Ek tile [128 s][M] in X2
-        for (int e = tid; e < 128 * (M / 8); e += kTcThreads) {
-            const int s = e / (M / 8), ch = e % (M / 8);
-            float f[8];
-#pragma unroll
-            for (int jj = 0; jj < 8; jj++) {
-                const int i = ch * 8 + jj;
-                f[jj] = s < nq ? expf(sRho[(s >> 6) * M + i] - sB[s * M + i]) * sU[s * M + i] : 0.0f;
-            }
-            *reinterpret_cast<uint4*>(X2 + sw_chunk(s, ch, 128)) = pack8(f);
-        }
         ok = ctl.wait();
         if (ok) {
-            // A = Q K_c^T, masked to the row's own chunk and s <= r
-            float vv[64];
-            tmem_ld(tl + tA + 64 * h, vv, 64);
-#pragma unroll
-            for (int jj = 0; jj < 64; jj++) {
-                const int col = 64 * h + jj;
-                if (!(h == cr && col <= r && r < nq)) vv[jj] = 0.0f;
-            }
-            store_row(X1, r, 64 * h, vv, 64);
-            // Sint (this row's chunk half) is kept in TMEM until the logits
-            load_state_pair<D, M>(a.SV + ((size_t)bh * sh.NC + c1) * M * D,
-                                  has2 ? a.SV + ((size_t)bh * sh.NC + c1 + 1) * M * D : nullptr, X3);
-        }
-        if (ok) {
+            // A = Q K_c^T masked to the row's own chunk and s <= r; [S^V] replaces [S^K]
+            mask_to_tile(tl + tA, KB[0], r, h, cr, row_ok, false);
+            load_state_pair<D, M>(SV1, has2 ? SV1 + M * D : nullptr, KB[1]);
             sync_for_mma();
             if (tid == 0) {
-                const uint32_t s1 = smem_u32(X1), s2 = smem_u32(X2);
+                const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[1]);
                 for (int kk = 0; kk < 8; kk++)
                     mma_bf16(tm + tA, desc_k(s1, 128, kk), desc_mn(s2, 128, kk), idesc_bf16(128, M, true), kk > 0);
                 mma_commit(&bar);
@@ -170,63 +151,45 @@ fwd_tc_kernel(const FwdArgs a, const float2* __restrict__ tab, int* __restrict__
             float mx = -INFINITY;
 #pragma unroll
             for (int jj = 0; jj < HM; jj++) {
-                const int i = h * HM + jj;
-                const float bb = sB[r * M + i];
-                const float eq = expf(bb - sRho[cr * M + i]);
-                const float eb = expf(bb);
-                L[jj] = (r < nq) ? sig2 * (eb * sint[jj] + eq * lin[jj]) : -INFINITY;
+                L[jj] = row_ok ? sig2 * (expf(b[jj]) * sint[jj] + expf(b[jj] - rho[jj]) * lin[jj]) : -INFINITY;
                 mx = fmaxf(mx, L[jj]);
             }
             redm[h * 128 + r] = mx;
             __syncthreads();
             m = fmaxf(redm[r], redm[128 + r]);
-            float ps = 0.0f, pe[HM], pq[HM];
+            float ps = 0.0f, pe[HM], pq[HM], z[HM];
 #pragma unroll
             for (int jj = 0; jj < HM; jj++) {
-                const int i = h * HM + jj;
                 const float p = (m == -INFINITY) ? 0.0f : ex2(L[jj] - m);
                 ps += p;
-                const float bb = sB[r * M + i];
-                pe[jj] = p * expf(bb);
-                pq[jj] = p * expf(bb - sRho[cr * M + i]);
+                pe[jj] = p * expf(b[jj]);
+                pq[jj] = p * expf(b[jj] - rho[jj]);
+                z[jj] = 0.0f;
             }
             reds[h * 128 + r] = ps;
-            // A_inter [128][2M] in X1: this row's chunk block holds p o Eb, the other block zero
-            float z[HM];
-#pragma unroll
-            for (int jj = 0; jj < HM; jj++) z[jj] = 0.0f;
-            store_row(X1, r, cr * M + h * HM, pe, HM);
-            store_row(X1, r, (1 - cr) * M + h * HM, z, HM);
-            // pEq [128][M] in the second half of X2 (after Ek; a 128-row swizzled
-            // tile spans 16 KB whatever its width)
-            store_row(X2 + 16384, r, h * HM, pq, HM);
+            // A_inter [128][2M]: this row's chunk block holds p o Eb, the other block zero
+            store_row(KB[0], r, cr * M + h * HM, pe, HM);
+            store_row(KB[0], r, (1 - cr) * M + h * HM, z, HM);
+            store_row(VB[1] + 16384, r, h * HM, pq, HM);  // pEq, after Ek
             __syncthreads();
             l = reds[r] + reds[128 + r];
             sync_for_mma();
             if (tid == 0) {
-                const uint32_t s1 = smem_u32(X1), s2 = smem_u32(X2), s3 = smem_u32(X3);
+                const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[1]), s3 = smem_u32(KB[1]);
                 for (int kk = 0; kk < 2 * M / 16; kk++)
                     mma_bf16(tm + tO, desc_k(s1, 128, kk), desc_mn(s3, 2 * M, kk), idesc_bf16(128, D, true), kk > 0);
                 for (int kk = 0; kk < M / 16; kk++)
-                    mma_bf16(tm + tA, desc_k(s2 + 16384, 128, kk), desc_k(s2, 128, kk),
-                             idesc_bf16(128, 128, false), kk > 0);
+                    mma_bf16(tm + tA, desc_k(s2 + 16384, 128, kk), desc_k(s2, 128, kk), idesc_bf16(128, 128, false),
+                             kk > 0);
                 mma_commit(&bar);
             }
             ok = ctl.wait();
         }
         if (ok) {
-            float vv[64];
-            tmem_ld(tl + tA + 64 * h, vv, 64);
-#pragma unroll
-            for (int jj = 0; jj < 64; jj++) {
-                const int col = 64 * h + jj;
-                if (!(h == cr && col <= r && r < nq)) vv[jj] = 0.0f;
-            }
-            store_row(X1, r, 64 * h, vv, 64);
-            load_tile<D>(v, j0, nq, X2, nullptr);
+            mask_to_tile(tl + tA, KB[0], r, h, cr, row_ok, false);
             sync_for_mma();
             if (tid == 0) {
-                const uint32_t s1 = smem_u32(X1), s2 = smem_u32(X2);
+                const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[0]);
                 for (int kk = 0; kk < 8; kk++)
                     mma_bf16(tm + tO, desc_k(s1, 128, kk), desc_mn(s2, 128, kk), idesc_bf16(128, D, true), 1);
                 mma_commit(&bar);
@@ -234,25 +197,33 @@ fwd_tc_kernel(const FwdArgs a, const float2* __restrict__ tab, int* __restrict__
             ok = ctl.wait();
             o_valid = true;
         }
-        if (ok) rotate_tile<D>(X0, tbase, nq, tab);
-    } else {
-        load_tile<D>(q, tbase, nq, X0, tab);
     }
 
-    // ---- window branch over the band of keys [tbase - w + 1, tbase + nq - 1]
+    // ---- window branch over the band of keys [tbase - w + 1, tbase + nq - 1],
+    // key/value blocks double-buffered: block i + 1 loads while block i computes
     if (ok && sh.w > 0) {
         const int klo = max(0, tbase - sh.w + 1), khi = tbase + nq - 1;
+        const int nb = (khi - klo) / 128 + 1;
         const int t = tbase + r;
-        for (int kb = klo; kb <= khi && ok; kb += 128) {
-            const int nk = min(128, khi - kb + 1);
-            load_tile<D>(k, kb, nk, X1, tab);
-            load_tile<D>(v, kb, nk, X2, nullptr);
+        load_tile_async<D>(qr, tbase, nq, X0);
+        load_tile_async<D>(kr, klo, min(128, khi - klo + 1), KB[0]);
+        load_tile_async<D>(v, klo, min(128, khi - klo + 1), VB[0]);
+        cp_async_commit();
+        for (int i = 0; i < nb && ok; i++) {
+            const int kb = klo + i * 128, nk = min(128, khi - kb + 1), cur = i & 1;
+            cp_async_wait<0>();
             sync_for_mma();
             if (tid == 0) {
-                const uint32_t s0 = smem_u32(X0), s1 = smem_u32(X1);
+                const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[cur]);
                 for (int kk = 0; kk < D / 16; kk++)
                     mma_bf16(tm + tA, desc_k(s0, 128, kk), desc_k(s1, 128, kk), idesc_bf16(128, 128, false), kk > 0);
                 mma_commit(&bar);
+            }
+            if (i + 1 < nb) {  // the other stage was last read by block i - 1's P V (complete)
+                const int kn = kb + 128, nn = min(128, khi - kn + 1);
+                load_tile_async<D>(kr, kn, nn, KB[cur ^ 1]);
+                load_tile_async<D>(v, kn, nn, VB[cur ^ 1]);
+                cp_async_commit();
             }
             ok = ctl.wait();
             if (!ok) break;
@@ -262,7 +233,7 @@ fwd_tc_kernel(const FwdArgs a, const float2* __restrict__ tab, int* __restrict__
 #pragma unroll
             for (int jj = 0; jj < 64; jj++) {
                 const int c = 64 * h + jj, key = kb + c;
-                const bool valid = r < nq && c < nk && key <= t && key > t - sh.w;
+                const bool valid = row_ok && c < nk && key <= t && key > t - sh.w;
                 sv[jj] = valid ? sv[jj] * sig2 : -INFINITY;
                 bm = fmaxf(bm, sv[jj]);
             }
@@ -297,11 +268,11 @@ fwd_tc_kernel(const FwdArgs a, const float2* __restrict__ tab, int* __restrict__
                 ps += p;
             }
             reds[h * 128 + r] = ps;
-            store_row(X1, r, 64 * h, sv, 64);
+            store_row(KB[cur], r, 64 * h, sv, 64);
             sync_for_mma();
             l += reds[r] + reds[128 + r];
             if (tid == 0) {
-                const uint32_t s1 = smem_u32(X1), s2 = smem_u32(X2);
+                const uint32_t s1 = smem_u32(KB[cur]), s2 = smem_u32(VB[cur]);
                 for (int kk = 0; kk < 8; kk++)
                     mma_bf16(tm + tO, desc_k(s1, 128, kk), desc_mn(s2, 128, kk), idesc_bf16(128, D, true),
                              (o_valid || kk > 0) ? 1u : 0u);
@@ -310,6 +281,7 @@ fwd_tc_kernel(const FwdArgs a, const float2* __restrict__ tab, int* __restrict__
             o_valid = true;
             ok = ctl.wait();
         }
+        cp_async_wait<0>();
     }
 
     // ---- epilogue: o = O / l, lse = m ln2 + log l
@@ -320,7 +292,7 @@ fwd_tc_kernel(const FwdArgs a, const float2* __restrict__ tab, int* __restrict__
         for (int c0 = 0; c0 < HD; c0 += 32) {
             float ov[32];
             tmem_ld32(tl + tO + h * HD + c0, ov);
-            if (r < nq) {
+            if (row_ok) {
 #pragma unroll
                 for (int jj = 0; jj < 32; jj++) ov[jj] *= inv;
 #pragma unroll
@@ -328,8 +300,8 @@ fwd_tc_kernel(const FwdArgs a, const float2* __restrict__ tab, int* __restrict__
                     *reinterpret_cast<uint4*>(orow + h * HD + c0 + qq * 8) = pack8(ov + qq * 8);
             }
         }
-        if (h == 0 && r < nq) a.lse[hoff + t] = m * kLn2 + logf(l);
-    } else if (h == 0 && r < nq) {
+        if (h == 0 && row_ok) a.lse[hoff + t] = m * kLn2 + logf(l);
+    } else if (h == 0 && row_ok) {
         a.lse[hoff + tbase + r] = __int_as_float(0x7fc00000);  // NaN marks the failed tile
     }
     if (!ok && tid == 0) mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);  // let in-flight MMAs drain
@@ -337,6 +309,45 @@ fwd_tc_kernel(const FwdArgs a, const float2* __restrict__ tab, int* __restrict__
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 256);
 }
+
+// RoPE applied once per call: qr = RoPE(q), kr = RoPE(k) at absolute positions.
+template <int D>
+__global__ void __launch_bounds__(256)
+rope_qk_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+               __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr, const float2* __restrict__ tab,
+               long rows, int T) {
+    constexpr int H = D / 2, CHH = D / 16;
+    const long e = (long)blockIdx.x * 256 + threadIdx.x;
+    if (e >= rows * CHH) return;
+    const long row = e / CHH;
+    const int ch = (int)(e % CHH), pos = (int)(row % T);
+    const float2* cs = tab + (size_t)pos * H + ch * 8;
+#pragma unroll
+    for (int which = 0; which < 2; which++) {
+        const __nv_bfloat16* src = (which == 0 ? q : k) + row * D;
+        __nv_bfloat16* dst = (which == 0 ? qr : kr) + row * D;
+        float x[8], y[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(src + ch * 8)), x);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(src + H + ch * 8)), y);
+        rotate8(x, y, cs);
+        *reinterpret_cast<uint4*>(dst + ch * 8) = pack8(x);
+        *reinterpret_cast<uint4*>(dst + H + ch * 8) = pack8(y);
+    }
+}
+
+template <int D>
+cudaError_t launch_rope_qk(const void* q, const void* k, __nv_bfloat16* qr, __nv_bfloat16* kr, const float2* tab,
+                           const Shape& sh, cudaStream_t st) {
+    const long rows = (long)sh.BH * sh.T, n = rows * (D / 16);
+    NHA_LAUNCH("rope_qk", st,
+               rope_qk_kernel<D><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
+                   (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, qr, kr, tab, rows, sh.T));
+    return cudaGetLastError();
+}
+template cudaError_t launch_rope_qk<64>(const void*, const void*, __nv_bfloat16*, __nv_bfloat16*, const float2*,
+                                        const Shape&, cudaStream_t);
+template cudaError_t launch_rope_qk<128>(const void*, const void*, __nv_bfloat16*, __nv_bfloat16*, const float2*,
+                                         const Shape&, cudaStream_t);
 
 cudaError_t launch_rope_table(float2* tab, int T, int H2, const RopeTab& rt, cudaStream_t st) {
     const int n = T * H2;
@@ -346,17 +357,19 @@ cudaError_t launch_rope_table(float2* tab, int T, int H2, const RopeTab& rt, cud
 
 template <int D, int M>
 size_t tc_fwd_smem() {
-    return 1024 + 128 * D * 2 + 32768 + 32768 + 2 * M * D * 2 + sizeof(float) * (2 * 128 * M + 2 * M + 512);
+    return 1024 + 128 * D * 2 + 4 * 32768 + sizeof(float) * (6 * M + 512);
 }
 
 template <int D, int M>
-cudaError_t tc_forward(const FwdArgs& a, float2* tab, int* status, cudaStream_t st) {
+cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bfloat16* kr, int* status,
+                       cudaStream_t st) {
     const Shape& sh = a.sh;
-    cudaError_t e = simt_states<__nv_bfloat16, D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
-                                                     a.la, a.SK, a.SV, a.G, sh, st);
+    cudaError_t e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV, a.G,
+                                    sh, status, st);
     if (e != cudaSuccess) return e;
     e = launch_rope_table(tab, sh.T, D / 2, a.rope, st);
     if (e != cudaSuccess) return e;
+    if (sh.w > 0 && (e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, sh, st)) != cudaSuccess) return e;
     const int W0 = sh.T - sh.R;
     const int tiles = (W0 + 127) / 128 + (sh.R + 127) / 128;
     const size_t sm = tc_fwd_smem<D, M>();
@@ -364,11 +377,12 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, int* status, cudaStream_t 
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     if (tiles > 0)
-        NHA_LAUNCH("fwd_tc", st, kern<<<dim3(tiles, sh.BH), kTcThreads, sm, st>>>(a, tab, status));
+        NHA_LAUNCH("fwd_tc", st, kern<<<dim3(tiles, sh.BH), kTcThreads, sm, st>>>(a, qr, kr, status));
     return cudaGetLastError();
 }
 
-#define NHA_TC_INST(D, M) template cudaError_t tc_forward<D, M>(const FwdArgs&, float2*, int*, cudaStream_t);
+#define NHA_TC_INST(D, M) \
+    template cudaError_t tc_forward<D, M>(const FwdArgs&, float2*, __nv_bfloat16*, __nv_bfloat16*, int*, cudaStream_t);
 NHA_TC_INST(64, 16)
 NHA_TC_INST(64, 32)
 NHA_TC_INST(64, 64)

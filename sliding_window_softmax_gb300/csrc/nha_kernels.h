@@ -65,8 +65,13 @@ template <typename Tin, int D, int M>
 cudaError_t simt_forward(const FwdArgs& a, cudaStream_t st);
 // bf16 tensor-core forward; tab: RoPE (cos, sin) table [T][D/2] in the workspace,
 // status: device word set non-zero if a kernel gave up waiting on its tensor core.
+// qr, kr: workspace [BH][T][D] bf16 for RoPE(q), RoPE(k).
 template <int D, int M>
-cudaError_t tc_forward(const FwdArgs& a, float2* tab, int* status, cudaStream_t st);
+cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bfloat16* kr, int* status,
+                       cudaStream_t st);
+template <int D>
+cudaError_t launch_rope_qk(const void* q, const void* k, __nv_bfloat16* qr, __nv_bfloat16* kr, const float2* tab,
+                           const Shape& sh, cudaStream_t st);
 template <typename Tin, int D, int M>
 cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st);
 // Slot-branch backward (query side, reverse adjoint scan, key side, dlog_alpha
@@ -84,6 +89,13 @@ template <int D>
 cudaError_t launch_wkv(const BwdArgs& a, const float2* tab, int* status, cudaStream_t st);
 cudaError_t launch_state_scan_rev(const BwdArgs& a, int M, int D, cudaStream_t st);
 cudaError_t launch_dla_carry(const BwdArgs& a, int M, int D, cudaStream_t st);
+// bf16 path: chunk states on the tensor core, then the forward chunk scan.
+template <int D, int M>
+cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const float* la, float* SK, float* SV,
+                      float* G, const Shape& sh, int* status, cudaStream_t st);
+// Chunk scan (dir > 0: states before each chunk; dir < 0: adjoints carried in).
+cudaError_t launch_scan8(float* X0, float* X1, const float* G, const Shape& sh, int M, int D, int dir,
+                         cudaStream_t st);
 // RoPE (cos, sin) table [T][H2] of the absolute positions.
 cudaError_t launch_rope_table(float2* tab, int T, int H2, const RopeTab& rt, cudaStream_t st);
 

@@ -32,96 +32,6 @@ __host__ __device__ constexpr uint32_t idesc_am(int M, int N, bool a_mn, bool b_
     return idesc_bf16(M, N, b_mn) | ((a_mn ? 1u : 0u) << 15);
 }
 
-// Inclusive cumsum of x over the 64 rows of this thread's chunk (tile rows
-// 0-63 or 64-127), for the HM slots i = h HM + jj.  s_tot: [4][M] scratch.
-template <int M>
-__device__ __forceinline__ void chunk_prefix(float (&x)[M / 2], float* s_tot, int warp, int lane, int h) {
-    constexpr int HM = M / 2;
-    const int wq = warp & 3;
-#pragma unroll
-    for (int jj = 0; jj < HM; jj++) {
-        float v = x[jj];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, v, off);
-            if (lane >= off) v += y;
-        }
-        x[jj] = v;
-        if (lane == 31) s_tot[wq * M + h * HM + jj] = v;
-    }
-    __syncthreads();
-    if (wq & 1)
-#pragma unroll
-        for (int jj = 0; jj < HM; jj++) x[jj] += s_tot[(wq - 1) * M + h * HM + jj];
-    __syncthreads();
-}
-
-// Inclusive suffix sum of x over the 64 rows of this thread's chunk.
-template <int M>
-__device__ __forceinline__ void chunk_suffix(float (&x)[M / 2], float* s_tot, int warp, int lane, int h) {
-    constexpr int HM = M / 2;
-    const int wq = warp & 3;
-#pragma unroll
-    for (int jj = 0; jj < HM; jj++) {
-        float v = x[jj];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_down_sync(0xffffffffu, v, off);
-            if (lane + off < 32) v += y;
-        }
-        x[jj] = v;
-        if (lane == 0) s_tot[wq * M + h * HM + jj] = v;
-    }
-    __syncthreads();
-    if (!(wq & 1))
-#pragma unroll
-        for (int jj = 0; jj < HM; jj++) x[jj] += s_tot[(wq + 1) * M + h * HM + jj];
-    __syncthreads();
-}
-
-// Gates of this thread's row: loads log_alpha (0 past the valid rows), the
-// chunk-local cumsum b and the chunk totals sG[2][M] (zero for an empty chunk).
-template <int M>
-__device__ __forceinline__ void row_gates(const float* __restrict__ la_row, bool valid, float (&l)[M / 2],
-                                          float (&b)[M / 2], float* s_tot, float* sG, int warp, int lane,
-                                          int h, int r, int nrows) {
-    constexpr int HM = M / 2;
-#pragma unroll
-    for (int jj = 0; jj < HM; jj += 4) {
-        const float4 v = valid ? __ldg(reinterpret_cast<const float4*>(la_row + h * HM + jj))
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-        l[jj] = v.x; l[jj + 1] = v.y; l[jj + 2] = v.z; l[jj + 3] = v.w;
-    }
-#pragma unroll
-    for (int jj = 0; jj < HM; jj++) b[jj] = l[jj];
-    chunk_prefix<M>(b, s_tot, warp, lane, h);
-    const int cc = r >> 6, last = min(nrows, 64 * (cc + 1)) - 1;
-    if (r == last)
-#pragma unroll
-        for (int jj = 0; jj < HM; jj++) sG[cc * M + h * HM + jj] = b[jj];
-    __syncthreads();
-}
-
-__device__ __forceinline__ void zero_cols(unsigned char* tile, int row, int c0, int c1) {
-    for (int c = c0; c < c1; c += 8)
-        *reinterpret_cast<uint4*>(tile + sw_chunk(row, c >> 3, 128)) = make_uint4(0, 0, 0, 0);
-}
-
-// Masked copy of 64 TMEM columns (this half's) into a bf16 tile row:
-// keep (row, col) iff h == own chunk and (upper ? col >= row : col <= row).
-__device__ __forceinline__ void mask_to_tile(uint32_t taddr, unsigned char* tile, int r, int h, int cr,
-                                             bool row_ok, bool upper) {
-    float vv[64];
-    tmem_ld(taddr + 64 * h, vv, 64);
-#pragma unroll
-    for (int jj = 0; jj < 64; jj++) {
-        const int col = 64 * h + jj;
-        const bool keep = row_ok && h == cr && (upper ? col >= r : col <= r);
-        if (!keep) vv[jj] = 0.0f;
-    }
-    store_row(tile, r, 64 * h, vv, 64);
-}
-
 // ---------------------------------------------------------------------------------------
 template <int D, int M>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -608,7 +518,7 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const float2* tab, int* status, cudaSt
     }
     if ((e = launch_wkv<D>(a, tab, status, st)) != cudaSuccess) return e;
     if (sh.NC > 0) {
-        if ((e = launch_state_scan_rev(a, M, D, st)) != cudaSuccess) return e;
+        if ((e = launch_scan8(a.RK, a.RV, a.G, sh, M, D, -1, st)) != cudaSuccess) return e;
     }
     {
         auto kern = bwd_sk_tc_kernel<D, M>;

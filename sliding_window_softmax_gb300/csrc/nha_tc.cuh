@@ -209,6 +209,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
     }
 }
 
+// ---- cp.async (16-byte global -> shared copies; src_bytes = 0 zero-fills) ----
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 // 2^x on the MUFU (ex2.approx, flushes denormals to zero; 2^-inf = 0).
 __device__ __forceinline__ float ex2(float x) {
     float y;
