@@ -94,6 +94,33 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
                           int C, nha_dtype_t dtype, float rope_base, void* workspace,
                           size_t ws_bytes, void* stream);
 
+/* ---- Forward without device allocation (the pages have no counterpart) ----
+ *
+ * Some callers cannot allocate device memory: code that runs while a CUDA
+ * graph is being captured, plugins that receive only their input and output
+ * buffers from a host framework, or processes whose device memory belongs to
+ * an allocator they may not call.  nha_forward_noalloc is nha_forward with
+ * its workspace taken from a fixed scratch array of NHA_NOALLOC_SCRATCH_BYTES
+ * compiled into the library (every GPU that loads the library keeps that
+ * array until the process exits).  It allocates and frees nothing.
+ *
+ * Limit: shapes whose forward workspace (nha_workspace_bytes(..., 0)) exceeds
+ * NHA_NOALLOC_SCRATCH_BYTES are rejected with NHA_ERR_WORKSPACE before any
+ * work is enqueued; 32 MiB covers, e.g., B*H = 8 heads of T = 2048 at
+ * d = 128, m = 64.
+ * Set-up: the first call on a device looks up the scratch's device address on
+ * the current device (cudaGetSymbolAddress); make that first call before any
+ * stream capture.
+ * Sharing: all calls use the same scratch, which keeps the last call's
+ * contents (the forward overwrites every part it reads, so nothing has to
+ * start at zero).  Calls whose execution overlaps on the GPU (different
+ * streams, or concurrent host threads) race on it: serialise them. */
+#define NHA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+nha_status_t nha_forward_noalloc(const void* q, const void* k, const void* v, const float* log_alpha,
+                                 void* o, float* lse, int B, int H, int T, int d, int m, int w, int C,
+                                 nha_dtype_t dtype, float rope_base, void* stream);
+
 /* ---- Instrumentation (the pages have no counterpart; used by the benchmark) ---- */
 
 /* Number of kernels this library has launched in this process so far. */

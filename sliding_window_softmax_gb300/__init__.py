@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     load_library,
     nha_backward,
     nha_forward,
+    nha_forward_noalloc,
     nha_workspace_bytes,
     profile_begin,
     profile_end,

@@ -25,7 +25,7 @@ STATUS = {0: "NHA_OK", 1: "NHA_ERR_INVALID_ARGUMENT", 2: "NHA_ERR_UNSUPPORTED",
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 
 # Every symbol include/nha.h declares (checked by the tests).
-EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward", "nha_launch_count",
+EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward", "nha_forward_noalloc", "nha_launch_count",
            "nha_profile_begin", "nha_profile_end", "nha_status_string", "nha_last_error")
 
 _lock = threading.Lock()
@@ -83,6 +83,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.nha_forward.argtypes = [vp] * 6 + [i] * 8 + [f, vp, sz, vp]
         lib.nha_backward.restype = i
         lib.nha_backward.argtypes = [vp] * 11 + [i] * 8 + [f, vp, sz, vp]
+        lib.nha_forward_noalloc.restype = i
+        lib.nha_forward_noalloc.argtypes = [vp] * 6 + [i] * 8 + [f, vp]
         lib.nha_status_string.restype = ctypes.c_char_p
         lib.nha_status_string.argtypes = [i]
         lib.nha_last_error.restype = ctypes.c_char_p
@@ -154,6 +156,32 @@ def nha_forward(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 1000
     rc = lib.nha_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(lse),
                          B, H, T, d, m, int(w), int(C), DTYPE[dt], float(rope_base),
                          _ptr(workspace), ws_bytes, _stream_handle(stream))
+    _raise(lib, rc)
+    return o, lse
+
+
+def nha_forward_noalloc(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 10000.0,
+                        o=None, lse=None, stream=None):
+    """nha_forward using the library's built-in scratch (no workspace argument).
+
+    For callers that cannot allocate device memory; see include/nha.h for the
+    size limit and the sharing rules."""
+    lib = load_library()
+    B, H, T, d = q.shape
+    m = log_alpha.shape[-1]
+    dt = q.dtype
+    if dt not in DTYPE:
+        raise TypeError(f"unsupported dtype {dt}")
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check(n, t, dt, (B, H, T, d))
+    _check("log_alpha", log_alpha, torch.float32, (B, H, T, m))
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check("o", o, dt, (B, H, T, d))
+    _check("lse", lse, torch.float32, (B, H, T))
+    rc = lib.nha_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(lse),
+                                 B, H, T, d, m, int(w), int(C), DTYPE[dt], float(rope_base),
+                                 _stream_handle(stream))
     _raise(lib, rc)
     return o, lse
 

@@ -176,6 +176,16 @@ cudaError_t run_backward(const Plan& p, const nha::BwdArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+namespace nha {
+nha_status_t set_error(nha_status_t s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return s;
+}
+}  // namespace nha
+
 extern "C" {
 
 size_t nha_workspace_bytes(int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dtype,

@@ -6,7 +6,12 @@
 
 #include "nha_common.cuh"
 
+#include "nha.h"
+
 namespace nha {
+
+// Records the thread-local message returned by nha_last_error and returns s.
+nha_status_t set_error(nha_status_t s, const char* fmt, ...);
 
 // Forward arguments.  q, k, v, o are [BH, T, D] in the element type; la is
 // [BH, T, M]; lse [BH, T].  Workspace: SK, SV [BH, NC, M, D] and G [BH, NC, M].

@@ -127,3 +127,13 @@ def test_product_does_not_import_the_oracle():
             src = open(os.path.join(dirpath, f), errors="ignore").read()
             assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
             assert "nha_oracle" not in src, f
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch(lib):
+    # 2 x 16 heads of 2048 tokens at d = 128, m = 64 need more than the 32 MiB
+    # built-in scratch: rejected during validation, before any CUDA call.
+    p = ctypes.c_void_p(4096)
+    rc = lib.nha_forward_noalloc(p, p, p, p, p, p, 2, 16, 2048, 128, 64, 512, 64, 1, 10000.0, None)
+    assert rc == 3 and b"built-in scratch" in lib.nha_last_error()
+    # an invalid shape reports its own reason
+    assert lib.nha_forward_noalloc(p, p, p, p, p, p, 1, 1, 16, 96, 16, 4, 64, 1, 10000.0, None) == 2
