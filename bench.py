@@ -62,14 +62,20 @@ def work_model(wl):
     fwd_flops = BH * (4 * d * n_sum + 8 * m * d * R)
     fwd_bytes = BH * T * (4 * d * e + 4 * m + 4)
     bwd_bytes = BH * T * (8 * d * e + 8 * m + 4)
+    fwd_main = (BH * (4 * d * n_sum + 4 * m * d * R), fwd_bytes)
+    wdq = (BH * 6 * d * n_sum, BH * T * (5 * d * e + 8))
+    wkv = (BH * 8 * d * n_sum, BH * T * (6 * d * e + 8))
+    sq = (BH * 12 * m * d * R, BH * T * (3 * d * e + 4 * m + 8))
+    sk = (BH * 12 * m * d * R, BH * T * (6 * d * e + 8 * m))
     k = {
-        # name: (flops, bytes) per launch
-        "fwd_main": (BH * (4 * d * n_sum + 4 * m * d * R), fwd_bytes),
+        # name: (algorithmic flops, algorithmic bytes) per launch; the tensor-core
+        # (bf16) and SIMT (fp32) kernels of the same step share a model
+        "fwd_tc": fwd_main, "fwd_main": fwd_main,
         "state_chunk": (BH * 4 * m * d * R, BH * R * (2 * d * e + 4 * m)),
-        "bwd_window_dq": (BH * 6 * d * n_sum, BH * T * (5 * d * e + 8)),
-        "bwd_window_dkdv": (BH * 8 * d * n_sum, BH * T * (6 * d * e + 8)),
-        "bwd_slot_query": (BH * 12 * m * d * R, BH * T * (3 * d * e + 4 * m + 8)),
-        "bwd_slot_key": (BH * 12 * m * d * R, BH * T * (6 * d * e + 8 * m)),
+        "bwd_wdq_tc": wdq, "bwd_window_dq": wdq,
+        "bwd_wkv_tc": wkv, "bwd_window_dkdv": wkv,
+        "bwd_sq_tc": sq, "bwd_slot_query": sq,
+        "bwd_sk_tc": sk, "bwd_slot_key": sk,
     }
     return dict(fwd_flops=fwd_flops, fwd_bytes=fwd_bytes, step_flops=3.5 * fwd_flops,
                 step_bytes=fwd_bytes + bwd_bytes, kernels=k, n_sum=n_sum, R=R)
@@ -113,7 +119,8 @@ def ncu_traffic(kernel: str, workload_key: str):
 
 # ----------------------------------------------------------------------------------------
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every 100 ms; summary() keeps those taken inside the
+    timed region (or the three nearest to it when the region is shorter)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -122,13 +129,14 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time, csv line)
+        self.window = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -138,7 +146,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0: float, t1: float):
+        """The timed region, in host time.time() seconds."""
+        self.window = (t0, t1)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -152,7 +164,14 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines
+        if self.window is not None:
+            inside = [x for x in lines if self.window[0] <= x[0] <= self.window[1]]
+            if len(inside) < 3:  # too short a region: take the samples nearest to it
+                mid = 0.5 * (self.window[0] + self.window[1])
+                inside = sorted(lines, key=lambda x: abs(x[0] - mid))[:3]
+            lines = inside
+        for _, ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -243,6 +262,7 @@ def run_nha(args, wl, wl_key):
     import torch.distributed as dist
 
     import sliding_window_softmax_gb300 as nha
+    from sliding_window_softmax_gb300.dist import max_over_ranks
     from sliding_window_softmax_gb300.synthetic import make_inputs
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -280,6 +300,7 @@ def run_nha(args, wl, wl_key):
                              wl.C, dq=dq, dk=dk, dv=dv, dlog_alpha=dla, workspace=wsb,
                              stream=stream)
 
+    clk = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -290,27 +311,26 @@ def run_nha(args, wl, wl_key):
     barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    with ClockSampler(local) as clk:
-        n0 = nha.launch_count()
-        nha.profile_begin()
-        for i in range(K):
-            flush.zero_()  # L2 flush between timed steps, outside the step's events
-            ev[i][0].record(stream)
-            step(ev[i][1])
-            ev[i][2].record(stream)
-        torch.cuda.synchronize()
-        prof = nha.profile_end()
-        launches = nha.launch_count() - n0
+    t_start = time.time()
+    n0 = nha.launch_count()
+    nha.profile_begin()
+    for i in range(K):
+        flush.zero_()  # L2 flush between timed steps, outside the step's events
+        ev[i][0].record(stream)
+        step(ev[i][1])
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    prof = nha.profile_end()
+    launches = nha.launch_count() - n0
+    clk.mark(t_start, time.time())
+    clk.__exit__(None, None, None)
     wall = time.perf_counter() - wall0
     barrier()
     step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
     fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     ms = statistics.mean(step_ms)
     ms_fwd = statistics.mean(fwd_ms)
-    if world > 1:
-        t = torch.tensor([ms, ms_fwd], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_fwd = float(t[0]), float(t[1])
+    ms, ms_fwd = max_over_ranks([ms, ms_fwd], device=dev)
 
     # ---- end to end through the public API with pinned host buffers
     hin = {n: t.pin_memory() for n, t in x.items()}
@@ -345,10 +365,7 @@ def run_nha(args, wl, wl_key):
         e_ev[i][1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e_ev)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    (e2e_ms,) = max_over_ranks([e2e_ms], device=dev)
 
     if rank == 0:
         model = work_model(wl)
@@ -411,8 +428,8 @@ def run_nha(args, wl, wl_key):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="1.3B")
     ap.add_argument("--impl", default="nha", choices=["nha", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
