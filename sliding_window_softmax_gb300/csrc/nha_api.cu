@@ -40,7 +40,7 @@ struct Plan {
     nha::Shape sh;
     int d, m;
     // workspace offsets, in floats
-    size_t SK, SV, G, TAB, STATUS, QR, KR, Dv, Dhat, Dwin, dqwV, dqw, dkw, dvw, DL, PL, DB1, RK, RV, total;
+    size_t SK, SV, SKb, SVb, G, TAB, STATUS, QR, KR, Dv, Dhat, Dwin, dqwV, dqw, dkw, dvw, DL, PL, DB1, RK, RV, RKb, RVb, total;
 };
 
 nha_status_t check_shape(int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dt) {
@@ -81,6 +81,8 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward) {
     const size_t BH = (size_t)sh.BH, NC = (size_t)sh.NC, Tz = (size_t)T;
     p.SK = take(BH * NC * m * d);
     p.SV = take(BH * NC * m * d);
+    p.SKb = take(BH * NC * m * d / 2);
+    p.SVb = take(BH * NC * m * d / 2);
     p.G = take(BH * NC * m);
     p.TAB = take(Tz * (size_t)d);  // RoPE (cos, sin) per position and frequency
     p.STATUS = take(16);
@@ -99,6 +101,8 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward) {
         p.DB1 = take(BH * NC * nha::kChunk * m);
         p.RK = take(BH * NC * m * d);
         p.RV = take(BH * NC * m * d);
+        p.RKb = take(BH * NC * m * d / 2);
+        p.RVb = take(BH * NC * m * d / 2);
     }
     p.total = off;
     return p;
@@ -150,13 +154,15 @@ cudaError_t run_forward(const Plan& p, const nha::FwdArgs& a, cudaStream_t s) {
 cudaError_t run_backward_tc(const Plan& p, const nha::BwdArgs& a, float* ws, cudaStream_t s) {
     float2* tab = (float2*)(ws + p.TAB);
     int* status = (int*)(ws + p.STATUS);
+    __nv_bfloat16* qr = (__nv_bfloat16*)(ws + p.QR);
+    __nv_bfloat16* kr = (__nv_bfloat16*)(ws + p.KR);
     switch (p.d * 1000 + p.m) {
-        case 64016: return nha::tc_backward<64, 16>(a, tab, status, s);
-        case 64032: return nha::tc_backward<64, 32>(a, tab, status, s);
-        case 64064: return nha::tc_backward<64, 64>(a, tab, status, s);
-        case 128016: return nha::tc_backward<128, 16>(a, tab, status, s);
-        case 128032: return nha::tc_backward<128, 32>(a, tab, status, s);
-        case 128064: return nha::tc_backward<128, 64>(a, tab, status, s);
+        case 64016: return nha::tc_backward<64, 16>(a, tab, qr, kr, status, s);
+        case 64032: return nha::tc_backward<64, 32>(a, tab, qr, kr, status, s);
+        case 64064: return nha::tc_backward<64, 64>(a, tab, qr, kr, status, s);
+        case 128016: return nha::tc_backward<128, 16>(a, tab, qr, kr, status, s);
+        case 128032: return nha::tc_backward<128, 32>(a, tab, qr, kr, status, s);
+        case 128064: return nha::tc_backward<128, 64>(a, tab, qr, kr, status, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -223,6 +229,7 @@ nha_status_t nha_forward(const void* q, const void* k, const void* v, const floa
     nha::FwdArgs a;
     a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.o = o; a.lse = lse;
     a.SK = ws + p.SK; a.SV = ws + p.SV; a.G = ws + p.G;
+    a.SKb = (__nv_bfloat16*)(ws + p.SKb); a.SVb = (__nv_bfloat16*)(ws + p.SVb);
     a.sh = p.sh;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
@@ -264,6 +271,8 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
     a.dqw = ws + p.dqw; a.dkw = ws + p.dkw; a.dvw = ws + p.dvw;
     a.wsDL = ws + p.DL; a.wsPL = ws + p.PL; a.wsDB1 = ws + p.DB1;
     a.RK = ws + p.RK; a.RV = ws + p.RV;
+    a.SKb = (__nv_bfloat16*)(ws + p.SKb); a.SVb = (__nv_bfloat16*)(ws + p.SVb);
+    a.RKb = (__nv_bfloat16*)(ws + p.RKb); a.RVb = (__nv_bfloat16*)(ws + p.RVb);
     a.sh = p.sh;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;

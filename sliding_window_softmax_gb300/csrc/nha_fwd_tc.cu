@@ -102,13 +102,13 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
     if (slot) {
         const int c1 = j0 / kChunk;
         const bool has2 = nq > kChunk;
+        const __nv_bfloat16* SK1 = a.SKb + ((size_t)bh * sh.NC + c1) * M * D;
+        const __nv_bfloat16* SV1 = a.SVb + ((size_t)bh * sh.NC + c1) * M * D;
         load_tile_async<D>(q, tbase, nq, X0);
         load_tile_async<D>(k, j0, nq, KB[0]);
         load_tile_async<D>(v, j0, nq, VB[0]);
+        load_state_pair_async<D, M>(SK1, has2 ? SK1 + M * D : nullptr, KB[1]);
         cp_async_commit();
-        const float* SK1 = a.SK + ((size_t)bh * sh.NC + c1) * M * D;
-        const float* SV1 = a.SV + ((size_t)bh * sh.NC + c1) * M * D;
-        load_state_pair<D, M>(SK1, has2 ? SK1 + M * D : nullptr, KB[1]);
         float lg[HM], b[HM], rho[HM];
         row_gates<M>(a.la + (hoff + j0 + r) * M, row_ok, lg, b, s_tot, sG, warp, lane, h, r, nq);
         {
@@ -116,7 +116,7 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
 #pragma unroll
             for (int jj = 0; jj < HM; jj++) {
                 rho[jj] = 0.5f * sG[cr * M + h * HM + jj];
-                ek[jj] = row_ok ? expf(rho[jj] - b[jj]) * (-expm1f(lg[jj])) : 0.0f;
+                ek[jj] = row_ok ? fexp(rho[jj] - b[jj]) * (-expm1f(lg[jj])) : 0.0f;
             }
             store_row(VB[1], r, h * HM, ek, HM);
         }
@@ -134,7 +134,8 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
         if (ok) {
             // A = Q K_c^T masked to the row's own chunk and s <= r; [S^V] replaces [S^K]
             mask_to_tile(tl + tA, KB[0], r, h, cr, row_ok, false);
-            load_state_pair<D, M>(SV1, has2 ? SV1 + M * D : nullptr, KB[1]);
+            load_state_pair_async<D, M>(SV1, has2 ? SV1 + M * D : nullptr, KB[1]);
+            cp_async_commit();
             sync_for_mma();
             if (tid == 0) {
                 const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[1]);
@@ -151,7 +152,7 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
             float mx = -INFINITY;
 #pragma unroll
             for (int jj = 0; jj < HM; jj++) {
-                L[jj] = row_ok ? sig2 * (expf(b[jj]) * sint[jj] + expf(b[jj] - rho[jj]) * lin[jj]) : -INFINITY;
+                L[jj] = row_ok ? sig2 * (fexp(b[jj]) * sint[jj] + fexp(b[jj] - rho[jj]) * lin[jj]) : -INFINITY;
                 mx = fmaxf(mx, L[jj]);
             }
             redm[h * 128 + r] = mx;
@@ -162,8 +163,8 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
             for (int jj = 0; jj < HM; jj++) {
                 const float p = (m == -INFINITY) ? 0.0f : ex2(L[jj] - m);
                 ps += p;
-                pe[jj] = p * expf(b[jj]);
-                pq[jj] = p * expf(b[jj] - rho[jj]);
+                pe[jj] = p * fexp(b[jj]);
+                pq[jj] = p * fexp(b[jj] - rho[jj]);
                 z[jj] = 0.0f;
             }
             reds[h * 128 + r] = ps;
@@ -173,6 +174,7 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
             store_row(VB[1] + 16384, r, h * HM, pq, HM);  // pEq, after Ek
             __syncthreads();
             l = reds[r] + reds[128 + r];
+            cp_async_wait<0>();  // [S^V] pair
             sync_for_mma();
             if (tid == 0) {
                 const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[1]), s3 = smem_u32(KB[1]);
@@ -209,32 +211,38 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
         load_tile_async<D>(kr, klo, min(128, khi - klo + 1), KB[0]);
         load_tile_async<D>(v, klo, min(128, khi - klo + 1), VB[0]);
         cp_async_commit();
+        auto issue_s = [&](int i) {
+            const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[i & 1]);
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_bf16(tm + tA, desc_k(s0, 128, kk), desc_k(s1, 128, kk), idesc_bf16(128, 128, false), kk > 0);
+        };
+        cp_async_wait<0>();
+        sync_for_mma();
+        if (tid == 0) {
+            issue_s(0);
+            mma_commit(&bar);
+        }
+        // One wait per block: the commit after block i's S also covers block
+        // i - 1's P V, issued just before it.
         for (int i = 0; i < nb && ok; i++) {
             const int kb = klo + i * 128, nk = min(128, khi - kb + 1), cur = i & 1;
-            cp_async_wait<0>();
-            sync_for_mma();
-            if (tid == 0) {
-                const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[cur]);
-                for (int kk = 0; kk < D / 16; kk++)
-                    mma_bf16(tm + tA, desc_k(s0, 128, kk), desc_k(s1, 128, kk), idesc_bf16(128, 128, false), kk > 0);
-                mma_commit(&bar);
-            }
-            if (i + 1 < nb) {  // the other stage was last read by block i - 1's P V (complete)
+            ok = ctl.wait();
+            if (!ok) break;
+            if (i + 1 < nb) {  // stage of block i - 1, whose P V is complete
                 const int kn = kb + 128, nn = min(128, khi - kn + 1);
                 load_tile_async<D>(kr, kn, nn, KB[cur ^ 1]);
                 load_tile_async<D>(v, kn, nn, VB[cur ^ 1]);
                 cp_async_commit();
             }
-            ok = ctl.wait();
-            if (!ok) break;
             float sv[64];
             tmem_ld(tl + tA + 64 * h, sv, 64);
             float bm = -INFINITY;
+            // valid keys of this row: columns [clo, chi] of the block
+            const int clo = max(0, t - sh.w + 1 - kb) - 64 * h;
+            const int chi = (row_ok ? min(nk - 1, t - kb) : -1) - 64 * h;
 #pragma unroll
             for (int jj = 0; jj < 64; jj++) {
-                const int c = 64 * h + jj, key = kb + c;
-                const bool valid = row_ok && c < nk && key <= t && key > t - sh.w;
-                sv[jj] = valid ? sv[jj] * sig2 : -INFINITY;
+                sv[jj] = (jj >= clo && jj <= chi) ? sv[jj] * sig2 : -INFINITY;
                 bm = fmaxf(bm, sv[jj]);
             }
             redm[h * 128 + r] = bm;
@@ -269,6 +277,7 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
             }
             reds[h * 128 + r] = ps;
             store_row(KB[cur], r, 64 * h, sv, 64);
+            if (i + 1 < nb) cp_async_wait<0>();
             sync_for_mma();
             l += reds[r] + reds[128 + r];
             if (tid == 0) {
@@ -276,11 +285,12 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
                 for (int kk = 0; kk < 8; kk++)
                     mma_bf16(tm + tO, desc_k(s1, 128, kk), desc_mn(s2, 128, kk), idesc_bf16(128, D, true),
                              (o_valid || kk > 0) ? 1u : 0u);
+                if (i + 1 < nb) issue_s(i + 1);
                 mma_commit(&bar);
             }
             o_valid = true;
-            ok = ctl.wait();
         }
+        if (ok) ok = ctl.wait();  // the last block's P V
         cp_async_wait<0>();
     }
 
@@ -364,8 +374,8 @@ template <int D, int M>
 cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bfloat16* kr, int* status,
                        cudaStream_t st) {
     const Shape& sh = a.sh;
-    cudaError_t e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV, a.G,
-                                    sh, status, st);
+    cudaError_t e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV,
+                                    a.SKb, a.SVb, a.G, sh, status, st);
     if (e != cudaSuccess) return e;
     e = launch_rope_table(tab, sh.T, D / 2, a.rope, st);
     if (e != cudaSuccess) return e;

@@ -25,6 +25,8 @@ struct FwdArgs {
     float* SK;
     float* SV;
     float* G;
+    __nv_bfloat16* SKb;  // bf16 copies of SK, SV (bf16 path)
+    __nv_bfloat16* SVb;
     Shape sh;
     RopeTab rope;
 };
@@ -59,6 +61,10 @@ struct BwdArgs {
     float* wsDB1;
     float* RK;
     float* RV;
+    __nv_bfloat16* SKb;  // bf16 copies of SK, SV, RK, RV (bf16 path)
+    __nv_bfloat16* SVb;
+    __nv_bfloat16* RKb;
+    __nv_bfloat16* RVb;
     Shape sh;
     RopeTab rope;
 };
@@ -85,22 +91,27 @@ template <typename Tin, int D, int M>
 cudaError_t simt_bwd_slot(const BwdArgs& a, cudaStream_t st);
 // bf16 backward: window branch on the tensor core, then the slot branch.
 template <int D, int M>
-cudaError_t tc_backward(const BwdArgs& a, float2* tab, int* status, cudaStream_t st);
+cudaError_t tc_backward(const BwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bfloat16* kr, int* status,
+                        cudaStream_t st);
 // bf16 slot-branch backward on the tensor core (same contract as simt_bwd_slot).
 template <int D, int M>
-cudaError_t tc_bwd_slot(const BwdArgs& a, const float2* tab, int* status, cudaStream_t st);
+cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bfloat16* kr, const float2* tab,
+                        int* status, cudaStream_t st);
 // Key-major window dk / dv (needs the exact D_t in a.Dv).
 template <int D>
-cudaError_t launch_wkv(const BwdArgs& a, const float2* tab, int* status, cudaStream_t st);
+cudaError_t launch_wkv(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bfloat16* kr, const float2* tab,
+                       int* status, cudaStream_t st);
 cudaError_t launch_state_scan_rev(const BwdArgs& a, int M, int D, cudaStream_t st);
 cudaError_t launch_dla_carry(const BwdArgs& a, int M, int D, cudaStream_t st);
 // bf16 path: chunk states on the tensor core, then the forward chunk scan.
 template <int D, int M>
 cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const float* la, float* SK, float* SV,
-                      float* G, const Shape& sh, int* status, cudaStream_t st);
-// Chunk scan (dir > 0: states before each chunk; dir < 0: adjoints carried in).
-cudaError_t launch_scan8(float* X0, float* X1, const float* G, const Shape& sh, int M, int D, int dir,
-                         cudaStream_t st);
+                      __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, const Shape& sh, int* status,
+                      cudaStream_t st);
+// Chunk scan (dir > 0: states before each chunk; dir < 0: adjoints carried in),
+// fp32 in place plus a bf16 copy in B0 / B1.
+cudaError_t launch_scan8(float* X0, float* X1, __nv_bfloat16* B0, __nv_bfloat16* B1, const float* G,
+                         const Shape& sh, int M, int D, int dir, cudaStream_t st);
 // RoPE (cos, sin) table [T][H2] of the absolute positions.
 cudaError_t launch_rope_table(float2* tab, int T, int H2, const RopeTab& rt, cudaStream_t st);
 

@@ -67,9 +67,10 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
             const float corr = a.Dhat[tt] - a.Dwin[tt];
             const float* src = a.dqw + (hoff + tb) * D + e * 8;
             const float* cv = a.dqwV + (hoff + tb) * D + e * 8;
-            float f[8];
-#pragma unroll
-            for (int q = 0; q < 8; q++) f[q] = src[q] + corr * cv[q];
+            const float4 s0 = *reinterpret_cast<const float4*>(src), s1 = *reinterpret_cast<const float4*>(src + 4);
+            const float4 v0 = *reinterpret_cast<const float4*>(cv), v1 = *reinterpret_cast<const float4*>(cv + 4);
+            const float f[8] = {s0.x + corr * v0.x, s0.y + corr * v0.y, s0.z + corr * v0.z, s0.w + corr * v0.w,
+                                s1.x + corr * v1.x, s1.y + corr * v1.y, s1.z + corr * v1.z, s1.w + corr * v1.w};
             *reinterpret_cast<uint4*>((__nv_bfloat16*)a.dq + (hoff + tb) * D + e * 8) = pack8(f);
         }
         for (int e = tid; e < n; e += kTcThreads) a.Dv[hoff + tb + e] = a.Dwin[hoff + tb + e];
@@ -110,20 +111,22 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     {  // Ek tile
         float ek[HM];
 #pragma unroll
-        for (int jj = 0; jj < HM; jj++) ek[jj] = row_ok ? expf(rho[jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
+        for (int jj = 0; jj < HM; jj++) ek[jj] = row_ok ? fexp(rho[jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
         store_row(XE, r, h * HM, ek, HM);
     }
     const float lse_r = row_ok ? a.lse[hoff + t] : 0.0f;
     const float Dwin_r = row_ok ? a.Dwin[hoff + t] : 0.0f;
     const float Dhat_r = row_ok ? a.Dhat[hoff + t] : 0.0f;
     float D_r = 0.0f;  // exact D = window part + slot part, set below
-    const float* SV1 = a.SV + ((size_t)bh * sh.NC + c1) * M * D;
-    const float* SK1 = a.SK + ((size_t)bh * sh.NC + c1) * M * D;
+    const __nv_bfloat16* SV1 = a.SVb + ((size_t)bh * sh.NC + c1) * M * D;
+    const __nv_bfloat16* SK1 = a.SKb + ((size_t)bh * sh.NC + c1) * M * D;
 
     // ---- value side: dP_L
-    load_tile<D>(dout, tbase, nq, XdO, nullptr);
-    load_tile<D>(v, j0, nq, XKV, nullptr);
-    load_state_pair<D, M>(SV1, has2 ? SV1 + M * D : nullptr, XS);
+    load_tile_async<D>(dout, tbase, nq, XdO);
+    load_tile_async<D>(v, j0, nq, XKV);
+    load_state_pair_async<D, M>(SV1, has2 ? SV1 + M * D : nullptr, XS);
+    cp_async_commit();
+    cp_async_wait<0>();
     sync_for_mma();
     if (tid == 0) {
         const uint32_t sd = smem_u32(XdO), sk = smem_u32(XKV), ss = smem_u32(XS);
@@ -150,11 +153,13 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         tmem_ld(tl + R1 + cr * M + h * HM, so, HM);
         tmem_ld(tl + R0 + h * HM, pin, HM);
 #pragma unroll
-        for (int jj = 0; jj < HM; jj++) dpl[jj] = expf(b[jj]) * so[jj] + expf(b[jj] - rho[jj]) * pin[jj];
+        for (int jj = 0; jj < HM; jj++) dpl[jj] = fexp(b[jj]) * so[jj] + fexp(b[jj] - rho[jj]) * pin[jj];
         // ---- key side: slot logits
-        load_tile<D>(q, tbase, nq, XQ, nullptr);
-        load_tile<D>(k, j0, nq, XKV, nullptr);
-        load_state_pair<D, M>(SK1, has2 ? SK1 + M * D : nullptr, XS);
+        load_tile_async<D>(q, tbase, nq, XQ);
+        load_tile_async<D>(k, j0, nq, XKV);
+        load_state_pair_async<D, M>(SK1, has2 ? SK1 + M * D : nullptr, XS);
+        cp_async_commit();
+        cp_async_wait<0>();
         sync_for_mma();
         if (tid == 0) {
             const uint32_t sq = smem_u32(XQ), sk = smem_u32(XKV), ss = smem_u32(XS);
@@ -189,29 +194,34 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         float sp = 0.0f;
 #pragma unroll
         for (int jj = 0; jj < HM; jj++) {
-            const float eb = expf(b[jj]), eq = expf(b[jj] - rho[jj]);
+            const float eb = fexp(b[jj]), eq = fexp(b[jj] - rho[jj]);
             Lv[jj] = sig * (eb * si[jj] + eq * lin[jj]);
-            pl[jj] = row_ok ? expf(Lv[jj] - lse_r) : 0.0f;
+            pl[jj] = row_ok ? fexp(Lv[jj] - lse_r) : 0.0f;
             sp += pl[jj] * dpl[jj];
         }
         red[h * 128 + r] = sp;
         __syncthreads();
         D_r = Dwin_r + red[r] + red[128 + r];
         if (h == 0 && row_ok) a.Dv[hoff + t] = D_r;
+        float sdl[HM], db1[HM];
 #pragma unroll
         for (int jj = 0; jj < HM; jj++) {
-            const float eb = expf(b[jj]), eq = expf(b[jj] - rho[jj]);
+            const float eb = fexp(b[jj]), eq = fexp(b[jj] - rho[jj]);
             const float dl = pl[jj] * (dpl[jj] - D_r);
-            const float db1 = dl * Lv[jj] + pl[jj] * dpl[jj];
-            if (row_ok) {
-                wsDL[jj] = sig * dl;
-                wsPL[jj] = pl[jj];
-                wsDB[jj] = db1;
-            }
+            db1[jj] = dl * Lv[jj] + pl[jj] * dpl[jj];
+            sdl[jj] = sig * dl;
             g1[jj] = sig * dl * eb;
             g2[jj] = pl[jj] * eb;
             weq[jj] = sig * dl * eq;
             z[jj] = 0.0f;
+        }
+        if (row_ok) {
+#pragma unroll
+            for (int jj = 0; jj < HM; jj += 4) {
+                *reinterpret_cast<float4*>(wsDL + jj) = make_float4(sdl[jj], sdl[jj + 1], sdl[jj + 2], sdl[jj + 3]);
+                *reinterpret_cast<float4*>(wsPL + jj) = make_float4(pl[jj], pl[jj + 1], pl[jj + 2], pl[jj + 3]);
+                *reinterpret_cast<float4*>(wsDB + jj) = make_float4(db1[jj], db1[jj + 1], db1[jj + 2], db1[jj + 3]);
+            }
         }
         // chunk-blocked [128][2M] tiles; columns >= 2M are zero
         store_row(XG, r, cr * M + h * HM, g1, HM);
@@ -285,7 +295,13 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
             tmem_ld32(tl + R3 + h * HD + c0, g);
             if (row_ok) {
 #pragma unroll
-                for (int e = 0; e < 32; e++) g[e] += corr * cv[c0 + e];
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(cv + c0 + e);
+                    g[e] += corr * c4.x;
+                    g[e + 1] += corr * c4.y;
+                    g[e + 2] += corr * c4.z;
+                    g[e + 3] += corr * c4.w;
+                }
 #pragma unroll
                 for (int e = 0; e < 32; e += 8) {
                     const float4 u0 = *reinterpret_cast<const float4*>(dqw + c0 + e);
@@ -383,13 +399,13 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     for (int jj = 0; jj < HM; jj++) {
         const float G = sG[cr * M + h * HM + jj];
         rho[jj] = 0.5f * G;
-        eG[jj] = expf(0.5f * G);
+        eG[jj] = fexp(0.5f * G);
     }
     {
         float ek[HM], eke[HM], z[HM];
 #pragma unroll
         for (int jj = 0; jj < HM; jj++) {
-            ek[jj] = slot_ok ? expf(rho[jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
+            ek[jj] = slot_ok ? fexp(rho[jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
             eke[jj] = ek[jj] * eG[jj];
             z[jj] = 0.0f;
         }
@@ -405,16 +421,24 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         const __nv_bfloat16* X = (const __nv_bfloat16*)(pass == 0 ? a.q : a.dout) + hoff * D;
         const __nv_bfloat16* Y = (const __nv_bfloat16*)(pass == 0 ? a.k : a.v) + hoff * D;
         const float* W = (pass == 0 ? a.wsDL : a.wsPL) + jrow * M + h * HM;
-        const float* Rc = (pass == 0 ? a.RK : a.RV) + ((size_t)bh * sh.NC + c1) * M * D;
-        load_tile<D>(X, sbase + sh.w, nc, XA, nullptr);
-        load_tile<D>(Y, sbase, nc, XB, nullptr);
-        load_state_pair<D, M>(Rc, has2 ? Rc + M * D : nullptr, XR);
+        const __nv_bfloat16* Rc = (pass == 0 ? a.RKb : a.RVb) + ((size_t)bh * sh.NC + c1) * M * D;
+        load_tile_async<D>(X, sbase + sh.w, nc, XA);
+        load_tile_async<D>(Y, sbase, nc, XB);
+        load_state_pair_async<D, M>(Rc, has2 ? Rc + M * D : nullptr, XR);
+        cp_async_commit();
         {
             float weq[HM];
 #pragma unroll
-            for (int jj = 0; jj < HM; jj++) weq[jj] = slot_ok ? W[jj] * expf(b[jj] - rho[jj]) : 0.0f;
+            for (int jj = 0; jj < HM; jj += 4) {
+                const float4 w4 = slot_ok ? *reinterpret_cast<const float4*>(W + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
+                weq[jj] = w4.x * fexp(b[jj] - rho[jj]);
+                weq[jj + 1] = w4.y * fexp(b[jj + 1] - rho[jj + 1]);
+                weq[jj + 2] = w4.z * fexp(b[jj + 2] - rho[jj + 2]);
+                weq[jj + 3] = w4.w * fexp(b[jj + 3] - rho[jj + 3]);
+            }
             store_row(XW, r, h * HM, weq, HM);
         }
+        cp_async_wait<0>();
         sync_for_mma();
         if (tid == 0) {
             const uint32_t se = smem_u32(XE), sw = smem_u32(XW), sa = smem_u32(XA), sb = smem_u32(XB),
@@ -449,7 +473,7 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
             float intra[HM];
             tmem_ld(tl + R0 + h * HM, intra, HM);
 #pragma unroll
-            for (int jj = 0; jj < HM; jj++) du[jj] += expf(rho[jj] - b[jj]) * (intra[jj] + eG[jj] * inter[jj]);
+            for (int jj = 0; jj < HM; jj++) du[jj] += fexp(rho[jj] - b[jj]) * (intra[jj] + eG[jj] * inter[jj]);
         }
         const float* gw = (pass == 0 ? a.dkw : a.dvw) + (hoff + s) * D + h * HD;
         __nv_bfloat16* go = (__nv_bfloat16*)(pass == 0 ? a.dk : a.dv) + (hoff + s) * D + h * HD;
@@ -475,12 +499,22 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         float db[HM];
         const float* db1 = a.wsDB1 + jrow * M + h * HM;
 #pragma unroll
-        for (int jj = 0; jj < HM; jj++) db[jj] = slot_ok ? db1[jj] - (-expm1f(l[jj])) * du[jj] : 0.0f;
+        for (int jj = 0; jj < HM; jj += 4) {
+            const float4 d4 = slot_ok ? *reinterpret_cast<const float4*>(db1 + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+            for (int q = 0; q < 4; q++) db[jj + q] = slot_ok ? dd[q] - (-expm1f(l[jj + q])) * du[jj + q] : 0.0f;
+        }
         chunk_suffix<M>(db, s_tot, warp, lane, h);
         if (row_ok) {
             float* dla = a.dla + (hoff + s) * M + h * HM;
 #pragma unroll
-            for (int jj = 0; jj < HM; jj++) dla[jj] = slot_ok ? db[jj] - expf(l[jj]) * du[jj] : 0.0f;
+            for (int jj = 0; jj < HM; jj += 4) {
+                float o4[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++) o4[q] = slot_ok ? db[jj + q] - fexp(l[jj + q]) * du[jj + q] : 0.0f;
+                *reinterpret_cast<float4*>(dla + jj) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+            }
         }
     } else if (row_ok && h == 0) {
         a.dla[(hoff + s) * M] = __int_as_float(0x7fc00000);
@@ -503,7 +537,8 @@ size_t sk_smem() {
 }
 
 template <int D, int M>
-cudaError_t tc_bwd_slot(const BwdArgs& a, const float2* tab, int* status, cudaStream_t st) {
+cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bfloat16* kr, const float2* tab,
+                        int* status, cudaStream_t st) {
     const Shape& sh = a.sh;
     cudaError_t e;
     const int W0 = sh.T - sh.R;
@@ -516,9 +551,9 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const float2* tab, int* status, cudaSt
             NHA_LAUNCH("bwd_sq_tc", st, kern<<<dim3(qtiles, sh.BH), kTcThreads, sq_smem<D, M>(), st>>>(a, status));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if ((e = launch_wkv<D>(a, tab, status, st)) != cudaSuccess) return e;
+    if ((e = launch_wkv<D>(a, qr, kr, tab, status, st)) != cudaSuccess) return e;
     if (sh.NC > 0) {
-        if ((e = launch_scan8(a.RK, a.RV, a.G, sh, M, D, -1, st)) != cudaSuccess) return e;
+        if ((e = launch_scan8(a.RK, a.RV, a.RKb, a.RVb, a.G, sh, M, D, -1, st)) != cudaSuccess) return e;
     }
     {
         auto kern = bwd_sk_tc_kernel<D, M>;
@@ -534,7 +569,9 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const float2* tab, int* status, cudaSt
     return cudaSuccess;
 }
 
-#define NHA_TCS_INST(D, M) template cudaError_t tc_bwd_slot<D, M>(const BwdArgs&, const float2*, int*, cudaStream_t);
+#define NHA_TCS_INST(D, M)                                                                              \
+    template cudaError_t tc_bwd_slot<D, M>(const BwdArgs&, const __nv_bfloat16*, const __nv_bfloat16*, \
+                                           const float2*, int*, cudaStream_t);
 NHA_TCS_INST(64, 16)
 NHA_TCS_INST(64, 32)
 NHA_TCS_INST(64, 64)

@@ -77,7 +77,7 @@ state_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
         float u[HM], z[HM];
 #pragma unroll
         for (int jj = 0; jj < HM; jj++) {
-            u[jj] = row_ok ? expf(sG[cr * M + h * HM + jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
+            u[jj] = row_ok ? fexp(sG[cr * M + h * HM + jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
             z[jj] = 0.0f;
         }
         store_row(XU, r, cr * M + h * HM, u, HM);
@@ -132,23 +132,26 @@ state_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
 
 // Exclusive scan over chunks, in place (forward dir > 0 or reverse dir < 0),
 // eight chunks of loads in flight per thread.  Same contract as the scan of
-// the fp32 path.
+// the fp32 path; also writes a bf16 copy of every result (the operand the
+// tensor-core kernels load).
 __global__ void __launch_bounds__(256)
-state_scan8_kernel(float* __restrict__ X0, float* __restrict__ X1, const float* __restrict__ G, int NC,
-                   int M, int D, int dir) {
-    const int e = blockIdx.x * 256 + threadIdx.x;
+state_scan8_kernel(float* __restrict__ X0, float* __restrict__ X1, __nv_bfloat16* __restrict__ B0,
+                   __nv_bfloat16* __restrict__ B1, const float* __restrict__ G, int NC, int M, int D, int dir) {
+    const int e = 2 * (blockIdx.x * 256 + threadIdx.x);  // two adjacent elements of one slot row
     if (e >= M * D) return;
     const int bh = blockIdx.y, i = e / D;
     float* X = (blockIdx.z == 0) ? X0 : X1;
-    float S = 0.0f;
+    __nv_bfloat16* Xb = (blockIdx.z == 0) ? B0 : B1;
+    float2 S = make_float2(0.0f, 0.0f);
     for (int n0 = 0; n0 < NC; n0 += 8) {
-        float x[8], g[8];
+        float2 x[8];
+        float g[8];
 #pragma unroll
         for (int q = 0; q < 8; q++) {
             const int n = n0 + q;
             const int c = dir > 0 ? n : NC - 1 - n;
             if (n < NC) {
-                x[q] = X[((size_t)bh * NC + c) * M * D + e];
+                x[q] = *reinterpret_cast<const float2*>(X + ((size_t)bh * NC + c) * M * D + e);
                 g[q] = G[((size_t)bh * NC + c) * M + i];
             }
         }
@@ -157,23 +160,29 @@ state_scan8_kernel(float* __restrict__ X0, float* __restrict__ X1, const float* 
             const int n = n0 + q;
             if (n < NC) {
                 const int c = dir > 0 ? n : NC - 1 - n;
-                X[((size_t)bh * NC + c) * M * D + e] = S;
-                S = expf(g[q]) * S + x[q];
+                const size_t o = ((size_t)bh * NC + c) * M * D + e;
+                *reinterpret_cast<float2*>(X + o) = S;
+                *reinterpret_cast<__nv_bfloat162*>(Xb + o) = __floats2bfloat162_rn(S.x, S.y);
+                const float f = expf(g[q]);
+                S.x = f * S.x + x[q].x;
+                S.y = f * S.y + x[q].y;
             }
         }
     }
 }
 
-cudaError_t launch_scan8(float* X0, float* X1, const float* G, const Shape& sh, int M, int D, int dir,
-                         cudaStream_t st) {
+cudaError_t launch_scan8(float* X0, float* X1, __nv_bfloat16* B0, __nv_bfloat16* B1, const float* G,
+                         const Shape& sh, int M, int D, int dir, cudaStream_t st) {
     NHA_LAUNCH(dir > 0 ? "state_scan" : "state_scan_rev", st,
-               state_scan8_kernel<<<dim3((M * D + 255) / 256, sh.BH, 2), 256, 0, st>>>(X0, X1, G, sh.NC, M, D, dir));
+               state_scan8_kernel<<<dim3((M * D / 2 + 255) / 256, sh.BH, 2), 256, 0, st>>>(X0, X1, B0, B1, G,
+                                                                                           sh.NC, M, D, dir));
     return cudaGetLastError();
 }
 
 template <int D, int M>
 cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const float* la, float* SK, float* SV,
-                      float* G, const Shape& sh, int* status, cudaStream_t st) {
+                      __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, const Shape& sh, int* status,
+                      cudaStream_t st) {
     if (sh.NC == 0) return cudaSuccess;
     const size_t sm = 1024 + 3 * 32768 + 6 * M * sizeof(float);
     auto kern = state_tc_kernel<D, M>;
@@ -182,12 +191,13 @@ cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const floa
     NHA_LAUNCH("state_chunk", st,
                kern<<<dim3((sh.R + 127) / 128, sh.BH), kTcThreads, sm, st>>>(k, v, la, SK, SV, G, sh, status));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    return launch_scan8(SK, SV, G, sh, M, D, +1, st);
+    return launch_scan8(SK, SV, SKb, SVb, G, sh, M, D, +1, st);
 }
 
 #define NHA_ST_INST(D, M)                                                                              \
     template cudaError_t tc_states<D, M>(const __nv_bfloat16*, const __nv_bfloat16*, const float*, float*, \
-                                         float*, float*, const Shape&, int*, cudaStream_t);
+                                         float*, __nv_bfloat16*, __nv_bfloat16*, float*, const Shape&, int*,  \
+                                         cudaStream_t);
 NHA_ST_INST(64, 16)
 NHA_ST_INST(64, 32)
 NHA_ST_INST(64, 64)

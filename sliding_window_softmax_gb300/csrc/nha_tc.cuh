@@ -188,23 +188,24 @@ __device__ __forceinline__ void mbar_fence_init() {
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
 
-// Waits for the phase with parity `parity` to complete.  Bounded: gives up
-// after `limit_cycles` SM clock cycles and returns false (the caller records
-// an error status and leaves without touching the results).
+// Waits for the phase with parity `parity` to complete.  mbarrier.try_wait
+// suspends the thread in hardware until the phase completes or a short
+// system-defined interval passes; the loop is bounded: after `limit_cycles`
+// SM clock cycles it gives up and returns false (the caller records an error
+// status and leaves without touching the results).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit_cycles) {
     const uint32_t a = smem_u32(bar);
     const long long t0 = clock64();
-    for (int it = 0;; it++) {
+    for (;;) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}\n"
             : "=r"(done)
             : "r"(a), "r"(parity)
             : "memory");
         if (done) return true;
-        if (it > 64) __nanosleep(32);
         if (clock64() - t0 > limit_cycles) return false;
     }
 }
@@ -213,6 +214,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
                  "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
+                 "r"(valid ? 4 : 0)
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
@@ -227,6 +233,10 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+
+// e^x through ex2.approx (relative error a few 1e-7 for the |x| < 90 used
+// here; denormal results flush to zero).
+__device__ __forceinline__ float fexp(float x) { return ex2(x * 1.4426950408889634f); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);

@@ -167,6 +167,20 @@ __device__ void load_state_pair(const float* __restrict__ S1, const float* __res
     }
 }
 
+// [S1; S2] from bf16 row-major [M][D] copies (S2 may be null = zeros) into a
+// 2M-row tile with cp.async; the caller commits / waits.
+template <int D, int M>
+__device__ __forceinline__ void load_state_pair_async(const __nv_bfloat16* __restrict__ S1,
+                                                      const __nv_bfloat16* __restrict__ S2, unsigned char* tile) {
+    constexpr int CH = D / 8;
+    for (int e = threadIdx.x; e < 2 * M * CH; e += kTcThreads) {
+        const int r = e / CH, ch = e % CH;
+        const bool valid = r < M || S2 != nullptr;
+        const __nv_bfloat16* src = (r < M ? S1 + (size_t)r * D : (S2 ? S2 + (size_t)(r - M) * D : S1)) + ch * 8;
+        cp_async16(tile + sw_chunk(r, ch, 2 * M), src, valid);
+    }
+}
+
 // Store n (multiple of 8) fp32 values as bf16 into row `row` of a 128-row tile
 // starting at column col0 (multiple of 8).
 __device__ __forceinline__ void store_row(unsigned char* tile, int row, int col0, const float* v, int n) {
