@@ -273,6 +273,9 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
     a.RK = ws + p.RK; a.RV = ws + p.RV;
     a.SKb = (__nv_bfloat16*)(ws + p.SKb); a.SVb = (__nv_bfloat16*)(ws + p.SVb);
     a.RKb = (__nv_bfloat16*)(ws + p.RKb); a.RVb = (__nv_bfloat16*)(ws + p.RVb);
+    a.hdqw = (__nv_bfloat16*)a.dqw; a.hdqwV = (__nv_bfloat16*)a.dqwV;
+    a.hdkw = (__nv_bfloat16*)a.dkw; a.hdvw = (__nv_bfloat16*)a.dvw;
+    a.hDL = (__nv_bfloat16*)a.wsDL; a.hPL = (__nv_bfloat16*)a.wsPL;
     a.sh = p.sh;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;

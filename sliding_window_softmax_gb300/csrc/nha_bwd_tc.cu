@@ -43,11 +43,11 @@ __device__ __forceinline__ float half_row_dot(const __nv_bfloat16* __restrict__ 
 
 // Epilogue shared by both kernels: read the rotated-space gradient of this
 // row from TMEM columns [col0, col0 + D), scale, rotate back by R_pos^T and
-// write fp32.  Thread half h owns frequency pairs [h D/4, (h + 1) D/4).
+// write bf16.  Thread half h owns frequency pairs [h D/4, (h + 1) D/4).
 template <int D>
 __device__ __forceinline__ void store_unrotated(uint32_t taddr, bool valid_acc, float scale, int pos,
                                                 bool row_ok, int h, const float2* __restrict__ tab,
-                                                float* __restrict__ out) {
+                                                __nv_bfloat16* __restrict__ out) {
     constexpr int Q4 = D / 4, H = D / 2;
     float g0[Q4], g1[Q4];
     if (valid_acc) {
@@ -60,20 +60,17 @@ __device__ __forceinline__ void store_unrotated(uint32_t taddr, bool valid_acc, 
     if (!row_ok) return;
     const float2* cs = tab + (size_t)pos * H + h * Q4;
 #pragma unroll
-    for (int i = 0; i < Q4; i += 4) {
-        float4 lo, hi;
-        float r0[4], r1[4];
+    for (int i = 0; i < Q4; i += 8) {
+        float r0[8], r1[8];
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
+        for (int j = 0; j < 8; j++) {
             const float2 c = __ldg(cs + i + j);
             const float a = g0[i + j] * scale, b = g1[i + j] * scale;
             r0[j] = a * c.x + b * c.y;
             r1[j] = b * c.x - a * c.y;
         }
-        lo = make_float4(r0[0], r0[1], r0[2], r0[3]);
-        hi = make_float4(r1[0], r1[1], r1[2], r1[3]);
-        *reinterpret_cast<float4*>(out + h * Q4 + i) = lo;
-        *reinterpret_cast<float4*>(out + H + h * Q4 + i) = hi;
+        *reinterpret_cast<uint4*>(out + h * Q4 + i) = pack8(r0);
+        *reinterpret_cast<uint4*>(out + H + h * Q4 + i) = pack8(r1);
     }
 }
 
@@ -208,10 +205,10 @@ bwd_wdq_tc_kernel(const BwdArgs a, const __nv_bfloat16* __restrict__ qr, const _
     __syncthreads();
     if (h == 0 && row_ok) a.Dwin[hoff + t] = red[r] + red[128 + r];
     if (ok) {
-        store_unrotated<D>(tl + tQ, acc, sh.sigma, t, row_ok, h, tab, a.dqw + (hoff + t) * D);
-        store_unrotated<D>(tl + tV, acc, sh.sigma, t, row_ok, h, tab, a.dqwV + (hoff + t) * D);
+        store_unrotated<D>(tl + tQ, acc, sh.sigma, t, row_ok, h, tab, a.hdqw + (hoff + t) * D);
+        store_unrotated<D>(tl + tV, acc, sh.sigma, t, row_ok, h, tab, a.hdqwV + (hoff + t) * D);
     } else if (row_ok) {
-        a.dqw[(hoff + t) * D + h] = __int_as_float(0x7fc00000);
+        a.hdqw[(hoff + t) * D + h] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
     }
     if (!ok && tid == 0) mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);
     fence_before_sync();
@@ -349,7 +346,7 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __nv_bfloat16* __restrict__ qr, const _
     cp_async_wait<0>();
     if (ok) {
         constexpr int HD = D / 2;
-        float* ov = a.dvw + (hoff + key) * D + h * HD;
+        __nv_bfloat16* ov = a.hdvw + (hoff + key) * D + h * HD;
         for (int c0 = 0; c0 < HD; c0 += 32) {
             float vv[32];
             if (acc) {
@@ -360,12 +357,11 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __nv_bfloat16* __restrict__ qr, const _
             }
             if (row_ok)
 #pragma unroll
-                for (int q = 0; q < 32; q += 4)
-                    *reinterpret_cast<float4*>(ov + c0 + q) = make_float4(vv[q], vv[q + 1], vv[q + 2], vv[q + 3]);
+                for (int q = 0; q < 32; q += 8) *reinterpret_cast<uint4*>(ov + c0 + q) = pack8(vv + q);
         }
-        store_unrotated<D>(tl + tK, acc, sh.sigma, key, row_ok, h, tab, a.dkw + (hoff + key) * D);
+        store_unrotated<D>(tl + tK, acc, sh.sigma, key, row_ok, h, tab, a.hdkw + (hoff + key) * D);
     } else if (row_ok) {
-        a.dkw[(hoff + key) * D + h] = __int_as_float(0x7fc00000);
+        a.hdkw[(hoff + key) * D + h] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
     }
     if (!ok && tid == 0) mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);
     fence_before_sync();

@@ -65,6 +65,14 @@ struct BwdArgs {
     __nv_bfloat16* SVb;
     __nv_bfloat16* RKb;
     __nv_bfloat16* RVb;
+    // bf16 path: the window partials and sigma dL, P_L are kept in bf16 (they
+    // alias the storage of the fp32 arrays above)
+    __nv_bfloat16* hdqw;
+    __nv_bfloat16* hdqwV;
+    __nv_bfloat16* hdkw;
+    __nv_bfloat16* hdvw;
+    __nv_bfloat16* hDL;
+    __nv_bfloat16* hPL;
     Shape sh;
     RopeTab rope;
 };

@@ -65,12 +65,11 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
             const int row = e / (D / 8);
             const size_t tt = hoff + tb + row;
             const float corr = a.Dhat[tt] - a.Dwin[tt];
-            const float* src = a.dqw + (hoff + tb) * D + e * 8;
-            const float* cv = a.dqwV + (hoff + tb) * D + e * 8;
-            const float4 s0 = *reinterpret_cast<const float4*>(src), s1 = *reinterpret_cast<const float4*>(src + 4);
-            const float4 v0 = *reinterpret_cast<const float4*>(cv), v1 = *reinterpret_cast<const float4*>(cv + 4);
-            const float f[8] = {s0.x + corr * v0.x, s0.y + corr * v0.y, s0.z + corr * v0.z, s0.w + corr * v0.w,
-                                s1.x + corr * v1.x, s1.y + corr * v1.y, s1.z + corr * v1.z, s1.w + corr * v1.w};
+            float f[8], cv[8];
+            unpack8(*reinterpret_cast<const uint4*>(a.hdqw + (hoff + tb) * D + e * 8), f);
+            unpack8(*reinterpret_cast<const uint4*>(a.hdqwV + (hoff + tb) * D + e * 8), cv);
+#pragma unroll
+            for (int q = 0; q < 8; q++) f[q] += corr * cv[q];
             *reinterpret_cast<uint4*>((__nv_bfloat16*)a.dq + (hoff + tb) * D + e * 8) = pack8(f);
         }
         for (int e = tid; e < n; e += kTcThreads) a.Dv[hoff + tb + e] = a.Dwin[hoff + tb + e];
@@ -187,8 +186,8 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         float si[HM], lin[HM], g1[HM], g2[HM], z[HM];
         tmem_ld(tl + R1 + cr * M + h * HM, si, HM);
         tmem_ld(tl + R0 + h * HM, lin, HM);
-        float* wsDL = a.wsDL + jrow * M + h * HM;
-        float* wsPL = a.wsPL + jrow * M + h * HM;
+        __nv_bfloat16* wsDL = a.hDL + jrow * M + h * HM;
+        __nv_bfloat16* wsPL = a.hPL + jrow * M + h * HM;
         float* wsDB = a.wsDB1 + jrow * M + h * HM;
         float Lv[HM], pl[HM];
         float sp = 0.0f;
@@ -217,11 +216,13 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         }
         if (row_ok) {
 #pragma unroll
-            for (int jj = 0; jj < HM; jj += 4) {
-                *reinterpret_cast<float4*>(wsDL + jj) = make_float4(sdl[jj], sdl[jj + 1], sdl[jj + 2], sdl[jj + 3]);
-                *reinterpret_cast<float4*>(wsPL + jj) = make_float4(pl[jj], pl[jj + 1], pl[jj + 2], pl[jj + 3]);
-                *reinterpret_cast<float4*>(wsDB + jj) = make_float4(db1[jj], db1[jj + 1], db1[jj + 2], db1[jj + 3]);
+            for (int jj = 0; jj < HM; jj += 8) {
+                *reinterpret_cast<uint4*>(wsDL + jj) = pack8(sdl + jj);
+                *reinterpret_cast<uint4*>(wsPL + jj) = pack8(pl + jj);
             }
+#pragma unroll
+            for (int jj = 0; jj < HM; jj += 4)
+                *reinterpret_cast<float4*>(wsDB + jj) = make_float4(db1[jj], db1[jj + 1], db1[jj + 2], db1[jj + 3]);
         }
         // chunk-blocked [128][2M] tiles; columns >= 2M are zero
         store_row(XG, r, cr * M + h * HM, g1, HM);
@@ -286,8 +287,8 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         ok = ctl.wait();
     }
     if (ok) {
-        const float* dqw = a.dqw + (hoff + t) * D + h * HD;
-        const float* cv = a.dqwV + (hoff + t) * D + h * HD;
+        const __nv_bfloat16* dqw = a.hdqw + (hoff + t) * D + h * HD;
+        const __nv_bfloat16* cv = a.hdqwV + (hoff + t) * D + h * HD;
         const float corr = Dhat_r - D_r;
         __nv_bfloat16* dq = (__nv_bfloat16*)a.dq + (hoff + t) * D + h * HD;
         for (int c0 = 0; c0 < HD; c0 += 32) {
@@ -295,19 +296,12 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
             tmem_ld32(tl + R3 + h * HD + c0, g);
             if (row_ok) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 c4 = *reinterpret_cast<const float4*>(cv + c0 + e);
-                    g[e] += corr * c4.x;
-                    g[e + 1] += corr * c4.y;
-                    g[e + 2] += corr * c4.z;
-                    g[e + 3] += corr * c4.w;
-                }
-#pragma unroll
                 for (int e = 0; e < 32; e += 8) {
-                    const float4 u0 = *reinterpret_cast<const float4*>(dqw + c0 + e);
-                    const float4 u1 = *reinterpret_cast<const float4*>(dqw + c0 + e + 4);
-                    const float f[8] = {u0.x + g[e], u0.y + g[e + 1], u0.z + g[e + 2], u0.w + g[e + 3],
-                                        u1.x + g[e + 4], u1.y + g[e + 5], u1.z + g[e + 6], u1.w + g[e + 7]};
+                    float f[8], c8[8];
+                    unpack8(*reinterpret_cast<const uint4*>(dqw + c0 + e), f);
+                    unpack8(*reinterpret_cast<const uint4*>(cv + c0 + e), c8);
+#pragma unroll
+                    for (int q = 0; q < 8; q++) f[q] += g[e + q] + corr * c8[q];
                     *reinterpret_cast<uint4*>(dq + c0 + e) = pack8(f);
                 }
             }
@@ -353,18 +347,13 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     const bool row_ok = r < nk, slot_ok = r < nc;
     if (nc == 0) {  // tokens that never enter a state read by a query
         if (row_ok) {
-            const float* gk = a.dkw + (hoff + s) * D + h * HD;
-            const float* gv = a.dvw + (hoff + s) * D + h * HD;
-            __nv_bfloat16* ok_ = (__nv_bfloat16*)a.dk + (hoff + s) * D + h * HD;
-            __nv_bfloat16* ov_ = (__nv_bfloat16*)a.dv + (hoff + s) * D + h * HD;
-            for (int c = 0; c < HD; c += 8) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; e++) f[e] = gk[c + e];
-                *reinterpret_cast<uint4*>(ok_ + c) = pack8(f);
-#pragma unroll
-                for (int e = 0; e < 8; e++) f[e] = gv[c + e];
-                *reinterpret_cast<uint4*>(ov_ + c) = pack8(f);
+            const uint4* gk = reinterpret_cast<const uint4*>(a.hdkw + (hoff + s) * D + h * HD);
+            const uint4* gv = reinterpret_cast<const uint4*>(a.hdvw + (hoff + s) * D + h * HD);
+            uint4* ok_ = reinterpret_cast<uint4*>((__nv_bfloat16*)a.dk + (hoff + s) * D + h * HD);
+            uint4* ov_ = reinterpret_cast<uint4*>((__nv_bfloat16*)a.dv + (hoff + s) * D + h * HD);
+            for (int c = 0; c < HD / 8; c++) {
+                ok_[c] = gk[c];
+                ov_[c] = gv[c];
             }
             float* dla = a.dla + (hoff + s) * M + h * HM;
 #pragma unroll
@@ -420,7 +409,7 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     for (int pass = 0; pass < 2 && ok; pass++) {
         const __nv_bfloat16* X = (const __nv_bfloat16*)(pass == 0 ? a.q : a.dout) + hoff * D;
         const __nv_bfloat16* Y = (const __nv_bfloat16*)(pass == 0 ? a.k : a.v) + hoff * D;
-        const float* W = (pass == 0 ? a.wsDL : a.wsPL) + jrow * M + h * HM;
+        const __nv_bfloat16* W = (pass == 0 ? a.hDL : a.hPL) + jrow * M + h * HM;
         const __nv_bfloat16* Rc = (pass == 0 ? a.RKb : a.RVb) + ((size_t)bh * sh.NC + c1) * M * D;
         load_tile_async<D>(X, sbase + sh.w, nc, XA);
         load_tile_async<D>(Y, sbase, nc, XB);
@@ -429,12 +418,16 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         {
             float weq[HM];
 #pragma unroll
-            for (int jj = 0; jj < HM; jj += 4) {
-                const float4 w4 = slot_ok ? *reinterpret_cast<const float4*>(W + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
-                weq[jj] = w4.x * fexp(b[jj] - rho[jj]);
-                weq[jj + 1] = w4.y * fexp(b[jj + 1] - rho[jj + 1]);
-                weq[jj + 2] = w4.z * fexp(b[jj + 2] - rho[jj + 2]);
-                weq[jj + 3] = w4.w * fexp(b[jj + 3] - rho[jj + 3]);
+            for (int jj = 0; jj < HM; jj += 8) {
+                float w8[8];
+                if (slot_ok) {
+                    unpack8(*reinterpret_cast<const uint4*>(W + jj), w8);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 8; q++) w8[q] = 0.0f;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; q++) weq[jj + q] = w8[q] * fexp(b[jj + q] - rho[jj + q]);
             }
             store_row(XW, r, h * HM, weq, HM);
         }
@@ -475,7 +468,7 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
 #pragma unroll
             for (int jj = 0; jj < HM; jj++) du[jj] += fexp(rho[jj] - b[jj]) * (intra[jj] + eG[jj] * inter[jj]);
         }
-        const float* gw = (pass == 0 ? a.dkw : a.dvw) + (hoff + s) * D + h * HD;
+        const __nv_bfloat16* gw = (pass == 0 ? a.hdkw : a.hdvw) + (hoff + s) * D + h * HD;
         __nv_bfloat16* go = (__nv_bfloat16*)(pass == 0 ? a.dk : a.dv) + (hoff + s) * D + h * HD;
         for (int c0 = 0; c0 < HD; c0 += 32) {
             float g[32];
@@ -483,10 +476,10 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
             if (row_ok) {
 #pragma unroll
                 for (int e = 0; e < 32; e += 8) {
-                    const float4 u0 = *reinterpret_cast<const float4*>(gw + c0 + e);
-                    const float4 u1 = *reinterpret_cast<const float4*>(gw + c0 + e + 4);
-                    const float f[8] = {u0.x + g[e], u0.y + g[e + 1], u0.z + g[e + 2], u0.w + g[e + 3],
-                                        u1.x + g[e + 4], u1.y + g[e + 5], u1.z + g[e + 6], u1.w + g[e + 7]};
+                    float f[8];
+                    unpack8(*reinterpret_cast<const uint4*>(gw + c0 + e), f);
+#pragma unroll
+                    for (int q = 0; q < 8; q++) f[q] += g[e + q];
                     *reinterpret_cast<uint4*>(go + c0 + e) = pack8(f);
                 }
             }
