@@ -102,6 +102,14 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     TcCtl ctl{&bar, 0u, &s_abort, status};
     bool ok = true;
 
+    // ---- value side: dP_L (tile loads in flight while the gates are computed)
+    const __nv_bfloat16* SV1 = a.SVb + ((size_t)bh * sh.NC + c1) * M * D;
+    const __nv_bfloat16* SK1 = a.SKb + ((size_t)bh * sh.NC + c1) * M * D;
+    load_tile_async<D>(dout, tbase, nq, XdO);
+    load_tile_async<D>(v, j0, nq, XKV);
+    load_state_pair_async<D, M>(SV1, has2 ? SV1 + M * D : nullptr, XS);
+    load_tile_async<D>(q, tbase, nq, XQ);
+    cp_async_commit();
     float l[HM], b[HM];
     row_gates<M>(a.la + (hoff + j) * M, row_ok, l, b, s_tot, sG, warp, lane, h, r, nq);
     float rho[HM];
@@ -117,14 +125,7 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     const float Dwin_r = row_ok ? a.Dwin[hoff + t] : 0.0f;
     const float Dhat_r = row_ok ? a.Dhat[hoff + t] : 0.0f;
     float D_r = 0.0f;  // exact D = window part + slot part, set below
-    const __nv_bfloat16* SV1 = a.SVb + ((size_t)bh * sh.NC + c1) * M * D;
-    const __nv_bfloat16* SK1 = a.SKb + ((size_t)bh * sh.NC + c1) * M * D;
 
-    // ---- value side: dP_L
-    load_tile_async<D>(dout, tbase, nq, XdO);
-    load_tile_async<D>(v, j0, nq, XKV);
-    load_state_pair_async<D, M>(SV1, has2 ? SV1 + M * D : nullptr, XS);
-    cp_async_commit();
     cp_async_wait<0>();
     sync_for_mma();
     if (tid == 0) {
@@ -154,7 +155,6 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
 #pragma unroll
         for (int jj = 0; jj < HM; jj++) dpl[jj] = fexp(b[jj]) * so[jj] + fexp(b[jj] - rho[jj]) * pin[jj];
         // ---- key side: slot logits
-        load_tile_async<D>(q, tbase, nq, XQ);
         load_tile_async<D>(k, j0, nq, XKV);
         load_state_pair_async<D, M>(SK1, has2 ? SK1 + M * D : nullptr, XS);
         cp_async_commit();
@@ -246,21 +246,34 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         ok = ctl.wait();
     }
     if (ok) {
-        // row r of the result = slot n = r of chunk r / M
-        const int cc = r / M, i = r % M;
-        const bool keep = r < 2 * M && (cc == 0 || has2);
-        float* RK = a.RK + (((size_t)bh * sh.NC + c1 + cc) * M + i) * D + h * HD;
-        float* RV = a.RV + (((size_t)bh * sh.NC + c1 + cc) * M + i) * D + h * HD;
-        for (int c0 = 0; c0 < HD; c0 += 32) {
-            float vk[32], vv[32];
-            tmem_ld32(tl + R1 + h * HD + c0, vk);
-            tmem_ld32(tl + R2 + h * HD + c0, vv);
-            if (keep)
+        // Row n of the result = slot n % M of chunk n / M.  Each 32-column slab of
+        // both results goes through shared memory so every global store is a
+        // run of whole rows.
+        float* slab = reinterpret_cast<float*>(XM);  // [2][128 rows][32] fp32 = 32 KB
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            if (h == (c0 < HD ? 0 : 1)) {
+                float vk[32], vv[32];
+                tmem_ld32(tl + R1 + c0, vk);
+                tmem_ld32(tl + R2 + c0, vv);
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
-                    *reinterpret_cast<float4*>(RK + c0 + e) = make_float4(vk[e], vk[e + 1], vk[e + 2], vk[e + 3]);
-                    *reinterpret_cast<float4*>(RV + c0 + e) = make_float4(vv[e], vv[e + 1], vv[e + 2], vv[e + 3]);
+                    const int sw = (e + 4 * (r & 7)) & 31;  // rotate 16-byte chunks across rows
+                    *reinterpret_cast<float4*>(slab + r * 32 + sw) = make_float4(vk[e], vk[e + 1], vk[e + 2], vk[e + 3]);
+                    *reinterpret_cast<float4*>(slab + 4096 + r * 32 + sw) = make_float4(vv[e], vv[e + 1], vv[e + 2], vv[e + 3]);
                 }
+            }
+            __syncthreads();
+            for (int e = tid; e < 2 * 2 * M * 8; e += kTcThreads) {  // (array, row n < 2M, 16-byte chunk)
+                const int arr = e / (2 * M * 8), n = (e / 8) % (2 * M), ch = e % 8;
+                const int cc = n / M, i = n % M;
+                if (cc == 0 || has2) {
+                    const int sw = (4 * ch + 4 * (n & 7)) & 31;
+                    const float4 val = *reinterpret_cast<const float4*>(slab + arr * 4096 + n * 32 + sw);
+                    float* dst = (arr == 0 ? a.RK : a.RV) + (((size_t)bh * sh.NC + c1 + cc) * M + i) * D + c0 + 4 * ch;
+                    *reinterpret_cast<float4*>(dst) = val;
+                }
+            }
+            __syncthreads();
         }
         // ---- dq_slot = G1 [S^K pair] + ((sigma dL o Eq) Ek^T o M) K_c
         store_row(XQ, r, h * HM, weq, HM);
@@ -291,6 +304,13 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         const __nv_bfloat16* cv = a.hdqwV + (hoff + t) * D + h * HD;
         const float corr = Dhat_r - D_r;
         __nv_bfloat16* dq = (__nv_bfloat16*)a.dq + (hoff + t) * D + h * HD;
+        uint4 pw[HD / 8], pv[HD / 8];  // all global loads first
+#pragma unroll
+        for (int e = 0; e < HD / 8; e++) {
+            pw[e] = row_ok ? *reinterpret_cast<const uint4*>(dqw + 8 * e) : make_uint4(0, 0, 0, 0);
+            pv[e] = row_ok ? *reinterpret_cast<const uint4*>(cv + 8 * e) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
         for (int c0 = 0; c0 < HD; c0 += 32) {
             float g[32];
             tmem_ld32(tl + R3 + h * HD + c0, g);
@@ -298,8 +318,8 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
 #pragma unroll
                 for (int e = 0; e < 32; e += 8) {
                     float f[8], c8[8];
-                    unpack8(*reinterpret_cast<const uint4*>(dqw + c0 + e), f);
-                    unpack8(*reinterpret_cast<const uint4*>(cv + c0 + e), c8);
+                    unpack8(pw[(c0 + e) / 8], f);
+                    unpack8(pv[(c0 + e) / 8], c8);
 #pragma unroll
                     for (int q = 0; q < 8; q++) f[q] += g[e + q] + corr * c8[q];
                     *reinterpret_cast<uint4*>(dq + c0 + e) = pack8(f);
@@ -381,6 +401,16 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     TcCtl ctl{&bar, 0u, &s_abort, status};
     bool ok = true;
 
+    auto issue_loads = [&](int pass) {
+        const __nv_bfloat16* X = (const __nv_bfloat16*)(pass == 0 ? a.q : a.dout) + hoff * D;
+        const __nv_bfloat16* Y = (const __nv_bfloat16*)(pass == 0 ? a.k : a.v) + hoff * D;
+        const __nv_bfloat16* Rc = (pass == 0 ? a.RKb : a.RVb) + ((size_t)bh * sh.NC + c1) * M * D;
+        load_tile_async<D>(X, sbase + sh.w, nc, XA);
+        load_tile_async<D>(Y, sbase, nc, XB);
+        load_state_pair_async<D, M>(Rc, has2 ? Rc + M * D : nullptr, XR);
+        cp_async_commit();
+    };
+    issue_loads(0);  // in flight while the gates are computed
     float l[HM], b[HM];
     row_gates<M>(a.la + (hoff + s) * M, slot_ok, l, b, s_tot, sG, warp, lane, h, r, nc);
     float rho[HM], eG[HM];
@@ -407,14 +437,8 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     for (int jj = 0; jj < HM; jj++) du[jj] = 0.0f;
 
     for (int pass = 0; pass < 2 && ok; pass++) {
-        const __nv_bfloat16* X = (const __nv_bfloat16*)(pass == 0 ? a.q : a.dout) + hoff * D;
-        const __nv_bfloat16* Y = (const __nv_bfloat16*)(pass == 0 ? a.k : a.v) + hoff * D;
         const __nv_bfloat16* W = (pass == 0 ? a.hDL : a.hPL) + jrow * M + h * HM;
-        const __nv_bfloat16* Rc = (pass == 0 ? a.RKb : a.RVb) + ((size_t)bh * sh.NC + c1) * M * D;
-        load_tile_async<D>(X, sbase + sh.w, nc, XA);
-        load_tile_async<D>(Y, sbase, nc, XB);
-        load_state_pair_async<D, M>(Rc, has2 ? Rc + M * D : nullptr, XR);
-        cp_async_commit();
+        if (pass > 0) issue_loads(pass);  // the previous pass's MMAs are complete
         {
             float weq[HM];
 #pragma unroll
@@ -470,6 +494,11 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         }
         const __nv_bfloat16* gw = (pass == 0 ? a.hdkw : a.hdvw) + (hoff + s) * D + h * HD;
         __nv_bfloat16* go = (__nv_bfloat16*)(pass == 0 ? a.dk : a.dv) + (hoff + s) * D + h * HD;
+        uint4 pw[HD / 8];  // all global loads first
+#pragma unroll
+        for (int e = 0; e < HD / 8; e++)
+            pw[e] = row_ok ? *reinterpret_cast<const uint4*>(gw + 8 * e) : make_uint4(0, 0, 0, 0);
+#pragma unroll
         for (int c0 = 0; c0 < HD; c0 += 32) {
             float g[32];
             tmem_ld32(tl + R3 + h * HD + c0, g);
@@ -477,7 +506,7 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
 #pragma unroll
                 for (int e = 0; e < 32; e += 8) {
                     float f[8];
-                    unpack8(*reinterpret_cast<const uint4*>(gw + c0 + e), f);
+                    unpack8(pw[(c0 + e) / 8], f);
 #pragma unroll
                     for (int q = 0; q < 8; q++) f[q] += g[e + q];
                     *reinterpret_cast<uint4*>(go + c0 + e) = pack8(f);
