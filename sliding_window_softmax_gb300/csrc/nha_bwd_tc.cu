@@ -21,6 +21,7 @@
 #include "nha_prof.h"
 #include "nha_tc.cuh"
 #include "nha_tc_tiles.cuh"
+#include "nha_tma.h"
 
 namespace nha {
 
@@ -217,162 +218,257 @@ bwd_wdq_tc_kernel(const BwdArgs a, const __nv_bfloat16* __restrict__ qr, const _
 }
 
 // ---------------------------------------------------------------------------------------
-// Key-major: one CTA per (128 keys, head).  Row of the tile = key.  Query
-// blocks of 64 are streamed through two cp.async stages.
+// Key-major: one CTA per (128 keys, head).  Row of the tile = key.  Warp 8 is
+// the producer: it streams 64-query blocks of RoPE(q) and dout through three
+// TMA stages (lse and D beside them by cp.async) and issues every MMA.  Warps
+// 0-7 turn S^T, dP^T into P^T, dS^T.  S^T / dP^T live in two TMEM buffers, so
+// block i + 1's run on the tensor core while block i's softmax runs.
+//
+// Per block i, barriers: full[i % 3] (stage landed), sfull[i & 1] (S^T, dP^T
+// of block i in TMEM), pready (P^T, dS^T of block i stored; 8 warp arrivals),
+// bdone[i & 1] (dV += P^T dout, dK += dS^T q of block i done).  Every wait is
+// bounded and gives up once any thread flags an abort.
+constexpr int kWkvThreads = 288, kWkvStages = 3;
+
+struct WkvMaps {
+    CUtensorMap q, dout, k, v, dk, dv;
+};
+
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
-bwd_wkv_tc_kernel(const BwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_bfloat16* __restrict__ kr,
-                  const float2* __restrict__ tab, int* __restrict__ status) {
+__global__ void __launch_bounds__(kWkvThreads, 1)
+bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, const float2* __restrict__ tab,
+                  int* __restrict__ status) {
     extern __shared__ unsigned char smem_raw[];
-    constexpr int TB = 128 * D * 2, QBB = 64 * D * 2;
+    constexpr int TB = 128 * D * 2, QBB = 64 * D * 2, NS = kWkvStages, HD = D / 2, Q4 = D / 4;
     unsigned char* XK = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char* XV = XK + TB;
-    unsigned char* QB[2];
-    unsigned char* OB[2];
-    QB[0] = XV + TB;
-    OB[0] = QB[0] + QBB;
-    QB[1] = OB[0] + QBB;
-    OB[1] = QB[1] + QBB;
-    unsigned char* PT = OB[1] + QBB;   // P^T  [128 keys][64 q]
-    unsigned char* ST = PT + 16384;    // dS^T [128 keys][64 q]
-    float* sL2 = reinterpret_cast<float*>(ST + 16384);  // [2][64] lse (log2 domain)
-    float* sD = sL2 + 128;                                // [2][64]
-    __shared__ uint64_t bar;
+    unsigned char* QB0 = XV + TB;                 // stage s: RoPE(q) at QB0 + 2 s QBB, dout after it
+    unsigned char* PT = QB0 + NS * 2 * QBB;       // P^T  [128 keys][64 q]
+    unsigned char* ST = PT + 16384;               // dS^T [128 keys][64 q]
+    float* sL = reinterpret_cast<float*>(ST + 16384);  // [NS][64] lse
+    float* sD = sL + NS * 64;                          // [NS][64] D
+    __shared__ uint64_t kvbar, full[NS], sfull[2], pready, bdone[2], drain;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
     const Shape sh = a.sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rk = ((warp & 3) << 5) | lane, h = warp >> 2;
-    const int sbase = blockIdx.x * 128, nk = min(128, sh.T - sbase), bh = blockIdx.y;
+    const int sbase = blockIdx.x * 128, bh = blockIdx.y;
     const size_t hoff = (size_t)bh * sh.T;
-    const __nv_bfloat16* dout = (const __nv_bfloat16*)a.dout + hoff * D;
-    qr += hoff * D;
-    kr += hoff * D;
-    const float sig2 = sh.sigma * kLog2e;
-    const int key = sbase + rk;
-    const bool row_ok = rk < nk;
-    const int thi = sh.w > 0 ? min(sh.T - 1, sbase + nk - 1 + sh.w - 1) : sbase - 1;
+    const int thi = sh.w > 0 ? min(sh.T - 1, sbase + min(128, sh.T - sbase) - 1 + sh.w - 1) : sbase - 1;
     const int nb = thi >= sbase ? (thi - sbase) / 64 + 1 : 0;
-
-    auto prefetch = [&](int i, int stage) {
-        const int qb = sbase + i * 64, nq = min(64, thi - qb + 1);
-        load_tile_async<D>(qr, qb, nq, QB[stage], 64);
-        load_tile_async<D>(dout, qb, nq, OB[stage], 64);
-        if (tid < 64) {
-            const int tt = tid < nq ? tid : 0;
-            cp_async4(sL2 + stage * 64 + tid, a.lse + hoff + qb + tt, tid < nq);
-            cp_async4(sD + stage * 64 + tid, a.Dv + hoff + qb + tt, tid < nq);
-        }
-        cp_async_commit();
-    };
+    volatile int* abort = &s_abort;
 
     if (tid == 0) {
-        mbar_init(&bar, 1);
-        mbar_fence_init();
+        mbar_init(&kvbar, 1);
+        for (int q = 0; q < NS; q++) mbar_init(&full[q], 33);  // expect_tx arrival + 32 cp.async arrivals
+        for (int q = 0; q < 2; q++) {
+            mbar_init(&sfull[q], 1);
+            mbar_init(&bdone[q], 1);
+        }
+        mbar_init(&pready, 8);
+        mbar_init(&drain, 1);
         s_abort = 0;
+        mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(&s_tmem, 512);
-    load_tile_async<D>(kr, sbase, nk, XK);
-    load_tile_async<D>((const __nv_bfloat16*)a.v + hoff * D, sbase, nk, XV);
-    cp_async_commit();
-    if (nb > 0) prefetch(0, 0);
-    cp_async_wait<0>();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tm = s_tmem;
-    const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t tS = 0, tP = 64, tV = 128, tK = 256;
-    TcCtl ctl{&bar, 0u, &s_abort, status};
-    bool ok = true, acc = false;
+    const uint32_t tV = 256, tK = 256 + D;  // S^T / dP^T of buffer b at columns 128 b and 128 b + 64
 
-    // S^T = K~ Q~_b^T and dP^T = V dout_b^T of block i (stage i & 1)
-    auto issue_a = [&](int i) {
-        const uint32_t sk = smem_u32(XK), sv = smem_u32(XV), sq = smem_u32(QB[i & 1]), so = smem_u32(OB[i & 1]);
-        for (int kk = 0; kk < D / 16; kk++)
-            mma_bf16(tm + tS, desc_k(sk, 128, kk), desc_k(sq, 64, kk), idesc_bf16(128, 64, false), kk > 0);
-        for (int kk = 0; kk < D / 16; kk++)
-            mma_bf16(tm + tP, desc_k(sv, 128, kk), desc_k(so, 64, kk), idesc_bf16(128, 64, false), kk > 0);
-    };
-    if (nb > 0) {
-        fence_async_smem();
-        __syncthreads();
-        fence_after_sync();
-        if (tid == 0) {
-            issue_a(0);
-            mma_commit(&bar);
-        }
-    }
-    // One wait per block: the commit after block i's S / dP also covers block
-    // i - 1's dV / dK, which were issued just before them.
-    for (int i = 0; i < nb && ok; i++) {
-        const int qb = sbase + i * 64, nq = min(64, thi - qb + 1), cur = i & 1;
-        ok = ctl.wait();
-        if (!ok) break;
-        if (i + 1 < nb) prefetch(i + 1, cur ^ 1);  // stage of block i - 1, whose MMAs are complete
-        float sv[32], dp[32];
-        tmem_ld(tl + tS + 32 * h, sv, 32);
-        tmem_ld(tl + tP + 32 * h, dp, 32);
-        // queries t = qb + c seeing this key: c in [key - qb, key + w - 1 - qb]
-        const int clo = key - qb - 32 * h;
-        const int chi = (row_ok ? min(nq - 1, key + sh.w - 1 - qb) : -1) - 32 * h;
+    int last_ph[NS];  // producer: phase of the last load issued into each stage
 #pragma unroll
-        for (int jj = 0; jj < 32; jj++) {
-            const int c = 32 * h + jj;
-            const bool valid = jj >= clo && jj <= chi;
-            const float p = valid ? ex2(sv[jj] * sig2 - sL2[cur * 64 + c] * kLog2e) : 0.0f;
-            sv[jj] = p;
-            dp[jj] = p * (dp[jj] - sD[cur * 64 + c]);
+    for (int q = 0; q < NS; q++) last_ph[q] = -1;
+    if (warp == 8) {
+        // ---------------- producer ----------------
+        auto load_stage = [&](int j) {
+            const int stg = j % NS, qb = sbase + j * 64;
+            unsigned char* qd = QB0 + stg * 2 * QBB;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[stg], 2 * QBB);
+#pragma unroll
+                for (int x = 0; x < D; x += 64) {
+                    tma_load_3d(qd + x * 128, &maps.q, x, qb, bh, &full[stg]);
+                    tma_load_3d(qd + QBB + x * 128, &maps.dout, x, qb, bh, &full[stg]);
+                }
+            }
+#pragma unroll
+            for (int c = lane; c < 64; c += 32) {
+                const bool in = qb + c < sh.T;
+                const size_t o = hoff + (in ? qb + c : 0);
+                cp_async4(sL + stg * 64 + c, a.lse + o, in);
+                cp_async4(sD + stg * 64 + c, a.Dv + o, in);
+            }
+            cp_async_mbar_arrive(&full[stg]);
+            last_ph[stg] = (j / NS) & 1;
+        };
+        auto issue_a = [&](int j) {  // S^T = K~ Q~_j^T, dP^T = V dout_j^T into buffer j & 1
+            const uint32_t tS = tm + 128 * (j & 1), tP = tS + 64;
+            const uint32_t qd = smem_u32(QB0 + (j % NS) * 2 * QBB), sk = smem_u32(XK), sv = smem_u32(XV);
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_bf16(tS, desc_k(sk, 128, kk), desc_k(qd, 64, kk), idesc_bf16(128, 64, false), kk > 0);
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_bf16(tP, desc_k(sv, 128, kk), desc_k(qd + QBB, 64, kk), idesc_bf16(128, 64, false), kk > 0);
+            mma_commit(&sfull[j & 1]);
+        };
+        bool ok = true;
+        if (nb > 0) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&kvbar, 2 * TB);
+#pragma unroll
+                for (int x = 0; x < D; x += 64) {
+                    tma_load_3d(XK + x * 256, &maps.k, x, sbase, bh, &kvbar);
+                    tma_load_3d(XV + x * 256, &maps.v, x, sbase, bh, &kvbar);
+                }
+            }
+            for (int j = 0; j < min(NS, nb); j++) load_stage(j);
+            ok = mbar_wait_ab(&kvbar, 0, kWaitCycles, abort) && mbar_wait_ab(&full[0], 0, kWaitCycles, abort);
+            if (ok && lane == 0) issue_a(0);
+            __syncwarp();
+            for (int i = 0; i < nb && ok; i++) {
+                if (i + 1 < nb) {  // buffer (i + 1) & 1 was read by block i - 1, released through pready
+                    if (!(ok = mbar_wait_ab(&full[(i + 1) % NS], ((i + 1) / NS) & 1, kWaitCycles, abort))) break;
+                    if (lane == 0) issue_a(i + 1);
+                    __syncwarp();
+                }
+                if (!(ok = mbar_wait_ab(&pready, i & 1, kWaitCycles, abort))) break;
+                fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t qd = smem_u32(QB0 + (i % NS) * 2 * QBB), sp = smem_u32(PT), ss = smem_u32(ST);
+                    for (int kk = 0; kk < 4; kk++)
+                        mma_bf16(tm + tV, desc_k(sp, 128, kk), desc_mn(qd + QBB, 64, kk), idesc_bf16(128, D, true),
+                                 (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; kk++)
+                        mma_bf16(tm + tK, desc_k(ss, 128, kk), desc_mn(qd, 64, kk), idesc_bf16(128, D, true),
+                                 (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bdone[i & 1]);
+                }
+                __syncwarp();
+                if (i >= 1 && i - 1 + NS < nb) {  // block i - 1 done with its stage: refill it
+                    if (!(ok = mbar_wait_ab(&bdone[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitCycles, abort))) break;
+                    load_stage(i - 1 + NS);
+                }
+            }
         }
-        store_row(PT, rk, 32 * h, sv, 32);
-        store_row(ST, rk, 32 * h, dp, 32);
-        if (i + 1 < nb) cp_async_wait<0>();
-        sync_for_mma();
-        if (tid == 0) {
-            const uint32_t sq = smem_u32(QB[cur]), so = smem_u32(OB[cur]), sp = smem_u32(PT), ss = smem_u32(ST);
-            for (int kk = 0; kk < 4; kk++)
-                mma_bf16(tm + tV, desc_k(sp, 128, kk), desc_mn(so, 64, kk), idesc_bf16(128, D, true),
-                         (acc || kk > 0) ? 1u : 0u);
-            for (int kk = 0; kk < 4; kk++)
-                mma_bf16(tm + tK, desc_k(ss, 128, kk), desc_mn(sq, 64, kk), idesc_bf16(128, D, true),
-                         (acc || kk > 0) ? 1u : 0u);
-            if (i + 1 < nb) issue_a(i + 1);
-            mma_commit(&bar);
+    } else {
+        // ---------------- softmax warps ----------------
+        const int rk = ((warp & 3) << 5) | lane, h = warp >> 2;
+        const int key = sbase + rk;
+        const bool row_ok = key < sh.T;
+        const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
+        const float sig2 = sh.sigma * kLog2e;
+        bool ok = true;
+        for (int i = 0; i < nb; i++) {
+            const int qb = sbase + i * 64, nq = min(64, thi - qb + 1), stg = i % NS, b = i & 1;
+            if (!(ok = mbar_wait_ab(&sfull[b], (i >> 1) & 1, kWaitCycles, abort) &&
+                       mbar_wait_ab(&full[stg], (i / NS) & 1, kWaitCycles, abort)))
+                break;
+            fence_after_sync();
+            float sv[32], dp[32];
+            tmem_ld(tl + 128 * b + 32 * h, sv, 32);
+            tmem_ld(tl + 128 * b + 64 + 32 * h, dp, 32);
+            // queries t = qb + c seeing this key: c in [key - qb, key + w - 1 - qb]
+            const int clo = key - qb - 32 * h;
+            const int chi = (row_ok ? min(nq - 1, key + sh.w - 1 - qb) : -1) - 32 * h;
+            const float* l2 = sL + stg * 64 + 32 * h;
+            const float* dd = sD + stg * 64 + 32 * h;
+#pragma unroll
+            for (int jj = 0; jj < 32; jj++) {
+                const bool valid = jj >= clo && jj <= chi;
+                const float p = valid ? ex2(sv[jj] * sig2 - l2[jj] * kLog2e) : 0.0f;
+                sv[jj] = p;
+                dp[jj] = valid ? p * (dp[jj] - dd[jj]) : 0.0f;
+            }
+            // P^T, dS^T of block i - 1 no longer read by the tensor core
+            if (i >= 1 && !(ok = mbar_wait_ab(&bdone[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitCycles, abort))) break;
+            store_row(PT, rk, 32 * h, sv, 32);
+            store_row(ST, rk, 32 * h, dp, 32);
+            fence_async_smem();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pready);
         }
-        acc = true;
-    }
-    if (ok && nb > 0) ok = ctl.wait();  // the last block's dV / dK
-    cp_async_wait<0>();
-    if (ok) {
-        constexpr int HD = D / 2;
-        __nv_bfloat16* ov = a.hdvw + (hoff + key) * D + h * HD;
-        for (int c0 = 0; c0 < HD; c0 += 32) {
-            float vv[32];
-            if (acc) {
-                tmem_ld32(tl + tV + h * HD + c0, vv);
+        // epilogue: dV = sum P^T dout, dK = sigma R^T(key) sum dS^T q~ in bf16,
+        // staged through the (now idle) stage buffers and written by TMA
+        float2 cs[Q4];
+        {
+            const float2* c = tab + (size_t)(row_ok ? key : 0) * HD + h * Q4;
+#pragma unroll
+            for (int q = 0; q < Q4; q++) cs[q] = __ldg(c + q);
+        }
+        if (ok && nb > 0) ok = mbar_wait_ab(&bdone[(nb - 1) & 1], ((nb - 1) >> 1) & 1, kWaitCycles, abort);
+        if (ok) {
+            fence_after_sync();
+            unsigned char* oV = QB0;       // [128 keys][D] tile
+            unsigned char* oK = QB0 + TB;  // [128 keys][D] tile
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                float vv[32];
+                if (nb > 0) {
+                    tmem_ld(tl + tV + h * HD + c0, vv, HD < 32 ? HD : 32);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; q++) vv[q] = 0.0f;
+                }
+                store_row(oV, rk, h * HD + c0, vv, HD < 32 ? HD : 32);
+            }
+            float g0[Q4], g1[Q4];
+            if (nb > 0) {
+                tmem_ld(tl + tK + h * Q4, g0, Q4);
+                tmem_ld(tl + tK + HD + h * Q4, g1, Q4);
             } else {
 #pragma unroll
-                for (int q = 0; q < 32; q++) vv[q] = 0.0f;
+                for (int q = 0; q < Q4; q++) g0[q] = g1[q] = 0.0f;
             }
-            if (row_ok)
 #pragma unroll
-                for (int q = 0; q < 32; q += 8) *reinterpret_cast<uint4*>(ov + c0 + q) = pack8(vv + q);
+            for (int q = 0; q < Q4; q++) {
+                const float x0 = g0[q] * sh.sigma, x1 = g1[q] * sh.sigma;
+                g0[q] = x0 * cs[q].x + x1 * cs[q].y;
+                g1[q] = x1 * cs[q].x - x0 * cs[q].y;
+            }
+            store_row(oK, rk, h * Q4, g0, Q4);
+            store_row(oK, rk, HD + h * Q4, g1, Q4);
+            fence_async_smem();
         }
-        store_unrotated<D>(tl + tK, acc, sh.sigma, key, row_ok, h, tab, a.hdkw + (hoff + key) * D);
-    } else if (row_ok) {
-        a.hdkw[(hoff + key) * D + h] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
+        // all 256 softmax threads agree before one of them issues the stores
+        const int bad = named_sync_or(1, 256, !ok);
+        if (!bad && tid == 0) {
+#pragma unroll
+            for (int x = 0; x < D; x += 64) {
+                tma_store_3d(&maps.dv, x, sbase, bh, QB0 + x * 256);
+                tma_store_3d(&maps.dk, x, sbase, bh, QB0 + TB + x * 256);
+            }
+            bulk_commit();
+            bulk_wait_read();
+        }
+        if (bad && row_ok) a.hdkw[(hoff + key) * D + h] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
     }
-    if (!ok && tid == 0) mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);
     fence_before_sync();
     __syncthreads();
+    if (s_abort) {  // let the copies and MMAs in flight land before the TMEM and the CTA go
+        if (warp == 8) {
+            if (lane == 0) {
+                mma_commit(&drain);
+                mbar_wait(&drain, 0, kWaitCycles);
+                if (nb > 0) mbar_wait(&kvbar, 0, kWaitCycles);
+                for (int q = 0; q < NS; q++)
+                    if (last_ph[q] >= 0) mbar_wait(&full[q], (uint32_t)last_ph[q], kWaitCycles);
+            }
+            cp_async_wait_all();
+        }
+        __syncthreads();
+        if (tid == 0) atomicExch(status, kStatusTimeout);
+    }
     if (warp == 0) tmem_dealloc(tm, 512);
 }
 
 template <int D>
 size_t wdq_smem() { return 1024 + 2 * 128 * D * 2 + 5 * 32768 + 256 * sizeof(float); }
 template <int D>
-size_t wkv_smem() { return 1024 + 2 * 128 * D * 2 + 4 * 64 * D * 2 + 2 * 16384 + 256 * sizeof(float); }
+size_t wkv_smem() {
+    return 1024 + 2 * 128 * D * 2 + 2 * kWkvStages * 64 * D * 2 + 2 * 16384 + 2 * kWkvStages * 64 * sizeof(float);
+}
 
 template <int D, int M>
 cudaError_t tc_backward(const BwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bfloat16* kr, int* status,
@@ -397,11 +493,21 @@ cudaError_t tc_backward(const BwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_b
 template <int D>
 cudaError_t launch_wkv(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bfloat16* kr, const float2* tab,
                        int* status, cudaStream_t st) {
-    const dim3 grid((a.sh.T + 127) / 128, a.sh.BH);
+    const Shape& sh = a.sh;
+    WkvMaps maps;
+    cudaError_t e;
+    if ((e = tmap_rows_bf16(&maps.q, qr, D, sh.T, sh.BH, 64)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.dout, a.dout, D, sh.T, sh.BH, 64)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.k, kr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.v, a.v, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.dk, a.hdkw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.dv, a.hdvw, D, sh.T, sh.BH, 128)) != cudaSuccess)
+        return e;
+    const dim3 grid((sh.T + 127) / 128, sh.BH);
     auto kern = bwd_wkv_tc_kernel<D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wkv_smem<D>());
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wkv_smem<D>());
     if (e != cudaSuccess) return e;
-    NHA_LAUNCH("bwd_wkv_tc", st, kern<<<grid, kTcThreads, wkv_smem<D>(), st>>>(a, qr, kr, tab, status));
+    NHA_LAUNCH("bwd_wkv_tc", st, kern<<<grid, kWkvThreads, wkv_smem<D>(), st>>>(a, maps, tab, status));
     return cudaGetLastError();
 }
 template cudaError_t launch_wkv<64>(const BwdArgs&, const __nv_bfloat16*, const __nv_bfloat16*, const float2*,

@@ -206,6 +206,19 @@ struct TcCtl {
     }
 };
 
+// One mbarrier that tensor-core commits arrive on, with its own phase bit.
+// wait() blocks the calling thread only (no CTA barrier); false on timeout.
+struct TcBar {
+    uint64_t* bar;
+    uint32_t phase;
+    __device__ bool wait() {
+        const bool ok = mbar_wait(bar, phase, kWaitCycles);
+        phase ^= 1u;
+        fence_after_sync();
+        return ok;
+    }
+};
+
 __device__ __forceinline__ void sync_for_mma() {
     fence_async_smem();
     fence_before_sync();
