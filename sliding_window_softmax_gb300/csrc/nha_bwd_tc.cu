@@ -76,144 +76,270 @@ __device__ __forceinline__ void store_unrotated(uint32_t taddr, bool valid_acc, 
 }
 
 // ---------------------------------------------------------------------------------------
-// Query-major: one CTA per (128 queries, head), all T queries.  Key/value
-// blocks are double-buffered cp.async copies of RoPE(k) and v; dS reuses the
-// block's V buffer once dP = dout V^T has been formed.
+// Query-major: one CTA per (128 queries, head).  Warp 8 is the producer: TMA
+// copies of the RoPE(q), dout and o tiles and of 128-key blocks of RoPE(k), v
+// through two stages; lane 0 issues every MMA.  Warps 0-7 turn S, dP into P,
+// dS.  The softmax warps hand the S / dP columns of TMEM back as soon as they
+// have read them, so block i + 1's S, dP run on the tensor core during block
+// i's softmax.  D^ = dout . o comes from the two tiles in shared memory.
+//
+// Barriers per block i: full[i & 1] (K, V block landed), sfull (S, dP in
+// TMEM), sfree (S, dP read out; 8 warp arrivals), pready (dS over the V block
+// and P stored; 8 warp arrivals), bdone[i & 1] (dq += dS K~, dqV += P K~ done).
+constexpr int kWdqThreads = 288;
+
+struct WdqMaps {
+    CUtensorMap q, dout, o, k, v, dq, dqv, tab;
+};
+
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
-bwd_wdq_tc_kernel(const BwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_bfloat16* __restrict__ kr,
-                  const float2* __restrict__ tab, int* __restrict__ status) {
+__global__ void __launch_bounds__(kWdqThreads, 1)
+bwd_wdq_tc_kernel(const BwdArgs a, const __grid_constant__ WdqMaps maps, int* __restrict__ status) {
     extern __shared__ unsigned char smem_raw[];
-    constexpr int TB = 128 * D * 2;
+    constexpr int TB = 128 * D * 2, HD = D / 2, Q4 = D / 4, CH = D / 8;
     unsigned char* X0 = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char* X3 = X0 + TB;  // dout tile
     unsigned char* KB[2];
-    unsigned char* VB[2];         // V block, then dS [128 q][128 keys]
+    unsigned char* VB[2];  // V block, then dS [128 q][128 keys]
     KB[0] = X3 + TB;
     VB[0] = KB[0] + 32768;
     KB[1] = VB[0] + 32768;
     VB[1] = KB[1] + 32768;
-    unsigned char* XP = VB[1] + 32768;  // P [128 q][128 keys]
+    unsigned char* XP = VB[1] + 32768;                  // o tile, then P [128 q][128 keys]
     float* red = reinterpret_cast<float*>(XP + 32768);  // [2][128]
-    __shared__ uint64_t bar;
+    __shared__ uint64_t qbar, full[2], sfull, sfree, pready, bdone[2], tbar, drain;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
     const Shape sh = a.sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = ((warp & 3) << 5) | lane, h = warp >> 2;
     const int tbase = blockIdx.x * 128, nq = min(128, sh.T - tbase), bh = blockIdx.y;
     const size_t hoff = (size_t)bh * sh.T;
-    const __nv_bfloat16* v = (const __nv_bfloat16*)a.v + hoff * D;
-    const __nv_bfloat16* dout = (const __nv_bfloat16*)a.dout + hoff * D;
-    qr += hoff * D;
-    kr += hoff * D;
-    const float sig2 = sh.sigma * kLog2e;
-    const int t = tbase + r;
-    const bool row_ok = r < nq;
     const int klo = max(0, tbase - sh.w + 1), khi = tbase + nq - 1;
     const int nb = sh.w > 0 ? (khi - klo) / 128 + 1 : 0;
+    volatile int* abort = &s_abort;
 
     if (tid == 0) {
-        mbar_init(&bar, 1);
-        mbar_fence_init();
+        mbar_init(&qbar, 1);
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(&sfull, 1);
+        mbar_init(&sfree, 8);
+        mbar_init(&pready, 8);
+        mbar_init(&bdone[0], 1);
+        mbar_init(&bdone[1], 1);
+        mbar_init(&tbar, 1);
+        mbar_init(&drain, 1);
         s_abort = 0;
+        mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(&s_tmem, 512);
-    load_tile_async<D>(qr, tbase, nq, X0);
-    load_tile_async<D>(dout, tbase, nq, X3);
-    if (nb > 0) {
-        load_tile_async<D>(kr, klo, min(128, khi - klo + 1), KB[0]);
-        load_tile_async<D>(v, klo, min(128, khi - klo + 1), VB[0]);
-    }
-    cp_async_commit();
-    const float dpart = row_ok ? half_row_dot<D>(dout + (size_t)t * D, (const __nv_bfloat16*)a.o + (hoff + t) * D, h) : 0.0f;
-    red[h * 128 + r] = dpart;
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tm = s_tmem;
-    const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t tS = 0, tP = 128, tQ = 256, tV = 384;
-    const float Dr = red[r] + red[128 + r];  // from the bf16 o
-    if (h == 0 && row_ok) a.Dhat[hoff + t] = Dr;
-    const float lse2 = row_ok ? a.lse[hoff + t] * kLog2e : 0.0f;
-    float dwin = 0.0f;
-    TcCtl ctl{&bar, 0u, &s_abort, status};
-    bool ok = true, acc = false;
 
-    // S = Q~ K~_b^T and dP = dout V_b^T of block i (stage i & 1)
-    auto issue_a = [&](int i) {
-        const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[i & 1]), s2 = smem_u32(VB[i & 1]), s3 = smem_u32(X3);
-        for (int kk = 0; kk < D / 16; kk++)
-            mma_bf16(tm + tS, desc_k(s0, 128, kk), desc_k(s1, 128, kk), idesc_bf16(128, 128, false), kk > 0);
-        for (int kk = 0; kk < D / 16; kk++)
-            mma_bf16(tm + tP, desc_k(s3, 128, kk), desc_k(s2, 128, kk), idesc_bf16(128, 128, false), kk > 0);
-    };
-    if (nb > 0) {
-        cp_async_wait<0>();
-        sync_for_mma();
-        if (tid == 0) {
-            issue_a(0);
-            mma_commit(&bar);
-        }
-    }
-    // One wait per block: the commit after block i's S / dP also covers block
-    // i - 1's dq MMAs, issued just before them.
-    for (int i = 0; i < nb && ok; i++) {
-        const int kb = klo + i * 128, nk = min(128, khi - kb + 1), cur = i & 1;
-        ok = ctl.wait();
-        if (!ok) break;
-        if (i + 1 < nb) {  // stage of block i - 1, whose MMAs are complete
-            const int kn = kb + 128, nn = min(128, khi - kn + 1);
-            load_tile_async<D>(kr, kn, nn, KB[cur ^ 1]);
-            load_tile_async<D>(v, kn, nn, VB[cur ^ 1]);
-            cp_async_commit();
-        }
-        float sv[64], dp[64];
-        tmem_ld(tl + tS + 64 * h, sv, 64);
-        tmem_ld(tl + tP + 64 * h, dp, 64);
-        const int clo = max(0, t - sh.w + 1 - kb) - 64 * h;
-        const int chi = (row_ok ? min(nk - 1, t - kb) : -1) - 64 * h;
+    int last_ph[2] = {-1, -1};  // producer: phase of the last block load into each stage
+    bool tab_issued = false;
+    if (warp == 8) {
+        // ---------------- producer (lane 0) ----------------
+        if (lane == 0) {
+            auto load_block = [&](int j) {
+                const int b = j & 1, kb = klo + j * 128;
+                mbar_arrive_expect_tx(&full[b], 2 * TB);
 #pragma unroll
-        for (int jj = 0; jj < 64; jj++) {
-            const bool valid = jj >= clo && jj <= chi;
-            const float p = valid ? ex2(sv[jj] * sig2 - lse2) : 0.0f;
-            dwin += p * dp[jj];
-            sv[jj] = p * (dp[jj] - Dr);
-            dp[jj] = p;
+                for (int x = 0; x < D; x += 64) {
+                    tma_load_3d(KB[b] + x * 256, &maps.k, x, kb, bh, &full[b]);
+                    tma_load_3d(VB[b] + x * 256, &maps.v, x, kb, bh, &full[b]);
+                }
+                last_ph[b] = (j >> 1) & 1;
+            };
+            auto issue_a = [&](int j) {  // S = Q~ K~_j^T, dP = dout V_j^T
+                const uint32_t s0 = smem_u32(X0), s3 = smem_u32(X3), sk = smem_u32(KB[j & 1]),
+                               sv = smem_u32(VB[j & 1]);
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_bf16(tm + tS, desc_k(s0, 128, kk), desc_k(sk, 128, kk), idesc_bf16(128, 128, false), kk > 0);
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_bf16(tm + tP, desc_k(s3, 128, kk), desc_k(sv, 128, kk), idesc_bf16(128, 128, false), kk > 0);
+                mma_commit(&sfull);
+            };
+            mbar_arrive_expect_tx(&qbar, (nb > 0 ? 3 : 2) * TB);
+#pragma unroll
+            for (int x = 0; x < D; x += 64) {
+                if (nb > 0) tma_load_3d(X0 + x * 256, &maps.q, x, tbase, bh, &qbar);
+                tma_load_3d(X3 + x * 256, &maps.dout, x, tbase, bh, &qbar);
+                tma_load_3d(XP + x * 256, &maps.o, x, tbase, bh, &qbar);
+            }
+            bool ok = true;
+            if (nb > 0) {
+                load_block(0);
+                if (nb > 1) load_block(1);
+                ok = mbar_wait_ab(&qbar, 0, kWaitCycles, abort) && mbar_wait_ab(&full[0], 0, kWaitCycles, abort);
+                if (ok) issue_a(0);
+                for (int i = 0; i < nb && ok; i++) {
+                    if (i + 1 < nb) {  // S, dP of block i read out; block i + 1 landed
+                        if (!(ok = mbar_wait_ab(&sfree, i & 1, kWaitCycles, abort))) break;
+                        if (!(ok = mbar_wait_ab(&full[(i + 1) & 1], ((i + 1) >> 1) & 1, kWaitCycles, abort))) break;
+                        fence_after_sync();
+                        issue_a(i + 1);
+                    }
+                    if (!(ok = mbar_wait_ab(&pready, i & 1, kWaitCycles, abort))) break;
+                    fence_after_sync();
+                    {
+                        const uint32_t sk = smem_u32(KB[i & 1]), sd = smem_u32(VB[i & 1]), sp = smem_u32(XP);
+                        for (int kk = 0; kk < 8; kk++)
+                            mma_bf16(tm + tQ, desc_k(sd, 128, kk), desc_mn(sk, 128, kk), idesc_bf16(128, D, true),
+                                     (i > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 8; kk++)
+                            mma_bf16(tm + tV, desc_k(sp, 128, kk), desc_mn(sk, 128, kk), idesc_bf16(128, D, true),
+                                     (i > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&bdone[i & 1]);
+                    }
+                    if (i + 2 < nb) {  // block i's stage is free once its dq MMAs are done
+                        if (!(ok = mbar_wait_ab(&bdone[i & 1], (i >> 1) & 1, kWaitCycles, abort))) break;
+                        load_block(i + 2);
+                    }
+                    if (i == nb - 1) {
+                        // RoPE table tile for the epilogue, into the stage of block
+                        // nb - 2 (its MMAs finished before pready of block nb - 1)
+                        unsigned char* dst = KB[(i + 1) & 1];
+                        mbar_arrive_expect_tx(&tbar, 128 * D * 4);
+#pragma unroll
+                        for (int x = 0; x < D; x += 32) tma_load_2d(dst + x * 512, &maps.tab, x, tbase, &tbar);
+                        tab_issued = true;
+                    }
+                }
+            }
         }
-        store_row(VB[cur], r, 64 * h, sv, 64);  // dS over the consumed V block
-        store_row(XP, r, 64 * h, dp, 64);
-        if (i + 1 < nb) cp_async_wait<0>();
-        sync_for_mma();
-        if (tid == 0) {
-            const uint32_t s1 = smem_u32(KB[cur]), s4 = smem_u32(VB[cur]), s5 = smem_u32(XP);
-            for (int kk = 0; kk < 8; kk++)
-                mma_bf16(tm + tQ, desc_k(s4, 128, kk), desc_mn(s1, 128, kk), idesc_bf16(128, D, true),
-                         (acc || kk > 0) ? 1u : 0u);
-            for (int kk = 0; kk < 8; kk++)
-                mma_bf16(tm + tV, desc_k(s5, 128, kk), desc_mn(s1, 128, kk), idesc_bf16(128, D, true),
-                         (acc || kk > 0) ? 1u : 0u);
-            if (i + 1 < nb) issue_a(i + 1);
-            mma_commit(&bar);
+    } else {
+        // ---------------- softmax warps ----------------
+        const int r = ((warp & 3) << 5) | lane, h = warp >> 2;
+        const int t = tbase + r;
+        const bool row_ok = r < nq;
+        const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
+        const float sig2 = sh.sigma * kLog2e;
+        const float lse2 = row_ok ? a.lse[hoff + t] * kLog2e : 0.0f;
+        bool ok = mbar_wait_ab(&qbar, 0, kWaitCycles, abort);
+        {  // D^ = dout_t . o_t (bf16 tiles), half a row per thread
+            float part = 0.0f;
+            if (ok)
+#pragma unroll
+                for (int c = 0; c < CH / 2; c++) {
+                    float x[8], y[8];
+                    unpack8(*reinterpret_cast<const uint4*>(X3 + sw_chunk(r, h * (CH / 2) + c, 128)), x);
+                    unpack8(*reinterpret_cast<const uint4*>(XP + sw_chunk(r, h * (CH / 2) + c, 128)), y);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) part += x[e] * y[e];
+                }
+            red[h * 128 + r] = part;
         }
-        acc = true;
+        named_sync(1, 256);  // also: every o read done before P overwrites the tile
+        const float Dr = red[r] + red[128 + r];
+        if (h == 0 && row_ok) a.Dhat[hoff + t] = Dr;
+        float dwin = 0.0f;
+        for (int i = 0; i < nb && ok; i++) {
+            const int kb = klo + i * 128, nk = min(128, khi - kb + 1), b = i & 1;
+            if (!(ok = mbar_wait_ab(&sfull, i & 1, kWaitCycles, abort))) break;
+            fence_after_sync();
+            float sv[64], dp[64];
+            tmem_ld64x2(tl + tS + 64 * h, tl + tP + 64 * h, sv, dp);
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sfree);
+            const int clo = max(0, t - sh.w + 1 - kb) - 64 * h;
+            const int chi = (row_ok ? min(nk - 1, t - kb) : -1) - 64 * h;
+#pragma unroll
+            for (int jj = 0; jj < 64; jj++) {
+                const bool valid = jj >= clo && jj <= chi;
+                const float p = valid ? ex2(sv[jj] * sig2 - lse2) : 0.0f;
+                dwin += p * dp[jj];
+                sv[jj] = p * (dp[jj] - Dr);
+                dp[jj] = p;
+            }
+            // P of block i - 1 no longer read by the tensor core
+            if (i >= 1 && !(ok = mbar_wait_ab(&bdone[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitCycles, abort))) break;
+            store_row(VB[b], r, 64 * h, sv, 64);  // dS over the consumed V block
+            store_row(XP, r, 64 * h, dp, 64);
+            fence_async_smem();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pready);
+        }
+        named_sync(1, 256);
+        red[h * 128 + r] = dwin;
+        named_sync(1, 256);
+        if (h == 0 && row_ok) a.Dwin[hoff + t] = red[r] + red[128 + r];
+        // epilogue: sigma R^T(t) of the dq and dqV accumulators, in bf16, staged
+        // in the stage of the last block and written by TMA
+        if (ok && nb > 0)
+            ok = mbar_wait_ab(&bdone[(nb - 1) & 1], ((nb - 1) >> 1) & 1, kWaitCycles, abort) &&
+                 mbar_wait_ab(&tbar, 0, kWaitCycles, abort);
+        unsigned char* stQ = KB[(nb + 1) & 1];
+        unsigned char* stV = VB[(nb + 1) & 1];
+        if (ok) {
+            fence_after_sync();
+            const unsigned char* tabs = KB[nb & 1];
+#pragma unroll
+            for (int pass = 0; pass < 2; pass++) {
+                float g0[Q4], g1[Q4];
+                if (nb > 0) {
+                    const uint32_t ta = tl + (pass == 0 ? tQ : tV) + h * Q4;
+                    if constexpr (Q4 == 32) {
+                        tmem_ld32x2(ta, ta + HD, g0, g1);
+                    } else {
+                        tmem_ld(ta, g0, Q4);
+                        tmem_ld(ta + HD, g1, Q4);
+                    }
+#pragma unroll
+                    for (int q = 0; q < Q4; q += 2) {
+                        // (cos, sin) pairs h Q4 + q, + 1: one 16-byte chunk of the swizzled tile
+                        const int pi = h * Q4 + q, bx = pi >> 4, c = (pi & 15) >> 1;
+                        const float4 cs = *reinterpret_cast<const float4*>(tabs + bx * 16384 + r * 128 +
+                                                                           ((c ^ (r & 7)) << 4));
+                        const float a0 = g0[q] * sh.sigma, b0 = g1[q] * sh.sigma;
+                        const float a1 = g0[q + 1] * sh.sigma, b1 = g1[q + 1] * sh.sigma;
+                        g0[q] = a0 * cs.x + b0 * cs.y;
+                        g1[q] = b0 * cs.x - a0 * cs.y;
+                        g0[q + 1] = a1 * cs.z + b1 * cs.w;
+                        g1[q + 1] = b1 * cs.z - a1 * cs.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < Q4; q++) g0[q] = g1[q] = 0.0f;
+                }
+                unsigned char* stg = pass == 0 ? stQ : stV;
+                store_row(stg, r, h * Q4, g0, Q4);
+                store_row(stg, r, HD + h * Q4, g1, Q4);
+            }
+            fence_async_smem();
+        }
+        const int bad = named_sync_or(1, 256, !ok);
+        if (!bad && tid == 0) {
+#pragma unroll
+            for (int x = 0; x < D; x += 64) {
+                tma_store_3d(&maps.dq, x, tbase, bh, stQ + x * 256);
+                tma_store_3d(&maps.dqv, x, tbase, bh, stV + x * 256);
+            }
+            bulk_commit();
+            bulk_wait_read();
+        }
+        if (bad && row_ok) a.hdqw[(hoff + t) * D + h] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
     }
-    if (ok && nb > 0) ok = ctl.wait();  // the last block's dq MMAs
-    cp_async_wait<0>();
-    red[h * 128 + r] = dwin;
-    __syncthreads();
-    if (h == 0 && row_ok) a.Dwin[hoff + t] = red[r] + red[128 + r];
-    if (ok) {
-        store_unrotated<D>(tl + tQ, acc, sh.sigma, t, row_ok, h, tab, a.hdqw + (hoff + t) * D);
-        store_unrotated<D>(tl + tV, acc, sh.sigma, t, row_ok, h, tab, a.hdqwV + (hoff + t) * D);
-    } else if (row_ok) {
-        a.hdqw[(hoff + t) * D + h] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
-    }
-    if (!ok && tid == 0) mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);
     fence_before_sync();
     __syncthreads();
+    if (s_abort) {  // let the copies and MMAs in flight land before the TMEM and the CTA go
+        if (warp == 8 && lane == 0) {
+            mma_commit(&drain);
+            mbar_wait(&drain, 0, kWaitCycles);
+            mbar_wait(&qbar, 0, kWaitCycles);
+            for (int q = 0; q < 2; q++)
+                if (last_ph[q] >= 0) mbar_wait(&full[q], (uint32_t)last_ph[q], kWaitCycles);
+            if (tab_issued) mbar_wait(&tbar, 0, kWaitCycles);
+        }
+        __syncthreads();
+        if (tid == 0) atomicExch(status, kStatusTimeout);
+    }
     if (warp == 0) tmem_dealloc(tm, 512);
 }
 
@@ -231,13 +357,12 @@ bwd_wdq_tc_kernel(const BwdArgs a, const __nv_bfloat16* __restrict__ qr, const _
 constexpr int kWkvThreads = 288, kWkvStages = 3;
 
 struct WkvMaps {
-    CUtensorMap q, dout, k, v, dk, dv;
+    CUtensorMap q, dout, k, v, dk, dv, tab;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kWkvThreads, 1)
-bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, const float2* __restrict__ tab,
-                  int* __restrict__ status) {
+bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, int* __restrict__ status) {
     extern __shared__ unsigned char smem_raw[];
     constexpr int TB = 128 * D * 2, QBB = 64 * D * 2, NS = kWkvStages, HD = D / 2, Q4 = D / 4;
     unsigned char* XK = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -247,7 +372,7 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, const f
     unsigned char* ST = PT + 16384;               // dS^T [128 keys][64 q]
     float* sL = reinterpret_cast<float*>(ST + 16384);  // [NS][64] lse
     float* sD = sL + NS * 64;                          // [NS][64] D
-    __shared__ uint64_t kvbar, full[NS], sfull[2], pready, bdone[2], drain;
+    __shared__ uint64_t kvbar, full[NS], sfull[2], pready, bdone[2], tbar, drain;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -267,6 +392,7 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, const f
             mbar_init(&bdone[q], 1);
         }
         mbar_init(&pready, 8);
+        mbar_init(&tbar, 1);
         mbar_init(&drain, 1);
         s_abort = 0;
         mbar_fence_init();
@@ -281,6 +407,7 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, const f
     int last_ph[NS];  // producer: phase of the last load issued into each stage
 #pragma unroll
     for (int q = 0; q < NS; q++) last_ph[q] = -1;
+    bool tab_issued = false;
     if (warp == 8) {
         // ---------------- producer ----------------
         auto load_stage = [&](int j) {
@@ -351,6 +478,15 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, const f
                     load_stage(i - 1 + NS);
                 }
             }
+            // RoPE table tile for the epilogue, over the last stage and P^T / dS^T
+            // once the last MMAs are done
+            if (ok && (ok = mbar_wait_ab(&bdone[(nb - 1) & 1], ((nb - 1) >> 1) & 1, kWaitCycles, abort)) &&
+                lane == 0) {
+                mbar_arrive_expect_tx(&tbar, 128 * D * 4);
+#pragma unroll
+                for (int x = 0; x < D; x += 32) tma_load_2d(QB0 + 2 * TB + x * 512, &maps.tab, x, sbase, &tbar);
+                tab_issued = true;
+            }
         }
     } else {
         // ---------------- softmax warps ----------------
@@ -367,8 +503,7 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, const f
                 break;
             fence_after_sync();
             float sv[32], dp[32];
-            tmem_ld(tl + 128 * b + 32 * h, sv, 32);
-            tmem_ld(tl + 128 * b + 64 + 32 * h, dp, 32);
+            tmem_ld32x2(tl + 128 * b + 32 * h, tl + 128 * b + 64 + 32 * h, sv, dp);
             // queries t = qb + c seeing this key: c in [key - qb, key + w - 1 - qb]
             const int clo = key - qb - 32 * h;
             const int chi = (row_ok ? min(nq - 1, key + sh.w - 1 - qb) : -1) - 32 * h;
@@ -392,12 +527,6 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, const f
         }
         // epilogue: dV = sum P^T dout, dK = sigma R^T(key) sum dS^T q~ in bf16,
         // staged through the (now idle) stage buffers and written by TMA
-        float2 cs[Q4];
-        {
-            const float2* c = tab + (size_t)(row_ok ? key : 0) * HD + h * Q4;
-#pragma unroll
-            for (int q = 0; q < Q4; q++) cs[q] = __ldg(c + q);
-        }
         if (ok && nb > 0) ok = mbar_wait_ab(&bdone[(nb - 1) & 1], ((nb - 1) >> 1) & 1, kWaitCycles, abort);
         if (ok) {
             fence_after_sync();
@@ -415,17 +544,30 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, const f
             }
             float g0[Q4], g1[Q4];
             if (nb > 0) {
-                tmem_ld(tl + tK + h * Q4, g0, Q4);
-                tmem_ld(tl + tK + HD + h * Q4, g1, Q4);
+                if constexpr (Q4 == 32) {
+                    tmem_ld32x2(tl + tK + h * Q4, tl + tK + HD + h * Q4, g0, g1);
+                } else {
+                    tmem_ld(tl + tK + h * Q4, g0, Q4);
+                    tmem_ld(tl + tK + HD + h * Q4, g1, Q4);
+                }
+                ok = mbar_wait_ab(&tbar, 0, kWaitCycles, abort);
+                const unsigned char* tabs = QB0 + 2 * TB;
+#pragma unroll
+                for (int q = 0; q < Q4; q += 2) {
+                    // (cos, sin) pairs h Q4 + q, + 1: one 16-byte chunk of the swizzled tile
+                    const int pi = h * Q4 + q, bx = pi >> 4, c = (pi & 15) >> 1;
+                    const float4 cs =
+                        *reinterpret_cast<const float4*>(tabs + bx * 16384 + rk * 128 + ((c ^ (rk & 7)) << 4));
+                    const float a0 = g0[q] * sh.sigma, b0 = g1[q] * sh.sigma;
+                    const float a1 = g0[q + 1] * sh.sigma, b1 = g1[q + 1] * sh.sigma;
+                    g0[q] = a0 * cs.x + b0 * cs.y;
+                    g1[q] = b0 * cs.x - a0 * cs.y;
+                    g0[q + 1] = a1 * cs.z + b1 * cs.w;
+                    g1[q + 1] = b1 * cs.z - a1 * cs.w;
+                }
             } else {
 #pragma unroll
                 for (int q = 0; q < Q4; q++) g0[q] = g1[q] = 0.0f;
-            }
-#pragma unroll
-            for (int q = 0; q < Q4; q++) {
-                const float x0 = g0[q] * sh.sigma, x1 = g1[q] * sh.sigma;
-                g0[q] = x0 * cs[q].x + x1 * cs[q].y;
-                g1[q] = x1 * cs[q].x - x0 * cs[q].y;
             }
             store_row(oK, rk, h * Q4, g0, Q4);
             store_row(oK, rk, HD + h * Q4, g1, Q4);
@@ -454,6 +596,7 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, const f
                 if (nb > 0) mbar_wait(&kvbar, 0, kWaitCycles);
                 for (int q = 0; q < NS; q++)
                     if (last_ph[q] >= 0) mbar_wait(&full[q], (uint32_t)last_ph[q], kWaitCycles);
+                if (tab_issued) mbar_wait(&tbar, 0, kWaitCycles);
             }
             cp_async_wait_all();
         }
@@ -481,10 +624,20 @@ cudaError_t tc_backward(const BwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_b
     if (sh.w > 0 && (e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, sh, st)) != cudaSuccess) return e;
     const dim3 grid((sh.T + 127) / 128, sh.BH);
     {
+        WdqMaps maps;
+        if ((e = tmap_rows_bf16(&maps.q, qr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.dout, a.dout, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.o, a.o, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.k, kr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.v, a.v, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.dq, a.hdqw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.dqv, a.hdqwV, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_tab(&maps.tab, tab, D / 2, sh.T)) != cudaSuccess)
+            return e;
         auto kern = bwd_wdq_tc_kernel<D>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wdq_smem<D>())) != cudaSuccess)
             return e;
-        NHA_LAUNCH("bwd_wdq_tc", st, kern<<<grid, kTcThreads, wdq_smem<D>(), st>>>(a, qr, kr, tab, status));
+        NHA_LAUNCH("bwd_wdq_tc", st, kern<<<grid, kWdqThreads, wdq_smem<D>(), st>>>(a, maps, status));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return tc_bwd_slot<D, M>(a, qr, kr, tab, status, st);
@@ -501,13 +654,14 @@ cudaError_t launch_wkv(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bfl
         (e = tmap_rows_bf16(&maps.k, kr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
         (e = tmap_rows_bf16(&maps.v, a.v, D, sh.T, sh.BH, 128)) != cudaSuccess ||
         (e = tmap_rows_bf16(&maps.dk, a.hdkw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
-        (e = tmap_rows_bf16(&maps.dv, a.hdvw, D, sh.T, sh.BH, 128)) != cudaSuccess)
+        (e = tmap_rows_bf16(&maps.dv, a.hdvw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+        (e = tmap_tab(&maps.tab, tab, D / 2, sh.T)) != cudaSuccess)
         return e;
     const dim3 grid((sh.T + 127) / 128, sh.BH);
     auto kern = bwd_wkv_tc_kernel<D>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wkv_smem<D>());
     if (e != cudaSuccess) return e;
-    NHA_LAUNCH("bwd_wkv_tc", st, kern<<<grid, kWkvThreads, wkv_smem<D>(), st>>>(a, maps, tab, status));
+    NHA_LAUNCH("bwd_wkv_tc", st, kern<<<grid, kWkvThreads, wkv_smem<D>(), st>>>(a, maps, status));
     return cudaGetLastError();
 }
 template cudaError_t launch_wkv<64>(const BwdArgs&, const __nv_bfloat16*, const __nv_bfloat16*, const float2*,

@@ -35,4 +35,17 @@ cudaError_t tmap_rows_bf16(CUtensorMap* map, const void* base, int D, int T, int
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t tmap_tab(CUtensorMap* map, const float2* tab, int H2, int T) {
+    std::call_once(g_encode_once, resolve_encode);
+    if (!g_encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)H2 * 2, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)H2 * 8};
+    const cuuint32_t box[2] = {32, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float2*>(tab), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace nha
