@@ -22,9 +22,17 @@
 #include "nha_prof.h"
 #include "nha_tc.cuh"
 #include "nha_tc_tiles.cuh"
+#include "nha_tma.h"
 
 namespace nha {
 using namespace tc;
+
+// Forward CTA: 8 tile warps and a producer warp; three K~ / V stages.
+constexpr int kFwdThreads = 288, kFwdStages = 3;
+
+struct FwdMaps {
+    CUtensorMap q, k, v;
+};
 
 __global__ void rope_table_kernel(float2* __restrict__ tab, int T, int H2, RopeTab rt) {
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -35,29 +43,30 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, int T, int H2, RopeT
 }
 
 template <int D, int M>
-__global__ void __launch_bounds__(kTcThreads, 1)
-fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_bfloat16* __restrict__ kr,
-              int* __restrict__ status) {
-    constexpr int HM = M / 2, HD = D / 2, TB = 128 * D * 2;
+__global__ void __launch_bounds__(kFwdThreads, 1)
+fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __restrict__ status) {
+    constexpr int HM = M / 2, HD = D / 2, TB = 128 * D * 2, NS = kFwdStages;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* X0 = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char* KB[2];
-    unsigned char* VB[2];
-    KB[0] = X0 + TB;        // K~ block / P      (slot phase: K_c, masks, A_inter)
-    VB[0] = KB[0] + 32768;  // V block           (slot phase: V_c)
-    KB[1] = VB[0] + 32768;  //                   (slot phase: [S^K] then [S^V] pair)
-    VB[1] = KB[1] + 32768;  //                   (slot phase: Ek, then pEq at +16 KB)
-    float* s_tot = reinterpret_cast<float*>(VB[1] + 32768);  // [4][M]
-    float* sG = s_tot + 4 * M;                                // [2][M]
-    float* redm = sG + 2 * M;                                 // [2][128]
-    float* reds = redm + 256;                                 // [2][128]
-    __shared__ uint64_t bar;
+    unsigned char* KB[NS];
+    unsigned char* VB[NS];
+#pragma unroll
+    for (int q = 0; q < NS; q++) {
+        KB[q] = X0 + TB + q * 65536;  // K~ block, then P  (slot phase: K_c, masks, A_inter / [S^K], [S^V] pair)
+        VB[q] = KB[q] + 32768;        // V block           (slot phase: V_c / Ek, then pEq at +16 KB)
+    }
+    // slot-phase scratch and the epilogue's (m, l) exchange, in the last stage's
+    // V buffer (free during both)
+    float* s_tot = reinterpret_cast<float*>(VB[NS - 1]);  // [4][M]
+    float* sG = s_tot + 4 * M;                             // [2][M]
+    float* redm = sG + 2 * M;                              // [2][128]
+    float* reds = redm + 256;                              // [2][128]
+    __shared__ uint64_t bar, qbar, full[NS], sfull[2], pready, bdone[2], drain[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
     const Shape sh = a.sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
     const int W0 = sh.T - sh.R;
     const int NLT = (W0 + 127) / 128;
     const int x = blockIdx.x, bh = blockIdx.y;
@@ -71,171 +80,225 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
         nq = min(128, sh.R - j0);
         tbase = j0 + sh.w;
     }
-    const bool row_ok = r < nq;
     const size_t hoff = (size_t)bh * sh.T;
-    const __nv_bfloat16* q = (const __nv_bfloat16*)a.q + hoff * D;
-    const __nv_bfloat16* k = (const __nv_bfloat16*)a.k + hoff * D;
-    const __nv_bfloat16* v = (const __nv_bfloat16*)a.v + hoff * D;
-    qr += hoff * D;
-    kr += hoff * D;
-    const float sig2 = sh.sigma * kLog2e;
+    const int klo = max(0, tbase - sh.w + 1), khi = tbase + nq - 1;
+    const int nb = sh.w > 0 ? (khi - klo) / 128 + 1 : 0;
+    volatile int* abort = &s_abort;
 
-    if (tid < 2 * M) sG[tid] = 0.0f;
     if (tid == 0) {
         mbar_init(&bar, 1);
-        mbar_fence_init();
+        mbar_init(&qbar, 1);
+        for (int q = 0; q < NS; q++) mbar_init(&full[q], 1);
+        for (int q = 0; q < 2; q++) {
+            mbar_init(&sfull[q], 1);
+            mbar_init(&bdone[q], 1);
+        }
+        mbar_init(&pready, 8);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         s_abort = 0;
+        mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(&s_tmem, 256);
+    if (warp == 0) tmem_alloc(&s_tmem, 512);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tm = s_tmem;
-    const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lanes
-    const uint32_t tA = 0, tO = 128;                                 // column offsets
-    TcCtl ctl{&bar, 0u, &s_abort, status};
-    bool ok = true;
+    // TMEM columns: S buffers at 0 and 128; O_0 (slot branch and the first 64
+    // keys of every window block) at 256, O_1 (the other 64 keys) at 256 + D
+    const uint32_t tA = 0, tO = 256, tO1 = 256 + D;
 
-    float m = -INFINITY, l = 0.0f;  // running max (log2 domain) and sum of the row
-    bool o_valid = false;
-
-    if (slot) {
-        const int c1 = j0 / kChunk;
-        const bool has2 = nq > kChunk;
-        const __nv_bfloat16* SK1 = a.SKb + ((size_t)bh * sh.NC + c1) * M * D;
-        const __nv_bfloat16* SV1 = a.SVb + ((size_t)bh * sh.NC + c1) * M * D;
-        load_tile_async<D>(q, tbase, nq, X0);
-        load_tile_async<D>(k, j0, nq, KB[0]);
-        load_tile_async<D>(v, j0, nq, VB[0]);
-        load_state_pair_async<D, M>(SK1, has2 ? SK1 + M * D : nullptr, KB[1]);
-        cp_async_commit();
-        float lg[HM], b[HM], rho[HM];
-        row_gates<M>(a.la + (hoff + j0 + r) * M, row_ok, lg, b, s_tot, sG, warp, lane, h, r, nq);
-        {
-            float ek[HM];
+    int last_ph[NS];  // producer: phase of the last load issued into each stage
 #pragma unroll
-            for (int jj = 0; jj < HM; jj++) {
-                rho[jj] = 0.5f * sG[cr * M + h * HM + jj];
-                ek[jj] = row_ok ? fexp(rho[jj] - b[jj]) * (-expm1f(lg[jj])) : 0.0f;
+    for (int q = 0; q < NS; q++) last_ph[q] = -1;
+
+    if (warp == 8) {
+        // ---------------- producer ----------------
+        named_sync(2, kFwdThreads);  // the slot phase is done with the stage buffers
+        if (lane == 0 && nb > 0 && !s_abort) {
+            const bool o0 = slot;  // O_0 already holds the slot branch
+            auto load_block = [&](int j) {
+                const int stg = j % NS, kb = klo + j * 128;
+                mbar_arrive_expect_tx(&full[stg], 2 * TB);
+#pragma unroll
+                for (int xx = 0; xx < D; xx += 64) {
+                    tma_load_3d(KB[stg] + xx * 256, &maps.k, xx, kb, bh, &full[stg]);
+                    tma_load_3d(VB[stg] + xx * 256, &maps.v, xx, kb, bh, &full[stg]);
+                }
+                last_ph[stg] = (j / NS) & 1;
+            };
+            auto issue_s = [&](int j) {
+                const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[j % NS]);
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_bf16(tm + 128 * (j & 1), desc_k(s0, 128, kk), desc_k(s1, 128, kk),
+                             idesc_bf16(128, 128, false), kk > 0);
+                mma_commit(&sfull[j & 1]);
+            };
+            mbar_arrive_expect_tx(&qbar, TB);
+#pragma unroll
+            for (int xx = 0; xx < D; xx += 64) tma_load_3d(X0 + xx * 256, &maps.q, xx, tbase, bh, &qbar);
+            for (int j = 0; j < min(NS, nb); j++) load_block(j);
+            bool ok = mbar_wait_ab(&qbar, 0, kWaitCycles, abort) && mbar_wait_ab(&full[0], 0, kWaitCycles, abort);
+            if (ok) issue_s(0);
+            for (int i = 0; i < nb && ok; i++) {
+                if (i + 1 < nb) {  // S buffer (i + 1) & 1 was read by block i - 1 (before its pready)
+                    if (!(ok = mbar_wait_ab(&full[(i + 1) % NS], ((i + 1) / NS) & 1, kWaitCycles, abort))) break;
+                    issue_s(i + 1);
+                }
+                if (!(ok = mbar_wait_ab(&pready, i & 1, kWaitCycles, abort))) break;
+                fence_after_sync();
+                {
+                    const uint32_t sp = smem_u32(KB[i % NS]), sv = smem_u32(VB[i % NS]);
+                    for (int kk = 0; kk < 4; kk++)
+                        mma_bf16(tm + tO, desc_k(sp, 128, kk), desc_mn(sv, 128, kk), idesc_bf16(128, D, true),
+                                 (o0 || i > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 4; kk < 8; kk++)
+                        mma_bf16(tm + tO1, desc_k(sp, 128, kk), desc_mn(sv, 128, kk), idesc_bf16(128, D, true),
+                                 (i > 0 || kk > 4) ? 1u : 0u);
+                    mma_commit(&bdone[i & 1]);
+                }
+                if (i >= 1 && i - 1 + NS < nb) {  // block i - 1 done with its stage: refill it
+                    if (!(ok = mbar_wait_ab(&bdone[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitCycles, abort))) break;
+                    load_block(i - 1 + NS);
+                }
             }
-            store_row(VB[1], r, h * HM, ek, HM);
         }
-        cp_async_wait<0>();
-        sync_for_mma();
-        if (tid == 0) {
-            const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[0]), s3 = smem_u32(KB[1]);
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_bf16(tm + tA, desc_k(s0, 128, kk), desc_k(s1, 128, kk), idesc_bf16(128, 128, false), kk > 0);
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_bf16(tm + tO, desc_k(s0, 128, kk), desc_k(s3, 2 * M, kk), idesc_bf16(128, 2 * M, false), kk > 0);
-            mma_commit(&bar);
-        }
-        ok = ctl.wait();
-        if (ok) {
-            // A = Q K_c^T masked to the row's own chunk and s <= r; [S^V] replaces [S^K]
-            mask_to_tile(tl + tA, KB[0], r, h, cr, row_ok, false);
-            load_state_pair_async<D, M>(SV1, has2 ? SV1 + M * D : nullptr, KB[1]);
+    } else {
+        // ---------------- tile threads (warps 0-7) ----------------
+        const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
+        const bool row_ok = r < nq;
+        const __nv_bfloat16* q = (const __nv_bfloat16*)a.q + hoff * D;
+        const __nv_bfloat16* k = (const __nv_bfloat16*)a.k + hoff * D;
+        const __nv_bfloat16* v = (const __nv_bfloat16*)a.v + hoff * D;
+        const float sig2 = sh.sigma * kLog2e;
+        const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lanes
+        if (tid < 2 * M) sG[tid] = 0.0f;
+        named_sync(1, kTcThreads);
+        TcCtl ctl{&bar, 0u, &s_abort, status, true};
+        bool ok = true;
+        // online-softmax state of this thread's half of the keys (log2 domain);
+        // half 0 also carries the slot branch
+        float m = -INFINITY, l = 0.0f;
+        bool o_valid = false;
+
+        if (slot) {
+            const int c1 = j0 / kChunk;
+            const bool has2 = nq > kChunk;
+            const __nv_bfloat16* SK1 = a.SKb + ((size_t)bh * sh.NC + c1) * M * D;
+            const __nv_bfloat16* SV1 = a.SVb + ((size_t)bh * sh.NC + c1) * M * D;
+            load_tile_async<D>(q, tbase, nq, X0);
+            load_tile_async<D>(k, j0, nq, KB[0]);
+            load_tile_async<D>(v, j0, nq, VB[0]);
+            load_state_pair_async<D, M>(SK1, has2 ? SK1 + M * D : nullptr, KB[1]);
             cp_async_commit();
-            sync_for_mma();
-            if (tid == 0) {
-                const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[1]);
-                for (int kk = 0; kk < 8; kk++)
-                    mma_bf16(tm + tA, desc_k(s1, 128, kk), desc_mn(s2, 128, kk), idesc_bf16(128, M, true), kk > 0);
-                mma_commit(&bar);
-            }
-            ok = ctl.wait();
-        }
-        if (ok) {
-            float sint[HM], lin[HM], L[HM];
-            tmem_ld(tl + tO + cr * M + h * HM, sint, HM);
-            tmem_ld(tl + tA + h * HM, lin, HM);
-            float mx = -INFINITY;
+            float lg[HM], b[HM], rho[HM];
+            row_gates<M, true>(a.la + (hoff + j0 + r) * M, row_ok, lg, b, s_tot, sG, warp, lane, h, r, nq);
+            {
+                float ek[HM];
 #pragma unroll
-            for (int jj = 0; jj < HM; jj++) {
-                L[jj] = row_ok ? sig2 * (fexp(b[jj]) * sint[jj] + fexp(b[jj] - rho[jj]) * lin[jj]) : -INFINITY;
-                mx = fmaxf(mx, L[jj]);
+                for (int jj = 0; jj < HM; jj++) {
+                    rho[jj] = 0.5f * sG[cr * M + h * HM + jj];
+                    ek[jj] = row_ok ? fexp(rho[jj] - b[jj]) * (-expm1f(lg[jj])) : 0.0f;
+                }
+                store_row(VB[1], r, h * HM, ek, HM);
             }
-            redm[h * 128 + r] = mx;
-            __syncthreads();
-            m = fmaxf(redm[r], redm[128 + r]);
-            float ps = 0.0f, pe[HM], pq[HM], z[HM];
-#pragma unroll
-            for (int jj = 0; jj < HM; jj++) {
-                const float p = (m == -INFINITY) ? 0.0f : ex2(L[jj] - m);
-                ps += p;
-                pe[jj] = p * fexp(b[jj]);
-                pq[jj] = p * fexp(b[jj] - rho[jj]);
-                z[jj] = 0.0f;
-            }
-            reds[h * 128 + r] = ps;
-            // A_inter [128][2M]: this row's chunk block holds p o Eb, the other block zero
-            store_row(KB[0], r, cr * M + h * HM, pe, HM);
-            store_row(KB[0], r, (1 - cr) * M + h * HM, z, HM);
-            store_row(VB[1] + 16384, r, h * HM, pq, HM);  // pEq, after Ek
-            __syncthreads();
-            l = reds[r] + reds[128 + r];
-            cp_async_wait<0>();  // [S^V] pair
-            sync_for_mma();
+            cp_async_wait<0>();
+            sync_for_mma<true>();
             if (tid == 0) {
-                const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[1]), s3 = smem_u32(KB[1]);
-                for (int kk = 0; kk < 2 * M / 16; kk++)
-                    mma_bf16(tm + tO, desc_k(s1, 128, kk), desc_mn(s3, 2 * M, kk), idesc_bf16(128, D, true), kk > 0);
-                for (int kk = 0; kk < M / 16; kk++)
-                    mma_bf16(tm + tA, desc_k(s2 + 16384, 128, kk), desc_k(s2, 128, kk), idesc_bf16(128, 128, false),
-                             kk > 0);
+                const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[0]), s3 = smem_u32(KB[1]);
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_bf16(tm + tA, desc_k(s0, 128, kk), desc_k(s1, 128, kk), idesc_bf16(128, 128, false), kk > 0);
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_bf16(tm + tO, desc_k(s0, 128, kk), desc_k(s3, 2 * M, kk), idesc_bf16(128, 2 * M, false), kk > 0);
                 mma_commit(&bar);
             }
             ok = ctl.wait();
-        }
-        if (ok) {
-            mask_to_tile(tl + tA, KB[0], r, h, cr, row_ok, false);
-            sync_for_mma();
-            if (tid == 0) {
-                const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[0]);
-                for (int kk = 0; kk < 8; kk++)
-                    mma_bf16(tm + tO, desc_k(s1, 128, kk), desc_mn(s2, 128, kk), idesc_bf16(128, D, true), 1);
-                mma_commit(&bar);
-            }
-            ok = ctl.wait();
-            o_valid = true;
-        }
-    }
-
-    // ---- window branch over the band of keys [tbase - w + 1, tbase + nq - 1],
-    // key/value blocks double-buffered: block i + 1 loads while block i computes
-    if (ok && sh.w > 0) {
-        const int klo = max(0, tbase - sh.w + 1), khi = tbase + nq - 1;
-        const int nb = (khi - klo) / 128 + 1;
-        const int t = tbase + r;
-        load_tile_async<D>(qr, tbase, nq, X0);
-        load_tile_async<D>(kr, klo, min(128, khi - klo + 1), KB[0]);
-        load_tile_async<D>(v, klo, min(128, khi - klo + 1), VB[0]);
-        cp_async_commit();
-        auto issue_s = [&](int i) {
-            const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[i & 1]);
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_bf16(tm + tA, desc_k(s0, 128, kk), desc_k(s1, 128, kk), idesc_bf16(128, 128, false), kk > 0);
-        };
-        cp_async_wait<0>();
-        sync_for_mma();
-        if (tid == 0) {
-            issue_s(0);
-            mma_commit(&bar);
-        }
-        // One wait per block: the commit after block i's S also covers block
-        // i - 1's P V, issued just before it.
-        for (int i = 0; i < nb && ok; i++) {
-            const int kb = klo + i * 128, nk = min(128, khi - kb + 1), cur = i & 1;
-            ok = ctl.wait();
-            if (!ok) break;
-            if (i + 1 < nb) {  // stage of block i - 1, whose P V is complete
-                const int kn = kb + 128, nn = min(128, khi - kn + 1);
-                load_tile_async<D>(kr, kn, nn, KB[cur ^ 1]);
-                load_tile_async<D>(v, kn, nn, VB[cur ^ 1]);
+            if (ok) {
+                // A = Q K_c^T masked to the row's own chunk and s <= r; [S^V] replaces [S^K]
+                mask_to_tile(tl + tA, KB[0], r, h, cr, row_ok, false);
+                load_state_pair_async<D, M>(SV1, has2 ? SV1 + M * D : nullptr, KB[1]);
                 cp_async_commit();
+                sync_for_mma<true>();
+                if (tid == 0) {
+                    const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[1]);
+                    for (int kk = 0; kk < 8; kk++)
+                        mma_bf16(tm + tA, desc_k(s1, 128, kk), desc_mn(s2, 128, kk), idesc_bf16(128, M, true), kk > 0);
+                    mma_commit(&bar);
+                }
+                ok = ctl.wait();
             }
+            if (ok) {
+                float sint[HM], lin[HM], L[HM];
+                tmem_ld(tl + tO + cr * M + h * HM, sint, HM);
+                tmem_ld(tl + tA + h * HM, lin, HM);
+                float mx = -INFINITY;
+#pragma unroll
+                for (int jj = 0; jj < HM; jj++) {
+                    L[jj] = row_ok ? sig2 * (fexp(b[jj]) * sint[jj] + fexp(b[jj] - rho[jj]) * lin[jj]) : -INFINITY;
+                    mx = fmaxf(mx, L[jj]);
+                }
+                redm[h * 128 + r] = mx;
+                named_sync(1, kTcThreads);
+                m = fmaxf(redm[r], redm[128 + r]);
+                float ps = 0.0f, pe[HM], pq[HM], z[HM];
+#pragma unroll
+                for (int jj = 0; jj < HM; jj++) {
+                    const float p = (m == -INFINITY) ? 0.0f : ex2(L[jj] - m);
+                    ps += p;
+                    pe[jj] = p * fexp(b[jj]);
+                    pq[jj] = p * fexp(b[jj] - rho[jj]);
+                    z[jj] = 0.0f;
+                }
+                reds[h * 128 + r] = ps;
+                // A_inter [128][2M]: this row's chunk block holds p o Eb, the other block zero
+                store_row(KB[0], r, cr * M + h * HM, pe, HM);
+                store_row(KB[0], r, (1 - cr) * M + h * HM, z, HM);
+                store_row(VB[1] + 16384, r, h * HM, pq, HM);  // pEq, after Ek
+                named_sync(1, kTcThreads);
+                l = reds[r] + reds[128 + r];
+                cp_async_wait<0>();  // [S^V] pair
+                sync_for_mma<true>();
+                if (tid == 0) {
+                    const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[1]), s3 = smem_u32(KB[1]);
+                    for (int kk = 0; kk < 2 * M / 16; kk++)
+                        mma_bf16(tm + tO, desc_k(s1, 128, kk), desc_mn(s3, 2 * M, kk), idesc_bf16(128, D, true), kk > 0);
+                    for (int kk = 0; kk < M / 16; kk++)
+                        mma_bf16(tm + tA, desc_k(s2 + 16384, 128, kk), desc_k(s2, 128, kk), idesc_bf16(128, 128, false),
+                                 kk > 0);
+                    mma_commit(&bar);
+                }
+                ok = ctl.wait();
+            }
+            if (ok) {
+                mask_to_tile(tl + tA, KB[0], r, h, cr, row_ok, false);
+                sync_for_mma<true>();
+                if (tid == 0) {
+                    const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[0]);
+                    for (int kk = 0; kk < 8; kk++)
+                        mma_bf16(tm + tO, desc_k(s1, 128, kk), desc_mn(s2, 128, kk), idesc_bf16(128, D, true), 1);
+                    mma_commit(&bar);
+                }
+                ok = ctl.wait();
+                o_valid = true;
+            }
+        }
+
+        if (h == 1) {  // the slot branch belongs to half 0's softmax state
+            m = -INFINITY;
+            l = 0.0f;
+        }
+        if (!ok && tid == 0) *abort = 1;  // slot phase gave up: the producer stands down
+        fence_before_sync();
+        asm volatile("bar.arrive 2, %0;\n" ::"n"(kFwdThreads) : "memory");  // stages free for the producer
+
+        // ---- window branch: 128-key blocks of the band [tbase - w + 1, tbase + nq - 1]
+        const int t = tbase + r;
+        for (int i = 0; i < nb && ok; i++) {
+            const int kb = klo + i * 128, nk = min(128, khi - kb + 1), b = i & 1, stg = i % NS;
+            if (!(ok = mbar_wait_ab(&sfull[b], (i >> 1) & 1, kWaitCycles, abort))) break;
+            fence_after_sync();
             float sv[64];
-            tmem_ld(tl + tA + 64 * h, sv, 64);
+            tmem_ld(tl + 128 * b + 64 * h, sv, 64);
             float bm = -INFINITY;
             // valid keys of this row: columns [clo, chi] of the block
             const int clo = max(0, t - sh.w + 1 - kb) - 64 * h;
@@ -245,13 +308,13 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
                 sv[jj] = (jj >= clo && jj <= chi) ? sv[jj] * sig2 : -INFINITY;
                 bm = fmaxf(bm, sv[jj]);
             }
-            redm[h * 128 + r] = bm;
-            __syncthreads();
-            bm = fmaxf(redm[r], redm[128 + r]);
+            // P V of block i - 1 done: its accumulator may be rescaled below
+            if (i >= 1 && !(ok = mbar_wait_ab(&bdone[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitCycles, abort))) break;
+            const bool acc_live = h == 0 ? (o_valid || i > 0) : i > 0;  // this half's O holds data
             const float mnew = fmaxf(m, bm);
             bool resc = false;
             float scale = 1.0f;
-            if (!o_valid || m == -INFINITY) {
+            if (!acc_live || m == -INFINITY) {
                 m = mnew;
             } else if (mnew > m + 8.0f) {
                 resc = true;
@@ -259,13 +322,14 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
                 m = mnew;
                 l *= scale;
             }
-            if (o_valid && __any_sync(0xffffffffu, resc)) {
-                for (int c0 = 0; c0 < HD; c0 += 32) {
+            if (__any_sync(0xffffffffu, resc)) {
+                const uint32_t to = tl + (h == 0 ? tO : tO1);
+                for (int c0 = 0; c0 < D; c0 += 32) {
                     float ov[32];
-                    tmem_ld32(tl + tO + h * HD + c0, ov);
+                    tmem_ld32(to + c0, ov);
 #pragma unroll
                     for (int jj = 0; jj < 32; jj++) ov[jj] *= scale;
-                    tmem_st32(tl + tO + h * HD + c0, ov);
+                    tmem_st32(to + c0, ov);
                 }
             }
             float ps = 0.0f;
@@ -275,49 +339,77 @@ fwd_tc_kernel(const FwdArgs a, const __nv_bfloat16* __restrict__ qr, const __nv_
                 sv[jj] = p;
                 ps += p;
             }
-            reds[h * 128 + r] = ps;
-            store_row(KB[cur], r, 64 * h, sv, 64);
-            if (i + 1 < nb) cp_async_wait<0>();
-            sync_for_mma();
-            l += reds[r] + reds[128 + r];
-            if (tid == 0) {
-                const uint32_t s1 = smem_u32(KB[cur]), s2 = smem_u32(VB[cur]);
-                for (int kk = 0; kk < 8; kk++)
-                    mma_bf16(tm + tO, desc_k(s1, 128, kk), desc_mn(s2, 128, kk), idesc_bf16(128, D, true),
-                             (o_valid || kk > 0) ? 1u : 0u);
-                if (i + 1 < nb) issue_s(i + 1);
-                mma_commit(&bar);
-            }
-            o_valid = true;
+            l += ps;
+            store_row(KB[stg], r, 64 * h, sv, 64);  // P over the consumed K~ block
+            fence_async_smem();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pready);
         }
-        if (ok) ok = ctl.wait();  // the last block's P V
-        cp_async_wait<0>();
-    }
+        if (ok && nb > 0) ok = mbar_wait_ab(&bdone[(nb - 1) & 1], ((nb - 1) >> 1) & 1, kWaitCycles, abort);
 
-    // ---- epilogue: o = O / l, lse = m ln2 + log l
-    if (ok) {
-        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-        const int t = tbase + r;
-        __nv_bfloat16* orow = (__nv_bfloat16*)a.o + (hoff + t) * D;
-        for (int c0 = 0; c0 < HD; c0 += 32) {
-            float ov[32];
-            tmem_ld32(tl + tO + h * HD + c0, ov);
-            if (row_ok) {
+        // ---- epilogue: merge the halves, o = (f0 O_0 + f1 O_1) / l, lse = m ln2 + log l
+        redm[h * 128 + r] = m;
+        reds[h * 128 + r] = l;
+        if (named_sync_or(1, kTcThreads, !ok)) ok = false;
+        const float m0 = redm[r], m1 = redm[128 + r];
+        const float mm = fmaxf(m0, m1);
+        const float f0 = m0 == -INFINITY ? 0.0f : ex2(m0 - mm), f1 = m1 == -INFINITY ? 0.0f : ex2(m1 - mm);
+        const float lt = reds[r] * f0 + reds[128 + r] * f1;
+        const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+        const bool o0 = o_valid || nb > 0, o1 = nb > 0;
+        unsigned char* stg = KB[0];
+        if (ok) {
+            fence_after_sync();
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                float u0[32], u1[32];
+                if (o0 && o1) {
+                    tmem_ld32x2(tl + tO + h * HD + c0, tl + tO1 + h * HD + c0, u0, u1);
+                } else {
+                    if (o0) tmem_ld32(tl + tO + h * HD + c0, u0);
 #pragma unroll
-                for (int jj = 0; jj < 32; jj++) ov[jj] *= inv;
+                    for (int jj = 0; jj < 32; jj++) {
+                        if (!o0) u0[jj] = 0.0f;
+                        u1[jj] = 0.0f;
+                    }
+                }
 #pragma unroll
-                for (int qq = 0; qq < 4; qq++)
-                    *reinterpret_cast<uint4*>(orow + h * HD + c0 + qq * 8) = pack8(ov + qq * 8);
+                for (int jj = 0; jj < 32; jj++) u0[jj] = (u0[jj] * f0 + u1[jj] * f1) * inv;
+                store_row(stg, r, h * HD + c0, u0, 32);
             }
         }
-        if (h == 0 && row_ok) a.lse[hoff + t] = m * kLn2 + logf(l);
-    } else if (h == 0 && row_ok) {
-        a.lse[hoff + tbase + r] = __int_as_float(0x7fc00000);  // NaN marks the failed tile
+        const int bad = named_sync_or(1, kTcThreads, !ok);
+        if (!bad) {  // rows [0, nq) of the tile, 16-byte chunks, coalesced
+            constexpr int CH = D / 8;
+            __nv_bfloat16* ob = (__nv_bfloat16*)a.o + (hoff + tbase) * D;
+            for (int e = tid; e < nq * CH; e += kTcThreads) {
+                const int rr = e / CH, ch = e % CH;
+                *reinterpret_cast<uint4*>(ob + (size_t)rr * D + ch * 8) =
+                    *reinterpret_cast<const uint4*>(stg + sw_chunk(rr, ch, 128));
+            }
+            if (h == 0 && row_ok) a.lse[hoff + t] = mm * kLn2 + logf(lt);
+        } else if (h == 0 && row_ok) {
+            a.lse[hoff + t] = __int_as_float(0x7fc00000);  // NaN marks the failed tile
+        }
     }
-    if (!ok && tid == 0) mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);  // let in-flight MMAs drain
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, 256);
+    if (s_abort) {  // let the copies and MMAs in flight land before the TMEM and the CTA go
+        if (tid == 0) {  // slot-branch MMAs (issued by this thread)
+            mma_commit(&drain[0]);
+            mbar_wait(&drain[0], 0, kWaitCycles);
+        }
+        if (warp == 8 && lane == 0) {  // window MMAs and copies
+            mma_commit(&drain[1]);
+            mbar_wait(&drain[1], 0, kWaitCycles);
+            if (nb > 0) mbar_wait(&qbar, 0, kWaitCycles);
+            for (int q = 0; q < NS; q++)
+                if (last_ph[q] >= 0) mbar_wait(&full[q], (uint32_t)last_ph[q], kWaitCycles);
+        }
+        __syncthreads();
+        if (tid == 0) atomicExch(status, kStatusTimeout);
+    }
+    if (warp == 0) tmem_dealloc(tm, 512);
 }
 
 // RoPE applied once per call: qr = RoPE(q), kr = RoPE(k) at absolute positions.
@@ -367,7 +459,7 @@ cudaError_t launch_rope_table(float2* tab, int T, int H2, const RopeTab& rt, cud
 
 template <int D, int M>
 size_t tc_fwd_smem() {
-    return 1024 + 128 * D * 2 + 4 * 32768 + sizeof(float) * (6 * M + 512);
+    return 1024 + 128 * D * 2 + kFwdStages * 65536;
 }
 
 template <int D, int M>
@@ -382,12 +474,17 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bf
     if (sh.w > 0 && (e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, sh, st)) != cudaSuccess) return e;
     const int W0 = sh.T - sh.R;
     const int tiles = (W0 + 127) / 128 + (sh.R + 127) / 128;
+    if (tiles == 0) return cudaSuccess;
+    FwdMaps maps;
+    if ((e = tmap_rows_bf16(&maps.q, qr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.k, kr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.v, a.v, D, sh.T, sh.BH, 128)) != cudaSuccess)
+        return e;
     const size_t sm = tc_fwd_smem<D, M>();
     auto kern = fwd_tc_kernel<D, M>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    if (tiles > 0)
-        NHA_LAUNCH("fwd_tc", st, kern<<<dim3(tiles, sh.BH), kTcThreads, sm, st>>>(a, qr, kr, status));
+    NHA_LAUNCH("fwd_tc", st, kern<<<dim3(tiles, sh.BH), kFwdThreads, sm, st>>>(a, maps, status));
     return cudaGetLastError();
 }
 

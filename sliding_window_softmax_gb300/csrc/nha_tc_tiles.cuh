@@ -188,17 +188,28 @@ __device__ __forceinline__ void store_row(unsigned char* tile, int row, int col0
         *reinterpret_cast<uint4*>(tile + sw_chunk(row, (col0 + c) >> 3, 128)) = pack8(v + c);
 }
 
+// Barrier over the tile threads: the whole CTA, or (kProd) the 256 tile
+// threads alone, on hardware barrier 1, in kernels that add a producer warp.
+template <bool kProd>
+__device__ __forceinline__ void tile_sync() {
+    if constexpr (kProd)
+        named_sync(1, kTcThreads);
+    else
+        __syncthreads();
+}
+
 struct TcCtl {
     uint64_t* bar;
     uint32_t phase;
     int* s_abort;
     int* status;
-    // Wait for the MMAs committed last; uniform across the CTA; false on timeout.
+    bool named = false;  // the 256 tile threads only (barrier 1), not the whole CTA
+    // Wait for the MMAs committed last; uniform across the tile threads; false on timeout.
     __device__ bool wait() {
         const bool ok = mbar_wait(bar, phase, kWaitCycles);
         phase ^= 1u;
         fence_after_sync();
-        if (__syncthreads_or(!ok)) {
+        if (named ? named_sync_or(1, kTcThreads, !ok) : __syncthreads_or(!ok)) {
             if (threadIdx.x == 0) atomicExch(status, kStatusTimeout);
             return false;
         }
@@ -219,17 +230,18 @@ struct TcBar {
     }
 };
 
+template <bool kProd = false>
 __device__ __forceinline__ void sync_for_mma() {
     fence_async_smem();
     fence_before_sync();
-    __syncthreads();
+    tile_sync<kProd>();
     fence_after_sync();
 }
 
 
 // Inclusive cumsum of x over the 64 rows of this thread's chunk (tile rows
 // 0-63 or 64-127), for the HM slots i = h HM + jj.  s_tot: [4][M] scratch.
-template <int M>
+template <int M, bool kProd = false>
 __device__ __forceinline__ void chunk_prefix(float (&x)[M / 2], float* s_tot, int warp, int lane, int h) {
     constexpr int HM = M / 2;
     const int wq = warp & 3;
@@ -244,11 +256,11 @@ __device__ __forceinline__ void chunk_prefix(float (&x)[M / 2], float* s_tot, in
         x[jj] = v;
         if (lane == 31) s_tot[wq * M + h * HM + jj] = v;
     }
-    __syncthreads();
+    tile_sync<kProd>();
     if (wq & 1)
 #pragma unroll
         for (int jj = 0; jj < HM; jj++) x[jj] += s_tot[(wq - 1) * M + h * HM + jj];
-    __syncthreads();
+    tile_sync<kProd>();
 }
 
 // Inclusive suffix sum of x over the 64 rows of this thread's chunk.
@@ -276,7 +288,7 @@ __device__ __forceinline__ void chunk_suffix(float (&x)[M / 2], float* s_tot, in
 
 // Gates of this thread's row: loads log_alpha (0 past the valid rows), the
 // chunk-local cumsum b and the chunk totals sG[2][M] (zero for an empty chunk).
-template <int M>
+template <int M, bool kProd = false>
 __device__ __forceinline__ void row_gates(const float* __restrict__ la_row, bool valid, float (&l)[M / 2],
                                           float (&b)[M / 2], float* s_tot, float* sG, int warp, int lane,
                                           int h, int r, int nrows) {
@@ -289,12 +301,12 @@ __device__ __forceinline__ void row_gates(const float* __restrict__ la_row, bool
     }
 #pragma unroll
     for (int jj = 0; jj < HM; jj++) b[jj] = l[jj];
-    chunk_prefix<M>(b, s_tot, warp, lane, h);
+    chunk_prefix<M, kProd>(b, s_tot, warp, lane, h);
     const int cc = r >> 6, last = min(nrows, 64 * (cc + 1)) - 1;
     if (r == last)
 #pragma unroll
         for (int jj = 0; jj < HM; jj++) sG[cc * M + h * HM + jj] = b[jj];
-    __syncthreads();
+    tile_sync<kProd>();
 }
 
 __device__ __forceinline__ void zero_cols(unsigned char* tile, int row, int c0, int c1) {
