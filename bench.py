@@ -72,6 +72,10 @@ def work_model(wl):
         # (bf16) and SIMT (fp32) kernels of the same step share a model
         "fwd_tc": fwd_main, "fwd_main": fwd_main,
         "state_chunk": (BH * 4 * m * d * R, BH * R * (2 * d * e + 4 * m)),
+        # bf16 path: chunk coefficients (log_alpha in, U and G out), then the
+        # fused chunk scan (K, V, U in; the bf16 states entering each chunk out)
+        "state_gates": (0, BH * R * (4 * m + 128)),
+        "state_scan": (BH * 4 * m * d * R, BH * R * (2 * d * e + 128) + BH * ((R + 63) // 64) * 4 * m * d),
         "bwd_wdq_tc": wdq, "bwd_window_dq": wdq,
         "bwd_wkv_tc": wkv, "bwd_window_dkdv": wkv,
         "bwd_sq_tc": sq, "bwd_slot_query": sq,

@@ -467,7 +467,7 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bf
                        cudaStream_t st) {
     const Shape& sh = a.sh;
     cudaError_t e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV,
-                                    a.SKb, a.SVb, a.G, sh, status, st);
+                                    a.SKb, a.SVb, a.G, a.U, false, sh, status, st);
     if (e != cudaSuccess) return e;
     e = launch_rope_table(tab, sh.T, D / 2, a.rope, st);
     if (e != cudaSuccess) return e;

@@ -27,6 +27,7 @@ struct FwdArgs {
     float* G;
     __nv_bfloat16* SKb;  // bf16 copies of SK, SV (bf16 path)
     __nv_bfloat16* SVb;
+    __nv_bfloat16* U;    // chunk coefficients (bf16 path)
     Shape sh;
     RopeTab rope;
 };
@@ -65,6 +66,7 @@ struct BwdArgs {
     __nv_bfloat16* SVb;
     __nv_bfloat16* RKb;
     __nv_bfloat16* RVb;
+    __nv_bfloat16* U;  // chunk coefficients (bf16 path)
     // bf16 path: the window partials and sigma dL, P_L are kept in bf16 (they
     // alias the storage of the fp32 arrays above)
     __nv_bfloat16* hdqw;
@@ -111,11 +113,12 @@ cudaError_t launch_wkv(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bfl
                        int* status, cudaStream_t st);
 cudaError_t launch_state_scan_rev(const BwdArgs& a, int M, int D, cudaStream_t st);
 cudaError_t launch_dla_carry(const BwdArgs& a, int M, int D, cudaStream_t st);
-// bf16 path: chunk states on the tensor core, then the forward chunk scan.
+// bf16 path: chunk coefficients U (workspace, [BH][NC * C][64] bf16) and
+// totals G, then the states entering every chunk in bf16 (and fp32 if want_f32).
 template <int D, int M>
 cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const float* la, float* SK, float* SV,
-                      __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, const Shape& sh, int* status,
-                      cudaStream_t st);
+                      __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, __nv_bfloat16* U, bool want_f32,
+                      const Shape& sh, int* status, cudaStream_t st);
 // Chunk scan (dir > 0: states before each chunk; dir < 0: adjoints carried in),
 // fp32 in place plus a bf16 copy in B0 / B1.
 cudaError_t launch_scan8(float* X0, float* X1, __nv_bfloat16* B0, __nv_bfloat16* B1, const float* G,

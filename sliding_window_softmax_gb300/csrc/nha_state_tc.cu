@@ -4,130 +4,191 @@
 // chunk's end is dS_c = U_c^T X_c with U_c[s][i] = exp(G_i - b_{s,i}) u_{s,i}
 // ("Native Hybrid Attention for Efficient Sequence Modeling", Paper-Notes page,
 // 关键设计/层内混合: K^long_t = Diag(alpha_t) K^long_{t-1} + (1 - alpha_t) (x) k_t,
-// unrolled over one chunk), for X = K and X = V.  A 128-row tile holds two
-// chunks; the tensor core forms dS^T = X^T [U_c1 | U_c2] (d rows, 2m columns)
-// in one MMA per tensor.  A second kernel scans the chunks:
-// S_prev(c + 1) = exp(G_c) S_prev(c) + dS_c.
+// unrolled over one chunk), for X = K and X = V, and the states entering the
+// chunks follow S_prev(c + 1) = exp(G_c) S_prev(c) + dS_c.
+//
+// Two kernels.  state_gates: every chunk in parallel, the coefficients U
+// (bf16, 64 columns, slots past m zero) and the chunk totals G.  state_scan:
+// one CTA per (head, K or V) walks the chunks in order; a producer warp
+// streams X_c and U_c through TMA stages and forms dS_c^T = X_c^T U_c on the
+// tensor core into one of two TMEM buffers, while four warps (thread = one
+// column d of the state) carry the state in fp32 registers and write S_prev(c).
 #include "nha_common.cuh"
 #include "nha_kernels.h"
 #include "nha_prof.h"
 #include "nha_tc.cuh"
 #include "nha_tc_tiles.cuh"
+#include "nha_tma.h"
 
 namespace nha {
 
-template <int D, int M>
-__global__ void __launch_bounds__(kTcThreads, 1)
-state_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
-                const float* __restrict__ la, float* __restrict__ SK, float* __restrict__ SV,
-                float* __restrict__ G, Shape sh, int* __restrict__ status) {
+// U row j (64 bf16) and G of the two chunks of a 128-row tile.
+template <int M>
+__global__ void __launch_bounds__(kTcThreads)
+state_gates_kernel(const float* __restrict__ la, __nv_bfloat16* __restrict__ U, float* __restrict__ G, Shape sh) {
     constexpr int HM = M / 2;
+    __shared__ float s_tot[4 * M];
+    __shared__ float sG[2 * M];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
+    const int bh = blockIdx.y, j0 = blockIdx.x * 128, n = max(0, min(128, sh.R - j0));
+    const int rows = min(128, sh.NC * kChunk - j0);  // rows of U this tile defines
+    const bool row_ok = r < n;
+    const size_t hoff = (size_t)bh * sh.T;
+    if (tid < 2 * M) sG[tid] = 0.0f;
+    __syncthreads();
+    float l[HM], b[HM];
+    row_gates<M>(la + (hoff + j0 + (row_ok ? r : 0)) * M, row_ok, l, b, s_tot, sG, warp, lane, h, r, n);
+    if (r < rows) {
+        float u[HM];
+#pragma unroll
+        for (int jj = 0; jj < HM; jj++) u[jj] = row_ok ? fexp(sG[cr * M + h * HM + jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
+        __nv_bfloat16* ur = U + ((size_t)bh * sh.NC * kChunk + j0 + r) * 64;
+#pragma unroll
+        for (int jj = 0; jj < HM; jj += 8) *reinterpret_cast<uint4*>(ur + h * HM + jj) = pack8(u + jj);
+        if (M < 64) {
+            constexpr int PAD = (64 - M) / 2;
+#pragma unroll
+            for (int jj = 0; jj < PAD; jj += 8)
+                *reinterpret_cast<uint4*>(ur + M + h * PAD + jj) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    if (tid < 2 * M) {
+        const int cc = tid / M, c = j0 / kChunk + cc;
+        if (c < sh.NC) G[((size_t)bh * sh.NC + c) * M + (tid % M)] = sG[tid];
+    }
+}
+
+constexpr int kScanThreads = 160, kScanStages = 4;
+
+struct StateMaps {
+    CUtensorMap x[2];  // K, V rows, box {64, 64}
+    CUtensorMap u;     // U rows, box {64, 64}
+};
+
+template <int D, int M>
+__global__ void __launch_bounds__(kScanThreads, 1)
+state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __restrict__ G, float* __restrict__ SK,
+                     float* __restrict__ SV, __nv_bfloat16* __restrict__ SKb, __nv_bfloat16* __restrict__ SVb,
+                     Shape sh, int want_f32, int* __restrict__ status) {
+    constexpr int NS = kScanStages;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* XK = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char* XV = XK + 32768;  // [128 s][128 d] (d >= D zero)
-    unsigned char* XU = XV + 32768;  // [128 s][2M] chunk-blocked coefficients
-    float* s_tot = reinterpret_cast<float*>(XU + 32768);  // [4][M]
-    float* sG = s_tot + 4 * M;                             // [2][M]
-    __shared__ uint64_t bar;
+    unsigned char* base = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // stage s: X_c [64 tokens][128 d] (d >= D zero), U_c [64 tokens][64], G_c [M]
+    auto XT = [&](int st) { return base + st * 16384; };
+    auto UT = [&](int st) { return base + NS * 16384 + st * 8192; };
+    auto GS = [&](int st) { return reinterpret_cast<float*>(base + NS * 24576 + st * 256); };
+    __shared__ uint64_t full[NS], empty[NS], sfull[2], tfree[2], drain;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
-    const int bh = blockIdx.y, j0 = blockIdx.x * 128, n = min(128, sh.R - j0);
-    const int c1 = j0 / kChunk;
-    const bool has2 = n > kChunk, row_ok = r < n;
-    const size_t hoff = (size_t)bh * sh.T;
-
-    if (tid < 2 * M) sG[tid] = 0.0f;
+    const int bh = blockIdx.x, tz = blockIdx.y;  // tz 0: K, 1: V
+    const int NC = sh.NC;
+    volatile int* abort = &s_abort;
     if (tid == 0) {
-        mbar_init(&bar, 1);
-        mbar_fence_init();
+        for (int q = 0; q < NS; q++) {
+            mbar_init(&full[q], 1);
+            mbar_init(&empty[q], 4);
+        }
+        for (int q = 0; q < 2; q++) {
+            mbar_init(&sfull[q], 1);
+            mbar_init(&tfree[q], 4);
+        }
+        mbar_init(&drain, 1);
         s_abort = 0;
+        mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(&s_tmem, 256);
-    load_tile<D>(k + hoff * D, j0, n, XK, nullptr);
-    load_tile<D>(v + hoff * D, j0, n, XV, nullptr);
-    if (D < 128) {  // the MMA reads 128 columns of d: zero the unused block
-        for (int e = tid; e < 128 * 8; e += kTcThreads) {
-            const int rr = e >> 3, ch = 8 + (e & 7);
-            *reinterpret_cast<uint4*>(XK + sw_chunk(rr, ch, 128)) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(XV + sw_chunk(rr, ch, 128)) = make_uint4(0, 0, 0, 0);
-        }
-    }
-    // gates of this row: b = chunk-local inclusive cumsum, G = chunk total
-    float l[HM], b[HM];
-#pragma unroll
-    for (int jj = 0; jj < HM; jj += 4) {
-        const float4 q = row_ok ? __ldg(reinterpret_cast<const float4*>(la + (hoff + j0 + r) * M + h * HM + jj))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-        l[jj] = q.x; l[jj + 1] = q.y; l[jj + 2] = q.z; l[jj + 3] = q.w;
-    }
-#pragma unroll
-    for (int jj = 0; jj < HM; jj++) b[jj] = l[jj];
-    chunk_prefix<M>(b, s_tot, warp, lane, h);
-    {
-        const int last = min(n, 64 * (cr + 1)) - 1;
-        if (r == last)
-#pragma unroll
-            for (int jj = 0; jj < HM; jj++) sG[cr * M + h * HM + jj] = b[jj];
-    }
-    __syncthreads();
-    {
-        float u[HM], z[HM];
-#pragma unroll
-        for (int jj = 0; jj < HM; jj++) {
-            u[jj] = row_ok ? fexp(sG[cr * M + h * HM + jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
-            z[jj] = 0.0f;
-        }
-        store_row(XU, r, cr * M + h * HM, u, HM);
-        store_row(XU, r, (1 - cr) * M + h * HM, z, HM);
-    }
-    if (tid < 2 * M) {
-        const int cc = tid / M;
-        if (cc == 0 || has2) G[((size_t)bh * sh.NC + c1 + cc) * M + (tid % M)] = sG[tid];
-    }
+    if (D < 128)  // the MMA spans 128 columns of d: the upper block stays zero
+        for (int e = tid; e < NS * 512; e += kScanThreads)
+            reinterpret_cast<uint4*>(XT(e / 512) + 8192)[e % 512] = make_uint4(0, 0, 0, 0);
+    if (warp == 0) tmem_alloc(&s_tmem, 128);
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tm = s_tmem;
-    if (tid == 0) {
-        const uint32_t sk = smem_u32(XK), sv = smem_u32(XV), su = smem_u32(XU);
-        for (int kk = 0; kk < 8; kk++)
-            mma_bf16(tm, desc_mn(sk, 128, kk), desc_mn(su, 128, kk), idesc_bf16(128, 2 * M, true) | (1u << 15), kk > 0);
-        for (int kk = 0; kk < 8; kk++)
-            mma_bf16(tm + 128, desc_mn(sv, 128, kk), desc_mn(su, 128, kk), idesc_bf16(128, 2 * M, true) | (1u << 15), kk > 0);
-        mma_commit(&bar);
-    }
-    const bool ok = mbar_wait(&bar, 0, kWaitCycles);
-    fence_after_sync();
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) {
-            atomicExch(status, kStatusTimeout);
-            mbar_wait(&bar, 0, kWaitCycles);
+
+    int last_ph[NS];
+#pragma unroll
+    for (int q = 0; q < NS; q++) last_ph[q] = -1;
+    if (warp == 4) {
+        // ---------------- producer (lane 0) ----------------
+        if (lane == 0) {
+            auto load = [&](int c) {
+                const int st = c % NS;
+                mbar_arrive_expect_tx(&full[st], (D / 64) * 8192 + 8192 + M * 4);
+#pragma unroll
+                for (int x = 0; x < D; x += 64) tma_load_3d(XT(st) + x * 128, &maps.x[tz], x, c * kChunk, bh, &full[st]);
+                tma_load_3d(UT(st), &maps.u, 0, c * kChunk, bh, &full[st]);
+                bulk_load(GS(st), G + ((size_t)bh * NC + c) * M, M * 4, &full[st]);
+                last_ph[st] = (c / NS) & 1;
+            };
+            for (int c = 0; c < min(NS, NC); c++) load(c);
+            for (int c = 0; c < NC; c++) {
+                const int st = c % NS;
+                if (!mbar_wait_ab(&full[st], (c / NS) & 1, kWaitCycles, abort)) break;
+                if (c >= 2 && !mbar_wait_ab(&tfree[c & 1], ((c - 2) >> 1) & 1, kWaitCycles, abort)) break;
+                fence_after_sync();
+                const uint32_t sx = smem_u32(XT(st)), su = smem_u32(UT(st));
+                for (int kk = 0; kk < 4; kk++)
+                    mma_bf16(tm + 64 * (c & 1), desc_mn(sx, 64, kk), desc_mn(su, 64, kk),
+                             idesc_bf16(128, M, true) | (1u << 15), kk > 0);
+                mma_commit(&sfull[c & 1]);
+                if (c >= 1 && c - 1 + NS < NC) {  // chunk c - 1 fully consumed: refill its stage
+                    if (!mbar_wait_ab(&empty[(c - 1) % NS], ((c - 1) / NS) & 1, kWaitCycles, abort)) break;
+                    load(c - 1 + NS);
+                }
+            }
         }
     } else {
-        // TMEM row = d; thread half h holds chunk h's M slots
-        const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
-        const int d = r;
-        const bool keep = d < D && (h == 0 || has2);
-        float* dk = SK + ((size_t)bh * sh.NC + c1 + h) * M * D + d;
-        float* dv = SV + ((size_t)bh * sh.NC + c1 + h) * M * D + d;
-        for (int c0 = 0; c0 < M; c0 += (M < 32 ? M : 32)) {
-            float vk[32], vv[32];
-            tmem_ld(tl + h * M + c0, vk, M < 32 ? M : 32);
-            tmem_ld(tl + 128 + h * M + c0, vv, M < 32 ? M : 32);
-            if (keep)
-                for (int i = 0; i < (M < 32 ? M : 32); i++) {
-                    dk[(size_t)(c0 + i) * D] = vk[i];
-                    dv[(size_t)(c0 + i) * D] = vv[i];
-                }
+        // ---------------- state warps: thread = column d ----------------
+        const int d = tid;
+        const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);
+        __nv_bfloat16* Sb = (tz == 0 ? SKb : SVb) + (size_t)bh * NC * M * D + d;
+        float* Sf = (tz == 0 ? SK : SV) + (size_t)bh * NC * M * D + d;
+        float S[M];
+#pragma unroll
+        for (int i = 0; i < M; i++) S[i] = 0.0f;
+        for (int c = 0; c < NC; c++) {
+            const int st = c % NS, b = c & 1;
+            if (!mbar_wait_ab(&sfull[b], (c >> 1) & 1, kWaitCycles, abort) ||
+                !mbar_wait_ab(&full[st], (c / NS) & 1, kWaitCycles, abort))
+                break;
+            fence_after_sync();
+            float dS[M];
+            tmem_ld(tl + 64 * b, dS, M);
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tfree[b]);
+            if (d < D) {
+                const size_t o = (size_t)c * M * D;
+#pragma unroll
+                for (int i = 0; i < M; i++) Sb[o + (size_t)i * D] = __float2bfloat16_rn(S[i]);
+                if (want_f32)
+#pragma unroll
+                    for (int i = 0; i < M; i++) Sf[o + (size_t)i * D] = S[i];
+            }
+            const float* g = GS(st);
+#pragma unroll
+            for (int i = 0; i < M; i++) S[i] = fexp(g[i]) * S[i] + dS[i];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
         }
     }
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, 256);
+    if (s_abort) {  // let the copies and MMAs in flight land before the TMEM and the CTA go
+        if (warp == 4 && lane == 0) {
+            mma_commit(&drain);
+            mbar_wait(&drain, 0, kWaitCycles);
+            for (int q = 0; q < NS; q++)
+                if (last_ph[q] >= 0) mbar_wait(&full[q], (uint32_t)last_ph[q], kWaitCycles);
+        }
+        __syncthreads();
+        if (tid == 0) atomicExch(status, kStatusTimeout);
+    }
+    if (warp == 0) tmem_dealloc(tm, 128);
 }
 
 // Exclusive scan over chunks, in place (forward dir > 0 or reverse dir < 0),
@@ -181,23 +242,31 @@ cudaError_t launch_scan8(float* X0, float* X1, __nv_bfloat16* B0, __nv_bfloat16*
 
 template <int D, int M>
 cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const float* la, float* SK, float* SV,
-                      __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, const Shape& sh, int* status,
-                      cudaStream_t st) {
+                      __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, __nv_bfloat16* U, bool want_f32,
+                      const Shape& sh, int* status, cudaStream_t st) {
     if (sh.NC == 0) return cudaSuccess;
-    const size_t sm = 1024 + 3 * 32768 + 6 * M * sizeof(float);
-    auto kern = state_tc_kernel<D, M>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    NHA_LAUNCH("state_gates", st,
+               state_gates_kernel<M><<<dim3((sh.NC * kChunk + 127) / 128, sh.BH), kTcThreads, 0, st>>>(la, U, G, sh));
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    NHA_LAUNCH("state_chunk", st,
-               kern<<<dim3((sh.R + 127) / 128, sh.BH), kTcThreads, sm, st>>>(k, v, la, SK, SV, G, sh, status));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    return launch_scan8(SK, SV, SKb, SVb, G, sh, M, D, +1, st);
+    StateMaps maps;
+    if ((e = tmap_rows_bf16(&maps.x[0], k, D, sh.T, sh.BH, 64)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.x[1], v, D, sh.T, sh.BH, 64)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.u, U, 64, sh.NC * kChunk, sh.BH, 64)) != cudaSuccess)
+        return e;
+    const size_t sm = 1024 + kScanStages * (16384 + 8192 + 256);
+    auto kern = state_scan_tc_kernel<D, M>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) != cudaSuccess)
+        return e;
+    NHA_LAUNCH("state_scan", st,
+               kern<<<dim3(sh.BH, 2), kScanThreads, sm, st>>>(maps, G, SK, SV, SKb, SVb, sh, want_f32 ? 1 : 0, status));
+    return cudaGetLastError();
 }
 
 #define NHA_ST_INST(D, M)                                                                              \
     template cudaError_t tc_states<D, M>(const __nv_bfloat16*, const __nv_bfloat16*, const float*, float*, \
-                                         float*, __nv_bfloat16*, __nv_bfloat16*, float*, const Shape&, int*,  \
-                                         cudaStream_t);
+                                         float*, __nv_bfloat16*, __nv_bfloat16*, float*, __nv_bfloat16*, bool, \
+                                         const Shape&, int*, cudaStream_t);
 NHA_ST_INST(64, 16)
 NHA_ST_INST(64, 32)
 NHA_ST_INST(64, 64)
