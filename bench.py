@@ -76,6 +76,9 @@ def work_model(wl):
         # fused chunk scan (K, V, U in; the bf16 states entering each chunk out)
         "state_gates": (0, BH * R * (4 * m + 128)),
         "state_scan": (BH * 4 * m * d * R, BH * R * (2 * d * e + 128) + BH * ((R + 63) // 64) * 4 * m * d),
+        # reverse adjoint scan + carry: fp32 contributions and fp32 states in,
+        # bf16 adjoints out, K and V
+        "adj_scan": (0, BH * ((R + 63) // 64) * m * d * 20),
         "bwd_wdq_tc": wdq, "bwd_window_dq": wdq,
         "bwd_wkv_tc": wkv, "bwd_window_dkdv": wkv,
         "bwd_sq_tc": sq, "bwd_slot_query": sq,

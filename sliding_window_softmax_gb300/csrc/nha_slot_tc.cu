@@ -529,12 +529,23 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         }
         chunk_suffix<M>(db, s_tot, warp, lane, h);
         if (row_ok) {
+            // + the carry of the row's chunk: the gate gradient of all later chunks
+            const size_t co = ((size_t)bh * sh.NC + c1 + cr) * M + h * HM;
+            const size_t cv = (size_t)sh.BH * sh.NC * M;
             float* dla = a.dla + (hoff + s) * M + h * HM;
 #pragma unroll
             for (int jj = 0; jj < HM; jj += 4) {
                 float o4[4];
+                if (slot_ok) {
+                    const float4 ck = *reinterpret_cast<const float4*>(a.carry + co + jj);
+                    const float4 cw = *reinterpret_cast<const float4*>(a.carry + cv + co + jj);
+                    const float cs[4] = {ck.x + cw.x, ck.y + cw.y, ck.z + cw.z, ck.w + cw.w};
 #pragma unroll
-                for (int q = 0; q < 4; q++) o4[q] = slot_ok ? db[jj + q] - fexp(l[jj + q]) * du[jj + q] : 0.0f;
+                    for (int q = 0; q < 4; q++) o4[q] = db[jj + q] - fexp(l[jj + q]) * du[jj + q] + cs[q];
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) o4[q] = 0.0f;
+                }
                 *reinterpret_cast<float4*>(dla + jj) = make_float4(o4[0], o4[1], o4[2], o4[3]);
             }
         }
@@ -574,9 +585,7 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if ((e = launch_wkv<D>(a, qr, kr, tab, status, st)) != cudaSuccess) return e;
-    if (sh.NC > 0) {
-        if ((e = launch_scan8(a.RK, a.RV, a.RKb, a.RVb, a.G, sh, M, D, -1, st)) != cudaSuccess) return e;
-    }
+    if ((e = launch_adj_scan(a, M, D, st)) != cudaSuccess) return e;
     {
         auto kern = bwd_sk_tc_kernel<D, M>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk_smem<D, M>())) != cudaSuccess)
@@ -584,9 +593,6 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
         NHA_LAUNCH("bwd_sk_tc", st,
                    kern<<<dim3((sh.T + 127) / 128, sh.BH), kTcThreads, sk_smem<D, M>(), st>>>(a, status));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    if (sh.NC > 1) {
-        if ((e = launch_dla_carry(a, M, D, st)) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
