@@ -620,8 +620,8 @@ cudaError_t tc_backward(const BwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_b
     cudaError_t e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV,
                                     a.SKb, a.SVb, a.G, a.U, true, sh, status, st);
     if (e != cudaSuccess) return e;
-    if ((e = launch_rope_table(tab, sh.T, D / 2, a.rope, st)) != cudaSuccess) return e;
-    if (sh.w > 0 && (e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, sh, st)) != cudaSuccess) return e;
+    // RoPE(q), RoPE(k) and the (cos, sin) table of the window kernels' epilogues
+    if (sh.w > 0 && (e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, a.rope, sh, st)) != cudaSuccess) return e;
     const dim3 grid((sh.T + 127) / 128, sh.BH);
     {
         WdqMaps maps;

@@ -34,14 +34,6 @@ struct FwdMaps {
     CUtensorMap q, k, v;
 };
 
-__global__ void rope_table_kernel(float2* __restrict__ tab, int T, int H2, RopeTab rt) {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= T * H2) return;
-    float c, s;
-    rope_cs(rt, e / H2, e % H2, c, s);
-    tab[e] = make_float2(c, s);
-}
-
 template <int D, int M>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __restrict__ status) {
@@ -413,49 +405,79 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
 }
 
 // RoPE applied once per call: qr = RoPE(q), kr = RoPE(k) at absolute positions.
+// RoPE(q), RoPE(k) in bf16.  Thread = (position t, 8 frequency pairs, 4
+// heads): the (cos, sin) pairs are formed once, with the exact reduction of
+// rope_cs, and serve the four heads; with tab != nullptr the threads of the
+// first head group also write them to the (cos, sin) table [T][D/2].
 template <int D>
 __global__ void __launch_bounds__(256)
 rope_qk_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-               __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr, const float2* __restrict__ tab,
-               long rows, int T) {
+               __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr, float2* __restrict__ tab,
+               const RopeTab rt, int BH, int T) {
     constexpr int H = D / 2, CHH = D / 16;
     const long e = (long)blockIdx.x * 256 + threadIdx.x;
-    if (e >= rows * CHH) return;
-    const long row = e / CHH;
-    const int ch = (int)(e % CHH), pos = (int)(row % T);
-    const float2* cs = tab + (size_t)pos * H + ch * 8;
+    const int HG = (BH + 3) / 4;
+    if (e >= (long)T * CHH * HG) return;
+    const int ch = (int)(e % CHH);
+    const long rest = e / CHH;
+    const int t = (int)(rest % T), hg = (int)(rest / T);
+    float4 c[4];
 #pragma unroll
-    for (int which = 0; which < 2; which++) {
-        const __nv_bfloat16* src = (which == 0 ? q : k) + row * D;
-        __nv_bfloat16* dst = (which == 0 ? qr : kr) + row * D;
-        float x[8], y[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(src + ch * 8)), x);
-        unpack8(__ldg(reinterpret_cast<const uint4*>(src + H + ch * 8)), y);
-        rotate8(x, y, cs);
-        *reinterpret_cast<uint4*>(dst + ch * 8) = pack8(x);
-        *reinterpret_cast<uint4*>(dst + H + ch * 8) = pack8(y);
+    for (int p = 0; p < 4; p++) {
+        float c0, s0, c1, s1;
+        rope_cs(rt, t, ch * 8 + 2 * p, c0, s0);
+        rope_cs(rt, t, ch * 8 + 2 * p + 1, c1, s1);
+        c[p] = make_float4(c0, s0, c1, s1);
+    }
+    if (tab != nullptr && hg == 0) {
+        float4* tp = reinterpret_cast<float4*>(tab + (size_t)t * H + ch * 8);
+#pragma unroll
+        for (int p = 0; p < 4; p++) tp[p] = c[p];
+    }
+    uint4 in[4][2][2];  // [head][q / k][half]: every load issued before any store
+#pragma unroll
+    for (int hh = 0; hh < 4; hh++) {
+        const int bh = hg * 4 + hh;
+        const size_t row = (size_t)(bh < BH ? bh : 0) * T + t;
+#pragma unroll
+        for (int which = 0; which < 2; which++) {
+            const __nv_bfloat16* src = (which == 0 ? q : k) + row * D + ch * 8;
+            in[hh][which][0] = __ldg(reinterpret_cast<const uint4*>(src));
+            in[hh][which][1] = __ldg(reinterpret_cast<const uint4*>(src + H));
+        }
+    }
+#pragma unroll
+    for (int hh = 0; hh < 4; hh++) {
+        const int bh = hg * 4 + hh;
+        if (bh >= BH) break;
+        const size_t row = (size_t)bh * T + t;
+#pragma unroll
+        for (int which = 0; which < 2; which++) {
+            float x[8], y[8];
+            unpack8(in[hh][which][0], x);
+            unpack8(in[hh][which][1], y);
+            rotate8v(x, y, c);
+            __nv_bfloat16* dst = (which == 0 ? qr : kr) + row * D + ch * 8;
+            *reinterpret_cast<uint4*>(dst) = pack8(x);
+            *reinterpret_cast<uint4*>(dst + H) = pack8(y);
+        }
     }
 }
 
 template <int D>
-cudaError_t launch_rope_qk(const void* q, const void* k, __nv_bfloat16* qr, __nv_bfloat16* kr, const float2* tab,
-                           const Shape& sh, cudaStream_t st) {
-    const long rows = (long)sh.BH * sh.T, n = rows * (D / 16);
+cudaError_t launch_rope_qk(const void* q, const void* k, __nv_bfloat16* qr, __nv_bfloat16* kr, float2* tab,
+                           const RopeTab& rt, const Shape& sh, cudaStream_t st) {
+    const long n = (long)sh.T * (D / 16) * ((sh.BH + 3) / 4);
+    if (n == 0) return cudaSuccess;
     NHA_LAUNCH("rope_qk", st,
                rope_qk_kernel<D><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
-                   (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, qr, kr, tab, rows, sh.T));
+                   (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, qr, kr, tab, rt, sh.BH, sh.T));
     return cudaGetLastError();
 }
-template cudaError_t launch_rope_qk<64>(const void*, const void*, __nv_bfloat16*, __nv_bfloat16*, const float2*,
-                                        const Shape&, cudaStream_t);
-template cudaError_t launch_rope_qk<128>(const void*, const void*, __nv_bfloat16*, __nv_bfloat16*, const float2*,
-                                         const Shape&, cudaStream_t);
-
-cudaError_t launch_rope_table(float2* tab, int T, int H2, const RopeTab& rt, cudaStream_t st) {
-    const int n = T * H2;
-    NHA_LAUNCH("rope_table", st, rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(tab, T, H2, rt));
-    return cudaGetLastError();
-}
+template cudaError_t launch_rope_qk<64>(const void*, const void*, __nv_bfloat16*, __nv_bfloat16*, float2*,
+                                        const RopeTab&, const Shape&, cudaStream_t);
+template cudaError_t launch_rope_qk<128>(const void*, const void*, __nv_bfloat16*, __nv_bfloat16*, float2*,
+                                         const RopeTab&, const Shape&, cudaStream_t);
 
 template <int D, int M>
 size_t tc_fwd_smem() {
@@ -469,9 +491,7 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bf
     cudaError_t e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV,
                                     a.SKb, a.SVb, a.G, a.U, false, sh, status, st);
     if (e != cudaSuccess) return e;
-    e = launch_rope_table(tab, sh.T, D / 2, a.rope, st);
-    if (e != cudaSuccess) return e;
-    if (sh.w > 0 && (e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, sh, st)) != cudaSuccess) return e;
+    if (sh.w > 0 && (e = launch_rope_qk<D>(a.q, a.k, qr, kr, nullptr, a.rope, sh, st)) != cudaSuccess) return e;
     const int W0 = sh.T - sh.R;
     const int tiles = (W0 + 127) / 128 + (sh.R + 127) / 128;
     if (tiles == 0) return cudaSuccess;

@@ -91,9 +91,10 @@ cudaError_t simt_forward(const FwdArgs& a, cudaStream_t st);
 template <int D, int M>
 cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bfloat16* kr, int* status,
                        cudaStream_t st);
+// RoPE(q), RoPE(k) into qr, kr; with tab != nullptr also the (cos, sin) table [T][D/2].
 template <int D>
-cudaError_t launch_rope_qk(const void* q, const void* k, __nv_bfloat16* qr, __nv_bfloat16* kr, const float2* tab,
-                           const Shape& sh, cudaStream_t st);
+cudaError_t launch_rope_qk(const void* q, const void* k, __nv_bfloat16* qr, __nv_bfloat16* kr, float2* tab,
+                           const RopeTab& rt, const Shape& sh, cudaStream_t st);
 template <typename Tin, int D, int M>
 cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st);
 // Slot-branch backward (query side, reverse adjoint scan, key side, dlog_alpha
@@ -127,7 +128,5 @@ cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const floa
 // fp32 in place plus a bf16 copy in B0 / B1.
 cudaError_t launch_scan8(float* X0, float* X1, __nv_bfloat16* B0, __nv_bfloat16* B1, const float* G,
                          const Shape& sh, int M, int D, int dir, cudaStream_t st);
-// RoPE (cos, sin) table [T][H2] of the absolute positions.
-cudaError_t launch_rope_table(float2* tab, int T, int H2, const RopeTab& rt, cudaStream_t st);
 
 }  // namespace nha
