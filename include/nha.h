@@ -37,9 +37,16 @@
  *
  * Ownership: the caller allocates every buffer, including the workspace
  * (size from nha_workspace_bytes).  The library never allocates or frees
- * device memory and never synchronises; all work is enqueued on `stream`
- * (a cudaStream_t; NULL means the legacy default stream).  Outputs are fully
- * overwritten, never accumulated.
+ * device memory and never synchronises; work is enqueued on `stream` (a
+ * cudaStream_t; NULL means the legacy default stream).  The bf16 path also
+ * runs independent kernels on an internal non-blocking stream, one per host
+ * thread and device with four events, created on the first bf16 call and
+ * kept until the process exits: that stream waits on `stream` before its
+ * kernels and `stream` waits on it after them (events), so all results are
+ * complete when the work enqueued on `stream` is, and stream capture records
+ * the fork and join as graph edges.  Make the first bf16 call of a host
+ * thread outside stream capture.  Outputs are fully overwritten, never
+ * accumulated.
  *
  * Errors: every entry point returns a status and never throws.  Arguments are
  * validated before anything is enqueued; a failed launch maps to
@@ -47,9 +54,9 @@
  * synchronisation.  nha_last_error() gives a thread-local message for the
  * last failing call on this thread.
  *
- * Re-entrancy: reentrant; the only process-wide state is lazily set kernel
- * attributes.  Calls on different streams with different workspaces may run
- * concurrently.
+ * Re-entrancy: reentrant; the process-wide state is lazily set kernel
+ * attributes and the per-thread side streams above.  Calls on different
+ * streams with different workspaces may run concurrently.
  */
 #ifndef NHA_H_
 #define NHA_H_

@@ -617,11 +617,19 @@ template <int D, int M>
 cudaError_t tc_backward(const BwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bfloat16* kr, int* status,
                         cudaStream_t st) {
     const Shape& sh = a.sh;
-    cudaError_t e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV,
-                                    a.SKb, a.SVb, a.G, a.U, true, sh, status, st);
+    Fork* f = nullptr;
+    cudaError_t e = get_fork(&f);
     if (e != cudaSuccess) return e;
-    // RoPE(q), RoPE(k) and the (cos, sin) table of the window kernels' epilogues
-    if (sh.w > 0 && (e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, a.rope, sh, st)) != cudaSuccess) return e;
+    // RoPE(q), RoPE(k) and the (cos, sin) table of the window kernels'
+    // epilogues on the side stream while the chunk states are formed
+    if (sh.w > 0) {
+        if ((e = fork_side(st, *f, 0)) != cudaSuccess) return e;
+        if ((e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, a.rope, sh, f->side)) != cudaSuccess) return e;
+    }
+    e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV, a.SKb, a.SVb, a.G,
+                        a.U, true, sh, status, st);
+    if (e != cudaSuccess) return e;
+    if (sh.w > 0 && (e = join_side(st, *f, 1)) != cudaSuccess) return e;
     const dim3 grid((sh.T + 127) / 128, sh.BH);
     {
         WdqMaps maps;

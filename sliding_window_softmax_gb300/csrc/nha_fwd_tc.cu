@@ -488,10 +488,18 @@ template <int D, int M>
 cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bfloat16* kr, int* status,
                        cudaStream_t st) {
     const Shape& sh = a.sh;
-    cudaError_t e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV,
-                                    a.SKb, a.SVb, a.G, a.U, false, sh, status, st);
+    Fork* f = nullptr;
+    cudaError_t e = get_fork(&f);
     if (e != cudaSuccess) return e;
-    if (sh.w > 0 && (e = launch_rope_qk<D>(a.q, a.k, qr, kr, nullptr, a.rope, sh, st)) != cudaSuccess) return e;
+    // RoPE(q), RoPE(k) on the side stream while the chunk states are formed
+    if (sh.w > 0) {
+        if ((e = fork_side(st, *f, 0)) != cudaSuccess) return e;
+        if ((e = launch_rope_qk<D>(a.q, a.k, qr, kr, nullptr, a.rope, sh, f->side)) != cudaSuccess) return e;
+    }
+    e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV, a.SKb, a.SVb, a.G,
+                        a.U, false, sh, status, st);
+    if (e != cudaSuccess) return e;
+    if (sh.w > 0 && (e = join_side(st, *f, 1)) != cudaSuccess) return e;
     const int W0 = sh.T - sh.R;
     const int tiles = (W0 + 127) / 128 + (sh.R + 127) / 128;
     if (tiles == 0) return cudaSuccess;

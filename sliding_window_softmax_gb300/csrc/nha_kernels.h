@@ -13,6 +13,19 @@ namespace nha {
 // Records the thread-local message returned by nha_last_error and returns s.
 nha_status_t set_error(nha_status_t s, const char* fmt, ...);
 
+// Side stream of this host thread on the current device, for work that runs
+// beside the caller's stream: fork_side makes the side stream wait for what
+// `main` has enqueued so far, join_side makes `main` wait for what the side
+// stream has; event k is used once per call (k < kEvents).
+struct Fork {
+    static constexpr int kEvents = 4;
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev[kEvents] = {};
+};
+cudaError_t get_fork(Fork** out);
+cudaError_t fork_side(cudaStream_t main, Fork& f, int k);
+cudaError_t join_side(cudaStream_t main, Fork& f, int k);
+
 // Forward arguments.  q, k, v, o are [BH, T, D] in the element type; la is
 // [BH, T, M]; lse [BH, T].  Workspace: SK, SV [BH, NC, M, D] and G [BH, NC, M].
 struct FwdArgs {

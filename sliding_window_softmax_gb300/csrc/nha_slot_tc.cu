@@ -584,8 +584,13 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
             NHA_LAUNCH("bwd_sq_tc", st, kern<<<dim3(qtiles, sh.BH), kTcThreads, sq_smem<D, M>(), st>>>(a, status));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    // the bandwidth-bound adjoint scan shares the SMs with the key-major kernel
+    Fork* f = nullptr;
+    if ((e = get_fork(&f)) != cudaSuccess) return e;
+    if ((e = fork_side(st, *f, 2)) != cudaSuccess) return e;
+    if ((e = launch_adj_scan(a, M, D, f->side)) != cudaSuccess) return e;
     if ((e = launch_wkv<D>(a, qr, kr, tab, status, st)) != cudaSuccess) return e;
-    if ((e = launch_adj_scan(a, M, D, st)) != cudaSuccess) return e;
+    if ((e = join_side(st, *f, 3)) != cudaSuccess) return e;
     {
         auto kern = bwd_sk_tc_kernel<D, M>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk_smem<D, M>())) != cudaSuccess)

@@ -191,6 +191,8 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
     if (warp == 0) tmem_dealloc(tm, 128);
 }
 
+constexpr int kAdjSlots = 8;
+
 // Reverse chunk scan of the slot adjoints, fused with the dlog_alpha carry.
 // R_c, the adjoint carried into chunk c from the later chunks, follows
 // R_{c - 1} = exp(G_c) R_c + dR_c (dR_c: the chunk's own contribution, from the
@@ -198,82 +200,86 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
 // of chunk c, carry_c[i] = sum_d R_c[i][d] S_prev(c + 1)[i][d], is the total
 // over all later rows of the gate gradient that every row of chunk c receives
 // (zero for the last chunk); K and V write their parts separately.  One CTA per
-// (head, 16 slots, K or V), thread = column d, two chunks of loads in flight.
+// (head, 8 slots, K or V), thread = column d, two chunks of loads in flight
+// (8 slots keep it small enough to share the SMs with the key-major kernel).
 template <int D>
 __global__ void __launch_bounds__(D)
 adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, const float* __restrict__ SK,
                 const float* __restrict__ SV, const float* __restrict__ G, __nv_bfloat16* __restrict__ RKb,
                 __nv_bfloat16* __restrict__ RVb, float* __restrict__ carry, Shape sh, int M) {
-    constexpr int NW = D / 32;
-    __shared__ float red[2][NW][16];
+    constexpr int NW = D / 32, SG = kAdjSlots;
+    __shared__ float red[2][NW][SG];
     const int d = threadIdx.x, warp = d >> 5, lane = d & 31;
-    const int bh = blockIdx.x, i0 = 16 * blockIdx.y, tz = blockIdx.z, NC = sh.NC;
+    const int bh = blockIdx.x, i0 = SG * blockIdx.y, tz = blockIdx.z, NC = sh.NC;
     const float* X = tz == 0 ? RK : RV;
     const float* S = tz == 0 ? SK : SV;
     __nv_bfloat16* Xb = tz == 0 ? RKb : RVb;
     float* car = carry + ((size_t)tz * sh.BH + bh) * NC * M + i0;
     auto at = [&](int c) { return (((size_t)bh * NC + c) * M + i0) * D + d; };
-    auto load = [&](int c, float (&x)[16], float (&sp)[16]) {
+    auto load = [&](int c, float (&x)[SG], float (&sp)[SG], float (&g)[SG]) {
         const size_t o = at(c);
+        const float* gc = G + ((size_t)bh * NC + c) * M + i0;
 #pragma unroll
-        for (int i = 0; i < 16; i++) x[i] = X[o + (size_t)i * D];
+        for (int i = 0; i < SG; i++) {
+            x[i] = X[o + (size_t)i * D];
+            g[i] = __ldg(gc + i);
+        }
         if (c + 1 < NC) {
             const size_t o1 = at(c + 1);
 #pragma unroll
-            for (int i = 0; i < 16; i++) sp[i] = S[o1 + (size_t)i * D];
+            for (int i = 0; i < SG; i++) sp[i] = S[o1 + (size_t)i * D];
         } else {
 #pragma unroll
-            for (int i = 0; i < 16; i++) sp[i] = 0.0f;
+            for (int i = 0; i < SG; i++) sp[i] = 0.0f;
         }
     };
-    float R[16];
+    float R[SG];
 #pragma unroll
-    for (int i = 0; i < 16; i++) R[i] = 0.0f;
+    for (int i = 0; i < SG; i++) R[i] = 0.0f;
     int parity = 0;
-    auto process = [&](int c, const float (&x)[16], const float (&sp)[16]) {
+    auto process = [&](int c, const float (&x)[SG], const float (&sp)[SG], const float (&g)[SG]) {
         const size_t o = at(c);
-        float part[16];
+        float part[SG];
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
+        for (int i = 0; i < SG; i++) {
             Xb[o + (size_t)i * D] = __float2bfloat16_rn(R[i]);
             part[i] = R[i] * sp[i];
         }
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
+        for (int i = 0; i < SG; i++) {
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
         }
         if (lane == 0)
 #pragma unroll
-            for (int i = 0; i < 16; i++) red[parity][warp][i] = part[i];
+            for (int i = 0; i < SG; i++) red[parity][warp][i] = part[i];
         __syncthreads();  // red[parity] complete; red[parity ^ 1] free again
-        if (d < 16) {
+        if (d < SG) {
             float t = 0.0f;
 #pragma unroll
             for (int q = 0; q < NW; q++) t += red[parity][q][d];
             car[(size_t)c * M + d] = t;
         }
         parity ^= 1;
-        const float* g = G + ((size_t)bh * NC + c) * M + i0;
 #pragma unroll
-        for (int i = 0; i < 16; i++) R[i] = fexp(__ldg(g + i)) * R[i] + x[i];
+        for (int i = 0; i < SG; i++) R[i] = fexp(g[i]) * R[i] + x[i];
     };
-    float xa[16], sa[16], xb[16], sb[16];
-    if (NC >= 1) load(NC - 1, xa, sa);
-    if (NC >= 2) load(NC - 2, xb, sb);
+    float xa[SG], sa[SG], ga[SG], xb[SG], sb[SG], gb[SG];
+    if (NC >= 1) load(NC - 1, xa, sa, ga);
+    if (NC >= 2) load(NC - 2, xb, sb, gb);
     for (int c = NC - 1; c >= 0; c -= 2) {
-        process(c, xa, sa);
-        if (c - 2 >= 0) load(c - 2, xa, sa);
+        process(c, xa, sa, ga);
+        if (c - 2 >= 0) load(c - 2, xa, sa, ga);
         if (c - 1 < 0) break;
-        process(c - 1, xb, sb);
-        if (c - 3 >= 0) load(c - 3, xb, sb);
+        process(c - 1, xb, sb, gb);
+        if (c - 3 >= 0) load(c - 3, xb, sb, gb);
     }
 }
 
 cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st) {
     const Shape& sh = a.sh;
     if (sh.NC == 0) return cudaSuccess;
-    const dim3 grid(sh.BH, M / 16, 2);
+    const dim3 grid(sh.BH, M / kAdjSlots, 2);
     if (D == 128)
         NHA_LAUNCH("adj_scan", st,
                    adj_scan_kernel<128><<<grid, 128, 0, st>>>(a.RK, a.RV, a.SK, a.SV, a.G, a.RKb, a.RVb, a.carry, sh, M));
