@@ -197,22 +197,23 @@ constexpr int kAdjSlots = 8;
 // R_c, the adjoint carried into chunk c from the later chunks, follows
 // R_{c - 1} = exp(G_c) R_c + dR_c (dR_c: the chunk's own contribution, from the
 // query-side kernel); it is written in bf16 for the key-side kernel.  The carry
-// of chunk c, carry_c[i] = sum_d R_c[i][d] S_prev(c + 1)[i][d], is the total
+// of chunk c, carry_c[i] = sum_d R_c[i][d] S_prev(c + 1)[i][d] (the bf16 states),
+// is the total
 // over all later rows of the gate gradient that every row of chunk c receives
 // (zero for the last chunk); K and V write their parts separately.  One CTA per
 // (head, 8 slots, K or V), thread = column d, two chunks of loads in flight
 // (8 slots keep it small enough to share the SMs with the key-major kernel).
 template <int D>
 __global__ void __launch_bounds__(D)
-adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, const float* __restrict__ SK,
-                const float* __restrict__ SV, const float* __restrict__ G, __nv_bfloat16* __restrict__ RKb,
+adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, const __nv_bfloat16* __restrict__ SK,
+                const __nv_bfloat16* __restrict__ SV, const float* __restrict__ G, __nv_bfloat16* __restrict__ RKb,
                 __nv_bfloat16* __restrict__ RVb, float* __restrict__ carry, Shape sh, int M) {
     constexpr int NW = D / 32, SG = kAdjSlots;
     __shared__ float red[2][NW][SG];
     const int d = threadIdx.x, warp = d >> 5, lane = d & 31;
     const int bh = blockIdx.x, i0 = SG * blockIdx.y, tz = blockIdx.z, NC = sh.NC;
     const float* X = tz == 0 ? RK : RV;
-    const float* S = tz == 0 ? SK : SV;
+    const __nv_bfloat16* S = tz == 0 ? SK : SV;
     __nv_bfloat16* Xb = tz == 0 ? RKb : RVb;
     float* car = carry + ((size_t)tz * sh.BH + bh) * NC * M + i0;
     auto at = [&](int c) { return (((size_t)bh * NC + c) * M + i0) * D + d; };
@@ -227,7 +228,7 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
         if (c + 1 < NC) {
             const size_t o1 = at(c + 1);
 #pragma unroll
-            for (int i = 0; i < SG; i++) sp[i] = S[o1 + (size_t)i * D];
+            for (int i = 0; i < SG; i++) sp[i] = __bfloat162float(S[o1 + (size_t)i * D]);
         } else {
 #pragma unroll
             for (int i = 0; i < SG; i++) sp[i] = 0.0f;
@@ -282,10 +283,10 @@ cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st) {
     const dim3 grid(sh.BH, M / kAdjSlots, 2);
     if (D == 128)
         NHA_LAUNCH("adj_scan", st,
-                   adj_scan_kernel<128><<<grid, 128, 0, st>>>(a.RK, a.RV, a.SK, a.SV, a.G, a.RKb, a.RVb, a.carry, sh, M));
+                   adj_scan_kernel<128><<<grid, 128, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.carry, sh, M));
     else
         NHA_LAUNCH("adj_scan", st,
-                   adj_scan_kernel<64><<<grid, 64, 0, st>>>(a.RK, a.RV, a.SK, a.SV, a.G, a.RKb, a.RVb, a.carry, sh, M));
+                   adj_scan_kernel<64><<<grid, 64, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.carry, sh, M));
     return cudaGetLastError();
 }
 
