@@ -25,6 +25,7 @@
 #include "nha_prof.h"
 #include "nha_tc.cuh"
 #include "nha_tc_tiles.cuh"
+#include "nha_tma.h"
 
 namespace nha {
 
@@ -336,9 +337,13 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
 }
 
 // ---------------------------------------------------------------------------------------
+struct SkMaps {
+    CUtensorMap q, dout, k, v, rk, rv, dkw, dvw;
+};
+
 template <int D, int M>
 __global__ void __launch_bounds__(kTcThreads, 1)
-bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
+bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __restrict__ status) {
     constexpr int HM = M / 2, HD = D / 2, TB = 128 * D * 2;
     constexpr int SSZ = ((2 * M * D * 2) + 1023) / 1024 * 1024;
     extern __shared__ unsigned char smem_raw[];
@@ -352,7 +357,7 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     unsigned char* XM2 = XM1 + 32768;
     float* s_tot = reinterpret_cast<float*>(XM2 + 32768);  // [4][M]
     float* sG = s_tot + 4 * M;                              // [2][M]
-    __shared__ uint64_t bar;
+    __shared__ uint64_t bar, lbar, ebar;  // MMAs; operand tiles of a pass; window partials
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -388,6 +393,8 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     if (tid < 2 * M) sG[tid] = 0.0f;
     if (tid == 0) {
         mbar_init(&bar, 1);
+        mbar_init(&lbar, 1);
+        mbar_init(&ebar, 1);
         mbar_fence_init();
         s_abort = 0;
     }
@@ -401,14 +408,29 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     TcCtl ctl{&bar, 0u, &s_abort, status};
     bool ok = true;
 
+    // TMA (thread 0): q_t / dout_t rows, k / v rows and the [Rc pair] of a
+    // pass.  Rows past the tile's states hold other tokens or zeros; every
+    // product they enter is multiplied by a zero gate or masked away.
+    int l_issued = 0, l_waited = 0, e_issued = 0, e_waited = 0;  // thread 0's copy bookkeeping
     auto issue_loads = [&](int pass) {
-        const __nv_bfloat16* X = (const __nv_bfloat16*)(pass == 0 ? a.q : a.dout) + hoff * D;
-        const __nv_bfloat16* Y = (const __nv_bfloat16*)(pass == 0 ? a.k : a.v) + hoff * D;
-        const __nv_bfloat16* Rc = (pass == 0 ? a.RKb : a.RVb) + ((size_t)bh * sh.NC + c1) * M * D;
-        load_tile_async<D>(X, sbase + sh.w, nc, XA);
-        load_tile_async<D>(Y, sbase, nc, XB);
-        load_state_pair_async<D, M>(Rc, has2 ? Rc + M * D : nullptr, XR);
-        cp_async_commit();
+        if (tid != 0) return;
+        l_issued++;
+        mbar_arrive_expect_tx(&lbar, 2 * TB + 2 * M * D * 2);
+#pragma unroll
+        for (int xx = 0; xx < D; xx += 64) {
+            tma_load_3d(XA + xx * 256, pass == 0 ? &maps.q : &maps.dout, xx, sbase + sh.w, bh, &lbar);
+            tma_load_3d(XB + xx * 256, pass == 0 ? &maps.k : &maps.v, xx, sbase, bh, &lbar);
+            tma_load_3d(XR + xx * 4 * M, pass == 0 ? &maps.rk : &maps.rv, xx, c1 * M, bh, &lbar);
+        }
+    };
+    // window partial dk or dv of the tile's rows into XM1 (its masks are consumed)
+    auto issue_partial = [&](int pass) {
+        if (tid != 0) return;
+        e_issued++;
+        mbar_arrive_expect_tx(&ebar, TB);
+#pragma unroll
+        for (int xx = 0; xx < D; xx += 64)
+            tma_load_3d(XM1 + xx * 256, pass == 0 ? &maps.dkw : &maps.dvw, xx, sbase, bh, &ebar);
     };
     issue_loads(0);  // in flight while the gates are computed
     float l[HM], b[HM];
@@ -438,7 +460,6 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
 
     for (int pass = 0; pass < 2 && ok; pass++) {
         const __nv_bfloat16* W = (pass == 0 ? a.hDL : a.hPL) + jrow * M + h * HM;
-        if (pass > 0) issue_loads(pass);  // the previous pass's MMAs are complete
         {
             float weq[HM];
 #pragma unroll
@@ -455,9 +476,14 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
             }
             store_row(XW, r, h * HM, weq, HM);
         }
-        cp_async_wait<0>();
         sync_for_mma();
         if (tid == 0) {
+            // this pass's tiles landed
+            if (mbar_wait(&lbar, (uint32_t)pass, kWaitCycles))
+                l_waited++;
+            else
+                atomicExch(&s_abort, 1);
+            fence_after_sync();
             const uint32_t se = smem_u32(XE), sw = smem_u32(XW), sa = smem_u32(XA), sb = smem_u32(XB),
                            sr = smem_u32(XR);
             for (int kk = 0; kk < M / 16; kk++)
@@ -485,36 +511,52 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
                 mma_bf16(tm + R0, desc_k(s2, 128, kk), desc_mn(sw, 128, kk), idesc_bf16(128, M, true), kk > 0);
             mma_commit(&bar);
         }
-        if (!(ok = ctl.wait())) break;
+        if (!(ok = ctl.wait()) || s_abort) {
+            ok = false;
+            break;
+        }
+        issue_partial(pass);
+        if (pass == 0) issue_loads(1);  // the operand tiles are free: next pass in flight
         {
             float intra[HM];
             tmem_ld(tl + R0 + h * HM, intra, HM);
 #pragma unroll
             for (int jj = 0; jj < HM; jj++) du[jj] += fexp(rho[jj] - b[jj]) * (intra[jj] + eG[jj] * inter[jj]);
         }
-        const __nv_bfloat16* gw = (pass == 0 ? a.hdkw : a.hdvw) + (hoff + s) * D + h * HD;
-        __nv_bfloat16* go = (__nv_bfloat16*)(pass == 0 ? a.dk : a.dv) + (hoff + s) * D + h * HD;
-        uint4 pw[HD / 8];  // all global loads first
-#pragma unroll
-        for (int e = 0; e < HD / 8; e++)
-            pw[e] = row_ok ? *reinterpret_cast<const uint4*>(gw + 8 * e) : make_uint4(0, 0, 0, 0);
+        // dk (dv) = window partial + slot part, staged in XM2, written by TMA
+        if (mbar_wait(&ebar, (uint32_t)pass, kWaitCycles)) {
+            if (tid == 0) e_waited++;
+        } else {
+            atomicExch(&s_abort, 1);
+        }
 #pragma unroll
         for (int c0 = 0; c0 < HD; c0 += 32) {
             float g[32];
             tmem_ld32(tl + R3 + h * HD + c0, g);
-            if (row_ok) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 8) {
-                    float f[8];
-                    unpack8(pw[(c0 + e) / 8], f);
+            for (int e = 0; e < 32; e += 8) {
+                const uint32_t off = sw_chunk(r, (h * HD + c0 + e) >> 3, 128);
+                float f[8];
+                unpack8(*reinterpret_cast<const uint4*>(XM1 + off), f);
 #pragma unroll
-                    for (int q = 0; q < 8; q++) f[q] += g[e + q];
-                    *reinterpret_cast<uint4*>(go + c0 + e) = pack8(f);
-                }
+                for (int q = 0; q < 8; q++) f[q] += g[e + q];
+                *reinterpret_cast<uint4*>(XM2 + off) = pack8(f);
             }
         }
         fence_before_sync();
-        __syncthreads();
+        if (__syncthreads_or(s_abort)) {
+            ok = false;
+            break;
+        }
+        {  // rows [0, nk) of the staged tile, 16-byte chunks, coalesced
+            constexpr int CH = D / 8;
+            __nv_bfloat16* ob = (__nv_bfloat16*)(pass == 0 ? a.dk : a.dv) + (hoff + sbase) * D;
+            for (int e = tid; e < nk * CH; e += kTcThreads) {
+                const int rr = e / CH, ch = e % CH;
+                *reinterpret_cast<uint4*>(ob + (size_t)rr * D + ch * 8) =
+                    *reinterpret_cast<const uint4*>(XM2 + sw_chunk(rr, ch, 128));
+            }
+        }
     }
     if (ok) {
         // db = db1 - u du;  dlog_alpha = (suffix sum of db in the chunk) - alpha du
@@ -552,7 +594,12 @@ bwd_sk_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     } else if (row_ok && h == 0) {
         a.dla[(hoff + s) * M] = __int_as_float(0x7fc00000);
     }
-    if (!ok && tid == 0) mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);
+    if (!ok && tid == 0) {  // let in-flight MMAs and copies drain
+        mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);
+        for (int q = l_waited; q < l_issued; q++) mbar_wait(&lbar, (uint32_t)(q & 1), kWaitCycles);
+        for (int q = e_waited; q < e_issued; q++) mbar_wait(&ebar, (uint32_t)(q & 1), kWaitCycles);
+        atomicExch(status, kStatusTimeout);
+    }
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 512);
@@ -592,11 +639,22 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
     if ((e = launch_wkv<D>(a, qr, kr, tab, status, st)) != cudaSuccess) return e;
     if ((e = join_side(st, *f, 3)) != cudaSuccess) return e;
     {
+        SkMaps maps;
+        const int ncm = (sh.NC > 0 ? sh.NC : 1) * M;
+        if ((e = tmap_rows_bf16(&maps.q, a.q, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.dout, a.dout, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.k, a.k, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.v, a.v, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.rk, a.RKb, D, ncm, sh.BH, 2 * M)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.rv, a.RVb, D, ncm, sh.BH, 2 * M)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.dkw, a.hdkw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.dvw, a.hdvw, D, sh.T, sh.BH, 128)) != cudaSuccess)
+            return e;
         auto kern = bwd_sk_tc_kernel<D, M>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk_smem<D, M>())) != cudaSuccess)
             return e;
         NHA_LAUNCH("bwd_sk_tc", st,
-                   kern<<<dim3((sh.T + 127) / 128, sh.BH), kTcThreads, sk_smem<D, M>(), st>>>(a, status));
+                   kern<<<dim3((sh.T + 127) / 128, sh.BH), kTcThreads, sk_smem<D, M>(), st>>>(a, maps, status));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
