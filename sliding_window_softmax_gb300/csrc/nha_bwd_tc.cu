@@ -89,7 +89,7 @@ __device__ __forceinline__ void store_unrotated(uint32_t taddr, bool valid_acc, 
 constexpr int kWdqThreads = 288;
 
 struct WdqMaps {
-    CUtensorMap q, dout, o, k, v, dq, dqv, tab;
+    CUtensorMap q, dout, o, k, v, tab;
 };
 
 template <int D>
@@ -315,14 +315,16 @@ bwd_wdq_tc_kernel(const BwdArgs a, const __grid_constant__ WdqMaps maps, int* __
             fence_async_smem();
         }
         const int bad = named_sync_or(1, 256, !ok);
-        if (!bad && tid == 0) {
-#pragma unroll
-            for (int x = 0; x < D; x += 64) {
-                tma_store_3d(&maps.dq, x, tbase, bh, stQ + x * 256);
-                tma_store_3d(&maps.dqv, x, tbase, bh, stV + x * 256);
+        if (!bad) {  // rows [0, nq) of both staged tiles, 16-byte chunks, coalesced
+            constexpr int CHR = D / 8;
+            __nv_bfloat16* o1 = a.hdqw + (hoff + tbase) * D;
+            __nv_bfloat16* o2 = a.hdqwV + (hoff + tbase) * D;
+            for (int e = tid; e < nq * CHR; e += 256) {
+                const int rr = e / CHR, ch = e % CHR;
+                const uint32_t off = sw_chunk(rr, ch, 128);
+                *reinterpret_cast<uint4*>(o1 + (size_t)rr * D + ch * 8) = *reinterpret_cast<const uint4*>(stQ + off);
+                *reinterpret_cast<uint4*>(o2 + (size_t)rr * D + ch * 8) = *reinterpret_cast<const uint4*>(stV + off);
             }
-            bulk_commit();
-            bulk_wait_read();
         }
         if (bad && row_ok) a.hdqw[(hoff + t) * D + h] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
     }
@@ -357,7 +359,7 @@ bwd_wdq_tc_kernel(const BwdArgs a, const __grid_constant__ WdqMaps maps, int* __
 constexpr int kWkvThreads = 288, kWkvStages = 3;
 
 struct WkvMaps {
-    CUtensorMap q, dout, k, v, dk, dv, tab;
+    CUtensorMap q, dout, k, v, tab;
 };
 
 template <int D>
@@ -575,14 +577,18 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, int* __
         }
         // all 256 softmax threads agree before one of them issues the stores
         const int bad = named_sync_or(1, 256, !ok);
-        if (!bad && tid == 0) {
-#pragma unroll
-            for (int x = 0; x < D; x += 64) {
-                tma_store_3d(&maps.dv, x, sbase, bh, QB0 + x * 256);
-                tma_store_3d(&maps.dk, x, sbase, bh, QB0 + TB + x * 256);
+        if (!bad) {  // rows [0, nk) of both staged tiles, 16-byte chunks, coalesced
+            constexpr int CHR = D / 8;
+            const int nk = min(128, sh.T - sbase);
+            __nv_bfloat16* o1 = a.hdvw + (hoff + sbase) * D;
+            __nv_bfloat16* o2 = a.hdkw + (hoff + sbase) * D;
+            for (int e = tid; e < nk * CHR; e += 256) {
+                const int rr = e / CHR, ch = e % CHR;
+                const uint32_t off = sw_chunk(rr, ch, 128);
+                *reinterpret_cast<uint4*>(o1 + (size_t)rr * D + ch * 8) = *reinterpret_cast<const uint4*>(QB0 + off);
+                *reinterpret_cast<uint4*>(o2 + (size_t)rr * D + ch * 8) =
+                    *reinterpret_cast<const uint4*>(QB0 + TB + off);
             }
-            bulk_commit();
-            bulk_wait_read();
         }
         if (bad && row_ok) a.hdkw[(hoff + key) * D + h] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
     }
@@ -638,8 +644,6 @@ cudaError_t tc_backward(const BwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_b
             (e = tmap_rows_bf16(&maps.o, a.o, D, sh.T, sh.BH, 128)) != cudaSuccess ||
             (e = tmap_rows_bf16(&maps.k, kr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
             (e = tmap_rows_bf16(&maps.v, a.v, D, sh.T, sh.BH, 128)) != cudaSuccess ||
-            (e = tmap_rows_bf16(&maps.dq, a.hdqw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
-            (e = tmap_rows_bf16(&maps.dqv, a.hdqwV, D, sh.T, sh.BH, 128)) != cudaSuccess ||
             (e = tmap_tab(&maps.tab, tab, D / 2, sh.T)) != cudaSuccess)
             return e;
         auto kern = bwd_wdq_tc_kernel<D>;
@@ -661,8 +665,6 @@ cudaError_t launch_wkv(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bfl
         (e = tmap_rows_bf16(&maps.dout, a.dout, D, sh.T, sh.BH, 64)) != cudaSuccess ||
         (e = tmap_rows_bf16(&maps.k, kr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
         (e = tmap_rows_bf16(&maps.v, a.v, D, sh.T, sh.BH, 128)) != cudaSuccess ||
-        (e = tmap_rows_bf16(&maps.dk, a.hdkw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
-        (e = tmap_rows_bf16(&maps.dv, a.hdvw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
         (e = tmap_tab(&maps.tab, tab, D / 2, sh.T)) != cudaSuccess)
         return e;
     const dim3 grid((sh.T + 127) / 128, sh.BH);
