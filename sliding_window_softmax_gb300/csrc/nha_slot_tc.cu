@@ -34,9 +34,13 @@ __host__ __device__ constexpr uint32_t idesc_am(int M, int N, bool a_mn, bool b_
 }
 
 // ---------------------------------------------------------------------------------------
+struct SqMaps {
+    CUtensorMap q, dout, k, v, sk, sv, dqw, dqwv;
+};
+
 template <int D, int M>
 __global__ void __launch_bounds__(kTcThreads, 1)
-bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
+bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __restrict__ status) {
     constexpr int HM = M / 2, HD = D / 2, TB = 128 * D * 2;
     constexpr int SSZ = ((2 * M * D * 2) + 1023) / 1024 * 1024;
     extern __shared__ unsigned char smem_raw[];
@@ -50,7 +54,7 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     float* s_tot = reinterpret_cast<float*>(XG + 32768);  // [4][M]
     float* sG = s_tot + 4 * M;                             // [2][M]
     float* red = sG + 2 * M;                               // [2][128]
-    __shared__ uint64_t bar;
+    __shared__ uint64_t bar, lbar, ebar[2];  // MMAs; operand tiles; the two window partials (one copy each)
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -81,15 +85,14 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     const bool has2 = nq > kChunk, row_ok = r < nq;
     const int t = tbase + r, j = j0 + r;
     const size_t jrow = (size_t)bh * sh.NC * kChunk + j;
-    const __nv_bfloat16* q = (const __nv_bfloat16*)a.q + hoff * D;
-    const __nv_bfloat16* k = (const __nv_bfloat16*)a.k + hoff * D;
-    const __nv_bfloat16* v = (const __nv_bfloat16*)a.v + hoff * D;
-    const __nv_bfloat16* dout = (const __nv_bfloat16*)a.dout + hoff * D;
     const float sig = sh.sigma;
 
     if (tid < 2 * M) sG[tid] = 0.0f;
     if (tid == 0) {
         mbar_init(&bar, 1);
+        mbar_init(&lbar, 1);
+        mbar_init(&ebar[0], 1);
+        mbar_init(&ebar[1], 1);
         mbar_fence_init();
         s_abort = 0;
     }
@@ -102,15 +105,34 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     const uint32_t R0 = 0, R1 = 128, R2 = 256, R3 = 384;
     TcCtl ctl{&bar, 0u, &s_abort, status};
     bool ok = true;
+    // TMA copies, issued by thread 0.  Rows past the tile's queries hold other
+    // rows or zeros; every product they enter is masked or has a zero factor.
+    int l_issued = 0, l_waited = 0, e_issued = 0, e_waited = 0;  // thread 0's bookkeeping
+    auto wait_copies = [&](uint64_t* b, int& waited) {  // thread 0
+        if (mbar_wait(b, (uint32_t)(waited & 1), kWaitCycles))
+            waited++;
+        else
+            atomicExch(&s_abort, 1);
+    };
+    auto wait_partial = [&](int i) {  // thread 0: partial i landed (its barrier's only phase)
+        if (mbar_wait(&ebar[i], 0, kWaitCycles))
+            e_waited++;
+        else
+            atomicExch(&s_abort, 1);
+    };
 
     // ---- value side: dP_L (tile loads in flight while the gates are computed)
-    const __nv_bfloat16* SV1 = a.SVb + ((size_t)bh * sh.NC + c1) * M * D;
-    const __nv_bfloat16* SK1 = a.SKb + ((size_t)bh * sh.NC + c1) * M * D;
-    load_tile_async<D>(dout, tbase, nq, XdO);
-    load_tile_async<D>(v, j0, nq, XKV);
-    load_state_pair_async<D, M>(SV1, has2 ? SV1 + M * D : nullptr, XS);
-    load_tile_async<D>(q, tbase, nq, XQ);
-    cp_async_commit();
+    if (tid == 0) {
+        l_issued++;
+        mbar_arrive_expect_tx(&lbar, 3 * TB + 2 * M * D * 2);
+#pragma unroll
+        for (int xx = 0; xx < D; xx += 64) {
+            tma_load_3d(XdO + xx * 256, &maps.dout, xx, tbase, bh, &lbar);
+            tma_load_3d(XKV + xx * 256, &maps.v, xx, j0, bh, &lbar);
+            tma_load_3d(XS + xx * 4 * M, &maps.sv, xx, c1 * M, bh, &lbar);
+            tma_load_3d(XQ + xx * 256, &maps.q, xx, tbase, bh, &lbar);
+        }
+    }
     float l[HM], b[HM];
     row_gates<M>(a.la + (hoff + j) * M, row_ok, l, b, s_tot, sG, warp, lane, h, r, nq);
     float rho[HM];
@@ -127,9 +149,10 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
     const float Dhat_r = row_ok ? a.Dhat[hoff + t] : 0.0f;
     float D_r = 0.0f;  // exact D = window part + slot part, set below
 
-    cp_async_wait<0>();
     sync_for_mma();
     if (tid == 0) {
+        wait_copies(&lbar, l_waited);
+        fence_after_sync();
         const uint32_t sd = smem_u32(XdO), sk = smem_u32(XKV), ss = smem_u32(XS);
         for (int kk = 0; kk < D / 16; kk++)
             mma_bf16(tm + R0, desc_k(sd, 128, kk), desc_k(sk, 128, kk), idesc_bf16(128, 128, false), kk > 0);
@@ -138,7 +161,16 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         mma_commit(&bar);
     }
     float dpl[HM];
-    if ((ok = ctl.wait())) {
+    if ((ok = ctl.wait() && !s_abort)) {
+        if (tid == 0) {  // V_c and [S^V] consumed: the key side's tiles go in flight
+            l_issued++;
+            mbar_arrive_expect_tx(&lbar, TB + 2 * M * D * 2);
+#pragma unroll
+            for (int xx = 0; xx < D; xx += 64) {
+                tma_load_3d(XKV + xx * 256, &maps.k, xx, j0, bh, &lbar);
+                tma_load_3d(XS + xx * 4 * M, &maps.sk, xx, c1 * M, bh, &lbar);
+            }
+        }
         mask_to_tile(tl + R0, XM, r, h, cr, row_ok, false);
         sync_for_mma();
         if (tid == 0) {
@@ -156,12 +188,10 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
 #pragma unroll
         for (int jj = 0; jj < HM; jj++) dpl[jj] = fexp(b[jj]) * so[jj] + fexp(b[jj] - rho[jj]) * pin[jj];
         // ---- key side: slot logits
-        load_tile_async<D>(k, j0, nq, XKV);
-        load_state_pair_async<D, M>(SK1, has2 ? SK1 + M * D : nullptr, XS);
-        cp_async_commit();
-        cp_async_wait<0>();
         sync_for_mma();
         if (tid == 0) {
+            wait_copies(&lbar, l_waited);
+            fence_after_sync();
             const uint32_t sq = smem_u32(XQ), sk = smem_u32(XKV), ss = smem_u32(XS);
             for (int kk = 0; kk < D / 16; kk++)
                 mma_bf16(tm + R0, desc_k(sq, 128, kk), desc_k(sk, 128, kk), idesc_bf16(128, 128, false), kk > 0);
@@ -244,9 +274,15 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
                 mma_bf16(tm + R2, desc_mn(sm, 128, kk), desc_mn(sd, 128, kk), idesc_am(128, D, true, true), kk > 0);
             mma_commit(&bar);
         }
-        ok = ctl.wait();
+        ok = ctl.wait() && !s_abort;
     }
     if (ok) {
+        if (tid == 0) {  // dout consumed: the window partial dq goes in flight into its tile
+            e_issued++;
+            mbar_arrive_expect_tx(&ebar[0], TB);
+#pragma unroll
+            for (int xx = 0; xx < D; xx += 64) tma_load_3d(XdO + xx * 256, &maps.dqw, xx, tbase, bh, &ebar[0]);
+        }
         // Row n of the result = slot n % M of chunk n / M.  Each 32-column slab of
         // both results goes through shared memory so every global store is a
         // run of whole rows.
@@ -290,6 +326,12 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         ok = ctl.wait();
     }
     if (ok) {
+        if (tid == 0) {  // G1 consumed: the dq correction partial goes in flight into its tile
+            e_issued++;
+            mbar_arrive_expect_tx(&ebar[1], TB);
+#pragma unroll
+            for (int xx = 0; xx < D; xx += 64) tma_load_3d(XG + xx * 256, &maps.dqwv, xx, tbase, bh, &ebar[1]);
+        }
         mask_to_tile(tl + R0, XM, r, h, cr, row_ok, false);
         sync_for_mma();
         if (tid == 0) {
@@ -301,36 +343,47 @@ bwd_sq_tc_kernel(const BwdArgs a, int* __restrict__ status) {
         ok = ctl.wait();
     }
     if (ok) {
-        const __nv_bfloat16* dqw = a.hdqw + (hoff + t) * D + h * HD;
-        const __nv_bfloat16* cv = a.hdqwV + (hoff + t) * D + h * HD;
+        // dq = window partial + (D^ - D) correction + slot part, staged in XM
+        // (its mask is consumed), copied out coalesced
         const float corr = Dhat_r - D_r;
-        __nv_bfloat16* dq = (__nv_bfloat16*)a.dq + (hoff + t) * D + h * HD;
-        uint4 pw[HD / 8], pv[HD / 8];  // all global loads first
-#pragma unroll
-        for (int e = 0; e < HD / 8; e++) {
-            pw[e] = row_ok ? *reinterpret_cast<const uint4*>(dqw + 8 * e) : make_uint4(0, 0, 0, 0);
-            pv[e] = row_ok ? *reinterpret_cast<const uint4*>(cv + 8 * e) : make_uint4(0, 0, 0, 0);
+        if (tid == 0) {
+            wait_partial(0);
+            wait_partial(1);
         }
+        ok = !__syncthreads_or(s_abort);
+        if (ok) {
 #pragma unroll
-        for (int c0 = 0; c0 < HD; c0 += 32) {
-            float g[32];
-            tmem_ld32(tl + R3 + h * HD + c0, g);
-            if (row_ok) {
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                float g[32];
+                tmem_ld32(tl + R3 + h * HD + c0, g);
 #pragma unroll
                 for (int e = 0; e < 32; e += 8) {
+                    const uint32_t off = sw_chunk(r, (h * HD + c0 + e) >> 3, 128);
                     float f[8], c8[8];
-                    unpack8(pw[(c0 + e) / 8], f);
-                    unpack8(pv[(c0 + e) / 8], c8);
+                    unpack8(*reinterpret_cast<const uint4*>(XdO + off), f);
+                    unpack8(*reinterpret_cast<const uint4*>(XG + off), c8);
 #pragma unroll
                     for (int q = 0; q < 8; q++) f[q] += g[e + q] + corr * c8[q];
-                    *reinterpret_cast<uint4*>(dq + c0 + e) = pack8(f);
+                    *reinterpret_cast<uint4*>(XM + off) = pack8(f);
                 }
             }
+            __syncthreads();
+            constexpr int CH = D / 8;
+            __nv_bfloat16* ob = (__nv_bfloat16*)a.dq + (hoff + tbase) * D;
+            for (int e = tid; e < nq * CH; e += kTcThreads) {
+                const int rr = e / CH, ch = e % CH;
+                *reinterpret_cast<uint4*>(ob + (size_t)rr * D + ch * 8) =
+                    *reinterpret_cast<const uint4*>(XM + sw_chunk(rr, ch, 128));
+            }
         }
-    } else if (row_ok && h == 0) {
-        ((__nv_bfloat16*)a.dq)[(hoff + t) * D] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
     }
-    if (!ok && tid == 0) mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);
+    if (!ok && row_ok && h == 0) ((__nv_bfloat16*)a.dq)[(hoff + t) * D] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
+    if (!ok && tid == 0) {  // let in-flight MMAs and copies drain
+        mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);
+        for (int q = l_waited; q < l_issued; q++) mbar_wait(&lbar, (uint32_t)(q & 1), kWaitCycles);
+        for (int q = e_waited; q < e_issued; q++) mbar_wait(&ebar[q], 0, kWaitCycles);
+        atomicExch(status, kStatusTimeout);
+    }
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 512);
@@ -624,11 +677,22 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
     const int W0 = sh.T - sh.R;
     const int qtiles = (W0 + 127) / 128 + (sh.R + 127) / 128;
     {
+        SqMaps maps;
+        const int ncm = (sh.NC > 0 ? sh.NC : 1) * M;
+        if ((e = tmap_rows_bf16(&maps.q, a.q, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.dout, a.dout, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.k, a.k, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.v, a.v, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.sk, a.SKb, D, ncm, sh.BH, 2 * M)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.sv, a.SVb, D, ncm, sh.BH, 2 * M)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.dqw, a.hdqw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.dqwv, a.hdqwV, D, sh.T, sh.BH, 128)) != cudaSuccess)
+            return e;
         auto kern = bwd_sq_tc_kernel<D, M>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sq_smem<D, M>())) != cudaSuccess)
             return e;
         if (qtiles > 0)
-            NHA_LAUNCH("bwd_sq_tc", st, kern<<<dim3(qtiles, sh.BH), kTcThreads, sq_smem<D, M>(), st>>>(a, status));
+            NHA_LAUNCH("bwd_sq_tc", st, kern<<<dim3(qtiles, sh.BH), kTcThreads, sq_smem<D, M>(), st>>>(a, maps, status));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // the bandwidth-bound adjoint scan shares the SMs with the key-major kernel
