@@ -40,7 +40,7 @@ struct Plan {
     nha::Shape sh;
     int d, m;
     // workspace offsets, in floats
-    size_t SK, SV, SKb, SVb, G, U, CAR, TAB, STATUS, QR, KR, Dv, Dhat, Dwin, dqwV, dqw, dkw, dvw, DL, PL, DB1, RK, RV, RKb, RVb, total;
+    size_t SK, SV, SKb, SVb, G, U, TAB, STATUS, QR, KR, Dv, Dhat, Dwin, dqwV, dqw, dkw, dvw, DL, PL, DB1, RK, RV, RKb, RVb, total;
 };
 
 nha_status_t check_shape(int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dt) {
@@ -104,7 +104,6 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward) {
         p.RV = take(BH * NC * m * d);
         p.RKb = take(BH * NC * m * d / 2);
         p.RVb = take(BH * NC * m * d / 2);
-        p.CAR = take(2 * BH * NC * m);
     }
     p.total = off;
     return p;
@@ -276,7 +275,6 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
     a.RK = ws + p.RK; a.RV = ws + p.RV;
     a.SKb = (__nv_bfloat16*)(ws + p.SKb); a.SVb = (__nv_bfloat16*)(ws + p.SVb);
     a.U = (__nv_bfloat16*)(ws + p.U);
-    a.carry = ws + p.CAR;
     a.RKb = (__nv_bfloat16*)(ws + p.RKb); a.RVb = (__nv_bfloat16*)(ws + p.RVb);
     a.hdqw = (__nv_bfloat16*)a.dqw; a.hdqwV = (__nv_bfloat16*)a.dqwV;
     a.hdkw = (__nv_bfloat16*)a.dkw; a.hdvw = (__nv_bfloat16*)a.dvw;

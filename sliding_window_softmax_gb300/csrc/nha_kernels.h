@@ -80,7 +80,6 @@ struct BwdArgs {
     __nv_bfloat16* RKb;
     __nv_bfloat16* RVb;
     __nv_bfloat16* U;  // chunk coefficients (bf16 path)
-    float* carry;      // [2][BH][NC][M] dlog_alpha carry per chunk, K and V parts (bf16 path)
     // bf16 path: the window partials and sigma dL, P_L are kept in bf16 (they
     // alias the storage of the fp32 arrays above)
     __nv_bfloat16* hdqw;
@@ -128,7 +127,7 @@ cudaError_t launch_wkv(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bfl
                        int* status, cudaStream_t st);
 cudaError_t launch_state_scan_rev(const BwdArgs& a, int M, int D, cudaStream_t st);
 // bf16 path: reverse adjoint scan (RK, RV contributions in; RKb, RVb out) and
-// the per-chunk dlog_alpha carry (a.carry), one pass.
+// the per-chunk dlog_alpha carry, added to wsDB1 of each chunk's last state row.
 cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st);
 cudaError_t launch_dla_carry(const BwdArgs& a, int M, int D, cudaStream_t st);
 // bf16 path: chunk coefficients U (workspace, [BH][NC * C][64] bf16) and

@@ -16,7 +16,8 @@
 //   dv  += ((Ek (P_L o Eq)^T) o M^T) dout_t + (Ek o eG) Rc^V
 //   du   = Fk o [((K_c Q_t^T o M^T)(sigma dL o Eq)) + eG o (K_c Rc^K^T)] + (same with V, dout, P_L, Rc^V)
 //   db   = db1 - u o du;  dlog_alpha = suffix-sum of db in the chunk - alpha o du
-//          (+ the totals of all later chunks, added by the carry kernel)
+//          (+ the totals of all later chunks: the adjoint scan adds them to db1
+//          of each chunk's last state row, so the suffix sum carries them)
 // ("Native Hybrid Attention for Efficient Sequence Modeling", Paper-Notes page,
 // 关键设计/层内混合 recurrence and Chunkwise 并行计算; the backward is the
 // derivative of that chunked form.)
@@ -410,7 +411,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
     unsigned char* XM2 = XM1 + 32768;
     float* s_tot = reinterpret_cast<float*>(XM2 + 32768);  // [4][M]
     float* sG = s_tot + 4 * M;                              // [2][M]
-    __shared__ uint64_t bar, lbar, ebar;  // MMAs; operand tiles of a pass; window partials
+    __shared__ uint64_t bar, lbar, ebar, dbar;  // MMAs; operand tiles of a pass; window partials; db1 rows
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -448,6 +449,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         mbar_init(&bar, 1);
         mbar_init(&lbar, 1);
         mbar_init(&ebar, 1);
+        mbar_init(&dbar, 1);
         mbar_fence_init();
         s_abort = 0;
     }
@@ -465,6 +467,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
     // pass.  Rows past the tile's states hold other tokens or zeros; every
     // product they enter is multiplied by a zero gate or masked away.
     int l_issued = 0, l_waited = 0, e_issued = 0, e_waited = 0;  // thread 0's copy bookkeeping
+    bool d_issued = false;
     auto issue_loads = [&](int pass) {
         if (tid != 0) return;
         l_issued++;
@@ -570,6 +573,12 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         }
         issue_partial(pass);
         if (pass == 0) issue_loads(1);  // the operand tiles are free: next pass in flight
+        if (pass == 1 && tid == 0) {    // db1 rows of the tile for the gate gradient, into XA
+            const int nrows = min(128, sh.NC * kChunk - sbase);
+            d_issued = true;
+            mbar_arrive_expect_tx(&dbar, (uint32_t)(nrows * M * 4));
+            bulk_load(XA, a.wsDB1 + (jrow - r) * M, (uint32_t)(nrows * M * 4), &dbar);
+        }
         {
             float intra[HM];
             tmem_ld(tl + R0 + h * HM, intra, HM);
@@ -612,9 +621,12 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         }
     }
     if (ok) {
-        // db = db1 - u du;  dlog_alpha = (suffix sum of db in the chunk) - alpha du
+        // db = db1 - u du;  dlog_alpha = (suffix sum of db in the chunk) - alpha du.
+        // The carry of all later chunks sits in db1 of the chunk's last state row
+        // (added by the adjoint scan), so the suffix sum hands it to every row.
+        if (!mbar_wait(&dbar, 0, kWaitCycles)) atomicExch(&s_abort, 1);
         float db[HM];
-        const float* db1 = a.wsDB1 + jrow * M + h * HM;
+        const float* db1 = reinterpret_cast<const float*>(XA) + r * M + h * HM;
 #pragma unroll
         for (int jj = 0; jj < HM; jj += 4) {
             const float4 d4 = slot_ok ? *reinterpret_cast<const float4*>(db1 + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -623,34 +635,36 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
             for (int q = 0; q < 4; q++) db[jj + q] = slot_ok ? dd[q] - (-expm1f(l[jj + q])) * du[jj + q] : 0.0f;
         }
         chunk_suffix<M>(db, s_tot, warp, lane, h);
-        if (row_ok) {
-            // + the carry of the row's chunk: the gate gradient of all later chunks
-            const size_t co = ((size_t)bh * sh.NC + c1 + cr) * M + h * HM;
-            const size_t cv = (size_t)sh.BH * sh.NC * M;
-            float* dla = a.dla + (hoff + s) * M + h * HM;
+        // staged in XB (16-byte chunk q of the half row at q ^ (r & 7)), copied out coalesced
+        constexpr int QM = HM / 4 - 1;
+        float* st = reinterpret_cast<float*>(XB) + r * M + h * HM;
 #pragma unroll
-            for (int jj = 0; jj < HM; jj += 4) {
-                float o4[4];
-                if (slot_ok) {
-                    const float4 ck = *reinterpret_cast<const float4*>(a.carry + co + jj);
-                    const float4 cw = *reinterpret_cast<const float4*>(a.carry + cv + co + jj);
-                    const float cs[4] = {ck.x + cw.x, ck.y + cw.y, ck.z + cw.z, ck.w + cw.w};
+        for (int jj = 0; jj < HM; jj += 4) {
+            float o4[4];
 #pragma unroll
-                    for (int q = 0; q < 4; q++) o4[q] = db[jj + q] - fexp(l[jj + q]) * du[jj + q] + cs[q];
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; q++) o4[q] = 0.0f;
-                }
-                *reinterpret_cast<float4*>(dla + jj) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+            for (int q = 0; q < 4; q++) o4[q] = slot_ok ? db[jj + q] - fexp(l[jj + q]) * du[jj + q] : 0.0f;
+            *reinterpret_cast<float4*>(st + 4 * ((jj / 4) ^ (r & QM))) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+        }
+        if (__syncthreads_or(s_abort)) {
+            ok = false;
+        } else {
+            constexpr int C4 = M / 4;  // 16-byte chunks per row
+            float* ob = a.dla + (hoff + sbase) * M;
+            for (int e = tid; e < nk * C4; e += kTcThreads) {
+                const int rr = e / C4, c = e % C4, hh = c / (HM / 4), q = c % (HM / 4);
+                *reinterpret_cast<float4*>(ob + (size_t)rr * M + 4 * c) = *reinterpret_cast<const float4*>(
+                    reinterpret_cast<const float*>(XB) + rr * M + hh * HM + 4 * (q ^ (rr & QM)));
             }
         }
-    } else if (row_ok && h == 0) {
+    }
+    if (!ok && row_ok && h == 0) {
         a.dla[(hoff + s) * M] = __int_as_float(0x7fc00000);
     }
     if (!ok && tid == 0) {  // let in-flight MMAs and copies drain
         mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);
         for (int q = l_waited; q < l_issued; q++) mbar_wait(&lbar, (uint32_t)(q & 1), kWaitCycles);
         for (int q = e_waited; q < e_issued; q++) mbar_wait(&ebar, (uint32_t)(q & 1), kWaitCycles);
+        if (d_issued) mbar_wait(&dbar, 0, kWaitCycles);
         atomicExch(status, kStatusTimeout);
     }
     fence_before_sync();

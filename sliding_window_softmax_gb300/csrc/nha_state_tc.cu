@@ -197,25 +197,26 @@ constexpr int kAdjSlots = 8;
 // R_c, the adjoint carried into chunk c from the later chunks, follows
 // R_{c - 1} = exp(G_c) R_c + dR_c (dR_c: the chunk's own contribution, from the
 // query-side kernel); it is written in bf16 for the key-side kernel.  The carry
-// of chunk c, carry_c[i] = sum_d R_c[i][d] S_prev(c + 1)[i][d] (the bf16 states),
-// is the total
-// over all later rows of the gate gradient that every row of chunk c receives
-// (zero for the last chunk); K and V write their parts separately.  One CTA per
-// (head, 8 slots, K or V), thread = column d, two chunks of loads in flight
-// (8 slots keep it small enough to share the SMs with the key-major kernel).
+// of chunk c, sum_d R_c[i][d] S_prev(c + 1)[i][d] (the bf16 states), is the
+// total over all later rows of the gate gradient that every row of chunk c
+// receives; it is added to db1 of the chunk's last state row, whose in-chunk
+// suffix sum then hands it to every row.  One CTA per (head, 8 slots): D
+// threads for K and D for V (thread = column d), so the carry's two parts
+// are summed in one CTA and added once; two chunks of loads in flight (8
+// slots keep it small enough to share the SMs with the key-major kernel).
 template <int D>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(2 * D)
 adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, const __nv_bfloat16* __restrict__ SK,
                 const __nv_bfloat16* __restrict__ SV, const float* __restrict__ G, __nv_bfloat16* __restrict__ RKb,
-                __nv_bfloat16* __restrict__ RVb, float* __restrict__ carry, Shape sh, int M) {
-    constexpr int NW = D / 32, SG = kAdjSlots;
+                __nv_bfloat16* __restrict__ RVb, float* __restrict__ db1, Shape sh, int M) {
+    constexpr int NW = 2 * D / 32, SG = kAdjSlots;
     __shared__ float red[2][NW][SG];
-    const int d = threadIdx.x, warp = d >> 5, lane = d & 31;
-    const int bh = blockIdx.x, i0 = SG * blockIdx.y, tz = blockIdx.z, NC = sh.NC;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tz = threadIdx.x / D, d = threadIdx.x % D;  // tz 0: K, 1: V
+    const int bh = blockIdx.x, i0 = SG * blockIdx.y, NC = sh.NC;
     const float* X = tz == 0 ? RK : RV;
     const __nv_bfloat16* S = tz == 0 ? SK : SV;
     __nv_bfloat16* Xb = tz == 0 ? RKb : RVb;
-    float* car = carry + ((size_t)tz * sh.BH + bh) * NC * M + i0;
     auto at = [&](int c) { return (((size_t)bh * NC + c) * M + i0) * D + d; };
     auto load = [&](int c, float (&x)[SG], float (&sp)[SG], float (&g)[SG]) {
         const size_t o = at(c);
@@ -255,11 +256,13 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
 #pragma unroll
             for (int i = 0; i < SG; i++) red[parity][warp][i] = part[i];
         __syncthreads();  // red[parity] complete; red[parity ^ 1] free again
-        if (d < SG) {
+        if (threadIdx.x < SG && c + 1 < NC) {
             float t = 0.0f;
 #pragma unroll
-            for (int q = 0; q < NW; q++) t += red[parity][q][d];
-            car[(size_t)c * M + d] = t;
+            for (int q = 0; q < NW; q++) t += red[parity][q][threadIdx.x];
+            // db1 of the chunk's last state row: the in-chunk suffix sum spreads it
+            const int last = min(c * kChunk + kChunk, sh.R) - 1;
+            db1[((size_t)bh * NC * kChunk + last) * M + i0 + threadIdx.x] += t;
         }
         parity ^= 1;
 #pragma unroll
@@ -280,13 +283,13 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
 cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st) {
     const Shape& sh = a.sh;
     if (sh.NC == 0) return cudaSuccess;
-    const dim3 grid(sh.BH, M / kAdjSlots, 2);
+    const dim3 grid(sh.BH, M / kAdjSlots);
     if (D == 128)
         NHA_LAUNCH("adj_scan", st,
-                   adj_scan_kernel<128><<<grid, 128, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.carry, sh, M));
+                   adj_scan_kernel<128><<<grid, 256, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.wsDB1, sh, M));
     else
         NHA_LAUNCH("adj_scan", st,
-                   adj_scan_kernel<64><<<grid, 64, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.carry, sh, M));
+                   adj_scan_kernel<64><<<grid, 128, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.wsDB1, sh, M));
     return cudaGetLastError();
 }
 
