@@ -392,7 +392,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
 
 // ---------------------------------------------------------------------------------------
 struct SkMaps {
-    CUtensorMap q, dout, k, v, rk, rv, dkw, dvw;
+    CUtensorMap q, dout, k, v, rk, rv, dkw, dvw, la, dl, pl;
 };
 
 template <int D, int M>
@@ -411,7 +411,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
     unsigned char* XM2 = XM1 + 32768;
     float* s_tot = reinterpret_cast<float*>(XM2 + 32768);  // [4][M]
     float* sG = s_tot + 4 * M;                              // [2][M]
-    __shared__ uint64_t bar, lbar, ebar, dbar;  // MMAs; operand tiles of a pass; window partials; db1 rows
+    __shared__ uint64_t bar, lbar, ebar, dbar, gbar;  // MMAs; pass operands; window partials; db1; log_alpha + dL
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -450,6 +450,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         mbar_init(&lbar, 1);
         mbar_init(&ebar, 1);
         mbar_init(&dbar, 1);
+        mbar_init(&gbar, 1);
         mbar_fence_init();
         s_abort = 0;
     }
@@ -467,17 +468,19 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
     // pass.  Rows past the tile's states hold other tokens or zeros; every
     // product they enter is multiplied by a zero gate or masked away.
     int l_issued = 0, l_waited = 0, e_issued = 0, e_waited = 0;  // thread 0's copy bookkeeping
-    bool d_issued = false;
+    bool d_issued = false, g_issued = false, g_waited = false;
+    // the second pass also brings P_L into XW (W o Eq is formed in place)
     auto issue_loads = [&](int pass) {
         if (tid != 0) return;
         l_issued++;
-        mbar_arrive_expect_tx(&lbar, 2 * TB + 2 * M * D * 2);
+        mbar_arrive_expect_tx(&lbar, 2 * TB + 2 * M * D * 2 + (pass == 1 ? 16384 : 0));
 #pragma unroll
         for (int xx = 0; xx < D; xx += 64) {
             tma_load_3d(XA + xx * 256, pass == 0 ? &maps.q : &maps.dout, xx, sbase + sh.w, bh, &lbar);
             tma_load_3d(XB + xx * 256, pass == 0 ? &maps.k : &maps.v, xx, sbase, bh, &lbar);
             tma_load_3d(XR + xx * 4 * M, pass == 0 ? &maps.rk : &maps.rv, xx, c1 * M, bh, &lbar);
         }
+        if (pass == 1) tma_load_3d(XW, &maps.pl, 0, sbase, bh, &lbar);
     };
     // window partial dk or dv of the tile's rows into XM1 (its masks are consumed)
     auto issue_partial = [&](int pass) {
@@ -488,9 +491,21 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         for (int xx = 0; xx < D; xx += 64)
             tma_load_3d(XM1 + xx * 256, pass == 0 ? &maps.dkw : &maps.dvw, xx, sbase, bh, &ebar);
     };
+    if (tid == 0) {  // log_alpha rows into XM1 (free until the first masks), sigma dL into XW
+        g_issued = true;
+        mbar_arrive_expect_tx(&gbar, (uint32_t)(((M + 31) / 32) * 16384 + 16384));
+#pragma unroll
+        for (int xx = 0; xx < M; xx += 32) tma_load_3d(XM1 + xx * 512, &maps.la, xx, sbase, bh, &gbar);
+        tma_load_3d(XW, &maps.dl, 0, sbase, bh, &gbar);
+    }
     issue_loads(0);  // in flight while the gates are computed
+    if (mbar_wait(&gbar, 0, kWaitCycles)) {
+        g_waited = true;
+    } else {
+        atomicExch(&s_abort, 1);
+    }
     float l[HM], b[HM];
-    row_gates<M>(a.la + (hoff + s) * M, slot_ok, l, b, s_tot, sG, warp, lane, h, r, nc);
+    row_gates_tile<M>(XM1, slot_ok, l, b, s_tot, sG, warp, lane, h, r, nc);
     float rho[HM], eG[HM];
 #pragma unroll
     for (int jj = 0; jj < HM; jj++) {
@@ -515,14 +530,20 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
     for (int jj = 0; jj < HM; jj++) du[jj] = 0.0f;
 
     for (int pass = 0; pass < 2 && ok; pass++) {
-        const __nv_bfloat16* W = (pass == 0 ? a.hDL : a.hPL) + jrow * M + h * HM;
+        if (pass == 1) {  // the second pass's tiles, P_L among them
+            if (mbar_wait(&lbar, 1, kWaitCycles)) {
+                if (tid == 0) l_waited++;
+            } else {
+                atomicExch(&s_abort, 1);
+            }
+        }
         {
             float weq[HM];
 #pragma unroll
             for (int jj = 0; jj < HM; jj += 8) {
                 float w8[8];
                 if (slot_ok) {
-                    unpack8(*reinterpret_cast<const uint4*>(W + jj), w8);
+                    unpack8(*reinterpret_cast<const uint4*>(XW + sw_chunk(r, (h * HM + jj) >> 3, 128)), w8);
                 } else {
 #pragma unroll
                     for (int q = 0; q < 8; q++) w8[q] = 0.0f;
@@ -534,11 +555,13 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         }
         sync_for_mma();
         if (tid == 0) {
-            // this pass's tiles landed
-            if (mbar_wait(&lbar, (uint32_t)pass, kWaitCycles))
-                l_waited++;
-            else
-                atomicExch(&s_abort, 1);
+            // the first pass's tiles landed (the second pass's were waited above)
+            if (pass == 0) {
+                if (mbar_wait(&lbar, 0, kWaitCycles))
+                    l_waited++;
+                else
+                    atomicExch(&s_abort, 1);
+            }
             fence_after_sync();
             const uint32_t se = smem_u32(XE), sw = smem_u32(XW), sa = smem_u32(XA), sb = smem_u32(XB),
                            sr = smem_u32(XR);
@@ -665,6 +688,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         for (int q = l_waited; q < l_issued; q++) mbar_wait(&lbar, (uint32_t)(q & 1), kWaitCycles);
         for (int q = e_waited; q < e_issued; q++) mbar_wait(&ebar, (uint32_t)(q & 1), kWaitCycles);
         if (d_issued) mbar_wait(&dbar, 0, kWaitCycles);
+        if (g_issued && !g_waited) mbar_wait(&gbar, 0, kWaitCycles);
         atomicExch(status, kStatusTimeout);
     }
     fence_before_sync();
@@ -726,7 +750,10 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
             (e = tmap_rows_bf16(&maps.rk, a.RKb, D, ncm, sh.BH, 2 * M)) != cudaSuccess ||
             (e = tmap_rows_bf16(&maps.rv, a.RVb, D, ncm, sh.BH, 2 * M)) != cudaSuccess ||
             (e = tmap_rows_bf16(&maps.dkw, a.hdkw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
-            (e = tmap_rows_bf16(&maps.dvw, a.hdvw, D, sh.T, sh.BH, 128)) != cudaSuccess)
+            (e = tmap_rows_bf16(&maps.dvw, a.hdvw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_f32(&maps.la, a.la, M, sh.T, sh.BH)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.dl, a.hDL, M, ncm / M * kChunk, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_bf16(&maps.pl, a.hPL, M, ncm / M * kChunk, sh.BH, 128)) != cudaSuccess)
             return e;
         auto kern = bwd_sk_tc_kernel<D, M>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk_smem<D, M>())) != cudaSuccess)

@@ -289,6 +289,10 @@ __device__ __forceinline__ void chunk_suffix(float (&x)[M / 2], float* s_tot, in
 // Gates of this thread's row: loads log_alpha (0 past the valid rows), the
 // chunk-local cumsum b and the chunk totals sG[2][M] (zero for an empty chunk).
 template <int M, bool kProd = false>
+__device__ __forceinline__ void gates_from_l(const float (&l)[M / 2], float (&b)[M / 2], float* s_tot, float* sG,
+                                             int warp, int lane, int h, int r, int nrows);
+
+template <int M, bool kProd = false>
 __device__ __forceinline__ void row_gates(const float* __restrict__ la_row, bool valid, float (&l)[M / 2],
                                           float (&b)[M / 2], float* s_tot, float* sG, int warp, int lane,
                                           int h, int r, int nrows) {
@@ -299,6 +303,31 @@ __device__ __forceinline__ void row_gates(const float* __restrict__ la_row, bool
                                : make_float4(0.f, 0.f, 0.f, 0.f);
         l[jj] = v.x; l[jj + 1] = v.y; l[jj + 2] = v.z; l[jj + 3] = v.w;
     }
+    gates_from_l<M, kProd>(l, b, s_tot, sG, warp, lane, h, r, nrows);
+}
+
+// Same, with log_alpha of the tile's 128 rows already in shared memory: the
+// fp32 [128][M] tile as TMA writes it in 32-column boxes of 16 KB with
+// 128-byte swizzle (columns past M read as zero).
+template <int M, bool kProd = false>
+__device__ __forceinline__ void row_gates_tile(const unsigned char* tile, bool valid, float (&l)[M / 2],
+                                               float (&b)[M / 2], float* s_tot, float* sG, int warp, int lane,
+                                               int h, int r, int nrows) {
+    constexpr int HM = M / 2;
+#pragma unroll
+    for (int jj = 0; jj < HM; jj += 4) {
+        const int col = h * HM + jj, c = (col & 31) >> 2;
+        const float4 v = valid ? *reinterpret_cast<const float4*>(tile + (col >> 5) * 16384 + r * 128 + ((c ^ (r & 7)) << 4))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        l[jj] = v.x; l[jj + 1] = v.y; l[jj + 2] = v.z; l[jj + 3] = v.w;
+    }
+    gates_from_l<M, kProd>(l, b, s_tot, sG, warp, lane, h, r, nrows);
+}
+
+template <int M, bool kProd>
+__device__ __forceinline__ void gates_from_l(const float (&l)[M / 2], float (&b)[M / 2], float* s_tot, float* sG,
+                                             int warp, int lane, int h, int r, int nrows) {
+    constexpr int HM = M / 2;
 #pragma unroll
     for (int jj = 0; jj < HM; jj++) b[jj] = l[jj];
     chunk_prefix<M, kProd>(b, s_tot, warp, lane, h);

@@ -35,6 +35,19 @@ cudaError_t tmap_rows_bf16(CUtensorMap* map, const void* base, int D, int T, int
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t tmap_rows_f32(CUtensorMap* map, const float* base, int width, int rows, int BH) {
+    std::call_once(g_encode_once, resolve_encode);
+    if (!g_encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)rows, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)width * 4, (cuuint64_t)rows * width * 4};
+    const cuuint32_t box[3] = {32, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t tmap_tab(CUtensorMap* map, const float2* tab, int H2, int T) {
     std::call_once(g_encode_once, resolve_encode);
     if (!g_encode) return cudaErrorNotSupported;
