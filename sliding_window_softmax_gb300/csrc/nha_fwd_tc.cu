@@ -31,7 +31,7 @@ using namespace tc;
 constexpr int kFwdThreads = 288, kFwdStages = 3;
 
 struct FwdMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, la;
 };
 
 template <int D, int M>
@@ -53,7 +53,7 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
     float* sG = s_tot + 4 * M;                             // [2][M]
     float* redm = sG + 2 * M;                              // [2][128]
     float* reds = redm + 256;                              // [2][128]
-    __shared__ uint64_t bar, qbar, full[NS], sfull[2], pready, bdone[2], drain[2];
+    __shared__ uint64_t bar, gbar, qbar, full[NS], sfull[2], pready, bdone[2], drain[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -79,6 +79,7 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
 
     if (tid == 0) {
         mbar_init(&bar, 1);
+        mbar_init(&gbar, 1);
         mbar_init(&qbar, 1);
         for (int q = 0; q < NS; q++) mbar_init(&full[q], 1);
         for (int q = 0; q < 2; q++) {
@@ -183,8 +184,14 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
             load_tile_async<D>(v, j0, nq, VB[0]);
             load_state_pair_async<D, M>(SK1, has2 ? SK1 + M * D : nullptr, KB[1]);
             cp_async_commit();
+            if (tid == 0) {  // log_alpha rows by TMA into the last stage's K~ buffer (idle here)
+                mbar_arrive_expect_tx(&gbar, (uint32_t)(((M + 31) / 32) * 16384));
+#pragma unroll
+                for (int xx = 0; xx < M; xx += 32) tma_load_3d(KB[NS - 1] + xx * 512, &maps.la, xx, j0, bh, &gbar);
+            }
+            if (!mbar_wait(&gbar, 0, kWaitCycles)) *abort = 1;
             float lg[HM], b[HM], rho[HM];
-            row_gates<M, true>(a.la + (hoff + j0 + r) * M, row_ok, lg, b, s_tot, sG, warp, lane, h, r, nq);
+            row_gates_tile<M, true>(KB[NS - 1], row_ok, lg, b, s_tot, sG, warp, lane, h, r, nq);
             {
                 float ek[HM];
 #pragma unroll
@@ -387,9 +394,10 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
     fence_before_sync();
     __syncthreads();
     if (s_abort) {  // let the copies and MMAs in flight land before the TMEM and the CTA go
-        if (tid == 0) {  // slot-branch MMAs (issued by this thread)
+        if (tid == 0) {  // slot-branch MMAs and log_alpha copy (issued by this thread)
             mma_commit(&drain[0]);
             mbar_wait(&drain[0], 0, kWaitCycles);
+            if (slot) mbar_wait(&gbar, 0, kWaitCycles);
         }
         if (warp == 8 && lane == 0) {  // window MMAs and copies
             mma_commit(&drain[1]);
@@ -506,7 +514,8 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bf
     FwdMaps maps;
     if ((e = tmap_rows_bf16(&maps.q, qr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
         (e = tmap_rows_bf16(&maps.k, kr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
-        (e = tmap_rows_bf16(&maps.v, a.v, D, sh.T, sh.BH, 128)) != cudaSuccess)
+        (e = tmap_rows_bf16(&maps.v, a.v, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+        (e = tmap_rows_f32(&maps.la, a.la, M, sh.T, sh.BH)) != cudaSuccess)
         return e;
     const size_t sm = tc_fwd_smem<D, M>();
     auto kern = fwd_tc_kernel<D, M>;

@@ -36,7 +36,7 @@ __host__ __device__ constexpr uint32_t idesc_am(int M, int N, bool a_mn, bool b_
 
 // ---------------------------------------------------------------------------------------
 struct SqMaps {
-    CUtensorMap q, dout, k, v, sk, sv, dqw, dqwv;
+    CUtensorMap q, dout, k, v, sk, sv, dqw, dqwv, la;
 };
 
 template <int D, int M>
@@ -55,7 +55,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
     float* s_tot = reinterpret_cast<float*>(XG + 32768);  // [4][M]
     float* sG = s_tot + 4 * M;                             // [2][M]
     float* red = sG + 2 * M;                               // [2][128]
-    __shared__ uint64_t bar, lbar, ebar[2];  // MMAs; operand tiles; the two window partials (one copy each)
+    __shared__ uint64_t bar, lbar, ebar[2], gbar;  // MMAs; operand tiles; the two window partials; log_alpha
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -94,6 +94,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
         mbar_init(&lbar, 1);
         mbar_init(&ebar[0], 1);
         mbar_init(&ebar[1], 1);
+        mbar_init(&gbar, 1);
         mbar_fence_init();
         s_abort = 0;
     }
@@ -109,6 +110,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
     // TMA copies, issued by thread 0.  Rows past the tile's queries hold other
     // rows or zeros; every product they enter is masked or has a zero factor.
     int l_issued = 0, l_waited = 0, e_issued = 0, e_waited = 0;  // thread 0's bookkeeping
+    bool g_issued = false, g_waited = false;
     auto wait_copies = [&](uint64_t* b, int& waited) {  // thread 0
         if (mbar_wait(b, (uint32_t)(waited & 1), kWaitCycles))
             waited++;
@@ -122,8 +124,13 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
             atomicExch(&s_abort, 1);
     };
 
-    // ---- value side: dP_L (tile loads in flight while the gates are computed)
+    // ---- value side: dP_L (tile loads in flight while the gates are computed);
+    // log_alpha rows into XG, free until G1 is formed
     if (tid == 0) {
+        g_issued = true;
+        mbar_arrive_expect_tx(&gbar, (uint32_t)(((M + 31) / 32) * 16384));
+#pragma unroll
+        for (int xx = 0; xx < M; xx += 32) tma_load_3d(XG + xx * 512, &maps.la, xx, j0, bh, &gbar);
         l_issued++;
         mbar_arrive_expect_tx(&lbar, 3 * TB + 2 * M * D * 2);
 #pragma unroll
@@ -134,8 +141,13 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
             tma_load_3d(XQ + xx * 256, &maps.q, xx, tbase, bh, &lbar);
         }
     }
+    if (mbar_wait(&gbar, 0, kWaitCycles)) {
+        g_waited = true;
+    } else {
+        atomicExch(&s_abort, 1);
+    }
     float l[HM], b[HM];
-    row_gates<M>(a.la + (hoff + j) * M, row_ok, l, b, s_tot, sG, warp, lane, h, r, nq);
+    row_gates_tile<M>(XG, row_ok, l, b, s_tot, sG, warp, lane, h, r, nq);
     float rho[HM];
 #pragma unroll
     for (int jj = 0; jj < HM; jj++) rho[jj] = 0.5f * sG[cr * M + h * HM + jj];
@@ -383,6 +395,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
         mbar_wait(&bar, ctl.phase ^ 1u, kWaitCycles);
         for (int q = l_waited; q < l_issued; q++) mbar_wait(&lbar, (uint32_t)(q & 1), kWaitCycles);
         for (int q = e_waited; q < e_issued; q++) mbar_wait(&ebar[q], 0, kWaitCycles);
+        if (g_issued && !g_waited) mbar_wait(&gbar, 0, kWaitCycles);
         atomicExch(status, kStatusTimeout);
     }
     fence_before_sync();
@@ -724,7 +737,8 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
             (e = tmap_rows_bf16(&maps.sk, a.SKb, D, ncm, sh.BH, 2 * M)) != cudaSuccess ||
             (e = tmap_rows_bf16(&maps.sv, a.SVb, D, ncm, sh.BH, 2 * M)) != cudaSuccess ||
             (e = tmap_rows_bf16(&maps.dqw, a.hdqw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
-            (e = tmap_rows_bf16(&maps.dqwv, a.hdqwV, D, sh.T, sh.BH, 128)) != cudaSuccess)
+            (e = tmap_rows_bf16(&maps.dqwv, a.hdqwV, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_f32(&maps.la, a.la, M, sh.T, sh.BH)) != cudaSuccess)
             return e;
         auto kern = bwd_sq_tc_kernel<D, M>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sq_smem<D, M>())) != cudaSuccess)
