@@ -52,6 +52,10 @@ def workloads():
 
 # ----------------------------------------------------------------------------------------
 # Algorithmic work model (per launch).
+# kernels the library runs on its side stream, beside the caller's stream
+SIDE_STREAM_KERNELS = ("rope_qk", "adj_scan")
+
+
 def work_model(wl):
     T, d, m = wl.T, wl.d, wl.m
     w = min(wl.w, T)
@@ -62,11 +66,27 @@ def work_model(wl):
     fwd_flops = BH * (4 * d * n_sum + 8 * m * d * R)
     fwd_bytes = BH * T * (4 * d * e + 4 * m + 4)
     bwd_bytes = BH * T * (8 * d * e + 8 * m + 4)
-    fwd_main = (BH * (4 * d * n_sum + 4 * m * d * R), fwd_bytes)
-    wdq = (BH * 6 * d * n_sum, BH * T * (5 * d * e + 8))
+    # Per-kernel algorithmic bytes: every input a kernel reads and every output
+    # it writes, once (the bf16 tensor-core kernels as designed).  Per token:
+    # e-byte rows of width d, fp32 log_alpha rows (4m), bf16 slot rows (2m);
+    # per 128-row tile, pairs of bf16 [m][d] chunk states (2 * 2 m d bytes).
+    tiles = (R + 127) // 128
+    pair = 2 * 2 * m * d  # one [2m][d] bf16 pair
+    fwd_main = (BH * (4 * d * n_sum + 8 * m * d * R),
+                BH * T * (6 * d * e + 4 * m + 4) + BH * tiles * 2 * pair)
+    # q~, dout, o, k~, v in; dq and its correction partial out; D^, D_win
+    wdq = (BH * 8 * d * n_sum, BH * T * (7 * d * e + 12))
+    # q~, dout, k~, v, lse, D in; dk, dv partials out
     wkv = (BH * 8 * d * n_sum, BH * T * (6 * d * e + 8))
-    sq = (BH * 12 * m * d * R, BH * T * (3 * d * e + 4 * m + 8))
-    sk = (BH * 12 * m * d * R, BH * T * (6 * d * e + 8 * m))
+    # q, k, v, dout, dq partials, log_alpha, lse, D_win, D^ in; state pairs in;
+    # dq, sigma dL, P_L (bf16), db1, D out; fp32 chunk adjoint contributions out
+    sq = (BH * 12 * m * d * R,
+          BH * T * (7 * d * e + 4 * m + 16) + BH * R * (2 * 2 * m + 4 * m) + BH * tiles * 2 * pair
+          + BH * ((R + 63) // 64) * 2 * m * d * 4)
+    # q, dout, k, v, dk / dv partials in; dk, dv out; log_alpha, sigma dL, P_L,
+    # db1 in; dlog_alpha out; adjoint pairs in
+    sk = (BH * 12 * m * d * R,
+          BH * T * (8 * d * e + 4 * m + 4 * m) + BH * R * (2 * 2 * m + 4 * m) + BH * tiles * 2 * pair)
     k = {
         # name: (algorithmic flops, algorithmic bytes) per launch; the tensor-core
         # (bf16) and SIMT (fp32) kernels of the same step share a model
@@ -76,15 +96,19 @@ def work_model(wl):
         # fused chunk scan (K, V, U in; the bf16 states entering each chunk out)
         "state_gates": (0, BH * R * (4 * m + 128)),
         "state_scan": (BH * 4 * m * d * R, BH * R * (2 * d * e + 128) + BH * ((R + 63) // 64) * 4 * m * d),
-        # reverse adjoint scan + carry: fp32 contributions and fp32 states in,
+        # reverse adjoint scan + carry: fp32 contributions and bf16 states in,
         # bf16 adjoints out, K and V
-        "adj_scan": (0, BH * ((R + 63) // 64) * m * d * 20),
+        "adj_scan": (0, BH * ((R + 63) // 64) * m * d * 16),
         "bwd_wdq_tc": wdq, "bwd_window_dq": wdq,
         "bwd_wkv_tc": wkv, "bwd_window_dkdv": wkv,
         "bwd_sq_tc": sq, "bwd_slot_query": sq,
         "bwd_sk_tc": sk, "bwd_slot_key": sk,
     }
-    return dict(fwd_flops=fwd_flops, fwd_bytes=fwd_bytes, step_flops=3.5 * fwd_flops,
+    # fwd + bwd flops: the forward's and the backward's kernels (the states are
+    # formed in both passes)
+    step_flops = (k["fwd_tc"][0] + 2 * k["state_scan"][0] + k["bwd_wdq_tc"][0] + k["bwd_wkv_tc"][0]
+                  + k["bwd_sq_tc"][0] + k["bwd_sk_tc"][0])
+    return dict(fwd_flops=fwd_flops, fwd_bytes=fwd_bytes, step_flops=step_flops,
                 step_bytes=fwd_bytes + bwd_bytes, kernels=k, n_sum=n_sum, R=R)
 
 
@@ -379,8 +403,11 @@ def run_nha(args, wl, wl_key):
         peaks = load_peaks()
         tokens = world * B * T
         value = tokens / (ms / 1e3)
-        # dominant kernel by measured time share
-        name, (cnt, tot) = max(prof.items(), key=lambda kv: kv[1][1])
+        # dominant kernel: the largest measured time among the kernels on the
+        # caller's stream (the side-stream kernels run beside others, so their
+        # durations include the sharing of the SMs)
+        main_prof = {k: v for k, v in prof.items() if k not in SIDE_STREAM_KERNELS} or prof
+        name, (cnt, tot) = max(main_prof.items(), key=lambda kv: kv[1][1])
         per_launch_ms = tot / cnt
         flops, nbytes = model["kernels"].get(name, (model["step_flops"], model["step_bytes"]))
         t_tc = flops / (peaks["bf16_tflops"] * 1e12)
