@@ -22,40 +22,58 @@
 
 namespace nha {
 
-// U row j (64 bf16) and G of the two chunks of a 128-row tile.
+// U row j (64 bf16) and G of the two chunks of a 128-row tile: log_alpha of
+// the tile by TMA, U staged in shared memory and copied out coalesced.
 template <int M>
 __global__ void __launch_bounds__(kTcThreads)
-state_gates_kernel(const float* __restrict__ la, __nv_bfloat16* __restrict__ U, float* __restrict__ G, Shape sh) {
-    constexpr int HM = M / 2;
+state_gates_kernel(const __grid_constant__ CUtensorMap la_map, __nv_bfloat16* __restrict__ U,
+                   float* __restrict__ G, Shape sh, int* __restrict__ status) {
+    constexpr int HM = M / 2, LAB = ((M + 31) / 32) * 16384;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* XL = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char* XU = XL + LAB;  // [128][64] bf16, 128-byte swizzled rows
     __shared__ float s_tot[4 * M];
     __shared__ float sG[2 * M];
+    __shared__ uint64_t gbar;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
     const int bh = blockIdx.y, j0 = blockIdx.x * 128, n = max(0, min(128, sh.R - j0));
     const int rows = min(128, sh.NC * kChunk - j0);  // rows of U this tile defines
     const bool row_ok = r < n;
-    const size_t hoff = (size_t)bh * sh.T;
     if (tid < 2 * M) sG[tid] = 0.0f;
+    if (tid == 0) {
+        mbar_init(&gbar, 1);
+        mbar_fence_init();
+    }
     __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&gbar, LAB);
+#pragma unroll
+        for (int xx = 0; xx < M; xx += 32) tma_load_3d(XL + xx * 512, &la_map, xx, j0, bh, &gbar);
+    }
+    if (!mbar_wait(&gbar, 0, kWaitCycles)) {
+        if (tid == 0) atomicExch(status, kStatusTimeout);
+        mbar_wait(&gbar, 0, kWaitCycles);  // let the copy land before the CTA leaves
+        return;
+    }
     float l[HM], b[HM];
-    row_gates<M>(la + (hoff + j0 + (row_ok ? r : 0)) * M, row_ok, l, b, s_tot, sG, warp, lane, h, r, n);
-    if (r < rows) {
+    row_gates_tile<M>(XL, row_ok, l, b, s_tot, sG, warp, lane, h, r, n);
+    {
         float u[HM];
 #pragma unroll
         for (int jj = 0; jj < HM; jj++) u[jj] = row_ok ? fexp(sG[cr * M + h * HM + jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
-        __nv_bfloat16* ur = U + ((size_t)bh * sh.NC * kChunk + j0 + r) * 64;
-#pragma unroll
-        for (int jj = 0; jj < HM; jj += 8) *reinterpret_cast<uint4*>(ur + h * HM + jj) = pack8(u + jj);
-        if (M < 64) {
-            constexpr int PAD = (64 - M) / 2;
-#pragma unroll
-            for (int jj = 0; jj < PAD; jj += 8)
-                *reinterpret_cast<uint4*>(ur + M + h * PAD + jj) = make_uint4(0, 0, 0, 0);
-        }
+        store_row(XU, r, h * HM, u, HM);
+        if (M < 64) zero_cols(XU, r, M + h * (64 - M) / 2, M + (h + 1) * (64 - M) / 2);
     }
     if (tid < 2 * M) {
         const int cc = tid / M, c = j0 / kChunk + cc;
         if (c < sh.NC) G[((size_t)bh * sh.NC + c) * M + (tid % M)] = sG[tid];
+    }
+    __syncthreads();
+    __nv_bfloat16* ub = U + ((size_t)bh * sh.NC * kChunk + j0) * 64;
+    for (int e = tid; e < rows * 8; e += kTcThreads) {
+        const int rr = e >> 3, ch = e & 7;
+        *reinterpret_cast<uint4*>(ub + (size_t)rr * 64 + ch * 8) = *reinterpret_cast<const uint4*>(XU + sw_chunk(rr, ch, 128));
     }
 }
 
@@ -72,6 +90,7 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
                      float* __restrict__ SV, __nv_bfloat16* __restrict__ SKb, __nv_bfloat16* __restrict__ SVb,
                      Shape sh, int want_f32, int* __restrict__ status) {
     constexpr int NS = kScanStages;
+    constexpr int NSL = M;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     // stage s: X_c [64 tokens][128 d] (d >= D zero), U_c [64 tokens][64], G_c [M]
@@ -83,7 +102,7 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x, tz = blockIdx.y;  // tz 0: K, 1: V
+    const int bh = blockIdx.x, tz = blockIdx.y, i0 = 0;  // tz 0: K, 1: V
     const int NC = sh.NC;
     volatile int* abort = &s_abort;
     if (tid == 0) {
@@ -133,7 +152,7 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
                 const uint32_t sx = smem_u32(XT(st)), su = smem_u32(UT(st));
                 for (int kk = 0; kk < 4; kk++)
                     mma_bf16(tm + 64 * (c & 1), desc_mn(sx, 64, kk), desc_mn(su, 64, kk),
-                             idesc_bf16(128, M, true) | (1u << 15), kk > 0);
+                             idesc_bf16(128, NSL, true) | (1u << 15), kk > 0);
                 mma_commit(&sfull[c & 1]);
                 if (c >= 1 && c - 1 + NS < NC) {  // chunk c - 1 fully consumed: refill its stage
                     if (!mbar_wait_ab(&empty[(c - 1) % NS], ((c - 1) / NS) & 1, kWaitCycles, abort)) break;
@@ -145,33 +164,33 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
         // ---------------- state warps: thread = column d ----------------
         const int d = tid;
         const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);
-        __nv_bfloat16* Sb = (tz == 0 ? SKb : SVb) + (size_t)bh * NC * M * D + d;
-        float* Sf = (tz == 0 ? SK : SV) + (size_t)bh * NC * M * D + d;
-        float S[M];
+        __nv_bfloat16* Sb = (tz == 0 ? SKb : SVb) + (size_t)bh * NC * M * D + (size_t)i0 * D + d;
+        float* Sf = (tz == 0 ? SK : SV) + (size_t)bh * NC * M * D + (size_t)i0 * D + d;
+        float S[NSL];
 #pragma unroll
-        for (int i = 0; i < M; i++) S[i] = 0.0f;
+        for (int i = 0; i < NSL; i++) S[i] = 0.0f;
         for (int c = 0; c < NC; c++) {
             const int st = c % NS, b = c & 1;
             if (!mbar_wait_ab(&sfull[b], (c >> 1) & 1, kWaitCycles, abort) ||
                 !mbar_wait_ab(&full[st], (c / NS) & 1, kWaitCycles, abort))
                 break;
             fence_after_sync();
-            float dS[M];
-            tmem_ld(tl + 64 * b, dS, M);
+            float dS[NSL];
+            tmem_ld(tl + 64 * b, dS, NSL);
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tfree[b]);
             if (d < D) {
                 const size_t o = (size_t)c * M * D;
 #pragma unroll
-                for (int i = 0; i < M; i++) Sb[o + (size_t)i * D] = __float2bfloat16_rn(S[i]);
+                for (int i = 0; i < NSL; i++) Sb[o + (size_t)i * D] = __float2bfloat16_rn(S[i]);
                 if (want_f32)
 #pragma unroll
-                    for (int i = 0; i < M; i++) Sf[o + (size_t)i * D] = S[i];
+                    for (int i = 0; i < NSL; i++) Sf[o + (size_t)i * D] = S[i];
             }
-            const float* g = GS(st);
+            const float* g = GS(st) + i0;
 #pragma unroll
-            for (int i = 0; i < M; i++) S[i] = fexp(g[i]) * S[i] + dS[i];
+            for (int i = 0; i < NSL; i++) S[i] = fexp(g[i]) * S[i] + dS[i];
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
         }
@@ -347,10 +366,18 @@ cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const floa
                       __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, __nv_bfloat16* U, bool want_f32,
                       const Shape& sh, int* status, cudaStream_t st) {
     if (sh.NC == 0) return cudaSuccess;
-    NHA_LAUNCH("state_gates", st,
-               state_gates_kernel<M><<<dim3((sh.NC * kChunk + 127) / 128, sh.BH), kTcThreads, 0, st>>>(la, U, G, sh));
-    cudaError_t e = cudaGetLastError();
+    CUtensorMap la_map;
+    cudaError_t e = tmap_rows_f32(&la_map, la, M, sh.T, sh.BH);
     if (e != cudaSuccess) return e;
+    {
+        const size_t gsm = 1024 + ((M + 31) / 32) * 16384 + 16384;
+        auto gk = state_gates_kernel<M>;
+        if ((e = cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsm)) != cudaSuccess)
+            return e;
+        NHA_LAUNCH("state_gates", st,
+                   gk<<<dim3((sh.NC * kChunk + 127) / 128, sh.BH), kTcThreads, gsm, st>>>(la_map, U, G, sh, status));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     StateMaps maps;
     if ((e = tmap_rows_bf16(&maps.x[0], k, D, sh.T, sh.BH, 64)) != cudaSuccess ||
         (e = tmap_rows_bf16(&maps.x[1], v, D, sh.T, sh.BH, 64)) != cudaSuccess ||
@@ -361,7 +388,8 @@ cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const floa
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) != cudaSuccess)
         return e;
     NHA_LAUNCH("state_scan", st,
-               kern<<<dim3(sh.BH, 2), kScanThreads, sm, st>>>(maps, G, SK, SV, SKb, SVb, sh, want_f32 ? 1 : 0, status));
+               kern<<<dim3(sh.BH, 2), kScanThreads, sm, st>>>(maps, G, SK, SV, SKb, SVb, sh, want_f32 ? 1 : 0,
+                                                              status));
     return cudaGetLastError();
 }
 
