@@ -104,11 +104,9 @@ def work_model(wl):
         "bwd_sq_tc": sq, "bwd_slot_query": sq,
         "bwd_sk_tc": sk, "bwd_slot_key": sk,
     }
-    # fwd + bwd flops: the forward's and the backward's kernels (the states are
-    # formed in both passes)
-    step_flops = (k["fwd_tc"][0] + 2 * k["state_scan"][0] + k["bwd_wdq_tc"][0] + k["bwd_wkv_tc"][0]
-                  + k["bwd_sq_tc"][0] + k["bwd_sk_tc"][0])
-    return dict(fwd_flops=fwd_flops, fwd_bytes=fwd_bytes, step_flops=step_flops,
+    # fwd + bwd flops: 3.5 x the forward (the FlashAttention convention: the
+    # backward counts 2.5 forwards)
+    return dict(fwd_flops=fwd_flops, fwd_bytes=fwd_bytes, step_flops=3.5 * fwd_flops,
                 step_bytes=fwd_bytes + bwd_bytes, kernels=k, n_sum=n_sum, R=R)
 
 
@@ -361,7 +359,22 @@ def run_nha(args, wl, wl_key):
     fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     ms = statistics.mean(step_ms)
     ms_fwd = statistics.mean(fwd_ms)
-    ms, ms_fwd = max_over_ranks([ms, ms_fwd], device=dev)
+    ms_med = statistics.median(step_ms)
+    ms, ms_fwd, ms_med = max_over_ranks([ms, ms_fwd, ms_med], device=dev)
+
+    # the same steps back to back without the L2 flush (inputs may stay in L2)
+    K2 = max(3, min(K, 100))
+    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K2)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(K2):
+        ev2[i][0].record(stream)
+        step(ev2[i][1])
+        ev2[i][2].record(stream)
+    torch.cuda.synchronize()
+    ms_unfl = statistics.median(ev2[i][0].elapsed_time(ev2[i][2]) for i in range(K2))
+    ms_unfl_fwd = statistics.median(ev2[i][0].elapsed_time(ev2[i][1]) for i in range(K2))
+    ms_unfl, ms_unfl_fwd = max_over_ranks([ms_unfl, ms_unfl_fwd], device=dev)
 
     # ---- end to end through the public API with pinned host buffers
     hin = {n: t.pin_memory() for n, t in x.items()}
@@ -442,6 +455,9 @@ def run_nha(args, wl, wl_key):
             "fwd": {"ms": ms_fwd, "tokens_per_s": tokens / (ms_fwd / 1e3),
                     "roofline_frac": t_roof_fwd / (ms_fwd / 1e3)},
             "step_roofline_frac": t_roof_step / (ms / 1e3),
+            "median_ms_per_step": ms_med,
+            "unflushed": {"ms_per_step": ms_unfl, "fwd_ms": ms_unfl_fwd, "steps": K2,
+                          "note": "median of back-to-back steps without the L2 flush"},
             "roofline": roof,
             "kernels": {k: {"launches": c, "ms_per_launch": t / c, "share": t / total_prof}
                         for k, (c, t) in sorted(prof.items(), key=lambda kv: -kv[1][1])},

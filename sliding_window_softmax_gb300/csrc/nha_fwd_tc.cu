@@ -31,7 +31,8 @@ using namespace tc;
 constexpr int kFwdThreads = 288, kFwdStages = 3;
 
 struct FwdMaps {
-    CUtensorMap q, k, v, la;
+    CUtensorMap q, k, v, la;  // RoPE(q), RoPE(k) and v rows (window); log_alpha rows
+    CUtensorMap qs, ks, sk, sv;  // q, k rows and [S^K], [S^V] pairs (slot branch)
 };
 
 template <int D, int M>
@@ -53,7 +54,7 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
     float* sG = s_tot + 4 * M;                             // [2][M]
     float* redm = sG + 2 * M;                              // [2][128]
     float* reds = redm + 256;                              // [2][128]
-    __shared__ uint64_t bar, gbar, qbar, full[NS], sfull[2], pready, bdone[2], drain[2];
+    __shared__ uint64_t bar, gbar, sbar, qbar, full[NS], sfull[2], pready, bdone[2], drain[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -80,6 +81,7 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
     if (tid == 0) {
         mbar_init(&bar, 1);
         mbar_init(&gbar, 1);
+        mbar_init(&sbar, 1);
         mbar_init(&qbar, 1);
         for (int q = 0; q < NS; q++) mbar_init(&full[q], 1);
         for (int q = 0; q < 2; q++) {
@@ -101,6 +103,7 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
     // keys of every window block) at 256, O_1 (the other 64 keys) at 256 + D
     const uint32_t tA = 0, tO = 256, tO1 = 256 + D;
 
+    int s_issued = 0;  // thread 0: slot-branch operand copies issued (phases of sbar)
     int last_ph[NS];  // producer: phase of the last load issued into each stage
 #pragma unroll
     for (int q = 0; q < NS; q++) last_ph[q] = -1;
@@ -160,9 +163,6 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
         // ---------------- tile threads (warps 0-7) ----------------
         const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
         const bool row_ok = r < nq;
-        const __nv_bfloat16* q = (const __nv_bfloat16*)a.q + hoff * D;
-        const __nv_bfloat16* k = (const __nv_bfloat16*)a.k + hoff * D;
-        const __nv_bfloat16* v = (const __nv_bfloat16*)a.v + hoff * D;
         const float sig2 = sh.sigma * kLog2e;
         const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lanes
         if (tid < 2 * M) sG[tid] = 0.0f;
@@ -176,14 +176,20 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
 
         if (slot) {
             const int c1 = j0 / kChunk;
-            const bool has2 = nq > kChunk;
-            const __nv_bfloat16* SK1 = a.SKb + ((size_t)bh * sh.NC + c1) * M * D;
-            const __nv_bfloat16* SV1 = a.SVb + ((size_t)bh * sh.NC + c1) * M * D;
-            load_tile_async<D>(q, tbase, nq, X0);
-            load_tile_async<D>(k, j0, nq, KB[0]);
-            load_tile_async<D>(v, j0, nq, VB[0]);
-            load_state_pair_async<D, M>(SK1, has2 ? SK1 + M * D : nullptr, KB[1]);
-            cp_async_commit();
+            // operand tiles by TMA (thread 0): q, k_c, v_c rows and the [S^K] pair.
+            // Rows past the tile's states are other rows or zeros; the masks and
+            // zero gates keep them out of every product.
+            if (tid == 0) {
+                s_issued = 1;
+                mbar_arrive_expect_tx(&sbar, 3 * TB + 2 * M * D * 2);
+#pragma unroll
+                for (int xx = 0; xx < D; xx += 64) {
+                    tma_load_3d(X0 + xx * 256, &maps.qs, xx, tbase, bh, &sbar);
+                    tma_load_3d(KB[0] + xx * 256, &maps.ks, xx, j0, bh, &sbar);
+                    tma_load_3d(VB[0] + xx * 256, &maps.v, xx, j0, bh, &sbar);
+                    tma_load_3d(KB[1] + xx * 4 * M, &maps.sk, xx, c1 * M, bh, &sbar);
+                }
+            }
             if (tid == 0) {  // log_alpha rows by TMA into the last stage's K~ buffer (idle here)
                 mbar_arrive_expect_tx(&gbar, (uint32_t)(((M + 31) / 32) * 16384));
 #pragma unroll
@@ -201,9 +207,10 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
                 }
                 store_row(VB[1], r, h * HM, ek, HM);
             }
-            cp_async_wait<0>();
             sync_for_mma<true>();
             if (tid == 0) {
+                if (!mbar_wait(&sbar, 0, kWaitCycles)) *abort = 1;
+                fence_after_sync();
                 const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[0]), s3 = smem_u32(KB[1]);
                 for (int kk = 0; kk < D / 16; kk++)
                     mma_bf16(tm + tA, desc_k(s0, 128, kk), desc_k(s1, 128, kk), idesc_bf16(128, 128, false), kk > 0);
@@ -215,8 +222,12 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
             if (ok) {
                 // A = Q K_c^T masked to the row's own chunk and s <= r; [S^V] replaces [S^K]
                 mask_to_tile(tl + tA, KB[0], r, h, cr, row_ok, false);
-                load_state_pair_async<D, M>(SV1, has2 ? SV1 + M * D : nullptr, KB[1]);
-                cp_async_commit();
+                if (tid == 0) {  // [S^K] consumed: the [S^V] pair in flight
+                    s_issued = 2;
+                    mbar_arrive_expect_tx(&sbar, 2 * M * D * 2);
+#pragma unroll
+                    for (int xx = 0; xx < D; xx += 64) tma_load_3d(KB[1] + xx * 4 * M, &maps.sv, xx, c1 * M, bh, &sbar);
+                }
                 sync_for_mma<true>();
                 if (tid == 0) {
                     const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[1]);
@@ -255,9 +266,10 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
                 store_row(VB[1] + 16384, r, h * HM, pq, HM);  // pEq, after Ek
                 named_sync(1, kTcThreads);
                 l = reds[r] + reds[128 + r];
-                cp_async_wait<0>();  // [S^V] pair
                 sync_for_mma<true>();
                 if (tid == 0) {
+                    if (!mbar_wait(&sbar, 1, kWaitCycles)) *abort = 1;  // the [S^V] pair
+                    fence_after_sync();
                     const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[1]), s3 = smem_u32(KB[1]);
                     for (int kk = 0; kk < 2 * M / 16; kk++)
                         mma_bf16(tm + tO, desc_k(s1, 128, kk), desc_mn(s3, 2 * M, kk), idesc_bf16(128, D, true), kk > 0);
@@ -398,6 +410,7 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
             mma_commit(&drain[0]);
             mbar_wait(&drain[0], 0, kWaitCycles);
             if (slot) mbar_wait(&gbar, 0, kWaitCycles);
+            for (int q = 0; q < s_issued; q++) mbar_wait(&sbar, (uint32_t)q, kWaitCycles);
         }
         if (warp == 8 && lane == 0) {  // window MMAs and copies
             mma_commit(&drain[1]);
@@ -515,7 +528,11 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bf
     if ((e = tmap_rows_bf16(&maps.q, qr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
         (e = tmap_rows_bf16(&maps.k, kr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
         (e = tmap_rows_bf16(&maps.v, a.v, D, sh.T, sh.BH, 128)) != cudaSuccess ||
-        (e = tmap_rows_f32(&maps.la, a.la, M, sh.T, sh.BH)) != cudaSuccess)
+        (e = tmap_rows_f32(&maps.la, a.la, M, sh.T, sh.BH)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.qs, a.q, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.ks, a.k, D, sh.T, sh.BH, 128)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.sk, a.SKb, D, (sh.NC > 0 ? sh.NC : 1) * M, sh.BH, 2 * M)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.sv, a.SVb, D, (sh.NC > 0 ? sh.NC : 1) * M, sh.BH, 2 * M)) != cudaSuccess)
         return e;
     const size_t sm = tc_fwd_smem<D, M>();
     auto kern = fwd_tc_kernel<D, M>;

@@ -454,7 +454,6 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         return;
     }
     const int c1 = sbase / kChunk;
-    const bool has2 = nc > kChunk;
     const size_t jrow = (size_t)bh * sh.NC * kChunk + s;
 
     if (tid < 2 * M) sG[tid] = 0.0f;
