@@ -518,19 +518,17 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
     }
     float l[HM], b[HM];
     row_gates_tile<M>(XM1, slot_ok, l, b, s_tot, sG, warp, lane, h, r, nc);
-    float rho[HM], eG[HM];
+    // bq = b - rho (rho = G / 2) is all the passes need of b; exp(G - rho) = exp(rho)
+    // comes back from the chunk totals in shared memory when it is used
+    const float* Grow = sG + cr * M + h * HM;
 #pragma unroll
-    for (int jj = 0; jj < HM; jj++) {
-        const float G = sG[cr * M + h * HM + jj];
-        rho[jj] = 0.5f * G;
-        eG[jj] = fexp(0.5f * G);
-    }
+    for (int jj = 0; jj < HM; jj++) b[jj] -= 0.5f * Grow[jj];
     {
         float ek[HM], eke[HM], z[HM];
 #pragma unroll
         for (int jj = 0; jj < HM; jj++) {
-            ek[jj] = slot_ok ? fexp(rho[jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
-            eke[jj] = ek[jj] * eG[jj];
+            ek[jj] = slot_ok ? fexp(-b[jj]) * (-expm1f(l[jj])) : 0.0f;
+            eke[jj] = ek[jj] * fexp(0.5f * Grow[jj]);
             z[jj] = 0.0f;
         }
         store_row(XE, r, h * HM, ek, HM);
@@ -561,7 +559,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
                     for (int q = 0; q < 8; q++) w8[q] = 0.0f;
                 }
 #pragma unroll
-                for (int q = 0; q < 8; q++) weq[jj + q] = w8[q] * fexp(b[jj + q] - rho[jj + q]);
+                for (int q = 0; q < 8; q++) weq[jj + q] = w8[q] * fexp(b[jj + q]);
             }
             store_row(XW, r, h * HM, weq, HM);
         }
@@ -618,7 +616,8 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
             float intra[HM];
             tmem_ld(tl + R0 + h * HM, intra, HM);
 #pragma unroll
-            for (int jj = 0; jj < HM; jj++) du[jj] += fexp(rho[jj] - b[jj]) * (intra[jj] + eG[jj] * inter[jj]);
+            for (int jj = 0; jj < HM; jj++)
+                du[jj] += fexp(-b[jj]) * (intra[jj] + fexp(0.5f * Grow[jj]) * inter[jj]);
         }
         // dk (dv) = window partial + slot part, staged in XM2, written by TMA
         if (mbar_wait(&ebar, (uint32_t)pass, kWaitCycles)) {
