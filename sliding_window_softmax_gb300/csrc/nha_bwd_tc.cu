@@ -25,56 +25,6 @@
 
 namespace nha {
 
-// dot of two bf16 half rows (columns [h D/2, (h + 1) D/2))
-template <int D>
-__device__ __forceinline__ float half_row_dot(const __nv_bfloat16* __restrict__ x,
-                                              const __nv_bfloat16* __restrict__ y, int h) {
-    constexpr int HD = D / 2;
-    float s = 0.0f;
-#pragma unroll
-    for (int c = 0; c < HD; c += 8) {
-        float fx[8], fy[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(x + h * HD + c)), fx);
-        unpack8(__ldg(reinterpret_cast<const uint4*>(y + h * HD + c)), fy);
-#pragma unroll
-        for (int i = 0; i < 8; i++) s += fx[i] * fy[i];
-    }
-    return s;
-}
-
-// Epilogue shared by both kernels: read the rotated-space gradient of this
-// row from TMEM columns [col0, col0 + D), scale, rotate back by R_pos^T and
-// write bf16.  Thread half h owns frequency pairs [h D/4, (h + 1) D/4).
-template <int D>
-__device__ __forceinline__ void store_unrotated(uint32_t taddr, bool valid_acc, float scale, int pos,
-                                                bool row_ok, int h, const float2* __restrict__ tab,
-                                                __nv_bfloat16* __restrict__ out) {
-    constexpr int Q4 = D / 4, H = D / 2;
-    float g0[Q4], g1[Q4];
-    if (valid_acc) {
-        tmem_ld(taddr + h * Q4, g0, Q4);
-        tmem_ld(taddr + H + h * Q4, g1, Q4);
-    } else {
-#pragma unroll
-        for (int i = 0; i < Q4; i++) g0[i] = g1[i] = 0.0f;
-    }
-    if (!row_ok) return;
-    const float2* cs = tab + (size_t)pos * H + h * Q4;
-#pragma unroll
-    for (int i = 0; i < Q4; i += 8) {
-        float r0[8], r1[8];
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const float2 c = __ldg(cs + i + j);
-            const float a = g0[i + j] * scale, b = g1[i + j] * scale;
-            r0[j] = a * c.x + b * c.y;
-            r1[j] = b * c.x - a * c.y;
-        }
-        *reinterpret_cast<uint4*>(out + h * Q4 + i) = pack8(r0);
-        *reinterpret_cast<uint4*>(out + H + h * Q4 + i) = pack8(r1);
-    }
-}
-
 // ---------------------------------------------------------------------------------------
 // Query-major: one CTA per (128 queries, head).  Warp 8 is the producer: TMA
 // copies of the RoPE(q), dout and o tiles and of 128-key blocks of RoPE(k), v

@@ -125,20 +125,15 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
 template <int D>
 cudaError_t launch_wkv(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bfloat16* kr, const float2* tab,
                        int* status, cudaStream_t st);
-cudaError_t launch_state_scan_rev(const BwdArgs& a, int M, int D, cudaStream_t st);
 // bf16 path: reverse adjoint scan (RK, RV contributions in; RKb, RVb out) and
 // the per-chunk dlog_alpha carry, added to wsDB1 of each chunk's last state row.
 cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st);
-cudaError_t launch_dla_carry(const BwdArgs& a, int M, int D, cudaStream_t st);
-// bf16 path: chunk coefficients U (workspace, [BH][NC * C][64] bf16) and
-// totals G, then the states entering every chunk in bf16 (and fp32 if want_f32).
+// bf16 path: chunk coefficients U (workspace, [BH][NC * C][64] bf16) and chunk
+// decays exp(G) (into G), then the states entering every chunk in bf16 (and
+// fp32 if want_f32).
 template <int D, int M>
 cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const float* la, float* SK, float* SV,
                       __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, __nv_bfloat16* U, bool want_f32,
                       const Shape& sh, int* status, cudaStream_t st);
-// Chunk scan (dir > 0: states before each chunk; dir < 0: adjoints carried in),
-// fp32 in place plus a bf16 copy in B0 / B1.
-cudaError_t launch_scan8(float* X0, float* X1, __nv_bfloat16* B0, __nv_bfloat16* B1, const float* G,
-                         const Shape& sh, int M, int D, int dir, cudaStream_t st);
 
 }  // namespace nha

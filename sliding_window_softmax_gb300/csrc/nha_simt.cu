@@ -832,24 +832,6 @@ cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st) {
     return simt_bwd_slot<Tin, D, M>(a, st);
 }
 
-cudaError_t launch_state_scan_rev(const BwdArgs& a, int M, int D, cudaStream_t st) {
-    NHA_LAUNCH("state_scan_rev", st,
-               state_scan_kernel<<<dim3((M * D + kThreads - 1) / kThreads, a.sh.BH, 2), kThreads, 0, st>>>(
-                   a.RK, a.RV, a.G, a.sh.NC, M, D, -1));
-    return cudaGetLastError();
-}
-
-cudaError_t launch_dla_carry(const BwdArgs& a, int M, int D, cudaStream_t st) {
-    const dim3 grid(a.sh.NC, a.sh.BH);
-    switch (M) {
-        case 16: NHA_LAUNCH("bwd_dla_carry", st, bwd_dla_carry_kernel<16><<<grid, kThreads, 0, st>>>(a, D)); break;
-        case 32: NHA_LAUNCH("bwd_dla_carry", st, bwd_dla_carry_kernel<32><<<grid, kThreads, 0, st>>>(a, D)); break;
-        case 64: NHA_LAUNCH("bwd_dla_carry", st, bwd_dla_carry_kernel<64><<<grid, kThreads, 0, st>>>(a, D)); break;
-        default: return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
-}
-
 #define NHA_INST(Tin, D, M)                                                          \
     template cudaError_t simt_states<Tin, D, M>(const Tin*, const Tin*, const float*, float*, \
                                                 float*, float*, const Shape&, cudaStream_t); \

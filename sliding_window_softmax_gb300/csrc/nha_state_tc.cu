@@ -8,7 +8,8 @@
 // chunks follow S_prev(c + 1) = exp(G_c) S_prev(c) + dS_c.
 //
 // Two kernels.  state_gates: every chunk in parallel, the coefficients U
-// (bf16, 64 columns, slots past m zero) and the chunk totals G.  state_scan:
+// (bf16, 64 columns, slots past m zero) and the chunk decays exp(G) (the array
+// named G holds exp(G_c) on this path: the scans use nothing else of it).  state_scan:
 // one CTA per (head, K or V) walks the chunks in order; a producer warp
 // streams X_c and U_c through TMA stages and forms dS_c^T = X_c^T U_c on the
 // tensor core into one of two TMEM buffers, while four warps (thread = one
@@ -67,7 +68,7 @@ state_gates_kernel(const __grid_constant__ CUtensorMap la_map, __nv_bfloat16* __
     }
     if (tid < 2 * M) {
         const int cc = tid / M, c = j0 / kChunk + cc;
-        if (c < sh.NC) G[((size_t)bh * sh.NC + c) * M + (tid % M)] = sG[tid];
+        if (c < sh.NC) G[((size_t)bh * sh.NC + c) * M + (tid % M)] = fexp(sG[tid]);  // exp(G_c)
     }
     __syncthreads();
     __nv_bfloat16* ub = U + ((size_t)bh * sh.NC * kChunk + j0) * 64;
@@ -180,17 +181,25 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tfree[b]);
-            if (d < D) {
+            {
+                // bf16 copies: lanes d, d ^ 1 swap one value so that each stores a
+                // packed pair (columns d & ~1, d | 1) of slot i (even lane) or i + 1 (odd)
                 const size_t o = (size_t)c * M * D;
+                const bool odd = lane & 1;
 #pragma unroll
-                for (int i = 0; i < NSL; i++) Sb[o + (size_t)i * D] = __float2bfloat16_rn(S[i]);
-                if (want_f32)
+                for (int i = 0; i < NSL; i += 2) {
+                    const float recv = __shfl_xor_sync(0xffffffffu, odd ? S[i] : S[i + 1], 1);
+                    const uint32_t pk = odd ? pack_bf16(recv, S[i + 1]) : pack_bf16(S[i], recv);
+                    if (d < D)
+                        *reinterpret_cast<uint32_t*>(Sb + o + (size_t)(i + (odd ? 1 : 0)) * D - (odd ? 1 : 0)) = pk;
+                }
+                if (want_f32 && d < D)
 #pragma unroll
                     for (int i = 0; i < NSL; i++) Sf[o + (size_t)i * D] = S[i];
             }
-            const float* g = GS(st) + i0;
+            const float* g = GS(st) + i0;  // exp(G_c)
 #pragma unroll
-            for (int i = 0; i < NSL; i++) S[i] = fexp(g[i]) * S[i] + dS[i];
+            for (int i = 0; i < NSL; i++) S[i] = g[i] * S[i] + dS[i];
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
         }
@@ -261,11 +270,15 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
     auto process = [&](int c, const float (&x)[SG], const float (&sp)[SG], const float (&g)[SG]) {
         const size_t o = at(c);
         float part[SG];
+        const bool odd = lane & 1;  // packed bf16 pairs, as in the state scan
 #pragma unroll
-        for (int i = 0; i < SG; i++) {
-            Xb[o + (size_t)i * D] = __float2bfloat16_rn(R[i]);
-            part[i] = R[i] * sp[i];
+        for (int i = 0; i < SG; i += 2) {
+            const float recv = __shfl_xor_sync(0xffffffffu, odd ? R[i] : R[i + 1], 1);
+            const uint32_t pk = odd ? pack_bf16(recv, R[i + 1]) : pack_bf16(R[i], recv);
+            *reinterpret_cast<uint32_t*>(Xb + o + (size_t)(i + (odd ? 1 : 0)) * D - (odd ? 1 : 0)) = pk;
         }
+#pragma unroll
+        for (int i = 0; i < SG; i++) part[i] = R[i] * sp[i];
 #pragma unroll
         for (int i = 0; i < SG; i++) {
 #pragma unroll
@@ -285,7 +298,7 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
         }
         parity ^= 1;
 #pragma unroll
-        for (int i = 0; i < SG; i++) R[i] = fexp(g[i]) * R[i] + x[i];
+        for (int i = 0; i < SG; i++) R[i] = g[i] * R[i] + x[i];  // g = exp(G_c)
     };
     float xa[SG], sa[SG], ga[SG], xb[SG], sb[SG], gb[SG];
     if (NC >= 1) load(NC - 1, xa, sa, ga);
@@ -309,55 +322,6 @@ cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st) {
     else
         NHA_LAUNCH("adj_scan", st,
                    adj_scan_kernel<64><<<grid, 128, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.wsDB1, sh, M));
-    return cudaGetLastError();
-}
-
-// Exclusive scan over chunks, in place (forward dir > 0 or reverse dir < 0),
-// eight chunks of loads in flight per thread.  Same contract as the scan of
-// the fp32 path; also writes a bf16 copy of every result (the operand the
-// tensor-core kernels load).
-__global__ void __launch_bounds__(256)
-state_scan8_kernel(float* __restrict__ X0, float* __restrict__ X1, __nv_bfloat16* __restrict__ B0,
-                   __nv_bfloat16* __restrict__ B1, const float* __restrict__ G, int NC, int M, int D, int dir) {
-    const int e = 2 * (blockIdx.x * 256 + threadIdx.x);  // two adjacent elements of one slot row
-    if (e >= M * D) return;
-    const int bh = blockIdx.y, i = e / D;
-    float* X = (blockIdx.z == 0) ? X0 : X1;
-    __nv_bfloat16* Xb = (blockIdx.z == 0) ? B0 : B1;
-    float2 S = make_float2(0.0f, 0.0f);
-    for (int n0 = 0; n0 < NC; n0 += 8) {
-        float2 x[8];
-        float g[8];
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            const int n = n0 + q;
-            const int c = dir > 0 ? n : NC - 1 - n;
-            if (n < NC) {
-                x[q] = *reinterpret_cast<const float2*>(X + ((size_t)bh * NC + c) * M * D + e);
-                g[q] = G[((size_t)bh * NC + c) * M + i];
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            const int n = n0 + q;
-            if (n < NC) {
-                const int c = dir > 0 ? n : NC - 1 - n;
-                const size_t o = ((size_t)bh * NC + c) * M * D + e;
-                *reinterpret_cast<float2*>(X + o) = S;
-                *reinterpret_cast<__nv_bfloat162*>(Xb + o) = __floats2bfloat162_rn(S.x, S.y);
-                const float f = expf(g[q]);
-                S.x = f * S.x + x[q].x;
-                S.y = f * S.y + x[q].y;
-            }
-        }
-    }
-}
-
-cudaError_t launch_scan8(float* X0, float* X1, __nv_bfloat16* B0, __nv_bfloat16* B1, const float* G,
-                         const Shape& sh, int M, int D, int dir, cudaStream_t st) {
-    NHA_LAUNCH(dir > 0 ? "state_scan" : "state_scan_rev", st,
-               state_scan8_kernel<<<dim3((M * D / 2 + 255) / 256, sh.BH, 2), 256, 0, st>>>(X0, X1, B0, B1, G,
-                                                                                           sh.NC, M, D, dir));
     return cudaGetLastError();
 }
 

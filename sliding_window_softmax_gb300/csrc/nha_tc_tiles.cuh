@@ -57,130 +57,6 @@ __device__ __forceinline__ void rotate8(float* x, float* y, const float2* __rest
     rotate8v(x, y, c);
 }
 
-// Rows [row0, row0 + n) of a [T][D] bf16 tensor into a 128-row swizzled tile;
-// rows >= n are zero.  With tab != nullptr the rows are rotated by RoPE at
-// absolute positions row0 + r.  Every thread issues all of its global loads
-// before it stores anything, so the load latency is paid once per tile.
-template <int D>
-__device__ void load_tile(const __nv_bfloat16* __restrict__ src, int row0, int n, unsigned char* tile,
-                          const float2* __restrict__ tab) {
-    constexpr int CH = D / 8, H = D / 2, CHH = CH / 2;
-    if (tab == nullptr) {
-        constexpr int IT = 128 * CH / kTcThreads;
-        uint4 buf[IT];
-#pragma unroll
-        for (int it = 0; it < IT; it++) {
-            const int e = threadIdx.x + it * kTcThreads, r = e / CH, ch = e % CH;
-            buf[it] = r < n ? __ldg(reinterpret_cast<const uint4*>(src + (size_t)(row0 + r) * D + ch * 8))
-                            : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int it = 0; it < IT; it++) {
-            const int e = threadIdx.x + it * kTcThreads, r = e / CH, ch = e % CH;
-            *reinterpret_cast<uint4*>(tile + sw_chunk(r, ch, 128)) = buf[it];
-        }
-    } else {
-        constexpr int IT = 128 * CHH / kTcThreads;
-        uint4 bx[IT], by[IT];
-        float4 cs[IT][4];
-#pragma unroll
-        for (int it = 0; it < IT; it++) {
-            const int e = threadIdx.x + it * kTcThreads, r = e / CHH, ch = e % CHH;
-            if (r < n) {
-                const __nv_bfloat16* row = src + (size_t)(row0 + r) * D;
-                bx[it] = __ldg(reinterpret_cast<const uint4*>(row + ch * 8));
-                by[it] = __ldg(reinterpret_cast<const uint4*>(row + H + ch * 8));
-                const float4* c4 = reinterpret_cast<const float4*>(tab + (size_t)(row0 + r) * H + ch * 8);
-#pragma unroll
-                for (int qq = 0; qq < 4; qq++) cs[it][qq] = __ldg(c4 + qq);
-            } else {
-                bx[it] = by[it] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                for (int qq = 0; qq < 4; qq++) cs[it][qq] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-#pragma unroll
-        for (int it = 0; it < IT; it++) {
-            const int e = threadIdx.x + it * kTcThreads, r = e / CHH, ch = e % CHH;
-            float x[8], y[8];
-            unpack8(bx[it], x);
-            unpack8(by[it], y);
-            rotate8v(x, y, cs[it]);
-            *reinterpret_cast<uint4*>(tile + sw_chunk(r, ch, 128)) = pack8(x);
-            *reinterpret_cast<uint4*>(tile + sw_chunk(r, ch + CHH, 128)) = pack8(y);
-        }
-    }
-}
-
-// Asynchronous form of load_tile without rotation: rows [row0, row0 + n) of
-// a [T][D] bf16 tensor into a `rows`-row swizzled tile with cp.async (rows >= n
-// zero-filled).  The caller commits / waits the group.  row0 must be a valid
-// row (it stands in as the address of the zero-filled rows).
-template <int D>
-__device__ __forceinline__ void load_tile_async(const __nv_bfloat16* __restrict__ src, int row0, int n,
-                                                unsigned char* tile, int rows = 128) {
-    constexpr int CH = D / 8;
-    for (int e = threadIdx.x; e < rows * CH; e += kTcThreads) {
-        const int r = e / CH, ch = e % CH;
-        const int rr = r < n ? r : 0;
-        cp_async16(tile + sw_chunk(r, ch, rows), src + (size_t)(row0 + rr) * D + ch * 8, r < n);
-    }
-}
-
-// Rotate rows [0, n) of a 128-row tile in place (positions row0 + r).
-template <int D>
-__device__ void rotate_tile(unsigned char* tile, int row0, int n, const float2* __restrict__ tab) {
-    constexpr int H = D / 2, CHH = D / 16;
-    for (int e = threadIdx.x; e < 128 * CHH; e += kTcThreads) {
-        const int r = e / CHH, ch = e % CHH;
-        if (r >= n) continue;
-        uint4* plo = reinterpret_cast<uint4*>(tile + sw_chunk(r, ch, 128));
-        uint4* phi = reinterpret_cast<uint4*>(tile + sw_chunk(r, ch + CHH, 128));
-        float x[8], y[8];
-        unpack8(*plo, x);
-        unpack8(*phi, y);
-        rotate8(x, y, tab + (size_t)(row0 + r) * H + ch * 8);
-        *plo = pack8(x);
-        *phi = pack8(y);
-    }
-}
-
-// [S1; S2] (fp32 [M][D] each, S2 may be null = zeros) into a 2M-row bf16 tile.
-template <int D, int M>
-__device__ void load_state_pair(const float* __restrict__ S1, const float* __restrict__ S2,
-                                unsigned char* tile) {
-    constexpr int CH = D / 8;
-    for (int e = threadIdx.x; e < 2 * M * CH; e += kTcThreads) {
-        const int r = e / CH, ch = e % CH;
-        const float* src = r < M ? S1 + (size_t)r * D : (S2 ? S2 + (size_t)(r - M) * D : nullptr);
-        float f[8];
-        if (src) {
-            const float4 a = __ldg(reinterpret_cast<const float4*>(src + ch * 8));
-            const float4 b = __ldg(reinterpret_cast<const float4*>(src + ch * 8 + 4));
-            f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-            f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; i++) f[i] = 0.0f;
-        }
-        *reinterpret_cast<uint4*>(tile + sw_chunk(r, ch, 2 * M)) = pack8(f);
-    }
-}
-
-// [S1; S2] from bf16 row-major [M][D] copies (S2 may be null = zeros) into a
-// 2M-row tile with cp.async; the caller commits / waits.
-template <int D, int M>
-__device__ __forceinline__ void load_state_pair_async(const __nv_bfloat16* __restrict__ S1,
-                                                      const __nv_bfloat16* __restrict__ S2, unsigned char* tile) {
-    constexpr int CH = D / 8;
-    for (int e = threadIdx.x; e < 2 * M * CH; e += kTcThreads) {
-        const int r = e / CH, ch = e % CH;
-        const bool valid = r < M || S2 != nullptr;
-        const __nv_bfloat16* src = (r < M ? S1 + (size_t)r * D : (S2 ? S2 + (size_t)(r - M) * D : S1)) + ch * 8;
-        cp_async16(tile + sw_chunk(r, ch, 2 * M), src, valid);
-    }
-}
-
 // Store n (multiple of 8) fp32 values as bf16 into row `row` of a 128-row tile
 // starting at column col0 (multiple of 8).
 __device__ __forceinline__ void store_row(unsigned char* tile, int row, int col0, const float* v, int n) {
@@ -214,19 +90,6 @@ struct TcCtl {
             return false;
         }
         return true;
-    }
-};
-
-// One mbarrier that tensor-core commits arrive on, with its own phase bit.
-// wait() blocks the calling thread only (no CTA barrier); false on timeout.
-struct TcBar {
-    uint64_t* bar;
-    uint32_t phase;
-    __device__ bool wait() {
-        const bool ok = mbar_wait(bar, phase, kWaitCycles);
-        phase ^= 1u;
-        fence_after_sync();
-        return ok;
     }
 };
 
