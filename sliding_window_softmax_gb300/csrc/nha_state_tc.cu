@@ -10,10 +10,11 @@
 // Two kernels.  state_gates: every chunk in parallel, the coefficients U
 // (bf16, 64 columns, slots past m zero) and the chunk decays exp(G) (the array
 // named G holds exp(G_c) on this path: the scans use nothing else of it).  state_scan:
-// one CTA per (head, K or V) walks the chunks in order; a producer warp
-// streams X_c and U_c through TMA stages and forms dS_c^T = X_c^T U_c on the
-// tensor core into one of two TMEM buffers, while four warps (thread = one
-// column d of the state) carry the state in fp32 registers and write S_prev(c).
+// one CTA per (head, K or V) walks the chunks in order: one warp streams X_c
+// and U_c through TMA stages, one forms dS_c^T = X_c^T U_c on the tensor core
+// into one of two TMEM buffers as soon as a chunk has landed, and four warps
+// (thread = one column d of the state) carry the state in fp32 registers and
+// write S_prev(c).
 #include "nha_common.cuh"
 #include "nha_kernels.h"
 #include "nha_prof.h"
@@ -78,7 +79,7 @@ state_gates_kernel(const __grid_constant__ CUtensorMap la_map, __nv_bfloat16* __
     }
 }
 
-constexpr int kScanThreads = 160, kScanStages = 4;
+constexpr int kScanThreads = 192, kScanStages = 4;  // 4 state warps, MMA warp, copy warp
 
 struct StateMaps {
     CUtensorMap x[2];  // K, V rows, box {64, 64}
@@ -133,7 +134,23 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
 #pragma unroll
     for (int q = 0; q < NS; q++) last_ph[q] = -1;
     if (warp == 4) {
-        // ---------------- producer (lane 0) ----------------
+        // ---------------- MMA issuer (lane 0): as soon as a chunk has landed and
+        // its TMEM buffer is read out ----------------
+        if (lane == 0) {
+            for (int c = 0; c < NC; c++) {
+                const int st = c % NS;
+                if (!mbar_wait_ab(&full[st], (c / NS) & 1, kWaitCycles, abort)) break;
+                if (c >= 2 && !mbar_wait_ab(&tfree[c & 1], ((c - 2) >> 1) & 1, kWaitCycles, abort)) break;
+                fence_after_sync();
+                const uint32_t sx = smem_u32(XT(st)), su = smem_u32(UT(st));
+                for (int kk = 0; kk < 4; kk++)
+                    mma_bf16(tm + 64 * (c & 1), desc_mn(sx, 64, kk), desc_mn(su, 64, kk),
+                             idesc_bf16(128, NSL, true) | (1u << 15), kk > 0);
+                mma_commit(&sfull[c & 1]);
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------- loader (lane 0): refills a stage once its chunk is consumed ----------------
         if (lane == 0) {
             auto load = [&](int c) {
                 const int st = c % NS;
@@ -145,20 +162,9 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
                 last_ph[st] = (c / NS) & 1;
             };
             for (int c = 0; c < min(NS, NC); c++) load(c);
-            for (int c = 0; c < NC; c++) {
-                const int st = c % NS;
-                if (!mbar_wait_ab(&full[st], (c / NS) & 1, kWaitCycles, abort)) break;
-                if (c >= 2 && !mbar_wait_ab(&tfree[c & 1], ((c - 2) >> 1) & 1, kWaitCycles, abort)) break;
-                fence_after_sync();
-                const uint32_t sx = smem_u32(XT(st)), su = smem_u32(UT(st));
-                for (int kk = 0; kk < 4; kk++)
-                    mma_bf16(tm + 64 * (c & 1), desc_mn(sx, 64, kk), desc_mn(su, 64, kk),
-                             idesc_bf16(128, NSL, true) | (1u << 15), kk > 0);
-                mma_commit(&sfull[c & 1]);
-                if (c >= 1 && c - 1 + NS < NC) {  // chunk c - 1 fully consumed: refill its stage
-                    if (!mbar_wait_ab(&empty[(c - 1) % NS], ((c - 1) / NS) & 1, kWaitCycles, abort)) break;
-                    load(c - 1 + NS);
-                }
+            for (int c = NS; c < NC; c++) {
+                if (!mbar_wait_ab(&empty[(c - NS) % NS], ((c - NS) / NS) & 1, kWaitCycles, abort)) break;
+                load(c);
             }
         }
     } else {
@@ -210,9 +216,10 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
         if (warp == 4 && lane == 0) {
             mma_commit(&drain);
             mbar_wait(&drain, 0, kWaitCycles);
+        }
+        if (warp == 5 && lane == 0)
             for (int q = 0; q < NS; q++)
                 if (last_ph[q] >= 0) mbar_wait(&full[q], (uint32_t)last_ph[q], kWaitCycles);
-        }
         __syncthreads();
         if (tid == 0) atomicExch(status, kStatusTimeout);
     }
