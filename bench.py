@@ -51,7 +51,7 @@ def workloads():
 
 
 # ----------------------------------------------------------------------------------------
-# Algorithmic work model (per launch).
+# Algorithmic work model: flops and bytes per launch, the roofline denominators.
 # kernels the library runs on its side stream, beside the caller's stream
 SIDE_STREAM_KERNELS = ("rope_qk", "adj_scan")
 
