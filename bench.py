@@ -17,6 +17,7 @@ this machine's host cores over a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -121,23 +122,46 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def source_hash() -> str:
+CSRC = os.path.join(ROOT, "sliding_window_softmax_gb300", "csrc")
+
+
+def kernel_source_hash(kernel: str, reader=None) -> str:
+    """Hash of the sources that define a kernel: the csrc .cu files that
+    launch a kernel under that name and the csrc headers they include, transitively.
+    ``reader(name) -> bytes`` reads a csrc file (default: the working tree)."""
+    if reader is None:
+        def reader(name):
+            with open(os.path.join(CSRC, name), "rb") as fh:
+                return fh.read()
+    names = sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
+    tag = ('NHA_LAUNCH("%s"' % kernel).encode()
+    todo = [f for f in names if tag in reader(f)]
+    if not todo:
+        return "none"
+    seen = []
+    while todo:
+        f = todo.pop()
+        if f in seen:
+            continue
+        seen.append(f)
+        for inc in re.findall(rb'#include "([^"]+)"', reader(f)):
+            inc = inc.decode()
+            if os.path.exists(os.path.join(CSRC, inc)):
+                todo.append(inc)
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "sliding_window_softmax_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in sorted(seen):
+        h.update(f.encode() + b"\0" + reader(f))
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, workload_key: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources (lines `traffic <kernel> <workload> <hash> <bytes>`)."""
+    the kernel's current sources (lines `traffic <kernel> <workload> <hash> <bytes>`,
+    the hash from kernel_source_hash)."""
     p = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(p):
         return None
-    cur = source_hash()
+    cur = kernel_source_hash(kernel)
     with open(p) as f:
         for line in f:
             mm = re.match(r"\s*traffic\s+(\S+)\s+(\S+)\s+(\S+)\s+([0-9.eE+]+)", line)
@@ -286,6 +310,101 @@ def run_reference(args, wl):
 
 
 # ----------------------------------------------------------------------------------------
+def decode_bytes(dw):
+    """Algorithmic bytes of one decode-step launch (one layer, all B*H heads)."""
+    d, m, w = dw.d, dw.m, dw.w
+    e = 2 if dw.dtype == "bf16" else 4
+    per_head = (16 * m * d                 # S^K, S^V read and written back, fp32
+                + 2 * d * e * max(w - 1, 0)  # window keys and values t-w+1 .. t-1 from the ring
+                + (2 * d * e + 4 * m) * (1 if dw.t >= w and w > 0 else 0)  # leaving token
+                + (2 * d * e + 4 * m) * (1 if w > 0 else 0)  # token t written into the ring
+                + 4 * d * e + 4 * m)         # q, k, v, log_alpha in; o out
+    return dw.B * dw.H * per_head
+
+
+def decode_cpu_baseline(dw, layers=3):
+    """The fp64 decode-step oracle on `layers` layer steps of the workload."""
+    import numpy as np
+
+    from oracle.decode import DecodeState, decode_step
+    from sliding_window_softmax_gb300.synthetic import make_decode_layer
+
+    secs = 0.0
+    for layer in range(layers):
+        x, state = make_decode_layer(dw, layer, device="cpu")
+        st = DecodeState(dw.B, dw.H, dw.d, dw.m, dw.w)
+        st.S_k, st.S_v, st.ring_k, st.ring_v, st.ring_la = (a.double().numpy() for a in state)
+        xs = {n: t.double().numpy() for n, t in x.items()}
+        t0 = time.perf_counter()
+        decode_step(st, xs["q"], xs["k"], xs["v"], xs["log_alpha"], dw.t)
+        secs += time.perf_counter() - t0
+    per_layer = secs / layers
+    return {"value": dw.B / (per_layer * dw.layers), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{layers} layer steps of all {dw.B * dw.H} heads (numpy fp64, one thread); "
+                      f"value = B / ({dw.layers} x the mean layer-step time)"}
+
+
+def run_decode(args, dev, stream, layers_override=None):
+    """One decode token for B sequences through every layer of the decode
+    workload: one nha_decode_step launch per layer, the layers' launches
+    captured in a CUDA graph and replayed.  Each layer keeps its own state,
+    so a step reads several times the L2 capacity and no layer's state is
+    still cached when its turn comes again."""
+    import torch
+
+    import sliding_window_softmax_gb300 as nha
+    from sliding_window_softmax_gb300.synthetic import DECODE_1P3B, make_decode_layer
+
+    dw = DECODE_1P3B
+    if layers_override:
+        dw = dataclasses.replace(dw, layers=layers_override,
+                                 name=dw.name.replace(f"{dw.layers} layers", f"{layers_override} layers"))
+    layers = [make_decode_layer(dw, i, device=dev) for i in range(dw.layers)]
+    outs = [torch.empty_like(x["q"]) for x, _ in layers]
+
+    def step():
+        for (x, st), o in zip(layers, outs):
+            nha.nha_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], dw.t, dw.w, st, o=o)
+
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()  # eager once: validates the arguments
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    n0 = nha.launch_count()
+    with torch.cuda.graph(graph):
+        step()
+    captured = nha.launch_count() - n0
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    K = max(10, min(args.steps, 200))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev:
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    step_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    per_launch_s = step_ms / 1e3 / dw.layers
+    peaks = load_peaks()
+    nbytes = decode_bytes(dw)
+    achieved = nbytes / per_launch_s / 1e9
+    return {
+        "workload": dw.name, "B": dw.B, "H": dw.H, "d": dw.d, "m": dw.m, "w": dw.w, "t": dw.t,
+        "layers": dw.layers, "dtype": dw.dtype,
+        "tokens_per_s": dw.B / (step_ms / 1e3), "ms_per_token_step": step_ms,
+        "us_per_layer": per_launch_s * 1e6, "launches_per_step": captured, "steps": K,
+        "timing": "CUDA graph of the layers' launches, median of replays; state of all layers "
+                  f"{dw.layers * nbytes / 2**30:.2f} GiB of algorithmic traffic per step, above the L2 capacity",
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic("decode_step", "decode"),
+                     "kernel": "decode_step", "bytes_per_launch": nbytes, "peak_source": peaks["source"]},
+    }
+
+
 def run_nha(args, wl, wl_key):
     import torch
     import torch.distributed as dist
@@ -411,6 +530,8 @@ def run_nha(args, wl, wl_key):
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e_ev)
     (e2e_ms,) = max_over_ranks([e2e_ms], device=dev)
 
+    decode = None if args.no_decode else run_decode(args, dev, stream)
+
     if rank == 0:
         model = work_model(wl)
         peaks = load_peaks()
@@ -470,6 +591,12 @@ def run_nha(args, wl, wl_key):
         }
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl)
+            if decode is not None:
+                from sliding_window_softmax_gb300.synthetic import DECODE_1P3B
+
+                decode["cpu_baseline"] = decode_cpu_baseline(DECODE_1P3B)
+        if decode is not None:
+            line["decode"] = decode
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -483,12 +610,23 @@ def main():
     ap.add_argument("--workload", default="1.3B")
     ap.add_argument("--impl", default="nha", choices=["nha", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="run only the decode-step measurement (one GPU) and print its object")
+    ap.add_argument("--decode-layers", type=int, default=0, help="layers of the decode run (default 24)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     wls = workloads()
     if args.workload not in wls:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(wls)}")
     wl = wls[args.workload]
+    if args.decode_only:
+        import torch
+
+        torch.cuda.set_device(0)
+        print(json.dumps(run_decode(args, torch.device("cuda", 0), torch.cuda.current_stream(),
+                                    args.decode_layers or None)), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -101,6 +101,41 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
                           int C, nha_dtype_t dtype, float rope_base, void* workspace,
                           size_t ws_bytes, void* stream);
 
+/* ---- Recurrent decode step ----
+ *
+ * The operator above taken for one new token t of every (b, h) (same page,
+ * section 关键设计/层内混合; section 局限 names this recurrent inference mode
+ * as the part its authors left unoptimised).  Per (b, h):
+ *   1. if t >= w, token j = t - w leaves the window and enters the long memory
+ *      with its own gate:  K^long = Diag(alpha_j) K^long + u_j (x) k_j, V^long
+ *      likewise (state_k, state_v updated in place); while t < w the slot
+ *      logits are masked and the states are left untouched;
+ *   2. slot logits q_t . K^long[i] / sqrt(d) (no position code); window logits
+ *      rope(q_t, t) . rope(k_s, s) / sqrt(d) for s in [max(0, t-w+1), t];
+ *   3. o_t = one softmax over [slots | window] applied to [V^long | v_s];
+ *   4. token t (raw k, v and log_alpha) is written into ring entry t mod w.
+ * Calling it for t = 0, 1, ..., T-1 from zero states gives the o of
+ * nha_forward on the same sequence (up to rounding).
+ *
+ * Layout (all DEVICE pointers, 16-byte aligned, contiguous row-major):
+ *   q, k, v, o     [B, H, d]     element type `dtype` (token t)
+ *   log_alpha      [B, H, m]     fp32 (token t)
+ *   state_k/_v     [B, H, m, d]  fp32, in/out: K^long, V^long after token
+ *                                t - w - 1 on entry, after t - w on return;
+ *                                zero before the first token is absorbed
+ *   ring_k/_v      [B, H, w, d]  element type, in/out: token s in entry s mod w
+ *   ring_la        [B, H, w, m]  fp32, in/out, same indexing
+ * Entries of the ring are read only for tokens s in [max(0, t-w), t-1], which
+ * earlier calls wrote; with w = 0 the ring pointers are not used (may be NULL).
+ * All heads share the position t.  Supported d, m as above; 0 <= t < 262144;
+ * 0 <= w <= 262144.  Ownership, errors and streams as for nha_forward; the
+ * call needs no workspace and runs on `stream` alone.  Two calls on the same
+ * state and ring must be ordered (same stream, or an event between them). */
+nha_status_t nha_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, void* o,
+                             float* state_k, float* state_v, void* ring_k, void* ring_v, float* ring_la,
+                             int t, int B, int H, int d, int m, int w, nha_dtype_t dtype, float rope_base,
+                             void* stream);
+
 /* ---- Forward without device allocation (the pages have no counterpart) ----
  *
  * Some callers cannot allocate device memory: code that runs while a CUDA

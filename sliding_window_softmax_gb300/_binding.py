@@ -25,8 +25,8 @@ STATUS = {0: "NHA_OK", 1: "NHA_ERR_INVALID_ARGUMENT", 2: "NHA_ERR_UNSUPPORTED",
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 
 # Every symbol include/nha.h declares (checked by the tests).
-EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward", "nha_forward_noalloc", "nha_launch_count",
-           "nha_profile_begin", "nha_profile_end", "nha_status_string", "nha_last_error")
+EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward", "nha_decode_step", "nha_forward_noalloc",
+           "nha_launch_count", "nha_profile_begin", "nha_profile_end", "nha_status_string", "nha_last_error")
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +83,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.nha_forward.argtypes = [vp] * 6 + [i] * 8 + [f, vp, sz, vp]
         lib.nha_backward.restype = i
         lib.nha_backward.argtypes = [vp] * 11 + [i] * 8 + [f, vp, sz, vp]
+        lib.nha_decode_step.restype = i
+        lib.nha_decode_step.argtypes = [vp] * 10 + [i] * 7 + [f, vp]
         lib.nha_forward_noalloc.restype = i
         lib.nha_forward_noalloc.argtypes = [vp] * 6 + [i] * 8 + [f, vp]
         lib.nha_status_string.restype = ctypes.c_char_p
@@ -217,3 +219,45 @@ def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
                           _ptr(workspace), ws_bytes, _stream_handle(stream))
     _raise(lib, rc)
     return dq, dk, dv, dlog_alpha
+
+
+def nha_decode_state(B, H, d, m, w, dtype=torch.bfloat16, device="cuda"):
+    """Zeroed decode state: (state_k, state_v [B,H,m,d] fp32, ring_k, ring_v [B,H,max(w,1),d] dtype,
+    ring_la [B,H,max(w,1),m] fp32)."""
+    n = max(int(w), 1)
+    return (torch.zeros((B, H, m, d), dtype=torch.float32, device=device),
+            torch.zeros((B, H, m, d), dtype=torch.float32, device=device),
+            torch.zeros((B, H, n, d), dtype=dtype, device=device),
+            torch.zeros((B, H, n, d), dtype=dtype, device=device),
+            torch.zeros((B, H, n, m), dtype=torch.float32, device=device))
+
+
+def nha_decode_step(q, k, v, log_alpha, t: int, w: int, state, rope_base: float = 10000.0, o=None,
+                     stream=None):
+    """o_t = nha_decode_step(q, k, v, log_alpha, t, w, state).
+
+    q, k, v [B,H,d] and log_alpha [B,H,m] (fp32) are token t of every head;
+    ``state`` is the tuple from :func:`nha_decode_state`, updated in place."""
+    lib = load_library()
+    B, H, d = q.shape
+    m = log_alpha.shape[-1]
+    dt = q.dtype
+    if dt not in DTYPE:
+        raise TypeError(f"unsupported dtype {dt}")
+    n = max(int(w), 1)
+    sk, sv, rk, rv, rla = state
+    for nm, x in (("q", q), ("k", k), ("v", v)):
+        _check(nm, x, dt, (B, H, d))
+    _check("log_alpha", log_alpha, torch.float32, (B, H, m))
+    _check("state_k", sk, torch.float32, (B, H, m, d))
+    _check("state_v", sv, torch.float32, (B, H, m, d))
+    _check("ring_k", rk, dt, (B, H, n, d))
+    _check("ring_v", rv, dt, (B, H, n, d))
+    _check("ring_la", rla, torch.float32, (B, H, n, m))
+    o = torch.empty_like(q) if o is None else o
+    _check("o", o, dt, (B, H, d))
+    rc = lib.nha_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(sk), _ptr(sv),
+                             _ptr(rk), _ptr(rv), _ptr(rla), int(t), B, H, d, m, int(w), DTYPE[dt],
+                             float(rope_base), _stream_handle(stream))
+    _raise(lib, rc)
+    return o

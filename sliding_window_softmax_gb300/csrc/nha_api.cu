@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include "nha.h"
+#include "nha_decode.h"
 #include "nha_kernels.h"
 
 namespace {
@@ -284,6 +285,60 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = dtype == NHA_DTYPE_F32 ? run_backward<float>(p, a, s) : run_backward_tc(p, a, ws, s);
     if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "backward launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+nha_status_t nha_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, void* o,
+                             float* state_k, float* state_v, void* ring_k, void* ring_v, float* ring_la, int t,
+                             int B, int H, int d, int m, int w, nha_dtype_t dtype, float rope_base, void* stream) {
+    if (inject("validate")) return fail(NHA_ERR_INTERNAL, "fault injected at validate");
+    if (B < 0 || H < 0 || t < 0 || w < 0 || d <= 0 || m <= 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "negative or zero size (B=%d H=%d t=%d d=%d m=%d w=%d)", B, H, t,
+                    d, m, w);
+    if (dtype != NHA_DTYPE_F32 && dtype != NHA_DTYPE_BF16)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "unknown dtype %d", (int)dtype);
+    if (d != 64 && d != 128) return fail(NHA_ERR_UNSUPPORTED, "head dim d=%d not in {64, 128}", d);
+    if (m != 16 && m != 32 && m != 64) return fail(NHA_ERR_UNSUPPORTED, "slots m=%d not in {16, 32, 64}", m);
+    if (t >= kMaxT) return fail(NHA_ERR_UNSUPPORTED, "position t=%d not below %d", t, kMaxT);
+    if (w > kMaxT) return fail(NHA_ERR_UNSUPPORTED, "window w=%d above %d", w, kMaxT);
+    const long long BH = (long long)B * H, wr = w > 0 ? w : 1;
+    if (BH * wr * (d > m ? d : m) >= (1LL << 31) || BH * 8 >= (1LL << 31))
+        return fail(NHA_ERR_UNSUPPORTED, "B*H*max(w,1)*max(d,m) >= 2^31");
+    if (!(rope_base > 1.0f) || !isfinite(rope_base))
+        return fail(NHA_ERR_INVALID_ARGUMENT, "rope_base must be a finite value > 1");
+    if (BH == 0) return ok();
+    const void* ptrs[] = {q, k, v, log_alpha, o, state_k, state_v, ring_k, ring_v, ring_la};
+    const char* names[] = {"q", "k", "v", "log_alpha", "o", "state_k", "state_v", "ring_k", "ring_v", "ring_la"};
+    const int nptr = w > 0 ? 10 : 7;  // the ring is not used when w = 0
+    for (int i = 0; i < nptr; i++) {
+        if (ptrs[i] == nullptr) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is NULL", names[i]);
+        if (misaligned(ptrs[i])) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", names[i]);
+    }
+    if (inject("decode_launch")) return fail(NHA_ERR_INTERNAL, "fault injected at decode_launch");
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
+    nha::DecodeArgs a;
+    a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.o = o;
+    a.SK = state_k; a.SV = state_v;
+    a.ring_k = w > 0 ? ring_k : nullptr;
+    a.ring_v = w > 0 ? ring_v : nullptr;
+    a.ring_la = w > 0 ? ring_la : nullptr;
+    a.BH = (int)BH; a.t = t; a.w = w; a.sms = sms;
+    make_rope(a.rope, d, rope_base);
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool f32 = dtype == NHA_DTYPE_F32;
+    switch (d * 1000 + m) {
+        case 64016: e = f32 ? nha::launch_decode<float, 64, 16>(a, s) : nha::launch_decode<__nv_bfloat16, 64, 16>(a, s); break;
+        case 64032: e = f32 ? nha::launch_decode<float, 64, 32>(a, s) : nha::launch_decode<__nv_bfloat16, 64, 32>(a, s); break;
+        case 64064: e = f32 ? nha::launch_decode<float, 64, 64>(a, s) : nha::launch_decode<__nv_bfloat16, 64, 64>(a, s); break;
+        case 128016: e = f32 ? nha::launch_decode<float, 128, 16>(a, s) : nha::launch_decode<__nv_bfloat16, 128, 16>(a, s); break;
+        case 128032: e = f32 ? nha::launch_decode<float, 128, 32>(a, s) : nha::launch_decode<__nv_bfloat16, 128, 32>(a, s); break;
+        case 128064: e = f32 ? nha::launch_decode<float, 128, 64>(a, s) : nha::launch_decode<__nv_bfloat16, 128, 64>(a, s); break;
+        default: e = cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "decode launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
 

@@ -1,0 +1,33 @@
+// Internal interface of the recurrent decode step (nha_decode.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "nha_common.cuh"
+
+namespace nha {
+
+// Decode step for token t.  q, k, v, o [BH, D] in the element type; la
+// [BH, M]; SK, SV [BH, M, D] fp32, updated in place; ring_k, ring_v
+// [BH, max(w, 1), D] in the element type and ring_la [BH, max(w, 1), M] fp32,
+// token s in entry s mod w (not used when w = 0).
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* la;
+    void* o;
+    float* SK;
+    float* SV;
+    void* ring_k;
+    void* ring_v;
+    float* ring_la;
+    int BH, t, w;
+    int sms;  // multiprocessors of the device (sizes the clusters)
+    RopeTab rope;
+};
+
+template <typename Tin, int D, int M>
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+
+}  // namespace nha

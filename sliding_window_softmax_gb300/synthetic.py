@@ -95,3 +95,52 @@ def make_inputs(wl: Workload, seed: Optional[int] = None, device="cpu", scale_qk
     if device != "cpu":
         out = {n: t.to(device) for n, t in out.items()}
     return out
+
+
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """One decode token for B sequences through `layers` NHA layers at position t."""
+    name: str
+    B: int
+    H: int
+    d: int
+    m: int
+    w: int
+    t: int
+    layers: int
+    dtype: str = "bf16"
+    seed: int = 1006
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+
+# Serving-style decode of the 1.3B-like layer: 16 sequences, 24 layers, a full
+# window and a long memory in use (t >= w).
+DECODE_1P3B = DecodeWorkload("1.3B-like decode B16 H16 d128 m64 w512 t4096, 24 layers", 16, 16, 128, 64, 512,
+                             4096, 24)
+
+
+def make_decode_layer(dw: DecodeWorkload, layer: int, device="cuda"):
+    """Token inputs (q, k, v, log_alpha [B,H,.]) and a state (state_k, state_v,
+    ring_k, ring_v, ring_la) for one layer, drawn on `device` from a generator
+    seeded with seed + layer: q, k, v and the ring's k, v ~ N(0,1) d**-0.25;
+    log_alpha and the ring's ~ logsigmoid(N(3, 1)); the slot states
+    ~ N(0,1) * 0.3 d**-0.25 (the size of a convex mix of keys)."""
+    g = torch.Generator(device=device).manual_seed(dw.seed + layer)
+    B, H, d, m, n = dw.B, dw.H, dw.d, dw.m, max(dw.w, 1)
+    s = d ** -0.25
+    dt = dw.torch_dtype
+
+    def rn(*shape):
+        return torch.randn(shape, generator=g, device=device)
+
+    def gate(*shape):
+        return torch.nn.functional.logsigmoid(rn(*shape) + 3.0)
+
+    x = dict(q=(rn(B, H, d) * s).to(dt), k=(rn(B, H, d) * s).to(dt), v=(rn(B, H, d) * s).to(dt),
+             log_alpha=gate(B, H, m))
+    state = (rn(B, H, m, d) * (0.3 * s), rn(B, H, m, d) * (0.3 * s), (rn(B, H, n, d) * s).to(dt),
+             (rn(B, H, n, d) * s).to(dt), gate(B, H, n, m))
+    return x, state

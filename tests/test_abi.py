@@ -137,3 +137,40 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(lib):
     assert rc == 3 and b"built-in scratch" in lib.nha_last_error()
     # an invalid shape reports its own reason
     assert lib.nha_forward_noalloc(p, p, p, p, p, p, 1, 1, 16, 96, 16, 4, 64, 1, 10000.0, None) == 2
+
+
+def _dec(lib, q=1, **kw):
+    args = dict(t=5, B=1, H=1, d=64, m=16, w=4, dt=1, base=10000.0, ring=True)
+    args.update(kw)
+    p = ctypes.c_void_p(q * 4096) if q else None  # never dereferenced: validation fails first
+    r = p if args["ring"] else None
+    return lib.nha_decode_step(p, p, p, p, p, p, p, r, r, r, args["t"], args["B"], args["H"], args["d"],
+                               args["m"], args["w"], args["dt"], args["base"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=96), 2), (dict(m=8), 2), (dict(t=1 << 18), 2), (dict(w=(1 << 18) + 1), 2),
+    (dict(t=-1), 1), (dict(w=-1), 1), (dict(B=-1), 1), (dict(dt=3), 1), (dict(base=1.0), 1),
+    (dict(base=float("inf")), 1), (dict(m=0), 1),
+])
+def test_decode_rejects_bad_arguments(lib, kw, status):
+    assert _dec(lib, **kw) == status
+    assert lib.nha_last_error()
+
+
+def test_decode_pointer_checks(lib):
+    assert _dec(lib, q=0) == 1 and b"NULL" in lib.nha_last_error()
+    # the ring is required when w > 0 ...
+    assert _dec(lib, ring=False) == 1 and b"ring_k" in lib.nha_last_error()
+    p, bad = ctypes.c_void_p(4096), ctypes.c_void_p(4096 + 8)
+    assert lib.nha_decode_step(p, p, p, p, p, bad, p, p, p, p, 0, 1, 1, 64, 16, 4, 1, 1e4, None) == 1
+    assert b"state_k" in lib.nha_last_error() and b"aligned" in lib.nha_last_error()
+    # no heads: a no-op that touches nothing
+    assert _dec(lib, q=0, B=0) == 0
+
+
+def test_decode_fault_injection_on_host(lib, monkeypatch):
+    # ... and unused when w = 0: validation passes, the injected failure stops the call
+    monkeypatch.setenv("NHA_FAULT_INJECT", "decode_launch")
+    assert _dec(lib, ring=False, w=0) == 5 and b"decode_launch" in lib.nha_last_error()
+    monkeypatch.delenv("NHA_FAULT_INJECT")

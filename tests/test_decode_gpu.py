@@ -1,0 +1,168 @@
+"""GPU parity of the recurrent decode step (nha_decode_step through the C ABI)
+against the fp64 oracle, on seeded inputs (bf16 inputs upcast exactly).
+
+* Step-by-step runs from zero states over ragged lengths: every o_t against
+  the oracle's full-sequence forward, and the final slot states against the
+  oracle's own decode recurrence; the ring holds raw copies (bit-exact).
+* Serving-sized batches at a late position t: one step from a random state
+  and ring, against the oracle's decode step on the same state.
+
+Tolerances: fp32: max |err| <= 1e-4 on o, <= 1e-5 on the states;
+bf16: o rel L2 <= 5e-3 and max |err| <= 2e-2 (o is rounded to bf16),
+states max |err| <= 1e-4 (fp32 arithmetic on exact inputs).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.decode import DecodeState, decode_step
+from sliding_window_softmax_gb300.synthetic import Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+def _nha():
+    import sliding_window_softmax_gb300 as nha
+
+    return nha
+
+
+def _np(t):
+    return t.double().cpu().numpy()
+
+
+def _check_o(g, r, dtype, tag):
+    assert np.all(np.isfinite(g)), tag
+    err = np.abs(g - r).max()
+    if dtype == "f32":
+        assert err <= 1e-4, f"{tag}: max abs {err:.3e}"
+    else:
+        rel = np.linalg.norm(g - r) / np.linalg.norm(r)
+        assert rel <= 5e-3 and err <= 2e-2, f"{tag}: rel {rel:.3e} max abs {err:.3e}"
+
+
+STEP_CASES = [
+    # B, H, T, d, m, w, dtype
+    (1, 2, 150, 64, 16, 37, "f32"),    # ring wraps several times, ragged T
+    (1, 2, 150, 64, 16, 37, "bf16"),
+    (2, 1, 70, 128, 64, 0, "bf16"),    # w = 0: slots only
+    (1, 1, 40, 128, 32, 1, "f32"),     # w = 1: the window is the token itself
+    (1, 3, 50, 64, 64, 80, "bf16"),    # w > T: window attention only
+    (2, 2, 300, 128, 64, 128, "bf16"),
+]
+
+
+@pytest.mark.parametrize("B,H,T,d,m,w,dtype", STEP_CASES)
+def test_decode_steps_match_the_forward_oracle(B, H, T, d, m, w, dtype):
+    nha = _nha()
+    wl = Workload("decode steps", B, H, T, d, m, w, dtype=dtype, seed=2000 + T + w + m)
+    x = make_inputs(wl)
+    dev = {n: t.cuda() for n, t in x.items()}
+    state = nha.nha_decode_state(B, H, d, m, w, dtype=wl.torch_dtype)
+    outs = []
+    for t in range(T):
+        o = nha.nha_decode_step(dev["q"][:, :, t].contiguous(), dev["k"][:, :, t].contiguous(),
+                                dev["v"][:, :, t].contiguous(), dev["log_alpha"][:, :, t].contiguous(),
+                                t, w, state)
+        outs.append(o)
+    torch.cuda.synchronize()
+    o_gpu = _np(torch.stack(outs, dim=2))
+    o_ref, _ = oracle.forward(x["q"], x["k"], x["v"], x["log_alpha"], w)
+    _check_o(o_gpu, o_ref, dtype, f"decode B{B} H{H} T{T} d{d} m{m} w{w} {dtype}")
+    # final states against the oracle's decode recurrence; the ring is raw copies
+    st = DecodeState(B, H, d, m, w)
+    for t in range(T):
+        decode_step(st, _np(x["q"][:, :, t]), _np(x["k"][:, :, t]), _np(x["v"][:, :, t]),
+                    _np(x["log_alpha"][:, :, t]), t)
+    tol = 1e-5 if dtype == "f32" else 1e-4
+    assert np.abs(_np(state[0]) - st.S_k).max() <= tol
+    assert np.abs(_np(state[1]) - st.S_v).max() <= tol
+    if w > 0:
+        assert np.array_equal(_np(state[2]), st.ring_k)
+        assert np.array_equal(_np(state[3]), st.ring_v)
+        assert np.array_equal(_np(state[4]), st.ring_la)
+
+
+BATCH_CASES = [
+    # B, H, d, m, w, t, dtype: decode batches of a 1.3B-like layer (d128 m64 w512)
+    (16, 16, 128, 64, 512, 4096, "bf16"),   # 256 heads: one CTA per head
+    (1, 2, 128, 64, 512, 4096, "bf16"),     # 2 heads: 8-CTA clusters
+    (4, 16, 128, 64, 512, 700, "f32"),
+    (8, 16, 64, 64, 64, 2047, "bf16"),      # 340M-like layer
+    (2, 16, 128, 32, 8192, 5000, "bf16"),   # window not yet full: slots masked
+    (1, 32, 128, 64, 512, 65535, "bf16"),   # long context, last position supported by the forward sizes
+]
+
+
+@pytest.mark.parametrize("B,H,d,m,w,t,dtype", BATCH_CASES)
+def test_decode_batch_matches_the_decode_oracle(B, H, d, m, w, t, dtype):
+    nha = _nha()
+    g = torch.Generator().manual_seed(3000 + B * H + w + t)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    n = max(w, 1)
+    s = d ** -0.25
+    q, k, v = ((torch.randn((B, H, d), generator=g) * s).to(tdt) for _ in range(3))
+    la = torch.nn.functional.logsigmoid(torch.randn((B, H, m), generator=g) + 3.0)
+    # a state of the magnitude the recurrence reaches (a convex mix of keys) and a full ring
+    sk0 = torch.randn((B, H, m, d), generator=g) * (0.3 * s)
+    sv0 = torch.randn((B, H, m, d), generator=g) * (0.3 * s)
+    rk0 = (torch.randn((B, H, n, d), generator=g) * s).to(tdt)
+    rv0 = (torch.randn((B, H, n, d), generator=g) * s).to(tdt)
+    rla0 = torch.nn.functional.logsigmoid(torch.randn((B, H, n, m), generator=g) + 3.0)
+    state = tuple(a.cuda() for a in (sk0, sv0, rk0, rv0, rla0))
+    o = nha.nha_decode_step(q.cuda(), k.cuda(), v.cuda(), la.cuda(), t, w, state)
+    torch.cuda.synchronize()
+    st = DecodeState(B, H, d, m, w)
+    st.S_k, st.S_v, st.ring_k, st.ring_v, st.ring_la = (_np(a) for a in (sk0, sv0, rk0, rv0, rla0))
+    o_ref = decode_step(st, _np(q), _np(k), _np(v), _np(la), t)
+    _check_o(_np(o), o_ref, dtype, f"decode batch B{B} H{H} d{d} m{m} w{w} t{t} {dtype}")
+    tol = 1e-5 if dtype == "f32" else 1e-4
+    assert np.abs(_np(state[0]) - st.S_k).max() <= tol
+    assert np.abs(_np(state[1]) - st.S_v).max() <= tol
+    assert np.array_equal(_np(state[2]), st.ring_k)
+    assert np.array_equal(_np(state[3]), st.ring_v)
+    assert np.array_equal(_np(state[4]), st.ring_la)
+
+
+def test_decode_matches_the_library_forward():
+    """Decoding a whole bf16 sequence token by token gives the o of the
+    library's chunkwise forward on the same inputs (two independent GPU paths)."""
+    nha = _nha()
+    wl = Workload("decode after prefill", 1, 4, 200, 128, 64, 48, seed=4000)
+    x = make_inputs(wl, device="cuda")
+    o_fwd, _ = nha.nha_forward(x["q"], x["k"], x["v"], x["log_alpha"], w=wl.w)
+    state = nha.nha_decode_state(1, 4, 128, 64, 48, dtype=torch.bfloat16)
+    outs = [nha.nha_decode_step(x["q"][:, :, t].contiguous(), x["k"][:, :, t].contiguous(),
+                                x["v"][:, :, t].contiguous(), x["log_alpha"][:, :, t].contiguous(),
+                                t, wl.w, state) for t in range(wl.T)]
+    o_dec = torch.stack(outs, dim=2)
+    torch.cuda.synchronize()
+    a, b = _np(o_dec), _np(o_fwd)
+    assert np.linalg.norm(a - b) / np.linalg.norm(b) <= 5e-3
+
+
+def test_decode_bench_workload_layer_matches_the_oracle():
+    """The decode workload the benchmark times (same inputs, same launch)."""
+    nha = _nha()
+    from sliding_window_softmax_gb300.synthetic import DECODE_1P3B, make_decode_layer
+
+    dw = DECODE_1P3B
+    x, state = make_decode_layer(dw, 0, device="cuda")
+    st = DecodeState(dw.B, dw.H, dw.d, dw.m, dw.w)
+    st.S_k, st.S_v, st.ring_k, st.ring_v, st.ring_la = (_np(a) for a in state)
+    o = nha.nha_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], dw.t, dw.w, state)
+    torch.cuda.synchronize()
+    o_ref = decode_step(st, _np(x["q"]), _np(x["k"]), _np(x["v"]), _np(x["log_alpha"]), dw.t)
+    _check_o(_np(o), o_ref, dw.dtype, dw.name)
+    assert np.abs(_np(state[0]) - st.S_k).max() <= 1e-4
+    assert np.abs(_np(state[1]) - st.S_v).max() <= 1e-4
