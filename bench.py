@@ -344,7 +344,7 @@ def decode_cpu_baseline(dw, layers=3):
                       f"value = B / ({dw.layers} x the mean layer-step time)"}
 
 
-def run_decode(args, dev, stream, layers_override=None):
+def run_decode(args, dev, stream, layers_override=None, batch_override=None):
     """One decode token for B sequences through every layer of the decode
     workload: one nha_decode_step launch per layer, the layers' launches
     captured in a CUDA graph and replayed.  Each layer keeps its own state,
@@ -359,6 +359,8 @@ def run_decode(args, dev, stream, layers_override=None):
     if layers_override:
         dw = dataclasses.replace(dw, layers=layers_override,
                                  name=dw.name.replace(f"{dw.layers} layers", f"{layers_override} layers"))
+    if batch_override:
+        dw = dataclasses.replace(dw, B=batch_override, name=dw.name.replace(f"B{dw.B} ", f"B{batch_override} "))
     layers = [make_decode_layer(dw, i, device=dev) for i in range(dw.layers)]
     outs = [torch.empty_like(x["q"]) for x, _ in layers]
 
@@ -614,6 +616,7 @@ def main():
     ap.add_argument("--decode-only", action="store_true",
                     help="run only the decode-step measurement (one GPU) and print its object")
     ap.add_argument("--decode-layers", type=int, default=0, help="layers of the decode run (default 24)")
+    ap.add_argument("--decode-batch", type=int, default=0, help="sequences of the decode run (default 16)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     wls = workloads()
@@ -625,7 +628,7 @@ def main():
 
         torch.cuda.set_device(0)
         print(json.dumps(run_decode(args, torch.device("cuda", 0), torch.cuda.current_stream(),
-                                    args.decode_layers or None)), flush=True)
+                                    args.decode_layers or None, args.decode_batch or None)), flush=True)
         return
     if args.impl == "reference":
         run_reference(args, wl)

@@ -2,17 +2,26 @@
 // Efficient Sequence Modeling", Paper-Notes page, 关键设计/层内混合: the K^long
 // recurrence, the token shift into the long memory and o_t, for a single
 // query; section 局限 names this recurrent mode as the part left unoptimised).
-// Matrix-vector work bound by the state and ring reads, so SIMT.
+// Matrix-vector work bound by the reads of the slot states and the ring, so
+// SIMT, organised around keeping enough of those reads in flight.
 //
-// One thread-block cluster of ks CTAs (1..8) per head, 8 warps each.  The
-// cluster's 8 ks warps share the head's work: warp g absorbs the leaving token
-// into slot rows i = g, g + 8 ks, ... (fp32 read-modify-write, coalesced over
-// the lanes) and scores them, and scores the window keys s0 + g, s0 + g + 8 ks,
-// ..., each with an online softmax and an output accumulator in its lanes.
-// Lane l holds the elements {l, l + 32, ...} of a d-vector, so a rotate-half
-// pair (i, i + d/2) sits in one lane.  The warps of a CTA merge in shared
-// memory, the CTAs of the cluster through distributed shared memory.
+// One thread-block cluster of ks CTAs (1..8) per head.  A CTA's 256 threads
+// form groups of D/8 lanes; a lane owns 8 elements of every d-vector: i and
+// i + d/2 for i in [4j, 4j + 4), j its index in the group, so each rotate-half
+// pair of RoPE sits in one lane.  The head's items, slot rows (when a token
+// leaves the window) and window tokens s in [max(0, t-w+1), t-1], are dealt
+// round-robin over the cluster's groups.  Every lane streams its own pieces of
+// its group's next items from global memory into its own shared-memory stages
+// with cp.async, kDecStages items deep, so no lane waits on another's copy and
+// the SM keeps tens of KB of reads in flight.  A slot item absorbs the
+// leaving token into the row (written back in place) and scores it; a window
+// item scores the raw key rotated to its position, the cos/sin advanced from
+// item to item by angle addition (the group's positions step by a constant)
+// and re-seeded exactly every kReseed items.  Each group runs an online
+// softmax with its lanes' share of the output; the groups of a CTA merge in
+// shared memory, the CTAs of the cluster through distributed shared memory.
 #include <cooperative_groups.h>
+#include <stdlib.h>
 
 #include "nha_common.cuh"
 #include "nha_decode.h"
@@ -23,64 +32,82 @@ namespace cg = cooperative_groups;
 namespace nha {
 
 namespace {
-constexpr int kDecThreads = 256, kDecWarps = kDecThreads / 32;
-constexpr int kDecBatch = 4;  // window keys a warp loads before it scores them
+constexpr int kDecThreads = 256;
+constexpr int kDecStages = 4;  // items a lane has in flight or ready
+constexpr int kReseed = 16;    // window items between exact cos/sin evaluations
+constexpr int kPieces = 4;     // 16-byte shared-memory pieces per lane and stage
 
-template <typename T>
-__device__ __forceinline__ float to_f(T x);
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+template <int BYTES>
+__device__ __forceinline__ void cp_async(void* smem, const void* gmem) {
+    if constexpr (BYTES == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], %2;\n" ::"r"(smem_u32(smem)), "l"(gmem), "n"(BYTES)
+                     : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// 4 consecutive elements as fp32
+__device__ __forceinline__ void load4(const float4* p, float (&x)[4]) {
+    const float4 v = *p;
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+__device__ __forceinline__ void load4(const uint2* p, float (&x)[4]) {
+    const uint2 v = *p;
+    x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xffff0000u);
+    x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+template <typename Tin>
+struct Vec4;  // 4 elements of Tin
 template <>
-__device__ __forceinline__ float to_f<float>(float x) { return x; }
+struct Vec4<float> { using T = float4; };
 template <>
-__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+struct Vec4<__nv_bfloat16> { using T = uint2; };
+
 template <typename T>
 __device__ __forceinline__ T from_f(float x);
 template <>
 __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-// Online softmax of one warp: running max and sum (same in every lane) and
-// the lane's share of the output accumulator.
-template <int E>
-struct WarpSoftmax {
-    float mx = -INFINITY, sum = 0.0f, acc[E];
-    __device__ WarpSoftmax() {
+template <int GL>
+__device__ __forceinline__ float group_sum(float x, unsigned mask) {
 #pragma unroll
-        for (int e = 0; e < E; e++) acc[e] = 0.0f;
-    }
-    __device__ void push(float logit, const float (&val)[E]) {
-        const float mn = fmaxf(mx, logit);
-        const float sc = expf(mx - mn);  // 0 while mx = -inf
-        const float p = expf(logit - mn);
-        sum = sum * sc + p;
-#pragma unroll
-        for (int e = 0; e < E; e++) acc[e] = acc[e] * sc + p * val[e];
-        mx = mn;
-    }
-};
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    for (int off = GL / 2; off > 0; off >>= 1) x += __shfl_xor_sync(mask, x, off);
     return x;
 }
 }  // namespace
 
 template <typename Tin, int D, int M>
 __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeArgs a) {
-    constexpr int E = D / 32, H2 = D / 2;
+    constexpr int H2 = D / 2, GL = D / 8, NG = kDecThreads / GL;
+    using V4 = typename Vec4<Tin>::T;
+    constexpr int PB = sizeof(V4);  // bytes of a lane's 4-element window piece
+    extern __shared__ float4 stage[];  // [kDecStages][kPieces][kDecThreads]; later the groups' partials
     __shared__ float sq[D], sqr[D], skj[D], svj[D], slj[M];
-    __shared__ float wm[kDecWarps], ws[kDecWarps], wacc[kDecWarps][D];
+    __shared__ float2 cst[H2];  // cos, sin at position t
+    __shared__ float gmx[NG], gsum[NG];
     __shared__ float bm, bs, bacc[D];  // this CTA's merged partial, read by the cluster
     cg::cluster_group cl = cg::this_cluster();
     const int ks = (int)cl.num_blocks(), rank = (int)cl.block_rank();
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, grp = tid / GL, j = tid % GL, lane = tid & 31;
+    const unsigned gmask = (GL == 32 ? 0xffffffffu : ((1u << GL) - 1u) << (lane / GL * GL));
     const int bh = blockIdx.x / ks;
-    const int g = rank * kDecWarps + warp, G = ks * kDecWarps;
+    const int g = rank * NG + grp, G = ks * NG;
     const int t = a.t, w = a.w, wr = w > 0 ? w : 1;
     const float scale = rsqrtf((float)D);
     const bool absorb = t - w >= 0;
     const int eo = absorb && w > 0 ? (t - w) % w : 0;  // ring entry of the token that leaves
+    const int s_lo = max(0, t - w + 1);                 // first window token
+    const int nwin = max(0, t - s_lo);                  // window tokens before t
 
     const Tin* q = (const Tin*)a.q + (size_t)bh * D;
     const Tin* k = (const Tin*)a.k + (size_t)bh * D;
@@ -88,8 +115,39 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
     const float* la = a.la + (size_t)bh * M;
     const Tin* rk = (const Tin*)a.ring_k + (size_t)bh * wr * D;
     const Tin* rv = (const Tin*)a.ring_v + (size_t)bh * wr * D;
+    float* SK = a.SK + (size_t)bh * M * D;
+    float* SV = a.SV + (size_t)bh * M * D;
 
-    // ---- q, RoPE(q, t), and the token that leaves the window
+    // ---- this group's items: slot rows g, g + G, ... then window tokens s_lo + g, s_lo + g + G, ...
+    const int ns = absorb && g < M ? (M - g + G - 1) / G : 0;
+    const int nw = g < nwin ? (nwin - g + G - 1) / G : 0;
+    const int n_items = ns + nw;
+    auto issue = [&](int it) {
+        float4* st = stage + (size_t)(it % kDecStages) * kPieces * kDecThreads + tid;
+        if (it < ns) {
+            const int i = g + G * it;
+            const float* rkp = SK + (size_t)i * D + 4 * j;
+            const float* rvp = SV + (size_t)i * D + 4 * j;
+            cp_async<16>(st, rkp);
+            cp_async<16>(st + kDecThreads, rkp + H2);
+            cp_async<16>(st + 2 * kDecThreads, rvp);
+            cp_async<16>(st + 3 * kDecThreads, rvp + H2);
+        } else {
+            const int s = s_lo + g + G * (it - ns);
+            const size_t e = (size_t)(s % wr) * D + 4 * j;
+            cp_async<PB>(st, rk + e);
+            cp_async<PB>(st + kDecThreads, rk + e + H2);
+            cp_async<PB>(st + 2 * kDecThreads, rv + e);
+            cp_async<PB>(st + 3 * kDecThreads, rv + e + H2);
+        }
+    };
+#pragma unroll
+    for (int it = 0; it < kDecStages - 1; it++) {
+        if (it < n_items) issue(it);
+        cp_async_commit();
+    }
+
+    // ---- q, RoPE(q, t), cos/sin at t, and the token that leaves the window
     for (int e = tid; e < D; e += kDecThreads) {
         sq[e] = to_f(q[e]);
         if (absorb) {
@@ -100,95 +158,140 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
     if (absorb)
         for (int i = tid; i < M; i += kDecThreads) slj[i] = w > 0 ? a.ring_la[((size_t)bh * wr + eo) * M + i] : la[i];
     for (int i = tid; i < H2; i += kDecThreads) {
-        float c, s;
-        rope_cs(a.rope, t, i, c, s);
+        float c, sn;
+        rope_cs(a.rope, t, i, c, sn);
+        cst[i] = make_float2(c, sn);
         const float x = to_f(q[i]), y = to_f(q[i + H2]);
-        sqr[i] = x * c - y * s;
-        sqr[i + H2] = y * c + x * s;
+        sqr[i] = x * c - y * sn;
+        sqr[i + H2] = y * c + x * sn;
     }
     __syncthreads();
 
-    WarpSoftmax<E> sm;
-    // ---- slots: absorb token t - w with its own gate, then L_i = q . S^K[i] / sqrt(d)
-    if (absorb) {
-        for (int i = g; i < M; i += G) {
-            const float al = expf(slj[i]), u = -expm1f(slj[i]);
-            float* sk = a.SK + ((size_t)bh * M + i) * D;
-            float* sv = a.SV + ((size_t)bh * M + i) * D;
-            float dot = 0.0f, val[E];
+    // the lane's elements: lo = 4j .. 4j+3, hi = d/2 + 4j .. d/2 + 4j+3
+    float ql[4], qh[4], rl[4], rh[4];
 #pragma unroll
-            for (int e = 0; e < E; e++) {
-                const int c = lane + 32 * e;
-                const float nk = al * sk[c] + u * skj[c];
-                const float nv = al * sv[c] + u * svj[c];
-                sk[c] = nk;
-                sv[c] = nv;
-                dot += sq[c] * nk;
-                val[e] = nv;
-            }
-            sm.push(warp_sum(dot) * scale, val);
-        }
+    for (int f = 0; f < 4; f++) {
+        ql[f] = sq[4 * j + f];
+        qh[f] = sq[H2 + 4 * j + f];
+        rl[f] = sqr[4 * j + f];
+        rh[f] = sqr[H2 + 4 * j + f];
     }
-    // ---- window keys s in [max(0, t - w + 1), t]: RoPE(q, t) . RoPE(k_s, s) / sqrt(d)
-    // (token t is read from the inputs, older ones from ring entry s mod w)
-    const int s0 = max(0, t - w + 1);
-    for (int base = s0 + g; base <= t; base += G * kDecBatch) {
-        float kv[kDecBatch][E], vv[kDecBatch][E];
+    float mx = -INFINITY, sum = 0.0f, acc[8];
 #pragma unroll
-        for (int b = 0; b < kDecBatch; b++) {
-            const int s = base + b * G;
-            if (s <= t) {
-                const Tin* ks_ = s == t ? k : rk + (size_t)(s % wr) * D;
-                const Tin* vs_ = s == t ? v : rv + (size_t)(s % wr) * D;
+    for (int f = 0; f < 8; f++) acc[f] = 0.0f;
+    auto push = [&](float logit, const float (&vl)[4], const float (&vh)[4]) {
+        const float mn = fmaxf(mx, logit);
+        const float sc = expf(mx - mn);  // 0 while mx = -inf
+        const float p = expf(logit - mn);
+        sum = sum * sc + p;
 #pragma unroll
-                for (int e = 0; e < E; e++) {
-                    kv[b][e] = to_f(ks_[lane + 32 * e]);
-                    vv[b][e] = to_f(vs_[lane + 32 * e]);
-                }
-            }
+        for (int f = 0; f < 4; f++) {
+            acc[f] = acc[f] * sc + p * vl[f];
+            acc[4 + f] = acc[4 + f] * sc + p * vh[f];
         }
+        mx = mn;
+    };
+    // cos/sin of the current window token and of the step G, per frequency 4j + f
+    float wc[4], wsn[4], stc[4], sts[4];
 #pragma unroll
-        for (int b = 0; b < kDecBatch; b++) {
-            const int s = base + b * G;
-            if (s > t) break;
+    for (int f = 0; f < 4; f++) rope_cs(a.rope, G, 4 * j + f, stc[f], sts[f]);
+
+    for (int it = 0; it < n_items; it++) {
+        if (it + kDecStages - 1 < n_items) issue(it + kDecStages - 1);
+        cp_async_commit();
+        cp_async_wait<kDecStages - 1>();
+        const float4* st = stage + (size_t)(it % kDecStages) * kPieces * kDecThreads + tid;
+        if (it < ns) {
+            // slot row i: absorb token t - w with its own gate, then L_i = q . S^K[i] / sqrt(d)
+            const int i = g + G * it;
+            const float al = expf(slj[i]), u = -expm1f(slj[i]);
+            float kl[4], kh[4], vl[4], vh[4];
+            load4(st, kl);
+            load4(st + kDecThreads, kh);
+            load4(st + 2 * kDecThreads, vl);
+            load4(st + 3 * kDecThreads, vh);
             float dot = 0.0f;
 #pragma unroll
-            for (int e = 0; e < E / 2; e++) {  // the pair (lane + 32 e, lane + 32 e + d/2)
-                const int i = lane + 32 * e;
-                float c, sn;
-                rope_cs(a.rope, s, i, c, sn);
-                const float x = kv[b][e], y = kv[b][e + E / 2];
-                dot += sqr[i] * (x * c - y * sn) + sqr[i + H2] * (y * c + x * sn);
+            for (int f = 0; f < 4; f++) {
+                kl[f] = al * kl[f] + u * skj[4 * j + f];
+                kh[f] = al * kh[f] + u * skj[H2 + 4 * j + f];
+                vl[f] = al * vl[f] + u * svj[4 * j + f];
+                vh[f] = al * vh[f] + u * svj[H2 + 4 * j + f];
+                dot += ql[f] * kl[f] + qh[f] * kh[f];
             }
-            sm.push(warp_sum(dot) * scale, vv[b]);
+            float* rkp = SK + (size_t)i * D + 4 * j;
+            float* rvp = SV + (size_t)i * D + 4 * j;
+            *(float4*)rkp = make_float4(kl[0], kl[1], kl[2], kl[3]);
+            *(float4*)(rkp + H2) = make_float4(kh[0], kh[1], kh[2], kh[3]);
+            *(float4*)rvp = make_float4(vl[0], vl[1], vl[2], vl[3]);
+            *(float4*)(rvp + H2) = make_float4(vh[0], vh[1], vh[2], vh[3]);
+            push(group_sum<GL>(dot, gmask) * scale, vl, vh);
+        } else {
+            // window token s: RoPE(q, t) . RoPE(k_s, s) / sqrt(d)
+            const int r = it - ns;
+            if (r % kReseed == 0) {
+                const int s = s_lo + g + G * r;
+#pragma unroll
+                for (int f = 0; f < 4; f++) rope_cs(a.rope, s, 4 * j + f, wc[f], wsn[f]);
+            }
+            float x[4], y[4], vl[4], vh[4];
+            load4((const V4*)st, x);
+            load4((const V4*)(st + kDecThreads), y);
+            load4((const V4*)(st + 2 * kDecThreads), vl);
+            load4((const V4*)(st + 3 * kDecThreads), vh);
+            float dot = 0.0f;
+#pragma unroll
+            for (int f = 0; f < 4; f++) {
+                dot += rl[f] * (x[f] * wc[f] - y[f] * wsn[f]) + rh[f] * (y[f] * wc[f] + x[f] * wsn[f]);
+                const float c2 = wc[f] * stc[f] - wsn[f] * sts[f];
+                wsn[f] = wsn[f] * stc[f] + wc[f] * sts[f];
+                wc[f] = c2;
+            }
+            push(group_sum<GL>(dot, gmask) * scale, vl, vh);
         }
     }
-    // ---- merge the warps of this CTA
-    if (lane == 0) {
-        wm[warp] = sm.mx;
-        ws[warp] = sm.sum;
+    cp_async_wait<0>();
+    // ---- token t itself (window, relative position 0), by group 0 of the cluster
+    if (g == 0 && w > 0) {
+        float x[4], y[4], vl[4], vh[4], dot = 0.0f;
+#pragma unroll
+        for (int f = 0; f < 4; f++) {
+            x[f] = to_f(k[4 * j + f]);
+            y[f] = to_f(k[H2 + 4 * j + f]);
+            vl[f] = to_f(v[4 * j + f]);
+            vh[f] = to_f(v[H2 + 4 * j + f]);
+            const float2 cs = cst[4 * j + f];
+            dot += rl[f] * (x[f] * cs.x - y[f] * cs.y) + rh[f] * (y[f] * cs.x + x[f] * cs.y);
+        }
+        push(group_sum<GL>(dot, gmask) * scale, vl, vh);
+    }
+    // ---- merge the groups of this CTA (their accumulators reuse the stages)
+    __syncthreads();
+    float* gacc = reinterpret_cast<float*>(stage);  // [NG][D]
+    if (j == 0) {
+        gmx[grp] = mx;
+        gsum[grp] = sum;
     }
 #pragma unroll
-    for (int e = 0; e < E; e++) wacc[warp][lane + 32 * e] = sm.acc[e];
+    for (int f = 0; f < 4; f++) {
+        gacc[grp * D + 4 * j + f] = acc[f];
+        gacc[grp * D + H2 + 4 * j + f] = acc[4 + f];
+    }
     __syncthreads();
     {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int x = 0; x < kDecWarps; x++) mx = fmaxf(mx, wm[x]);
-        float f[kDecWarps], tot = 0.0f;
-#pragma unroll
-        for (int x = 0; x < kDecWarps; x++) {
-            f[x] = wm[x] == -INFINITY ? 0.0f : expf(wm[x] - mx);
-            tot += ws[x] * f[x];
-        }
+        float m = -INFINITY;
+        for (int x = 0; x < NG; x++) m = fmaxf(m, gmx[x]);
         for (int e = tid; e < D; e += kDecThreads) {
             float r = 0.0f;
-#pragma unroll
-            for (int x = 0; x < kDecWarps; x++) r += wacc[x][e] * f[x];
+            for (int x = 0; x < NG; x++)
+                if (gmx[x] != -INFINITY) r += gacc[x * D + e] * expf(gmx[x] - m);
             bacc[e] = r;
         }
         if (tid == 0) {
-            bm = mx;
+            float tot = 0.0f;
+            for (int x = 0; x < NG; x++)
+                if (gmx[x] != -INFINITY) tot += gsum[x] * expf(gmx[x] - m);
+            bm = m;
             bs = tot;
         }
     }
@@ -230,24 +333,44 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
     cl.sync();
 }
 
-// Cluster size: doubled, up to 8 (the portable limit), while the grid fits
-// in one wave of four CTAs per SM (the register file holds four 256-thread
-// CTAs at 64 registers) and every warp keeps at least one slot or key.
-static int decode_cluster(const DecodeArgs& a, int m) {
-    const int s0 = a.t - a.w + 1 > 0 ? a.t - a.w + 1 : 0;
-    const int items = (a.t - a.w >= 0 ? m : 0) + (a.t - s0 + 1);
+constexpr size_t kDecSmem = (size_t)kDecStages * kPieces * kDecThreads * sizeof(float4);
+
+// Cluster size: doubled, up to 8 (the portable limit), while the grid stays
+// within one wave of resident CTAs and every group keeps at least four items.
+static int decode_cluster(const DecodeArgs& a, int m, int d, int resident) {
+    const int s_lo = a.t - a.w + 1 > 0 ? a.t - a.w + 1 : 0;
+    const int items = (a.t - a.w >= 0 ? m : 0) + (a.t - s_lo > 0 ? a.t - s_lo : 0);
+    const int groups = kDecThreads / (d / 8);
     int ks = 1;
-    while (ks < 8 && (long long)a.BH * ks * 2 <= 4LL * a.sms && ks * 2 * kDecWarps <= items) ks *= 2;
+    while (ks < 8 && (long long)a.BH * ks * 2 <= (long long)resident * a.sms && ks * 2 * groups * 4 <= items)
+        ks *= 2;
     return ks;
 }
 
 template <typename Tin, int D, int M>
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
     if (a.BH == 0) return cudaSuccess;
-    const int ks = decode_cluster(a, M);
+    static_assert(kDecStages * kPieces * kDecThreads * sizeof(float4) >= (kDecThreads / (D / 8)) * D * sizeof(float),
+                  "the group partials reuse the stages");
+    auto kern = decode_step_kernel<Tin, D, M>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmem);
+    if (e != cudaSuccess) return e;
+    static const int resident = [&] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kDecThreads, kDecSmem) != cudaSuccess || n < 1)
+            n = 1;
+        return n;
+    }();
+    int ks = decode_cluster(a, M, D, resident);
+    // tuning override of the cluster size (1, 2, 4 or 8 CTAs per head)
+    if (const char* env = getenv("NHA_DECODE_CLUSTER")) {
+        const int v = atoi(env);
+        if (v == 1 || v == 2 || v == 4 || v == 8) ks = v;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.BH * ks));
     cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = kDecSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -256,8 +379,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaSuccess;
-    NHA_LAUNCH("decode_step", st, e = cudaLaunchKernelEx(&cfg, decode_step_kernel<Tin, D, M>, a));
+    NHA_LAUNCH("decode_step", st, e = cudaLaunchKernelEx(&cfg, kern, a));
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

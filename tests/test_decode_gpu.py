@@ -166,3 +166,11 @@ def test_decode_bench_workload_layer_matches_the_oracle():
     _check_o(_np(o), o_ref, dw.dtype, dw.name)
     assert np.abs(_np(state[0]) - st.S_k).max() <= 1e-4
     assert np.abs(_np(state[1]) - st.S_v).max() <= 1e-4
+
+
+@pytest.mark.parametrize("ks", ["1", "2", "4", "8"])
+def test_decode_every_cluster_size(ks, monkeypatch):
+    """The result does not depend on how many CTAs share a head (tuning override)."""
+    monkeypatch.setenv("NHA_DECODE_CLUSTER", ks)
+    test_decode_batch_matches_the_decode_oracle(2, 4, 128, 64, 512, 1000, "bf16")
+    test_decode_batch_matches_the_decode_oracle(1, 3, 64, 16, 100, 60, "f32")
