@@ -33,9 +33,9 @@ namespace nha {
 
 namespace {
 constexpr int kDecThreads = 256;
-constexpr int kDecStages = 4;  // items a lane has in flight or ready
+constexpr int kDecStages = 8;  // pipeline entries a lane has in flight or ready
 constexpr int kReseed = 16;    // window items between exact cos/sin evaluations
-constexpr int kPieces = 4;     // 16-byte shared-memory pieces per lane and stage
+constexpr int kPieces = 2;     // 16-byte shared-memory pieces per lane and stage
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -90,7 +90,6 @@ template <typename Tin, int D, int M>
 __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeArgs a) {
     constexpr int H2 = D / 2, GL = D / 8, NG = kDecThreads / GL;
     using V4 = typename Vec4<Tin>::T;
-    constexpr int PB = sizeof(V4);  // bytes of a lane's 4-element window piece
     extern __shared__ float4 stage[];  // [kDecStages][kPieces][kDecThreads]; later the groups' partials
     __shared__ float sq[D], sqr[D], skj[D], svj[D], slj[M];
     __shared__ float2 cst[H2];  // cos, sin at position t
@@ -119,31 +118,41 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
     float* SV = a.SV + (size_t)bh * M * D;
 
     // ---- this group's items: slot rows g, g + G, ... then window tokens s_lo + g, s_lo + g + G, ...
+    // Each item streams through the lane's stages as pipeline entries of two
+    // 16-byte pieces: a slot row as two entries (its S^K pieces, then its S^V
+    // pieces), a bf16 window token as one entry (k lo|hi, then v lo|hi, 8 bytes
+    // each), an fp32 window token as two (k lo, k hi; then v lo, v hi).
+    constexpr int EW = sizeof(Tin) == 2 ? 1 : 2;  // entries of a window token
     const int ns = absorb && g < M ? (M - g + G - 1) / G : 0;
     const int nw = g < nwin ? (nwin - g + G - 1) / G : 0;
-    const int n_items = ns + nw;
-    auto issue = [&](int it) {
-        float4* st = stage + (size_t)(it % kDecStages) * kPieces * kDecThreads + tid;
-        if (it < ns) {
-            const int i = g + G * it;
-            const float* rkp = SK + (size_t)i * D + 4 * j;
-            const float* rvp = SV + (size_t)i * D + 4 * j;
-            cp_async<16>(st, rkp);
-            cp_async<16>(st + kDecThreads, rkp + H2);
-            cp_async<16>(st + 2 * kDecThreads, rvp);
-            cp_async<16>(st + 3 * kDecThreads, rvp + H2);
+    const int n_entries = 2 * ns + EW * nw;
+    auto issue = [&](int en) {
+        float4* st = stage + (size_t)(en % kDecStages) * kPieces * kDecThreads + tid;
+        if (en < 2 * ns) {
+            const int i = g + G * (en >> 1);
+            const float* src = ((en & 1) ? SV : SK) + (size_t)i * D + 4 * j;
+            cp_async<16>(st, src);
+            cp_async<16>(st + kDecThreads, src + H2);
         } else {
-            const int s = s_lo + g + G * (it - ns);
+            const int x = en - 2 * ns;
+            const int s = s_lo + g + G * (x / EW);
             const size_t e = (size_t)(s % wr) * D + 4 * j;
-            cp_async<PB>(st, rk + e);
-            cp_async<PB>(st + kDecThreads, rk + e + H2);
-            cp_async<PB>(st + 2 * kDecThreads, rv + e);
-            cp_async<PB>(st + 3 * kDecThreads, rv + e + H2);
+            if constexpr (EW == 1) {
+                char* b = reinterpret_cast<char*>(st);
+                cp_async<8>(b, rk + e);
+                cp_async<8>(b + 8, rk + e + H2);
+                cp_async<8>(b + 16 * kDecThreads, rv + e);
+                cp_async<8>(b + 16 * kDecThreads + 8, rv + e + H2);
+            } else {
+                const Tin* src = (x & 1) ? rv : rk;
+                cp_async<16>(st, src + e);
+                cp_async<16>(st + kDecThreads, src + e + H2);
+            }
         }
     };
 #pragma unroll
-    for (int it = 0; it < kDecStages - 1; it++) {
-        if (it < n_items) issue(it);
+    for (int en = 0; en < kDecStages - 1; en++) {
+        if (en < n_entries) issue(en);
         cp_async_commit();
     }
 
@@ -196,58 +205,76 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
 #pragma unroll
     for (int f = 0; f < 4; f++) rope_cs(a.rope, G, 4 * j + f, stc[f], sts[f]);
 
-    for (int it = 0; it < n_items; it++) {
-        if (it + kDecStages - 1 < n_items) issue(it + kDecStages - 1);
+    float kl[4], kh[4], dot = 0.0f;  // a two-entry item's key part, kept for its value entry
+    for (int en = 0; en < n_entries; en++) {
+        if (en + kDecStages - 1 < n_entries) issue(en + kDecStages - 1);
         cp_async_commit();
         cp_async_wait<kDecStages - 1>();
-        const float4* st = stage + (size_t)(it % kDecStages) * kPieces * kDecThreads + tid;
-        if (it < ns) {
+        const float4* st = stage + (size_t)(en % kDecStages) * kPieces * kDecThreads + tid;
+        if (en < 2 * ns) {
             // slot row i: absorb token t - w with its own gate, then L_i = q . S^K[i] / sqrt(d)
-            const int i = g + G * it;
+            const int i = g + G * (en >> 1);
             const float al = expf(slj[i]), u = -expm1f(slj[i]);
-            float kl[4], kh[4], vl[4], vh[4];
-            load4(st, kl);
-            load4(st + kDecThreads, kh);
-            load4(st + 2 * kDecThreads, vl);
-            load4(st + 3 * kDecThreads, vh);
-            float dot = 0.0f;
+            float lo[4], hi[4];
+            load4(st, lo);
+            load4(st + kDecThreads, hi);
+            const float* src = (en & 1) ? svj : skj;
 #pragma unroll
             for (int f = 0; f < 4; f++) {
-                kl[f] = al * kl[f] + u * skj[4 * j + f];
-                kh[f] = al * kh[f] + u * skj[H2 + 4 * j + f];
-                vl[f] = al * vl[f] + u * svj[4 * j + f];
-                vh[f] = al * vh[f] + u * svj[H2 + 4 * j + f];
-                dot += ql[f] * kl[f] + qh[f] * kh[f];
+                lo[f] = al * lo[f] + u * src[4 * j + f];
+                hi[f] = al * hi[f] + u * src[H2 + 4 * j + f];
             }
-            float* rkp = SK + (size_t)i * D + 4 * j;
-            float* rvp = SV + (size_t)i * D + 4 * j;
-            *(float4*)rkp = make_float4(kl[0], kl[1], kl[2], kl[3]);
-            *(float4*)(rkp + H2) = make_float4(kh[0], kh[1], kh[2], kh[3]);
-            *(float4*)rvp = make_float4(vl[0], vl[1], vl[2], vl[3]);
-            *(float4*)(rvp + H2) = make_float4(vh[0], vh[1], vh[2], vh[3]);
-            push(group_sum<GL>(dot, gmask) * scale, vl, vh);
+            float* dst = ((en & 1) ? SV : SK) + (size_t)i * D + 4 * j;
+            *(float4*)dst = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            *(float4*)(dst + H2) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+            if (!(en & 1)) {
+                dot = 0.0f;
+#pragma unroll
+                for (int f = 0; f < 4; f++) dot += ql[f] * lo[f] + qh[f] * hi[f];
+                dot = group_sum<GL>(dot, gmask) * scale;
+            } else {
+                push(dot, lo, hi);
+            }
         } else {
             // window token s: RoPE(q, t) . RoPE(k_s, s) / sqrt(d)
-            const int r = it - ns;
-            if (r % kReseed == 0) {
-                const int s = s_lo + g + G * r;
+            const int x = en - 2 * ns, r = x / EW;
+            const bool key_part = EW == 1 || !(x & 1);
+            if (key_part) {
+                if (r % kReseed == 0) {
+                    const int s = s_lo + g + G * r;
 #pragma unroll
-                for (int f = 0; f < 4; f++) rope_cs(a.rope, s, 4 * j + f, wc[f], wsn[f]);
-            }
-            float x[4], y[4], vl[4], vh[4];
-            load4((const V4*)st, x);
-            load4((const V4*)(st + kDecThreads), y);
-            load4((const V4*)(st + 2 * kDecThreads), vl);
-            load4((const V4*)(st + 3 * kDecThreads), vh);
-            float dot = 0.0f;
+                    for (int f = 0; f < 4; f++) rope_cs(a.rope, s, 4 * j + f, wc[f], wsn[f]);
+                }
+                if constexpr (EW == 1) {
+                    const char* b = reinterpret_cast<const char*>(st);
+                    load4((const V4*)b, kl);
+                    load4((const V4*)(b + 8), kh);
+                } else {
+                    load4((const V4*)st, kl);
+                    load4((const V4*)(st + kDecThreads), kh);
+                }
+                dot = 0.0f;
 #pragma unroll
-            for (int f = 0; f < 4; f++) {
-                dot += rl[f] * (x[f] * wc[f] - y[f] * wsn[f]) + rh[f] * (y[f] * wc[f] + x[f] * wsn[f]);
-                const float c2 = wc[f] * stc[f] - wsn[f] * sts[f];
-                wsn[f] = wsn[f] * stc[f] + wc[f] * sts[f];
-                wc[f] = c2;
+                for (int f = 0; f < 4; f++) {
+                    dot += rl[f] * (kl[f] * wc[f] - kh[f] * wsn[f]) + rh[f] * (kh[f] * wc[f] + kl[f] * wsn[f]);
+                    const float c2 = wc[f] * stc[f] - wsn[f] * sts[f];
+                    wsn[f] = wsn[f] * stc[f] + wc[f] * sts[f];
+                    wc[f] = c2;
+                }
+                dot = group_sum<GL>(dot, gmask) * scale;
             }
-            push(group_sum<GL>(dot, gmask) * scale, vl, vh);
+            if (EW == 1 || !key_part) {
+                float vl[4], vh[4];
+                if constexpr (EW == 1) {
+                    const char* b = reinterpret_cast<const char*>(st + kDecThreads);
+                    load4((const V4*)b, vl);
+                    load4((const V4*)(b + 8), vh);
+                } else {
+                    load4((const V4*)st, vl);
+                    load4((const V4*)(st + kDecThreads), vh);
+                }
+                push(dot, vl, vh);
+            }
         }
     }
     cp_async_wait<0>();
