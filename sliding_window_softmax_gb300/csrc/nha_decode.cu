@@ -14,12 +14,14 @@
 // its group's next items from global memory into its own shared-memory stages
 // with cp.async, kDecStages items deep, so no lane waits on another's copy and
 // the SM keeps tens of KB of reads in flight.  A slot item absorbs the
-// leaving token into the row (written back in place) and scores it; a window
-// item scores the raw key rotated to its position, the cos/sin advanced from
-// item to item by angle addition (the group's positions step by a constant)
-// and re-seeded exactly every kReseed items.  Each group runs an online
-// softmax with its lanes' share of the output; the groups of a CTA merge in
-// shared memory, the CTAs of the cluster through distributed shared memory.
+// leaving token into the row (written back in place) and scores it.  A window
+// item scores the raw key: with pairs taken as complex numbers, the rotary
+// logit RoPE(q, t) . RoPE(k_s, s) = Re(k_s conj(W_s)), W_s = RoPE(q, t) e^{-i theta s},
+// and W advances from one of the group's tokens to the next (positions step
+// by a constant) by one complex product, re-seeded exactly every kReseed
+// items.  Each group runs an online softmax in base 2 with its lanes' share of
+// the output; the groups of a CTA merge in shared memory, the CTAs of the
+// cluster through distributed shared memory.
 #include <cooperative_groups.h>
 #include <stdlib.h>
 
@@ -33,7 +35,7 @@ namespace nha {
 
 namespace {
 constexpr int kDecThreads = 256;
-constexpr int kDecStages = 8;  // pipeline entries a lane has in flight or ready
+constexpr int kDecStages = 6;  // pipeline entries a lane has in flight or ready
 constexpr int kReseed = 16;    // window items between exact cos/sin evaluations
 constexpr int kPieces = 2;     // 16-byte shared-memory pieces per lane and stage
 
@@ -78,6 +80,13 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// 2^x (the MUFU approximation, relative error below 2^-22; ex2(-inf) = 0)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <int GL>
 __device__ __forceinline__ float group_sum(float x, unsigned mask) {
 #pragma unroll
@@ -87,7 +96,7 @@ __device__ __forceinline__ float group_sum(float x, unsigned mask) {
 }  // namespace
 
 template <typename Tin, int D, int M>
-__global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const DecodeArgs a) {
     constexpr int H2 = D / 2, GL = D / 8, NG = kDecThreads / GL;
     using V4 = typename Vec4<Tin>::T;
     extern __shared__ float4 stage[];  // [kDecStages][kPieces][kDecThreads]; later the groups' partials
@@ -126,17 +135,19 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
     const int ns = absorb && g < M ? (M - g + G - 1) / G : 0;
     const int nw = g < nwin ? (nwin - g + G - 1) / G : 0;
     const int n_entries = 2 * ns + EW * nw;
-    auto issue = [&](int en) {
-        float4* st = stage + (size_t)(en % kDecStages) * kPieces * kDecThreads + tid;
-        if (en < 2 * ns) {
-            const int i = g + G * (en >> 1);
-            const float* src = ((en & 1) ? SV : SK) + (size_t)i * D + 4 * j;
+    // issue cursor: the next entry, its stage and (window part) ring entry
+    int i_en = 0, i_stage = 0, i_ring = (s_lo + g) % wr;
+    const int ring_step = G % wr;
+    auto issue_next = [&]() {
+        float4* st = stage + (size_t)i_stage * kPieces * kDecThreads + tid;
+        if (i_en < 2 * ns) {
+            const int i = g + G * (i_en >> 1);
+            const float* src = ((i_en & 1) ? SV : SK) + (size_t)i * D + 4 * j;
             cp_async<16>(st, src);
             cp_async<16>(st + kDecThreads, src + H2);
         } else {
-            const int x = en - 2 * ns;
-            const int s = s_lo + g + G * (x / EW);
-            const size_t e = (size_t)(s % wr) * D + 4 * j;
+            const size_t e = (size_t)i_ring * D + 4 * j;
+            const int x = i_en - 2 * ns;
             if constexpr (EW == 1) {
                 char* b = reinterpret_cast<char*>(st);
                 cp_async<8>(b, rk + e);
@@ -148,11 +159,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
                 cp_async<16>(st, src + e);
                 cp_async<16>(st + kDecThreads, src + e + H2);
             }
+            if (EW == 1 || (x & 1)) {  // the token's last entry: move to the group's next token
+                i_ring += ring_step;
+                if (i_ring >= wr) i_ring -= wr;
+            }
         }
+        i_en++;
+        i_stage = i_stage + 1 == kDecStages ? 0 : i_stage + 1;
     };
 #pragma unroll
-    for (int en = 0; en < kDecStages - 1; en++) {
-        if (en < n_entries) issue(en);
+    for (int x = 0; x < kDecStages - 1; x++) {
+        if (i_en < n_entries) issue_next();
         cp_async_commit();
     }
 
@@ -177,40 +194,45 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
     __syncthreads();
 
     // the lane's elements: lo = 4j .. 4j+3, hi = d/2 + 4j .. d/2 + 4j+3
-    float ql[4], qh[4], rl[4], rh[4];
-#pragma unroll
-    for (int f = 0; f < 4; f++) {
-        ql[f] = sq[4 * j + f];
-        qh[f] = sq[H2 + 4 * j + f];
-        rl[f] = sqr[4 * j + f];
-        rh[f] = sqr[H2 + 4 * j + f];
-    }
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float l2scale = scale * kLog2e;  // logits in base-2 units
     float mx = -INFINITY, sum = 0.0f, acc[8];
 #pragma unroll
     for (int f = 0; f < 8; f++) acc[f] = 0.0f;
-    auto push = [&](float logit, const float (&vl)[4], const float (&vh)[4]) {
-        const float mn = fmaxf(mx, logit);
-        const float sc = expf(mx - mn);  // 0 while mx = -inf
-        const float p = expf(logit - mn);
-        sum = sum * sc + p;
+    auto push = [&](float l, const float (&vl)[4], const float (&vh)[4]) {
+        if (l > mx) {  // uniform in the group (every lane holds the group's sum)
+            const float sc = ex2(mx - l);
+            sum *= sc;
+#pragma unroll
+            for (int f = 0; f < 8; f++) acc[f] *= sc;
+            mx = l;
+        }
+        const float p = ex2(l - mx);
+        sum += p;
 #pragma unroll
         for (int f = 0; f < 4; f++) {
-            acc[f] = acc[f] * sc + p * vl[f];
-            acc[4 + f] = acc[4 + f] * sc + p * vh[f];
+            acc[f] = fmaf(p, vl[f], acc[f]);
+            acc[4 + f] = fmaf(p, vh[f], acc[4 + f]);
         }
-        mx = mn;
     };
-    // cos/sin of the current window token and of the step G, per frequency 4j + f
-    float wc[4], wsn[4], stc[4], sts[4];
+    // W = RoPE(q, t) e^{-i theta s} of the group's current token, and the step e^{-i theta G}
+    float wre[4], wim[4], gre[4], gim[4];
 #pragma unroll
-    for (int f = 0; f < 4; f++) rope_cs(a.rope, G, 4 * j + f, stc[f], sts[f]);
+    for (int f = 0; f < 4; f++) {
+        float c, sn;
+        rope_cs(a.rope, G, 4 * j + f, c, sn);
+        gre[f] = c;
+        gim[f] = -sn;
+    }
 
-    float kl[4], kh[4], dot = 0.0f;  // a two-entry item's key part, kept for its value entry
+    float dot = 0.0f;  // a slot row's logit, kept from its S^K entry for its S^V entry
+    int c_stage = 0;
     for (int en = 0; en < n_entries; en++) {
-        if (en + kDecStages - 1 < n_entries) issue(en + kDecStages - 1);
+        if (i_en < n_entries) issue_next();
         cp_async_commit();
         cp_async_wait<kDecStages - 1>();
-        const float4* st = stage + (size_t)(en % kDecStages) * kPieces * kDecThreads + tid;
+        const float4* st = stage + (size_t)c_stage * kPieces * kDecThreads + tid;
+        c_stage = c_stage + 1 == kDecStages ? 0 : c_stage + 1;
         if (en < 2 * ns) {
             // slot row i: absorb token t - w with its own gate, then L_i = q . S^K[i] / sqrt(d)
             const int i = g + G * (en >> 1);
@@ -230,21 +252,28 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
             if (!(en & 1)) {
                 dot = 0.0f;
 #pragma unroll
-                for (int f = 0; f < 4; f++) dot += ql[f] * lo[f] + qh[f] * hi[f];
-                dot = group_sum<GL>(dot, gmask) * scale;
+                for (int f = 0; f < 4; f++) dot += sq[4 * j + f] * lo[f] + sq[H2 + 4 * j + f] * hi[f];
+                dot = group_sum<GL>(dot, gmask) * l2scale;
             } else {
                 push(dot, lo, hi);
             }
         } else {
-            // window token s: RoPE(q, t) . RoPE(k_s, s) / sqrt(d)
+            // window token s: Re(k_s conj(W_s)) / sqrt(d)
             const int x = en - 2 * ns, r = x / EW;
             const bool key_part = EW == 1 || !(x & 1);
             if (key_part) {
                 if (r % kReseed == 0) {
                     const int s = s_lo + g + G * r;
 #pragma unroll
-                    for (int f = 0; f < 4; f++) rope_cs(a.rope, s, 4 * j + f, wc[f], wsn[f]);
+                    for (int f = 0; f < 4; f++) {
+                        float c, sn;
+                        rope_cs(a.rope, s, 4 * j + f, c, sn);
+                        const float ql = sqr[4 * j + f], qh = sqr[H2 + 4 * j + f];
+                        wre[f] = ql * c + qh * sn;
+                        wim[f] = qh * c - ql * sn;
+                    }
                 }
+                float kl[4], kh[4];
                 if constexpr (EW == 1) {
                     const char* b = reinterpret_cast<const char*>(st);
                     load4((const V4*)b, kl);
@@ -256,12 +285,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
                 dot = 0.0f;
 #pragma unroll
                 for (int f = 0; f < 4; f++) {
-                    dot += rl[f] * (kl[f] * wc[f] - kh[f] * wsn[f]) + rh[f] * (kh[f] * wc[f] + kl[f] * wsn[f]);
-                    const float c2 = wc[f] * stc[f] - wsn[f] * sts[f];
-                    wsn[f] = wsn[f] * stc[f] + wc[f] * sts[f];
-                    wc[f] = c2;
+                    dot = fmaf(kl[f], wre[f], fmaf(kh[f], wim[f], dot));
+                    const float re = wre[f] * gre[f] - wim[f] * gim[f];
+                    wim[f] = wre[f] * gim[f] + wim[f] * gre[f];
+                    wre[f] = re;
                 }
-                dot = group_sum<GL>(dot, gmask) * scale;
+                dot = group_sum<GL>(dot, gmask) * l2scale;
             }
             if (EW == 1 || !key_part) {
                 float vl[4], vh[4];
@@ -280,17 +309,16 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
     cp_async_wait<0>();
     // ---- token t itself (window, relative position 0), by group 0 of the cluster
     if (g == 0 && w > 0) {
-        float x[4], y[4], vl[4], vh[4], dot = 0.0f;
+        float vl[4], vh[4], d0 = 0.0f;
 #pragma unroll
         for (int f = 0; f < 4; f++) {
-            x[f] = to_f(k[4 * j + f]);
-            y[f] = to_f(k[H2 + 4 * j + f]);
+            const float x = to_f(k[4 * j + f]), y = to_f(k[H2 + 4 * j + f]);
             vl[f] = to_f(v[4 * j + f]);
             vh[f] = to_f(v[H2 + 4 * j + f]);
             const float2 cs = cst[4 * j + f];
-            dot += rl[f] * (x[f] * cs.x - y[f] * cs.y) + rh[f] * (y[f] * cs.x + x[f] * cs.y);
+            d0 += sqr[4 * j + f] * (x * cs.x - y * cs.y) + sqr[H2 + 4 * j + f] * (y * cs.x + x * cs.y);
         }
-        push(group_sum<GL>(dot, gmask) * scale, vl, vh);
+        push(group_sum<GL>(d0, gmask) * l2scale, vl, vh);
     }
     // ---- merge the groups of this CTA (their accumulators reuse the stages)
     __syncthreads();
@@ -311,13 +339,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
         for (int e = tid; e < D; e += kDecThreads) {
             float r = 0.0f;
             for (int x = 0; x < NG; x++)
-                if (gmx[x] != -INFINITY) r += gacc[x * D + e] * expf(gmx[x] - m);
+                if (gmx[x] != -INFINITY) r += gacc[x * D + e] * ex2(gmx[x] - m);
             bacc[e] = r;
         }
         if (tid == 0) {
             float tot = 0.0f;
             for (int x = 0; x < NG; x++)
-                if (gmx[x] != -INFINITY) tot += gsum[x] * expf(gmx[x] - m);
+                if (gmx[x] != -INFINITY) tot += gsum[x] * ex2(gmx[x] - m);
             bm = m;
             bs = tot;
         }
@@ -343,7 +371,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
         float tot = 0.0f;
         for (int r = 0; r < ks; r++) {
             const float mr = *cl.map_shared_rank(&bm, r);
-            tot += mr == -INFINITY ? 0.0f : *cl.map_shared_rank(&bs, r) * expf(mr - mx);
+            tot += mr == -INFINITY ? 0.0f : *cl.map_shared_rank(&bs, r) * ex2(mr - mx);
         }
         const float inv = 1.0f / tot;  // tot >= 1: the largest logit contributes exp(0)
         const int per = D / ks;
@@ -351,7 +379,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const DecodeAr
             float o = 0.0f;
             for (int r = 0; r < ks; r++) {
                 const float mr = *cl.map_shared_rank(&bm, r);
-                if (mr != -INFINITY) o += cl.map_shared_rank(bacc, r)[e] * expf(mr - mx);
+                if (mr != -INFINITY) o += cl.map_shared_rank(bacc, r)[e] * ex2(mr - mx);
             }
             ((Tin*)a.o)[(size_t)bh * D + e] = from_f<Tin>(o * inv);
         }
