@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
     extern __shared__ float4 stage[];  // [kDecStages][kPieces][kDecThreads]; later the groups' partials
     __shared__ float sq[D], sqr[D], skj[D], svj[D], slj[M];
     __shared__ float2 cst[H2];  // cos, sin at position t
+    __shared__ float2 gst[H2];  // e^{-i theta G}: the rotation between a group's consecutive tokens
     __shared__ float gmx[NG], gsum[NG];
     __shared__ float bm, bs, bacc[D];  // this CTA's merged partial, read by the cluster
     cg::cluster_group cl = cg::this_cluster();
@@ -138,40 +139,42 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
     // issue cursor: the next entry, its stage and (window part) ring entry
     int i_en = 0, i_stage = 0, i_ring = (s_lo + g) % wr;
     const int ring_step = G % wr;
-    auto issue_next = [&]() {
-        float4* st = stage + (size_t)i_stage * kPieces * kDecThreads + tid;
-        if (i_en < 2 * ns) {
-            const int i = g + G * (i_en >> 1);
-            const float* src = ((i_en & 1) ? SV : SK) + (size_t)i * D + 4 * j;
-            cp_async<16>(st, src);
-            cp_async<16>(st + kDecThreads, src + H2);
-        } else {
-            const size_t e = (size_t)i_ring * D + 4 * j;
-            const int x = i_en - 2 * ns;
-            if constexpr (EW == 1) {
-                char* b = reinterpret_cast<char*>(st);
-                cp_async<8>(b, rk + e);
-                cp_async<8>(b + 8, rk + e + H2);
-                cp_async<8>(b + 16 * kDecThreads, rv + e);
-                cp_async<8>(b + 16 * kDecThreads + 8, rv + e + H2);
+    // issue the next entry (if any) as its own commit group: every call commits
+    // one group, so "entry n complete" is "all but the last (issued - n - 1) groups"
+    auto issue_commit = [&]() {
+        if (i_en < n_entries) {
+            float4* st = stage + (size_t)i_stage * kPieces * kDecThreads + tid;
+            if (i_en < 2 * ns) {
+                const int i = g + G * (i_en >> 1);
+                const float* src = ((i_en & 1) ? SV : SK) + (size_t)i * D + 4 * j;
+                cp_async<16>(st, src);
+                cp_async<16>(st + kDecThreads, src + H2);
             } else {
-                const Tin* src = (x & 1) ? rv : rk;
-                cp_async<16>(st, src + e);
-                cp_async<16>(st + kDecThreads, src + e + H2);
+                const size_t e = (size_t)i_ring * D + 4 * j;
+                const int x = i_en - 2 * ns;
+                if constexpr (EW == 1) {
+                    char* b = reinterpret_cast<char*>(st);
+                    cp_async<8>(b, rk + e);
+                    cp_async<8>(b + 8, rk + e + H2);
+                    cp_async<8>(b + 16 * kDecThreads, rv + e);
+                    cp_async<8>(b + 16 * kDecThreads + 8, rv + e + H2);
+                } else {
+                    const Tin* src = (x & 1) ? rv : rk;
+                    cp_async<16>(st, src + e);
+                    cp_async<16>(st + kDecThreads, src + e + H2);
+                }
+                if (EW == 1 || (x & 1)) {  // the token's last entry: on to the group's next token
+                    i_ring += ring_step;
+                    if (i_ring >= wr) i_ring -= wr;
+                }
             }
-            if (EW == 1 || (x & 1)) {  // the token's last entry: move to the group's next token
-                i_ring += ring_step;
-                if (i_ring >= wr) i_ring -= wr;
-            }
+            i_en++;
+            i_stage = i_stage + 1 == kDecStages ? 0 : i_stage + 1;
         }
-        i_en++;
-        i_stage = i_stage + 1 == kDecStages ? 0 : i_stage + 1;
+        cp_async_commit();
     };
 #pragma unroll
-    for (int x = 0; x < kDecStages - 1; x++) {
-        if (i_en < n_entries) issue_next();
-        cp_async_commit();
-    }
+    for (int x = 0; x < kDecStages - 1; x++) issue_commit();
 
     // ---- q, RoPE(q, t), cos/sin at t, and the token that leaves the window
     for (int e = tid; e < D; e += kDecThreads) {
@@ -190,6 +193,8 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
         const float x = to_f(q[i]), y = to_f(q[i + H2]);
         sqr[i] = x * c - y * sn;
         sqr[i + H2] = y * c + x * sn;
+        rope_cs(a.rope, G, i, c, sn);
+        gst[i] = make_float2(c, -sn);
     }
     __syncthreads();
 
@@ -215,96 +220,124 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
             acc[4 + f] = fmaf(p, vh[f], acc[4 + f]);
         }
     };
-    // W = RoPE(q, t) e^{-i theta s} of the group's current token, and the step e^{-i theta G}
-    float wre[4], wim[4], gre[4], gim[4];
-#pragma unroll
-    for (int f = 0; f < 4; f++) {
-        float c, sn;
-        rope_cs(a.rope, G, 4 * j + f, c, sn);
-        gre[f] = c;
-        gim[f] = -sn;
-    }
+    // W = RoPE(q, t) e^{-i theta s} of the group's current token
+    float wre[4], wim[4];
 
-    float dot = 0.0f;  // a slot row's logit, kept from its S^K entry for its S^V entry
-    int c_stage = 0;
-    for (int en = 0; en < n_entries; en++) {
-        if (i_en < n_entries) issue_next();
-        cp_async_commit();
-        cp_async_wait<kDecStages - 1>();
-        const float4* st = stage + (size_t)c_stage * kPieces * kDecThreads + tid;
-        c_stage = c_stage + 1 == kDecStages ? 0 : c_stage + 1;
-        if (en < 2 * ns) {
-            // slot row i: absorb token t - w with its own gate, then L_i = q . S^K[i] / sqrt(d)
-            const int i = g + G * (en >> 1);
-            const float al = expf(slj[i]), u = -expm1f(slj[i]);
-            float lo[4], hi[4];
-            load4(st, lo);
-            load4(st + kDecThreads, hi);
-            const float* src = (en & 1) ? svj : skj;
+    int c_stage = 0;  // stage of the next entry to consume
+    auto stage_at = [&](int ahead) {
+        const int x = c_stage + ahead;
+        return stage + (size_t)(x >= kDecStages ? x - kDecStages : x) * kPieces * kDecThreads + tid;
+    };
+    auto advance = [&](int n) {
+        c_stage += n;
+        if (c_stage >= kDecStages) c_stage -= kDecStages;
+    };
+    // ---- slot rows: absorb token t - w with its own gate, then L_i = q . S^K[i] / sqrt(d)
+    for (int r = 0; r < ns; r++) {
+        cp_async_wait<kDecStages - 3>();  // the row's S^K and S^V entries
+        const int i = g + G * r;
+        const float al = expf(slj[i]), u = -expm1f(slj[i]);
+        float kl[4], kh[4], vl[4], vh[4];
+        load4(stage_at(0), kl);
+        load4(stage_at(0) + kDecThreads, kh);
+        load4(stage_at(1), vl);
+        load4(stage_at(1) + kDecThreads, vh);
+        advance(2);
+        float dot = 0.0f;
+#pragma unroll
+        for (int f = 0; f < 4; f++) {
+            kl[f] = al * kl[f] + u * skj[4 * j + f];
+            kh[f] = al * kh[f] + u * skj[H2 + 4 * j + f];
+            vl[f] = al * vl[f] + u * svj[4 * j + f];
+            vh[f] = al * vh[f] + u * svj[H2 + 4 * j + f];
+            dot += sq[4 * j + f] * kl[f] + sq[H2 + 4 * j + f] * kh[f];
+        }
+        float* dk = SK + (size_t)i * D + 4 * j;
+        float* dv = SV + (size_t)i * D + 4 * j;
+        *(float4*)dk = make_float4(kl[0], kl[1], kl[2], kl[3]);
+        *(float4*)(dk + H2) = make_float4(kh[0], kh[1], kh[2], kh[3]);
+        *(float4*)dv = make_float4(vl[0], vl[1], vl[2], vl[3]);
+        *(float4*)(dv + H2) = make_float4(vh[0], vh[1], vh[2], vh[3]);
+        push(group_sum<GL>(dot, gmask) * l2scale, vl, vh);
+        issue_commit();
+        issue_commit();
+    }
+    // ---- window tokens, two per iteration: Re(k_s conj(W_s)) / sqrt(d)
+    int reseed = 0;  // items until the next exact evaluation of W
+    for (int r = 0; r < nw; r += 2) {
+        const bool two = r + 1 < nw;
+        cp_async_wait<kDecStages - 1 - 2 * EW>();  // both tokens' entries (a missing one's groups are empty)
+        if (reseed == 0) {
+            const int s = s_lo + g + G * r;
 #pragma unroll
             for (int f = 0; f < 4; f++) {
-                lo[f] = al * lo[f] + u * src[4 * j + f];
-                hi[f] = al * hi[f] + u * src[H2 + 4 * j + f];
+                float c, sn;
+                rope_cs(a.rope, s, 4 * j + f, c, sn);
+                const float ql = sqr[4 * j + f], qh = sqr[H2 + 4 * j + f];
+                wre[f] = ql * c + qh * sn;
+                wim[f] = qh * c - ql * sn;
             }
-            float* dst = ((en & 1) ? SV : SK) + (size_t)i * D + 4 * j;
-            *(float4*)dst = make_float4(lo[0], lo[1], lo[2], lo[3]);
-            *(float4*)(dst + H2) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-            if (!(en & 1)) {
-                dot = 0.0f;
-#pragma unroll
-                for (int f = 0; f < 4; f++) dot += sq[4 * j + f] * lo[f] + sq[H2 + 4 * j + f] * hi[f];
-                dot = group_sum<GL>(dot, gmask) * l2scale;
-            } else {
-                push(dot, lo, hi);
-            }
-        } else {
-            // window token s: Re(k_s conj(W_s)) / sqrt(d)
-            const int x = en - 2 * ns, r = x / EW;
-            const bool key_part = EW == 1 || !(x & 1);
-            if (key_part) {
-                if (r % kReseed == 0) {
-                    const int s = s_lo + g + G * r;
-#pragma unroll
-                    for (int f = 0; f < 4; f++) {
-                        float c, sn;
-                        rope_cs(a.rope, s, 4 * j + f, c, sn);
-                        const float ql = sqr[4 * j + f], qh = sqr[H2 + 4 * j + f];
-                        wre[f] = ql * c + qh * sn;
-                        wim[f] = qh * c - ql * sn;
-                    }
-                }
-                float kl[4], kh[4];
-                if constexpr (EW == 1) {
-                    const char* b = reinterpret_cast<const char*>(st);
-                    load4((const V4*)b, kl);
-                    load4((const V4*)(b + 8), kh);
-                } else {
-                    load4((const V4*)st, kl);
-                    load4((const V4*)(st + kDecThreads), kh);
-                }
-                dot = 0.0f;
-#pragma unroll
-                for (int f = 0; f < 4; f++) {
-                    dot = fmaf(kl[f], wre[f], fmaf(kh[f], wim[f], dot));
-                    const float re = wre[f] * gre[f] - wim[f] * gim[f];
-                    wim[f] = wre[f] * gim[f] + wim[f] * gre[f];
-                    wre[f] = re;
-                }
-                dot = group_sum<GL>(dot, gmask) * l2scale;
-            }
-            if (EW == 1 || !key_part) {
-                float vl[4], vh[4];
-                if constexpr (EW == 1) {
-                    const char* b = reinterpret_cast<const char*>(st + kDecThreads);
-                    load4((const V4*)b, vl);
-                    load4((const V4*)(b + 8), vh);
-                } else {
-                    load4((const V4*)st, vl);
-                    load4((const V4*)(st + kDecThreads), vh);
-                }
-                push(dot, vl, vh);
-            }
+            reseed = kReseed;
         }
+        reseed -= 2;
+        float k1l[4], k1h[4], k2l[4], k2h[4], v1l[4], v1h[4], v2l[4], v2h[4];
+        if constexpr (EW == 1) {
+            const char* b1 = reinterpret_cast<const char*>(stage_at(0));
+            const char* b2 = reinterpret_cast<const char*>(stage_at(1));
+            load4((const V4*)b1, k1l);
+            load4((const V4*)(b1 + 8), k1h);
+            load4((const V4*)b2, k2l);
+            load4((const V4*)(b2 + 8), k2h);
+        } else {
+            load4((const V4*)stage_at(0), k1l);
+            load4((const V4*)(stage_at(0) + kDecThreads), k1h);
+            load4((const V4*)stage_at(2), k2l);
+            load4((const V4*)(stage_at(2) + kDecThreads), k2h);
+        }
+        float d1 = 0.0f, d2 = 0.0f;
+#pragma unroll
+        for (int f = 0; f < 4; f++) {
+            const float2 gs = gst[4 * j + f];
+            d1 = fmaf(k1l[f], wre[f], fmaf(k1h[f], wim[f], d1));
+            float re = wre[f] * gs.x - wim[f] * gs.y;
+            float im = wre[f] * gs.y + wim[f] * gs.x;
+            d2 = fmaf(k2l[f], re, fmaf(k2h[f], im, d2));
+            wre[f] = re * gs.x - im * gs.y;
+            wim[f] = re * gs.y + im * gs.x;
+        }
+#pragma unroll
+        for (int off = GL / 2; off > 0; off >>= 1) {
+            d1 += __shfl_xor_sync(gmask, d1, off);
+            d2 += __shfl_xor_sync(gmask, d2, off);
+        }
+        if constexpr (EW == 1) {
+            const char* b1 = reinterpret_cast<const char*>(stage_at(0) + kDecThreads);
+            const char* b2 = reinterpret_cast<const char*>(stage_at(1) + kDecThreads);
+            load4((const V4*)b1, v1l);
+            load4((const V4*)(b1 + 8), v1h);
+            load4((const V4*)b2, v2l);
+            load4((const V4*)(b2 + 8), v2h);
+        } else {
+            load4((const V4*)stage_at(1), v1l);
+            load4((const V4*)(stage_at(1) + kDecThreads), v1h);
+            load4((const V4*)stage_at(3), v2l);
+            load4((const V4*)(stage_at(3) + kDecThreads), v2h);
+        }
+        advance(2 * EW);
+        // one online-softmax update for both (a missing second token weighs 0)
+        const float l1 = d1 * l2scale, l2 = two ? d2 * l2scale : -INFINITY;
+        const float mn = fmaxf(mx, fmaxf(l1, l2));
+        const float sc = ex2(mx - mn), p1 = ex2(l1 - mn), p2 = ex2(l2 - mn);
+        sum = fmaf(sum, sc, p1 + p2);
+#pragma unroll
+        for (int f = 0; f < 4; f++) {
+            const float b2l = two ? v2l[f] : 0.0f, b2h = two ? v2h[f] : 0.0f;
+            acc[f] = fmaf(acc[f], sc, fmaf(p1, v1l[f], p2 * b2l));
+            acc[4 + f] = fmaf(acc[4 + f], sc, fmaf(p1, v1h[f], p2 * b2h));
+        }
+        mx = mn;
+#pragma unroll
+        for (int x = 0; x < 2 * EW; x++) issue_commit();
     }
     cp_async_wait<0>();
     // ---- token t itself (window, relative position 0), by group 0 of the cluster
