@@ -136,6 +136,22 @@ nha_status_t nha_decode_step(const void* q, const void* k, const void* v, const 
                              int t, int B, int H, int d, int m, int w, nha_dtype_t dtype, float rope_base,
                              void* stream);
 
+/* Decode state after a prompt of T tokens (the same recurrence and token shift
+ * as above): writes state_k, state_v = K^long, V^long after token T - w - 1
+ * (zero when T <= w) and puts token s of the prompt (raw k, v and log_alpha)
+ * into ring entry s mod w for s in [max(0, T-w), T-1]; other ring entries
+ * are left as they are (the decode step never reads them before writing
+ * them).  nha_decode_step(..., t = T, ...) then continues the sequence: its
+ * o equals that of nha_forward on the prompt extended by token T.
+ * Layout: k, v [B, H, T, d] (dtype), log_alpha [B, H, T, m] fp32, the state
+ * as for nha_decode_step; all fully written except the ring entries named
+ * above.  With T = 0, k, v and log_alpha are not read (may be NULL); with
+ * w = 0 the ring pointers are not used.  0 <= T <= 262144; d, m, w as for
+ * nha_decode_step.  No workspace; runs on `stream`. */
+nha_status_t nha_decode_prefill(const void* k, const void* v, const float* log_alpha, float* state_k,
+                                float* state_v, void* ring_k, void* ring_v, float* ring_la, int B, int H,
+                                int T, int d, int m, int w, nha_dtype_t dtype, void* stream);
+
 /* ---- Forward without device allocation (the pages have no counterpart) ----
  *
  * Some callers cannot allocate device memory: code that runs while a CUDA

@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     launch_count,
     load_library,
     nha_backward,
+    nha_decode_prefill,
     nha_decode_state,
     nha_decode_step,
     nha_forward,

@@ -25,7 +25,8 @@ STATUS = {0: "NHA_OK", 1: "NHA_ERR_INVALID_ARGUMENT", 2: "NHA_ERR_UNSUPPORTED",
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 
 # Every symbol include/nha.h declares (checked by the tests).
-EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward", "nha_decode_step", "nha_forward_noalloc",
+EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward", "nha_decode_step", "nha_decode_prefill",
+           "nha_forward_noalloc",
            "nha_launch_count", "nha_profile_begin", "nha_profile_end", "nha_status_string", "nha_last_error")
 
 _lock = threading.Lock()
@@ -85,6 +86,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.nha_backward.argtypes = [vp] * 11 + [i] * 8 + [f, vp, sz, vp]
         lib.nha_decode_step.restype = i
         lib.nha_decode_step.argtypes = [vp] * 10 + [i] * 7 + [f, vp]
+        lib.nha_decode_prefill.restype = i
+        lib.nha_decode_prefill.argtypes = [vp] * 8 + [i] * 7 + [vp]
         lib.nha_forward_noalloc.restype = i
         lib.nha_forward_noalloc.argtypes = [vp] * 6 + [i] * 8 + [f, vp]
         lib.nha_status_string.restype = ctypes.c_char_p
@@ -261,3 +264,31 @@ def nha_decode_step(q, k, v, log_alpha, t: int, w: int, state, rope_base: float 
                              float(rope_base), _stream_handle(stream))
     _raise(lib, rc)
     return o
+
+
+def nha_decode_prefill(k, v, log_alpha, w: int, state=None, stream=None):
+    """Decode state after the prompt k, v [B,H,T,d], log_alpha [B,H,T,m]:
+    returns (or fills) the tuple of :func:`nha_decode_state`, ready for
+    :func:`nha_decode_step` at t = T."""
+    lib = load_library()
+    B, H, T, d = k.shape
+    m = log_alpha.shape[-1]
+    dt = k.dtype
+    if dt not in DTYPE:
+        raise TypeError(f"unsupported dtype {dt}")
+    _check("k", k, dt, (B, H, T, d))
+    _check("v", v, dt, (B, H, T, d))
+    _check("log_alpha", log_alpha, torch.float32, (B, H, T, m))
+    if state is None:
+        state = nha_decode_state(B, H, d, m, w, dtype=dt, device=k.device)
+    n = max(int(w), 1)
+    sk, sv, rk, rv, rla = state
+    _check("state_k", sk, torch.float32, (B, H, m, d))
+    _check("state_v", sv, torch.float32, (B, H, m, d))
+    _check("ring_k", rk, dt, (B, H, n, d))
+    _check("ring_v", rv, dt, (B, H, n, d))
+    _check("ring_la", rla, torch.float32, (B, H, n, m))
+    rc = lib.nha_decode_prefill(_ptr(k), _ptr(v), _ptr(log_alpha), _ptr(sk), _ptr(sv), _ptr(rk), _ptr(rv),
+                                _ptr(rla), B, H, T, d, m, int(w), DTYPE[dt], _stream_handle(stream))
+    _raise(lib, rc)
+    return state

@@ -10,6 +10,7 @@
 #include "nha.h"
 #include "nha_decode.h"
 #include "nha_kernels.h"
+#include "nha_prefill.h"
 
 namespace {
 
@@ -339,6 +340,56 @@ nha_status_t nha_decode_step(const void* q, const void* k, const void* v, const 
         default: e = cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "decode launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+nha_status_t nha_decode_prefill(const void* k, const void* v, const float* log_alpha, float* state_k,
+                                float* state_v, void* ring_k, void* ring_v, float* ring_la, int B, int H, int T,
+                                int d, int m, int w, nha_dtype_t dtype, void* stream) {
+    if (inject("validate")) return fail(NHA_ERR_INTERNAL, "fault injected at validate");
+    if (B < 0 || H < 0 || T < 0 || w < 0 || d <= 0 || m <= 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "negative or zero size (B=%d H=%d T=%d d=%d m=%d w=%d)", B, H, T,
+                    d, m, w);
+    if (dtype != NHA_DTYPE_F32 && dtype != NHA_DTYPE_BF16)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "unknown dtype %d", (int)dtype);
+    if (d != 64 && d != 128) return fail(NHA_ERR_UNSUPPORTED, "head dim d=%d not in {64, 128}", d);
+    if (m != 16 && m != 32 && m != 64) return fail(NHA_ERR_UNSUPPORTED, "slots m=%d not in {16, 32, 64}", m);
+    if (T > kMaxT) return fail(NHA_ERR_UNSUPPORTED, "T=%d above the supported %d", T, kMaxT);
+    if (w > kMaxT) return fail(NHA_ERR_UNSUPPORTED, "window w=%d above %d", w, kMaxT);
+    const long long BH = (long long)B * H, wr = w > 0 ? w : 1;
+    const long long rows = T > wr ? T : wr;
+    if (BH * rows * (d > m ? d : m) >= (1LL << 31) || 2 * BH >= (1LL << 31))
+        return fail(NHA_ERR_UNSUPPORTED, "B*H*max(T,w,1)*max(d,m) >= 2^31");
+    if (BH == 0) return ok();
+    const void* ptrs[] = {k, v, log_alpha, state_k, state_v, ring_k, ring_v, ring_la};
+    const char* names[] = {"k", "v", "log_alpha", "state_k", "state_v", "ring_k", "ring_v", "ring_la"};
+    const int first = T > 0 ? 0 : 3;       // no prompt: k, v, log_alpha are not read
+    const int nptr = w > 0 ? 8 : 5;       // the ring is not used when w = 0
+    for (int i = first; i < nptr; i++) {
+        if (ptrs[i] == nullptr) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is NULL", names[i]);
+        if (misaligned(ptrs[i])) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", names[i]);
+    }
+    if (inject("prefill_launch")) return fail(NHA_ERR_INTERNAL, "fault injected at prefill_launch");
+    nha::PrefillArgs a;
+    a.k = k; a.v = v; a.la = log_alpha;
+    a.SK = state_k; a.SV = state_v;
+    a.ring_k = w > 0 ? ring_k : nullptr;
+    a.ring_v = w > 0 ? ring_v : nullptr;
+    a.ring_la = w > 0 ? ring_la : nullptr;
+    a.BH = (int)BH; a.T = T; a.w = w;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool f32 = dtype == NHA_DTYPE_F32;
+    cudaError_t e;
+    switch (d * 1000 + m) {
+        case 64016: e = f32 ? nha::launch_prefill<float, 64, 16>(a, s) : nha::launch_prefill<__nv_bfloat16, 64, 16>(a, s); break;
+        case 64032: e = f32 ? nha::launch_prefill<float, 64, 32>(a, s) : nha::launch_prefill<__nv_bfloat16, 64, 32>(a, s); break;
+        case 64064: e = f32 ? nha::launch_prefill<float, 64, 64>(a, s) : nha::launch_prefill<__nv_bfloat16, 64, 64>(a, s); break;
+        case 128016: e = f32 ? nha::launch_prefill<float, 128, 16>(a, s) : nha::launch_prefill<__nv_bfloat16, 128, 16>(a, s); break;
+        case 128032: e = f32 ? nha::launch_prefill<float, 128, 32>(a, s) : nha::launch_prefill<__nv_bfloat16, 128, 32>(a, s); break;
+        case 128064: e = f32 ? nha::launch_prefill<float, 128, 64>(a, s) : nha::launch_prefill<__nv_bfloat16, 128, 64>(a, s); break;
+        default: e = cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "prefill launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
 

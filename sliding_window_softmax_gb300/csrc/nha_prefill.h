@@ -1,0 +1,28 @@
+// Internal interface of the decode-state prefill (nha_prefill.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace nha {
+
+// Decode state after a prompt of T tokens.  k, v [BH, T, D] in the element
+// type, la [BH, T, M]; out: SK, SV [BH, M, D] fp32 = the long memory after
+// token T - w - 1 (zero when T <= w), ring_k, ring_v [BH, max(w, 1), D] and
+// ring_la [BH, max(w, 1), M] with token s in entry s mod w for
+// s in [max(0, T - w), T - 1] (other entries untouched; no ring when w = 0).
+struct PrefillArgs {
+    const void* k;
+    const void* v;
+    const float* la;
+    float* SK;
+    float* SV;
+    void* ring_k;
+    void* ring_v;
+    float* ring_la;
+    int BH, T, w;
+};
+
+template <typename Tin, int D, int M>
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st);
+
+}  // namespace nha

@@ -174,3 +174,34 @@ def test_decode_fault_injection_on_host(lib, monkeypatch):
     monkeypatch.setenv("NHA_FAULT_INJECT", "decode_launch")
     assert _dec(lib, ring=False, w=0) == 5 and b"decode_launch" in lib.nha_last_error()
     monkeypatch.delenv("NHA_FAULT_INJECT")
+
+
+def _pre(lib, q=1, **kw):
+    args = dict(B=1, H=1, T=16, d=64, m=16, w=4, dt=1, ring=True)
+    args.update(kw)
+    p = ctypes.c_void_p(q * 4096) if q else None  # never dereferenced: validation fails first
+    r = p if args["ring"] else None
+    return lib.nha_decode_prefill(p, p, p, p, p, r, r, r, args["B"], args["H"], args["T"], args["d"],
+                                  args["m"], args["w"], args["dt"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=96), 2), (dict(m=8), 2), (dict(T=(1 << 18) + 1), 2), (dict(w=(1 << 18) + 1), 2),
+    (dict(T=-1), 1), (dict(w=-1), 1), (dict(H=-1), 1), (dict(dt=9), 1), (dict(m=0), 1),
+])
+def test_prefill_rejects_bad_arguments(lib, kw, status):
+    assert _pre(lib, **kw) == status
+    assert lib.nha_last_error()
+
+
+def test_prefill_pointer_checks(lib, monkeypatch):
+    assert _pre(lib, q=0) == 1 and b"NULL" in lib.nha_last_error()
+    assert _pre(lib, ring=False) == 1 and b"ring_k" in lib.nha_last_error()
+    p = ctypes.c_void_p(4096)
+    assert lib.nha_decode_prefill(p, None, p, p, p, p, p, p, 1, 1, 16, 64, 16, 4, 1, None) == 1
+    assert b"v is NULL" in lib.nha_last_error()
+    assert _pre(lib, q=0, B=0) == 0  # no heads: nothing to do
+    # T = 0 reads no prompt and w = 0 uses no ring: validation passes, the injected failure stops the call
+    monkeypatch.setenv("NHA_FAULT_INJECT", "prefill_launch")
+    assert lib.nha_decode_prefill(None, None, None, p, p, None, None, None, 1, 1, 0, 64, 16, 0, 1, None) == 5
+    monkeypatch.delenv("NHA_FAULT_INJECT")

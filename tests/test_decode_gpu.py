@@ -174,3 +174,45 @@ def test_decode_every_cluster_size(ks, monkeypatch):
     monkeypatch.setenv("NHA_DECODE_CLUSTER", ks)
     test_decode_batch_matches_the_decode_oracle(2, 4, 128, 64, 512, 1000, "bf16")
     test_decode_batch_matches_the_decode_oracle(1, 3, 64, 16, 100, 60, "f32")
+
+
+PREFILL_CASES = [
+    # B, H, T (prompt), K (decoded after it), d, m, w, dtype
+    (1, 2, 200, 30, 128, 64, 48, "bf16"),
+    (2, 1, 100, 20, 64, 16, 0, "f32"),     # w = 0: no ring
+    (1, 2, 20, 40, 64, 32, 64, "bf16"),    # prompt shorter than the window: no slot state yet
+    (1, 1, 0, 12, 128, 16, 5, "f32"),      # empty prompt
+    (2, 4, 1000, 6, 128, 64, 512, "bf16"), # 1.3B-like head shape, ring wrapped
+    (1, 2, 333, 25, 64, 64, 37, "f32"),
+]
+
+
+@pytest.mark.parametrize("B,H,T,K,d,m,w,dtype", PREFILL_CASES)
+def test_prefill_then_decode_matches_the_forward_oracle(B, H, T, K, d, m, w, dtype):
+    """nha_decode_prefill on a prompt of T tokens, then nha_decode_step for
+    t = T .. T+K-1: the o of those tokens against the oracle's forward over all
+    T+K tokens; the prefilled state against the decode oracle after T steps."""
+    nha = _nha()
+    wl = Workload("prefill", B, H, T + K, d, m, w, dtype=dtype, seed=5000 + T + K + w)
+    x = make_inputs(wl)
+    dev = {n: t.cuda() for n, t in x.items()}
+    state = nha.nha_decode_prefill(dev["k"][:, :, :T].contiguous(), dev["v"][:, :, :T].contiguous(),
+                                   dev["log_alpha"][:, :, :T].contiguous(), w)
+    torch.cuda.synchronize()
+    st = DecodeState(B, H, d, m, w)
+    for t in range(T):
+        decode_step(st, _np(x["q"][:, :, t]), _np(x["k"][:, :, t]), _np(x["v"][:, :, t]),
+                    _np(x["log_alpha"][:, :, t]), t)
+    tol = 1e-5 if dtype == "f32" else 1e-4
+    assert np.abs(_np(state[0]) - st.S_k).max() <= tol
+    assert np.abs(_np(state[1]) - st.S_v).max() <= tol
+    if w > 0:
+        assert np.array_equal(_np(state[2]), st.ring_k)
+        assert np.array_equal(_np(state[3]), st.ring_v)
+        assert np.array_equal(_np(state[4]), st.ring_la)
+    outs = [nha.nha_decode_step(dev["q"][:, :, t].contiguous(), dev["k"][:, :, t].contiguous(),
+                                dev["v"][:, :, t].contiguous(), dev["log_alpha"][:, :, t].contiguous(),
+                                t, w, state) for t in range(T, T + K)]
+    torch.cuda.synchronize()
+    o_ref, _ = oracle.forward(x["q"], x["k"], x["v"], x["log_alpha"], w)
+    _check_o(_np(torch.stack(outs, dim=2)), o_ref[:, :, T:], dtype, f"prefill T{T} + decode {K} w{w} {dtype}")
