@@ -182,7 +182,7 @@ PREFILL_CASES = [
     (2, 1, 100, 20, 64, 16, 0, "f32"),     # w = 0: no ring
     (1, 2, 20, 40, 64, 32, 64, "bf16"),    # prompt shorter than the window: no slot state yet
     (1, 1, 0, 12, 128, 16, 5, "f32"),      # empty prompt
-    (2, 4, 1000, 6, 128, 64, 512, "bf16"), # 1.3B-like head shape, ring wrapped
+    (2, 4, 700, 6, 128, 64, 512, "bf16"),  # 1.3B-like head shape, ring wrapped
     (1, 2, 333, 25, 64, 64, 37, "f32"),
 ]
 
