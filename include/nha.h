@@ -136,6 +136,18 @@ nha_status_t nha_decode_step(const void* q, const void* k, const void* v, const 
                              int t, int B, int H, int d, int m, int w, nha_dtype_t dtype, float rope_base,
                              void* stream);
 
+/* nha_decode_step with a position per sequence: sequence b's heads decode
+ * token positions[b] (positions: DEVICE array [B] of int32, read by the
+ * kernel, so a captured CUDA graph can be replayed while the caller advances
+ * the positions on the device).  Sequences at different positions share one
+ * launch (continuous batching).  A sequence whose position lies outside
+ * [0, 262144) gets o = NaN and its state and ring are left untouched; the
+ * host cannot check device values.  Everything else as nha_decode_step. */
+nha_status_t nha_decode_step_varlen(const void* q, const void* k, const void* v, const float* log_alpha,
+                                    void* o, float* state_k, float* state_v, void* ring_k, void* ring_v,
+                                    float* ring_la, const int* positions, int B, int H, int d, int m, int w,
+                                    nha_dtype_t dtype, float rope_base, void* stream);
+
 /* Decode state after a prompt of T tokens (the same recurrence and token shift
  * as above): writes state_k, state_v = K^long, V^long after token T - w - 1
  * (zero when T <= w) and puts token s of the prompt (raw k, v and log_alpha)

@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     nha_decode_prefill,
     nha_decode_state,
     nha_decode_step,
+    nha_decode_step_varlen,
     nha_forward,
     nha_forward_noalloc,
     nha_workspace_bytes,

@@ -25,7 +25,8 @@ STATUS = {0: "NHA_OK", 1: "NHA_ERR_INVALID_ARGUMENT", 2: "NHA_ERR_UNSUPPORTED",
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 
 # Every symbol include/nha.h declares (checked by the tests).
-EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward", "nha_decode_step", "nha_decode_prefill",
+EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward", "nha_decode_step", "nha_decode_step_varlen",
+           "nha_decode_prefill",
            "nha_forward_noalloc",
            "nha_launch_count", "nha_profile_begin", "nha_profile_end", "nha_status_string", "nha_last_error")
 
@@ -86,6 +87,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.nha_backward.argtypes = [vp] * 11 + [i] * 8 + [f, vp, sz, vp]
         lib.nha_decode_step.restype = i
         lib.nha_decode_step.argtypes = [vp] * 10 + [i] * 7 + [f, vp]
+        lib.nha_decode_step_varlen.restype = i
+        lib.nha_decode_step_varlen.argtypes = [vp] * 11 + [i] * 6 + [f, vp]
         lib.nha_decode_prefill.restype = i
         lib.nha_decode_prefill.argtypes = [vp] * 8 + [i] * 7 + [vp]
         lib.nha_forward_noalloc.restype = i
@@ -292,3 +295,34 @@ def nha_decode_prefill(k, v, log_alpha, w: int, state=None, stream=None):
                                 _ptr(rla), B, H, T, d, m, int(w), DTYPE[dt], _stream_handle(stream))
     _raise(lib, rc)
     return state
+
+
+def nha_decode_step_varlen(q, k, v, log_alpha, positions, w: int, state, rope_base: float = 10000.0, o=None,
+                           stream=None):
+    """o = nha_decode_step_varlen(q, k, v, log_alpha, positions, w, state): like
+    :func:`nha_decode_step`, sequence b at position ``positions[b]`` (a CUDA
+    int32 tensor [B], read on the device)."""
+    lib = load_library()
+    B, H, d = q.shape
+    m = log_alpha.shape[-1]
+    dt = q.dtype
+    if dt not in DTYPE:
+        raise TypeError(f"unsupported dtype {dt}")
+    n = max(int(w), 1)
+    sk, sv, rk, rv, rla = state
+    for nm, x in (("q", q), ("k", k), ("v", v)):
+        _check(nm, x, dt, (B, H, d))
+    _check("log_alpha", log_alpha, torch.float32, (B, H, m))
+    _check("positions", positions, torch.int32, (B,))
+    _check("state_k", sk, torch.float32, (B, H, m, d))
+    _check("state_v", sv, torch.float32, (B, H, m, d))
+    _check("ring_k", rk, dt, (B, H, n, d))
+    _check("ring_v", rv, dt, (B, H, n, d))
+    _check("ring_la", rla, torch.float32, (B, H, n, m))
+    o = torch.empty_like(q) if o is None else o
+    _check("o", o, dt, (B, H, d))
+    rc = lib.nha_decode_step_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(sk), _ptr(sv),
+                                    _ptr(rk), _ptr(rv), _ptr(rla), _ptr(positions), B, H, d, m, int(w),
+                                    DTYPE[dt], float(rope_base), _stream_handle(stream))
+    _raise(lib, rc)
+    return o

@@ -111,7 +111,13 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
     const unsigned gmask = (GL == 32 ? 0xffffffffu : ((1u << GL) - 1u) << (lane / GL * GL));
     const int bh = blockIdx.x / ks;
     const int g = rank * NG + grp, G = ks * NG;
-    const int t = a.t, w = a.w, wr = w > 0 ? w : 1;
+    const int t = a.tpos ? a.tpos[bh / a.H] : a.t;
+    const int w = a.w, wr = w > 0 ? w : 1;
+    if (t < 0 || t >= (1 << 18)) {  // a position outside the supported range: NaN out, state untouched
+        for (int e = rank * (D / ks) + tid; e < (rank + 1) * (D / ks); e += kDecThreads)
+            ((Tin*)a.o)[(size_t)bh * D + e] = from_f<Tin>(__int_as_float(0x7fc00000));
+        return;  // every CTA of the cluster serves this head and returns here, before any cluster barrier
+    }
     const float scale = rsqrtf((float)D);
     const bool absorb = t - w >= 0;
     const int eo = absorb && w > 0 ? (t - w) % w : 0;  // ring entry of the token that leaves
@@ -425,9 +431,12 @@ constexpr size_t kDecSmem = (size_t)kDecStages * kPieces * kDecThreads * sizeof(
 
 // Cluster size: doubled, up to 8 (the portable limit), while the grid stays
 // within one wave of resident CTAs and every group keeps at least four items.
+// (With per-sequence positions the host does not know them: sized as if every
+// window were full and a token leaving it.)
 static int decode_cluster(const DecodeArgs& a, int m, int d, int resident) {
-    const int s_lo = a.t - a.w + 1 > 0 ? a.t - a.w + 1 : 0;
-    const int items = (a.t - a.w >= 0 ? m : 0) + (a.t - s_lo > 0 ? a.t - s_lo : 0);
+    const int t = a.tpos ? a.w + 1 : a.t;
+    const int s_lo = t - a.w + 1 > 0 ? t - a.w + 1 : 0;
+    const int items = (t - a.w >= 0 ? m : 0) + (t - s_lo > 0 ? t - s_lo : 0);
     const int groups = kDecThreads / (d / 8);
     int ks = 1;
     while (ks < 8 && (long long)a.BH * ks * 2 <= (long long)resident * a.sms && ks * 2 * groups * 4 <= items)

@@ -10,7 +10,9 @@ namespace nha {
 // Decode step for token t.  q, k, v, o [BH, D] in the element type; la
 // [BH, M]; SK, SV [BH, M, D] fp32, updated in place; ring_k, ring_v
 // [BH, max(w, 1), D] in the element type and ring_la [BH, max(w, 1), M] fp32,
-// token s in entry s mod w (not used when w = 0).
+// token s in entry s mod w (not used when w = 0).  With tpos, sequence b's
+// heads decode their own position tpos[b]; a head whose position lies outside
+// [0, 2^18) gets o = NaN and its state and ring are left untouched.
 struct DecodeArgs {
     const void* q;
     const void* k;
@@ -23,7 +25,9 @@ struct DecodeArgs {
     void* ring_v;
     float* ring_la;
     int BH, t, w;
-    int sms;  // multiprocessors of the device (sizes the clusters)
+    const int* tpos;  // if set: device array [B] of per-sequence positions (t unused)
+    int H;            // heads per sequence (b = bh / H indexes tpos)
+    int sms;          // multiprocessors of the device (sizes the clusters)
     RopeTab rope;
 };
 

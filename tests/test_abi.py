@@ -205,3 +205,18 @@ def test_prefill_pointer_checks(lib, monkeypatch):
     monkeypatch.setenv("NHA_FAULT_INJECT", "prefill_launch")
     assert lib.nha_decode_prefill(None, None, None, p, p, None, None, None, 1, 1, 0, 64, 16, 0, 1, None) == 5
     monkeypatch.delenv("NHA_FAULT_INJECT")
+
+
+def test_decode_varlen_validation(lib, monkeypatch):
+    p = ctypes.c_void_p(4096)
+    args = [p] * 10
+    # positions are required (unless there are no heads) and must be 4-byte aligned
+    assert lib.nha_decode_step_varlen(*args, None, 2, 1, 64, 16, 4, 1, 1e4, None) == 1
+    assert b"positions" in lib.nha_last_error()
+    assert lib.nha_decode_step_varlen(*args, ctypes.c_void_p(4098), 2, 1, 64, 16, 4, 1, 1e4, None) == 1
+    assert b"aligned" in lib.nha_last_error()
+    assert lib.nha_decode_step_varlen(*([None] * 10), None, 0, 1, 64, 16, 4, 1, 1e4, None) == 0
+    assert lib.nha_decode_step_varlen(*args, p, 2, 1, 96, 16, 4, 1, 1e4, None) == 2
+    monkeypatch.setenv("NHA_FAULT_INJECT", "decode_launch")
+    assert lib.nha_decode_step_varlen(*args, p, 2, 1, 64, 16, 4, 1, 1e4, None) == 5
+    monkeypatch.delenv("NHA_FAULT_INJECT")

@@ -216,3 +216,79 @@ def test_prefill_then_decode_matches_the_forward_oracle(B, H, T, K, d, m, w, dty
     torch.cuda.synchronize()
     o_ref, _ = oracle.forward(x["q"], x["k"], x["v"], x["log_alpha"], w)
     _check_o(_np(torch.stack(outs, dim=2)), o_ref[:, :, T:], dtype, f"prefill T{T} + decode {K} w{w} {dtype}")
+
+
+def test_varlen_decode_continuous_batch():
+    """Sequences with prompts of different lengths, each prefilled on its own,
+    then decoded together with nha_decode_step_varlen: every sequence against
+    the oracle's forward over its own tokens.  The last steps replay a CUDA
+    graph that decodes and then advances the positions on the device."""
+    nha = _nha()
+    B, H, d, m, w, K = 4, 2, 128, 64, 64, 8
+    prompts = [0, 30, 300, 1000]
+    wl = Workload("varlen", B, H, max(prompts) + K, d, m, w, seed=6000)
+    x = make_inputs(wl)
+    dev = {n: t.cuda() for n, t in x.items()}
+    state = nha.nha_decode_state(B, H, d, m, w, dtype=torch.bfloat16)
+    for b, T in enumerate(prompts):
+        sub = tuple(a[b:b + 1] for a in state)
+        nha.nha_decode_prefill(dev["k"][b:b + 1, :, :T].contiguous(), dev["v"][b:b + 1, :, :T].contiguous(),
+                               dev["log_alpha"][b:b + 1, :, :T].contiguous(), w, state=sub)
+    pos = torch.tensor(prompts, dtype=torch.int32, device="cuda")
+    idx = (pos.long()[:, None, None].expand(B, H, 1))
+
+    def token(n, step):  # token prompts[b] + step of every sequence, [B, H, .]
+        src = dev[n]
+        i = (idx + step)[..., None].expand(B, H, 1, src.shape[-1])
+        return torch.gather(src, 2, i)[:, :, 0].contiguous()
+
+    outs = []
+    for step in range(K // 2):  # eager calls
+        outs.append(nha.nha_decode_step_varlen(token("q", step), token("k", step), token("v", step),
+                                               token("log_alpha", step), pos, w, state))
+        pos += 1
+    # graph: fixed input buffers, decode, then advance the positions on the device
+    bufs = {n: token(n, K // 2) for n in ("q", "k", "v", "log_alpha")}
+    o_buf = torch.empty_like(bufs["q"])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        nha.nha_decode_step_varlen(bufs["q"], bufs["k"], bufs["v"], bufs["log_alpha"], pos, w, state, o=o_buf)
+        pos.add_(1)
+    for step in range(K // 2, K):
+        for n in bufs:
+            bufs[n].copy_(token(n, step))
+        g.replay()
+        outs.append(o_buf.clone())
+    torch.cuda.synchronize()
+    assert pos.cpu().tolist() == [T + K for T in prompts]
+    got = _np(torch.stack(outs, dim=2))
+    for b, T in enumerate(prompts):
+        sel = {n: t[b:b + 1, :, :T + K] for n, t in x.items()}
+        o_ref, _ = oracle.forward(sel["q"], sel["k"], sel["v"], sel["log_alpha"], w)
+        _check_o(got[b:b + 1], o_ref[:, :, T:], "bf16", f"varlen sequence {b} (prompt {T})")
+
+
+def test_varlen_position_out_of_range_is_nan_and_leaves_the_state():
+    nha = _nha()
+    B, H, d, m, w = 2, 2, 64, 16, 8
+    g = torch.Generator().manual_seed(6100)
+    q, k, v = ((torch.randn((B, H, d), generator=g) * d ** -0.25).float() for _ in range(3))
+    la = torch.nn.functional.logsigmoid(torch.randn((B, H, m), generator=g) + 3.0)
+    sk0 = torch.randn((B, H, m, d), generator=g) * 0.1
+    sv0 = torch.randn((B, H, m, d), generator=g) * 0.1
+    rk0, rv0 = (torch.randn((B, H, w, d), generator=g) * 0.3 for _ in range(2))
+    rla0 = torch.nn.functional.logsigmoid(torch.randn((B, H, w, m), generator=g) + 3.0)
+    state = tuple(a.cuda() for a in (sk0, sv0, rk0, rv0, rla0))
+    pos = torch.tensor([-1, 20], dtype=torch.int32, device="cuda")
+    o = nha.nha_decode_step_varlen(q.cuda(), k.cuda(), v.cuda(), la.cuda(), pos, w, state)
+    torch.cuda.synchronize()
+    o = _np(o)
+    assert np.all(np.isnan(o[0]))
+    for a, a0 in zip(state, (sk0, sv0, rk0, rv0, rla0)):
+        assert np.array_equal(_np(a[0]), _np(a0[0]))
+    st = DecodeState(1, H, d, m, w)
+    st.S_k, st.S_v, st.ring_k, st.ring_v, st.ring_la = (_np(a[1:2]) for a in (sk0, sv0, rk0, rv0, rla0))
+    o_ref = decode_step(st, _np(q[1:2]), _np(k[1:2]), _np(v[1:2]), _np(la[1:2]), 20)
+    _check_o(o[1:2], o_ref, "f32", "varlen sequence 1")
+    assert np.abs(_np(state[0][1:2]) - st.S_k).max() <= 1e-5
