@@ -136,17 +136,23 @@ nha_status_t nha_decode_step(const void* q, const void* k, const void* v, const 
                              int t, int B, int H, int d, int m, int w, nha_dtype_t dtype, float rope_base,
                              void* stream);
 
-/* nha_decode_step with a position per sequence: sequence b's heads decode
- * token positions[b] (positions: DEVICE array [B] of int32, read by the
- * kernel, so a captured CUDA graph can be replayed while the caller advances
- * the positions on the device).  Sequences at different positions share one
- * launch (continuous batching).  A sequence whose position lies outside
- * [0, 262144) gets o = NaN and its state and ring are left untouched; the
- * host cannot check device values.  Everything else as nha_decode_step. */
+/* nha_decode_step with a position per sequence and, optionally, a window per
+ * head.  Sequence b's heads decode token positions[b] (positions: DEVICE
+ * array [B] of int32, read by the kernel, so a captured CUDA graph can be
+ * replayed while the caller advances the positions on the device);
+ * sequences at different positions share one launch (continuous batching).
+ * windows (DEVICE array [H] of int32, or NULL for w everywhere): head h keeps
+ * a window of windows[h] tokens, 0 <= windows[h] <= w, in the first
+ * windows[h] entries of its w-entry ring (token s in entry s mod windows[h];
+ * a window of 0 makes that head a pure slot RNN); per-head windows in one
+ * launch (the pages' non-uniform window schedules, Future Directions).
+ * A head whose position lies outside [0, 262144) or whose window lies outside
+ * [0, w] gets o = NaN and its state and ring are left untouched (the host
+ * cannot check device values).  Everything else as nha_decode_step. */
 nha_status_t nha_decode_step_varlen(const void* q, const void* k, const void* v, const float* log_alpha,
                                     void* o, float* state_k, float* state_v, void* ring_k, void* ring_v,
-                                    float* ring_la, const int* positions, int B, int H, int d, int m, int w,
-                                    nha_dtype_t dtype, float rope_base, void* stream);
+                                    float* ring_la, const int* positions, const int* windows, int B, int H,
+                                    int d, int m, int w, nha_dtype_t dtype, float rope_base, void* stream);
 
 /* Decode state after a prompt of T tokens (the same recurrence and token shift
  * as above): writes state_k, state_v = K^long, V^long after token T - w - 1
@@ -159,10 +165,13 @@ nha_status_t nha_decode_step_varlen(const void* q, const void* k, const void* v,
  * as for nha_decode_step; all fully written except the ring entries named
  * above.  With T = 0, k, v and log_alpha are not read (may be NULL); with
  * w = 0 the ring pointers are not used.  0 <= T <= 262144; d, m, w as for
- * nha_decode_step.  No workspace; runs on `stream`. */
+ * nha_decode_step.  windows: as for nha_decode_step_varlen (DEVICE array [H]
+ * or NULL); a head with a window outside [0, w] gets NaN states and no ring
+ * writes.  No workspace; runs on `stream`. */
 nha_status_t nha_decode_prefill(const void* k, const void* v, const float* log_alpha, float* state_k,
-                                float* state_v, void* ring_k, void* ring_v, float* ring_la, int B, int H,
-                                int T, int d, int m, int w, nha_dtype_t dtype, void* stream);
+                                float* state_v, void* ring_k, void* ring_v, float* ring_la,
+                                const int* windows, int B, int H, int T, int d, int m, int w,
+                                nha_dtype_t dtype, void* stream);
 
 /* ---- Forward without device allocation (the pages have no counterpart) ----
  *

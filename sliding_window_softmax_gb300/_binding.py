@@ -88,9 +88,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.nha_decode_step.restype = i
         lib.nha_decode_step.argtypes = [vp] * 10 + [i] * 7 + [f, vp]
         lib.nha_decode_step_varlen.restype = i
-        lib.nha_decode_step_varlen.argtypes = [vp] * 11 + [i] * 6 + [f, vp]
+        lib.nha_decode_step_varlen.argtypes = [vp] * 12 + [i] * 6 + [f, vp]
         lib.nha_decode_prefill.restype = i
-        lib.nha_decode_prefill.argtypes = [vp] * 8 + [i] * 7 + [vp]
+        lib.nha_decode_prefill.argtypes = [vp] * 9 + [i] * 7 + [vp]
         lib.nha_forward_noalloc.restype = i
         lib.nha_forward_noalloc.argtypes = [vp] * 6 + [i] * 8 + [f, vp]
         lib.nha_status_string.restype = ctypes.c_char_p
@@ -269,10 +269,11 @@ def nha_decode_step(q, k, v, log_alpha, t: int, w: int, state, rope_base: float 
     return o
 
 
-def nha_decode_prefill(k, v, log_alpha, w: int, state=None, stream=None):
+def nha_decode_prefill(k, v, log_alpha, w: int, state=None, windows=None, stream=None):
     """Decode state after the prompt k, v [B,H,T,d], log_alpha [B,H,T,m]:
     returns (or fills) the tuple of :func:`nha_decode_state`, ready for
-    :func:`nha_decode_step` at t = T."""
+    :func:`nha_decode_step` at t = T (``windows``: per-head windows, as for
+    :func:`nha_decode_step_varlen`)."""
     lib = load_library()
     B, H, T, d = k.shape
     m = log_alpha.shape[-1]
@@ -291,17 +292,20 @@ def nha_decode_prefill(k, v, log_alpha, w: int, state=None, stream=None):
     _check("ring_k", rk, dt, (B, H, n, d))
     _check("ring_v", rv, dt, (B, H, n, d))
     _check("ring_la", rla, torch.float32, (B, H, n, m))
+    if windows is not None:
+        _check("windows", windows, torch.int32, (H,))
     rc = lib.nha_decode_prefill(_ptr(k), _ptr(v), _ptr(log_alpha), _ptr(sk), _ptr(sv), _ptr(rk), _ptr(rv),
-                                _ptr(rla), B, H, T, d, m, int(w), DTYPE[dt], _stream_handle(stream))
+                                _ptr(rla), _ptr(windows), B, H, T, d, m, int(w), DTYPE[dt], _stream_handle(stream))
     _raise(lib, rc)
     return state
 
 
 def nha_decode_step_varlen(q, k, v, log_alpha, positions, w: int, state, rope_base: float = 10000.0, o=None,
-                           stream=None):
+                           windows=None, stream=None):
     """o = nha_decode_step_varlen(q, k, v, log_alpha, positions, w, state): like
     :func:`nha_decode_step`, sequence b at position ``positions[b]`` (a CUDA
-    int32 tensor [B], read on the device)."""
+    int32 tensor [B], read on the device); ``windows`` (CUDA int32 [H], each in
+    [0, w]) gives every head its own window inside the w-entry ring."""
     lib = load_library()
     B, H, d = q.shape
     m = log_alpha.shape[-1]
@@ -314,6 +318,8 @@ def nha_decode_step_varlen(q, k, v, log_alpha, positions, w: int, state, rope_ba
         _check(nm, x, dt, (B, H, d))
     _check("log_alpha", log_alpha, torch.float32, (B, H, m))
     _check("positions", positions, torch.int32, (B,))
+    if windows is not None:
+        _check("windows", windows, torch.int32, (H,))
     _check("state_k", sk, torch.float32, (B, H, m, d))
     _check("state_v", sv, torch.float32, (B, H, m, d))
     _check("ring_k", rk, dt, (B, H, n, d))
@@ -322,7 +328,7 @@ def nha_decode_step_varlen(q, k, v, log_alpha, positions, w: int, state, rope_ba
     o = torch.empty_like(q) if o is None else o
     _check("o", o, dt, (B, H, d))
     rc = lib.nha_decode_step_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(sk), _ptr(sv),
-                                    _ptr(rk), _ptr(rv), _ptr(rla), _ptr(positions), B, H, d, m, int(w),
+                                    _ptr(rk), _ptr(rv), _ptr(rla), _ptr(positions), _ptr(windows), B, H, d, m, int(w),
                                     DTYPE[dt], float(rope_base), _stream_handle(stream))
     _raise(lib, rc)
     return o

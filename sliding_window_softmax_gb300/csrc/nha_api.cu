@@ -296,8 +296,8 @@ namespace {
 // (device positions tpos[B], t unused).
 nha_status_t decode_call(const void* q, const void* k, const void* v, const float* log_alpha, void* o,
                          float* state_k, float* state_v, void* ring_k, void* ring_v, float* ring_la, int t,
-                         const int* tpos, int B, int H, int d, int m, int w, nha_dtype_t dtype, float rope_base,
-                         void* stream) {
+                         const int* tpos, const int* wvec, int B, int H, int d, int m, int w, nha_dtype_t dtype,
+                         float rope_base, void* stream) {
     if (inject("validate")) return fail(NHA_ERR_INTERNAL, "fault injected at validate");
     if (B < 0 || H < 0 || t < 0 || w < 0 || d <= 0 || m <= 0)
         return fail(NHA_ERR_INVALID_ARGUMENT, "negative or zero size (B=%d H=%d t=%d d=%d m=%d w=%d)", B, H, t,
@@ -323,6 +323,8 @@ nha_status_t decode_call(const void* q, const void* k, const void* v, const floa
     }
     if (tpos != nullptr && ((uintptr_t)tpos & 3u) != 0)
         return fail(NHA_ERR_INVALID_ARGUMENT, "positions array is not 4-byte aligned");
+    if (wvec != nullptr && ((uintptr_t)wvec & 3u) != 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "windows array is not 4-byte aligned");
     if (inject("decode_launch")) return fail(NHA_ERR_INTERNAL, "fault injected at decode_launch");
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -334,7 +336,7 @@ nha_status_t decode_call(const void* q, const void* k, const void* v, const floa
     a.ring_k = w > 0 ? ring_k : nullptr;
     a.ring_v = w > 0 ? ring_v : nullptr;
     a.ring_la = w > 0 ? ring_la : nullptr;
-    a.BH = (int)BH; a.t = t; a.w = w; a.tpos = tpos; a.H = H; a.sms = sms;
+    a.BH = (int)BH; a.t = t; a.w = w; a.tpos = tpos; a.wvec = wvec; a.H = H; a.sms = sms;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
     const bool f32 = dtype == NHA_DTYPE_F32;
@@ -357,23 +359,23 @@ extern "C" {
 nha_status_t nha_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, void* o,
                              float* state_k, float* state_v, void* ring_k, void* ring_v, float* ring_la, int t,
                              int B, int H, int d, int m, int w, nha_dtype_t dtype, float rope_base, void* stream) {
-    return decode_call(q, k, v, log_alpha, o, state_k, state_v, ring_k, ring_v, ring_la, t, nullptr, B, H, d, m, w,
-                       dtype, rope_base, stream);
+    return decode_call(q, k, v, log_alpha, o, state_k, state_v, ring_k, ring_v, ring_la, t, nullptr, nullptr, B, H,
+                       d, m, w, dtype, rope_base, stream);
 }
 
 nha_status_t nha_decode_step_varlen(const void* q, const void* k, const void* v, const float* log_alpha, void* o,
                                     float* state_k, float* state_v, void* ring_k, void* ring_v, float* ring_la,
-                                    const int* positions, int B, int H, int d, int m, int w, nha_dtype_t dtype,
-                                    float rope_base, void* stream) {
+                                    const int* positions, const int* windows, int B, int H, int d, int m, int w,
+                                    nha_dtype_t dtype, float rope_base, void* stream) {
     if (positions == nullptr && (long long)B * H > 0)
         return fail(NHA_ERR_INVALID_ARGUMENT, "positions is NULL");
-    return decode_call(q, k, v, log_alpha, o, state_k, state_v, ring_k, ring_v, ring_la, 0, positions, B, H, d, m,
-                       w, dtype, rope_base, stream);
+    return decode_call(q, k, v, log_alpha, o, state_k, state_v, ring_k, ring_v, ring_la, 0, positions, windows, B, H,
+                       d, m, w, dtype, rope_base, stream);
 }
 
 nha_status_t nha_decode_prefill(const void* k, const void* v, const float* log_alpha, float* state_k,
-                                float* state_v, void* ring_k, void* ring_v, float* ring_la, int B, int H, int T,
-                                int d, int m, int w, nha_dtype_t dtype, void* stream) {
+                                float* state_v, void* ring_k, void* ring_v, float* ring_la, const int* windows,
+                                int B, int H, int T, int d, int m, int w, nha_dtype_t dtype, void* stream) {
     if (inject("validate")) return fail(NHA_ERR_INTERNAL, "fault injected at validate");
     if (B < 0 || H < 0 || T < 0 || w < 0 || d <= 0 || m <= 0)
         return fail(NHA_ERR_INVALID_ARGUMENT, "negative or zero size (B=%d H=%d T=%d d=%d m=%d w=%d)", B, H, T,
@@ -397,6 +399,8 @@ nha_status_t nha_decode_prefill(const void* k, const void* v, const float* log_a
         if (ptrs[i] == nullptr) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is NULL", names[i]);
         if (misaligned(ptrs[i])) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", names[i]);
     }
+    if (windows != nullptr && ((uintptr_t)windows & 3u) != 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "windows array is not 4-byte aligned");
     if (inject("prefill_launch")) return fail(NHA_ERR_INTERNAL, "fault injected at prefill_launch");
     nha::PrefillArgs a;
     a.k = k; a.v = v; a.la = log_alpha;
@@ -404,7 +408,7 @@ nha_status_t nha_decode_prefill(const void* k, const void* v, const float* log_a
     a.ring_k = w > 0 ? ring_k : nullptr;
     a.ring_v = w > 0 ? ring_v : nullptr;
     a.ring_la = w > 0 ? ring_la : nullptr;
-    a.BH = (int)BH; a.T = T; a.w = w;
+    a.BH = (int)BH; a.T = T; a.w = w; a.wvec = windows; a.H = H;
     cudaStream_t s = (cudaStream_t)stream;
     const bool f32 = dtype == NHA_DTYPE_F32;
     cudaError_t e;

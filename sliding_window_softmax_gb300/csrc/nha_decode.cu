@@ -112,8 +112,11 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
     const int bh = blockIdx.x / ks;
     const int g = rank * NG + grp, G = ks * NG;
     const int t = a.tpos ? a.tpos[bh / a.H] : a.t;
-    const int w = a.w, wr = w > 0 ? w : 1;
-    if (t < 0 || t >= (1 << 18)) {  // a position outside the supported range: NaN out, state untouched
+    const int w = a.wvec ? a.wvec[bh % a.H] : a.w;  // this head's window
+    const int wr = w > 0 ? w : 1;                    // ring entries the head cycles through
+    const size_t wst = a.w > 0 ? a.w : 1;            // ring entries per head in memory
+    // a position or window outside the supported range: NaN out, state untouched
+    if (t < 0 || t >= (1 << 18) || w < 0 || w > a.w) {
         for (int e = rank * (D / ks) + tid; e < (rank + 1) * (D / ks); e += kDecThreads)
             ((Tin*)a.o)[(size_t)bh * D + e] = from_f<Tin>(__int_as_float(0x7fc00000));
         return;  // every CTA of the cluster serves this head and returns here, before any cluster barrier
@@ -128,8 +131,8 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
     const Tin* k = (const Tin*)a.k + (size_t)bh * D;
     const Tin* v = (const Tin*)a.v + (size_t)bh * D;
     const float* la = a.la + (size_t)bh * M;
-    const Tin* rk = (const Tin*)a.ring_k + (size_t)bh * wr * D;
-    const Tin* rv = (const Tin*)a.ring_v + (size_t)bh * wr * D;
+    const Tin* rk = (const Tin*)a.ring_k + (size_t)bh * wst * D;
+    const Tin* rv = (const Tin*)a.ring_v + (size_t)bh * wst * D;
     float* SK = a.SK + (size_t)bh * M * D;
     float* SV = a.SV + (size_t)bh * M * D;
 
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
         }
     }
     if (absorb)
-        for (int i = tid; i < M; i += kDecThreads) slj[i] = w > 0 ? a.ring_la[((size_t)bh * wr + eo) * M + i] : la[i];
+        for (int i = tid; i < M; i += kDecThreads) slj[i] = w > 0 ? a.ring_la[((size_t)bh * wst + eo) * M + i] : la[i];
     for (int i = tid; i < H2; i += kDecThreads) {
         float c, sn;
         rope_cs(a.rope, t, i, c, sn);
@@ -395,13 +398,13 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
     // s < t read other entries
     if (w > 0 && rank == 0) {
         const int en = t % w;
-        Tin* wk = (Tin*)a.ring_k + ((size_t)bh * wr + en) * D;
-        Tin* wv = (Tin*)a.ring_v + ((size_t)bh * wr + en) * D;
+        Tin* wk = (Tin*)a.ring_k + ((size_t)bh * wst + en) * D;
+        Tin* wv = (Tin*)a.ring_v + ((size_t)bh * wst + en) * D;
         for (int e = tid; e < D; e += kDecThreads) {
             wk[e] = k[e];
             wv[e] = v[e];
         }
-        for (int i = tid; i < M; i += kDecThreads) a.ring_la[((size_t)bh * wr + en) * M + i] = la[i];
+        for (int i = tid; i < M; i += kDecThreads) a.ring_la[((size_t)bh * wst + en) * M + i] = la[i];
     }
     // ---- merge the cluster: CTA `rank` writes o[e] for e in its share of d
     {

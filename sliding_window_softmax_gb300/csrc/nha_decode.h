@@ -12,7 +12,9 @@ namespace nha {
 // [BH, max(w, 1), D] in the element type and ring_la [BH, max(w, 1), M] fp32,
 // token s in entry s mod w (not used when w = 0).  With tpos, sequence b's
 // heads decode their own position tpos[b]; a head whose position lies outside
-// [0, 2^18) gets o = NaN and its state and ring are left untouched.
+// [0, 2^18) gets o = NaN and its state and ring are left untouched.  With
+// wvec, head h keeps a window of wvec[h] tokens in the first wvec[h] entries
+// of its w-entry ring (same NaN rule for a window outside [0, w]).
 struct DecodeArgs {
     const void* q;
     const void* k;
@@ -26,6 +28,7 @@ struct DecodeArgs {
     float* ring_la;
     int BH, t, w;
     const int* tpos;  // if set: device array [B] of per-sequence positions (t unused)
+    const int* wvec;  // if set: device array [H] of per-head windows in [0, w] (w = the ring's length)
     int H;            // heads per sequence (b = bh / H indexes tpos)
     int sms;          // multiprocessors of the device (sizes the clusters)
     RopeTab rope;

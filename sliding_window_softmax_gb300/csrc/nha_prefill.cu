@@ -28,9 +28,15 @@ __global__ void __launch_bounds__(8 * D) prefill_state_kernel(const PrefillArgs 
     __shared__ float s_al[kPrefillChunk][M], s_u[kPrefillChunk][M], s_x[kPrefillChunk][D];
     const int bh = blockIdx.x >> 1, which = blockIdx.x & 1;  // which: 0 = K, 1 = V
     const int tid = threadIdx.x, c = tid % D, ig = tid / D;  // slots ig * SPT .. ig * SPT + SPT - 1
-    const int T = a.T, w = a.w;
+    const int T = a.T, w = a.wvec ? a.wvec[bh % a.H] : a.w;  // this head's window
+    const size_t wst = a.w > 0 ? a.w : 1;                       // ring entries per head in memory
     const Tin* X = (const Tin*)(which ? a.v : a.k) + (size_t)bh * T * D;
     const float* la = a.la + (size_t)bh * T * M;
+    if (w < 0 || w > a.w) {  // a window outside the ring: NaN states, ring untouched
+        float* out = (which ? a.SV : a.SK) + (size_t)bh * M * D;
+        for (int x = tid; x < M * D; x += NT) out[x] = __int_as_float(0x7fc00000);
+        return;
+    }
     const int J = T - w;  // tokens 0 .. J - 1 have left the window
     float S[SPT];
 #pragma unroll
@@ -64,13 +70,13 @@ __global__ void __launch_bounds__(8 * D) prefill_state_kernel(const PrefillArgs 
     // the window: the last min(w, T) tokens, token s in ring entry s mod w
     if (w > 0) {
         const int s0 = max(0, T - w), n = T - s0;
-        Tin* ring = (Tin*)(which ? a.ring_v : a.ring_k) + (size_t)bh * w * D;
+        Tin* ring = (Tin*)(which ? a.ring_v : a.ring_k) + (size_t)bh * wst * D;
         for (int x = tid; x < n * D; x += NT) {
             const int s = s0 + x / D, e = x % D;
             ring[(size_t)(s % w) * D + e] = X[(size_t)s * D + e];
         }
         if (which == 0) {
-            float* rl = a.ring_la + (size_t)bh * w * M;
+            float* rl = a.ring_la + (size_t)bh * wst * M;
             for (int x = tid; x < n * M; x += NT) {
                 const int s = s0 + x / M, i = x % M;
                 rl[(size_t)(s % w) * M + i] = la[(size_t)s * M + i];

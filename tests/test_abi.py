@@ -181,8 +181,8 @@ def _pre(lib, q=1, **kw):
     args.update(kw)
     p = ctypes.c_void_p(q * 4096) if q else None  # never dereferenced: validation fails first
     r = p if args["ring"] else None
-    return lib.nha_decode_prefill(p, p, p, p, p, r, r, r, args["B"], args["H"], args["T"], args["d"],
-                                  args["m"], args["w"], args["dt"], None)
+    return lib.nha_decode_prefill(p, p, p, p, p, r, r, r, args.get("win"), args["B"], args["H"], args["T"],
+                                  args["d"], args["m"], args["w"], args["dt"], None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -198,12 +198,13 @@ def test_prefill_pointer_checks(lib, monkeypatch):
     assert _pre(lib, q=0) == 1 and b"NULL" in lib.nha_last_error()
     assert _pre(lib, ring=False) == 1 and b"ring_k" in lib.nha_last_error()
     p = ctypes.c_void_p(4096)
-    assert lib.nha_decode_prefill(p, None, p, p, p, p, p, p, 1, 1, 16, 64, 16, 4, 1, None) == 1
+    assert lib.nha_decode_prefill(p, None, p, p, p, p, p, p, None, 1, 1, 16, 64, 16, 4, 1, None) == 1
     assert b"v is NULL" in lib.nha_last_error()
     assert _pre(lib, q=0, B=0) == 0  # no heads: nothing to do
+    assert _pre(lib, win=ctypes.c_void_p(4097)) == 1 and b"windows" in lib.nha_last_error()
     # T = 0 reads no prompt and w = 0 uses no ring: validation passes, the injected failure stops the call
     monkeypatch.setenv("NHA_FAULT_INJECT", "prefill_launch")
-    assert lib.nha_decode_prefill(None, None, None, p, p, None, None, None, 1, 1, 0, 64, 16, 0, 1, None) == 5
+    assert lib.nha_decode_prefill(None, None, None, p, p, None, None, None, None, 1, 1, 0, 64, 16, 0, 1, None) == 5
     monkeypatch.delenv("NHA_FAULT_INJECT")
 
 
@@ -211,12 +212,14 @@ def test_decode_varlen_validation(lib, monkeypatch):
     p = ctypes.c_void_p(4096)
     args = [p] * 10
     # positions are required (unless there are no heads) and must be 4-byte aligned
-    assert lib.nha_decode_step_varlen(*args, None, 2, 1, 64, 16, 4, 1, 1e4, None) == 1
+    assert lib.nha_decode_step_varlen(*args, None, None, 2, 1, 64, 16, 4, 1, 1e4, None) == 1
     assert b"positions" in lib.nha_last_error()
-    assert lib.nha_decode_step_varlen(*args, ctypes.c_void_p(4098), 2, 1, 64, 16, 4, 1, 1e4, None) == 1
+    assert lib.nha_decode_step_varlen(*args, ctypes.c_void_p(4098), None, 2, 1, 64, 16, 4, 1, 1e4, None) == 1
     assert b"aligned" in lib.nha_last_error()
-    assert lib.nha_decode_step_varlen(*([None] * 10), None, 0, 1, 64, 16, 4, 1, 1e4, None) == 0
-    assert lib.nha_decode_step_varlen(*args, p, 2, 1, 96, 16, 4, 1, 1e4, None) == 2
+    assert lib.nha_decode_step_varlen(*args, p, ctypes.c_void_p(4097), 2, 1, 64, 16, 4, 1, 1e4, None) == 1
+    assert b"windows" in lib.nha_last_error()
+    assert lib.nha_decode_step_varlen(*([None] * 10), None, None, 0, 1, 64, 16, 4, 1, 1e4, None) == 0
+    assert lib.nha_decode_step_varlen(*args, p, None, 2, 1, 96, 16, 4, 1, 1e4, None) == 2
     monkeypatch.setenv("NHA_FAULT_INJECT", "decode_launch")
-    assert lib.nha_decode_step_varlen(*args, p, 2, 1, 64, 16, 4, 1, 1e4, None) == 5
+    assert lib.nha_decode_step_varlen(*args, p, p, 2, 1, 64, 16, 4, 1, 1e4, None) == 5
     monkeypatch.delenv("NHA_FAULT_INJECT")

@@ -292,3 +292,45 @@ def test_varlen_position_out_of_range_is_nan_and_leaves_the_state():
     o_ref = decode_step(st, _np(q[1:2]), _np(k[1:2]), _np(v[1:2]), _np(la[1:2]), 20)
     _check_o(o[1:2], o_ref, "f32", "varlen sequence 1")
     assert np.abs(_np(state[0][1:2]) - st.S_k).max() <= 1e-5
+
+
+@pytest.mark.parametrize("d,m,dtype", [(64, 16, "f32"), (128, 64, "bf16")])
+def test_per_head_windows_prefill_and_varlen_decode(d, m, dtype):
+    """Heads with windows 0, 5, 37 and 64 inside one 64-entry ring: prefill on
+    prompts of 50 and 200 tokens, then varlen decode; each (sequence, head)
+    against the oracle's forward with that head's own window."""
+    nha = _nha()
+    B, H, w, K = 2, 4, 64, 6
+    wins, prompts = [0, 5, 37, 64], [50, 200]
+    wl = Workload("per-head windows", B, H, max(prompts) + K, d, m, w, dtype=dtype, seed=7000 + d)
+    x = make_inputs(wl)
+    dev = {n: t.cuda() for n, t in x.items()}
+    windows = torch.tensor(wins, dtype=torch.int32, device="cuda")
+    state = nha.nha_decode_state(B, H, d, m, w, dtype=wl.torch_dtype)
+    for b, T in enumerate(prompts):
+        sub = tuple(a[b:b + 1] for a in state)
+        nha.nha_decode_prefill(dev["k"][b:b + 1, :, :T].contiguous(), dev["v"][b:b + 1, :, :T].contiguous(),
+                               dev["log_alpha"][b:b + 1, :, :T].contiguous(), w, state=sub, windows=windows)
+    pos = torch.tensor(prompts, dtype=torch.int32, device="cuda")
+    outs = []
+    for step in range(K):
+        tok = {n: torch.stack([dev[n][b, :, prompts[b] + step] for b in range(B)]).contiguous() for n in dev}
+        outs.append(nha.nha_decode_step_varlen(tok["q"], tok["k"], tok["v"], tok["log_alpha"], pos, w, state,
+                                               windows=windows))
+        pos += 1
+    torch.cuda.synchronize()
+    got = _np(torch.stack(outs, dim=2))
+    for b, T in enumerate(prompts):
+        for h, wh in enumerate(wins):
+            sel = {n: t[b:b + 1, h:h + 1, :T + K] for n, t in x.items()}
+            o_ref, _ = oracle.forward(sel["q"], sel["k"], sel["v"], sel["log_alpha"], wh)
+            _check_o(got[b:b + 1, h:h + 1], o_ref[:, :, T:], dtype, f"sequence {b} head {h} window {wh}")
+    # a window beyond the ring: NaN for that head, its state untouched
+    before = [a.clone() for a in state]
+    bad = torch.tensor([w + 1] + wins[1:], dtype=torch.int32, device="cuda")
+    tok = {n: torch.stack([dev[n][b, :, prompts[b] + K] for b in range(B)]).contiguous() for n in dev}
+    o = nha.nha_decode_step_varlen(tok["q"], tok["k"], tok["v"], tok["log_alpha"], pos, w, state, windows=bad)
+    torch.cuda.synchronize()
+    assert torch.isnan(o[:, 0]).all() and not torch.isnan(o[:, 1:]).any()
+    for a, a0 in zip(state, before):
+        assert torch.equal(a[:, 0], a0[:, 0])
