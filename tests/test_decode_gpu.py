@@ -302,7 +302,7 @@ def test_per_head_windows_prefill_and_varlen_decode(d, m, dtype):
     nha = _nha()
     B, H, w, K = 2, 4, 64, 6
     wins, prompts = [0, 5, 37, 64], [50, 200]
-    wl = Workload("per-head windows", B, H, max(prompts) + K, d, m, w, dtype=dtype, seed=7000 + d)
+    wl = Workload("per-head windows", B, H, max(prompts) + K + 1, d, m, w, dtype=dtype, seed=7000 + d)
     x = make_inputs(wl)
     dev = {n: t.cuda() for n, t in x.items()}
     windows = torch.tensor(wins, dtype=torch.int32, device="cuda")
