@@ -41,8 +41,8 @@ def _rope_polar(x, base=10000.0):
 
 # --------------------------------------------------------------------------------------
 # w >= T: long memory never receives a token (all slots masked) -> causal softmax
-# attention with RoPE (Paper-Notes, 整体框架: a window as long as the sequence
-# recovers full attention).  Checked against torch's SDPA.
+# attention with RoPE (Paper-Notes, 关键设计/层间混合: a window as long as the
+# sequence recovers full attention).  Checked against torch's SDPA.
 @pytest.mark.parametrize("T,d,m,extra", [(33, 8, 3, 0), (40, 16, 4, 7), (1, 4, 2, 0)])
 def test_full_window_is_causal_attention(T, d, m, extra):
     q, k, v, la, _ = _rand(2, 3, T, d, m, seed=11 + T)
@@ -54,7 +54,7 @@ def test_full_window_is_causal_attention(T, d, m, extra):
 
 # --------------------------------------------------------------------------------------
 # w = 0: a pure gated-slot linear RNN read by a softmax over the m slots
-# (Paper-Notes, 整体框架: an empty window leaves a linear RNN).  With per-slot
+# (Paper-Notes, 关键设计/层间混合: an empty window leaves a linear RNN).  With per-slot
 # gates that are constant in time, each
 # slot state is a first-order IIR filter of the key/value stream, which
 # scipy.signal.lfilter computes: y_t = alpha y_{t-1} + (1 - alpha) x_t.
