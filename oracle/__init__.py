@@ -55,10 +55,10 @@ def _load():
             L = ctypes.c_long
             lib.nha_oracle_forward.restype = ctypes.c_int
             lib.nha_oracle_forward.argtypes = [dp, dp, dp, dp, dp, dp, dp, L, L, L, L, L, L,
-                                               ctypes.c_double, ctypes.c_int]
+                                               ctypes.c_double, ctypes.c_int, dp, dp]
             lib.nha_oracle_backward.restype = ctypes.c_int
             lib.nha_oracle_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, L, L, L, L,
-                                                L, L, ctypes.c_double, ctypes.c_int]
+                                                L, L, ctypes.c_double, ctypes.c_int, dp, dp, dp, dp]
             lib.nha_oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -77,39 +77,62 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
+def _ptr_or_null(a):
+    return None if a is None else _ptr(a)
+
+
 def num_threads() -> int:
     """OpenMP threads the oracle uses by default (all host cores)."""
     return int(_load().nha_oracle_num_threads())
 
 
+def _h0(h0, B, H, m, d):
+    """(h0k, h0v) as contiguous float64 [B,H,m,d] arrays, or (None, None)."""
+    if h0 is None:
+        return None, None
+    hk, hv = _f64(h0[0]), _f64(h0[1])
+    assert hk.shape == (B, H, m, d) and hv.shape == (B, H, m, d)
+    return hk, hv
+
+
 def forward(q, k, v, log_alpha, w: int, rope_base: float = 10000.0, nthreads: int = 0,
-            with_omega: bool = False):
-    """fp64 NHA forward.  Returns (o, lse) or (o, lse, omega_L)."""
+            with_omega: bool = False, h0=None):
+    """fp64 NHA forward.  Returns (o, lse) or (o, lse, omega_L).
+
+    h0 = (h0k, h0v), each [B,H,m,d]: initial slot states (the long memory before
+    token 0); with them no slot logit is masked."""
     q, k, v, la = _f64(q), _f64(k), _f64(v), _f64(log_alpha)
     B, H, T, d = q.shape
     m = la.shape[-1]
     assert k.shape == q.shape and v.shape == q.shape and la.shape[:3] == (B, H, T)
+    hk, hv = _h0(h0, B, H, m, d)
     o = np.zeros_like(q)
     lse = np.zeros((B, H, T), dtype=np.float64)
     om = np.zeros((B, H, T), dtype=np.float64)
     rc = _load().nha_oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(o), _ptr(lse),
                                     _ptr(om), B, H, T, d, m, int(w), float(rope_base),
-                                    int(nthreads))
+                                    int(nthreads), _ptr_or_null(hk), _ptr_or_null(hv))
     if rc != 0:
         raise ValueError(f"oracle forward rejected the shape (rc={rc})")
     return (o, lse, om) if with_omega else (o, lse)
 
 
-def backward(q, k, v, log_alpha, dout, w: int, rope_base: float = 10000.0, nthreads: int = 0):
-    """fp64 NHA backward of loss = sum(o * dout).  Returns (dq, dk, dv, dlog_alpha)."""
+def backward(q, k, v, log_alpha, dout, w: int, rope_base: float = 10000.0, nthreads: int = 0,
+             h0=None):
+    """fp64 NHA backward of loss = sum(o * dout).  Returns (dq, dk, dv, dlog_alpha),
+    and with h0 = (h0k, h0v) also (dh0k, dh0v)."""
     q, k, v, la, g = _f64(q), _f64(k), _f64(v), _f64(log_alpha), _f64(dout)
     B, H, T, d = q.shape
     m = la.shape[-1]
+    hk, hv = _h0(h0, B, H, m, d)
     dq, dk, dv = np.zeros_like(q), np.zeros_like(q), np.zeros_like(q)
     dla = np.zeros_like(la)
+    dhk = np.zeros((B, H, m, d)) if hk is not None else None
+    dhv = np.zeros((B, H, m, d)) if hk is not None else None
     rc = _load().nha_oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(g), _ptr(dq),
                                      _ptr(dk), _ptr(dv), _ptr(dla), B, H, T, d, m, int(w),
-                                     float(rope_base), int(nthreads))
+                                     float(rope_base), int(nthreads), _ptr_or_null(hk),
+                                     _ptr_or_null(hv), _ptr_or_null(dhk), _ptr_or_null(dhv))
     if rc != 0:
         raise ValueError(f"oracle backward rejected the shape (rc={rc})")
-    return dq, dk, dv, dla
+    return (dq, dk, dv, dla) if hk is None else (dq, dk, dv, dla, dhk, dhv)

@@ -18,6 +18,10 @@ softmax over the m slots and the window) taken for a single new token t:
 
 Between steps the caller keeps the slot states and a ring of the last w tokens
 (raw k, v and log_alpha; token s in entry s mod w).  Everything is float64.
+
+A state may start from initial slot states h0 (``DecodeState(..., init=(h0k, h0v))``):
+the long memory before token 0 is then h0, and since it is never empty the
+slot logits are not masked while t < w (those queries read h0 itself).
 """
 from __future__ import annotations
 
@@ -40,10 +44,14 @@ def rope(x: np.ndarray, pos: int, base: float) -> np.ndarray:
 class DecodeState:
     """Slot states S^K, S^V [B, H, m, d] and the window ring [B, H, w, .] of one layer."""
 
-    def __init__(self, B: int, H: int, d: int, m: int, w: int):
+    def __init__(self, B: int, H: int, d: int, m: int, w: int, init=None):
         self.w = w
         self.S_k = np.zeros((B, H, m, d))
         self.S_v = np.zeros((B, H, m, d))
+        self.has_init = init is not None
+        if init is not None:
+            self.S_k = np.array(init[0], dtype=np.float64).reshape(B, H, m, d)
+            self.S_v = np.array(init[1], dtype=np.float64).reshape(B, H, m, d)
         n = max(w, 1)
         self.ring_k = np.zeros((B, H, n, d))
         self.ring_v = np.zeros((B, H, n, d))
@@ -66,6 +74,8 @@ def decode_step(st: DecodeState, q, k, v, log_alpha, t: int, base: float = 10000
         alpha, u = np.exp(lj), -np.expm1(lj)
         st.S_k = alpha[..., None] * st.S_k + u[..., None] * kj[:, :, None, :]
         st.S_v = alpha[..., None] * st.S_v + u[..., None] * vj[:, :, None, :]
+    slots = t - w >= 0 or st.has_init
+    if slots:
         L = np.einsum("bhd,bhmd->bhm", q, st.S_k) * scale
     else:
         L = np.full(q.shape[:2] + (st.S_k.shape[2],), -np.inf)
@@ -85,7 +95,7 @@ def decode_step(st: DecodeState, q, k, v, log_alpha, t: int, base: float = 10000
     p = np.exp(logits - mx)
     p /= p.sum(axis=-1, keepdims=True)
     m = L.shape[-1]
-    o = np.einsum("bhm,bhmd->bhd", p[..., :m], st.S_v) if t - w >= 0 else np.zeros_like(q)
+    o = np.einsum("bhm,bhmd->bhd", p[..., :m], st.S_v) if slots else np.zeros_like(q)
     for n, vs in enumerate(vals):
         o = o + p[..., m + n, None] * vs
     # the ring keeps the last w tokens (token t takes the entry of the token that left)

@@ -16,6 +16,10 @@ its complex form: the pair (x_i, x_{i+d/2}) is the complex number
 x_i + i x_{i+d/2}, multiplied by exp(i * pos * base^(-2i/d)).  One softmax
 with scale 1/sqrt(d) runs over [slot logits | window logits].
 
+With initial slot states h0 (the long memory before token 0) the state after
+token j gains (prod_{r=0..j} alpha_r) h0 = exp(cumsum(log_alpha)_j) h0, queries
+t < w read h0 itself, and no slot logit is masked.
+
 Only for tiny shapes: memory is O(B H T^2 m).
 """
 from __future__ import annotations
@@ -38,8 +42,8 @@ def rope_complex(x: torch.Tensor, base: float) -> torch.Tensor:
     return torch.cat([z.real, z.imag], dim=-1)
 
 
-def slot_states(x: torch.Tensor, log_alpha: torch.Tensor) -> torch.Tensor:
-    """Closed-form slot state after each token: [B,H,T(j),m,d]."""
+def slot_states(x: torch.Tensor, log_alpha: torch.Tensor, h0=None) -> torch.Tensor:
+    """Closed-form slot state after each token: [B,H,T(j),m,d] (h0 [B,H,m,d] or None)."""
     T = x.shape[-2]
     b = torch.cumsum(log_alpha, dim=-2)  # [B,H,T,m]
     u = -torch.expm1(log_alpha)
@@ -49,22 +53,32 @@ def slot_states(x: torch.Tensor, log_alpha: torch.Tensor) -> torch.Tensor:
     expo = b[:, :, :, None, :] - b[:, :, None, :, :]  # [B,H,j,s,m]
     expo = torch.where(causal, expo, torch.full_like(expo, -math.inf))
     decay = torch.exp(expo)
-    return torch.einsum("bhjsi,bhsi,bhsd->bhjid", decay, u, x)
+    S = torch.einsum("bhjsi,bhsi,bhsd->bhjid", decay, u, x)
+    if h0 is not None:
+        S = S + torch.exp(b)[..., None] * h0[:, :, None]
+    return S
 
 
-def nha_naive(q, k, v, log_alpha, w: int, rope_base: float = 10000.0, return_omega=False):
-    """Forward of NHA for float64 tensors; returns (o, lse) [, omega_L]."""
+def nha_naive(q, k, v, log_alpha, w: int, rope_base: float = 10000.0, return_omega=False, h0k=None, h0v=None):
+    """Forward of NHA for float64 tensors; returns (o, lse) [, omega_L].
+    h0k, h0v [B,H,m,d]: optional initial slot states."""
     B, H, T, d = q.shape
     m = log_alpha.shape[-1]
     w = min(int(w), T)
     sigma = 1.0 / math.sqrt(d)
-    SK = slot_states(k, log_alpha)  # [B,H,T,m,d]
-    SV = slot_states(v, log_alpha)
+    SK = slot_states(k, log_alpha, h0k)  # [B,H,T,m,d]
+    SV = slot_states(v, log_alpha, h0v)
     t = torch.arange(T)
-    has = t >= w
     jidx = (t - w).clamp(min=0)
     SKq = SK[:, :, jidx]  # state read by query t
     SVq = SV[:, :, jidx]
+    if h0k is None:
+        has = t >= w
+    else:  # the long memory is never empty: queries t < w read h0
+        has = torch.ones(T, dtype=torch.bool)
+        early = (t < w)[None, None, :, None, None]
+        SKq = torch.where(early, h0k[:, :, None], SKq)
+        SVq = torch.where(early, h0v[:, :, None], SVq)
     L = sigma * torch.einsum("bhtd,bhtid->bhti", q, SKq)
     L = torch.where(has[None, None, :, None], L, torch.full_like(L, -math.inf))
     qr, kr = rope_complex(q, rope_base), rope_complex(k, rope_base)
@@ -82,10 +96,11 @@ def nha_naive(q, k, v, log_alpha, w: int, rope_base: float = 10000.0, return_ome
     return o, lse
 
 
-def nha_naive_grads(q, k, v, log_alpha, dout, w: int, rope_base: float = 10000.0):
-    """Autograd gradients of sum(o * dout): (dq, dk, dv, dlog_alpha), float64."""
-    leaves = [x.detach().clone().to(torch.float64).requires_grad_(True)
-              for x in (q, k, v, log_alpha)]
-    o, _ = nha_naive(*leaves, w=w, rope_base=rope_base)
+def nha_naive_grads(q, k, v, log_alpha, dout, w: int, rope_base: float = 10000.0, h0k=None, h0v=None):
+    """Autograd gradients of sum(o * dout): (dq, dk, dv, dlog_alpha[, dh0k, dh0v]), float64."""
+    inputs = (q, k, v, log_alpha) + ((h0k, h0v) if h0k is not None else ())
+    leaves = [x.detach().clone().to(torch.float64).requires_grad_(True) for x in inputs]
+    h0 = dict(h0k=leaves[4], h0v=leaves[5]) if h0k is not None else {}
+    o, _ = nha_naive(*leaves[:4], w=w, rope_base=rope_base, **h0)
     (o * dout.to(torch.float64)).sum().backward()
     return tuple(x.grad for x in leaves)

@@ -24,6 +24,12 @@
  *     one softmax over the m + n_win logits; lse_t = log of its partition
  *     o_t = sum_i p_i S^V[i] + sum_s p_s v_s
  *
+ * Optional initial slot states (h0k, h0v in R^{m x d} per head; the pages'
+ * Future Directions name learned initial states): the long memory before
+ * token 0 is h0 instead of zero, and because it is then never empty the
+ * slot logits are not masked for t < w (query t < w reads h0 itself).
+ * The backward returns dh0 = the state adjoint carried back past token 0.
+ *
  * Readings of points the pages leave open:
  *   - token j is absorbed with its own gate alpha_j, and the query at t reads
  *     the state after token t-w (the token shift);
@@ -138,21 +144,23 @@ static long window_lo(long t, long w) {
     return lo < 0 ? 0 : lo;
 }
 
-/* One (b,h) head, forward. */
+/* One (b,h) head, forward.  h0k, h0v: initial states [m][d] or NULL. */
 static void head_forward(const shape_t* sh, const double* q, const double* k, const double* v,
                          const double* la, double* o, double* lse, double* omega,
-                         const double* cs, const double* sn) {
+                         const double* cs, const double* sn, const double* h0k, const double* h0v) {
     long T = sh->T, d = sh->d, m = sh->m, w = sh->w, h = d / 2;
     double* SK = calloc((size_t)(m * d), sizeof(double));
     double* SV = calloc((size_t)(m * d), sizeof(double));
+    if (h0k) memcpy(SK, h0k, sizeof(double) * (size_t)(m * d));
+    if (h0v) memcpy(SV, h0v, sizeof(double) * (size_t)(m * d));
     double* kr = malloc(sizeof(double) * (size_t)(T * d));
     double* qr = malloc(sizeof(double) * (size_t)d);
     double* L = malloc(sizeof(double) * (size_t)(m > 0 ? m : 1));
     double* Sw = malloc(sizeof(double) * (size_t)(T + 1));
     for (long s = 0; s < T; s++) rope_apply(k + s * d, kr + s * d, d, cs + s * h, sn + s * h);
     for (long t = 0; t < T; t++) {
-        int have_slots = (t >= w);
-        if (have_slots) {
+        int have_slots = (t >= w) || h0k != NULL;
+        if (t >= w) {
             long j = t - w;
             absorb(SK, la + j * m, k + j * d, m, d);
             absorb(SV, la + j * m, v + j * d, m, d);
@@ -180,10 +188,13 @@ static void head_forward(const shape_t* sh, const double* q, const double* k, co
     free(SK); free(SV); free(kr); free(qr); free(L); free(Sw);
 }
 
-/* One (b,h) head, backward (reverse sweep with state adjoints). */
+/* One (b,h) head, backward (reverse sweep with state adjoints).  h0k, h0v:
+ * initial states or NULL; dh0k, dh0v (written when h0k is given): their
+ * gradients. */
 static void head_backward(const shape_t* sh, const double* q, const double* k, const double* v,
                           const double* la, const double* dout, double* dq, double* dk,
-                          double* dv, double* dla, const double* cs, const double* sn) {
+                          double* dv, double* dla, const double* cs, const double* sn,
+                          const double* h0k, const double* h0v, double* dh0k, double* dh0v) {
     long T = sh->T, d = sh->d, m = sh->m, w = sh->w, h = d / 2;
     long md = m * d;
     double sigma = 1.0 / sqrt((double)d);
@@ -218,6 +229,8 @@ static void head_backward(const shape_t* sh, const double* q, const double* k, c
     {
         double* SK = calloc((size_t)md, sizeof(double));
         double* SV = calloc((size_t)md, sizeof(double));
+        if (h0k) memcpy(SK, h0k, sizeof(double) * (size_t)md);
+        if (h0v) memcpy(SV, h0v, sizeof(double) * (size_t)md);
         for (long j = 0; j < R; j++) {
             if (j % CKPT == 0) {
                 memcpy(ckK + (j / CKPT) * md, SK, sizeof(double) * (size_t)md);
@@ -313,10 +326,15 @@ static void head_backward(const shape_t* sh, const double* q, const double* k, c
             }
         }
     }
-    /* window-only queries t < w */
+    /* queries t < w: window only, or (with initial states) reading h0; dSK,
+     * dSV now hold the adjoint of the state before token 0, which is h0 */
     {
         long tw = w < T ? w : T;
-        for (long t = tw - 1; t >= 0; t--) QUERY_BACKWARD(t, (const double*)NULL, (const double*)NULL);
+        for (long t = tw - 1; t >= 0; t--) QUERY_BACKWARD(t, h0k, h0v);
+    }
+    if (h0k) {
+        memcpy(dh0k, dSK, sizeof(double) * (size_t)md);
+        memcpy(dh0v, dSV, sizeof(double) * (size_t)md);
     }
 #undef QUERY_BACKWARD
     for (long s = 0; s < T; s++) rope_apply_t_acc(dkr + s * d, dk + s * d, d, cs + s * h, sn + s * h);
@@ -333,9 +351,12 @@ static int check_shape(long B, long H, long T, long d, long m, long w) {
 /* o[B,H,T,d], lse[B,H,T], omega[B,H,T] (optional, may be NULL): the share of
  * softmax mass on the long-memory slots (the omega_L diagnostic of the same
  * section). */
+/* h0k, h0v [B,H,m,d]: optional initial slot states (both or neither). */
 int nha_oracle_forward(const double* q, const double* k, const double* v, const double* log_alpha,
                        double* o, double* lse, double* omega, long B, long H, long T, long d,
-                       long m, long w, double rope_base, int nthreads) {
+                       long m, long w, double rope_base, int nthreads, const double* h0k,
+                       const double* h0v) {
+    if ((h0k == NULL) != (h0v == NULL)) return -1;
     if (check_shape(B, H, T, d, m, w)) return -1;
     if (T == 0 || B * H == 0) return 0;
     shape_t sh = {T, d, m, w > T ? T : w, rope_base};
@@ -350,17 +371,23 @@ int nha_oracle_forward(const double* q, const double* k, const double* v, const 
 #endif
     for (long bh = 0; bh < nbh; bh++) {
         head_forward(&sh, q + bh * T * d, k + bh * T * d, v + bh * T * d, log_alpha + bh * T * m,
-                     o + bh * T * d, lse + bh * T, omega ? omega + bh * T : NULL, cs, sn);
+                     o + bh * T * d, lse + bh * T, omega ? omega + bh * T : NULL, cs, sn,
+                     h0k ? h0k + bh * m * d : NULL, h0v ? h0v + bh * m * d : NULL);
     }
     (void)nthreads;
     free(cs); free(sn);
     return 0;
 }
 
+/* h0k, h0v [B,H,m,d]: optional initial slot states; dh0k, dh0v [B,H,m,d]
+ * receive their gradients (all four given, or none). */
 int nha_oracle_backward(const double* q, const double* k, const double* v, const double* log_alpha,
                         const double* dout, double* dq, double* dk, double* dv, double* dlog_alpha,
                         long B, long H, long T, long d, long m, long w, double rope_base,
-                        int nthreads) {
+                        int nthreads, const double* h0k, const double* h0v, double* dh0k,
+                        double* dh0v) {
+    int given = (h0k != NULL) + (h0v != NULL) + (dh0k != NULL) + (dh0v != NULL);
+    if (given != 0 && given != 4) return -1;
     if (check_shape(B, H, T, d, m, w)) return -1;
     if (T == 0 || B * H == 0) return 0;
     shape_t sh = {T, d, m, w > T ? T : w, rope_base};
@@ -376,7 +403,9 @@ int nha_oracle_backward(const double* q, const double* k, const double* v, const
     for (long bh = 0; bh < nbh; bh++) {
         head_backward(&sh, q + bh * T * d, k + bh * T * d, v + bh * T * d, log_alpha + bh * T * m,
                       dout + bh * T * d, dq + bh * T * d, dk + bh * T * d, dv + bh * T * d,
-                      dlog_alpha + bh * T * m, cs, sn);
+                      dlog_alpha + bh * T * m, cs, sn, h0k ? h0k + bh * m * d : NULL,
+                      h0v ? h0v + bh * m * d : NULL, dh0k ? dh0k + bh * m * d : NULL,
+                      dh0v ? dh0v + bh * m * d : NULL);
     }
     (void)nthreads;
     free(cs); free(sn);
