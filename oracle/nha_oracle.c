@@ -24,8 +24,8 @@
  *     one softmax over the m + n_win logits; lse_t = log of its partition
  *     o_t = sum_i p_i S^V[i] + sum_s p_s v_s
  *
- * Optional initial slot states (h0k, h0v in R^{m x d} per head; the pages'
- * Future Directions name learned initial states): the long memory before
+ * Optional initial slot states (h0k, h0v in R^{m x d} per head; the ai.info
+ * page, Future Directions, names learned initial slot states): the long memory before
  * token 0 is h0 instead of zero, and because it is then never empty the
  * slot logits are not masked for t < w (query t < w reads h0 itself).
  * The backward returns dh0 = the state adjoint carried back past token 0.

@@ -1,7 +1,7 @@
 """Pins of the oracle's optional initial slot states h0 (CPU only).
 
-Reading: h0 = (h0k, h0v) is the long memory before token 0 (the pages' Future
-Directions name learned initial states); the memory is then never empty, so
+Reading: h0 = (h0k, h0v) is the long memory before token 0 (the ai.info page,
+Future Directions, names learned initial slot states); the memory is then never empty, so
 no slot logit is masked and queries t < w read h0 itself.  The C oracle's
 forward and hand-derived backward are pinned to the unrolled closed form with
 autograd, to finite differences, to the decode restatement started from h0,
