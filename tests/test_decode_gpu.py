@@ -6,6 +6,9 @@ against the fp64 oracle, on seeded inputs (bf16 inputs upcast exactly).
   oracle's own decode recurrence; the ring holds raw copies (bit-exact).
 * Serving-sized batches at a late position t: one step from a random state
   and ring, against the oracle's decode step on the same state.
+* The prefill entry point, per-sequence positions (continuous batching, CUDA
+  graph replay with positions advanced on the device) and per-head windows:
+  every output against the oracle's forward over that sequence and head.
 
 Tolerances: fp32: max |err| <= 1e-4 on o, <= 1e-5 on the states;
 bf16: o rel L2 <= 5e-3 and max |err| <= 2e-2 (o is rounded to bf16),
