@@ -223,3 +223,25 @@ def test_decode_varlen_validation(lib, monkeypatch):
     monkeypatch.setenv("NHA_FAULT_INJECT", "decode_launch")
     assert lib.nha_decode_step_varlen(*args, p, p, 2, 1, 64, 16, 4, 1, 1e4, None) == 5
     monkeypatch.delenv("NHA_FAULT_INJECT")
+
+
+def test_public_header_is_plain_c_and_links_against_the_library(lib, tmp_path):
+    """include/nha.h compiles as C99 (no C++ in the ABI), and a C program that
+    takes the address of every declared entry point links against libnha.so."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = sorted(_declared_symbols())
+    src = tmp_path / "abi.c"
+    src.write_text('#include "nha.h"\ntypedef void (*fn_t)(void);\n'
+                   + "static fn_t volatile table[] = {\n"
+                   + "".join(f"    (fn_t){n},\n" for n in names)
+                   + "};\nint main(void) { return table[0] == 0; }\n")
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(_binding.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic", f"-I{os.path.join(ROOT, 'include')}",
+                        str(src), "-o", str(exe), f"-L{libdir}", "-l:libnha.so"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
