@@ -185,11 +185,13 @@ nha_status_t nha_decode_prefill(const void* k, const void* v, const float* log_a
  *
  * Limit: shapes whose forward workspace (nha_workspace_bytes(..., 0)) exceeds
  * NHA_NOALLOC_SCRATCH_BYTES are rejected with NHA_ERR_WORKSPACE before any
- * work is enqueued; 32 MiB covers, e.g., B*H = 8 heads of T = 2048 at
- * d = 128, m = 64.
- * Set-up: the first call on a device looks up the scratch's device address on
- * the current device (cudaGetSymbolAddress); make that first call before any
- * stream capture.
+ * work is enqueued.  The workspace grows as w shrinks (more tokens leave the
+ * window), so compare nha_workspace_bytes(..., 0) for the shape and window at
+ * hand against NHA_NOALLOC_SCRATCH_BYTES.
+ * Set-up: the first call on a device (and the first call after that device's
+ * context was replaced, e.g. by cudaDeviceReset) looks up the scratch's
+ * device address in the current context (cudaGetSymbolAddress); make that
+ * call before any stream capture.
  * Sharing: all calls use the same scratch, which keeps the last call's
  * contents (the forward overwrites every part it reads, so nothing has to
  * start at zero).  Calls whose execution overlaps on the GPU (different

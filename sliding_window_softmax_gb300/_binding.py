@@ -126,6 +126,12 @@ def _stream_handle(stream) -> ctypes.c_void_p:
 def _check(name, t, dtype=None, shape=None):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    # the library launches on the current device and takes that device's stream
+    # (and, for the no-allocation forward, its scratch): tensors elsewhere would
+    # be read through the wrong device's context
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{torch.cuda.current_device()}; "
+                         "call under torch.cuda.device(...)")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:

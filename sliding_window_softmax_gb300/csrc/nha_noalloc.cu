@@ -3,6 +3,8 @@
 // (code running inside a CUDA-graph capture or under an allocator that is
 // owned by someone else, or plugins that receive only input and output
 // buffers from their host).  The operation itself is nha_forward's.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "nha.h"
@@ -19,7 +21,21 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char nha_noalloc_scratch[NHA_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_mu;
+// Per device: the context the address was looked up in, and the address.  A
+// new primary context (after cudaDeviceReset) reloads the module, so the
+// lookup is repeated whenever the current context differs.
+void* g_ctx[kMaxDevices] = {nullptr};
 void* g_addr[kMaxDevices] = {nullptr};
+PFN_cuCtxGetCurrent_v4000 g_get_ctx = nullptr;
+std::once_flag g_get_ctx_once;
+
+void resolve_get_ctx() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_get_ctx = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+}
 
 }  // namespace
 
@@ -42,16 +58,25 @@ extern "C" nha_status_t nha_forward_noalloc(const void* q, const void* k, const 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return nha::set_error(NHA_ERR_CUDA, "nha_forward_noalloc: no usable current device");
+    std::call_once(g_get_ctx_once, resolve_get_ctx);
+    if (g_get_ctx == nullptr)
+        return nha::set_error(NHA_ERR_CUDA, "nha_forward_noalloc: cuCtxGetCurrent is not available");
+    CUcontext ctx = nullptr;  // null until the runtime has set up the device's context
+    if (g_get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
     void* ptr = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        if (g_addr[dev] == nullptr) {
+        if (ctx == nullptr || g_addr[dev] == nullptr || g_ctx[dev] != (void*)ctx) {
             void* p = nullptr;
             const cudaError_t e = cudaGetSymbolAddress(&p, nha_noalloc_scratch);
             if (e != cudaSuccess || p == nullptr)
                 return nha::set_error(NHA_ERR_CUDA, "nha_forward_noalloc: cudaGetSymbolAddress failed: %s",
                                       cudaGetErrorString(e));
+            // the lookup has made the device's primary context current
+            if (g_get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+                return nha::set_error(NHA_ERR_CUDA, "nha_forward_noalloc: no current CUDA context");
             g_addr[dev] = p;
+            g_ctx[dev] = (void*)ctx;
         }
         ptr = g_addr[dev];
     }

@@ -79,3 +79,25 @@ def test_traffic_lines_parse_and_match_only_their_sources():
         else:
             assert got is None
         assert bench.ncu_traffic(kernel, workload + "-other") is None
+
+
+def test_step_roofline_frac_is_the_step_figure():
+    mdl = bench.work_model(LAYER_1P3B)
+    peaks = {"hbm_gbs": 6781.4, "bf16_tflops": 1926.9}
+    t_roof, roof = bench.step_roofline(mdl, peaks, 0.5)
+    # the 1.3B-like layer is HBM-bound: 504 MB of algorithmic bytes per step
+    assert roof["bound"] == "hbm" and roof["algorithmic_bytes"] == mdl["step_bytes"]
+    assert abs(mdl["step_bytes"] / 1e6 - 503.3) < 1.5
+    assert roof["frac"] == pytest.approx(t_roof / 0.5e-3)
+    assert t_roof == pytest.approx(mdl["step_bytes"] / 6781.4e9)
+    # the w = T endpoint is tensor-bound
+    wt = bench.work_model(LAYER_1P3B.with_(w=2048))
+    t2, r2 = bench.step_roofline(wt, peaks, 1.0)
+    assert r2["bound"] == "tensor" and r2["frac"] == pytest.approx(t2 / 1e-3)
+    _, rf = bench.step_roofline(mdl, peaks, 0.2, backward=False)
+    assert rf["algorithmic_bytes"] == mdl["fwd_bytes"]
+
+
+def test_step_traffic_needs_every_kernel():
+    assert bench.step_traffic({"no_such_kernel": 1.0}, "1.3B") is None
+    assert bench.step_traffic({}, "1.3B") == 0.0
