@@ -2,6 +2,8 @@
 """Benchmark of the NHA layer operator (forward + backward) on GB300.
 
 One step = nha_forward + nha_backward over one batch of the chosen workload
+(the backward given the forward's workspace, so it reuses the chunk states and
+rotated q, k the forward formed, as a training step keeps them)
 (default: the 1.3B-like layer, B4 H16 T2048 d128 m64 w512 C64, bf16), inputs
 resident in HBM.  Prints ONE JSON line (rank 0).
 
@@ -469,8 +471,11 @@ def run_nha(args, wl, wl_key):
     dla = torch.empty_like(d["log_alpha"])
     wsf = torch.empty(max(1, nha.nha_workspace_bytes(B, H, T, D, wl.m, wl.w, wl.C, d["q"].dtype)),
                       dtype=torch.uint8, device=dev)
+    # the backward reuses what the forward left in its workspace (chunk states,
+    # rotated q and k): the saved-for-backward context of a training step
     wsb = torch.empty(max(1, nha.nha_workspace_bytes(B, H, T, D, wl.m, wl.w, wl.C, d["q"].dtype,
-                                                     backward=True)), dtype=torch.uint8, device=dev)
+                                                     backward=True, reuse_forward=True)),
+                      dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step(fwd_evt=None):
@@ -481,7 +486,7 @@ def run_nha(args, wl, wl_key):
         if wl.backward:
             nha.nha_backward(d["q"], d["k"], d["v"], d["log_alpha"], o, lse, d["dout"], wl.w,
                              wl.C, dq=dq, dk=dk, dv=dv, dlog_alpha=dla, workspace=wsb,
-                             stream=stream)
+                             stream=stream, fwd_workspace=wsf)
 
     clk = ClockSampler(local).__enter__()
     for _ in range(args.warmup):

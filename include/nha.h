@@ -101,6 +101,42 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
                           int C, nha_dtype_t dtype, float rope_base, void* workspace,
                           size_t ws_bytes, void* stream);
 
+/* ---- Extended calls: optional inputs and outputs ----
+ *
+ * nha_forward_ex / nha_backward_ex are nha_forward / nha_backward with an
+ * optional nha_extras_t (NULL, or a zero-initialised struct, gives exactly
+ * the plain calls).  Every pointer in it is optional (NULL = not used) and, if
+ * given, a DEVICE pointer with the layout stated beside it.
+ *
+ * fwd_workspace (backward only): the workspace the forward of the same
+ * inputs ran with (nha_forward or nha_forward_ex, same shape, dtype and
+ * rope_base), untouched since.  The backward then reads the chunk states,
+ * gate totals, RoPE table and rotated q, k the forward left there instead of
+ * forming them again, and its own workspace shrinks accordingly
+ * (nha_workspace_bytes_ex with the same extras).  This is the usual
+ * saved-for-backward context of a training step: keep the forward's
+ * workspace alive until the backward has been enqueued after it. */
+typedef struct {
+    const void* fwd_workspace; /* backward: the forward's workspace, read only */
+    size_t fwd_ws_bytes;       /* its size in bytes */
+} nha_extras_t;
+
+/* Workspace bytes of nha_forward_ex (backward = 0) / nha_backward_ex
+ * (backward = 1) with these extras; 0 for an invalid or unsupported shape. */
+size_t nha_workspace_bytes_ex(int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dtype,
+                              int backward, const nha_extras_t* extras);
+
+nha_status_t nha_forward_ex(const void* q, const void* k, const void* v, const float* log_alpha,
+                            void* o, float* lse, int B, int H, int T, int d, int m, int w, int C,
+                            nha_dtype_t dtype, float rope_base, const nha_extras_t* extras,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+nha_status_t nha_backward_ex(const void* q, const void* k, const void* v, const float* log_alpha,
+                             const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                             void* dv, float* dlog_alpha, int B, int H, int T, int d, int m, int w,
+                             int C, nha_dtype_t dtype, float rope_base, const nha_extras_t* extras,
+                             void* workspace, size_t ws_bytes, void* stream);
+
 /* ---- Recurrent decode step ----
  *
  * The operator above taken for one new token t of every (b, h) (same page,

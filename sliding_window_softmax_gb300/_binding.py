@@ -25,13 +25,20 @@ STATUS = {0: "NHA_OK", 1: "NHA_ERR_INVALID_ARGUMENT", 2: "NHA_ERR_UNSUPPORTED",
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 
 # Every symbol include/nha.h declares (checked by the tests).
-EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward", "nha_decode_step", "nha_decode_step_varlen",
+EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward",
+           "nha_workspace_bytes_ex", "nha_forward_ex", "nha_backward_ex",
+           "nha_decode_step", "nha_decode_step_varlen",
            "nha_decode_prefill",
            "nha_forward_noalloc",
            "nha_launch_count", "nha_profile_begin", "nha_profile_end", "nha_status_string", "nha_last_error")
 
 _lock = threading.Lock()
 _lib = None
+
+
+class Extras(ctypes.Structure):
+    """nha_extras_t of include/nha.h (optional inputs and outputs of the _ex calls)."""
+    _fields_ = [("fwd_workspace", ctypes.c_void_p), ("fwd_ws_bytes", ctypes.c_size_t)]
 
 
 class ProfileRecord(ctypes.Structure):
@@ -85,6 +92,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.nha_forward.argtypes = [vp] * 6 + [i] * 8 + [f, vp, sz, vp]
         lib.nha_backward.restype = i
         lib.nha_backward.argtypes = [vp] * 11 + [i] * 8 + [f, vp, sz, vp]
+        ep = ctypes.POINTER(Extras)
+        lib.nha_workspace_bytes_ex.restype = sz
+        lib.nha_workspace_bytes_ex.argtypes = [i] * 9 + [ep]
+        lib.nha_forward_ex.restype = i
+        lib.nha_forward_ex.argtypes = [vp] * 6 + [i] * 8 + [f, ep, vp, sz, vp]
+        lib.nha_backward_ex.restype = i
+        lib.nha_backward_ex.argtypes = [vp] * 11 + [i] * 8 + [f, ep, vp, sz, vp]
         lib.nha_decode_step.restype = i
         lib.nha_decode_step.argtypes = [vp] * 10 + [i] * 7 + [f, vp]
         lib.nha_decode_step_varlen.restype = i
@@ -140,8 +154,16 @@ def _check(name, t, dtype=None, shape=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
-def nha_workspace_bytes(B, H, T, d, m, w, C=64, dtype=torch.bfloat16, backward=False) -> int:
+def nha_workspace_bytes(B, H, T, d, m, w, C=64, dtype=torch.bfloat16, backward=False,
+                        reuse_forward=False) -> int:
+    """Workspace bytes of the forward (or backward); ``reuse_forward``: of a
+    backward given the forward's workspace (nha_workspace_bytes_ex)."""
     lib = load_library()
+    if reuse_forward:
+        ex = Extras()
+        ex.fwd_workspace = 16  # any non-NULL value: only its presence counts here
+        return int(lib.nha_workspace_bytes_ex(B, H, T, d, m, w, C, DTYPE[dtype], int(bool(backward)),
+                                              ctypes.byref(ex)))
     return int(lib.nha_workspace_bytes(B, H, T, d, m, w, C, DTYPE[dtype], int(bool(backward))))
 
 
@@ -200,10 +222,23 @@ def nha_forward_noalloc(q, k, v, log_alpha, w: int, C: int = 64, rope_base: floa
     return o, lse
 
 
+def _extras(fwd_workspace=None):
+    ex = Extras()
+    if fwd_workspace is not None:
+        _check("fwd_workspace", fwd_workspace)
+        ex.fwd_workspace = fwd_workspace.data_ptr()
+        ex.fwd_ws_bytes = fwd_workspace.numel() * fwd_workspace.element_size()
+    return ex
+
+
 def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
                  rope_base: float = 10000.0, dq=None, dk=None, dv=None, dlog_alpha=None,
-                 workspace=None, stream=None):
-    """dq, dk, dv, dlog_alpha = nha_backward(q, k, v, log_alpha, o, lse, dout, w)."""
+                 workspace=None, stream=None, fwd_workspace=None):
+    """dq, dk, dv, dlog_alpha = nha_backward(q, k, v, log_alpha, o, lse, dout, w).
+
+    ``fwd_workspace``: the workspace tensor the forward of these inputs ran
+    with, untouched since; the backward then reuses the chunk states and
+    rotated q, k it holds (nha_backward_ex)."""
     lib = load_library()
     B, H, T, d = q.shape
     m = log_alpha.shape[-1]
@@ -221,14 +256,15 @@ def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
     for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _check(n, t, dt, (B, H, T, d))
     _check("dlog_alpha", dlog_alpha, torch.float32, (B, H, T, m))
-    need = int(lib.nha_workspace_bytes(B, H, T, d, m, w, C, DTYPE[dt], 1))
+    ex = _extras(fwd_workspace)
+    need = int(lib.nha_workspace_bytes_ex(B, H, T, d, m, w, C, DTYPE[dt], 1, ctypes.byref(ex)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib.nha_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(lse),
-                          _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dlog_alpha),
-                          B, H, T, d, m, int(w), int(C), DTYPE[dt], float(rope_base),
-                          _ptr(workspace), ws_bytes, _stream_handle(stream))
+    rc = lib.nha_backward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(lse),
+                             _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dlog_alpha),
+                             B, H, T, d, m, int(w), int(C), DTYPE[dt], float(rope_base), ctypes.byref(ex),
+                             _ptr(workspace), ws_bytes, _stream_handle(stream))
     _raise(lib, rc)
     return dq, dk, dv, dlog_alpha
 

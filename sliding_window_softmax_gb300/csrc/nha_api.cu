@@ -60,7 +60,10 @@ nha_status_t check_shape(int B, int H, int T, int d, int m, int w, int C, nha_dt
     return NHA_OK;
 }
 
-Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward) {
+// backward && reuse: the chunk states, gate totals, RoPE table and rotated q, k
+// come from the forward's workspace, so this plan holds only the backward's own
+// buffers.
+Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward, bool reuse = false) {
     Plan p;
     memset(&p, 0, sizeof(p));
     p.d = d;
@@ -81,16 +84,18 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward) {
         return o;
     };
     const size_t BH = (size_t)sh.BH, NC = (size_t)sh.NC, Tz = (size_t)T;
-    p.SK = take(BH * NC * m * d);
-    p.SV = take(BH * NC * m * d);
-    p.SKb = take(BH * NC * m * d / 2);
-    p.SVb = take(BH * NC * m * d / 2);
-    p.G = take(BH * NC * m);
-    p.U = take(BH * NC * nha::kChunk * 64 / 2);  // chunk coefficients, bf16 [BH][NC * C][64]
-    p.TAB = take(Tz * (size_t)d);  // RoPE (cos, sin) per position and frequency
     p.STATUS = take(16);
-    p.QR = take(BH * Tz * d / 2);  // RoPE(q), bf16
-    p.KR = take(BH * Tz * d / 2);  // RoPE(k), bf16
+    if (!(backward && reuse)) {
+        p.SK = take(BH * NC * m * d);
+        p.SV = take(BH * NC * m * d);
+        p.SKb = take(BH * NC * m * d / 2);
+        p.SVb = take(BH * NC * m * d / 2);
+        p.G = take(BH * NC * m);
+        p.U = take(BH * NC * nha::kChunk * 64 / 2);  // chunk coefficients, bf16 [BH][NC * C][64]
+        p.TAB = take(Tz * (size_t)d);  // RoPE (cos, sin) per position and frequency
+        p.QR = take(BH * Tz * d / 2);  // RoPE(q), bf16
+        p.KR = take(BH * Tz * d / 2);  // RoPE(k), bf16
+    }
     if (backward) {
         p.Dv = take(BH * Tz);
         p.Dhat = take(BH * Tz);
@@ -125,6 +130,15 @@ void make_rope(nha::RopeTab& rt, int d, float base) {
 
 bool misaligned(const void* p) { return ((uintptr_t)p & 15u) != 0; }
 
+// Optional arguments of the _ex entry points: which are set, and that each
+// is valid for the call (forward or backward) it is given to.
+nha_status_t check_extras(const nha_extras_t* ex, bool backward) {
+    if (ex == nullptr) return NHA_OK;
+    if (!backward && ex->fwd_workspace != nullptr)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "fwd_workspace is an input of the backward only");
+    return NHA_OK;
+}
+
 cudaError_t run_forward_tc(const Plan& p, const nha::FwdArgs& a, float* ws, cudaStream_t s) {
     float2* tab = (float2*)(ws + p.TAB);
     int* status = (int*)(ws + p.STATUS);
@@ -154,11 +168,14 @@ cudaError_t run_forward(const Plan& p, const nha::FwdArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
 }
 
-cudaError_t run_backward_tc(const Plan& p, const nha::BwdArgs& a, float* ws, cudaStream_t s) {
-    float2* tab = (float2*)(ws + p.TAB);
+// fws, fp: the workspace and plan holding the forward's buffers (the
+// backward's own, or the forward's when they are reused)
+cudaError_t run_backward_tc(const Plan& p, const nha::BwdArgs& a, float* ws, const Plan& fp, float* fws,
+                            cudaStream_t s) {
+    float2* tab = (float2*)(fws + fp.TAB);
     int* status = (int*)(ws + p.STATUS);
-    __nv_bfloat16* qr = (__nv_bfloat16*)(ws + p.QR);
-    __nv_bfloat16* kr = (__nv_bfloat16*)(ws + p.KR);
+    __nv_bfloat16* qr = (__nv_bfloat16*)(fws + fp.QR);
+    __nv_bfloat16* kr = (__nv_bfloat16*)(fws + fp.KR);
     switch (p.d * 1000 + p.m) {
         case 64016: return nha::tc_backward<64, 16>(a, tab, qr, kr, status, s);
         case 64032: return nha::tc_backward<64, 32>(a, tab, qr, kr, status, s);
@@ -208,11 +225,37 @@ nha_status_t nha_forward(const void* q, const void* k, const void* v, const floa
                          void* o, float* lse, int B, int H, int T, int d, int m, int w, int C,
                          nha_dtype_t dtype, float rope_base, void* workspace, size_t ws_bytes,
                          void* stream) {
+    return nha_forward_ex(q, k, v, log_alpha, o, lse, B, H, T, d, m, w, C, dtype, rope_base, nullptr, workspace,
+                          ws_bytes, stream);
+}
+
+nha_status_t nha_backward(const void* q, const void* k, const void* v, const float* log_alpha,
+                          const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                          void* dv, float* dlog_alpha, int B, int H, int T, int d, int m, int w,
+                          int C, nha_dtype_t dtype, float rope_base, void* workspace,
+                          size_t ws_bytes, void* stream) {
+    return nha_backward_ex(q, k, v, log_alpha, o, lse, dout, dq, dk, dv, dlog_alpha, B, H, T, d, m, w, C, dtype,
+                           rope_base, nullptr, workspace, ws_bytes, stream);
+}
+
+size_t nha_workspace_bytes_ex(int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dtype, int backward,
+                              const nha_extras_t* ex) {
+    if (check_shape(B, H, T, d, m, w, C, dtype) != NHA_OK) return 0;
+    const bool reuse = backward && ex != nullptr && ex->fwd_workspace != nullptr;
+    Plan p = make_plan(B, H, T, d, m, w, backward != 0, reuse);
+    return p.total * sizeof(float);
+}
+
+nha_status_t nha_forward_ex(const void* q, const void* k, const void* v, const float* log_alpha, void* o,
+                            float* lse, int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dtype,
+                            float rope_base, const nha_extras_t* ex, void* workspace, size_t ws_bytes,
+                            void* stream) {
     if (inject("validate")) return fail(NHA_ERR_INTERNAL, "fault injected at validate");
     nha_status_t st = check_shape(B, H, T, d, m, w, C, dtype);
     if (st != NHA_OK) return st;
     if (!(rope_base > 1.0f) || !isfinite(rope_base))
         return fail(NHA_ERR_INVALID_ARGUMENT, "rope_base must be a finite value > 1");
+    if ((st = check_extras(ex, false)) != NHA_OK) return st;
     if ((long long)B * H * T == 0) return ok();
     const void* ptrs[] = {q, k, v, log_alpha, o, lse};
     const char* names[] = {"q", "k", "v", "log_alpha", "o", "lse"};
@@ -242,16 +285,16 @@ nha_status_t nha_forward(const void* q, const void* k, const void* v, const floa
     return ok();
 }
 
-nha_status_t nha_backward(const void* q, const void* k, const void* v, const float* log_alpha,
-                          const void* o, const float* lse, const void* dout, void* dq, void* dk,
-                          void* dv, float* dlog_alpha, int B, int H, int T, int d, int m, int w,
-                          int C, nha_dtype_t dtype, float rope_base, void* workspace,
-                          size_t ws_bytes, void* stream) {
+nha_status_t nha_backward_ex(const void* q, const void* k, const void* v, const float* log_alpha, const void* o,
+                             const float* lse, const void* dout, void* dq, void* dk, void* dv, float* dlog_alpha,
+                             int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dtype, float rope_base,
+                             const nha_extras_t* ex, void* workspace, size_t ws_bytes, void* stream) {
     if (inject("validate")) return fail(NHA_ERR_INTERNAL, "fault injected at validate");
     nha_status_t st = check_shape(B, H, T, d, m, w, C, dtype);
     if (st != NHA_OK) return st;
     if (!(rope_base > 1.0f) || !isfinite(rope_base))
         return fail(NHA_ERR_INVALID_ARGUMENT, "rope_base must be a finite value > 1");
+    if ((st = check_extras(ex, true)) != NHA_OK) return st;
     if ((long long)B * H * T == 0) return ok();
     const void* ptrs[] = {q, k, v, log_alpha, o, lse, dout, dq, dk, dv, dlog_alpha};
     const char* names[] = {"q", "k", "v", "log_alpha", "o", "lse", "dout", "dq", "dk", "dv", "dlog_alpha"};
@@ -259,32 +302,46 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
         if (ptrs[i] == nullptr) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is NULL", names[i]);
         if (misaligned(ptrs[i])) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", names[i]);
     }
-    Plan p = make_plan(B, H, T, d, m, w, true);
+    const bool reuse = ex != nullptr && ex->fwd_workspace != nullptr;
+    Plan p = make_plan(B, H, T, d, m, w, true, reuse);
     const size_t need = p.total * sizeof(float);
     if (workspace == nullptr || ws_bytes < need)
         return fail(NHA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                     workspace ? ws_bytes : (size_t)0);
     if (misaligned(workspace)) return fail(NHA_ERR_INVALID_ARGUMENT, "workspace is not 16-byte aligned");
-    if (inject("backward_launch")) return fail(NHA_ERR_INTERNAL, "fault injected at backward_launch");
+    Plan fp = p;
     float* ws = (float*)workspace;
+    float* fws = ws;
+    if (reuse) {
+        fp = make_plan(B, H, T, d, m, w, false);
+        const size_t fneed = fp.total * sizeof(float);
+        if (ex->fwd_ws_bytes < fneed)
+            return fail(NHA_ERR_WORKSPACE, "forward workspace of %zu bytes expected, %zu given", fneed,
+                        ex->fwd_ws_bytes);
+        if (misaligned(ex->fwd_workspace))
+            return fail(NHA_ERR_INVALID_ARGUMENT, "forward workspace is not 16-byte aligned");
+        fws = (float*)const_cast<void*>(ex->fwd_workspace);
+    }
+    if (inject("backward_launch")) return fail(NHA_ERR_INTERNAL, "fault injected at backward_launch");
     nha::BwdArgs a;
     a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.o = o; a.lse = lse; a.dout = dout;
     a.dq = dq; a.dk = dk; a.dv = dv; a.dla = dlog_alpha;
-    a.SK = ws + p.SK; a.SV = ws + p.SV; a.G = ws + p.G; a.Dv = ws + p.Dv;
+    a.SK = fws + fp.SK; a.SV = fws + fp.SV; a.G = fws + fp.G; a.Dv = ws + p.Dv;
     a.Dhat = ws + p.Dhat; a.Dwin = ws + p.Dwin; a.dqwV = ws + p.dqwV;
     a.dqw = ws + p.dqw; a.dkw = ws + p.dkw; a.dvw = ws + p.dvw;
     a.wsDL = ws + p.DL; a.wsPL = ws + p.PL; a.wsDB1 = ws + p.DB1;
     a.RK = ws + p.RK; a.RV = ws + p.RV;
-    a.SKb = (__nv_bfloat16*)(ws + p.SKb); a.SVb = (__nv_bfloat16*)(ws + p.SVb);
-    a.U = (__nv_bfloat16*)(ws + p.U);
+    a.SKb = (__nv_bfloat16*)(fws + fp.SKb); a.SVb = (__nv_bfloat16*)(fws + fp.SVb);
+    a.U = (__nv_bfloat16*)(fws + fp.U);
     a.RKb = (__nv_bfloat16*)(ws + p.RKb); a.RVb = (__nv_bfloat16*)(ws + p.RVb);
     a.hdqw = (__nv_bfloat16*)a.dqw; a.hdqwV = (__nv_bfloat16*)a.dqwV;
     a.hdkw = (__nv_bfloat16*)a.dkw; a.hdvw = (__nv_bfloat16*)a.dvw;
     a.hDL = (__nv_bfloat16*)a.wsDL; a.hPL = (__nv_bfloat16*)a.wsPL;
+    a.reuse = reuse;
     a.sh = p.sh;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = dtype == NHA_DTYPE_F32 ? run_backward<float>(p, a, s) : run_backward_tc(p, a, ws, s);
+    cudaError_t e = dtype == NHA_DTYPE_F32 ? run_backward<float>(p, a, s) : run_backward_tc(p, a, ws, fp, fws, s);
     if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "backward launch failed: %s", cudaGetErrorString(e));
     return ok();
 }

@@ -187,7 +187,8 @@ bwd_wdq_tc_kernel(const BwdArgs a, const __grid_constant__ WdqMaps maps, int* __
         named_sync(1, 256);  // also: every o read done before P overwrites the tile
         const float Dr = red[r] + red[128 + r];
         if (h == 0 && row_ok) a.Dhat[hoff + t] = Dr;
-        float dwin = 0.0f;
+        float2 dwin2 = make_float2(0.0f, 0.0f), dwin2b = make_float2(0.0f, 0.0f);
+        const float2 sg2 = make_float2(sig2, sig2), nl2 = make_float2(-lse2, -lse2), nD2 = make_float2(-Dr, -Dr);
         for (int i = 0; i < nb && ok; i++) {
             const int kb = klo + i * 128, nk = min(128, khi - kb + 1), b = i & 1;
             if (!(ok = mbar_wait_ab(&sfull, i & 1, kWaitCycles, abort))) break;
@@ -199,13 +200,29 @@ bwd_wdq_tc_kernel(const BwdArgs a, const __grid_constant__ WdqMaps maps, int* __
             if (lane == 0) mbar_arrive(&sfree);
             const int clo = max(0, t - sh.w + 1 - kb) - 64 * h;
             const int chi = (row_ok ? min(nk - 1, t - kb) : -1) - 64 * h;
+            if (clo <= 0 && chi >= 63) {
+                // every key of this half-row is in the band: packed pairs, no masks
 #pragma unroll
-            for (int jj = 0; jj < 64; jj++) {
-                const bool valid = jj >= clo && jj <= chi;
-                const float p = valid ? ex2(sv[jj] * sig2 - lse2) : 0.0f;
-                dwin += p * dp[jj];
-                sv[jj] = p * (dp[jj] - Dr);
-                dp[jj] = p;
+                for (int jj = 0; jj < 64; jj += 4) {
+                    const float2 s0 = __ffma2_rn(make_float2(sv[jj], sv[jj + 1]), sg2, nl2);
+                    const float2 s1 = __ffma2_rn(make_float2(sv[jj + 2], sv[jj + 3]), sg2, nl2);
+                    const float2 p0 = make_float2(ex2(s0.x), ex2(s0.y)), p1 = make_float2(ex2(s1.x), ex2(s1.y));
+                    const float2 d0 = make_float2(dp[jj], dp[jj + 1]), d1 = make_float2(dp[jj + 2], dp[jj + 3]);
+                    dwin2 = __ffma2_rn(p0, d0, dwin2);
+                    dwin2b = __ffma2_rn(p1, d1, dwin2b);
+                    const float2 g0 = __fmul2_rn(p0, __fadd2_rn(d0, nD2)), g1 = __fmul2_rn(p1, __fadd2_rn(d1, nD2));
+                    sv[jj] = g0.x; sv[jj + 1] = g0.y; sv[jj + 2] = g1.x; sv[jj + 3] = g1.y;
+                    dp[jj] = p0.x; dp[jj + 1] = p0.y; dp[jj + 2] = p1.x; dp[jj + 3] = p1.y;
+                }
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 64; jj++) {
+                    const bool valid = jj >= clo && jj <= chi;
+                    const float p = valid ? ex2(sv[jj] * sig2 - lse2) : 0.0f;
+                    dwin2.x += p * dp[jj];
+                    sv[jj] = p * (dp[jj] - Dr);
+                    dp[jj] = p;
+                }
             }
             // P of block i - 1 no longer read by the tensor core
             if (i >= 1 && !(ok = mbar_wait_ab(&bdone[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitCycles, abort))) break;
@@ -216,6 +233,7 @@ bwd_wdq_tc_kernel(const BwdArgs a, const __grid_constant__ WdqMaps maps, int* __
             __syncwarp();
             if (lane == 0) mbar_arrive(&pready);
         }
+        const float dwin = (dwin2.x + dwin2.y) + (dwin2b.x + dwin2b.y);
         named_sync(1, 256);
         red[h * 128 + r] = dwin;
         named_sync(1, 256);
@@ -461,12 +479,33 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, int* __
             const int chi = (row_ok ? min(nq - 1, key + sh.w - 1 - qb) : -1) - 32 * h;
             const float* l2 = sL + stg * 64 + 32 * h;
             const float* dd = sD + stg * 64 + 32 * h;
+            if (clo <= 0 && chi >= 31) {
+                // every query of this half-row sees the key: packed pairs, no masks
+                const float2 sg2 = make_float2(sig2, sig2), nlg = make_float2(-kLog2e, -kLog2e);
 #pragma unroll
-            for (int jj = 0; jj < 32; jj++) {
-                const bool valid = jj >= clo && jj <= chi;
-                const float p = valid ? ex2(sv[jj] * sig2 - l2[jj] * kLog2e) : 0.0f;
-                sv[jj] = p;
-                dp[jj] = valid ? p * (dp[jj] - dd[jj]) : 0.0f;
+                for (int jj = 0; jj < 32; jj += 4) {
+                    const float4 L4 = *reinterpret_cast<const float4*>(l2 + jj);
+                    const float4 D4 = *reinterpret_cast<const float4*>(dd + jj);
+                    const float2 s0 = __ffma2_rn(make_float2(sv[jj], sv[jj + 1]), sg2,
+                                                 __fmul2_rn(make_float2(L4.x, L4.y), nlg));
+                    const float2 s1 = __ffma2_rn(make_float2(sv[jj + 2], sv[jj + 3]), sg2,
+                                                 __fmul2_rn(make_float2(L4.z, L4.w), nlg));
+                    const float2 p0 = make_float2(ex2(s0.x), ex2(s0.y)), p1 = make_float2(ex2(s1.x), ex2(s1.y));
+                    const float2 g0 = __fmul2_rn(p0, __fadd2_rn(make_float2(dp[jj], dp[jj + 1]),
+                                                                make_float2(-D4.x, -D4.y)));
+                    const float2 g1 = __fmul2_rn(p1, __fadd2_rn(make_float2(dp[jj + 2], dp[jj + 3]),
+                                                                make_float2(-D4.z, -D4.w)));
+                    sv[jj] = p0.x; sv[jj + 1] = p0.y; sv[jj + 2] = p1.x; sv[jj + 3] = p1.y;
+                    dp[jj] = g0.x; dp[jj + 1] = g0.y; dp[jj + 2] = g1.x; dp[jj + 3] = g1.y;
+                }
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 32; jj++) {
+                    const bool valid = jj >= clo && jj <= chi;
+                    const float p = valid ? ex2(sv[jj] * sig2 - l2[jj] * kLog2e) : 0.0f;
+                    sv[jj] = p;
+                    dp[jj] = valid ? p * (dp[jj] - dd[jj]) : 0.0f;
+                }
             }
             // P^T, dS^T of block i - 1 no longer read by the tensor core
             if (i >= 1 && !(ok = mbar_wait_ab(&bdone[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitCycles, abort))) break;
@@ -577,15 +616,18 @@ cudaError_t tc_backward(const BwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_b
     cudaError_t e = get_fork(&f);
     if (e != cudaSuccess) return e;
     // RoPE(q), RoPE(k) and the (cos, sin) table of the window kernels'
-    // epilogues on the side stream while the chunk states are formed
-    if (sh.w > 0) {
-        if ((e = fork_side(st, *f, 0)) != cudaSuccess) return e;
-        if ((e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, a.rope, sh, f->side)) != cudaSuccess) return e;
+    // epilogues on the side stream while the chunk states are formed (unless
+    // the forward's are reused)
+    if (!a.reuse) {
+        if (sh.w > 0) {
+            if ((e = fork_side(st, *f, 0)) != cudaSuccess) return e;
+            if ((e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, a.rope, sh, f->side)) != cudaSuccess) return e;
+        }
+        e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV, a.SKb, a.SVb,
+                            a.G, a.U, false, sh, status, st);
+        if (e != cudaSuccess) return e;
+        if (sh.w > 0 && (e = join_side(st, *f, 1)) != cudaSuccess) return e;
     }
-    e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV, a.SKb, a.SVb, a.G,
-                        a.U, false, sh, status, st);
-    if (e != cudaSuccess) return e;
-    if (sh.w > 0 && (e = join_side(st, *f, 1)) != cudaSuccess) return e;
     const dim3 grid((sh.T + 127) / 128, sh.BH);
     {
         WdqMaps maps;

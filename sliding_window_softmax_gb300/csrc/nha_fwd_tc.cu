@@ -314,10 +314,24 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
             // valid keys of this row: columns [clo, chi] of the block
             const int clo = max(0, t - sh.w + 1 - kb) - 64 * h;
             const int chi = (row_ok ? min(nk - 1, t - kb) : -1) - 64 * h;
+            const bool full = clo <= 0 && chi >= 63;  // the whole half-row is in the band
+            if (full) {
+                // raw scores: max first (sig2 > 0 keeps the order), scaled in the exponent below
+                float m0 = sv[0], m1 = sv[1], m2 = sv[2], m3 = sv[3];
 #pragma unroll
-            for (int jj = 0; jj < 64; jj++) {
-                sv[jj] = (jj >= clo && jj <= chi) ? sv[jj] * sig2 : -INFINITY;
-                bm = fmaxf(bm, sv[jj]);
+                for (int jj = 4; jj < 64; jj += 4) {
+                    m0 = fmaxf(m0, sv[jj]);
+                    m1 = fmaxf(m1, sv[jj + 1]);
+                    m2 = fmaxf(m2, sv[jj + 2]);
+                    m3 = fmaxf(m3, sv[jj + 3]);
+                }
+                bm = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sig2;
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 64; jj++) {
+                    sv[jj] = (jj >= clo && jj <= chi) ? sv[jj] * sig2 : -INFINITY;
+                    bm = fmaxf(bm, sv[jj]);
+                }
             }
             // P V of block i - 1 done: its accumulator may be rescaled below
             if (i >= 1 && !(ok = mbar_wait_ab(&bdone[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitCycles, abort))) break;
@@ -344,11 +358,26 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
                 }
             }
             float ps = 0.0f;
+            if (full) {  // m is finite here: the half-row has at least one key
+                const float2 sg2 = make_float2(sig2, sig2), nm2 = make_float2(-m, -m);
+                float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int jj = 0; jj < 64; jj++) {
-                const float p = (m == -INFINITY) ? 0.0f : ex2(sv[jj] - m);
-                sv[jj] = p;
-                ps += p;
+                for (int jj = 0; jj < 64; jj += 4) {
+                    const float2 s0 = __ffma2_rn(make_float2(sv[jj], sv[jj + 1]), sg2, nm2);
+                    const float2 s1 = __ffma2_rn(make_float2(sv[jj + 2], sv[jj + 3]), sg2, nm2);
+                    const float2 p0 = make_float2(ex2(s0.x), ex2(s0.y)), p1 = make_float2(ex2(s1.x), ex2(s1.y));
+                    a0 = __fadd2_rn(a0, p0);
+                    a1 = __fadd2_rn(a1, p1);
+                    sv[jj] = p0.x; sv[jj + 1] = p0.y; sv[jj + 2] = p1.x; sv[jj + 3] = p1.y;
+                }
+                ps = (a0.x + a0.y) + (a1.x + a1.y);
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 64; jj++) {
+                    const float p = (m == -INFINITY) ? 0.0f : ex2(sv[jj] - m);
+                    sv[jj] = p;
+                    ps += p;
+                }
             }
             l += ps;
             store_row(KB[stg], r, 64 * h, sv, 64);  // P over the consumed K~ block
@@ -512,10 +541,11 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bf
     Fork* f = nullptr;
     cudaError_t e = get_fork(&f);
     if (e != cudaSuccess) return e;
-    // RoPE(q), RoPE(k) on the side stream while the chunk states are formed
+    // RoPE(q), RoPE(k) on the side stream while the chunk states are formed;
+    // the (cos, sin) table too, for a backward that reuses this workspace
     if (sh.w > 0) {
         if ((e = fork_side(st, *f, 0)) != cudaSuccess) return e;
-        if ((e = launch_rope_qk<D>(a.q, a.k, qr, kr, nullptr, a.rope, sh, f->side)) != cudaSuccess) return e;
+        if ((e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, a.rope, sh, f->side)) != cudaSuccess) return e;
     }
     e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV, a.SKb, a.SVb, a.G,
                         a.U, false, sh, status, st);

@@ -88,6 +88,9 @@ struct BwdArgs {
     __nv_bfloat16* hdvw;
     __nv_bfloat16* hDL;
     __nv_bfloat16* hPL;
+    // the chunk states, gate totals, RoPE table and RoPE(q), RoPE(k) above are
+    // the forward's, left in its workspace: the backward does not recompute them
+    bool reuse;
     Shape sh;
     RopeTab rope;
 };

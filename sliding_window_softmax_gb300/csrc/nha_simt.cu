@@ -809,7 +809,7 @@ template <typename Tin, int D, int M>
 cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st) {
     const Shape& sh = a.sh;
     constexpr int LX = D + 1, LP = kChunk + 1;
-    NHA_CHECK(simt_states<Tin, D, M>((const Tin*)a.k, (const Tin*)a.v, a.la, a.SK, a.SV, a.G, sh, st));
+    if (!a.reuse) NHA_CHECK(simt_states<Tin, D, M>((const Tin*)a.k, (const Tin*)a.v, a.la, a.SK, a.SV, a.G, sh, st));
     const long rows = (long)sh.BH * sh.T;
     NHA_LAUNCH("bwd_rowdot", st,
                bwd_rowdot_kernel<Tin, D><<<(unsigned)((rows + 7) / 8), kThreads, 0, st>>>(

@@ -245,3 +245,30 @@ def test_public_header_is_plain_c_and_links_against_the_library(lib, tmp_path):
     r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic", f"-I{os.path.join(ROOT, 'include')}",
                         str(src), "-o", str(exe), f"-L{libdir}", "-l:libnha.so"], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_extended_calls_validate_their_extras(lib):
+    ex = _binding.Extras()
+    f = lib.nha_workspace_bytes_ex
+    full = lib.nha_workspace_bytes(1, 2, 256, 64, 16, 32, 64, 1, 1)
+    # without extras the _ex sizes are the plain ones
+    assert f(1, 2, 256, 64, 16, 32, 64, 1, 1, None) == full
+    assert f(1, 2, 256, 64, 16, 32, 64, 1, 1, ctypes.byref(ex)) == full
+    ex.fwd_workspace = 4096
+    own = f(1, 2, 256, 64, 16, 32, 64, 1, 1, ctypes.byref(ex))
+    assert 0 < own < full
+    p = ctypes.c_void_p(4096)
+    fwd_need = lib.nha_workspace_bytes(1, 2, 256, 64, 16, 32, 64, 1, 0)
+    # the forward takes no forward workspace
+    rc = lib.nha_forward_ex(p, p, p, p, p, p, 1, 2, 256, 64, 16, 32, 64, 1, 10000.0, ctypes.byref(ex), p,
+                            1 << 30, None)
+    assert rc == 1 and b"backward only" in lib.nha_last_error()
+    # a forward workspace smaller than the forward's plan is refused
+    ex.fwd_ws_bytes = fwd_need - 256
+    rc = lib.nha_backward_ex(p, p, p, p, p, p, p, p, p, p, p, 1, 2, 256, 64, 16, 32, 64, 1, 10000.0,
+                             ctypes.byref(ex), p, own, None)
+    assert rc == 3 and b"forward workspace" in lib.nha_last_error()
+    # the backward's own workspace may be the smaller size
+    rc = lib.nha_backward_ex(p, p, p, p, p, p, p, p, p, p, p, 1, 2, 256, 64, 16, 32, 64, 1, 10000.0,
+                             ctypes.byref(ex), p, own - 256, None)
+    assert rc == 3
