@@ -55,10 +55,11 @@ def _load():
             L = ctypes.c_long
             lib.nha_oracle_forward.restype = ctypes.c_int
             lib.nha_oracle_forward.argtypes = [dp, dp, dp, dp, dp, dp, dp, L, L, L, L, L, L,
-                                               ctypes.c_double, ctypes.c_int, dp, dp]
+                                               ctypes.c_double, ctypes.c_int, dp, dp, dp, dp]
             lib.nha_oracle_backward.restype = ctypes.c_int
             lib.nha_oracle_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, L, L, L, L,
-                                                L, L, ctypes.c_double, ctypes.c_int, dp, dp, dp, dp]
+                                                L, L, ctypes.c_double, ctypes.c_int, dp, dp, dp, dp,
+                                                dp, dp]
             lib.nha_oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -96,8 +97,11 @@ def _h0(h0, B, H, m, d):
 
 
 def forward(q, k, v, log_alpha, w: int, rope_base: float = 10000.0, nthreads: int = 0,
-            with_omega: bool = False, h0=None):
-    """fp64 NHA forward.  Returns (o, lse) or (o, lse, omega_L).
+            with_omega: bool = False, h0=None, return_state: bool = False):
+    """fp64 NHA forward.  Returns (o, lse) or (o, lse, omega_L); with
+    ``return_state`` the tuple ends with (hTk, hTv), each [B,H,m,d]: the final
+    slot states, the long memory after the last token that left the window
+    (token T - w - 1), h0 (or zero) when no token has.
 
     h0 = (h0k, h0v), each [B,H,m,d]: initial slot states (the long memory before
     token 0); with them no slot logit is masked."""
@@ -109,22 +113,28 @@ def forward(q, k, v, log_alpha, w: int, rope_base: float = 10000.0, nthreads: in
     o = np.zeros_like(q)
     lse = np.zeros((B, H, T), dtype=np.float64)
     om = np.zeros((B, H, T), dtype=np.float64)
+    hTk = np.zeros((B, H, m, d)) if return_state else None
+    hTv = np.zeros((B, H, m, d)) if return_state else None
     rc = _load().nha_oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(o), _ptr(lse),
                                     _ptr(om), B, H, T, d, m, int(w), float(rope_base),
-                                    int(nthreads), _ptr_or_null(hk), _ptr_or_null(hv))
+                                    int(nthreads), _ptr_or_null(hk), _ptr_or_null(hv),
+                                    _ptr_or_null(hTk), _ptr_or_null(hTv))
     if rc != 0:
         raise ValueError(f"oracle forward rejected the shape (rc={rc})")
-    return (o, lse, om) if with_omega else (o, lse)
+    out = (o, lse, om) if with_omega else (o, lse)
+    return out + (hTk, hTv) if return_state else out
 
 
 def backward(q, k, v, log_alpha, dout, w: int, rope_base: float = 10000.0, nthreads: int = 0,
-             h0=None):
-    """fp64 NHA backward of loss = sum(o * dout).  Returns (dq, dk, dv, dlog_alpha),
-    and with h0 = (h0k, h0v) also (dh0k, dh0v)."""
+             h0=None, dhT=None):
+    """fp64 NHA backward of loss = sum(o * dout) (+ <hTk, dhTk> + <hTv, dhTv> with
+    dhT = (dhTk, dhTv), the gradient with respect to the final states).  Returns
+    (dq, dk, dv, dlog_alpha), and with h0 = (h0k, h0v) also (dh0k, dh0v)."""
     q, k, v, la, g = _f64(q), _f64(k), _f64(v), _f64(log_alpha), _f64(dout)
     B, H, T, d = q.shape
     m = la.shape[-1]
     hk, hv = _h0(h0, B, H, m, d)
+    gk, gv = _h0(dhT, B, H, m, d)
     dq, dk, dv = np.zeros_like(q), np.zeros_like(q), np.zeros_like(q)
     dla = np.zeros_like(la)
     dhk = np.zeros((B, H, m, d)) if hk is not None else None
@@ -132,7 +142,8 @@ def backward(q, k, v, log_alpha, dout, w: int, rope_base: float = 10000.0, nthre
     rc = _load().nha_oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(g), _ptr(dq),
                                      _ptr(dk), _ptr(dv), _ptr(dla), B, H, T, d, m, int(w),
                                      float(rope_base), int(nthreads), _ptr_or_null(hk),
-                                     _ptr_or_null(hv), _ptr_or_null(dhk), _ptr_or_null(dhv))
+                                     _ptr_or_null(hv), _ptr_or_null(dhk), _ptr_or_null(dhv),
+                                     _ptr_or_null(gk), _ptr_or_null(gv))
     if rc != 0:
         raise ValueError(f"oracle backward rejected the shape (rc={rc})")
     return (dq, dk, dv, dla) if hk is None else (dq, dk, dv, dla, dhk, dhv)

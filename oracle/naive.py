@@ -96,11 +96,30 @@ def nha_naive(q, k, v, log_alpha, w: int, rope_base: float = 10000.0, return_ome
     return o, lse
 
 
-def nha_naive_grads(q, k, v, log_alpha, dout, w: int, rope_base: float = 10000.0, h0k=None, h0v=None):
-    """Autograd gradients of sum(o * dout): (dq, dk, dv, dlog_alpha[, dh0k, dh0v]), float64."""
+def final_states(k, v, log_alpha, w: int, h0k=None, h0v=None):
+    """(hTk, hTv) [B,H,m,d]: the long memory after the last token that left the
+    window, token T - w - 1 (the closed-form state there; h0, or zero, when no
+    token has left)."""
+    B, H, T, d = k.shape
+    m = log_alpha.shape[-1]
+    R = T - min(int(w), T)
+    if R == 0:
+        z = torch.zeros(B, H, m, d, dtype=k.dtype)
+        return (z if h0k is None else h0k), (z if h0v is None else h0v)
+    return (slot_states(k, log_alpha, h0k)[:, :, R - 1], slot_states(v, log_alpha, h0v)[:, :, R - 1])
+
+
+def nha_naive_grads(q, k, v, log_alpha, dout, w: int, rope_base: float = 10000.0, h0k=None, h0v=None,
+                    dhTk=None, dhTv=None):
+    """Autograd gradients of sum(o * dout) (+ <hT, dhT> when dhTk, dhTv are given):
+    (dq, dk, dv, dlog_alpha[, dh0k, dh0v]), float64."""
     inputs = (q, k, v, log_alpha) + ((h0k, h0v) if h0k is not None else ())
     leaves = [x.detach().clone().to(torch.float64).requires_grad_(True) for x in inputs]
     h0 = dict(h0k=leaves[4], h0v=leaves[5]) if h0k is not None else {}
     o, _ = nha_naive(*leaves[:4], w=w, rope_base=rope_base, **h0)
-    (o * dout.to(torch.float64)).sum().backward()
-    return tuple(x.grad for x in leaves)
+    loss = (o * dout.to(torch.float64)).sum()
+    if dhTk is not None:
+        hk, hv = final_states(leaves[1], leaves[2], leaves[3], w, **h0)
+        loss = loss + (hk * dhTk.to(torch.float64)).sum() + (hv * dhTv.to(torch.float64)).sum()
+    loss.backward()
+    return tuple(x.grad if x.grad is not None else torch.zeros_like(x) for x in leaves)

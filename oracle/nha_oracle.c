@@ -144,10 +144,14 @@ static long window_lo(long t, long w) {
     return lo < 0 ? 0 : lo;
 }
 
-/* One (b,h) head, forward.  h0k, h0v: initial states [m][d] or NULL. */
+/* One (b,h) head, forward.  h0k, h0v: initial states [m][d] or NULL; hTk,
+ * hTv: [m][d] outputs (or NULL) for the final states, the long memory after the
+ * last token that left the window (token T - w - 1; h0, or zero, when none
+ * has). */
 static void head_forward(const shape_t* sh, const double* q, const double* k, const double* v,
                          const double* la, double* o, double* lse, double* omega,
-                         const double* cs, const double* sn, const double* h0k, const double* h0v) {
+                         const double* cs, const double* sn, const double* h0k, const double* h0v,
+                         double* hTk, double* hTv) {
     long T = sh->T, d = sh->d, m = sh->m, w = sh->w, h = d / 2;
     double* SK = calloc((size_t)(m * d), sizeof(double));
     double* SV = calloc((size_t)(m * d), sizeof(double));
@@ -185,16 +189,21 @@ static void head_forward(const shape_t* sh, const double* q, const double* k, co
         }
         if (omega) omega[t] = wl;
     }
+    if (hTk) memcpy(hTk, SK, sizeof(double) * (size_t)(m * d));
+    if (hTv) memcpy(hTv, SV, sizeof(double) * (size_t)(m * d));
     free(SK); free(SV); free(kr); free(qr); free(L); free(Sw);
 }
 
 /* One (b,h) head, backward (reverse sweep with state adjoints).  h0k, h0v:
  * initial states or NULL; dh0k, dh0v (written when h0k is given): their
- * gradients. */
+ * gradients.  dhTk, dhTv: [m][d] or NULL: the gradient of the loss with
+ * respect to the final states (the loss is then sum(o * dout) + <hT, dhT>);
+ * it is the state adjoint the reverse sweep starts from. */
 static void head_backward(const shape_t* sh, const double* q, const double* k, const double* v,
                           const double* la, const double* dout, double* dq, double* dk,
                           double* dv, double* dla, const double* cs, const double* sn,
-                          const double* h0k, const double* h0v, double* dh0k, double* dh0v) {
+                          const double* h0k, const double* h0v, double* dh0k, double* dh0v,
+                          const double* dhTk, const double* dhTv) {
     long T = sh->T, d = sh->d, m = sh->m, w = sh->w, h = d / 2;
     long md = m * d;
     double sigma = 1.0 / sqrt((double)d);
@@ -217,6 +226,8 @@ static void head_backward(const shape_t* sh, const double* q, const double* k, c
     double* segV = malloc(sizeof(double) * (size_t)((CKPT + 1) * md));
     double* dSK = calloc((size_t)md, sizeof(double));
     double* dSV = calloc((size_t)md, sizeof(double));
+    if (dhTk) memcpy(dSK, dhTk, sizeof(double) * (size_t)md);
+    if (dhTv) memcpy(dSV, dhTv, sizeof(double) * (size_t)md);
 
     memset(dq, 0, sizeof(double) * (size_t)(T * d));
     memset(dk, 0, sizeof(double) * (size_t)(T * d));
@@ -351,12 +362,21 @@ static int check_shape(long B, long H, long T, long d, long m, long w) {
 /* o[B,H,T,d], lse[B,H,T], omega[B,H,T] (optional, may be NULL): the share of
  * softmax mass on the long-memory slots (the omega_L diagnostic of the same
  * section). */
-/* h0k, h0v [B,H,m,d]: optional initial slot states (both or neither). */
+/* h0k, h0v [B,H,m,d]: optional initial slot states (both or neither); hTk,
+ * hTv [B,H,m,d]: optional final states (both or neither). */
 int nha_oracle_forward(const double* q, const double* k, const double* v, const double* log_alpha,
                        double* o, double* lse, double* omega, long B, long H, long T, long d,
                        long m, long w, double rope_base, int nthreads, const double* h0k,
-                       const double* h0v) {
+                       const double* h0v, double* hTk, double* hTv) {
     if ((h0k == NULL) != (h0v == NULL)) return -1;
+    if ((hTk == NULL) != (hTv == NULL)) return -1;
+    if (hTk && B * H > 0 && (T == 0 || w >= T)) {
+        /* no token leaves the window: the final states are the initial ones */
+        for (long e = 0; e < B * H * m * d; e++) {
+            hTk[e] = h0k ? h0k[e] : 0.0;
+            hTv[e] = h0v ? h0v[e] : 0.0;
+        }
+    }
     if (check_shape(B, H, T, d, m, w)) return -1;
     if (T == 0 || B * H == 0) return 0;
     shape_t sh = {T, d, m, w > T ? T : w, rope_base};
@@ -372,7 +392,8 @@ int nha_oracle_forward(const double* q, const double* k, const double* v, const 
     for (long bh = 0; bh < nbh; bh++) {
         head_forward(&sh, q + bh * T * d, k + bh * T * d, v + bh * T * d, log_alpha + bh * T * m,
                      o + bh * T * d, lse + bh * T, omega ? omega + bh * T : NULL, cs, sn,
-                     h0k ? h0k + bh * m * d : NULL, h0v ? h0v + bh * m * d : NULL);
+                     h0k ? h0k + bh * m * d : NULL, h0v ? h0v + bh * m * d : NULL,
+                     hTk ? hTk + bh * m * d : NULL, hTv ? hTv + bh * m * d : NULL);
     }
     (void)nthreads;
     free(cs); free(sn);
@@ -380,15 +401,23 @@ int nha_oracle_forward(const double* q, const double* k, const double* v, const 
 }
 
 /* h0k, h0v [B,H,m,d]: optional initial slot states; dh0k, dh0v [B,H,m,d]
- * receive their gradients (all four given, or none). */
+ * receive their gradients (all four given, or none).  dhTk, dhTv [B,H,m,d]:
+ * optional gradient with respect to the final states (both or neither). */
 int nha_oracle_backward(const double* q, const double* k, const double* v, const double* log_alpha,
                         const double* dout, double* dq, double* dk, double* dv, double* dlog_alpha,
                         long B, long H, long T, long d, long m, long w, double rope_base,
                         int nthreads, const double* h0k, const double* h0v, double* dh0k,
-                        double* dh0v) {
+                        double* dh0v, const double* dhTk, const double* dhTv) {
     int given = (h0k != NULL) + (h0v != NULL) + (dh0k != NULL) + (dh0v != NULL);
     if (given != 0 && given != 4) return -1;
+    if ((dhTk == NULL) != (dhTv == NULL)) return -1;
     if (check_shape(B, H, T, d, m, w)) return -1;
+    if (B * H > 0 && T == 0 && dh0k) {  /* no query: the final states are the initial ones */
+        for (long e = 0; e < B * H * m * d; e++) {
+            dh0k[e] = dhTk ? dhTk[e] : 0.0;
+            dh0v[e] = dhTv ? dhTv[e] : 0.0;
+        }
+    }
     if (T == 0 || B * H == 0) return 0;
     shape_t sh = {T, d, m, w > T ? T : w, rope_base};
     long h = d / 2;
@@ -405,7 +434,8 @@ int nha_oracle_backward(const double* q, const double* k, const double* v, const
                       dout + bh * T * d, dq + bh * T * d, dk + bh * T * d, dv + bh * T * d,
                       dlog_alpha + bh * T * m, cs, sn, h0k ? h0k + bh * m * d : NULL,
                       h0v ? h0v + bh * m * d : NULL, dh0k ? dh0k + bh * m * d : NULL,
-                      dh0v ? dh0v + bh * m * d : NULL);
+                      dh0v ? dh0v + bh * m * d : NULL, dhTk ? dhTk + bh * m * d : NULL,
+                      dhTv ? dhTv + bh * m * d : NULL);
     }
     (void)nthreads;
     free(cs); free(sn);

@@ -108,3 +108,96 @@ def test_zero_h0_adds_zero_keys_before_the_window_fills():
     Z = np.exp(lse0[:, :, :w])
     assert np.abs(lsez[:, :, :w] - np.log(Z + m)).max() <= 1e-12
     assert np.abs(oz[:, :, :w] - o0[:, :, :w] * (Z / (Z + m))[..., None]).max() <= 1e-12
+
+
+# ------------------------------------------------------------------------------------------
+# Final states hT (the long memory after token T - w - 1) and their gradient dhT.
+@pytest.mark.parametrize("w,with_h0", [(0, False), (4, True), (7, False), (17, True), (30, True)])
+def test_final_states_equal_the_decode_restatement_and_closed_form(w, with_h0):
+    from oracle.naive import final_states
+
+    T = 17
+    q, k, v, la, h0k, h0v, _ = _inputs(1, 2, T, 8, 3, seed=200 + w)
+    h0 = (h0k, h0v) if with_h0 else None
+    _, _, hTk, hTv = oracle.forward(q, k, v, la, w, h0=h0, return_state=True)
+    # the decode restatement, run over every token, holds the same long memory
+    st = DecodeState(1, 2, 8, 3, w, init=(h0k.numpy(), h0v.numpy()) if with_h0 else None)
+    for t in range(T):
+        decode_step(st, q[:, :, t].numpy(), k[:, :, t].numpy(), v[:, :, t].numpy(), la[:, :, t].numpy(), t)
+    assert np.abs(hTk - st.S_k).max() <= 1e-12 and np.abs(hTv - st.S_v).max() <= 1e-12
+    rk, rv = final_states(k, v, la, w, h0k=h0k if with_h0 else None, h0v=h0v if with_h0 else None)
+    assert np.abs(hTk - rk.numpy()).max() <= 1e-12 and np.abs(hTv - rv.numpy()).max() <= 1e-12
+
+
+@pytest.mark.parametrize("w,with_h0", [(0, False), (3, True), (5, False), (12, True), (20, True)])
+def test_final_state_gradient_equals_autograd(w, with_h0):
+    q, k, v, la, h0k, h0v, dout = _inputs(1, 2, 12, 6, 2, seed=300 + w)
+    g = torch.Generator().manual_seed(301 + w)
+    dhk = torch.randn(1, 2, 2, 6, generator=g, dtype=torch.float64)
+    dhv = torch.randn(1, 2, 2, 6, generator=g, dtype=torch.float64)
+    h0 = (h0k, h0v) if with_h0 else None
+    got = oracle.backward(q, k, v, la, dout, w, h0=h0, dhT=(dhk, dhv))
+    kw = dict(h0k=h0k, h0v=h0v) if with_h0 else {}
+    ref = nha_naive_grads(q, k, v, la, dout, w, dhTk=dhk, dhTv=dhv, **kw)
+    assert len(got) == len(ref)
+    for name, a, b in zip(("dq", "dk", "dv", "dla", "dh0k", "dh0v"), got, ref):
+        b = b.numpy()
+        assert np.linalg.norm(a - b) <= 1e-10 * max(np.linalg.norm(b), 1e-30), name
+
+
+def test_final_state_gradient_by_finite_differences():
+    q, k, v, la, h0k, h0v, dout = _inputs(1, 1, 11, 4, 2, seed=401)
+    w = 3
+    g = torch.Generator().manual_seed(402)
+    dhk = torch.randn(1, 1, 2, 4, generator=g, dtype=torch.float64).numpy()
+    dhv = torch.randn(1, 1, 2, 4, generator=g, dtype=torch.float64).numpy()
+    _, dk, _, dla, dh0k, _ = oracle.backward(q, k, v, la, dout, w, h0=(h0k, h0v), dhT=(dhk, dhv))
+
+    def loss(kk, ll, hk):
+        o, _, tk, tv = oracle.forward(q, kk, v, ll, w, h0=(hk, h0v), return_state=True)
+        return float((o * dout.numpy()).sum() + (tk * dhk).sum() + (tv * dhv).sum())
+
+    eps = 1e-6
+    for idx in [(0, 0, 2, 1), (0, 0, 7, 0)]:  # a key that leaves the window, one still in it
+        kp, km = k.clone(), k.clone()
+        kp[idx] += eps
+        km[idx] -= eps
+        fd = (loss(kp, la, h0k) - loss(km, la, h0k)) / (2 * eps)
+        assert abs(fd - dk[idx]) <= 1e-6 * max(1.0, abs(fd))
+    for idx in [(0, 0, 1, 0), (0, 0, 6, 1)]:
+        lp, lm = la.clone(), la.clone()
+        lp[idx] += eps
+        lm[idx] -= eps
+        fd = (loss(k, lp, h0k) - loss(k, lm, h0k)) / (2 * eps)
+        assert abs(fd - dla[idx]) <= 1e-6 * max(1.0, abs(fd))
+    for idx in [(0, 0, 0, 0), (0, 0, 1, 3)]:
+        hp, hm = h0k.clone(), h0k.clone()
+        hp[idx] += eps
+        hm[idx] -= eps
+        fd = (loss(k, la, hp) - loss(k, la, hm)) / (2 * eps)
+        assert abs(fd - dh0k[idx]) <= 1e-6 * max(1.0, abs(fd))
+
+
+def test_segments_chained_through_final_states_reproduce_the_sequence():
+    """A sequence cut into segments: each later segment runs on [the previous w
+    tokens; its own tokens] from the previous segment's final state (the long
+    memory after the token that left the window before the segment's halo;
+    the halo's own queries read it and are dropped); the segment outputs after
+    the halo are the full sequence's, and the last segment's final state is
+    the full sequence's."""
+    T, w = 40, 6
+    q, k, v, la, _, _, _ = _inputs(1, 2, T, 8, 3, seed=501)
+    o_all, lse_all, hk_all, hv_all = oracle.forward(q, k, v, la, w, return_state=True)
+    # RoPE window logits depend on t - s only, so each segment may use its own positions
+    cuts = [0, 13, 13 + 15, T]
+    state = None  # the first segment starts the sequence: no initial state, slots masked
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        lo = max(0, a - w)
+        sl = slice(lo, b)
+        o, lse, hk, hv = oracle.forward(q[:, :, sl], k[:, :, sl], v[:, :, sl], la[:, :, sl], w, h0=state,
+                                        return_state=True)
+        keep = a - lo
+        assert np.abs(o[:, :, keep:] - o_all[:, :, a:b]).max() <= 1e-10
+        assert np.abs(lse[:, :, keep:] - lse_all[:, :, a:b]).max() <= 1e-10
+        state = (hk, hv)
+    assert np.abs(state[0] - hk_all).max() <= 1e-12 and np.abs(state[1] - hv_all).max() <= 1e-12
