@@ -115,10 +115,37 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
  * forming them again, and its own workspace shrinks accordingly
  * (nha_workspace_bytes_ex with the same extras).  This is the usual
  * saved-for-backward context of a training step: keep the forward's
- * workspace alive until the backward has been enqueued after it. */
+ * workspace alive until the backward has been enqueued after it.
+ *
+ * Slot states (fp32 [B, H, m, d] each, K and V parts given together):
+ *   h0_k, h0_v   initial states: the long memory before token 0 (the ai.info
+ *                page, Future Directions: learned initial slot states).  The
+ *                memory is then never empty: no slot logit is masked, and the
+ *                queries t < w read h0 itself (no gate applies to it before
+ *                token 0).  Forward and backward take the same h0.
+ *   hT_k, hT_v   forward output: the final states, the long memory after the
+ *                last token that left the window (token T - w - 1), i.e. the
+ *                state nha_decode_step continues from at t = T; h0 (or zero)
+ *                when w >= T.  A sequence cut into segments continues exactly
+ *                when each later segment runs on [the previous w tokens; its
+ *                own tokens] with the previous segment's hT as h0 and drops
+ *                the outputs of those first w queries (window logits depend
+ *                on positions only through t - s, so each segment may count
+ *                positions from its own start).
+ *   dhT_k, dhT_v backward input: the gradient of the loss with respect to hT
+ *                (the loss is then <o, dout> + <hT, dhT>).
+ *   dh0_k, dh0_v backward output: the gradient with respect to h0 (needs h0). */
 typedef struct {
     const void* fwd_workspace; /* backward: the forward's workspace, read only */
     size_t fwd_ws_bytes;       /* its size in bytes */
+    const float* h0_k;
+    const float* h0_v;
+    float* hT_k;
+    float* hT_v;
+    const float* dhT_k;
+    const float* dhT_v;
+    float* dh0_k;
+    float* dh0_v;
 } nha_extras_t;
 
 /* Workspace bytes of nha_forward_ex (backward = 0) / nha_backward_ex

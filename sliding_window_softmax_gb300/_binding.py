@@ -38,7 +38,11 @@ _lib = None
 
 class Extras(ctypes.Structure):
     """nha_extras_t of include/nha.h (optional inputs and outputs of the _ex calls)."""
-    _fields_ = [("fwd_workspace", ctypes.c_void_p), ("fwd_ws_bytes", ctypes.c_size_t)]
+    _fields_ = [("fwd_workspace", ctypes.c_void_p), ("fwd_ws_bytes", ctypes.c_size_t),
+                ("h0_k", ctypes.c_void_p), ("h0_v", ctypes.c_void_p),
+                ("hT_k", ctypes.c_void_p), ("hT_v", ctypes.c_void_p),
+                ("dhT_k", ctypes.c_void_p), ("dhT_v", ctypes.c_void_p),
+                ("dh0_k", ctypes.c_void_p), ("dh0_v", ctypes.c_void_p)]
 
 
 class ProfileRecord(ctypes.Structure):
@@ -168,8 +172,12 @@ def nha_workspace_bytes(B, H, T, d, m, w, C=64, dtype=torch.bfloat16, backward=F
 
 
 def nha_forward(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 10000.0,
-                o=None, lse=None, workspace=None, stream=None):
-    """o, lse = nha_forward(q, k, v, log_alpha, w).  q, k, v [B,H,T,d]; log_alpha [B,H,T,m] fp32."""
+                o=None, lse=None, workspace=None, stream=None, h0=None, return_state=False):
+    """o, lse = nha_forward(q, k, v, log_alpha, w).  q, k, v [B,H,T,d]; log_alpha [B,H,T,m] fp32.
+
+    ``h0`` = (h0k, h0v): initial slot states, fp32 [B,H,m,d] each.  With
+    ``return_state`` the result is (o, lse, (hTk, hTv)), the final slot states
+    (the long memory after token T - w - 1).  Either calls nha_forward_ex."""
     lib = load_library()
     B, H, T, d = q.shape
     m = log_alpha.shape[-1]
@@ -189,11 +197,16 @@ def nha_forward(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 1000
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib.nha_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(lse),
-                         B, H, T, d, m, int(w), int(C), DTYPE[dt], float(rope_base),
-                         _ptr(workspace), ws_bytes, _stream_handle(stream))
+    hT = None
+    if return_state:
+        hT = (torch.empty((B, H, m, d), dtype=torch.float32, device=q.device),
+              torch.empty((B, H, m, d), dtype=torch.float32, device=q.device))
+    ex = _extras(shape=(B, H, m, d), h0=h0, hT=hT)
+    rc = lib.nha_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(lse),
+                            B, H, T, d, m, int(w), int(C), DTYPE[dt], float(rope_base), ctypes.byref(ex),
+                            _ptr(workspace), ws_bytes, _stream_handle(stream))
     _raise(lib, rc)
-    return o, lse
+    return (o, lse, hT) if return_state else (o, lse)
 
 
 def nha_forward_noalloc(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 10000.0,
@@ -222,23 +235,35 @@ def nha_forward_noalloc(q, k, v, log_alpha, w: int, C: int = 64, rope_base: floa
     return o, lse
 
 
-def _extras(fwd_workspace=None):
+def _extras(fwd_workspace=None, shape=None, **states):
+    """Extras from tensors: fwd_workspace, and state pairs given as (K, V)
+    tuples of fp32 [B,H,m,d] CUDA tensors under the names h0, hT, dhT, dh0."""
     ex = Extras()
     if fwd_workspace is not None:
         _check("fwd_workspace", fwd_workspace)
         ex.fwd_workspace = fwd_workspace.data_ptr()
         ex.fwd_ws_bytes = fwd_workspace.numel() * fwd_workspace.element_size()
+    for name, pair in states.items():
+        if pair is None:
+            continue
+        kt, vt = pair
+        _check(f"{name}[0]", kt, torch.float32, shape)
+        _check(f"{name}[1]", vt, torch.float32, shape)
+        setattr(ex, f"{name}_k", kt.data_ptr())
+        setattr(ex, f"{name}_v", vt.data_ptr())
     return ex
 
 
 def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
                  rope_base: float = 10000.0, dq=None, dk=None, dv=None, dlog_alpha=None,
-                 workspace=None, stream=None, fwd_workspace=None):
+                 workspace=None, stream=None, fwd_workspace=None, h0=None, dhT=None):
     """dq, dk, dv, dlog_alpha = nha_backward(q, k, v, log_alpha, o, lse, dout, w).
 
     ``fwd_workspace``: the workspace tensor the forward of these inputs ran
     with, untouched since; the backward then reuses the chunk states and
-    rotated q, k it holds (nha_backward_ex)."""
+    rotated q, k it holds.  ``h0``: the forward's initial slot states; the
+    result then ends with (dh0k, dh0v).  ``dhT``: the gradient with respect to
+    the forward's final slot states.  Calls nha_backward_ex."""
     lib = load_library()
     B, H, T, d = q.shape
     m = log_alpha.shape[-1]
@@ -256,7 +281,11 @@ def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
     for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _check(n, t, dt, (B, H, T, d))
     _check("dlog_alpha", dlog_alpha, torch.float32, (B, H, T, m))
-    ex = _extras(fwd_workspace)
+    dh0 = None
+    if h0 is not None:
+        dh0 = (torch.empty((B, H, m, d), dtype=torch.float32, device=q.device),
+               torch.empty((B, H, m, d), dtype=torch.float32, device=q.device))
+    ex = _extras(fwd_workspace, shape=(B, H, m, d), h0=h0, dhT=dhT, dh0=dh0)
     need = int(lib.nha_workspace_bytes_ex(B, H, T, d, m, w, C, DTYPE[dt], 1, ctypes.byref(ex)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -266,7 +295,7 @@ def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
                              B, H, T, d, m, int(w), int(C), DTYPE[dt], float(rope_base), ctypes.byref(ex),
                              _ptr(workspace), ws_bytes, _stream_handle(stream))
     _raise(lib, rc)
-    return dq, dk, dv, dlog_alpha
+    return (dq, dk, dv, dlog_alpha) if dh0 is None else (dq, dk, dv, dlog_alpha) + dh0
 
 
 def nha_decode_state(B, H, d, m, w, dtype=torch.bfloat16, device="cuda"):

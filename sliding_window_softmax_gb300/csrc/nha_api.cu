@@ -42,7 +42,8 @@ struct Plan {
     nha::Shape sh;
     int d, m;
     // workspace offsets, in floats
-    size_t SK, SV, SKb, SVb, G, U, TAB, STATUS, QR, KR, Dv, Dhat, Dwin, dqwV, dqw, dkw, dvw, DL, PL, DB1, RK, RV, RKb, RVb, total;
+    size_t SK, SV, SKb, SVb, G, U, TAB, STATUS, QR, KR, HTB, HTF, Dv, Dhat, Dwin, dqwV, dqw, dkw, dvw, DL, PL, DB1, RK,
+        RV, RKb, RVb, REND, LDL, LPL, total;
 };
 
 nha_status_t check_shape(int B, int H, int T, int d, int m, int w, int C, nha_dtype_t dt) {
@@ -95,6 +96,8 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward, bool reu
         p.TAB = take(Tz * (size_t)d);  // RoPE (cos, sin) per position and frequency
         p.QR = take(BH * Tz * d / 2);  // RoPE(q), bf16
         p.KR = take(BH * Tz * d / 2);  // RoPE(k), bf16
+        p.HTB = take(BH * 2 * m * d / 2);  // final states, bf16 [BH][2][m][d] (last chunk's carry)
+        p.HTF = take(BH * 2 * m * d);      // final states, fp32 (same, fp32 path)
     }
     if (backward) {
         p.Dv = take(BH * Tz);
@@ -111,6 +114,10 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward, bool reu
         p.RV = take(BH * NC * m * d);
         p.RKb = take(BH * NC * m * d / 2);
         p.RVb = take(BH * NC * m * d / 2);
+        p.REND = take(BH * 2 * m * d);  // the state adjoint carried past chunk 0
+        const size_t W0 = (size_t)(T - sh.R);
+        p.LDL = take(BH * W0 * m);  // sigma dL of the queries t < w (initial states)
+        p.LPL = take(BH * W0 * m);  // their P_L
     }
     p.total = off;
     return p;
@@ -136,7 +143,41 @@ nha_status_t check_extras(const nha_extras_t* ex, bool backward) {
     if (ex == nullptr) return NHA_OK;
     if (!backward && ex->fwd_workspace != nullptr)
         return fail(NHA_ERR_INVALID_ARGUMENT, "fwd_workspace is an input of the backward only");
+    const struct {
+        const void* k;
+        const void* v;
+        const char* name;
+        bool fwd, bwd;  // the call that takes it
+    } pairs[] = {{ex->h0_k, ex->h0_v, "h0", true, true},
+                 {ex->hT_k, ex->hT_v, "hT", true, false},
+                 {ex->dhT_k, ex->dhT_v, "dhT", false, true},
+                 {ex->dh0_k, ex->dh0_v, "dh0", false, true}};
+    for (const auto& pr : pairs) {
+        if ((pr.k == nullptr) != (pr.v == nullptr))
+            return fail(NHA_ERR_INVALID_ARGUMENT, "%s_k and %s_v must be given together", pr.name, pr.name);
+        if (pr.k == nullptr) continue;
+        if (backward ? !pr.bwd : !pr.fwd)
+            return fail(NHA_ERR_INVALID_ARGUMENT, "%s is not an argument of the %s", pr.name,
+                        backward ? "backward" : "forward");
+        if (misaligned(pr.k) || misaligned(pr.v))
+            return fail(NHA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", pr.name);
+    }
+    if (ex->dh0_k != nullptr && ex->h0_k == nullptr)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "dh0 needs h0 (the gradient of an input that is not given)");
     return NHA_OK;
+}
+
+nha::StateIO state_io(const nha_extras_t* ex, bool forward) {
+    nha::StateIO io{};
+    if (ex != nullptr) {
+        io.h0k = ex->h0_k;
+        io.h0v = ex->h0_v;
+        if (forward) {
+            io.hTk = ex->hT_k;
+            io.hTv = ex->hT_v;
+        }
+    }
+    return io;
 }
 
 cudaError_t run_forward_tc(const Plan& p, const nha::FwdArgs& a, float* ws, cudaStream_t s) {
@@ -277,6 +318,9 @@ nha_status_t nha_forward_ex(const void* q, const void* k, const void* v, const f
     a.SK = ws + p.SK; a.SV = ws + p.SV; a.G = ws + p.G;
     a.SKb = (__nv_bfloat16*)(ws + p.SKb); a.SVb = (__nv_bfloat16*)(ws + p.SVb);
     a.U = (__nv_bfloat16*)(ws + p.U);
+    a.io = state_io(ex, true);
+    a.io.htb = (__nv_bfloat16*)(ws + p.HTB);
+    a.io.htf = ws + p.HTF;
     a.sh = p.sh;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
@@ -338,6 +382,16 @@ nha_status_t nha_backward_ex(const void* q, const void* k, const void* v, const 
     a.hdkw = (__nv_bfloat16*)a.dkw; a.hdvw = (__nv_bfloat16*)a.dvw;
     a.hDL = (__nv_bfloat16*)a.wsDL; a.hPL = (__nv_bfloat16*)a.wsPL;
     a.reuse = reuse;
+    a.io = state_io(ex, false);
+    a.io.htb = (__nv_bfloat16*)(fws + fp.HTB);
+    a.io.htf = fws + fp.HTF;
+    a.dhTk = ex ? ex->dhT_k : nullptr;
+    a.dhTv = ex ? ex->dhT_v : nullptr;
+    a.dh0k = ex ? ex->dh0_k : nullptr;
+    a.dh0v = ex ? ex->dh0_v : nullptr;
+    a.rend = ws + p.REND;
+    a.ldl = ws + p.LDL;
+    a.lpl = ws + p.LPL;
     a.sh = p.sh;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;

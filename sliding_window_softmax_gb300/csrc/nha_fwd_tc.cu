@@ -548,7 +548,7 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bf
         if ((e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, a.rope, sh, f->side)) != cudaSuccess) return e;
     }
     e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV, a.SKb, a.SVb, a.G,
-                        a.U, false, sh, status, st);
+                        a.U, false, a.io, sh, status, st);
     if (e != cudaSuccess) return e;
     if (sh.w > 0 && (e = join_side(st, *f, 1)) != cudaSuccess) return e;
     const int W0 = sh.T - sh.R;
@@ -569,7 +569,8 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bf
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     NHA_LAUNCH("fwd_tc", st, kern<<<dim3(tiles, sh.BH), kFwdThreads, sm, st>>>(a, maps, status));
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_h0_fwd_lead<__nv_bfloat16, D, M>(a, st);  // queries t < w reading initial states
 }
 
 #define NHA_TC_INST(D, M) \

@@ -26,6 +26,19 @@ cudaError_t get_fork(Fork** out);
 cudaError_t fork_side(cudaStream_t main, Fork& f, int k);
 cudaError_t join_side(cudaStream_t main, Fork& f, int k);
 
+// Optional initial / final slot states of a call (fp32 [BH, M, D] each, NULL
+// when absent) and the workspace copies the chunk scans keep of the final
+// states: htb bf16 [BH][2 (K, V)][M][D] (bf16 path), htf fp32 [BH][2][M][D]
+// (fp32 path).
+struct StateIO {
+    const float* h0k;
+    const float* h0v;
+    float* hTk;
+    float* hTv;
+    __nv_bfloat16* htb;
+    float* htf;
+};
+
 // Forward arguments.  q, k, v, o are [BH, T, D] in the element type; la is
 // [BH, T, M]; lse [BH, T].  Workspace: SK, SV [BH, NC, M, D] and G [BH, NC, M].
 struct FwdArgs {
@@ -41,6 +54,7 @@ struct FwdArgs {
     __nv_bfloat16* SKb;  // bf16 copies of SK, SV (bf16 path)
     __nv_bfloat16* SVb;
     __nv_bfloat16* U;    // chunk coefficients (bf16 path)
+    StateIO io;
     Shape sh;
     RopeTab rope;
 };
@@ -91,13 +105,43 @@ struct BwdArgs {
     // the chunk states, gate totals, RoPE table and RoPE(q), RoPE(k) above are
     // the forward's, left in its workspace: the backward does not recompute them
     bool reuse;
+    // initial states h0 (io.h0k, io.h0v) and the final states' workspace copies;
+    // the gradient with respect to the final states (dhTk, dhTv [BH, M, D] or
+    // NULL) and the initial states' gradient (dh0k, dh0v, written when h0 is
+    // given); rend [BH][2][M][D]: the state adjoint the reverse scan carries past
+    // chunk 0; ldl, lpl [BH][W0][M]: sigma dL and P_L of the queries t < w that
+    // read h0
+    StateIO io;
+    const float* dhTk;
+    const float* dhTv;
+    float* dh0k;
+    float* dh0v;
+    float* rend;
+    float* ldl;
+    float* lpl;
     Shape sh;
     RopeTab rope;
 };
 
+// Initial / final slot states outside the chunk kernels.
+// hT = h0 (or zero) when no token leaves the window (no chunk to scan).
+cudaError_t launch_final_states_copy(const StateIO& io, int BH, int M, int D, cudaStream_t st);
+// Queries t < w reading h0, forward: merges the slot branch of h0 into the
+// window-only o, lse the chunk kernels wrote for those rows.
+template <typename Tin, int D, int M>
+cudaError_t launch_h0_fwd_lead(const FwdArgs& a, cudaStream_t st);
+// Same queries, backward: their slot-branch gradients (dq; the exact D for the
+// bf16 path), and sigma dL, P_L for dh0.  tc: the bf16 path's partials (window
+// dq and its D correction); otherwise dq already holds the window part.
+template <typename Tin, int D, int M>
+cudaError_t launch_h0_bwd_lead(const BwdArgs& a, bool tc, cudaStream_t st);
+// dh0 = the adjoint carried past chunk 0 (dhT when no chunk) + the t < w queries' terms.
+template <typename Tin, int D, int M>
+cudaError_t launch_dh0(const BwdArgs& a, cudaStream_t st);
+
 template <typename Tin, int D, int M>
 cudaError_t simt_states(const Tin* k, const Tin* v, const float* la, float* SK, float* SV, float* G,
-                        const Shape& sh, cudaStream_t st);
+                        const StateIO& io, const Shape& sh, cudaStream_t st);
 template <typename Tin, int D, int M>
 cudaError_t simt_forward(const FwdArgs& a, cudaStream_t st);
 // bf16 tensor-core forward; tab: RoPE (cos, sin) table [T][D/2] in the workspace,
@@ -137,6 +181,6 @@ cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st);
 template <int D, int M>
 cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const float* la, float* SK, float* SV,
                       __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, __nv_bfloat16* U, bool want_f32,
-                      const Shape& sh, int* status, cudaStream_t st);
+                      const StateIO& io, const Shape& sh, int* status, cudaStream_t st);
 
 }  // namespace nha

@@ -69,18 +69,23 @@ state_chunk_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
 
 // ---------------------------------------------------------------------------------------
 // Exclusive scan over chunks, in place:
-//   forward (dir > 0):  X[c] <- S_c,  S_{c+1} = exp(G_c) S_c + X[c],  S_0 = 0
-//   reverse (dir < 0):  X[c] <- S_c,  S_{c-1} = exp(G_c) S_c + X[c],  S_{NC-1} = 0
+//   forward (dir > 0):  X[c] <- S_c,  S_{c+1} = exp(G_c) S_c + X[c],  S_0 = init (h0 or 0)
+//   reverse (dir < 0):  X[c] <- S_c,  S_{c-1} = exp(G_c) S_c + X[c],  S_{NC-1} = init (dhT or 0)
 // Forward gives the slot state before each chunk; reverse gives, per chunk,
-// the adjoint carried in from all later chunks.  Grid (ceil(M*D/256), BH, 2).
+// the adjoint carried in from all later chunks.  init0 / init1 ([BH, M, D] or
+// NULL) seed the K / V scans; out0 / out1 ([BH, M, D] or NULL) and outw
+// ([BH][2][M][D] or NULL) receive the value after the last step (the final
+// state; the adjoint carried past chunk 0).  Grid (ceil(M*D/256), BH, 2).
 __global__ void __launch_bounds__(kThreads)
 state_scan_kernel(float* __restrict__ X0, float* __restrict__ X1, const float* __restrict__ G,
-                  int NC, int M, int D, int dir) {
+                  int NC, int M, int D, int dir, const float* __restrict__ init0, const float* __restrict__ init1,
+                  float* __restrict__ out0, float* __restrict__ out1, float* __restrict__ outw) {
     const int e = blockIdx.x * kThreads + threadIdx.x;
     if (e >= M * D) return;
-    const int bh = blockIdx.y, i = e / D;
-    float* X = (blockIdx.z == 0) ? X0 : X1;
-    float S = 0.0f;
+    const int bh = blockIdx.y, i = e / D, z = blockIdx.z;
+    float* X = (z == 0) ? X0 : X1;
+    const float* init = z == 0 ? init0 : init1;
+    float S = init != nullptr ? init[(size_t)bh * M * D + e] : 0.0f;
     for (int n = 0; n < NC; n++) {
         const int c = dir > 0 ? n : NC - 1 - n;
         const size_t idx = ((size_t)bh * NC + c) * M * D + e;
@@ -88,6 +93,9 @@ state_scan_kernel(float* __restrict__ X0, float* __restrict__ X1, const float* _
         X[idx] = S;
         S = expf(G[((size_t)bh * NC + c) * M + i]) * S + x;
     }
+    float* out = z == 0 ? out0 : out1;
+    if (out != nullptr) out[(size_t)bh * M * D + e] = S;
+    if (outw != nullptr) outw[((size_t)bh * 2 + z) * M * D + e] = S;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -712,13 +720,16 @@ __global__ void __launch_bounds__(kThreads) bwd_dla_carry_kernel(const BwdArgs a
     const int j0 = c * kChunk, nc = min(kChunk, sh.R - j0);
     __shared__ float carry[64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (c + 1 < sh.NC) {
-        const size_t cur = ((size_t)bh * sh.NC + c) * M * D, nxt = ((size_t)bh * sh.NC + c + 1) * M * D;
+    if (c + 1 < sh.NC || a.dhTk != nullptr) {
+        // the state after chunk c: the next chunk's entering state, or the final state
+        const size_t cur = ((size_t)bh * sh.NC + c) * M * D;
+        const float* SKn = c + 1 < sh.NC ? a.SK + cur + (size_t)M * D : a.io.htf + (size_t)bh * 2 * M * D;
+        const float* SVn = c + 1 < sh.NC ? a.SV + cur + (size_t)M * D : a.io.htf + ((size_t)bh * 2 + 1) * M * D;
         for (int i = warp; i < M; i += kThreads / 32) {
             float acc = 0.0f;
             for (int d = lane; d < D; d += 32) {
                 const size_t o = (size_t)i * D + d;
-                acc += a.RK[cur + o] * a.SK[nxt + o] + a.RV[cur + o] * a.SV[nxt + o];
+                acc += a.RK[cur + o] * SKn[o] + a.RV[cur + o] * SVn[o];
             }
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (lane == 0) carry[i] = acc;
@@ -746,8 +757,8 @@ static cudaError_t set_smem(K kernel, size_t bytes) {
 
 template <typename Tin, int D, int M>
 cudaError_t simt_states(const Tin* k, const Tin* v, const float* la, float* SK, float* SV,
-                               float* G, const Shape& sh, cudaStream_t st) {
-    if (sh.NC == 0) return cudaSuccess;
+                               float* G, const StateIO& io, const Shape& sh, cudaStream_t st) {
+    if (sh.NC == 0) return launch_final_states_copy(io, sh.BH, M, D, st);
     constexpr int LX = D + 1, LG = M + 1;
     size_t sm = sizeof(float) * (size_t)(kChunk * LX + 2 * kChunk * LG);
     auto kern = state_chunk_kernel<Tin, D, M>;
@@ -756,21 +767,22 @@ cudaError_t simt_states(const Tin* k, const Tin* v, const float* la, float* SK, 
     NHA_CHECK(cudaGetLastError());
     NHA_LAUNCH("state_scan", st,
                state_scan_kernel<<<dim3((M * D + kThreads - 1) / kThreads, sh.BH, 2), kThreads, 0, st>>>(
-                   SK, SV, G, sh.NC, M, D, +1));
+                   SK, SV, G, sh.NC, M, D, +1, io.h0k, io.h0v, io.hTk, io.hTv, io.htf));
     return cudaGetLastError();
 }
 
 template <typename Tin, int D, int M>
 cudaError_t simt_forward(const FwdArgs& a, cudaStream_t st) {
     const Shape& sh = a.sh;
-    NHA_CHECK(simt_states<Tin, D, M>((const Tin*)a.k, (const Tin*)a.v, a.la, a.SK, a.SV, a.G, sh, st));
+    NHA_CHECK(simt_states<Tin, D, M>((const Tin*)a.k, (const Tin*)a.v, a.la, a.SK, a.SV, a.G, a.io, sh, st));
     constexpr int LX = D + 1, LP = kChunk + 1, LG = M + 1;
     size_t sm = sizeof(float) * (size_t)(3 * kChunk * LX + kChunk * LP + 3 * kChunk * LG + 2 * M);
     auto kern = fwd_main_kernel<Tin, D, M>;
     NHA_CHECK(set_smem(kern, sm));
     if (sh.NL + sh.NC > 0)
         NHA_LAUNCH("fwd_main", st, kern<<<dim3(sh.NL + sh.NC, sh.BH), kThreads, sm, st>>>(a));
-    return cudaGetLastError();
+    NHA_CHECK(cudaGetLastError());
+    return launch_h0_fwd_lead<Tin, D, M>(a, st);  // queries t < w reading initial states
 }
 
 template <typename Tin, int D, int M>
@@ -784,11 +796,12 @@ cudaError_t simt_bwd_slot(const BwdArgs& a, cudaStream_t st) {
         if (sh.NL + sh.NC > 0)
             NHA_LAUNCH("bwd_slot_query", st, kern<<<dim3(sh.NL + sh.NC, sh.BH), kThreads, sm, st>>>(a));
         NHA_CHECK(cudaGetLastError());
+        NHA_CHECK(launch_h0_bwd_lead<Tin, D, M>(a, false, st));  // queries t < w reading initial states
     }
     if (sh.NC > 0) {
         NHA_LAUNCH("state_scan_rev", st,
                    state_scan_kernel<<<dim3((M * D + kThreads - 1) / kThreads, sh.BH, 2), kThreads, 0, st>>>(
-                       a.RK, a.RV, a.G, sh.NC, M, D, -1));
+                       a.RK, a.RV, a.G, sh.NC, M, D, -1, a.dhTk, a.dhTv, nullptr, nullptr, a.rend));
         NHA_CHECK(cudaGetLastError());
     }
     {
@@ -798,18 +811,19 @@ cudaError_t simt_bwd_slot(const BwdArgs& a, cudaStream_t st) {
         NHA_LAUNCH("bwd_slot_key", st, kern<<<dim3(sh.NKT, sh.BH), kThreads, sm, st>>>(a));
         NHA_CHECK(cudaGetLastError());
     }
-    if (sh.NC > 1) {
+    if (sh.NC > 1 || (sh.NC > 0 && a.dhTk != nullptr)) {
         NHA_LAUNCH("bwd_dla_carry", st, bwd_dla_carry_kernel<M><<<dim3(sh.NC, sh.BH), kThreads, 0, st>>>(a, D));
         NHA_CHECK(cudaGetLastError());
     }
-    return cudaSuccess;
+    return launch_dh0<Tin, D, M>(a, st);
 }
 
 template <typename Tin, int D, int M>
 cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st) {
     const Shape& sh = a.sh;
     constexpr int LX = D + 1, LP = kChunk + 1;
-    if (!a.reuse) NHA_CHECK(simt_states<Tin, D, M>((const Tin*)a.k, (const Tin*)a.v, a.la, a.SK, a.SV, a.G, sh, st));
+    if (!a.reuse)
+        NHA_CHECK(simt_states<Tin, D, M>((const Tin*)a.k, (const Tin*)a.v, a.la, a.SK, a.SV, a.G, a.io, sh, st));
     const long rows = (long)sh.BH * sh.T;
     NHA_LAUNCH("bwd_rowdot", st,
                bwd_rowdot_kernel<Tin, D><<<(unsigned)((rows + 7) / 8), kThreads, 0, st>>>(
@@ -834,7 +848,7 @@ cudaError_t simt_backward(const BwdArgs& a, cudaStream_t st) {
 
 #define NHA_INST(Tin, D, M)                                                          \
     template cudaError_t simt_states<Tin, D, M>(const Tin*, const Tin*, const float*, float*, \
-                                                float*, float*, const Shape&, cudaStream_t); \
+                                                float*, float*, const StateIO&, const Shape&, cudaStream_t); \
     template cudaError_t simt_forward<Tin, D, M>(const FwdArgs&, cudaStream_t);      \
     template cudaError_t simt_backward<Tin, D, M>(const BwdArgs&, cudaStream_t);    \
     template cudaError_t simt_bwd_slot<Tin, D, M>(const BwdArgs&, cudaStream_t);

@@ -744,6 +744,8 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
         if (qtiles > 0)
             NHA_LAUNCH("bwd_sq_tc", st, kern<<<dim3(qtiles, sh.BH), kTcThreads, sq_smem<D, M>(), st>>>(a, maps, status));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // queries t < w reading initial states: their slot part of D and dq
+        if ((e = launch_h0_bwd_lead<__nv_bfloat16, D, M>(a, true, st)) != cudaSuccess) return e;
     }
     // the bandwidth-bound adjoint scan shares the SMs with the key-major kernel
     Fork* f = nullptr;
@@ -774,7 +776,7 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
                    kern<<<dim3((sh.T + 127) / 128, sh.BH), kTcThreads, sk_smem<D, M>(), st>>>(a, maps, status));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    return cudaSuccess;
+    return launch_dh0<__nv_bfloat16, D, M>(a, st);
 }
 
 #define NHA_TCS_INST(D, M)                                                                              \

@@ -90,7 +90,7 @@ template <int D, int M>
 __global__ void __launch_bounds__(kScanThreads, 1)
 state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __restrict__ G, float* __restrict__ SK,
                      float* __restrict__ SV, __nv_bfloat16* __restrict__ SKb, __nv_bfloat16* __restrict__ SVb,
-                     Shape sh, int want_f32, int* __restrict__ status) {
+                     const StateIO io, Shape sh, int want_f32, int* __restrict__ status) {
     constexpr int NS = kScanStages;
     constexpr int NSL = M;
     extern __shared__ unsigned char smem_raw[];
@@ -173,14 +173,20 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
         const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);
         __nv_bfloat16* Sb = (tz == 0 ? SKb : SVb) + (size_t)bh * NC * M * D + (size_t)i0 * D + d;
         float* Sf = (tz == 0 ? SK : SV) + (size_t)bh * NC * M * D + (size_t)i0 * D + d;
-        float S[NSL];
+        float S[NSL];  // the state entering chunk c: h0 (or zero) before chunk 0
+        {
+            const float* h0 = tz == 0 ? io.h0k : io.h0v;
 #pragma unroll
-        for (int i = 0; i < NSL; i++) S[i] = 0.0f;
+            for (int i = 0; i < NSL; i++) S[i] = (h0 != nullptr && d < D) ? h0[((size_t)bh * M + i) * D + d] : 0.0f;
+        }
+        bool done = true;
         for (int c = 0; c < NC; c++) {
             const int st = c % NS, b = c & 1;
             if (!mbar_wait_ab(&sfull[b], (c >> 1) & 1, kWaitCycles, abort) ||
-                !mbar_wait_ab(&full[st], (c / NS) & 1, kWaitCycles, abort))
+                !mbar_wait_ab(&full[st], (c / NS) & 1, kWaitCycles, abort)) {
+                done = false;
                 break;
+            }
             fence_after_sync();
             float dS[NSL];
             tmem_ld(tl + 64 * b, dS, NSL);
@@ -208,6 +214,17 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
             for (int i = 0; i < NSL; i++) S[i] = g[i] * S[i] + dS[i];
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        // the final state (after the last chunk): fp32 for the caller, bf16 for
+        // the backward's carry of the last chunk; NaN if the scan gave up
+        if (d < D) {
+            float* hT = tz == 0 ? io.hTk : io.hTv;
+#pragma unroll
+            for (int i = 0; i < NSL; i++) {
+                const float val = done ? S[i] : __int_as_float(0x7fc00000);
+                if (hT != nullptr) hT[((size_t)bh * M + i) * D + d] = val;
+                if (io.htb != nullptr) io.htb[(((size_t)bh * 2 + tz) * M + i) * D + d] = __float2bfloat16_rn(val);
+            }
         }
     }
     fence_before_sync();
@@ -243,7 +260,9 @@ template <int D>
 __global__ void __launch_bounds__(2 * D)
 adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, const __nv_bfloat16* __restrict__ SK,
                 const __nv_bfloat16* __restrict__ SV, const float* __restrict__ G, __nv_bfloat16* __restrict__ RKb,
-                __nv_bfloat16* __restrict__ RVb, float* __restrict__ db1, Shape sh, int M) {
+                __nv_bfloat16* __restrict__ RVb, float* __restrict__ db1, const float* __restrict__ dhTk,
+                const float* __restrict__ dhTv, const __nv_bfloat16* __restrict__ htb, float* __restrict__ rend,
+                Shape sh, int M) {
     constexpr int NW = 2 * D / 32, SG = kAdjSlots;
     __shared__ float red[2][NW][SG];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -253,6 +272,7 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
     const __nv_bfloat16* S = tz == 0 ? SK : SV;
     __nv_bfloat16* Xb = tz == 0 ? RKb : RVb;
     auto at = [&](int c) { return (((size_t)bh * NC + c) * M + i0) * D + d; };
+    const float* dh = tz == 0 ? dhTk : dhTv;
     auto load = [&](int c, float (&x)[SG], float (&sp)[SG], float (&g)[SG]) {
         const size_t o = at(c);
         const float* gc = G + ((size_t)bh * NC + c) * M + i0;
@@ -265,14 +285,19 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
             const size_t o1 = at(c + 1);
 #pragma unroll
             for (int i = 0; i < SG; i++) sp[i] = __bfloat162float(S[o1 + (size_t)i * D]);
+        } else if (dh != nullptr) {  // the last chunk's carry: the final state (with its gradient)
+            const __nv_bfloat16* hb = htb + (((size_t)bh * 2 + tz) * M + i0) * D + d;
+#pragma unroll
+            for (int i = 0; i < SG; i++) sp[i] = __bfloat162float(hb[(size_t)i * D]);
         } else {
 #pragma unroll
             for (int i = 0; i < SG; i++) sp[i] = 0.0f;
         }
     };
+    // R enters the last chunk as the gradient of the final state (zero without one)
     float R[SG];
 #pragma unroll
-    for (int i = 0; i < SG; i++) R[i] = 0.0f;
+    for (int i = 0; i < SG; i++) R[i] = dh != nullptr ? dh[((size_t)bh * M + i0 + i) * D + d] : 0.0f;
     int parity = 0;
     auto process = [&](int c, const float (&x)[SG], const float (&sp)[SG], const float (&g)[SG]) {
         const size_t o = at(c);
@@ -295,7 +320,7 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
 #pragma unroll
             for (int i = 0; i < SG; i++) red[parity][warp][i] = part[i];
         __syncthreads();  // red[parity] complete; red[parity ^ 1] free again
-        if (threadIdx.x < SG && c + 1 < NC) {
+        if (threadIdx.x < SG && (c + 1 < NC || dhTk != nullptr)) {
             float t = 0.0f;
 #pragma unroll
             for (int q = 0; q < NW; q++) t += red[parity][q][threadIdx.x];
@@ -317,6 +342,9 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
         process(c - 1, xb, sb, gb);
         if (c - 3 >= 0) load(c - 3, xb, sb, gb);
     }
+    if (rend != nullptr)  // the adjoint of the state before chunk 0 (part of dh0)
+#pragma unroll
+        for (int i = 0; i < SG; i++) rend[(((size_t)bh * 2 + tz) * M + i0 + i) * D + d] = R[i];
 }
 
 cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st) {
@@ -325,18 +353,20 @@ cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st) {
     const dim3 grid(sh.BH, M / kAdjSlots);
     if (D == 128)
         NHA_LAUNCH("adj_scan", st,
-                   adj_scan_kernel<128><<<grid, 256, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.wsDB1, sh, M));
+                   adj_scan_kernel<128><<<grid, 256, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.wsDB1,
+                                                              a.dhTk, a.dhTv, a.io.htb, a.rend, sh, M));
     else
         NHA_LAUNCH("adj_scan", st,
-                   adj_scan_kernel<64><<<grid, 128, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.wsDB1, sh, M));
+                   adj_scan_kernel<64><<<grid, 128, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.wsDB1,
+                                                             a.dhTk, a.dhTv, a.io.htb, a.rend, sh, M));
     return cudaGetLastError();
 }
 
 template <int D, int M>
 cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const float* la, float* SK, float* SV,
                       __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, __nv_bfloat16* U, bool want_f32,
-                      const Shape& sh, int* status, cudaStream_t st) {
-    if (sh.NC == 0) return cudaSuccess;
+                      const StateIO& io, const Shape& sh, int* status, cudaStream_t st) {
+    if (sh.NC == 0) return launch_final_states_copy(io, sh.BH, M, D, st);
     CUtensorMap la_map;
     cudaError_t e = tmap_rows_f32(&la_map, la, M, sh.T, sh.BH);
     if (e != cudaSuccess) return e;
@@ -359,7 +389,7 @@ cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const floa
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) != cudaSuccess)
         return e;
     NHA_LAUNCH("state_scan", st,
-               kern<<<dim3(sh.BH, 2), kScanThreads, sm, st>>>(maps, G, SK, SV, SKb, SVb, sh, want_f32 ? 1 : 0,
+               kern<<<dim3(sh.BH, 2), kScanThreads, sm, st>>>(maps, G, SK, SV, SKb, SVb, io, sh, want_f32 ? 1 : 0,
                                                               status));
     return cudaGetLastError();
 }
@@ -367,7 +397,7 @@ cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const floa
 #define NHA_ST_INST(D, M)                                                                              \
     template cudaError_t tc_states<D, M>(const __nv_bfloat16*, const __nv_bfloat16*, const float*, float*, \
                                          float*, __nv_bfloat16*, __nv_bfloat16*, float*, __nv_bfloat16*, bool, \
-                                         const Shape&, int*, cudaStream_t);
+                                         const StateIO&, const Shape&, int*, cudaStream_t);
 NHA_ST_INST(64, 16)
 NHA_ST_INST(64, 32)
 NHA_ST_INST(64, 64)

@@ -272,3 +272,26 @@ def test_extended_calls_validate_their_extras(lib):
     rc = lib.nha_backward_ex(p, p, p, p, p, p, p, p, p, p, p, 1, 2, 256, 64, 16, 32, 64, 1, 10000.0,
                              ctypes.byref(ex), p, own - 256, None)
     assert rc == 3
+
+
+def test_extended_calls_validate_state_pointers(lib):
+    p = ctypes.c_void_p(4096)
+    args = (p, p, p, p, p, p, 1, 2, 256, 64, 16, 32, 64, 1, 10000.0)
+    ex = _binding.Extras()
+    ex.h0_k = 4096  # without h0_v
+    assert lib.nha_forward_ex(*args, ctypes.byref(ex), p, 1 << 30, None) == 1
+    assert b"together" in lib.nha_last_error()
+    ex = _binding.Extras()
+    ex.dhT_k = ex.dhT_v = 4096  # a backward input given to the forward
+    assert lib.nha_forward_ex(*args, ctypes.byref(ex), p, 1 << 30, None) == 1
+    ex = _binding.Extras()
+    ex.h0_k, ex.h0_v = 4096, 4100  # misaligned
+    assert lib.nha_forward_ex(*args, ctypes.byref(ex), p, 1 << 30, None) == 1
+    ex = _binding.Extras()
+    ex.dh0_k = ex.dh0_v = 4096  # dh0 without h0
+    bargs = (p, p, p, p, p, p, p, p, p, p, p, 1, 2, 256, 64, 16, 32, 64, 1, 10000.0)
+    assert lib.nha_backward_ex(*bargs, ctypes.byref(ex), p, 1 << 30, None) == 1
+    assert b"needs h0" in lib.nha_last_error()
+    ex = _binding.Extras()
+    ex.hT_k = ex.hT_v = 4096  # a forward output given to the backward
+    assert lib.nha_backward_ex(*bargs, ctypes.byref(ex), p, 1 << 30, None) == 1
