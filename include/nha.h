@@ -134,7 +134,16 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
  *                positions from its own start).
  *   dhT_k, dhT_v backward input: the gradient of the loss with respect to hT
  *                (the loss is then <o, dout> + <hT, dhT>).
- *   dh0_k, dh0_v backward output: the gradient with respect to h0 (needs h0). */
+ *   dh0_k, dh0_v backward output: the gradient with respect to h0 (needs h0).
+ *
+ * windows: DEVICE array [H] of int32, or NULL: head h (of every batch entry)
+ * has its own window min(max(windows[h], 0), w), so w is the largest window;
+ * all heads still run in the same launches (the ai.info page: randomised
+ * window sizes in training, per-layer / per-head window schedules).  The
+ * workspace is then laid out for the smallest possible window (w = 0), so
+ * pass the same extras to nha_workspace_bytes_ex; forward and backward (and
+ * a forward workspace the backward reuses) must see the same windows.  The
+ * host cannot check device values: a value outside [0, w] is clamped. */
 typedef struct {
     const void* fwd_workspace; /* backward: the forward's workspace, read only */
     size_t fwd_ws_bytes;       /* its size in bytes */
@@ -146,6 +155,7 @@ typedef struct {
     const float* dhT_v;
     float* dh0_k;
     float* dh0_v;
+    const int* windows; /* DEVICE [H] int32 per-head windows, or NULL */
 } nha_extras_t;
 
 /* Workspace bytes of nha_forward_ex (backward = 0) / nha_backward_ex

@@ -42,7 +42,8 @@ class Extras(ctypes.Structure):
                 ("h0_k", ctypes.c_void_p), ("h0_v", ctypes.c_void_p),
                 ("hT_k", ctypes.c_void_p), ("hT_v", ctypes.c_void_p),
                 ("dhT_k", ctypes.c_void_p), ("dhT_v", ctypes.c_void_p),
-                ("dh0_k", ctypes.c_void_p), ("dh0_v", ctypes.c_void_p)]
+                ("dh0_k", ctypes.c_void_p), ("dh0_v", ctypes.c_void_p),
+                ("windows", ctypes.c_void_p)]
 
 
 class ProfileRecord(ctypes.Structure):
@@ -159,20 +160,24 @@ def _check(name, t, dtype=None, shape=None):
 
 
 def nha_workspace_bytes(B, H, T, d, m, w, C=64, dtype=torch.bfloat16, backward=False,
-                        reuse_forward=False) -> int:
+                        reuse_forward=False, per_head_windows=False) -> int:
     """Workspace bytes of the forward (or backward); ``reuse_forward``: of a
-    backward given the forward's workspace (nha_workspace_bytes_ex)."""
+    backward given the forward's workspace; ``per_head_windows``: of a call
+    with a windows array (nha_workspace_bytes_ex)."""
     lib = load_library()
-    if reuse_forward:
+    if reuse_forward or per_head_windows:
         ex = Extras()
-        ex.fwd_workspace = 16  # any non-NULL value: only its presence counts here
+        if reuse_forward:
+            ex.fwd_workspace = 16  # any non-NULL value: only its presence counts here
+        if per_head_windows:
+            ex.windows = 16
         return int(lib.nha_workspace_bytes_ex(B, H, T, d, m, w, C, DTYPE[dtype], int(bool(backward)),
                                               ctypes.byref(ex)))
     return int(lib.nha_workspace_bytes(B, H, T, d, m, w, C, DTYPE[dtype], int(bool(backward))))
 
 
 def nha_forward(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 10000.0,
-                o=None, lse=None, workspace=None, stream=None, h0=None, return_state=False):
+                o=None, lse=None, workspace=None, stream=None, h0=None, return_state=False, windows=None):
     """o, lse = nha_forward(q, k, v, log_alpha, w).  q, k, v [B,H,T,d]; log_alpha [B,H,T,m] fp32.
 
     ``h0`` = (h0k, h0v): initial slot states, fp32 [B,H,m,d] each.  With
@@ -193,7 +198,8 @@ def nha_forward(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 1000
         lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     _check("o", o, dt, (B, H, T, d))
     _check("lse", lse, torch.float32, (B, H, T))
-    need = int(lib.nha_workspace_bytes(B, H, T, d, m, w, C, DTYPE[dt], 0))
+    ex = _extras(shape=(B, H, m, d), windows=windows)
+    need = int(lib.nha_workspace_bytes_ex(B, H, T, d, m, w, C, DTYPE[dt], 0, ctypes.byref(ex)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -201,7 +207,7 @@ def nha_forward(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 1000
     if return_state:
         hT = (torch.empty((B, H, m, d), dtype=torch.float32, device=q.device),
               torch.empty((B, H, m, d), dtype=torch.float32, device=q.device))
-    ex = _extras(shape=(B, H, m, d), h0=h0, hT=hT)
+    ex = _extras(shape=(B, H, m, d), windows=windows, h0=h0, hT=hT)
     rc = lib.nha_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(lse),
                             B, H, T, d, m, int(w), int(C), DTYPE[dt], float(rope_base), ctypes.byref(ex),
                             _ptr(workspace), ws_bytes, _stream_handle(stream))
@@ -235,10 +241,14 @@ def nha_forward_noalloc(q, k, v, log_alpha, w: int, C: int = 64, rope_base: floa
     return o, lse
 
 
-def _extras(fwd_workspace=None, shape=None, **states):
-    """Extras from tensors: fwd_workspace, and state pairs given as (K, V)
-    tuples of fp32 [B,H,m,d] CUDA tensors under the names h0, hT, dhT, dh0."""
+def _extras(fwd_workspace=None, shape=None, windows=None, **states):
+    """Extras from tensors: fwd_workspace, windows (int32 CUDA [H]), and state
+    pairs given as (K, V) tuples of fp32 [B,H,m,d] CUDA tensors under the names
+    h0, hT, dhT, dh0."""
     ex = Extras()
+    if windows is not None:
+        _check("windows", windows, torch.int32, (shape[1],) if shape is not None else None)
+        ex.windows = windows.data_ptr()
     if fwd_workspace is not None:
         _check("fwd_workspace", fwd_workspace)
         ex.fwd_workspace = fwd_workspace.data_ptr()
@@ -256,7 +266,7 @@ def _extras(fwd_workspace=None, shape=None, **states):
 
 def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
                  rope_base: float = 10000.0, dq=None, dk=None, dv=None, dlog_alpha=None,
-                 workspace=None, stream=None, fwd_workspace=None, h0=None, dhT=None):
+                 workspace=None, stream=None, fwd_workspace=None, h0=None, dhT=None, windows=None):
     """dq, dk, dv, dlog_alpha = nha_backward(q, k, v, log_alpha, o, lse, dout, w).
 
     ``fwd_workspace``: the workspace tensor the forward of these inputs ran
@@ -285,7 +295,7 @@ def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
     if h0 is not None:
         dh0 = (torch.empty((B, H, m, d), dtype=torch.float32, device=q.device),
                torch.empty((B, H, m, d), dtype=torch.float32, device=q.device))
-    ex = _extras(fwd_workspace, shape=(B, H, m, d), h0=h0, dhT=dhT, dh0=dh0)
+    ex = _extras(fwd_workspace, shape=(B, H, m, d), windows=windows, h0=h0, dhT=dhT, dh0=dh0)
     need = int(lib.nha_workspace_bytes_ex(B, H, T, d, m, w, C, DTYPE[dt], 1, ctypes.byref(ex)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

@@ -64,7 +64,9 @@ nha_status_t check_shape(int B, int H, int T, int d, int m, int w, int C, nha_dt
 // backward && reuse: the chunk states, gate totals, RoPE table and rotated q, k
 // come from the forward's workspace, so this plan holds only the backward's own
 // buffers.
-Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward, bool reuse = false) {
+// per_head: the heads have their own windows in [0, w]; the per-head arrays are
+// then laid out for the largest number of chunks (w = 0).
+Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward, bool reuse = false, bool per_head = false) {
     Plan p;
     memset(&p, 0, sizeof(p));
     p.d = d;
@@ -78,13 +80,17 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward, bool reu
     sh.NL = (sh.w + nha::kChunk - 1) / nha::kChunk;
     sh.NKT = (T + nha::kChunk - 1) / nha::kChunk;
     sh.sigma = (float)(1.0 / sqrt((double)d));
+    sh.NCS = per_head ? sh.NKT : sh.NC;
+    sh.W0S = T - sh.R;
+    sh.windows = nullptr;
+    sh.H = H;
     size_t off = 0;
     auto take = [&](size_t n) {
         size_t o = off;
         off += (n + 63) & ~(size_t)63;  // keep every sub-buffer 256-byte aligned
         return o;
     };
-    const size_t BH = (size_t)sh.BH, NC = (size_t)sh.NC, Tz = (size_t)T;
+    const size_t BH = (size_t)sh.BH, NC = (size_t)sh.NCS, Tz = (size_t)T;
     p.STATUS = take(16);
     if (!(backward && reuse)) {
         p.SK = take(BH * NC * m * d);
@@ -115,7 +121,7 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward, bool reu
         p.RKb = take(BH * NC * m * d / 2);
         p.RVb = take(BH * NC * m * d / 2);
         p.REND = take(BH * 2 * m * d);  // the state adjoint carried past chunk 0
-        const size_t W0 = (size_t)(T - sh.R);
+        const size_t W0 = (size_t)sh.W0S;
         p.LDL = take(BH * W0 * m);  // sigma dL of the queries t < w (initial states)
         p.LPL = take(BH * W0 * m);  // their P_L
     }
@@ -164,8 +170,12 @@ nha_status_t check_extras(const nha_extras_t* ex, bool backward) {
     }
     if (ex->dh0_k != nullptr && ex->h0_k == nullptr)
         return fail(NHA_ERR_INVALID_ARGUMENT, "dh0 needs h0 (the gradient of an input that is not given)");
+    if (ex->windows != nullptr && ((uintptr_t)ex->windows & 3u) != 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "windows array is not 4-byte aligned");
     return NHA_OK;
 }
+
+bool per_head(const nha_extras_t* ex) { return ex != nullptr && ex->windows != nullptr; }
 
 nha::StateIO state_io(const nha_extras_t* ex, bool forward) {
     nha::StateIO io{};
@@ -283,7 +293,7 @@ size_t nha_workspace_bytes_ex(int B, int H, int T, int d, int m, int w, int C, n
                               const nha_extras_t* ex) {
     if (check_shape(B, H, T, d, m, w, C, dtype) != NHA_OK) return 0;
     const bool reuse = backward && ex != nullptr && ex->fwd_workspace != nullptr;
-    Plan p = make_plan(B, H, T, d, m, w, backward != 0, reuse);
+    Plan p = make_plan(B, H, T, d, m, w, backward != 0, reuse, per_head(ex));
     return p.total * sizeof(float);
 }
 
@@ -304,7 +314,7 @@ nha_status_t nha_forward_ex(const void* q, const void* k, const void* v, const f
         if (ptrs[i] == nullptr) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is NULL", names[i]);
         if (misaligned(ptrs[i])) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", names[i]);
     }
-    Plan p = make_plan(B, H, T, d, m, w, false);
+    Plan p = make_plan(B, H, T, d, m, w, false, false, per_head(ex));
     const size_t need = p.total * sizeof(float);
     if (need > 0 && (workspace == nullptr || ws_bytes < need))
         return fail(NHA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
@@ -322,6 +332,7 @@ nha_status_t nha_forward_ex(const void* q, const void* k, const void* v, const f
     a.io.htb = (__nv_bfloat16*)(ws + p.HTB);
     a.io.htf = ws + p.HTF;
     a.sh = p.sh;
+    a.sh.windows = per_head(ex) ? ex->windows : nullptr;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = dtype == NHA_DTYPE_F32 ? run_forward<float>(p, a, s) : run_forward_tc(p, a, ws, s);
@@ -347,7 +358,7 @@ nha_status_t nha_backward_ex(const void* q, const void* k, const void* v, const 
         if (misaligned(ptrs[i])) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", names[i]);
     }
     const bool reuse = ex != nullptr && ex->fwd_workspace != nullptr;
-    Plan p = make_plan(B, H, T, d, m, w, true, reuse);
+    Plan p = make_plan(B, H, T, d, m, w, true, reuse, per_head(ex));
     const size_t need = p.total * sizeof(float);
     if (workspace == nullptr || ws_bytes < need)
         return fail(NHA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
@@ -357,7 +368,7 @@ nha_status_t nha_backward_ex(const void* q, const void* k, const void* v, const 
     float* ws = (float*)workspace;
     float* fws = ws;
     if (reuse) {
-        fp = make_plan(B, H, T, d, m, w, false);
+        fp = make_plan(B, H, T, d, m, w, false, false, per_head(ex));
         const size_t fneed = fp.total * sizeof(float);
         if (ex->fwd_ws_bytes < fneed)
             return fail(NHA_ERR_WORKSPACE, "forward workspace of %zu bytes expected, %zu given", fneed,
@@ -393,6 +404,7 @@ nha_status_t nha_backward_ex(const void* q, const void* k, const void* v, const 
     a.ldl = ws + p.LDL;
     a.lpl = ws + p.LPL;
     a.sh = p.sh;
+    a.sh.windows = per_head(ex) ? ex->windows : nullptr;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = dtype == NHA_DTYPE_F32 ? run_backward<float>(p, a, s) : run_backward_tc(p, a, ws, fp, fws, s);

@@ -37,7 +37,28 @@ struct Shape {
     int NL;      // ceil(min(w, T) / C): leading window-only query tiles
     int NKT;     // ceil(T / C): key tiles
     float sigma; // 1 / sqrt(d)
+    // Layout of the per-head workspace arrays, the same for every head:
+    int NCS;     // chunks per head in the [BH, NCS, ...] arrays (NC, or ceil(T / C) with per-head windows)
+    int W0S;     // rows per head of the [BH, W0S, m] arrays of the queries t < w (the largest min(w, T))
+    // Per-head windows (device [H], or null): head h = bh % H has window
+    // min(max(windows[h], 0), w); w above is then the largest window.
+    const int* windows;
+    int H;
 };
+
+// The shape seen by head bh: its own window and the counts that follow from
+// it (the layout fields NCS, W0S are the call's).
+__device__ __forceinline__ Shape head_shape(const Shape& call, int bh) {
+    Shape s = call;
+    if (call.windows != nullptr) {
+        const int wh = min(max(__ldg(call.windows + bh % call.H), 0), call.w);
+        s.w = wh;
+        s.R = s.T - wh;
+        s.NC = (s.R + kChunk - 1) / kChunk;
+        s.NL = (wh + kChunk - 1) / kChunk;
+    }
+    return s;
+}
 
 __device__ __forceinline__ float ld(const float* p) { return *p; }
 __device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }

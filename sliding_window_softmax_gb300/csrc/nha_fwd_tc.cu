@@ -58,11 +58,12 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
-    const Shape sh = a.sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int x = blockIdx.x, bh = blockIdx.y;
+    const Shape sh = head_shape(a.sh, bh);
     const int W0 = sh.T - sh.R;
     const int NLT = (W0 + 127) / 128;
-    const int x = blockIdx.x, bh = blockIdx.y;
+    if (x >= NLT + (sh.R + 127) / 128) return;  // past this head's tiles (per-head windows)
     const bool slot = x >= NLT;
     int tbase, nq, j0 = 0;
     if (!slot) {
@@ -552,7 +553,8 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bf
     if (e != cudaSuccess) return e;
     if (sh.w > 0 && (e = join_side(st, *f, 1)) != cudaSuccess) return e;
     const int W0 = sh.T - sh.R;
-    const int tiles = (W0 + 127) / 128 + (sh.R + 127) / 128;
+    // with per-head windows a head has at most ceil(T / 128) + 1 tiles
+    const int tiles = sh.windows ? (sh.T + 127) / 128 + 1 : (W0 + 127) / 128 + (sh.R + 127) / 128;
     if (tiles == 0) return cudaSuccess;
     FwdMaps maps;
     if ((e = tmap_rows_bf16(&maps.q, qr, D, sh.T, sh.BH, 128)) != cudaSuccess ||
@@ -561,8 +563,8 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bf
         (e = tmap_rows_f32(&maps.la, a.la, M, sh.T, sh.BH)) != cudaSuccess ||
         (e = tmap_rows_bf16(&maps.qs, a.q, D, sh.T, sh.BH, 128)) != cudaSuccess ||
         (e = tmap_rows_bf16(&maps.ks, a.k, D, sh.T, sh.BH, 128)) != cudaSuccess ||
-        (e = tmap_rows_bf16(&maps.sk, a.SKb, D, (sh.NC > 0 ? sh.NC : 1) * M, sh.BH, 2 * M)) != cudaSuccess ||
-        (e = tmap_rows_bf16(&maps.sv, a.SVb, D, (sh.NC > 0 ? sh.NC : 1) * M, sh.BH, 2 * M)) != cudaSuccess)
+        (e = tmap_rows_bf16(&maps.sk, a.SKb, D, (sh.NCS > 0 ? sh.NCS : 1) * M, sh.BH, 2 * M)) != cudaSuccess ||
+        (e = tmap_rows_bf16(&maps.sv, a.SVb, D, (sh.NCS > 0 ? sh.NCS : 1) * M, sh.BH, 2 * M)) != cudaSuccess)
         return e;
     const size_t sm = tc_fwd_smem<D, M>();
     auto kern = fwd_tc_kernel<D, M>;

@@ -79,8 +79,10 @@ h0_fwd_lead_kernel(const FwdArgs a) {
     float* sV = sK + M * (D + 1);        // [M][D + 1]
     float* sRow = sV + M * (D + 1);      // [8 warps][D]  q row
     float* sP = sRow + 8 * D;            // [8 warps][M]  slot weights
-    const Shape sh = a.sh;
-    const int W0 = sh.T - sh.R, bh = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Shape sh = head_shape(a.sh, bh);
+    const int W0 = sh.T - sh.R;
+    if (blockIdx.x * kH0Rows >= W0) return;  // past this head's rows (per-head windows)
     load_h0<D, M>(a.io, bh, sK, sV);
     __syncthreads();
     const size_t hoff = (size_t)bh * sh.T;
@@ -133,8 +135,10 @@ h0_bwd_lead_kernel(const BwdArgs a) {
     float* sV = sK + M * (D + 1);
     float* sRow = sV + M * (D + 1);  // [8 warps][2][D]  q row, dout row
     float* sP = sRow + 16 * D;       // [8 warps][M]     sigma dL
-    const Shape sh = a.sh;
-    const int W0 = sh.T - sh.R, bh = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Shape sh = head_shape(a.sh, bh);
+    const int W0 = sh.T - sh.R, W0S = a.sh.W0S;
+    if (blockIdx.x * kH0Rows >= W0) return;  // past this head's rows (per-head windows)
     load_h0<D, M>(a.io, bh, sK, sV);
     __syncthreads();
     const size_t hoff = (size_t)bh * sh.T;
@@ -177,8 +181,8 @@ h0_bwd_lead_kernel(const BwdArgs a) {
             if (i < M) {
                 const float sdl = sh.sigma * P[s] * (dP[s] - Dt);
                 prow[i] = sdl;
-                a.ldl[((size_t)bh * W0 + t) * M + i] = sdl;
-                a.lpl[((size_t)bh * W0 + t) * M + i] = P[s];
+                a.ldl[((size_t)bh * W0S + t) * M + i] = sdl;
+                a.lpl[((size_t)bh * W0S + t) * M + i] = P[s];
             }
         }
         __syncwarp();
@@ -214,8 +218,9 @@ h0_bwd_lead_kernel(const BwdArgs a) {
 template <typename Tin, int D, int M>
 __global__ void __launch_bounds__(256)
 dh0_kernel(const BwdArgs a) {
-    const Shape sh = a.sh;
-    const int W0 = sh.T - sh.R, bh = blockIdx.y, z = blockIdx.z;
+    const int bh = blockIdx.y, z = blockIdx.z;
+    const Shape sh = head_shape(a.sh, bh);
+    const int W0 = sh.T - sh.R;
     const int e = blockIdx.x * 256 + threadIdx.x;  // over (M / 4) * D
     if (e >= (M / 4) * D) return;
     const int i0 = 4 * (e / D), d = e % D;
@@ -231,7 +236,7 @@ dh0_kernel(const BwdArgs a) {
         }
     }
     if (W0 > 0) {
-        const float* X = (z == 0 ? a.ldl : a.lpl) + (size_t)bh * W0 * M + i0;
+        const float* X = (z == 0 ? a.ldl : a.lpl) + (size_t)bh * a.sh.W0S * M + i0;
         const Tin* Y = (const Tin*)(z == 0 ? a.q : a.dout) + (size_t)bh * sh.T * D + d;
         for (int t = 0; t < W0; t++) {
             const float4 x = *reinterpret_cast<const float4*>(X + (size_t)t * M);

@@ -30,13 +30,15 @@ template <typename Tin, int D, int M>
 __global__ void __launch_bounds__(kThreads)
 state_chunk_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
                    const float* __restrict__ la, float* __restrict__ SK, float* __restrict__ SV,
-                   float* __restrict__ G, Shape sh) {
+                   float* __restrict__ G, Shape call) {
     extern __shared__ float smem[];
     constexpr int LX = D + 1, LG = M + 1;
     float* sX = smem;                  // [C][LX]
     float* sCoef = sX + kChunk * LX;   // [C][LG]
     float* sU = sCoef + kChunk * LG;   // [C][LG]
     const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+    const Shape sh = head_shape(call, bh);
+    if (c >= sh.NC) return;  // past this head's chunks (per-head windows)
     const int j0 = c * kChunk, nc = min(kChunk, sh.R - j0);
     const size_t row0 = (size_t)bh * sh.T;
     if (tid < M) {
@@ -50,11 +52,11 @@ state_chunk_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
         }
         for (int r = 0; r < kChunk; r++)
             sCoef[r * LG + tid] = (r < nc) ? expf(b - sCoef[r * LG + tid]) * sU[r * LG + tid] : 0.0f;
-        G[((size_t)bh * sh.NC + c) * M + tid] = b;
+        G[((size_t)bh * sh.NCS + c) * M + tid] = b;
     }
     for (int pass = 0; pass < 2; pass++) {
         const Tin* src = (pass == 0 ? k : v) + row0 * D;
-        float* dst = (pass == 0 ? SK : SV) + ((size_t)bh * sh.NC + c) * M * D;
+        float* dst = (pass == 0 ? SK : SV) + ((size_t)bh * sh.NCS + c) * M * D;
         __syncthreads();
         load_rows<Tin, D>(src, j0, nc, sX, LX, nullptr);
         __syncthreads();
@@ -78,20 +80,21 @@ state_chunk_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
 // state; the adjoint carried past chunk 0).  Grid (ceil(M*D/256), BH, 2).
 __global__ void __launch_bounds__(kThreads)
 state_scan_kernel(float* __restrict__ X0, float* __restrict__ X1, const float* __restrict__ G,
-                  int NC, int M, int D, int dir, const float* __restrict__ init0, const float* __restrict__ init1,
+                  Shape call, int M, int D, int dir, const float* __restrict__ init0, const float* __restrict__ init1,
                   float* __restrict__ out0, float* __restrict__ out1, float* __restrict__ outw) {
     const int e = blockIdx.x * kThreads + threadIdx.x;
     if (e >= M * D) return;
     const int bh = blockIdx.y, i = e / D, z = blockIdx.z;
+    const int NC = head_shape(call, bh).NC, NCS = call.NCS;  // this head's chunks; chunks per head in the arrays
     float* X = (z == 0) ? X0 : X1;
     const float* init = z == 0 ? init0 : init1;
     float S = init != nullptr ? init[(size_t)bh * M * D + e] : 0.0f;
     for (int n = 0; n < NC; n++) {
         const int c = dir > 0 ? n : NC - 1 - n;
-        const size_t idx = ((size_t)bh * NC + c) * M * D + e;
+        const size_t idx = ((size_t)bh * NCS + c) * M * D + e;
         float x = X[idx];
         X[idx] = S;
-        S = expf(G[((size_t)bh * NC + c) * M + i]) * S + x;
+        S = expf(G[((size_t)bh * NCS + c) * M + i]) * S + x;
     }
     float* out = z == 0 ? out0 : out1;
     if (out != nullptr) out[(size_t)bh * M * D + e] = S;
@@ -116,9 +119,10 @@ __global__ void __launch_bounds__(kThreads) fwd_main_kernel(const FwdArgs a) {
     float* sL = sEk + kChunk * LG;
     float* sG = sL + kChunk * LG;
     float* sER = sG + M;
-    const Shape sh = a.sh;
     const int tid = threadIdx.x, r = tid >> 2, tq = tid & 3;
     const int x = blockIdx.x, bh = blockIdx.y;
+    const Shape sh = head_shape(a.sh, bh);
+    if (x >= sh.NL + sh.NC) return;  // past this head's tiles (per-head windows)
     const bool slot = x >= sh.NL;
     int tbase, nq, c = 0, j0 = 0;
     if (!slot) {
@@ -145,7 +149,7 @@ __global__ void __launch_bounds__(kThreads) fwd_main_kernel(const FwdArgs a) {
     if (slot) {
         chunk_gates<M>(a.la + (hoff + j0) * M, nq, sEq, sEk, nullptr, LG, sG, sER);
         load_rows<Tin, D>(k, j0, nq, sX1, LX, nullptr);
-        const float* SKp = a.SK + ((size_t)bh * sh.NC + c) * M * D;
+        const float* SKp = a.SK + ((size_t)bh * sh.NCS + c) * M * D;
         for (int e = tid; e < M * D; e += kThreads) sX2[(e / D) * LX + e % D] = SKp[e];
         __syncthreads();
         // A[r][s] = q_{t(r)} . k_{j0+s}, causal s <= r (un-rotated)
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(kThreads) fwd_main_kernel(const FwdArgs a) {
             sP[r * LP + s] = t;
         }
         load_rows<Tin, D>(v, j0, nq, sX1, LX, nullptr);
-        const float* SVp = a.SV + ((size_t)bh * sh.NC + c) * M * D;
+        const float* SVp = a.SV + ((size_t)bh * sh.NCS + c) * M * D;
         for (int e = tid; e < M * D; e += kThreads) sX2[(e / D) * LX + e % D] = SVp[e];
         __syncthreads();
         for (int n = 0; n < NCOL; n++) {
@@ -293,8 +297,8 @@ __global__ void __launch_bounds__(kThreads) bwd_window_dq_kernel(const BwdArgs a
     float* sK = sdO + kChunk * LX;
     float* sV = sK + kChunk * LX;
     float* sP = sV + kChunk * LX;
-    const Shape sh = a.sh;
     const int tid = threadIdx.x, r = tid >> 2, tq = tid & 3, bh = blockIdx.y;
+    const Shape sh = head_shape(a.sh, bh);
     const int tbase = blockIdx.x * kChunk, nq = min(kChunk, sh.T - tbase);
     const size_t hoff = (size_t)bh * sh.T;
     const Tin* k = (const Tin*)a.k + hoff * D;
@@ -365,8 +369,8 @@ __global__ void __launch_bounds__(kThreads) bwd_window_dkdv_kernel(const BwdArgs
     float* sDt = sPt + kChunk * LP;
     float* sLse = sDt + kChunk * LP;
     float* sD = sLse + kChunk;
-    const Shape sh = a.sh;
     const int tid = threadIdx.x, s = tid >> 2, tq = tid & 3, bh = blockIdx.y;
+    const Shape sh = head_shape(a.sh, bh);
     const int sbase = blockIdx.x * kChunk, nk = min(kChunk, sh.T - sbase);
     const size_t hoff = (size_t)bh * sh.T;
     const Tin* q = (const Tin*)a.q + hoff * D;
@@ -455,8 +459,9 @@ __global__ void __launch_bounds__(kThreads) bwd_slot_query_kernel(const BwdArgs 
     float* sPL = sDL + kChunk * LG;
     float* sG = sPL + kChunk * LG;
     float* sER = sG + M;
-    const Shape sh = a.sh;
     const int tid = threadIdx.x, r = tid >> 2, tq = tid & 3, bh = blockIdx.y, x = blockIdx.x;
+    const Shape sh = head_shape(a.sh, bh);
+    if (x >= sh.NL + sh.NC) return;  // past this head's tiles (per-head windows)
     const size_t hoff = (size_t)bh * sh.T;
     if (x < sh.NL) {
         const int tbase = x * kChunk, nq = min(kChunk, min(sh.w, sh.T) - tbase);
@@ -478,7 +483,7 @@ __global__ void __launch_bounds__(kThreads) bwd_slot_query_kernel(const BwdArgs 
     // --- value side: dP_L = Eb o (dO S^V_prev^T) + Eq o ((dO V_c^T o causal) Ek)
     load_rows<Tin, D>(v, j0, nq, sX1, LX, nullptr);
     {
-        const float* SVp = a.SV + ((size_t)bh * sh.NC + c) * M * D;
+        const float* SVp = a.SV + ((size_t)bh * sh.NCS + c) * M * D;
         for (int e = tid; e < M * D; e += kThreads) sX2[(e / D) * LX + e % D] = SVp[e];
     }
     __syncthreads();
@@ -503,7 +508,7 @@ __global__ void __launch_bounds__(kThreads) bwd_slot_query_kernel(const BwdArgs 
     // --- key side: slot logits L, P_L, dL
     load_rows<Tin, D>(k, j0, nq, sX1, LX, nullptr);
     {
-        const float* SKp = a.SK + ((size_t)bh * sh.NC + c) * M * D;
+        const float* SKp = a.SK + ((size_t)bh * sh.NCS + c) * M * D;
         for (int e = tid; e < M * D; e += kThreads) sX2[(e / D) * LX + e % D] = SKp[e];
     }
     __syncthreads();
@@ -515,7 +520,7 @@ __global__ void __launch_bounds__(kThreads) bwd_slot_query_kernel(const BwdArgs 
         sP[r * LP + s] = t;
     }
     __syncthreads();
-    const size_t jrow = (size_t)bh * sh.NC * kChunk + j0 + r;  // row in [BH][NC*C][M] arrays
+    const size_t jrow = (size_t)bh * sh.NCS * kChunk + j0 + r;  // row in [BH][NCS*C][M] arrays
     for (int n = 0; n < NSL; n++) {
         const int i = tq + 4 * n;
         float inter = 0.0f, intra = 0.0f;
@@ -556,8 +561,8 @@ __global__ void __launch_bounds__(kThreads) bwd_slot_query_kernel(const BwdArgs 
         }
     }
     // dR^K_c[i][col] = sum_r Eb[r][i] sigma dL[r][i] q_r[col];  dR^V_c likewise with P_L, dout
-    float* RK = a.RK + ((size_t)bh * sh.NC + c) * M * D;
-    float* RV = a.RV + ((size_t)bh * sh.NC + c) * M * D;
+    float* RK = a.RK + ((size_t)bh * sh.NCS + c) * M * D;
+    float* RV = a.RV + ((size_t)bh * sh.NCS + c) * M * D;
     for (int e = tid; e < M * D; e += kThreads) {
         const int i = e / D, col = e % D;
         float rk = 0.0f, rv = 0.0f;
@@ -633,8 +638,8 @@ __global__ void __launch_bounds__(kThreads) bwd_slot_key_kernel(const BwdArgs a)
     float* sG = sM2 + kChunk * LP;
     float* sER = sG + M;
     float* sEG = sER + M;  // exp(G / 2) = exp(G - rho)
-    const Shape sh = a.sh;
     const int tid = threadIdx.x, s = tid >> 2, tq = tid & 3, bh = blockIdx.y, x = blockIdx.x;
+    const Shape sh = head_shape(a.sh, bh);
     const size_t hoff = (size_t)bh * sh.T;
     const int sbase = x * kChunk, nk = min(kChunk, sh.T - sbase);
     const int nc = (x < sh.NC) ? min(kChunk, sh.R - sbase) : 0;
@@ -646,13 +651,13 @@ __global__ void __launch_bounds__(kThreads) bwd_slot_key_kernel(const BwdArgs a)
         const Tin* k = (const Tin*)a.k + hoff * D;
         const Tin* v = (const Tin*)a.v + hoff * D;
         const Tin* dout = (const Tin*)a.dout + hoff * D;
-        const size_t jrow0 = (size_t)bh * sh.NC * kChunk + sbase;
+        const size_t jrow0 = (size_t)bh * sh.NCS * kChunk + sbase;
         chunk_gates<M>(a.la + (hoff + sbase) * M, nc, sEq, sEk, sFk, LG, sG, sER);
         __syncthreads();
         if (tid < M) sEG[tid] = expf(0.5f * sG[tid]);
         for (int pass = 0; pass < 2; pass++) {
             const float* W = pass == 0 ? a.wsDL : a.wsPL;
-            const float* Rc = (pass == 0 ? a.RK : a.RV) + ((size_t)bh * sh.NC + x) * M * D;
+            const float* Rc = (pass == 0 ? a.RK : a.RV) + ((size_t)bh * sh.NCS + x) * M * D;
             load_rows<Tin, D>(pass == 0 ? q : dout, sbase + sh.w, nc, sA, LX, nullptr);
             load_rows<Tin, D>(pass == 0 ? k : v, sbase, nc, sB, LX, nullptr);
             for (int e = tid; e < M * D; e += kThreads) sRc[(e / D) * LX + e % D] = Rc[e];
@@ -715,14 +720,15 @@ __global__ void __launch_bounds__(kThreads) bwd_slot_key_kernel(const BwdArgs a)
 // thousands of terms whose total is zero.  Grid (NC, BH); one warp per slot.
 template <int M>
 __global__ void __launch_bounds__(kThreads) bwd_dla_carry_kernel(const BwdArgs a, int D) {
-    const Shape sh = a.sh;
     const int c = blockIdx.x, bh = blockIdx.y;
+    const Shape sh = head_shape(a.sh, bh);
+    if (c >= sh.NC) return;  // past this head's chunks (per-head windows)
     const int j0 = c * kChunk, nc = min(kChunk, sh.R - j0);
     __shared__ float carry[64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (c + 1 < sh.NC || a.dhTk != nullptr) {
         // the state after chunk c: the next chunk's entering state, or the final state
-        const size_t cur = ((size_t)bh * sh.NC + c) * M * D;
+        const size_t cur = ((size_t)bh * sh.NCS + c) * M * D;
         const float* SKn = c + 1 < sh.NC ? a.SK + cur + (size_t)M * D : a.io.htf + (size_t)bh * 2 * M * D;
         const float* SVn = c + 1 < sh.NC ? a.SV + cur + (size_t)M * D : a.io.htf + ((size_t)bh * 2 + 1) * M * D;
         for (int i = warp; i < M; i += kThreads / 32) {
@@ -758,16 +764,16 @@ static cudaError_t set_smem(K kernel, size_t bytes) {
 template <typename Tin, int D, int M>
 cudaError_t simt_states(const Tin* k, const Tin* v, const float* la, float* SK, float* SV,
                                float* G, const StateIO& io, const Shape& sh, cudaStream_t st) {
-    if (sh.NC == 0) return launch_final_states_copy(io, sh.BH, M, D, st);
+    if (sh.NCS == 0) return launch_final_states_copy(io, sh.BH, M, D, st);
     constexpr int LX = D + 1, LG = M + 1;
     size_t sm = sizeof(float) * (size_t)(kChunk * LX + 2 * kChunk * LG);
     auto kern = state_chunk_kernel<Tin, D, M>;
     NHA_CHECK(set_smem(kern, sm));
-    NHA_LAUNCH("state_chunk", st, kern<<<dim3(sh.NC, sh.BH), kThreads, sm, st>>>(k, v, la, SK, SV, G, sh));
+    NHA_LAUNCH("state_chunk", st, kern<<<dim3(sh.NCS, sh.BH), kThreads, sm, st>>>(k, v, la, SK, SV, G, sh));
     NHA_CHECK(cudaGetLastError());
     NHA_LAUNCH("state_scan", st,
                state_scan_kernel<<<dim3((M * D + kThreads - 1) / kThreads, sh.BH, 2), kThreads, 0, st>>>(
-                   SK, SV, G, sh.NC, M, D, +1, io.h0k, io.h0v, io.hTk, io.hTv, io.htf));
+                   SK, SV, G, sh, M, D, +1, io.h0k, io.h0v, io.hTk, io.hTv, io.htf));
     return cudaGetLastError();
 }
 
@@ -779,8 +785,9 @@ cudaError_t simt_forward(const FwdArgs& a, cudaStream_t st) {
     size_t sm = sizeof(float) * (size_t)(3 * kChunk * LX + kChunk * LP + 3 * kChunk * LG + 2 * M);
     auto kern = fwd_main_kernel<Tin, D, M>;
     NHA_CHECK(set_smem(kern, sm));
-    if (sh.NL + sh.NC > 0)
-        NHA_LAUNCH("fwd_main", st, kern<<<dim3(sh.NL + sh.NC, sh.BH), kThreads, sm, st>>>(a));
+    // with per-head windows a head has at most ceil(T / C) + 1 tiles
+    const int tiles = sh.windows ? sh.NKT + 1 : sh.NL + sh.NC;
+    if (tiles > 0) NHA_LAUNCH("fwd_main", st, kern<<<dim3(tiles, sh.BH), kThreads, sm, st>>>(a));
     NHA_CHECK(cudaGetLastError());
     return launch_h0_fwd_lead<Tin, D, M>(a, st);  // queries t < w reading initial states
 }
@@ -793,15 +800,15 @@ cudaError_t simt_bwd_slot(const BwdArgs& a, cudaStream_t st) {
         size_t sm = sizeof(float) * (size_t)(4 * kChunk * LX + kChunk * LP + 4 * kChunk * LG + 2 * M);
         auto kern = bwd_slot_query_kernel<Tin, D, M>;
         NHA_CHECK(set_smem(kern, sm));
-        if (sh.NL + sh.NC > 0)
-            NHA_LAUNCH("bwd_slot_query", st, kern<<<dim3(sh.NL + sh.NC, sh.BH), kThreads, sm, st>>>(a));
+        const int tiles = sh.windows ? sh.NKT + 1 : sh.NL + sh.NC;
+        if (tiles > 0) NHA_LAUNCH("bwd_slot_query", st, kern<<<dim3(tiles, sh.BH), kThreads, sm, st>>>(a));
         NHA_CHECK(cudaGetLastError());
         NHA_CHECK(launch_h0_bwd_lead<Tin, D, M>(a, false, st));  // queries t < w reading initial states
     }
-    if (sh.NC > 0) {
+    if (sh.NCS > 0) {
         NHA_LAUNCH("state_scan_rev", st,
                    state_scan_kernel<<<dim3((M * D + kThreads - 1) / kThreads, sh.BH, 2), kThreads, 0, st>>>(
-                       a.RK, a.RV, a.G, sh.NC, M, D, -1, a.dhTk, a.dhTv, nullptr, nullptr, a.rend));
+                       a.RK, a.RV, a.G, sh, M, D, -1, a.dhTk, a.dhTv, nullptr, nullptr, a.rend));
         NHA_CHECK(cudaGetLastError());
     }
     {
@@ -811,8 +818,8 @@ cudaError_t simt_bwd_slot(const BwdArgs& a, cudaStream_t st) {
         NHA_LAUNCH("bwd_slot_key", st, kern<<<dim3(sh.NKT, sh.BH), kThreads, sm, st>>>(a));
         NHA_CHECK(cudaGetLastError());
     }
-    if (sh.NC > 1 || (sh.NC > 0 && a.dhTk != nullptr)) {
-        NHA_LAUNCH("bwd_dla_carry", st, bwd_dla_carry_kernel<M><<<dim3(sh.NC, sh.BH), kThreads, 0, st>>>(a, D));
+    if (sh.NCS > 1 || (sh.NCS > 0 && a.dhTk != nullptr)) {
+        NHA_LAUNCH("bwd_dla_carry", st, bwd_dla_carry_kernel<M><<<dim3(sh.NCS, sh.BH), kThreads, 0, st>>>(a, D));
         NHA_CHECK(cudaGetLastError());
     }
     return launch_dh0<Tin, D, M>(a, st);

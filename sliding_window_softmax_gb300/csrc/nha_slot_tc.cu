@@ -59,11 +59,12 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
-    const Shape sh = a.sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
-    const int W0 = sh.T - sh.R, NLT = (W0 + 127) / 128;
     const int x = blockIdx.x, bh = blockIdx.y;
+    const Shape sh = head_shape(a.sh, bh);
+    const int W0 = sh.T - sh.R, NLT = (W0 + 127) / 128;
+    if (x >= NLT + (sh.R + 127) / 128) return;  // past this head's tiles (per-head windows)
     const size_t hoff = (size_t)bh * sh.T;
     if (x < NLT) {  // window-only queries: D = its window part; dq = window branch only
         const int tb = x * 128, n = min(128, W0 - tb);
@@ -85,7 +86,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
     const int c1 = j0 / kChunk;
     const bool has2 = nq > kChunk, row_ok = r < nq;
     const int t = tbase + r, j = j0 + r;
-    const size_t jrow = (size_t)bh * sh.NC * kChunk + j;
+    const size_t jrow = (size_t)bh * sh.NCS * kChunk + j;
     const float sig = sh.sigma;
 
     if (tid < 2 * M) sG[tid] = 0.0f;
@@ -319,7 +320,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
                 if (cc == 0 || has2) {
                     const int sw = (4 * ch + 4 * (n & 7)) & 31;
                     const float4 val = *reinterpret_cast<const float4*>(slab + arr * 4096 + n * 32 + sw);
-                    float* dst = (arr == 0 ? a.RK : a.RV) + (((size_t)bh * sh.NC + c1 + cc) * M + i) * D + c0 + 4 * ch;
+                    float* dst = (arr == 0 ? a.RK : a.RV) + (((size_t)bh * sh.NCS + c1 + cc) * M + i) * D + c0 + 4 * ch;
                     *reinterpret_cast<float4*>(dst) = val;
                 }
             }
@@ -428,10 +429,10 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
-    const Shape sh = a.sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
     const int x = blockIdx.x, bh = blockIdx.y;
+    const Shape sh = head_shape(a.sh, bh);
     const size_t hoff = (size_t)bh * sh.T;
     const int sbase = x * 128, nk = min(128, sh.T - sbase);
     const int nc = max(0, min(128, sh.R - sbase));
@@ -454,7 +455,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         return;
     }
     const int c1 = sbase / kChunk;
-    const size_t jrow = (size_t)bh * sh.NC * kChunk + s;
+    const size_t jrow = (size_t)bh * sh.NCS * kChunk + s;
 
     if (tid < 2 * M) sG[tid] = 0.0f;
     if (tid == 0) {
@@ -724,10 +725,11 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
     const Shape& sh = a.sh;
     cudaError_t e;
     const int W0 = sh.T - sh.R;
-    const int qtiles = (W0 + 127) / 128 + (sh.R + 127) / 128;
+    // with per-head windows a head has at most ceil(T / 128) + 1 query tiles
+    const int qtiles = sh.windows ? (sh.T + 127) / 128 + 1 : (W0 + 127) / 128 + (sh.R + 127) / 128;
     {
         SqMaps maps;
-        const int ncm = (sh.NC > 0 ? sh.NC : 1) * M;
+        const int ncm = (sh.NCS > 0 ? sh.NCS : 1) * M;
         if ((e = tmap_rows_bf16(&maps.q, a.q, D, sh.T, sh.BH, 128)) != cudaSuccess ||
             (e = tmap_rows_bf16(&maps.dout, a.dout, D, sh.T, sh.BH, 128)) != cudaSuccess ||
             (e = tmap_rows_bf16(&maps.k, a.k, D, sh.T, sh.BH, 128)) != cudaSuccess ||
@@ -756,7 +758,7 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
     if ((e = join_side(st, *f, 3)) != cudaSuccess) return e;
     {
         SkMaps maps;
-        const int ncm = (sh.NC > 0 ? sh.NC : 1) * M;
+        const int ncm = (sh.NCS > 0 ? sh.NCS : 1) * M;
         if ((e = tmap_rows_bf16(&maps.q, a.q, D, sh.T, sh.BH, 128)) != cudaSuccess ||
             (e = tmap_rows_bf16(&maps.dout, a.dout, D, sh.T, sh.BH, 128)) != cudaSuccess ||
             (e = tmap_rows_bf16(&maps.k, a.k, D, sh.T, sh.BH, 128)) != cudaSuccess ||

@@ -29,7 +29,7 @@ namespace nha {
 template <int M>
 __global__ void __launch_bounds__(kTcThreads)
 state_gates_kernel(const __grid_constant__ CUtensorMap la_map, __nv_bfloat16* __restrict__ U,
-                   float* __restrict__ G, Shape sh, int* __restrict__ status) {
+                   float* __restrict__ G, Shape call, int* __restrict__ status) {
     constexpr int HM = M / 2, LAB = ((M + 31) / 32) * 16384;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* XL = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -39,7 +39,10 @@ state_gates_kernel(const __grid_constant__ CUtensorMap la_map, __nv_bfloat16* __
     __shared__ uint64_t gbar;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
-    const int bh = blockIdx.y, j0 = blockIdx.x * 128, n = max(0, min(128, sh.R - j0));
+    const int bh = blockIdx.y, j0 = blockIdx.x * 128;
+    const Shape sh = head_shape(call, bh);
+    if (j0 >= sh.NC * kChunk) return;  // past this head's chunks (per-head windows)
+    const int n = max(0, min(128, sh.R - j0));
     const int rows = min(128, sh.NC * kChunk - j0);  // rows of U this tile defines
     const bool row_ok = r < n;
     if (tid < 2 * M) sG[tid] = 0.0f;
@@ -69,10 +72,10 @@ state_gates_kernel(const __grid_constant__ CUtensorMap la_map, __nv_bfloat16* __
     }
     if (tid < 2 * M) {
         const int cc = tid / M, c = j0 / kChunk + cc;
-        if (c < sh.NC) G[((size_t)bh * sh.NC + c) * M + (tid % M)] = fexp(sG[tid]);  // exp(G_c)
+        if (c < sh.NC) G[((size_t)bh * sh.NCS + c) * M + (tid % M)] = fexp(sG[tid]);  // exp(G_c)
     }
     __syncthreads();
-    __nv_bfloat16* ub = U + ((size_t)bh * sh.NC * kChunk + j0) * 64;
+    __nv_bfloat16* ub = U + ((size_t)bh * sh.NCS * kChunk + j0) * 64;
     for (int e = tid; e < rows * 8; e += kTcThreads) {
         const int rr = e >> 3, ch = e & 7;
         *reinterpret_cast<uint4*>(ub + (size_t)rr * 64 + ch * 8) = *reinterpret_cast<const uint4*>(XU + sw_chunk(rr, ch, 128));
@@ -90,7 +93,7 @@ template <int D, int M>
 __global__ void __launch_bounds__(kScanThreads, 1)
 state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __restrict__ G, float* __restrict__ SK,
                      float* __restrict__ SV, __nv_bfloat16* __restrict__ SKb, __nv_bfloat16* __restrict__ SVb,
-                     const StateIO io, Shape sh, int want_f32, int* __restrict__ status) {
+                     const StateIO io, Shape call, int want_f32, int* __restrict__ status) {
     constexpr int NS = kScanStages;
     constexpr int NSL = M;
     extern __shared__ unsigned char smem_raw[];
@@ -105,7 +108,8 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x, tz = blockIdx.y, i0 = 0;  // tz 0: K, 1: V
-    const int NC = sh.NC;
+    const Shape sh = head_shape(call, bh);
+    const int NC = sh.NC, NCS = sh.NCS;  // this head's chunks; chunks per head in the arrays
     volatile int* abort = &s_abort;
     if (tid == 0) {
         for (int q = 0; q < NS; q++) {
@@ -158,7 +162,7 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
 #pragma unroll
                 for (int x = 0; x < D; x += 64) tma_load_3d(XT(st) + x * 128, &maps.x[tz], x, c * kChunk, bh, &full[st]);
                 tma_load_3d(UT(st), &maps.u, 0, c * kChunk, bh, &full[st]);
-                bulk_load(GS(st), G + ((size_t)bh * NC + c) * M, M * 4, &full[st]);
+                bulk_load(GS(st), G + ((size_t)bh * NCS + c) * M, M * 4, &full[st]);
                 last_ph[st] = (c / NS) & 1;
             };
             for (int c = 0; c < min(NS, NC); c++) load(c);
@@ -171,8 +175,8 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
         // ---------------- state warps: thread = column d ----------------
         const int d = tid;
         const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);
-        __nv_bfloat16* Sb = (tz == 0 ? SKb : SVb) + (size_t)bh * NC * M * D + (size_t)i0 * D + d;
-        float* Sf = (tz == 0 ? SK : SV) + (size_t)bh * NC * M * D + (size_t)i0 * D + d;
+        __nv_bfloat16* Sb = (tz == 0 ? SKb : SVb) + (size_t)bh * NCS * M * D + (size_t)i0 * D + d;
+        float* Sf = (tz == 0 ? SK : SV) + (size_t)bh * NCS * M * D + (size_t)i0 * D + d;
         float S[NSL];  // the state entering chunk c: h0 (or zero) before chunk 0
         {
             const float* h0 = tz == 0 ? io.h0k : io.h0v;
@@ -225,6 +229,12 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
                 if (hT != nullptr) hT[((size_t)bh * M + i) * D + d] = val;
                 if (io.htb != nullptr) io.htb[(((size_t)bh * 2 + tz) * M + i) * D + d] = __float2bfloat16_rn(val);
             }
+            // with per-head windows the arrays hold more chunks than this head
+            // has: the consumers read states in pairs (c, c + 1), so the chunk
+            // after the last one must hold zeros, not stale memory
+            if (NC < NCS)
+#pragma unroll
+                for (int i = 0; i < NSL; i++) Sb[(size_t)NC * M * D + (size_t)i * D] = __float2bfloat16_rn(0.0f);
         }
     }
     fence_before_sync();
@@ -262,20 +272,22 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
                 const __nv_bfloat16* __restrict__ SV, const float* __restrict__ G, __nv_bfloat16* __restrict__ RKb,
                 __nv_bfloat16* __restrict__ RVb, float* __restrict__ db1, const float* __restrict__ dhTk,
                 const float* __restrict__ dhTv, const __nv_bfloat16* __restrict__ htb, float* __restrict__ rend,
-                Shape sh, int M) {
+                Shape call, int M) {
     constexpr int NW = 2 * D / 32, SG = kAdjSlots;
     __shared__ float red[2][NW][SG];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tz = threadIdx.x / D, d = threadIdx.x % D;  // tz 0: K, 1: V
-    const int bh = blockIdx.x, i0 = SG * blockIdx.y, NC = sh.NC;
+    const int bh = blockIdx.x, i0 = SG * blockIdx.y;
+    const Shape sh = head_shape(call, bh);
+    const int NC = sh.NC, NCS = sh.NCS;  // this head's chunks; chunks per head in the arrays
     const float* X = tz == 0 ? RK : RV;
     const __nv_bfloat16* S = tz == 0 ? SK : SV;
     __nv_bfloat16* Xb = tz == 0 ? RKb : RVb;
-    auto at = [&](int c) { return (((size_t)bh * NC + c) * M + i0) * D + d; };
+    auto at = [&](int c) { return (((size_t)bh * NCS + c) * M + i0) * D + d; };
     const float* dh = tz == 0 ? dhTk : dhTv;
     auto load = [&](int c, float (&x)[SG], float (&sp)[SG], float (&g)[SG]) {
         const size_t o = at(c);
-        const float* gc = G + ((size_t)bh * NC + c) * M + i0;
+        const float* gc = G + ((size_t)bh * NCS + c) * M + i0;
 #pragma unroll
         for (int i = 0; i < SG; i++) {
             x[i] = X[o + (size_t)i * D];
@@ -326,7 +338,7 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
             for (int q = 0; q < NW; q++) t += red[parity][q][threadIdx.x];
             // db1 of the chunk's last state row: the in-chunk suffix sum spreads it
             const int last = min(c * kChunk + kChunk, sh.R) - 1;
-            db1[((size_t)bh * NC * kChunk + last) * M + i0 + threadIdx.x] += t;
+            db1[((size_t)bh * NCS * kChunk + last) * M + i0 + threadIdx.x] += t;
         }
         parity ^= 1;
 #pragma unroll
@@ -345,11 +357,16 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
     if (rend != nullptr)  // the adjoint of the state before chunk 0 (part of dh0)
 #pragma unroll
         for (int i = 0; i < SG; i++) rend[(((size_t)bh * 2 + tz) * M + i0 + i) * D + d] = R[i];
+    // per-head windows: zeros after this head's last chunk (read as the pair's
+    // second half by the key-side kernel)
+    if (NC < NCS)
+#pragma unroll
+        for (int i = 0; i < SG; i++) Xb[at(NC) + (size_t)i * D] = __float2bfloat16_rn(0.0f);
 }
 
 cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st) {
     const Shape& sh = a.sh;
-    if (sh.NC == 0) return cudaSuccess;
+    if (sh.NCS == 0) return cudaSuccess;
     const dim3 grid(sh.BH, M / kAdjSlots);
     if (D == 128)
         NHA_LAUNCH("adj_scan", st,
@@ -366,7 +383,7 @@ template <int D, int M>
 cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const float* la, float* SK, float* SV,
                       __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, __nv_bfloat16* U, bool want_f32,
                       const StateIO& io, const Shape& sh, int* status, cudaStream_t st) {
-    if (sh.NC == 0) return launch_final_states_copy(io, sh.BH, M, D, st);
+    if (sh.NCS == 0) return launch_final_states_copy(io, sh.BH, M, D, st);
     CUtensorMap la_map;
     cudaError_t e = tmap_rows_f32(&la_map, la, M, sh.T, sh.BH);
     if (e != cudaSuccess) return e;
@@ -376,13 +393,13 @@ cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const floa
         if ((e = cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsm)) != cudaSuccess)
             return e;
         NHA_LAUNCH("state_gates", st,
-                   gk<<<dim3((sh.NC * kChunk + 127) / 128, sh.BH), kTcThreads, gsm, st>>>(la_map, U, G, sh, status));
+                   gk<<<dim3((sh.NCS * kChunk + 127) / 128, sh.BH), kTcThreads, gsm, st>>>(la_map, U, G, sh, status));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     StateMaps maps;
     if ((e = tmap_rows_bf16(&maps.x[0], k, D, sh.T, sh.BH, 64)) != cudaSuccess ||
         (e = tmap_rows_bf16(&maps.x[1], v, D, sh.T, sh.BH, 64)) != cudaSuccess ||
-        (e = tmap_rows_bf16(&maps.u, U, 64, sh.NC * kChunk, sh.BH, 64)) != cudaSuccess)
+        (e = tmap_rows_bf16(&maps.u, U, 64, sh.NCS * kChunk, sh.BH, 64)) != cudaSuccess)
         return e;
     const size_t sm = 1024 + kScanStages * (16384 + 8192 + 256);
     auto kern = state_scan_tc_kernel<D, M>;
