@@ -174,6 +174,34 @@ nha_status_t nha_backward_ex(const void* q, const void* k, const void* v, const 
                              int C, nha_dtype_t dtype, float rope_base, const nha_extras_t* extras,
                              void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- Segments of one sequence (sequence parallelism) ----
+ *
+ * A sequence cut into segments [a_r, b_r) continues exactly when segment r runs
+ * nha_forward_ex on [the w tokens before a_r; its own tokens] with h0 = the
+ * long memory after token a_r - w - 1, and drops the first w outputs (see
+ * hT above).  That h0 follows from per-segment summaries by an associative
+ * scan: with S_r the final state of segment r's run started from zero states
+ * and A_r the product of the gates of the tokens that left its window,
+ *   h0_{r+1} = A_r o h0_r + S_r   (o: per slot, broadcast over d),
+ * so every segment can form its summary at once and the scan is the only
+ * exchange.  In the backward the state adjoint runs the other way:
+ *   g_r = dh0_r + A_r o g_{r+1},  and segment r's dhT is g_{r+1}.
+ * (The Paper-Notes page, 局限, leaves contexts beyond 128K unvalidated; this is
+ * the exchange a sequence split across ranks needs.) */
+
+/* decay[b,h,i] = exp(sum of log_alpha[b,h,j,i] over j < T - w) (1 when T <= w):
+ * A_r above for a run of T tokens.  log_alpha [B,H,T,m] fp32, decay [B,H,m]
+ * fp32, DEVICE pointers (log_alpha unused when T <= w). */
+nha_status_t nha_gate_total(const float* log_alpha, float* decay, int B, int H, int T, int m, int w,
+                            void* stream);
+
+/* out = decay o prev + cur for the K and V parts ([B,H,m,d] fp32 each, decay
+ * [B,H,m] broadcast over d): one step of the scan above, forward or
+ * backward.  out may be the same arrays as cur. */
+nha_status_t nha_state_combine(const float* decay, const float* prev_k, const float* prev_v,
+                               const float* cur_k, const float* cur_v, float* out_k, float* out_v,
+                               int B, int H, int m, int d, void* stream);
+
 /* ---- Recurrent decode step ----
  *
  * The operator above taken for one new token t of every (b, h) (same page,

@@ -20,6 +20,8 @@ from ._binding import (  # noqa: F401
     nha_decode_step_varlen,
     nha_forward,
     nha_forward_noalloc,
+    nha_gate_total,
+    nha_state_combine,
     nha_workspace_bytes,
     profile_begin,
     profile_end,

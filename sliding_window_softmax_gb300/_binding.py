@@ -27,6 +27,7 @@ DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 # Every symbol include/nha.h declares (checked by the tests).
 EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward",
            "nha_workspace_bytes_ex", "nha_forward_ex", "nha_backward_ex",
+           "nha_gate_total", "nha_state_combine",
            "nha_decode_step", "nha_decode_step_varlen",
            "nha_decode_prefill",
            "nha_forward_noalloc",
@@ -104,6 +105,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.nha_forward_ex.argtypes = [vp] * 6 + [i] * 8 + [f, ep, vp, sz, vp]
         lib.nha_backward_ex.restype = i
         lib.nha_backward_ex.argtypes = [vp] * 11 + [i] * 8 + [f, ep, vp, sz, vp]
+        lib.nha_gate_total.restype = i
+        lib.nha_gate_total.argtypes = [vp, vp] + [i] * 5 + [vp]
+        lib.nha_state_combine.restype = i
+        lib.nha_state_combine.argtypes = [vp] * 7 + [i] * 4 + [vp]
         lib.nha_decode_step.restype = i
         lib.nha_decode_step.argtypes = [vp] * 10 + [i] * 7 + [f, vp]
         lib.nha_decode_step_varlen.restype = i
@@ -413,3 +418,29 @@ def nha_decode_step_varlen(q, k, v, log_alpha, positions, w: int, state, rope_ba
                                     DTYPE[dt], float(rope_base), _stream_handle(stream))
     _raise(lib, rc)
     return o
+
+
+def nha_gate_total(log_alpha, w: int, stream=None):
+    """decay [B,H,m] = exp(sum of log_alpha over the tokens j < T - w): the factor
+    a run of these tokens applies to the state it starts from."""
+    lib = load_library()
+    B, H, T, m = log_alpha.shape
+    _check("log_alpha", log_alpha, torch.float32, (B, H, T, m))
+    decay = torch.empty((B, H, m), dtype=torch.float32, device=log_alpha.device)
+    _raise(lib, lib.nha_gate_total(_ptr(log_alpha), _ptr(decay), B, H, T, m, int(w), _stream_handle(stream)))
+    return decay
+
+
+def nha_state_combine(decay, prev, cur, out=None, stream=None):
+    """(out_k, out_v) = decay o prev + cur for state pairs (K, V) of fp32 [B,H,m,d]."""
+    lib = load_library()
+    B, H, m, d = cur[0].shape
+    _check("decay", decay, torch.float32, (B, H, m))
+    for n, t in (("prev_k", prev[0]), ("prev_v", prev[1]), ("cur_k", cur[0]), ("cur_v", cur[1])):
+        _check(n, t, torch.float32, (B, H, m, d))
+    if out is None:
+        out = (torch.empty_like(cur[0]), torch.empty_like(cur[1]))
+    rc = lib.nha_state_combine(_ptr(decay), _ptr(prev[0]), _ptr(prev[1]), _ptr(cur[0]), _ptr(cur[1]),
+                               _ptr(out[0]), _ptr(out[1]), B, H, m, d, _stream_handle(stream))
+    _raise(lib, rc)
+    return out

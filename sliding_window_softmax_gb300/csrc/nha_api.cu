@@ -548,6 +548,43 @@ nha_status_t nha_decode_prefill(const void* k, const void* v, const float* log_a
     return ok();
 }
 
+nha_status_t nha_gate_total(const float* log_alpha, float* decay, int B, int H, int T, int m, int w, void* stream) {
+    if (inject("validate")) return fail(NHA_ERR_INTERNAL, "fault injected at validate");
+    if (B < 0 || H < 0 || T < 0 || w < 0 || m <= 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "negative or zero size (B=%d H=%d T=%d m=%d w=%d)", B, H, T, m, w);
+    if (m != 16 && m != 32 && m != 64) return fail(NHA_ERR_UNSUPPORTED, "slots m=%d not in {16, 32, 64}", m);
+    if (T > kMaxT) return fail(NHA_ERR_UNSUPPORTED, "T=%d above the supported %d", T, kMaxT);
+    if ((long long)B * H * T * m >= (1LL << 31)) return fail(NHA_ERR_UNSUPPORTED, "B*H*T*m >= 2^31");
+    if ((long long)B * H == 0) return ok();
+    if (decay == nullptr || misaligned(decay)) return fail(NHA_ERR_INVALID_ARGUMENT, "decay is NULL or misaligned");
+    const int R = T > w ? T - w : 0;
+    if (R > 0 && (log_alpha == nullptr || misaligned(log_alpha)))
+        return fail(NHA_ERR_INVALID_ARGUMENT, "log_alpha is NULL or misaligned");
+    cudaError_t e = nha::launch_gate_total(log_alpha, decay, B * H, T, m, R, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "gate_total launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+nha_status_t nha_state_combine(const float* decay, const float* prev_k, const float* prev_v, const float* cur_k,
+                               const float* cur_v, float* out_k, float* out_v, int B, int H, int m, int d,
+                               void* stream) {
+    if (inject("validate")) return fail(NHA_ERR_INTERNAL, "fault injected at validate");
+    if (B < 0 || H < 0 || m <= 0 || d <= 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "negative or zero size (B=%d H=%d m=%d d=%d)", B, H, m, d);
+    if ((long long)B * H * m * d >= (1LL << 31)) return fail(NHA_ERR_UNSUPPORTED, "B*H*m*d >= 2^31");
+    if ((long long)B * H == 0) return ok();
+    const void* ptrs[] = {decay, prev_k, prev_v, cur_k, cur_v, out_k, out_v};
+    const char* names[] = {"decay", "prev_k", "prev_v", "cur_k", "cur_v", "out_k", "out_v"};
+    for (int i = 0; i < 7; i++) {
+        if (ptrs[i] == nullptr) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is NULL", names[i]);
+        if (misaligned(ptrs[i])) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", names[i]);
+    }
+    cudaError_t e = nha::launch_state_combine(decay, prev_k, prev_v, cur_k, cur_v, out_k, out_v, B * H, m, d,
+                                              (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "state_combine launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 const char* nha_status_string(nha_status_t status) {
     switch (status) {
         case NHA_OK: return "NHA_OK";

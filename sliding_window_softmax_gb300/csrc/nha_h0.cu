@@ -252,12 +252,56 @@ dh0_kernel(const BwdArgs a) {
     for (int s = 0; s < 4; s++) out[((size_t)bh * M + i0 + s) * D + d] = acc[s];
 }
 
+// decay[bh][i] = exp(sum of log_alpha[bh][j][i] over j < T - w): the factor the
+// tokens that leave the window apply to the state a segment starts from.
+// Thread = (head, slot), a sequential sum in fp32.
+__global__ void __launch_bounds__(256)
+gate_total_kernel(const float* __restrict__ la, float* __restrict__ decay, int BH, int T, int M, int R) {
+    const long e = (long)blockIdx.x * 256 + threadIdx.x;
+    if (e >= (long)BH * M) return;
+    const long bh = e / M, i = e % M;
+    const float* p = la + (size_t)bh * T * M + i;
+    float s = 0.0f;
+    for (int j = 0; j < R; j++) s += p[(size_t)j * M];
+    decay[e] = expf(s);
+}
+
+// out = decay o prev + cur for K and V (decay [BH][M] broadcast over d); out
+// may be cur.
+__global__ void __launch_bounds__(256)
+state_combine_kernel(const float* __restrict__ decay, const float* __restrict__ pk, const float* __restrict__ pv,
+                     const float* ck, const float* cv, float* ok, float* ov, int BH, int M, int D) {
+    const long e = (long)blockIdx.x * 256 + threadIdx.x;
+    if (e >= (long)BH * M * D) return;
+    const float a = decay[e / D];
+    ok[e] = fmaf(a, pk[e], ck[e]);
+    ov[e] = fmaf(a, pv[e], cv[e]);
+}
+
 template <int D, int M>
 size_t h0_smem(int rowfloats) {
     return sizeof(float) * (size_t)(2 * M * (D + 1) + 8 * rowfloats * D + 8 * M);
 }
 
 }  // namespace
+
+cudaError_t launch_gate_total(const float* la, float* decay, int BH, int T, int M, int R, cudaStream_t st) {
+    const long n = (long)BH * M;
+    if (n == 0) return cudaSuccess;
+    NHA_LAUNCH("gate_total", st,
+               gate_total_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(la, decay, BH, T, M, R));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_combine(const float* decay, const float* pk, const float* pv, const float* ck,
+                                 const float* cv, float* ok, float* ov, int BH, int M, int D, cudaStream_t st) {
+    const long n = (long)BH * M * D;
+    if (n == 0) return cudaSuccess;
+    NHA_LAUNCH("state_combine", st,
+               state_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(decay, pk, pv, ck, cv, ok, ov, BH,
+                                                                                 M, D));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_final_states_copy(const StateIO& io, int BH, int M, int D, cudaStream_t st) {
     if (io.hTk == nullptr && io.hTv == nullptr && io.htb == nullptr && io.htf == nullptr) return cudaSuccess;

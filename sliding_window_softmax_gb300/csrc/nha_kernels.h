@@ -123,6 +123,12 @@ struct BwdArgs {
     RopeTab rope;
 };
 
+// Segment summaries for cutting a sequence into segments: the gate product of
+// the tokens that leave the window (decay [BH][M]) and out = decay o prev + cur.
+cudaError_t launch_gate_total(const float* la, float* decay, int BH, int T, int M, int R, cudaStream_t st);
+cudaError_t launch_state_combine(const float* decay, const float* pk, const float* pv, const float* ck,
+                                 const float* cv, float* ok, float* ov, int BH, int M, int D, cudaStream_t st);
+
 // Initial / final slot states outside the chunk kernels.
 // hT = h0 (or zero) when no token leaves the window (no chunk to scan).
 cudaError_t launch_final_states_copy(const StateIO& io, int BH, int M, int D, cudaStream_t st);
