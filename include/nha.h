@@ -156,7 +156,31 @@ typedef struct {
     float* dh0_k;
     float* dh0_v;
     const int* windows; /* DEVICE [H] int32 per-head windows, or NULL */
+    int* status;        /* DEVICE int32, or NULL: the call's status word (below) */
 } nha_extras_t;
+
+/* Device-side status of a call.  Conditions only the GPU sees cannot be
+ * returned by the call itself (it returns once the work is enqueued), so
+ * every forward / backward keeps a status word: it sets the word to zero on
+ * its stream first, and its kernels OR in these bits.  The word is
+ * extras->status when given (read it after the stream has finished the
+ * call), else a word in the workspace.
+ *   NHA_STATUS_TIMEOUT     a tensor-core kernel's bounded wait on its copies or
+ *                          MMAs gave up (about 2 s); its outputs are NaN or
+ *                          incomplete and the call's results are void.
+ *   NHA_STATUS_GATE_RANGE  the per-slot sum of log_alpha over some chunk of C
+ *                          tokens is below -160, outside the range where the
+ *                          intra-chunk gate factorisation is exact in fp32; the
+ *                          results may hold inf or NaN (see "Numerical range"). */
+#define NHA_STATUS_TIMEOUT 1
+#define NHA_STATUS_GATE_RANGE 2
+
+/* Sets *status (DEVICE int32) to zero, then runs one bounded wait on a
+ * barrier that nothing arrives at, giving up after `cycles` SM clock cycles
+ * (0 < cycles <= 2^32): *status becomes NHA_STATUS_TIMEOUT.  Checks, on the
+ * GPU, the path by which kernels report a wait that ran out, without any
+ * copy or tensor-core work in flight. */
+nha_status_t nha_selftest_wait(int* status, long long cycles, void* stream);
 
 /* Workspace bytes of nha_forward_ex (backward = 0) / nha_backward_ex
  * (backward = 1) with these extras; 0 for an invalid or unsupported shape. */

@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     nha_forward,
     nha_forward_noalloc,
     nha_gate_total,
+    nha_selftest_wait,
     nha_state_combine,
     nha_workspace_bytes,
     profile_begin,

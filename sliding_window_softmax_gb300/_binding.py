@@ -27,7 +27,7 @@ DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 # Every symbol include/nha.h declares (checked by the tests).
 EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward",
            "nha_workspace_bytes_ex", "nha_forward_ex", "nha_backward_ex",
-           "nha_gate_total", "nha_state_combine",
+           "nha_gate_total", "nha_state_combine", "nha_selftest_wait",
            "nha_decode_step", "nha_decode_step_varlen",
            "nha_decode_prefill",
            "nha_forward_noalloc",
@@ -44,7 +44,7 @@ class Extras(ctypes.Structure):
                 ("hT_k", ctypes.c_void_p), ("hT_v", ctypes.c_void_p),
                 ("dhT_k", ctypes.c_void_p), ("dhT_v", ctypes.c_void_p),
                 ("dh0_k", ctypes.c_void_p), ("dh0_v", ctypes.c_void_p),
-                ("windows", ctypes.c_void_p)]
+                ("windows", ctypes.c_void_p), ("status", ctypes.c_void_p)]
 
 
 class ProfileRecord(ctypes.Structure):
@@ -105,6 +105,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.nha_forward_ex.argtypes = [vp] * 6 + [i] * 8 + [f, ep, vp, sz, vp]
         lib.nha_backward_ex.restype = i
         lib.nha_backward_ex.argtypes = [vp] * 11 + [i] * 8 + [f, ep, vp, sz, vp]
+        lib.nha_selftest_wait.restype = i
+        lib.nha_selftest_wait.argtypes = [vp, ctypes.c_longlong, vp]
         lib.nha_gate_total.restype = i
         lib.nha_gate_total.argtypes = [vp, vp] + [i] * 5 + [vp]
         lib.nha_state_combine.restype = i
@@ -182,7 +184,8 @@ def nha_workspace_bytes(B, H, T, d, m, w, C=64, dtype=torch.bfloat16, backward=F
 
 
 def nha_forward(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 10000.0,
-                o=None, lse=None, workspace=None, stream=None, h0=None, return_state=False, windows=None):
+                o=None, lse=None, workspace=None, stream=None, h0=None, return_state=False, windows=None,
+                status=None):
     """o, lse = nha_forward(q, k, v, log_alpha, w).  q, k, v [B,H,T,d]; log_alpha [B,H,T,m] fp32.
 
     ``h0`` = (h0k, h0v): initial slot states, fp32 [B,H,m,d] each.  With
@@ -212,7 +215,7 @@ def nha_forward(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 1000
     if return_state:
         hT = (torch.empty((B, H, m, d), dtype=torch.float32, device=q.device),
               torch.empty((B, H, m, d), dtype=torch.float32, device=q.device))
-    ex = _extras(shape=(B, H, m, d), windows=windows, h0=h0, hT=hT)
+    ex = _extras(shape=(B, H, m, d), windows=windows, status=status, h0=h0, hT=hT)
     rc = lib.nha_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(lse),
                             B, H, T, d, m, int(w), int(C), DTYPE[dt], float(rope_base), ctypes.byref(ex),
                             _ptr(workspace), ws_bytes, _stream_handle(stream))
@@ -246,11 +249,18 @@ def nha_forward_noalloc(q, k, v, log_alpha, w: int, C: int = 64, rope_base: floa
     return o, lse
 
 
-def _extras(fwd_workspace=None, shape=None, windows=None, **states):
+STATUS_TIMEOUT = 1      # NHA_STATUS_TIMEOUT
+STATUS_GATE_RANGE = 2   # NHA_STATUS_GATE_RANGE
+
+
+def _extras(fwd_workspace=None, shape=None, windows=None, status=None, **states):
     """Extras from tensors: fwd_workspace, windows (int32 CUDA [H]), and state
     pairs given as (K, V) tuples of fp32 [B,H,m,d] CUDA tensors under the names
     h0, hT, dhT, dh0."""
     ex = Extras()
+    if status is not None:
+        _check("status", status, torch.int32, (1,))
+        ex.status = status.data_ptr()
     if windows is not None:
         _check("windows", windows, torch.int32, (shape[1],) if shape is not None else None)
         ex.windows = windows.data_ptr()
@@ -271,7 +281,8 @@ def _extras(fwd_workspace=None, shape=None, windows=None, **states):
 
 def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
                  rope_base: float = 10000.0, dq=None, dk=None, dv=None, dlog_alpha=None,
-                 workspace=None, stream=None, fwd_workspace=None, h0=None, dhT=None, windows=None):
+                 workspace=None, stream=None, fwd_workspace=None, h0=None, dhT=None, windows=None,
+                 status=None):
     """dq, dk, dv, dlog_alpha = nha_backward(q, k, v, log_alpha, o, lse, dout, w).
 
     ``fwd_workspace``: the workspace tensor the forward of these inputs ran
@@ -300,7 +311,7 @@ def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
     if h0 is not None:
         dh0 = (torch.empty((B, H, m, d), dtype=torch.float32, device=q.device),
                torch.empty((B, H, m, d), dtype=torch.float32, device=q.device))
-    ex = _extras(fwd_workspace, shape=(B, H, m, d), windows=windows, h0=h0, dhT=dhT, dh0=dh0)
+    ex = _extras(fwd_workspace, shape=(B, H, m, d), windows=windows, status=status, h0=h0, dhT=dhT, dh0=dh0)
     need = int(lib.nha_workspace_bytes_ex(B, H, T, d, m, w, C, DTYPE[dt], 1, ctypes.byref(ex)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -444,3 +455,14 @@ def nha_state_combine(decay, prev, cur, out=None, stream=None):
                                _ptr(out[0]), _ptr(out[1]), B, H, m, d, _stream_handle(stream))
     _raise(lib, rc)
     return out
+
+
+def nha_selftest_wait(cycles: int, status=None, stream=None):
+    """Runs one bounded wait that runs out after ``cycles`` SM clocks; returns the
+    status word (int32 CUDA tensor [1]), NHA_STATUS_TIMEOUT once it has run."""
+    lib = load_library()
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device="cuda")
+    _check("status", status, torch.int32, (1,))
+    _raise(lib, lib.nha_selftest_wait(_ptr(status), int(cycles), _stream_handle(stream)))
+    return status

@@ -84,6 +84,7 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward, bool reu
     sh.W0S = T - sh.R;
     sh.windows = nullptr;
     sh.H = H;
+    sh.status = nullptr;
     size_t off = 0;
     auto take = [&](size_t n) {
         size_t o = off;
@@ -172,6 +173,8 @@ nha_status_t check_extras(const nha_extras_t* ex, bool backward) {
         return fail(NHA_ERR_INVALID_ARGUMENT, "dh0 needs h0 (the gradient of an input that is not given)");
     if (ex->windows != nullptr && ((uintptr_t)ex->windows & 3u) != 0)
         return fail(NHA_ERR_INVALID_ARGUMENT, "windows array is not 4-byte aligned");
+    if (ex->status != nullptr && ((uintptr_t)ex->status & 3u) != 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "status is not 4-byte aligned");
     return NHA_OK;
 }
 
@@ -192,7 +195,7 @@ nha::StateIO state_io(const nha_extras_t* ex, bool forward) {
 
 cudaError_t run_forward_tc(const Plan& p, const nha::FwdArgs& a, float* ws, cudaStream_t s) {
     float2* tab = (float2*)(ws + p.TAB);
-    int* status = (int*)(ws + p.STATUS);
+    int* status = a.sh.status;
     __nv_bfloat16* qr = (__nv_bfloat16*)(ws + p.QR);
     __nv_bfloat16* kr = (__nv_bfloat16*)(ws + p.KR);
     switch (p.d * 1000 + p.m) {
@@ -224,7 +227,7 @@ cudaError_t run_forward(const Plan& p, const nha::FwdArgs& a, cudaStream_t s) {
 cudaError_t run_backward_tc(const Plan& p, const nha::BwdArgs& a, float* ws, const Plan& fp, float* fws,
                             cudaStream_t s) {
     float2* tab = (float2*)(fws + fp.TAB);
-    int* status = (int*)(ws + p.STATUS);
+    int* status = a.sh.status;
     __nv_bfloat16* qr = (__nv_bfloat16*)(fws + fp.QR);
     __nv_bfloat16* kr = (__nv_bfloat16*)(fws + fp.KR);
     switch (p.d * 1000 + p.m) {
@@ -333,9 +336,12 @@ nha_status_t nha_forward_ex(const void* q, const void* k, const void* v, const f
     a.io.htf = ws + p.HTF;
     a.sh = p.sh;
     a.sh.windows = per_head(ex) ? ex->windows : nullptr;
+    a.sh.status = (ex != nullptr && ex->status != nullptr) ? ex->status : (int*)(ws + p.STATUS);
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = dtype == NHA_DTYPE_F32 ? run_forward<float>(p, a, s) : run_forward_tc(p, a, ws, s);
+    cudaError_t e = cudaMemsetAsync(a.sh.status, 0, sizeof(int), s);
+    if (e == cudaSuccess)
+        e = dtype == NHA_DTYPE_F32 ? run_forward<float>(p, a, s) : run_forward_tc(p, a, ws, s);
     if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "forward launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -405,9 +411,12 @@ nha_status_t nha_backward_ex(const void* q, const void* k, const void* v, const 
     a.lpl = ws + p.LPL;
     a.sh = p.sh;
     a.sh.windows = per_head(ex) ? ex->windows : nullptr;
+    a.sh.status = (ex != nullptr && ex->status != nullptr) ? ex->status : (int*)(ws + p.STATUS);
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = dtype == NHA_DTYPE_F32 ? run_backward<float>(p, a, s) : run_backward_tc(p, a, ws, fp, fws, s);
+    cudaError_t e = cudaMemsetAsync(a.sh.status, 0, sizeof(int), s);
+    if (e == cudaSuccess)
+        e = dtype == NHA_DTYPE_F32 ? run_backward<float>(p, a, s) : run_backward_tc(p, a, ws, fp, fws, s);
     if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "backward launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -582,6 +591,18 @@ nha_status_t nha_state_combine(const float* decay, const float* prev_k, const fl
     cudaError_t e = nha::launch_state_combine(decay, prev_k, prev_v, cur_k, cur_v, out_k, out_v, B * H, m, d,
                                               (cudaStream_t)stream);
     if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "state_combine launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+nha_status_t nha_selftest_wait(int* status, long long cycles, void* stream) {
+    if (status == nullptr || ((uintptr_t)status & 3u) != 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "status is NULL or not 4-byte aligned");
+    if (cycles <= 0 || cycles > (1LL << 32))
+        return fail(NHA_ERR_INVALID_ARGUMENT, "cycles=%lld outside (0, 2^32]", cycles);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = nha::launch_selftest_wait(status, cycles, s);
+    if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "selftest launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
 

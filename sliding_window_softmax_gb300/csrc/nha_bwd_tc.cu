@@ -309,7 +309,7 @@ bwd_wdq_tc_kernel(const BwdArgs a, const __grid_constant__ WdqMaps maps, int* __
             if (tab_issued) mbar_wait(&tbar, 0, kWaitCycles);
         }
         __syncthreads();
-        if (tid == 0) atomicExch(status, kStatusTimeout);
+        if (tid == 0) atomicOr(status, kStatusTimeoutBit);
     }
     if (warp == 0) tmem_dealloc(tm, 512);
 }
@@ -597,7 +597,7 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, int* __
             cp_async_wait_all();
         }
         __syncthreads();
-        if (tid == 0) atomicExch(status, kStatusTimeout);
+        if (tid == 0) atomicOr(status, kStatusTimeoutBit);
     }
     if (warp == 0) tmem_dealloc(tm, 512);
 }

@@ -44,7 +44,15 @@ struct Shape {
     // min(max(windows[h], 0), w); w above is then the largest window.
     const int* windows;
     int H;
+    // The call's status word (device int): kernels OR in kStatus* bits for
+    // conditions only the device sees; the call sets it to zero first.
+    int* status;
 };
+
+// Status bits (include/nha.h: NHA_STATUS_*).
+constexpr int kStatusTimeoutBit = 1;    // a bounded wait gave up; the results are void
+constexpr int kStatusGateRangeBit = 2;  // a chunk's per-slot log_alpha sum fell below kGateRange
+constexpr float kGateRange = -160.0f;   // the intra-chunk gate factorisation is exact in fp32 above it
 
 // The shape seen by head bh: its own window and the counts that follow from
 // it (the layout fields NCS, W0S are the call's).

@@ -450,7 +450,7 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
                 if (last_ph[q] >= 0) mbar_wait(&full[q], (uint32_t)last_ph[q], kWaitCycles);
         }
         __syncthreads();
-        if (tid == 0) atomicExch(status, kStatusTimeout);
+        if (tid == 0) atomicOr(status, kStatusTimeoutBit);
     }
     if (warp == 0) tmem_dealloc(tm, 512);
 }

@@ -16,6 +16,7 @@
 #include "nha_common.cuh"
 #include "nha_kernels.h"
 #include "nha_prof.h"
+#include "nha_tc.cuh"
 
 namespace nha {
 
@@ -278,12 +279,29 @@ state_combine_kernel(const float* __restrict__ decay, const float* __restrict__ 
     ov[e] = fmaf(a, pv[e], cv[e]);
 }
 
+// A bounded wait on an mbarrier that nothing arrives at: it gives up after
+// `cycles` SM clock cycles and reports it in the status word, the way every
+// tensor-core kernel reports a wait that ran out.  One thread, no copies or
+// tensor-core work in flight.
+__global__ void selftest_wait_kernel(int* status, long long cycles) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    tc::mbar_init(&bar, 1);
+    tc::mbar_fence_init();
+    if (!tc::mbar_wait(&bar, 0, cycles)) atomicOr(status, kStatusTimeoutBit);
+}
+
 template <int D, int M>
 size_t h0_smem(int rowfloats) {
     return sizeof(float) * (size_t)(2 * M * (D + 1) + 8 * rowfloats * D + 8 * M);
 }
 
 }  // namespace
+
+cudaError_t launch_selftest_wait(int* status, long long cycles, cudaStream_t st) {
+    NHA_LAUNCH("selftest_wait", st, selftest_wait_kernel<<<1, 32, 0, st>>>(status, cycles));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gate_total(const float* la, float* decay, int BH, int T, int M, int R, cudaStream_t st) {
     const long n = (long)BH * M;

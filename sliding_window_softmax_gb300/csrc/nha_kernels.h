@@ -123,6 +123,9 @@ struct BwdArgs {
     RopeTab rope;
 };
 
+// A wait that runs out on purpose (status word check).
+cudaError_t launch_selftest_wait(int* status, long long cycles, cudaStream_t st);
+
 // Segment summaries for cutting a sequence into segments: the gate product of
 // the tokens that leave the window (decay [BH][M]) and out = decay o prev + cur.
 cudaError_t launch_gate_total(const float* la, float* decay, int BH, int T, int M, int R, cudaStream_t st);

@@ -53,6 +53,7 @@ state_chunk_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
         for (int r = 0; r < kChunk; r++)
             sCoef[r * LG + tid] = (r < nc) ? expf(b - sCoef[r * LG + tid]) * sU[r * LG + tid] : 0.0f;
         G[((size_t)bh * sh.NCS + c) * M + tid] = b;
+        if (b < kGateRange && sh.status != nullptr) atomicOr(sh.status, kStatusGateRangeBit);
     }
     for (int pass = 0; pass < 2; pass++) {
         const Tin* src = (pass == 0 ? k : v) + row0 * D;

@@ -397,7 +397,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
         for (int q = l_waited; q < l_issued; q++) mbar_wait(&lbar, (uint32_t)(q & 1), kWaitCycles);
         for (int q = e_waited; q < e_issued; q++) mbar_wait(&ebar[q], 0, kWaitCycles);
         if (g_issued && !g_waited) mbar_wait(&gbar, 0, kWaitCycles);
-        atomicExch(status, kStatusTimeout);
+        atomicOr(status, kStatusTimeoutBit);
     }
     fence_before_sync();
     __syncthreads();
@@ -701,7 +701,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         for (int q = e_waited; q < e_issued; q++) mbar_wait(&ebar, (uint32_t)(q & 1), kWaitCycles);
         if (d_issued) mbar_wait(&dbar, 0, kWaitCycles);
         if (g_issued && !g_waited) mbar_wait(&gbar, 0, kWaitCycles);
-        atomicExch(status, kStatusTimeout);
+        atomicOr(status, kStatusTimeoutBit);
     }
     fence_before_sync();
     __syncthreads();

@@ -57,7 +57,7 @@ state_gates_kernel(const __grid_constant__ CUtensorMap la_map, __nv_bfloat16* __
         for (int xx = 0; xx < M; xx += 32) tma_load_3d(XL + xx * 512, &la_map, xx, j0, bh, &gbar);
     }
     if (!mbar_wait(&gbar, 0, kWaitCycles)) {
-        if (tid == 0) atomicExch(status, kStatusTimeout);
+        if (tid == 0) atomicOr(status, kStatusTimeoutBit);
         mbar_wait(&gbar, 0, kWaitCycles);  // let the copy land before the CTA leaves
         return;
     }
@@ -72,7 +72,10 @@ state_gates_kernel(const __grid_constant__ CUtensorMap la_map, __nv_bfloat16* __
     }
     if (tid < 2 * M) {
         const int cc = tid / M, c = j0 / kChunk + cc;
-        if (c < sh.NC) G[((size_t)bh * sh.NCS + c) * M + (tid % M)] = fexp(sG[tid]);  // exp(G_c)
+        if (c < sh.NC) {
+            G[((size_t)bh * sh.NCS + c) * M + (tid % M)] = fexp(sG[tid]);  // exp(G_c)
+            if (sG[tid] < kGateRange) atomicOr(status, kStatusGateRangeBit);
+        }
     }
     __syncthreads();
     __nv_bfloat16* ub = U + ((size_t)bh * sh.NCS * kChunk + j0) * 64;
@@ -248,7 +251,7 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
             for (int q = 0; q < NS; q++)
                 if (last_ph[q] >= 0) mbar_wait(&full[q], (uint32_t)last_ph[q], kWaitCycles);
         __syncthreads();
-        if (tid == 0) atomicExch(status, kStatusTimeout);
+        if (tid == 0) atomicOr(status, kStatusTimeoutBit);
     }
     if (warp == 0) tmem_dealloc(tm, 128);
 }

@@ -12,7 +12,6 @@ constexpr int kTcThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr long long kWaitCycles = 1LL << 32;  // about 2 s at 2 GHz
-constexpr int kStatusTimeout = 1;
 
 __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -86,7 +85,7 @@ struct TcCtl {
         phase ^= 1u;
         fence_after_sync();
         if (named ? named_sync_or(1, kTcThreads, !ok) : __syncthreads_or(!ok)) {
-            if (threadIdx.x == 0) atomicExch(status, kStatusTimeout);
+            if (threadIdx.x == 0) atomicOr(status, kStatusTimeoutBit);
             return false;
         }
         return true;

@@ -295,3 +295,11 @@ def test_extended_calls_validate_state_pointers(lib):
     ex = _binding.Extras()
     ex.hT_k = ex.hT_v = 4096  # a forward output given to the backward
     assert lib.nha_backward_ex(*bargs, ctypes.byref(ex), p, 1 << 30, None) == 1
+
+
+def test_selftest_wait_validates(lib):
+    p = ctypes.c_void_p(4096)
+    assert lib.nha_selftest_wait(None, 1000, None) == 1
+    assert lib.nha_selftest_wait(ctypes.c_void_p(4098), 1000, None) == 1
+    assert lib.nha_selftest_wait(p, 0, None) == 1
+    assert lib.nha_selftest_wait(p, (1 << 32) + 1, None) == 1

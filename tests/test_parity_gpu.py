@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from sliding_window_softmax_gb300.synthetic import (GRID_M, GRID_W, LAYER_1P3B, LAYER_340M,
-                                                    TINY_F32, Workload, grid_point,
+                                                    LONG_CONTEXT_T, TINY_F32, Workload, grid_point,
                                                     long_context, make_inputs)
 
 pytestmark = pytest.mark.gpu
@@ -188,7 +188,7 @@ def test_layer_workloads(wl):
     assert_parity(pick(gpu, heads), run_oracle(x, wl.w, heads=heads), wl.dtype, tag=wl.name)
 
 
-@pytest.mark.parametrize("T", [4096, 65536])
+@pytest.mark.parametrize("T", LONG_CONTEXT_T)
 def test_long_context_forward(T):
     wl = long_context(T)
     x = make_inputs(wl)
@@ -201,9 +201,19 @@ def test_long_context_forward(T):
 @pytest.mark.parametrize("w", GRID_W)
 @pytest.mark.parametrize("m", GRID_M)
 def test_window_slot_grid(w, m):
+    """Forward and backward at every grid point; one whole head (at w = 8192 the
+    oracle's backward of one head is a full causal attention over 8192 tokens)."""
     wl = grid_point(w, m)
     x = make_inputs(wl)
-    gpu = run_gpu(x, wl.w, backward=w <= 1024)
+    gpu = run_gpu(x, wl.w)
     heads = [(1, 15)]
-    ref = run_oracle(x, wl.w, backward=w <= 1024, heads=heads)
+    ref = run_oracle(x, wl.w, heads=heads)
     assert_parity(pick(gpu, heads), ref, "bf16", tag=wl.name)
+
+
+def test_layer_1p3b_every_head():
+    """The 1.3B-like layer (B4 H16 T2048 d128 m64 w512, bf16): all 64 heads,
+    forward and backward, element by element."""
+    wl = LAYER_1P3B
+    x = make_inputs(wl)
+    assert_parity(run_gpu(x, wl.w), run_oracle(x, wl.w), "bf16", tag=wl.name + " all heads")
