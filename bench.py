@@ -91,10 +91,10 @@ def work_model(wl):
         # (bf16) and SIMT (fp32) kernels of the same step share a model
         "fwd_tc": fwd_main, "fwd_main": fwd_main,
         "state_chunk": (BH * 4 * m * d * R, BH * R * (2 * d * e + 4 * m)),
-        # bf16 path: chunk coefficients (log_alpha in, U and G out), then the
-        # fused chunk scan (K, V, U in; the bf16 states entering each chunk out)
-        "state_gates": (0, BH * R * (4 * m + 128)),
-        "state_scan": (BH * 4 * m * d * R, BH * R * (2 * d * e + 128) + BH * ((R + 63) // 64) * 4 * m * d),
+        # bf16 path: the chunk scan with the chunk coefficients formed inside
+        # (K, V in; log_alpha in by the K and the V CTA; the bf16 states
+        # entering each chunk out)
+        "state_scan": (BH * 4 * m * d * R, BH * R * (2 * d * e + 8 * m) + BH * ((R + 63) // 64) * 4 * m * d),
         # reverse adjoint scan + carry: fp32 contributions and bf16 states in,
         # bf16 adjoints out, K and V
         "adj_scan": (0, BH * ((R + 63) // 64) * m * d * 16),
@@ -501,10 +501,13 @@ def run_nha(args, wl, wl_key):
     wall0 = time.perf_counter()
     t_start = time.time()
     n0 = nha.launch_count()
+    enq = 0.0  # host time spent enqueuing the steps (argument checks, tensor maps, launches)
     for i in range(K):
         flush.zero_()  # L2 flush between timed steps, outside the step's events
         ev[i][0].record(stream)
+        h0 = time.perf_counter()
         step(ev[i][1])
+        enq += time.perf_counter() - h0
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     launches = nha.launch_count() - n0
@@ -635,6 +638,7 @@ def run_nha(args, wl, wl_key):
                     "ms_per_step": e2e_ms},
             "clocks": clk.summary(),
             "wall_s_timed_region": wall,
+            "host_enqueue_ms_per_step": 1e3 * enq / K,
         }
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl)

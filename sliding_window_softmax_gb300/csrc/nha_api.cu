@@ -42,7 +42,7 @@ struct Plan {
     nha::Shape sh;
     int d, m;
     // workspace offsets, in floats
-    size_t SK, SV, SKb, SVb, G, U, TAB, STATUS, QR, KR, HTB, HTF, Dv, Dhat, Dwin, dqwV, dqw, dkw, dvw, DL, PL, DB1, RK,
+    size_t SK, SV, SKb, SVb, G, TAB, STATUS, QR, KR, HTB, HTF, Dv, Dhat, Dwin, dqwV, dqw, dkw, dvw, DL, PL, DB1, RK,
         RV, RKb, RVb, REND, LDL, LPL, total;
 };
 
@@ -99,7 +99,6 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward, bool reu
         p.SKb = take(BH * NC * m * d / 2);
         p.SVb = take(BH * NC * m * d / 2);
         p.G = take(BH * NC * m);
-        p.U = take(BH * NC * nha::kChunk * 64 / 2);  // chunk coefficients, bf16 [BH][NC * C][64]
         p.TAB = take(Tz * (size_t)d);  // RoPE (cos, sin) per position and frequency
         p.QR = take(BH * Tz * d / 2);  // RoPE(q), bf16
         p.KR = take(BH * Tz * d / 2);  // RoPE(k), bf16
@@ -330,7 +329,6 @@ nha_status_t nha_forward_ex(const void* q, const void* k, const void* v, const f
     a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.o = o; a.lse = lse;
     a.SK = ws + p.SK; a.SV = ws + p.SV; a.G = ws + p.G;
     a.SKb = (__nv_bfloat16*)(ws + p.SKb); a.SVb = (__nv_bfloat16*)(ws + p.SVb);
-    a.U = (__nv_bfloat16*)(ws + p.U);
     a.io = state_io(ex, true);
     a.io.htb = (__nv_bfloat16*)(ws + p.HTB);
     a.io.htf = ws + p.HTF;
@@ -393,7 +391,6 @@ nha_status_t nha_backward_ex(const void* q, const void* k, const void* v, const 
     a.wsDL = ws + p.DL; a.wsPL = ws + p.PL; a.wsDB1 = ws + p.DB1;
     a.RK = ws + p.RK; a.RV = ws + p.RV;
     a.SKb = (__nv_bfloat16*)(fws + fp.SKb); a.SVb = (__nv_bfloat16*)(fws + fp.SVb);
-    a.U = (__nv_bfloat16*)(fws + fp.U);
     a.RKb = (__nv_bfloat16*)(ws + p.RKb); a.RVb = (__nv_bfloat16*)(ws + p.RVb);
     a.hdqw = (__nv_bfloat16*)a.dqw; a.hdqwV = (__nv_bfloat16*)a.dqwV;
     a.hdkw = (__nv_bfloat16*)a.dkw; a.hdvw = (__nv_bfloat16*)a.dvw;

@@ -625,7 +625,7 @@ cudaError_t tc_backward(const BwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_b
             if ((e = launch_rope_qk<D>(a.q, a.k, qr, kr, tab, a.rope, sh, f->side)) != cudaSuccess) return e;
         }
         e = tc_states<D, M>((const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, a.la, a.SK, a.SV, a.SKb, a.SVb,
-                            a.G, a.U, false, a.io, sh, status, st);
+                            a.G, false, a.io, sh, status, st);
         if (e != cudaSuccess) return e;
         if (sh.w > 0 && (e = join_side(st, *f, 1)) != cudaSuccess) return e;
     }

@@ -53,7 +53,6 @@ struct FwdArgs {
     float* G;
     __nv_bfloat16* SKb;  // bf16 copies of SK, SV (bf16 path)
     __nv_bfloat16* SVb;
-    __nv_bfloat16* U;    // chunk coefficients (bf16 path)
     StateIO io;
     Shape sh;
     RopeTab rope;
@@ -93,7 +92,6 @@ struct BwdArgs {
     __nv_bfloat16* SVb;
     __nv_bfloat16* RKb;
     __nv_bfloat16* RVb;
-    __nv_bfloat16* U;  // chunk coefficients (bf16 path)
     // bf16 path: the window partials and sigma dL, P_L are kept in bf16 (they
     // alias the storage of the fp32 arrays above)
     __nv_bfloat16* hdqw;
@@ -184,12 +182,11 @@ cudaError_t launch_wkv(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bfl
 // bf16 path: reverse adjoint scan (RK, RV contributions in; RKb, RVb out) and
 // the per-chunk dlog_alpha carry, added to wsDB1 of each chunk's last state row.
 cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st);
-// bf16 path: chunk coefficients U (workspace, [BH][NC * C][64] bf16) and chunk
-// decays exp(G) (into G), then the states entering every chunk in bf16 (and
-// fp32 if want_f32).
+// bf16 path: the chunk decays exp(G) (into G) and the states entering every
+// chunk in bf16 (and fp32 if want_f32), the chunk coefficients formed on chip.
 template <int D, int M>
 cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const float* la, float* SK, float* SV,
-                      __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, __nv_bfloat16* U, bool want_f32,
+                      __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, bool want_f32,
                       const StateIO& io, const Shape& sh, int* status, cudaStream_t st);
 
 }  // namespace nha

@@ -7,14 +7,14 @@
 // unrolled over one chunk), for X = K and X = V, and the states entering the
 // chunks follow S_prev(c + 1) = exp(G_c) S_prev(c) + dS_c.
 //
-// Two kernels.  state_gates: every chunk in parallel, the coefficients U
-// (bf16, 64 columns, slots past m zero) and the chunk decays exp(G) (the array
-// named G holds exp(G_c) on this path: the scans use nothing else of it).  state_scan:
-// one CTA per (head, K or V) walks the chunks in order: one warp streams X_c
-// and U_c through TMA stages, one forms dS_c^T = X_c^T U_c on the tensor core
-// into one of two TMEM buffers as soon as a chunk has landed, and four warps
-// (thread = one column d of the state) carry the state in fp32 registers and
-// write S_prev(c).
+// One kernel, state_scan: one CTA per (head, K or V) walks the chunks in
+// order.  A copy warp streams X_c and the chunk's log_alpha rows through
+// shared-memory stages; eight gate warps form U_c (bf16, 64 columns, slots
+// past m zero) and exp(G_c) from the log_alpha rows (the array named G holds
+// exp(G_c) on this path: the scans use nothing else of it); one warp forms
+// dS_c^T = X_c^T U_c on the tensor core into one of two TMEM buffers; four
+// warps (thread = one column d of the state) carry the state in fp32
+// registers and write S_prev(c).
 #include "nha_common.cuh"
 #include "nha_kernels.h"
 #include "nha_prof.h"
@@ -24,88 +24,38 @@
 
 namespace nha {
 
-// U row j (64 bf16) and G of the two chunks of a 128-row tile: log_alpha of
-// the tile by TMA, U staged in shared memory and copied out coalesced.
-template <int M>
-__global__ void __launch_bounds__(kTcThreads)
-state_gates_kernel(const __grid_constant__ CUtensorMap la_map, __nv_bfloat16* __restrict__ U,
-                   float* __restrict__ G, Shape call, int* __restrict__ status) {
-    constexpr int HM = M / 2, LAB = ((M + 31) / 32) * 16384;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* XL = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char* XU = XL + LAB;  // [128][64] bf16, 128-byte swizzled rows
-    __shared__ float s_tot[4 * M];
-    __shared__ float sG[2 * M];
-    __shared__ uint64_t gbar;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
-    const int bh = blockIdx.y, j0 = blockIdx.x * 128;
-    const Shape sh = head_shape(call, bh);
-    if (j0 >= sh.NC * kChunk) return;  // past this head's chunks (per-head windows)
-    const int n = max(0, min(128, sh.R - j0));
-    const int rows = min(128, sh.NC * kChunk - j0);  // rows of U this tile defines
-    const bool row_ok = r < n;
-    if (tid < 2 * M) sG[tid] = 0.0f;
-    if (tid == 0) {
-        mbar_init(&gbar, 1);
-        mbar_fence_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&gbar, LAB);
-#pragma unroll
-        for (int xx = 0; xx < M; xx += 32) tma_load_3d(XL + xx * 512, &la_map, xx, j0, bh, &gbar);
-    }
-    if (!mbar_wait(&gbar, 0, kWaitCycles)) {
-        if (tid == 0) atomicOr(status, kStatusTimeoutBit);
-        mbar_wait(&gbar, 0, kWaitCycles);  // let the copy land before the CTA leaves
-        return;
-    }
-    float l[HM], b[HM];
-    row_gates_tile<M>(XL, row_ok, l, b, s_tot, sG, warp, lane, h, r, n);
-    {
-        float u[HM];
-#pragma unroll
-        for (int jj = 0; jj < HM; jj++) u[jj] = row_ok ? fexp(sG[cr * M + h * HM + jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
-        store_row(XU, r, h * HM, u, HM);
-        if (M < 64) zero_cols(XU, r, M + h * (64 - M) / 2, M + (h + 1) * (64 - M) / 2);
-    }
-    if (tid < 2 * M) {
-        const int cc = tid / M, c = j0 / kChunk + cc;
-        if (c < sh.NC) {
-            G[((size_t)bh * sh.NCS + c) * M + (tid % M)] = fexp(sG[tid]);  // exp(G_c)
-            if (sG[tid] < kGateRange) atomicOr(status, kStatusGateRangeBit);
-        }
-    }
-    __syncthreads();
-    __nv_bfloat16* ub = U + ((size_t)bh * sh.NCS * kChunk + j0) * 64;
-    for (int e = tid; e < rows * 8; e += kTcThreads) {
-        const int rr = e >> 3, ch = e & 7;
-        *reinterpret_cast<uint4*>(ub + (size_t)rr * 64 + ch * 8) = *reinterpret_cast<const uint4*>(XU + sw_chunk(rr, ch, 128));
-    }
-}
-
-constexpr int kScanThreads = 192, kScanStages = 4;  // 4 state warps, MMA warp, copy warp
+constexpr int kScanThreads = 448, kScanStages = 4;  // 4 state warps (0-3), 8 gate warps (4-11), MMA warp, copy warp
 
 struct StateMaps {
     CUtensorMap x[2];  // K, V rows, box {64, 64}
-    CUtensorMap u;     // U rows, box {64, 64}
 };
 
+// One CTA per (head, K or V) walks the chunks in order.  The copy warp
+// streams chunk c's rows X_c (TMA) and its log_alpha rows (bulk copy) into a
+// stage; the gate warps form the chunk coefficients from log_alpha (per slot:
+// the chunk-local cumsum b, the total G, U[s][i] = exp(G_i - b_{s,i}) u_{s,i}
+// with u = -expm1(log_alpha), written as the bf16 MMA operand) and exp(G);
+// the MMA warp forms dS_c^T = X_c^T U_c on the tensor core into one of two
+// TMEM buffers; the state warps (thread = one column d) carry the state in
+// fp32 registers, S_prev(c + 1) = exp(G_c) S_prev(c) + dS_c, and write the
+// bf16 state entering every chunk.
 template <int D, int M>
 __global__ void __launch_bounds__(kScanThreads, 1)
-state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __restrict__ G, float* __restrict__ SK,
-                     float* __restrict__ SV, __nv_bfloat16* __restrict__ SKb, __nv_bfloat16* __restrict__ SVb,
-                     const StateIO io, Shape call, int want_f32, int* __restrict__ status) {
+state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __restrict__ la, float* __restrict__ G,
+                     float* __restrict__ SK, float* __restrict__ SV, __nv_bfloat16* __restrict__ SKb,
+                     __nv_bfloat16* __restrict__ SVb, const StateIO io, Shape call, int want_f32,
+                     int* __restrict__ status) {
     constexpr int NS = kScanStages;
     constexpr int NSL = M;
+    constexpr int TPS = 256 / M, RPT = kChunk / TPS;  // gate threads per slot, rows per gate thread
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    // stage s: X_c [64 tokens][128 d] (d >= D zero), U_c [64 tokens][64], G_c [M]
+    // stage s: X_c [64 tokens][128 d] (d >= D zero), U_c [64 tokens][64], log_alpha [64][M], exp(G_c) [M]
     auto XT = [&](int st) { return base + st * 16384; };
     auto UT = [&](int st) { return base + NS * 16384 + st * 8192; };
-    auto GS = [&](int st) { return reinterpret_cast<float*>(base + NS * 24576 + st * 256); };
-    __shared__ uint64_t full[NS], empty[NS], sfull[2], tfree[2], drain;
+    auto LA = [&](int st) { return reinterpret_cast<float*>(base + NS * 24576 + st * 16384); };
+    auto GS = [&](int st) { return reinterpret_cast<float*>(base + NS * 40960 + st * 256); };
+    __shared__ uint64_t full[NS], ufull[NS], empty[NS], sfull[2], tfree[2], drain;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -117,6 +67,7 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
     if (tid == 0) {
         for (int q = 0; q < NS; q++) {
             mbar_init(&full[q], 1);
+            mbar_init(&ufull[q], 8);
             mbar_init(&empty[q], 4);
         }
         for (int q = 0; q < 2; q++) {
@@ -140,13 +91,15 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
     int last_ph[NS];
 #pragma unroll
     for (int q = 0; q < NS; q++) last_ph[q] = -1;
-    if (warp == 4) {
-        // ---------------- MMA issuer (lane 0): as soon as a chunk has landed and
-        // its TMEM buffer is read out ----------------
+    auto rows_of = [&](int c) { return min(kChunk, sh.R - c * kChunk); };  // tokens of chunk c
+    if (warp == 12) {
+        // ---------------- MMA issuer (lane 0): once a chunk's coefficients are
+        // formed and its TMEM buffer is read out ----------------
         if (lane == 0) {
             for (int c = 0; c < NC; c++) {
                 const int st = c % NS;
                 if (!mbar_wait_ab(&full[st], (c / NS) & 1, kWaitCycles, abort)) break;
+                if (!mbar_wait_ab(&ufull[st], (c / NS) & 1, kWaitCycles, abort)) break;
                 if (c >= 2 && !mbar_wait_ab(&tfree[c & 1], ((c - 2) >> 1) & 1, kWaitCycles, abort)) break;
                 fence_after_sync();
                 const uint32_t sx = smem_u32(XT(st)), su = smem_u32(UT(st));
@@ -156,16 +109,15 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
                 mma_commit(&sfull[c & 1]);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 13) {
         // ---------------- loader (lane 0): refills a stage once its chunk is consumed ----------------
         if (lane == 0) {
             auto load = [&](int c) {
-                const int st = c % NS;
-                mbar_arrive_expect_tx(&full[st], (D / 64) * 8192 + 8192 + M * 4);
+                const int st = c % NS, nr = rows_of(c);
+                mbar_arrive_expect_tx(&full[st], (D / 64) * 8192 + (uint32_t)(nr * M * 4));
 #pragma unroll
                 for (int x = 0; x < D; x += 64) tma_load_3d(XT(st) + x * 128, &maps.x[tz], x, c * kChunk, bh, &full[st]);
-                tma_load_3d(UT(st), &maps.u, 0, c * kChunk, bh, &full[st]);
-                bulk_load(GS(st), G + ((size_t)bh * NCS + c) * M, M * 4, &full[st]);
+                bulk_load(LA(st), la + ((size_t)bh * sh.T + (size_t)c * kChunk) * M, (uint32_t)(nr * M * 4), &full[st]);
                 last_ph[st] = (c / NS) & 1;
             };
             for (int c = 0; c < min(NS, NC); c++) load(c);
@@ -173,6 +125,48 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
                 if (!mbar_wait_ab(&empty[(c - NS) % NS], ((c - NS) / NS) & 1, kWaitCycles, abort)) break;
                 load(c);
             }
+        }
+    } else if (warp >= 4) {
+        // ---------------- gate warps: thread = (slot i, RPT rows) ----------------
+        // the TPS parts of a slot sit in consecutive lanes, so the chunk's
+        // cumsum is finished with shuffles inside the warp
+        const int g = tid - 128, i = g / TPS, part = g % TPS, r0 = part * RPT;
+        for (int c = 0; c < NC; c++) {
+            const int st = c % NS, nr = rows_of(c);
+            if (!mbar_wait_ab(&full[st], (c / NS) & 1, kWaitCycles, abort)) break;
+            const float* lr = LA(st);
+            float l[RPT], b[RPT], acc = 0.0f;
+#pragma unroll
+            for (int r = 0; r < RPT; r++) {
+                l[r] = (r0 + r < nr) ? lr[(r0 + r) * M + i] : 0.0f;
+                acc += l[r];
+                b[r] = acc;
+            }
+            // exclusive prefix of the parts' sums (offset) and the chunk total
+            float off = 0.0f, Gt = acc;
+#pragma unroll
+            for (int sft = 1; sft < TPS; sft <<= 1) {
+                const float up = __shfl_up_sync(0xffffffffu, Gt, sft);
+                if (part >= sft) Gt += up;
+            }
+            off = Gt - acc;                                                // parts before this one
+            Gt = __shfl_sync(0xffffffffu, Gt, (lane / TPS) * TPS + TPS - 1);  // the last part's inclusive sum
+            unsigned char* ut = UT(st);
+#pragma unroll
+            for (int r = 0; r < RPT; r++) {
+                const int row = r0 + r;
+                const float u = row < nr ? fexp(Gt - (b[r] + off)) * one_minus_exp(l[r]) : 0.0f;
+                *reinterpret_cast<__nv_bfloat16*>(ut + sw_off(row, i, 64)) = __float2bfloat16_rn(u);
+            }
+            if (part == 0) {
+                const float eg = fexp(Gt);
+                GS(st)[i] = eg;
+                if (tz == 0) G[((size_t)bh * NCS + c) * M + i] = eg;  // for the backward's adjoint scan
+                if (Gt < kGateRange) atomicOr(status, kStatusGateRangeBit);
+            }
+            fence_async_smem();  // U is an MMA operand: generic writes -> async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ufull[st]);
         }
     } else {
         // ---------------- state warps: thread = column d ----------------
@@ -190,16 +184,11 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
         for (int c = 0; c < NC; c++) {
             const int st = c % NS, b = c & 1;
             if (!mbar_wait_ab(&sfull[b], (c >> 1) & 1, kWaitCycles, abort) ||
-                !mbar_wait_ab(&full[st], (c / NS) & 1, kWaitCycles, abort)) {
+                !mbar_wait_ab(&ufull[st], (c / NS) & 1, kWaitCycles, abort)) {
                 done = false;
                 break;
             }
             fence_after_sync();
-            float dS[NSL];
-            tmem_ld(tl + 64 * b, dS, NSL);
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tfree[b]);
             {
                 // bf16 copies: lanes d, d ^ 1 swap one value so that each stores a
                 // packed pair (columns d & ~1, d | 1) of slot i (even lane) or i + 1 (odd)
@@ -216,11 +205,23 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
 #pragma unroll
                     for (int i = 0; i < NSL; i++) Sf[o + (size_t)i * D] = S[i];
             }
+            // S_prev(c + 1) = exp(G_c) S_prev(c) + dS_c, dS_c read from TMEM in
+            // groups of at most 32 columns (fewer registers live at once)
             const float* g = GS(st) + i0;  // exp(G_c)
+            constexpr int GRP = NSL < 32 ? NSL : 32;
 #pragma unroll
-            for (int i = 0; i < NSL; i++) S[i] = g[i] * S[i] + dS[i];
+            for (int h = 0; h < NSL; h += GRP) {
+                float dS[GRP];
+                tmem_ld(tl + 64 * b + h, dS, GRP);
+#pragma unroll
+                for (int i = 0; i < GRP; i++) S[h + i] = g[h + i] * S[h + i] + dS[i];
+            }
+            fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
+            if (lane == 0) {
+                mbar_arrive(&tfree[b]);
+                mbar_arrive(&empty[st]);
+            }
         }
         // the final state (after the last chunk): fp32 for the caller, bf16 for
         // the backward's carry of the last chunk; NaN if the scan gave up
@@ -243,11 +244,11 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
     fence_before_sync();
     __syncthreads();
     if (s_abort) {  // let the copies and MMAs in flight land before the TMEM and the CTA go
-        if (warp == 4 && lane == 0) {
+        if (warp == 12 && lane == 0) {
             mma_commit(&drain);
             mbar_wait(&drain, 0, kWaitCycles);
         }
-        if (warp == 5 && lane == 0)
+        if (warp == 13 && lane == 0)
             for (int q = 0; q < NS; q++)
                 if (last_ph[q] >= 0) mbar_wait(&full[q], (uint32_t)last_ph[q], kWaitCycles);
         __syncthreads();
@@ -384,39 +385,27 @@ cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st) {
 
 template <int D, int M>
 cudaError_t tc_states(const __nv_bfloat16* k, const __nv_bfloat16* v, const float* la, float* SK, float* SV,
-                      __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, __nv_bfloat16* U, bool want_f32,
+                      __nv_bfloat16* SKb, __nv_bfloat16* SVb, float* G, bool want_f32,
                       const StateIO& io, const Shape& sh, int* status, cudaStream_t st) {
     if (sh.NCS == 0) return launch_final_states_copy(io, sh.BH, M, D, st);
-    CUtensorMap la_map;
-    cudaError_t e = tmap_rows_f32(&la_map, la, M, sh.T, sh.BH);
-    if (e != cudaSuccess) return e;
-    {
-        const size_t gsm = 1024 + ((M + 31) / 32) * 16384 + 16384;
-        auto gk = state_gates_kernel<M>;
-        if ((e = cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsm)) != cudaSuccess)
-            return e;
-        NHA_LAUNCH("state_gates", st,
-                   gk<<<dim3((sh.NCS * kChunk + 127) / 128, sh.BH), kTcThreads, gsm, st>>>(la_map, U, G, sh, status));
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
     StateMaps maps;
+    cudaError_t e;
     if ((e = tmap_rows_bf16(&maps.x[0], k, D, sh.T, sh.BH, 64)) != cudaSuccess ||
-        (e = tmap_rows_bf16(&maps.x[1], v, D, sh.T, sh.BH, 64)) != cudaSuccess ||
-        (e = tmap_rows_bf16(&maps.u, U, 64, sh.NCS * kChunk, sh.BH, 64)) != cudaSuccess)
+        (e = tmap_rows_bf16(&maps.x[1], v, D, sh.T, sh.BH, 64)) != cudaSuccess)
         return e;
-    const size_t sm = 1024 + kScanStages * (16384 + 8192 + 256);
+    const size_t sm = 1024 + kScanStages * (16384 + 8192 + 16384 + 256);
     auto kern = state_scan_tc_kernel<D, M>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) != cudaSuccess)
         return e;
     NHA_LAUNCH("state_scan", st,
-               kern<<<dim3(sh.BH, 2), kScanThreads, sm, st>>>(maps, G, SK, SV, SKb, SVb, io, sh, want_f32 ? 1 : 0,
-                                                              status));
+               kern<<<dim3(sh.BH, 2), kScanThreads, sm, st>>>(maps, la, G, SK, SV, SKb, SVb, io, sh,
+                                                              want_f32 ? 1 : 0, status));
     return cudaGetLastError();
 }
 
 #define NHA_ST_INST(D, M)                                                                              \
     template cudaError_t tc_states<D, M>(const __nv_bfloat16*, const __nv_bfloat16*, const float*, float*, \
-                                         float*, __nv_bfloat16*, __nv_bfloat16*, float*, __nv_bfloat16*, bool, \
+                                         float*, __nv_bfloat16*, __nv_bfloat16*, float*, bool,                 \
                                          const StateIO&, const Shape&, int*, cudaStream_t);
 NHA_ST_INST(64, 16)
 NHA_ST_INST(64, 32)

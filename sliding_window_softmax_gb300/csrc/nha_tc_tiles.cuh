@@ -13,6 +13,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr long long kWaitCycles = 1LL << 32;  // about 2 s at 2 GHz
 
+// u = 1 - exp(l) for l <= 0 without the cancellation of 1 - exp(l) near 0:
+// for |l| < 1/16 the Taylor series of exp(l) - 1 to the cubic term (relative
+// error below l^3 / 24, under 1e-5), else 1 - 2^(l log2 e) on the MUFU
+// (relative error of the difference below 1e-6 there).
+__device__ __forceinline__ float one_minus_exp(float l) {
+    if (l > -0.0625f) return -l * fmaf(l, fmaf(l, 1.0f / 6.0f, 0.5f), 1.0f);
+    return 1.0f - fexp(l);
+}
+
 __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
