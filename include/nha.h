@@ -143,7 +143,25 @@ nha_status_t nha_backward(const void* q, const void* k, const void* v, const flo
  * workspace is then laid out for the smallest possible window (w = 0), so
  * pass the same extras to nha_workspace_bytes_ex; forward and backward (and
  * a forward workspace the backward reuses) must see the same windows.  The
- * host cannot check device values: a value outside [0, w] is clamped. */
+ * host cannot check device values: a value outside [0, w] is clamped.
+ *
+ * windows_per_sequence: 0, or 1 when windows holds B * H entries, entry
+ * b * H + h for head h of batch entry b (per-sequence windows).
+ *
+ * cu_seqlens: DEVICE array [B + 1] of int32 offsets, or NULL (varlen
+ * batches: sequences of different lengths in one call).  Batch entry b is
+ * then a sequence of
+ * T_b = cu_seqlens[b + 1] - cu_seqlens[b] tokens (clamped to [0, T]) held in
+ * rows t < T_b of its T rows in every token array (q, k, v, log_alpha, o,
+ * lse, dout, dq, dk, dv, dlog_alpha), and is computed exactly as a call of
+ * T_b tokens would compute it: its own window clamp min(w, T_b), hT the
+ * state after its token T_b - w - 1, h0 / dh0 / dhT per sequence.  Tiles
+ * overlapping rows t >= T_b read them as padding, so those rows of every
+ * input must hold finite values (zeros will do), o and lse included when the
+ * backward reads them; the forward and backward leave those rows of their
+ * outputs unspecified.  The workspace is laid out as for per-head windows
+ * (pass the same extras to nha_workspace_bytes_ex).  nha_varlen_pad /
+ * nha_varlen_unpad move packed sequences into and out of this layout. */
 typedef struct {
     const void* fwd_workspace; /* backward: the forward's workspace, read only */
     size_t fwd_ws_bytes;       /* its size in bytes */
@@ -155,9 +173,27 @@ typedef struct {
     const float* dhT_v;
     float* dh0_k;
     float* dh0_v;
-    const int* windows; /* DEVICE [H] int32 per-head windows, or NULL */
+    const int* windows; /* DEVICE [H] (or [B * H]) int32 windows, or NULL */
     int* status;        /* DEVICE int32, or NULL: the call's status word (below) */
+    int windows_per_sequence; /* 1: windows holds B * H entries */
+    const int* cu_seqlens;    /* DEVICE [B + 1] int32 sequence offsets, or NULL */
 } nha_extras_t;
+
+/* Packed <-> padded token rows for cu_seqlens calls.
+ *   packed: [H, Ttot, width]: the B sequences concatenated along the token
+ *           axis, sequence b in rows cu_seqlens[b] .. cu_seqlens[b + 1] - 1
+ *           (the layout of a B = 1 call over all Ttot tokens);
+ *   padded: [B, H, T, width]: sequence b in rows t < T_b of batch entry b.
+ * width elements of elem_bytes bytes (2 or 4) per row, width * elem_bytes a
+ * multiple of 4; both arrays DEVICE, 4-byte aligned, on `stream`.
+ * nha_varlen_pad writes every padded row: rows t < T_b from the packed
+ * array, the rest zero.  nha_varlen_unpad writes packed rows only, those of
+ * rows t < T_b.  A row whose packed index falls outside [0, Ttot) is skipped
+ * (zero in the padded array); T_b is clamped to [0, T] as in the calls. */
+nha_status_t nha_varlen_pad(const void* packed, void* padded, const int* cu_seqlens, int B, int H, int T,
+                            int Ttot, int width, int elem_bytes, void* stream);
+nha_status_t nha_varlen_unpad(const void* padded, void* packed, const int* cu_seqlens, int B, int H, int T,
+                              int Ttot, int width, int elem_bytes, void* stream);
 
 /* Device-side status of a call.  Conditions only the GPU sees cannot be
  * returned by the call itself (it returns once the work is enqueued), so

@@ -14,15 +14,19 @@ from ._binding import (  # noqa: F401
     launch_count,
     load_library,
     nha_backward,
+    nha_backward_varlen,
     nha_decode_prefill,
     nha_decode_state,
     nha_decode_step,
     nha_decode_step_varlen,
     nha_forward,
     nha_forward_noalloc,
+    nha_forward_varlen,
     nha_gate_total,
     nha_selftest_wait,
     nha_state_combine,
+    nha_varlen_pad,
+    nha_varlen_unpad,
     nha_workspace_bytes,
     profile_begin,
     profile_end,

@@ -28,6 +28,7 @@ DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward",
            "nha_workspace_bytes_ex", "nha_forward_ex", "nha_backward_ex",
            "nha_gate_total", "nha_state_combine", "nha_selftest_wait",
+           "nha_varlen_pad", "nha_varlen_unpad",
            "nha_decode_step", "nha_decode_step_varlen",
            "nha_decode_prefill",
            "nha_forward_noalloc",
@@ -44,7 +45,8 @@ class Extras(ctypes.Structure):
                 ("hT_k", ctypes.c_void_p), ("hT_v", ctypes.c_void_p),
                 ("dhT_k", ctypes.c_void_p), ("dhT_v", ctypes.c_void_p),
                 ("dh0_k", ctypes.c_void_p), ("dh0_v", ctypes.c_void_p),
-                ("windows", ctypes.c_void_p), ("status", ctypes.c_void_p)]
+                ("windows", ctypes.c_void_p), ("status", ctypes.c_void_p),
+                ("windows_per_sequence", ctypes.c_int), ("cu_seqlens", ctypes.c_void_p)]
 
 
 class ProfileRecord(ctypes.Structure):
@@ -110,6 +112,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.nha_gate_total.restype = i
         lib.nha_gate_total.argtypes = [vp, vp] + [i] * 5 + [vp]
         lib.nha_state_combine.restype = i
+        lib.nha_varlen_pad.restype = i
+        lib.nha_varlen_pad.argtypes = [vp, vp, vp] + [i] * 6 + [vp]
+        lib.nha_varlen_unpad.restype = i
+        lib.nha_varlen_unpad.argtypes = [vp, vp, vp] + [i] * 6 + [vp]
         lib.nha_state_combine.argtypes = [vp] * 7 + [i] * 4 + [vp]
         lib.nha_decode_step.restype = i
         lib.nha_decode_step.argtypes = [vp] * 10 + [i] * 7 + [f, vp]
@@ -170,7 +176,7 @@ def nha_workspace_bytes(B, H, T, d, m, w, C=64, dtype=torch.bfloat16, backward=F
                         reuse_forward=False, per_head_windows=False) -> int:
     """Workspace bytes of the forward (or backward); ``reuse_forward``: of a
     backward given the forward's workspace; ``per_head_windows``: of a call
-    with a windows array (nha_workspace_bytes_ex)."""
+    with a windows array or sequence lengths (nha_workspace_bytes_ex)."""
     lib = load_library()
     if reuse_forward or per_head_windows:
         ex = Extras()
@@ -185,12 +191,15 @@ def nha_workspace_bytes(B, H, T, d, m, w, C=64, dtype=torch.bfloat16, backward=F
 
 def nha_forward(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 10000.0,
                 o=None, lse=None, workspace=None, stream=None, h0=None, return_state=False, windows=None,
-                status=None):
+                status=None, cu_seqlens=None):
     """o, lse = nha_forward(q, k, v, log_alpha, w).  q, k, v [B,H,T,d]; log_alpha [B,H,T,m] fp32.
 
     ``h0`` = (h0k, h0v): initial slot states, fp32 [B,H,m,d] each.  With
     ``return_state`` the result is (o, lse, (hTk, hTv)), the final slot states
-    (the long memory after token T - w - 1).  Either calls nha_forward_ex."""
+    (the long memory after token T - w - 1).  ``windows``: int32 [H] per-head
+    or [B*H] per-sequence windows.  ``cu_seqlens``: int32 [B+1] offsets, batch
+    entry b then holds a sequence of cu_seqlens[b+1] - cu_seqlens[b] tokens in
+    its first rows (the rest finite padding).  Either calls nha_forward_ex."""
     lib = load_library()
     B, H, T, d = q.shape
     m = log_alpha.shape[-1]
@@ -206,7 +215,7 @@ def nha_forward(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 1000
         lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     _check("o", o, dt, (B, H, T, d))
     _check("lse", lse, torch.float32, (B, H, T))
-    ex = _extras(shape=(B, H, m, d), windows=windows)
+    ex = _extras(shape=(B, H, m, d), windows=windows, cu_seqlens=cu_seqlens)
     need = int(lib.nha_workspace_bytes_ex(B, H, T, d, m, w, C, DTYPE[dt], 0, ctypes.byref(ex)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -215,7 +224,7 @@ def nha_forward(q, k, v, log_alpha, w: int, C: int = 64, rope_base: float = 1000
     if return_state:
         hT = (torch.empty((B, H, m, d), dtype=torch.float32, device=q.device),
               torch.empty((B, H, m, d), dtype=torch.float32, device=q.device))
-    ex = _extras(shape=(B, H, m, d), windows=windows, status=status, h0=h0, hT=hT)
+    ex = _extras(shape=(B, H, m, d), windows=windows, status=status, cu_seqlens=cu_seqlens, h0=h0, hT=hT)
     rc = lib.nha_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(lse),
                             B, H, T, d, m, int(w), int(C), DTYPE[dt], float(rope_base), ctypes.byref(ex),
                             _ptr(workspace), ws_bytes, _stream_handle(stream))
@@ -253,17 +262,28 @@ STATUS_TIMEOUT = 1      # NHA_STATUS_TIMEOUT
 STATUS_GATE_RANGE = 2   # NHA_STATUS_GATE_RANGE
 
 
-def _extras(fwd_workspace=None, shape=None, windows=None, status=None, **states):
-    """Extras from tensors: fwd_workspace, windows (int32 CUDA [H]), and state
-    pairs given as (K, V) tuples of fp32 [B,H,m,d] CUDA tensors under the names
-    h0, hT, dhT, dh0."""
+def _extras(fwd_workspace=None, shape=None, windows=None, status=None, cu_seqlens=None, **states):
+    """Extras from tensors: fwd_workspace, windows (int32 CUDA [H] per head,
+    or [B*H] per sequence), cu_seqlens (int32 CUDA [B+1]), and state pairs
+    given as (K, V) tuples of fp32 [B,H,m,d] CUDA tensors under the names h0,
+    hT, dhT, dh0."""
     ex = Extras()
     if status is not None:
         _check("status", status, torch.int32, (1,))
         ex.status = status.data_ptr()
     if windows is not None:
-        _check("windows", windows, torch.int32, (shape[1],) if shape is not None else None)
+        _check("windows", windows, torch.int32)
+        B, H = shape[0], shape[1]
+        if windows.numel() == H:
+            ex.windows_per_sequence = 0
+        elif windows.numel() == B * H:
+            ex.windows_per_sequence = 1
+        else:
+            raise ValueError(f"windows has {windows.numel()} entries: expected H={H} or B*H={B * H}")
         ex.windows = windows.data_ptr()
+    if cu_seqlens is not None:
+        _check("cu_seqlens", cu_seqlens, torch.int32, (shape[0] + 1,))
+        ex.cu_seqlens = cu_seqlens.data_ptr()
     if fwd_workspace is not None:
         _check("fwd_workspace", fwd_workspace)
         ex.fwd_workspace = fwd_workspace.data_ptr()
@@ -282,14 +302,15 @@ def _extras(fwd_workspace=None, shape=None, windows=None, status=None, **states)
 def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
                  rope_base: float = 10000.0, dq=None, dk=None, dv=None, dlog_alpha=None,
                  workspace=None, stream=None, fwd_workspace=None, h0=None, dhT=None, windows=None,
-                 status=None):
+                 status=None, cu_seqlens=None):
     """dq, dk, dv, dlog_alpha = nha_backward(q, k, v, log_alpha, o, lse, dout, w).
 
     ``fwd_workspace``: the workspace tensor the forward of these inputs ran
     with, untouched since; the backward then reuses the chunk states and
     rotated q, k it holds.  ``h0``: the forward's initial slot states; the
     result then ends with (dh0k, dh0v).  ``dhT``: the gradient with respect to
-    the forward's final slot states.  Calls nha_backward_ex."""
+    the forward's final slot states.  ``windows``, ``cu_seqlens``: as for
+    nha_forward (the same ones).  Calls nha_backward_ex."""
     lib = load_library()
     B, H, T, d = q.shape
     m = log_alpha.shape[-1]
@@ -311,7 +332,8 @@ def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
     if h0 is not None:
         dh0 = (torch.empty((B, H, m, d), dtype=torch.float32, device=q.device),
                torch.empty((B, H, m, d), dtype=torch.float32, device=q.device))
-    ex = _extras(fwd_workspace, shape=(B, H, m, d), windows=windows, status=status, h0=h0, dhT=dhT, dh0=dh0)
+    ex = _extras(fwd_workspace, shape=(B, H, m, d), windows=windows, status=status, cu_seqlens=cu_seqlens, h0=h0,
+                 dhT=dhT, dh0=dh0)
     need = int(lib.nha_workspace_bytes_ex(B, H, T, d, m, w, C, DTYPE[dt], 1, ctypes.byref(ex)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -322,6 +344,88 @@ def nha_backward(q, k, v, log_alpha, o, lse, dout, w: int, C: int = 64,
                              _ptr(workspace), ws_bytes, _stream_handle(stream))
     _raise(lib, rc)
     return (dq, dk, dv, dlog_alpha) if dh0 is None else (dq, dk, dv, dlog_alpha) + dh0
+
+
+def nha_varlen_pad(packed, cu_seqlens, T: int, stream=None):
+    """Packed rows [H, Ttot, *row] -> padded [B, H, T, *row] (B = len(cu_seqlens) - 1;
+    rows past each sequence zero).  nha_varlen_pad of include/nha.h."""
+    lib = load_library()
+    _check("packed", packed)
+    _check("cu_seqlens", cu_seqlens, torch.int32)
+    B = cu_seqlens.numel() - 1
+    H, Ttot = packed.shape[0], packed.shape[1]
+    row = tuple(packed.shape[2:])
+    width = 1
+    for n in row:
+        width *= n
+    out = torch.empty((B, H, T) + row, dtype=packed.dtype, device=packed.device)
+    rc = lib.nha_varlen_pad(_ptr(packed), _ptr(out), _ptr(cu_seqlens), B, H, int(T), Ttot, width,
+                            packed.element_size(), _stream_handle(stream))
+    _raise(lib, rc)
+    return out
+
+
+def nha_varlen_unpad(padded, cu_seqlens, Ttot: int, out=None, stream=None):
+    """Padded rows [B, H, T, *row] -> packed [H, Ttot, *row] (each sequence's
+    rows only).  nha_varlen_unpad of include/nha.h."""
+    lib = load_library()
+    _check("padded", padded)
+    _check("cu_seqlens", cu_seqlens, torch.int32)
+    B, H, T = padded.shape[0], padded.shape[1], padded.shape[2]
+    row = tuple(padded.shape[3:])
+    width = 1
+    for n in row:
+        width *= n
+    if out is None:
+        out = torch.zeros((H, int(Ttot)) + row, dtype=padded.dtype, device=padded.device)
+    _check("out", out, padded.dtype, (H, int(Ttot)) + row)
+    rc = lib.nha_varlen_unpad(_ptr(padded), _ptr(out), _ptr(cu_seqlens), B, H, T, int(Ttot), width,
+                              padded.element_size(), _stream_handle(stream))
+    _raise(lib, rc)
+    return out
+
+
+def nha_forward_varlen(q, k, v, log_alpha, cu_seqlens, max_seqlen: int, w: int, C: int = 64,
+                       rope_base: float = 10000.0, stream=None, h0=None, return_state=False, windows=None,
+                       status=None):
+    """Forward over packed sequences: q, k, v [H, Ttot, d], log_alpha [H, Ttot, m]
+    with sequence b in rows cu_seqlens[b] .. cu_seqlens[b+1] - 1 (int32 [B+1]),
+    each no longer than max_seqlen.  Returns (o [H,Ttot,d], lse [H,Ttot],
+    ctx) and, with return_state, the per-sequence final states [B,H,m,d]
+    before ctx; ctx holds the padded tensors nha_backward_varlen needs.
+    The rows move through nha_varlen_pad / nha_varlen_unpad; the sequences
+    run in one nha_forward_ex call with cu_seqlens."""
+    Ttot = q.shape[1]
+    T = int(max_seqlen)
+    qp, kp, vp = (nha_varlen_pad(x, cu_seqlens, T, stream) for x in (q, k, v))
+    lp = nha_varlen_pad(log_alpha, cu_seqlens, T, stream)
+    B, H = qp.shape[0], qp.shape[1]
+    op = torch.zeros_like(qp)  # rows past a sequence stay finite for the backward
+    lsep = torch.zeros((B, H, T), dtype=torch.float32, device=q.device)
+    m, d = log_alpha.shape[-1], q.shape[-1]
+    need = nha_workspace_bytes(B, H, T, d, m, w, C, q.dtype, per_head_windows=True)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    res = nha_forward(qp, kp, vp, lp, w, C, rope_base, o=op, lse=lsep, workspace=ws, stream=stream, h0=h0,
+                      return_state=return_state, windows=windows, status=status, cu_seqlens=cu_seqlens)
+    o = nha_varlen_unpad(op, cu_seqlens, Ttot, stream=stream)
+    lse = nha_varlen_unpad(lsep.unsqueeze(-1), cu_seqlens, Ttot, stream=stream).squeeze(-1)
+    ctx = dict(q=qp, k=kp, v=vp, log_alpha=lp, o=op, lse=lsep, workspace=ws, T=T, Ttot=Ttot)
+    return (o, lse, res[2], ctx) if return_state else (o, lse, ctx)
+
+
+def nha_backward_varlen(ctx, dout, cu_seqlens, w: int, C: int = 64, rope_base: float = 10000.0, stream=None,
+                        h0=None, dhT=None, windows=None, status=None):
+    """Backward of nha_forward_varlen: dout [H, Ttot, d] -> (dq, dk, dv [H,Ttot,d],
+    dlog_alpha [H,Ttot,m]) and, with h0, the per-sequence (dh0k, dh0v).
+    Reuses the forward's workspace held in ctx (same w, C, rope_base,
+    windows and cu_seqlens)."""
+    T, Ttot = ctx["T"], ctx["Ttot"]
+    dop = nha_varlen_pad(dout, cu_seqlens, T, stream)
+    res = nha_backward(ctx["q"], ctx["k"], ctx["v"], ctx["log_alpha"], ctx["o"], ctx["lse"], dop, w, C,
+                       rope_base, stream=stream, fwd_workspace=ctx["workspace"], h0=h0, dhT=dhT,
+                       windows=windows, status=status, cu_seqlens=cu_seqlens)
+    grads = tuple(nha_varlen_unpad(g, cu_seqlens, Ttot, stream=stream) for g in res[:4])
+    return grads + tuple(res[4:])
 
 
 def nha_decode_state(B, H, d, m, w, dtype=torch.bfloat16, device="cuda"):

@@ -64,8 +64,9 @@ nha_status_t check_shape(int B, int H, int T, int d, int m, int w, int C, nha_dt
 // backward && reuse: the chunk states, gate totals, RoPE table and rotated q, k
 // come from the forward's workspace, so this plan holds only the backward's own
 // buffers.
-// per_head: the heads have their own windows in [0, w]; the per-head arrays are
-// then laid out for the largest number of chunks (w = 0).
+// per_head: the heads have their own windows in [0, w] or sequences their own
+// lengths in [0, T]; the per-head arrays are then laid out for the largest
+// number of chunks (w = 0, T tokens).
 Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward, bool reuse = false, bool per_head = false) {
     Plan p;
     memset(&p, 0, sizeof(p));
@@ -84,6 +85,9 @@ Plan make_plan(int B, int H, int T, int d, int m, int w, bool backward, bool reu
     sh.W0S = T - sh.R;
     sh.windows = nullptr;
     sh.H = H;
+    sh.wbh = 0;
+    sh.seq = nullptr;
+    sh.TS = T;
     sh.status = nullptr;
     size_t off = 0;
     auto take = [&](size_t n) {
@@ -172,12 +176,26 @@ nha_status_t check_extras(const nha_extras_t* ex, bool backward) {
         return fail(NHA_ERR_INVALID_ARGUMENT, "dh0 needs h0 (the gradient of an input that is not given)");
     if (ex->windows != nullptr && ((uintptr_t)ex->windows & 3u) != 0)
         return fail(NHA_ERR_INVALID_ARGUMENT, "windows array is not 4-byte aligned");
+    if (ex->windows_per_sequence != 0 && ex->windows_per_sequence != 1)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "windows_per_sequence=%d is neither 0 nor 1", ex->windows_per_sequence);
+    if (ex->windows_per_sequence && ex->windows == nullptr)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "windows_per_sequence without a windows array");
+    if (ex->cu_seqlens != nullptr && ((uintptr_t)ex->cu_seqlens & 3u) != 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "cu_seqlens array is not 4-byte aligned");
     if (ex->status != nullptr && ((uintptr_t)ex->status & 3u) != 0)
         return fail(NHA_ERR_INVALID_ARGUMENT, "status is not 4-byte aligned");
     return NHA_OK;
 }
 
-bool per_head(const nha_extras_t* ex) { return ex != nullptr && ex->windows != nullptr; }
+bool per_head(const nha_extras_t* ex) { return ex != nullptr && (ex->windows != nullptr || ex->cu_seqlens != nullptr); }
+
+// The per-head and per-sequence fields of a call's shape.
+void set_varied(nha::Shape& sh, const nha_extras_t* ex) {
+    if (ex == nullptr) return;
+    sh.windows = ex->windows;
+    sh.wbh = ex->windows_per_sequence;
+    sh.seq = ex->cu_seqlens;
+}
 
 nha::StateIO state_io(const nha_extras_t* ex, bool forward) {
     nha::StateIO io{};
@@ -333,7 +351,7 @@ nha_status_t nha_forward_ex(const void* q, const void* k, const void* v, const f
     a.io.htb = (__nv_bfloat16*)(ws + p.HTB);
     a.io.htf = ws + p.HTF;
     a.sh = p.sh;
-    a.sh.windows = per_head(ex) ? ex->windows : nullptr;
+    set_varied(a.sh, ex);
     a.sh.status = (ex != nullptr && ex->status != nullptr) ? ex->status : (int*)(ws + p.STATUS);
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
@@ -407,7 +425,7 @@ nha_status_t nha_backward_ex(const void* q, const void* k, const void* v, const 
     a.ldl = ws + p.LDL;
     a.lpl = ws + p.LPL;
     a.sh = p.sh;
-    a.sh.windows = per_head(ex) ? ex->windows : nullptr;
+    set_varied(a.sh, ex);
     a.sh.status = (ex != nullptr && ex->status != nullptr) ? ex->status : (int*)(ws + p.STATUS);
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
@@ -569,6 +587,40 @@ nha_status_t nha_gate_total(const float* log_alpha, float* decay, int B, int H, 
     cudaError_t e = nha::launch_gate_total(log_alpha, decay, B * H, T, m, R, (cudaStream_t)stream);
     if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "gate_total launch failed: %s", cudaGetErrorString(e));
     return ok();
+}
+
+static nha_status_t varlen_call(const void* src, void* dst, const int* cu, int B, int H, int T, int Ttot, int width,
+                                int elem_bytes, bool pad, void* stream) {
+    if (inject("validate")) return fail(NHA_ERR_INTERNAL, "fault injected at validate");
+    if (B < 0 || H < 0 || T < 0 || Ttot < 0 || width <= 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "negative or zero size (B=%d H=%d T=%d Ttot=%d width=%d)", B, H, T, Ttot,
+                    width);
+    if (elem_bytes != 2 && elem_bytes != 4)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "elem_bytes=%d is neither 2 nor 4", elem_bytes);
+    const long long row_bytes = (long long)width * elem_bytes;
+    if (row_bytes % 4 != 0) return fail(NHA_ERR_INVALID_ARGUMENT, "row of %lld bytes is not a multiple of 4", row_bytes);
+    if ((long long)B * H * T * row_bytes / 4 >= (1LL << 31) || (long long)H * Ttot * row_bytes / 4 >= (1LL << 31))
+        return fail(NHA_ERR_UNSUPPORTED, "arrays of 2^31 or more 4-byte words");
+    if ((long long)B * H * T == 0) return ok();
+    const void* ptrs[] = {src, dst, cu};
+    const char* names[] = {pad ? "packed" : "padded", pad ? "padded" : "packed", "cu_seqlens"};
+    for (int i = 0; i < 3; i++) {
+        if (ptrs[i] == nullptr) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is NULL", names[i]);
+        if (((uintptr_t)ptrs[i] & 3u) != 0) return fail(NHA_ERR_INVALID_ARGUMENT, "%s is not 4-byte aligned", names[i]);
+    }
+    cudaError_t e = nha::launch_varlen_copy(src, dst, cu, B, H, T, Ttot, (int)row_bytes, pad, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail(NHA_ERR_CUDA, "varlen copy launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+nha_status_t nha_varlen_pad(const void* packed, void* padded, const int* cu_seqlens, int B, int H, int T, int Ttot,
+                            int width, int elem_bytes, void* stream) {
+    return varlen_call(packed, padded, cu_seqlens, B, H, T, Ttot, width, elem_bytes, true, stream);
+}
+
+nha_status_t nha_varlen_unpad(const void* padded, void* packed, const int* cu_seqlens, int B, int H, int T, int Ttot,
+                              int width, int elem_bytes, void* stream) {
+    return varlen_call(padded, packed, cu_seqlens, B, H, T, Ttot, width, elem_bytes, false, stream);
 }
 
 nha_status_t nha_state_combine(const float* decay, const float* prev_k, const float* prev_v, const float* cur_k,

@@ -65,7 +65,8 @@ bwd_wdq_tc_kernel(const BwdArgs a, const __grid_constant__ WdqMaps maps, int* __
     const int bh = blockIdx.y;
     const Shape sh = head_shape(a.sh, bh);
     const int tbase = blockIdx.x * 128, nq = min(128, sh.T - tbase);
-    const size_t hoff = (size_t)bh * sh.T;
+    if (nq <= 0) return;  // past this head's queries (per-sequence lengths)
+    const size_t hoff = (size_t)bh * sh.TS;
     const int klo = max(0, tbase - sh.w + 1), khi = tbase + nq - 1;
     const int nb = sh.w > 0 ? (khi - klo) / 128 + 1 : 0;
     volatile int* abort = &s_abort;
@@ -350,7 +351,8 @@ bwd_wkv_tc_kernel(const BwdArgs a, const __grid_constant__ WkvMaps maps, int* __
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sbase = blockIdx.x * 128, bh = blockIdx.y;
     const Shape sh = head_shape(a.sh, bh);
-    const size_t hoff = (size_t)bh * sh.T;
+    if (sbase >= sh.T) return;  // past this head's keys (per-sequence lengths)
+    const size_t hoff = (size_t)bh * sh.TS;
     const int thi = sh.w > 0 ? min(sh.T - 1, sbase + min(128, sh.T - sbase) - 1 + sh.w - 1) : sbase - 1;
     const int nb = thi >= sbase ? (thi - sbase) / 64 + 1 : 0;
     volatile int* abort = &s_abort;

@@ -40,10 +40,18 @@ struct Shape {
     // Layout of the per-head workspace arrays, the same for every head:
     int NCS;     // chunks per head in the [BH, NCS, ...] arrays (NC, or ceil(T / C) with per-head windows)
     int W0S;     // rows per head of the [BH, W0S, m] arrays of the queries t < w (the largest min(w, T))
-    // Per-head windows (device [H], or null): head h = bh % H has window
-    // min(max(windows[h], 0), w); w above is then the largest window.
+    // Per-head windows (device [H], or [B * H] when wbh is set; or null):
+    // head h = bh % H (or the pair bh) has window min(max(windows[.], 0), w);
+    // w above is then the largest window.
     const int* windows;
     int H;
+    int wbh;
+    // Sequence lengths (device [B + 1] offsets, or null): sequence b = bh / H
+    // holds T_b = seq[b + 1] - seq[b] tokens (clamped to [0, TS]) in the first
+    // rows of its [TS] rows; the head's shape is that of a T_b-token call.
+    const int* seq;
+    int TS;      // rows per head in the [BH, TS, ...] token arrays: the call's T
+
     // The call's status word (device int): kernels OR in kStatus* bits for
     // conditions only the device sees; the call sets it to zero first.
     int* status;
@@ -54,16 +62,29 @@ constexpr int kStatusTimeoutBit = 1;    // a bounded wait gave up; the results a
 constexpr int kStatusGateRangeBit = 2;  // a chunk's per-slot log_alpha sum fell below kGateRange
 constexpr float kGateRange = -160.0f;   // the intra-chunk gate factorisation is exact in fp32 above it
 
-// The shape seen by head bh: its own window and the counts that follow from
-// it (the layout fields NCS, W0S are the call's).
+// True when heads differ in shape (per-head windows or per-sequence lengths):
+// grids are then sized for the largest head and CTAs past a head's own tiles
+// return at once.
+__host__ __device__ __forceinline__ bool varied(const Shape& sh) { return sh.windows != nullptr || sh.seq != nullptr; }
+
+// The shape seen by head bh: its own tokens and window and the counts that
+// follow from them (the layout fields NCS, W0S, TS are the call's).
 __device__ __forceinline__ Shape head_shape(const Shape& call, int bh) {
     Shape s = call;
-    if (call.windows != nullptr) {
-        const int wh = min(max(__ldg(call.windows + bh % call.H), 0), call.w);
-        s.w = wh;
-        s.R = s.T - wh;
+    if (varied(call)) {
+        int Tb = call.T;
+        if (call.seq != nullptr) {
+            const int b = bh / call.H;
+            Tb = min(max(__ldg(call.seq + b + 1) - __ldg(call.seq + b), 0), call.TS);
+        }
+        int wh = call.w;
+        if (call.windows != nullptr) wh = min(max(__ldg(call.windows + (call.wbh ? bh : bh % call.H)), 0), call.w);
+        s.T = Tb;
+        s.w = min(wh, Tb);
+        s.R = Tb - s.w;
         s.NC = (s.R + kChunk - 1) / kChunk;
-        s.NL = (wh + kChunk - 1) / kChunk;
+        s.NL = (s.w + kChunk - 1) / kChunk;
+        s.NKT = (Tb + kChunk - 1) / kChunk;
     }
     return s;
 }

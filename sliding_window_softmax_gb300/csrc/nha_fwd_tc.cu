@@ -74,7 +74,7 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
         nq = min(128, sh.R - j0);
         tbase = j0 + sh.w;
     }
-    const size_t hoff = (size_t)bh * sh.T;
+    const size_t hoff = (size_t)bh * sh.TS;
     const int klo = max(0, tbase - sh.w + 1), khi = tbase + nq - 1;
     const int nb = sh.w > 0 ? (khi - klo) / 128 + 1 : 0;
     volatile int* abort = &s_abort;
@@ -554,7 +554,7 @@ cudaError_t tc_forward(const FwdArgs& a, float2* tab, __nv_bfloat16* qr, __nv_bf
     if (sh.w > 0 && (e = join_side(st, *f, 1)) != cudaSuccess) return e;
     const int W0 = sh.T - sh.R;
     // with per-head windows a head has at most ceil(T / 128) + 1 tiles
-    const int tiles = sh.windows ? (sh.T + 127) / 128 + 1 : (W0 + 127) / 128 + (sh.R + 127) / 128;
+    const int tiles = varied(sh) ? (sh.T + 127) / 128 + 1 : (W0 + 127) / 128 + (sh.R + 127) / 128;
     if (tiles == 0) return cudaSuccess;
     FwdMaps maps;
     if ((e = tmap_rows_bf16(&maps.q, qr, D, sh.T, sh.BH, 128)) != cudaSuccess ||

@@ -86,7 +86,7 @@ h0_fwd_lead_kernel(const FwdArgs a) {
     if (blockIdx.x * kH0Rows >= W0) return;  // past this head's rows (per-head windows)
     load_h0<D, M>(a.io, bh, sK, sV);
     __syncthreads();
-    const size_t hoff = (size_t)bh * sh.T;
+    const size_t hoff = (size_t)bh * sh.TS;
     float* qrow = sRow + warp * D;
     float* prow = sP + warp * M;
     for (int rr = warp; rr < kH0Rows; rr += 8) {
@@ -142,7 +142,7 @@ h0_bwd_lead_kernel(const BwdArgs a) {
     if (blockIdx.x * kH0Rows >= W0) return;  // past this head's rows (per-head windows)
     load_h0<D, M>(a.io, bh, sK, sV);
     __syncthreads();
-    const size_t hoff = (size_t)bh * sh.T;
+    const size_t hoff = (size_t)bh * sh.TS;
     float* qrow = sRow + warp * 2 * D;
     float* grow = qrow + D;
     float* prow = sP + warp * M;
@@ -238,7 +238,7 @@ dh0_kernel(const BwdArgs a) {
     }
     if (W0 > 0) {
         const float* X = (z == 0 ? a.ldl : a.lpl) + (size_t)bh * a.sh.W0S * M + i0;
-        const Tin* Y = (const Tin*)(z == 0 ? a.q : a.dout) + (size_t)bh * sh.T * D + d;
+        const Tin* Y = (const Tin*)(z == 0 ? a.q : a.dout) + (size_t)bh * sh.TS * D + d;
         for (int t = 0; t < W0; t++) {
             const float4 x = *reinterpret_cast<const float4*>(X + (size_t)t * M);
             const float y = ld(Y + (size_t)t * D);

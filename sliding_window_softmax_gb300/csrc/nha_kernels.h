@@ -127,6 +127,10 @@ cudaError_t launch_selftest_wait(int* status, long long cycles, cudaStream_t st)
 // Segment summaries for cutting a sequence into segments: the gate product of
 // the tokens that leave the window (decay [BH][M]) and out = decay o prev + cur.
 cudaError_t launch_gate_total(const float* la, float* decay, int BH, int T, int M, int R, cudaStream_t st);
+// Packed [H, Ttot, row] <-> padded [B, H, T, row] token rows by sequence
+// offsets cu [B + 1] (pad: rows past a sequence zero; unpad: its rows only).
+cudaError_t launch_varlen_copy(const void* src, void* dst, const int* cu, int B, int H, int T, int Ttot,
+                               int row_bytes, bool pad, cudaStream_t st);
 cudaError_t launch_state_combine(const float* decay, const float* pk, const float* pv, const float* ck,
                                  const float* cv, float* ok, float* ov, int BH, int M, int D, cudaStream_t st);
 

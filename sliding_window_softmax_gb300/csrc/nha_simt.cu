@@ -40,7 +40,7 @@ state_chunk_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
     const Shape sh = head_shape(call, bh);
     if (c >= sh.NC) return;  // past this head's chunks (per-head windows)
     const int j0 = c * kChunk, nc = min(kChunk, sh.R - j0);
-    const size_t row0 = (size_t)bh * sh.T;
+    const size_t row0 = (size_t)bh * sh.TS;
     if (tid < M) {
         const float* lr = la + (row0 + j0) * M;
         float b = 0.0f;
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads) fwd_main_kernel(const FwdArgs a) {
         nq = min(kChunk, sh.R - j0);
         tbase = j0 + sh.w;
     }
-    const size_t hoff = (size_t)bh * sh.T;
+    const size_t hoff = (size_t)bh * sh.TS;
     const Tin* q = (const Tin*)a.q + hoff * D;
     const Tin* k = (const Tin*)a.k + hoff * D;
     const Tin* v = (const Tin*)a.v + hoff * D;
@@ -301,7 +301,8 @@ __global__ void __launch_bounds__(kThreads) bwd_window_dq_kernel(const BwdArgs a
     const int tid = threadIdx.x, r = tid >> 2, tq = tid & 3, bh = blockIdx.y;
     const Shape sh = head_shape(a.sh, bh);
     const int tbase = blockIdx.x * kChunk, nq = min(kChunk, sh.T - tbase);
-    const size_t hoff = (size_t)bh * sh.T;
+    if (nq <= 0) return;  // past this head's queries (per-sequence lengths)
+    const size_t hoff = (size_t)bh * sh.TS;
     const Tin* k = (const Tin*)a.k + hoff * D;
     const Tin* v = (const Tin*)a.v + hoff * D;
     load_rows<Tin, D>((const Tin*)a.q + hoff * D, tbase, nq, sQ, LX, &a.rope);
@@ -373,7 +374,8 @@ __global__ void __launch_bounds__(kThreads) bwd_window_dkdv_kernel(const BwdArgs
     const int tid = threadIdx.x, s = tid >> 2, tq = tid & 3, bh = blockIdx.y;
     const Shape sh = head_shape(a.sh, bh);
     const int sbase = blockIdx.x * kChunk, nk = min(kChunk, sh.T - sbase);
-    const size_t hoff = (size_t)bh * sh.T;
+    if (nk <= 0) return;  // past this head's keys (per-sequence lengths)
+    const size_t hoff = (size_t)bh * sh.TS;
     const Tin* q = (const Tin*)a.q + hoff * D;
     const Tin* dout = (const Tin*)a.dout + hoff * D;
     load_rows<Tin, D>((const Tin*)a.k + hoff * D, sbase, nk, sK, LX, &a.rope);
@@ -463,7 +465,7 @@ __global__ void __launch_bounds__(kThreads) bwd_slot_query_kernel(const BwdArgs 
     const int tid = threadIdx.x, r = tid >> 2, tq = tid & 3, bh = blockIdx.y, x = blockIdx.x;
     const Shape sh = head_shape(a.sh, bh);
     if (x >= sh.NL + sh.NC) return;  // past this head's tiles (per-head windows)
-    const size_t hoff = (size_t)bh * sh.T;
+    const size_t hoff = (size_t)bh * sh.TS;
     if (x < sh.NL) {
         const int tbase = x * kChunk, nq = min(kChunk, min(sh.w, sh.T) - tbase);
         for (int e = tid; e < nq * D; e += kThreads)
@@ -641,8 +643,9 @@ __global__ void __launch_bounds__(kThreads) bwd_slot_key_kernel(const BwdArgs a)
     float* sEG = sER + M;  // exp(G / 2) = exp(G - rho)
     const int tid = threadIdx.x, s = tid >> 2, tq = tid & 3, bh = blockIdx.y, x = blockIdx.x;
     const Shape sh = head_shape(a.sh, bh);
-    const size_t hoff = (size_t)bh * sh.T;
+    const size_t hoff = (size_t)bh * sh.TS;
     const int sbase = x * kChunk, nk = min(kChunk, sh.T - sbase);
+    if (nk <= 0) return;  // past this head's keys (per-sequence lengths)
     const int nc = (x < sh.NC) ? min(kChunk, sh.R - sbase) : 0;
     float gk[NCOL], gv[NCOL], du[NSL];
     for (int n = 0; n < NCOL; n++) gk[n] = gv[n] = 0.0f;
@@ -745,7 +748,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dla_carry_kernel(const BwdArgs a
         carry[threadIdx.x] = 0.0f;
     }
     __syncthreads();
-    const size_t hoff = (size_t)bh * sh.T;
+    const size_t hoff = (size_t)bh * sh.TS;
     for (int e = threadIdx.x; e < nc * M; e += kThreads) a.dla[(hoff + j0) * M + e] += carry[e % M];
 }
 
@@ -787,7 +790,7 @@ cudaError_t simt_forward(const FwdArgs& a, cudaStream_t st) {
     auto kern = fwd_main_kernel<Tin, D, M>;
     NHA_CHECK(set_smem(kern, sm));
     // with per-head windows a head has at most ceil(T / C) + 1 tiles
-    const int tiles = sh.windows ? sh.NKT + 1 : sh.NL + sh.NC;
+    const int tiles = varied(sh) ? sh.NKT + 1 : sh.NL + sh.NC;
     if (tiles > 0) NHA_LAUNCH("fwd_main", st, kern<<<dim3(tiles, sh.BH), kThreads, sm, st>>>(a));
     NHA_CHECK(cudaGetLastError());
     return launch_h0_fwd_lead<Tin, D, M>(a, st);  // queries t < w reading initial states
@@ -801,7 +804,7 @@ cudaError_t simt_bwd_slot(const BwdArgs& a, cudaStream_t st) {
         size_t sm = sizeof(float) * (size_t)(4 * kChunk * LX + kChunk * LP + 4 * kChunk * LG + 2 * M);
         auto kern = bwd_slot_query_kernel<Tin, D, M>;
         NHA_CHECK(set_smem(kern, sm));
-        const int tiles = sh.windows ? sh.NKT + 1 : sh.NL + sh.NC;
+        const int tiles = varied(sh) ? sh.NKT + 1 : sh.NL + sh.NC;
         if (tiles > 0) NHA_LAUNCH("bwd_slot_query", st, kern<<<dim3(tiles, sh.BH), kThreads, sm, st>>>(a));
         NHA_CHECK(cudaGetLastError());
         NHA_CHECK(launch_h0_bwd_lead<Tin, D, M>(a, false, st));  // queries t < w reading initial states

@@ -65,7 +65,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
     const Shape sh = head_shape(a.sh, bh);
     const int W0 = sh.T - sh.R, NLT = (W0 + 127) / 128;
     if (x >= NLT + (sh.R + 127) / 128) return;  // past this head's tiles (per-head windows)
-    const size_t hoff = (size_t)bh * sh.T;
+    const size_t hoff = (size_t)bh * sh.TS;
     if (x < NLT) {  // window-only queries: D = its window part; dq = window branch only
         const int tb = x * 128, n = min(128, W0 - tb);
         for (int e = tid; e < n * D / 8; e += kTcThreads) {
@@ -433,8 +433,9 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
     const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
     const int x = blockIdx.x, bh = blockIdx.y;
     const Shape sh = head_shape(a.sh, bh);
-    const size_t hoff = (size_t)bh * sh.T;
+    const size_t hoff = (size_t)bh * sh.TS;
     const int sbase = x * 128, nk = min(128, sh.T - sbase);
+    if (nk <= 0) return;  // past this head's keys (per-sequence lengths)
     const int nc = max(0, min(128, sh.R - sbase));
     const int s = sbase + r;
     const bool row_ok = r < nk, slot_ok = r < nc;
@@ -726,7 +727,7 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
     cudaError_t e;
     const int W0 = sh.T - sh.R;
     // with per-head windows a head has at most ceil(T / 128) + 1 query tiles
-    const int qtiles = sh.windows ? (sh.T + 127) / 128 + 1 : (W0 + 127) / 128 + (sh.R + 127) / 128;
+    const int qtiles = varied(sh) ? (sh.T + 127) / 128 + 1 : (W0 + 127) / 128 + (sh.R + 127) / 128;
     {
         SqMaps maps;
         const int ncm = (sh.NCS > 0 ? sh.NCS : 1) * M;

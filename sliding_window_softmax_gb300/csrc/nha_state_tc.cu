@@ -117,7 +117,7 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
                 mbar_arrive_expect_tx(&full[st], (D / 64) * 8192 + (uint32_t)(nr * M * 4));
 #pragma unroll
                 for (int x = 0; x < D; x += 64) tma_load_3d(XT(st) + x * 128, &maps.x[tz], x, c * kChunk, bh, &full[st]);
-                bulk_load(LA(st), la + ((size_t)bh * sh.T + (size_t)c * kChunk) * M, (uint32_t)(nr * M * 4), &full[st]);
+                bulk_load(LA(st), la + ((size_t)bh * sh.TS + (size_t)c * kChunk) * M, (uint32_t)(nr * M * 4), &full[st]);
                 last_ph[st] = (c / NS) & 1;
             };
             for (int c = 0; c < min(NS, NC); c++) load(c);

@@ -303,3 +303,38 @@ def test_selftest_wait_validates(lib):
     assert lib.nha_selftest_wait(ctypes.c_void_p(4098), 1000, None) == 1
     assert lib.nha_selftest_wait(p, 0, None) == 1
     assert lib.nha_selftest_wait(p, (1 << 32) + 1, None) == 1
+
+
+def test_varlen_extras_and_copies_validate(lib):
+    p = ctypes.c_void_p(4096)
+    args = (p, p, p, p, p, p, 1, 2, 256, 64, 16, 32, 64, 1, 10000.0)
+    ex = _binding.Extras()
+    ex.windows_per_sequence = 1  # without a windows array
+    assert lib.nha_forward_ex(*args, ctypes.byref(ex), p, 1 << 30, None) == 1
+    assert b"without a windows array" in lib.nha_last_error()
+    ex = _binding.Extras()
+    ex.windows, ex.windows_per_sequence = 4096, 2
+    assert lib.nha_forward_ex(*args, ctypes.byref(ex), p, 1 << 30, None) == 1
+    ex = _binding.Extras()
+    ex.cu_seqlens = 4098  # misaligned
+    assert lib.nha_forward_ex(*args, ctypes.byref(ex), p, 1 << 30, None) == 1
+    assert b"cu_seqlens" in lib.nha_last_error()
+    # sequence lengths lay the workspace out like per-head windows
+    ex = _binding.Extras()
+    ex.cu_seqlens = 4096
+    win = _binding.Extras()
+    win.windows = 4096
+    f = lib.nha_workspace_bytes_ex
+    assert f(2, 2, 300, 64, 16, 100, 64, 1, 1, ctypes.byref(ex)) == f(2, 2, 300, 64, 16, 100, 64, 1, 1,
+                                                                       ctypes.byref(win))
+    assert f(2, 2, 300, 64, 16, 100, 64, 1, 1, ctypes.byref(ex)) > lib.nha_workspace_bytes(2, 2, 300, 64, 16, 100,
+                                                                                          64, 1, 1)
+    # pad / unpad: sizes, element size, row bytes, pointers
+    for fn in (lib.nha_varlen_pad, lib.nha_varlen_unpad):
+        assert fn(p, p, p, 2, 2, 10, 20, 8, 3, None) == 1           # elem_bytes neither 2 nor 4
+        assert fn(p, p, p, 2, 2, 10, 20, 3, 2, None) == 1           # 6-byte rows
+        assert fn(p, p, p, -1, 2, 10, 20, 8, 4, None) == 1
+        assert fn(p, p, p, 2, 2, 10, 20, 0, 4, None) == 1
+        assert fn(None, p, p, 2, 2, 10, 20, 8, 4, None) == 1
+        assert fn(p, p, ctypes.c_void_p(4098), 2, 2, 10, 20, 8, 4, None) == 1
+        assert fn(p, p, p, 0, 2, 10, 20, 8, 4, None) == 0           # nothing to move
