@@ -257,39 +257,33 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
     if (warp == 0) tmem_dealloc(tm, 128);
 }
 
-constexpr int kAdjSlots = 8;
+constexpr int kAdjSlots = 4, kAdjDepth = 4;
 
-// Reverse chunk scan of the slot adjoints, fused with the dlog_alpha carry.
-// R_c, the adjoint carried into chunk c from the later chunks, follows
-// R_{c - 1} = exp(G_c) R_c + dR_c (dR_c: the chunk's own contribution, from the
-// query-side kernel); it is written in bf16 for the key-side kernel.  The carry
-// of chunk c, sum_d R_c[i][d] S_prev(c + 1)[i][d] (the bf16 states), is the
-// total over all later rows of the gate gradient that every row of chunk c
-// receives; it is added to db1 of the chunk's last state row, whose in-chunk
-// suffix sum then hands it to every row.  One CTA per (head, 8 slots): D
-// threads for K and D for V (thread = column d), so the carry's two parts
-// are summed in one CTA and added once; two chunks of loads in flight (8
-// slots keep it small enough to share the SMs with the key-major kernel).
+// Reverse chunk scan of the slot adjoints.  R_c, the adjoint carried into
+// chunk c from the later chunks, follows R_{c - 1} = exp(G_c) R_c + dR_c
+// (dR_c: the chunk's own contribution, from the query-side kernel); it is
+// written in bf16 for the key-side kernel and the carry kernel below.  One
+// CTA per (head, 4 slots): D threads for K and D for V (thread = column d),
+// each with the loads of kAdjDepth chunks in flight and nothing else on its
+// path (no block barrier).  At most 64 registers a thread: a CTA then fits
+// beside a key-major window CTA on one SM, so the scan runs in that kernel's
+// shadow on the side stream.
 template <int D>
-__global__ void __launch_bounds__(2 * D)
-adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, const __nv_bfloat16* __restrict__ SK,
-                const __nv_bfloat16* __restrict__ SV, const float* __restrict__ G, __nv_bfloat16* __restrict__ RKb,
-                __nv_bfloat16* __restrict__ RVb, float* __restrict__ db1, const float* __restrict__ dhTk,
-                const float* __restrict__ dhTv, const __nv_bfloat16* __restrict__ htb, float* __restrict__ rend,
-                Shape call, int M) {
-    constexpr int NW = 2 * D / 32, SG = kAdjSlots;
-    __shared__ float red[2][NW][SG];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(2 * D, 4)
+adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, const float* __restrict__ G,
+                __nv_bfloat16* __restrict__ RKb, __nv_bfloat16* __restrict__ RVb, const float* __restrict__ dhTk,
+                const float* __restrict__ dhTv, float* __restrict__ rend, Shape call, int M) {
+    constexpr int SG = kAdjSlots, NP = kAdjDepth;
+    const int lane = threadIdx.x & 31;
     const int tz = threadIdx.x / D, d = threadIdx.x % D;  // tz 0: K, 1: V
     const int bh = blockIdx.x, i0 = SG * blockIdx.y;
     const Shape sh = head_shape(call, bh);
     const int NC = sh.NC, NCS = sh.NCS;  // this head's chunks; chunks per head in the arrays
     const float* X = tz == 0 ? RK : RV;
-    const __nv_bfloat16* S = tz == 0 ? SK : SV;
     __nv_bfloat16* Xb = tz == 0 ? RKb : RVb;
     auto at = [&](int c) { return (((size_t)bh * NCS + c) * M + i0) * D + d; };
     const float* dh = tz == 0 ? dhTk : dhTv;
-    auto load = [&](int c, float (&x)[SG], float (&sp)[SG], float (&g)[SG]) {
+    auto load = [&](int c, float (&x)[SG], float (&g)[SG]) {
         const size_t o = at(c);
         const float* gc = G + ((size_t)bh * NCS + c) * M + i0;
 #pragma unroll
@@ -297,66 +291,32 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
             x[i] = X[o + (size_t)i * D];
             g[i] = __ldg(gc + i);
         }
-        if (c + 1 < NC) {
-            const size_t o1 = at(c + 1);
-#pragma unroll
-            for (int i = 0; i < SG; i++) sp[i] = __bfloat162float(S[o1 + (size_t)i * D]);
-        } else if (dh != nullptr) {  // the last chunk's carry: the final state (with its gradient)
-            const __nv_bfloat16* hb = htb + (((size_t)bh * 2 + tz) * M + i0) * D + d;
-#pragma unroll
-            for (int i = 0; i < SG; i++) sp[i] = __bfloat162float(hb[(size_t)i * D]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < SG; i++) sp[i] = 0.0f;
-        }
     };
     // R enters the last chunk as the gradient of the final state (zero without one)
     float R[SG];
 #pragma unroll
     for (int i = 0; i < SG; i++) R[i] = dh != nullptr ? dh[((size_t)bh * M + i0 + i) * D + d] : 0.0f;
-    int parity = 0;
-    auto process = [&](int c, const float (&x)[SG], const float (&sp)[SG], const float (&g)[SG]) {
-        const size_t o = at(c);
-        float part[SG];
-        const bool odd = lane & 1;  // packed bf16 pairs, as in the state scan
+    float x[NP][SG], g[NP][SG];
 #pragma unroll
-        for (int i = 0; i < SG; i += 2) {
-            const float recv = __shfl_xor_sync(0xffffffffu, odd ? R[i] : R[i + 1], 1);
-            const uint32_t pk = odd ? pack_bf16(recv, R[i + 1]) : pack_bf16(R[i], recv);
-            *reinterpret_cast<uint32_t*>(Xb + o + (size_t)(i + (odd ? 1 : 0)) * D - (odd ? 1 : 0)) = pk;
+    for (int p = 0; p < NP; p++)
+        if (NC - 1 - p >= 0) load(NC - 1 - p, x[p], g[p]);
+    const bool odd = lane & 1;  // packed bf16 pairs, as in the state scan
+    for (int base = NC - 1; base >= 0; base -= NP) {
+#pragma unroll
+        for (int p = 0; p < NP; p++) {
+            const int c = base - p;
+            if (c < 0) break;  // uniform over the CTA
+            const size_t o = at(c);
+#pragma unroll
+            for (int i = 0; i < SG; i += 2) {
+                const float recv = __shfl_xor_sync(0xffffffffu, odd ? R[i] : R[i + 1], 1);
+                const uint32_t pk = odd ? pack_bf16(recv, R[i + 1]) : pack_bf16(R[i], recv);
+                *reinterpret_cast<uint32_t*>(Xb + o + (size_t)(i + (odd ? 1 : 0)) * D - (odd ? 1 : 0)) = pk;
+            }
+#pragma unroll
+            for (int i = 0; i < SG; i++) R[i] = g[p][i] * R[i] + x[p][i];  // g = exp(G_c)
+            if (c - NP >= 0) load(c - NP, x[p], g[p]);
         }
-#pragma unroll
-        for (int i = 0; i < SG; i++) part[i] = R[i] * sp[i];
-#pragma unroll
-        for (int i = 0; i < SG; i++) {
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
-        }
-        if (lane == 0)
-#pragma unroll
-            for (int i = 0; i < SG; i++) red[parity][warp][i] = part[i];
-        __syncthreads();  // red[parity] complete; red[parity ^ 1] free again
-        if (threadIdx.x < SG && (c + 1 < NC || dhTk != nullptr)) {
-            float t = 0.0f;
-#pragma unroll
-            for (int q = 0; q < NW; q++) t += red[parity][q][threadIdx.x];
-            // db1 of the chunk's last state row: the in-chunk suffix sum spreads it
-            const int last = min(c * kChunk + kChunk, sh.R) - 1;
-            db1[((size_t)bh * NCS * kChunk + last) * M + i0 + threadIdx.x] += t;
-        }
-        parity ^= 1;
-#pragma unroll
-        for (int i = 0; i < SG; i++) R[i] = g[i] * R[i] + x[i];  // g = exp(G_c)
-    };
-    float xa[SG], sa[SG], ga[SG], xb[SG], sb[SG], gb[SG];
-    if (NC >= 1) load(NC - 1, xa, sa, ga);
-    if (NC >= 2) load(NC - 2, xb, sb, gb);
-    for (int c = NC - 1; c >= 0; c -= 2) {
-        process(c, xa, sa, ga);
-        if (c - 2 >= 0) load(c - 2, xa, sa, ga);
-        if (c - 1 < 0) break;
-        process(c - 1, xb, sb, gb);
-        if (c - 3 >= 0) load(c - 3, xb, sb, gb);
     }
     if (rend != nullptr)  // the adjoint of the state before chunk 0 (part of dh0)
 #pragma unroll
@@ -368,18 +328,68 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
         for (int i = 0; i < SG; i++) Xb[at(NC) + (size_t)i * D] = __float2bfloat16_rn(0.0f);
 }
 
+// The dlog_alpha carry of every chunk, in parallel: chunk c receives from all
+// later rows the gate gradient sum_d R_c[i][d] S_prev(c + 1)[i][d] over K and
+// V (the bf16 adjoints and states; for the last chunk S_prev(c + 1) is the
+// final state, present only with its gradient), added to db1 of the chunk's
+// last state row, whose in-chunk suffix sum in the key-side kernel then hands
+// it to every row.  One warp per (head, chunk, slot); lanes split d.
+template <int D>
+__global__ void __launch_bounds__(256)
+adj_carry_kernel(const __nv_bfloat16* __restrict__ RKb, const __nv_bfloat16* __restrict__ RVb,
+                 const __nv_bfloat16* __restrict__ SKb, const __nv_bfloat16* __restrict__ SVb,
+                 const __nv_bfloat16* __restrict__ htb, float* __restrict__ db1, Shape call, int M, int has_dhT) {
+    constexpr int PL = D / 32;  // elements per lane
+    const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int i = (int)(wid % M), c = (int)((wid / M) % call.NCS), bh = (int)(wid / ((long)M * call.NCS));
+    if (bh >= call.BH) return;
+    const Shape sh = head_shape(call, bh);
+    if (c >= sh.NC || (c + 1 >= sh.NC && !has_dhT)) return;  // whole warp
+    const size_t ro = (((size_t)bh * sh.NCS + c) * M + i) * D + lane * PL;
+    const __nv_bfloat16 *sk, *sv;
+    if (c + 1 < sh.NC) {
+        const size_t so = (((size_t)bh * sh.NCS + c + 1) * M + i) * D + lane * PL;
+        sk = SKb + so;
+        sv = SVb + so;
+    } else {
+        sk = htb + (((size_t)bh * 2 + 0) * M + i) * D + lane * PL;
+        sv = htb + (((size_t)bh * 2 + 1) * M + i) * D + lane * PL;
+    }
+    float t = 0.0f;
+#pragma unroll
+    for (int e = 0; e < PL; e++)
+        t += __bfloat162float(RKb[ro + e]) * __bfloat162float(sk[e]) + __bfloat162float(RVb[ro + e]) * __bfloat162float(sv[e]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    if (lane == 0) {
+        const int last = min(c * kChunk + kChunk, sh.R) - 1;
+        db1[((size_t)bh * sh.NCS * kChunk + last) * M + i] += t;
+    }
+}
+
 cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st) {
     const Shape& sh = a.sh;
     if (sh.NCS == 0) return cudaSuccess;
     const dim3 grid(sh.BH, M / kAdjSlots);
-    if (D == 128)
+    const long warps = (long)sh.BH * sh.NCS * M;
+    const unsigned cgrid = (unsigned)((warps + 7) / 8);
+    const int has_dhT = a.dhTk != nullptr ? 1 : 0;
+    if (D == 128) {
         NHA_LAUNCH("adj_scan", st,
-                   adj_scan_kernel<128><<<grid, 256, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.wsDB1,
-                                                              a.dhTk, a.dhTv, a.io.htb, a.rend, sh, M));
-    else
+                   adj_scan_kernel<128><<<grid, 256, 0, st>>>(a.RK, a.RV, a.G, a.RKb, a.RVb, a.dhTk, a.dhTv, a.rend,
+                                                              sh, M));
+        NHA_LAUNCH("adj_carry", st,
+                   adj_carry_kernel<128><<<cgrid, 256, 0, st>>>(a.RKb, a.RVb, a.SKb, a.SVb, a.io.htb, a.wsDB1, sh, M,
+                                                                has_dhT));
+    } else {
         NHA_LAUNCH("adj_scan", st,
-                   adj_scan_kernel<64><<<grid, 128, 0, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb, a.wsDB1,
-                                                             a.dhTk, a.dhTv, a.io.htb, a.rend, sh, M));
+                   adj_scan_kernel<64><<<grid, 128, 0, st>>>(a.RK, a.RV, a.G, a.RKb, a.RVb, a.dhTk, a.dhTv, a.rend,
+                                                             sh, M));
+        NHA_LAUNCH("adj_carry", st,
+                   adj_carry_kernel<64><<<cgrid, 256, 0, st>>>(a.RKb, a.RVb, a.SKb, a.SVb, a.io.htb, a.wsDB1, sh, M,
+                                                               has_dhT));
+    }
     return cudaGetLastError();
 }
 
