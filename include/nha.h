@@ -297,6 +297,25 @@ nha_status_t nha_decode_step(const void* q, const void* k, const void* v, const 
                              int t, int B, int H, int d, int m, int w, nha_dtype_t dtype, float rope_base,
                              void* stream);
 
+/* nha_decode_step with launch flags (0 gives exactly nha_decode_step).
+ *
+ * Every decode launch may start before the kernel enqueued just before it on
+ * `stream` has finished (programmatic dependent launch): it reads and writes
+ * nothing before that kernel is done, so only its setup overlaps.
+ * NHA_DECODE_OVERLAP: the caller states that the kernel enqueued just before
+ * this call writes none of this call's state_k, state_v, ring_k, ring_v,
+ * ring_la (they belong to another layer, as in a stack of layers decoding
+ * one token each in turn).  The step then starts streaming its slot states
+ * and window ring in while that kernel is still running, and waits for it
+ * only before reading q, k, v, log_alpha and before writing.  Wrong when the
+ * previous kernel updates the same state (two steps of one layer back to
+ * back): leave the flag off there.  Unknown flag bits are rejected. */
+#define NHA_DECODE_OVERLAP 1u
+nha_status_t nha_decode_step_ex(const void* q, const void* k, const void* v, const float* log_alpha, void* o,
+                                float* state_k, float* state_v, void* ring_k, void* ring_v, float* ring_la, int t,
+                                int B, int H, int d, int m, int w, nha_dtype_t dtype, float rope_base, unsigned flags,
+                                void* stream);
+
 /* nha_decode_step with a position per sequence and, optionally, a window per
  * head.  Sequence b's heads decode token positions[b] (positions: DEVICE
  * array [B] of int32, read by the kernel, so a captured CUDA graph can be

@@ -29,7 +29,7 @@ EXPORTS = ("nha_workspace_bytes", "nha_forward", "nha_backward",
            "nha_workspace_bytes_ex", "nha_forward_ex", "nha_backward_ex",
            "nha_gate_total", "nha_state_combine", "nha_selftest_wait",
            "nha_varlen_pad", "nha_varlen_unpad",
-           "nha_decode_step", "nha_decode_step_varlen",
+           "nha_decode_step", "nha_decode_step_ex", "nha_decode_step_varlen",
            "nha_decode_prefill",
            "nha_forward_noalloc",
            "nha_launch_count", "nha_profile_begin", "nha_profile_end", "nha_status_string", "nha_last_error")
@@ -119,6 +119,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.nha_state_combine.argtypes = [vp] * 7 + [i] * 4 + [vp]
         lib.nha_decode_step.restype = i
         lib.nha_decode_step.argtypes = [vp] * 10 + [i] * 7 + [f, vp]
+        lib.nha_decode_step_ex.restype = i
+        lib.nha_decode_step_ex.argtypes = [vp] * 10 + [i] * 7 + [f, ctypes.c_uint, vp]
         lib.nha_decode_step_varlen.restype = i
         lib.nha_decode_step_varlen.argtypes = [vp] * 12 + [i] * 6 + [f, vp]
         lib.nha_decode_prefill.restype = i
@@ -439,12 +441,18 @@ def nha_decode_state(B, H, d, m, w, dtype=torch.bfloat16, device="cuda"):
             torch.zeros((B, H, n, m), dtype=torch.float32, device=device))
 
 
+DECODE_OVERLAP = 1  # NHA_DECODE_OVERLAP
+
+
 def nha_decode_step(q, k, v, log_alpha, t: int, w: int, state, rope_base: float = 10000.0, o=None,
-                     stream=None):
+                     stream=None, overlap=False):
     """o_t = nha_decode_step(q, k, v, log_alpha, t, w, state).
 
     q, k, v [B,H,d] and log_alpha [B,H,m] (fp32) are token t of every head;
-    ``state`` is the tuple from :func:`nha_decode_state`, updated in place."""
+    ``state`` is the tuple from :func:`nha_decode_state`, updated in place.
+    ``overlap``: the kernel enqueued just before on the stream writes none of
+    this state (another layer's step, say), so the step may stream its state
+    in while that kernel runs (nha_decode_step_ex with NHA_DECODE_OVERLAP)."""
     lib = load_library()
     B, H, d = q.shape
     m = log_alpha.shape[-1]
@@ -463,9 +471,9 @@ def nha_decode_step(q, k, v, log_alpha, t: int, w: int, state, rope_base: float 
     _check("ring_la", rla, torch.float32, (B, H, n, m))
     o = torch.empty_like(q) if o is None else o
     _check("o", o, dt, (B, H, d))
-    rc = lib.nha_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(sk), _ptr(sv),
-                             _ptr(rk), _ptr(rv), _ptr(rla), int(t), B, H, d, m, int(w), DTYPE[dt],
-                             float(rope_base), _stream_handle(stream))
+    rc = lib.nha_decode_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(o), _ptr(sk), _ptr(sv),
+                                _ptr(rk), _ptr(rv), _ptr(rla), int(t), B, H, d, m, int(w), DTYPE[dt],
+                                float(rope_base), DECODE_OVERLAP if overlap else 0, _stream_handle(stream))
     _raise(lib, rc)
     return o
 

@@ -444,7 +444,7 @@ namespace {
 nha_status_t decode_call(const void* q, const void* k, const void* v, const float* log_alpha, void* o,
                          float* state_k, float* state_v, void* ring_k, void* ring_v, float* ring_la, int t,
                          const int* tpos, const int* wvec, int B, int H, int d, int m, int w, nha_dtype_t dtype,
-                         float rope_base, void* stream) {
+                         float rope_base, void* stream, unsigned flags = 0) {
     if (inject("validate")) return fail(NHA_ERR_INTERNAL, "fault injected at validate");
     if (B < 0 || H < 0 || t < 0 || w < 0 || d <= 0 || m <= 0)
         return fail(NHA_ERR_INVALID_ARGUMENT, "negative or zero size (B=%d H=%d t=%d d=%d m=%d w=%d)", B, H, t,
@@ -484,6 +484,7 @@ nha_status_t decode_call(const void* q, const void* k, const void* v, const floa
     a.ring_v = w > 0 ? ring_v : nullptr;
     a.ring_la = w > 0 ? ring_la : nullptr;
     a.BH = (int)BH; a.t = t; a.w = w; a.tpos = tpos; a.wvec = wvec; a.H = H; a.sms = sms;
+    a.overlap = (flags & NHA_DECODE_OVERLAP) ? 1 : 0;
     make_rope(a.rope, d, rope_base);
     cudaStream_t s = (cudaStream_t)stream;
     const bool f32 = dtype == NHA_DTYPE_F32;
@@ -508,6 +509,16 @@ nha_status_t nha_decode_step(const void* q, const void* k, const void* v, const 
                              int B, int H, int d, int m, int w, nha_dtype_t dtype, float rope_base, void* stream) {
     return decode_call(q, k, v, log_alpha, o, state_k, state_v, ring_k, ring_v, ring_la, t, nullptr, nullptr, B, H,
                        d, m, w, dtype, rope_base, stream);
+}
+
+nha_status_t nha_decode_step_ex(const void* q, const void* k, const void* v, const float* log_alpha, void* o,
+                                float* state_k, float* state_v, void* ring_k, void* ring_v, float* ring_la, int t,
+                                int B, int H, int d, int m, int w, nha_dtype_t dtype, float rope_base, unsigned flags,
+                                void* stream) {
+    if ((flags & ~(unsigned)NHA_DECODE_OVERLAP) != 0)
+        return fail(NHA_ERR_INVALID_ARGUMENT, "unknown decode flags 0x%x", flags);
+    return decode_call(q, k, v, log_alpha, o, state_k, state_v, ring_k, ring_v, ring_la, t, nullptr, nullptr, B, H,
+                       d, m, w, dtype, rope_base, stream, flags);
 }
 
 nha_status_t nha_decode_step_varlen(const void* q, const void* k, const void* v, const float* log_alpha, void* o,

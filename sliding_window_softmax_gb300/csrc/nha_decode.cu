@@ -87,6 +87,11 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have finished and their writes are visible; let the next launch start.
+__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 template <int GL>
 __device__ __forceinline__ float group_sum(float x, unsigned mask) {
 #pragma unroll
@@ -111,12 +116,21 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
     const unsigned gmask = (GL == 32 ? 0xffffffffu : ((1u << GL) - 1u) << (lane / GL * GL));
     const int bh = blockIdx.x / ks;
     const int g = rank * NG + grp, G = ks * NG;
+    // Launched as a programmatic dependent of the kernel before it on the
+    // stream: nothing that kernel may write is read before grid_wait().  With
+    // `overlap` (positions and windows from the host, and the caller's word
+    // that the earlier kernel writes none of this call's states and ring) the
+    // first stages of states and ring are requested before the wait.
+    const bool early = a.overlap && a.tpos == nullptr && a.wvec == nullptr;
+    if (!early) grid_wait();
     const int t = a.tpos ? a.tpos[bh / a.H] : a.t;
     const int w = a.wvec ? a.wvec[bh % a.H] : a.w;  // this head's window
     const int wr = w > 0 ? w : 1;                    // ring entries the head cycles through
     const size_t wst = a.w > 0 ? a.w : 1;            // ring entries per head in memory
     // a position or window outside the supported range: NaN out, state untouched
     if (t < 0 || t >= (1 << 18) || w < 0 || w > a.w) {
+        if (early) grid_wait();
+        grid_launch_dependents();
         for (int e = rank * (D / ks) + tid; e < (rank + 1) * (D / ks); e += kDecThreads)
             ((Tin*)a.o)[(size_t)bh * D + e] = from_f<Tin>(__int_as_float(0x7fc00000));
         return;  // every CTA of the cluster serves this head and returns here, before any cluster barrier
@@ -184,6 +198,8 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
     };
 #pragma unroll
     for (int x = 0; x < kDecStages - 1; x++) issue_commit();
+    if (early) grid_wait();
+    grid_launch_dependents();  // the next launch may start; it waits for this grid to finish
 
     // ---- q, RoPE(q, t), cos/sin at t, and the token that leaves the window
     for (int e = tid; e < D; e += kDecThreads) {
@@ -406,24 +422,28 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
         }
         for (int i = tid; i < M; i += kDecThreads) a.ring_la[((size_t)bh * wst + en) * M + i] = la[i];
     }
-    // ---- merge the cluster: CTA `rank` writes o[e] for e in its share of d
+    // ---- merge the cluster: CTA `rank` writes o[e] for e in its share of d.
+    // Every remote read is issued at once: threads 0..ks-1 fetch the ranks'
+    // (max, sum); thread (e, r) of the first D threads fetches rank r's
+    // accumulator entry e, and the ks lanes of an e sum by shuffles.
     {
-        float mx = -INFINITY;
-        for (int r = 0; r < ks; r++) mx = fmaxf(mx, *cl.map_shared_rank(&bm, r));
-        float tot = 0.0f;
-        for (int r = 0; r < ks; r++) {
-            const float mr = *cl.map_shared_rank(&bm, r);
-            tot += mr == -INFINITY ? 0.0f : *cl.map_shared_rank(&bs, r) * ex2(mr - mx);
+        __shared__ float rm[8], rs[8];
+        if (tid < ks) {
+            rm[tid] = *cl.map_shared_rank(&bm, tid);
+            rs[tid] = *cl.map_shared_rank(&bs, tid);
         }
+        __syncthreads();
+        float mx = -INFINITY;
+        for (int r = 0; r < ks; r++) mx = fmaxf(mx, rm[r]);
+        float tot = 0.0f;
+        for (int r = 0; r < ks; r++) tot += rm[r] == -INFINITY ? 0.0f : rs[r] * ex2(rm[r] - mx);
         const float inv = 1.0f / tot;  // tot >= 1: the largest logit contributes exp(0)
         const int per = D / ks;
-        for (int e = rank * per + tid; e < (rank + 1) * per; e += kDecThreads) {
-            float o = 0.0f;
-            for (int r = 0; r < ks; r++) {
-                const float mr = *cl.map_shared_rank(&bm, r);
-                if (mr != -INFINITY) o += cl.map_shared_rank(bacc, r)[e] * ex2(mr - mx);
-            }
-            ((Tin*)a.o)[(size_t)bh * D + e] = from_f<Tin>(o * inv);
+        if (tid < D) {  // whole warps: D is a multiple of 32
+            const int e = rank * per + tid / ks, r = tid % ks;
+            float o = rm[r] == -INFINITY ? 0.0f : cl.map_shared_rank(bacc, r)[e] * ex2(rm[r] - mx);
+            for (int off = ks / 2; off > 0; off >>= 1) o += __shfl_xor_sync(0xffffffffu, o, off);
+            if (r == 0) ((Tin*)a.o)[(size_t)bh * D + e] = from_f<Tin>(o * inv);
         }
     }
     // keep this CTA's shared memory alive until the cluster has read it
@@ -472,13 +492,17 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
     cfg.blockDim = dim3(kDecThreads);
     cfg.dynamicSmemBytes = kDecSmem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)ks;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // may start before the previous kernel on the stream has finished (the
+    // kernel waits for it before touching anything it may write)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     NHA_LAUNCH("decode_step", st, e = cudaLaunchKernelEx(&cfg, kern, a));
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -31,6 +31,7 @@ struct DecodeArgs {
     const int* wvec;  // if set: device array [H] of per-head windows in [0, w] (w = the ring's length)
     int H;            // heads per sequence (b = bh / H indexes tpos)
     int sms;          // multiprocessors of the device (sizes the clusters)
+    int overlap;      // the kernel before this launch writes none of its states and ring: stream them in early
     RopeTab rope;
 };
 

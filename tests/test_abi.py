@@ -338,3 +338,10 @@ def test_varlen_extras_and_copies_validate(lib):
         assert fn(None, p, p, 2, 2, 10, 20, 8, 4, None) == 1
         assert fn(p, p, ctypes.c_void_p(4098), 2, 2, 10, 20, 8, 4, None) == 1
         assert fn(p, p, p, 0, 2, 10, 20, 8, 4, None) == 0           # nothing to move
+
+
+def test_decode_ex_rejects_unknown_flags(lib):
+    p = ctypes.c_void_p(4096)
+    args = (p,) * 10 + (0, 1, 1, 64, 16, 4, 1, 10000.0)
+    assert lib.nha_decode_step_ex(*args, 2, None) == 1 and b"flags" in lib.nha_last_error()
+    assert lib.nha_decode_step_ex(*args, 0x80000000, None) == 1

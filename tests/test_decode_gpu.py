@@ -337,3 +337,68 @@ def test_per_head_windows_prefill_and_varlen_decode(d, m, dtype):
     assert torch.isnan(o[:, 0]).all() and not torch.isnan(o[:, 1:]).any()
     for a, a0 in zip(state, before):
         assert torch.equal(a[:, 0], a0[:, 0])
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_overlapped_launches_of_interleaved_layers(graph):
+    """Layers decoding in turn with NHA_DECODE_OVERLAP (each launch streams its
+    state in while the previous layer's kernel runs) give the plain launches'
+    outputs and states bit for bit, eagerly and replayed from a CUDA graph;
+    the first layer's outputs also match the decode oracle."""
+    from sliding_window_softmax_gb300.synthetic import DecodeWorkload, make_decode_layer
+
+    nha = _nha()
+    dw = DecodeWorkload("overlap", B=3, H=4, d=128, m=64, w=96, t=500, layers=3, dtype="bf16", seed=2101)
+    base = [make_decode_layer(dw, i) for i in range(dw.layers)]
+
+    def clone(st):
+        return tuple(x.clone() for x in st)
+
+    plain = [clone(st) for _, st in base]
+    over = [clone(st) for _, st in base]
+    ref = DecodeState(dw.B, dw.H, dw.d, dw.m, dw.w)
+    ref.S_k, ref.S_v, ref.ring_k, ref.ring_v, ref.ring_la = (_np(x) for x in base[0][1])
+    g = torch.Generator(device="cuda").manual_seed(2102)
+    steps = 4
+    xs = [[dict(q=(torch.randn(3, 4, 128, generator=g, device="cuda") * 128 ** -0.25).bfloat16(),
+                k=(torch.randn(3, 4, 128, generator=g, device="cuda") * 128 ** -0.25).bfloat16(),
+                v=(torch.randn(3, 4, 128, generator=g, device="cuda") * 128 ** -0.25).bfloat16(),
+                log_alpha=torch.nn.functional.logsigmoid(torch.randn(3, 4, 64, generator=g, device="cuda") + 3))
+           for _ in range(dw.layers)] for _ in range(steps)]
+    o_plain = [[torch.empty(3, 4, 128, dtype=torch.bfloat16, device="cuda") for _ in range(dw.layers)]
+               for _ in range(steps)]
+    o_over = [[torch.empty_like(o) for o in row] for row in o_plain]
+    for s in range(steps):
+        for i in range(dw.layers):
+            x = xs[s][i]
+            nha.nha_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], dw.t + s, dw.w, plain[i], o=o_plain[s][i])
+
+    def run_overlapped():
+        for s in range(steps):
+            for i in range(dw.layers):
+                x = xs[s][i]
+                nha.nha_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], dw.t + s, dw.w, over[i],
+                                    o=o_over[s][i], overlap=True)
+
+    if graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=side):
+            run_overlapped()
+        torch.cuda.current_stream().wait_stream(side)
+        cg.replay()
+    else:
+        run_overlapped()
+    torch.cuda.synchronize()
+    for s in range(steps):
+        for i in range(dw.layers):
+            assert torch.equal(o_plain[s][i], o_over[s][i]), f"step {s} layer {i}"
+    for i in range(dw.layers):
+        for a, b in zip(plain[i], over[i]):
+            assert torch.equal(a, b), f"layer {i} state"
+    for s in range(steps):
+        x = xs[s][0]
+        ro = decode_step(ref, _np(x["q"]), _np(x["k"]), _np(x["v"]), _np(x["log_alpha"]), dw.t + s)
+        _check_o(_np(o_plain[s][0]), ro, "bf16", f"layer 0 step {s}")
+
