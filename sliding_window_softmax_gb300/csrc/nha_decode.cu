@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
     using V4 = typename Vec4<Tin>::T;
     extern __shared__ float4 stage[];  // [kDecStages][kPieces][kDecThreads]; later the groups' partials
     __shared__ float sq[D], sqr[D], skj[D], svj[D], slj[M];
+    __shared__ Tin tk[D], tv[D];  // token t's k, v (raw), its log_alpha
+    __shared__ float tla[M];
     __shared__ float2 cst[H2];  // cos, sin at position t
     __shared__ float2 gst[H2];  // e^{-i theta G}: the rotation between a group's consecutive tokens
     __shared__ float gmx[NG], gsum[NG];
@@ -198,28 +200,49 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
     };
 #pragma unroll
     for (int x = 0; x < kDecStages - 1; x++) issue_commit();
-    if (early) grid_wait();
-    grid_launch_dependents();  // the next launch may start; it waits for this grid to finish
 
-    // ---- q, RoPE(q, t), cos/sin at t, and the token that leaves the window
-    for (int e = tid; e < D; e += kDecThreads) {
-        sq[e] = to_f(q[e]);
-        if (absorb) {
-            skj[e] = to_f(w > 0 ? rk[(size_t)eo * D + e] : k[e]);
-            svj[e] = to_f(w > 0 ? rv[(size_t)eo * D + e] : v[e]);
-        }
-    }
-    if (absorb)
-        for (int i = tid; i < M; i += kDecThreads) slj[i] = w > 0 ? a.ring_la[((size_t)bh * wst + eo) * M + i] : la[i];
+    // ---- cos/sin at t and G, and the token that leaves the window when it
+    // comes from the ring (none of it from the earlier kernel, so before the
+    // wait when the launch overlaps)
     for (int i = tid; i < H2; i += kDecThreads) {
         float c, sn;
         rope_cs(a.rope, t, i, c, sn);
         cst[i] = make_float2(c, sn);
-        const float x = to_f(q[i]), y = to_f(q[i + H2]);
-        sqr[i] = x * c - y * sn;
-        sqr[i + H2] = y * c + x * sn;
         rope_cs(a.rope, G, i, c, sn);
         gst[i] = make_float2(c, -sn);
+    }
+    if (absorb && w > 0) {
+        for (int e = tid; e < D; e += kDecThreads) {
+            skj[e] = to_f(rk[(size_t)eo * D + e]);
+            svj[e] = to_f(rv[(size_t)eo * D + e]);
+        }
+        for (int i = tid; i < M; i += kDecThreads) slj[i] = a.ring_la[((size_t)bh * wst + eo) * M + i];
+    }
+    if (early) grid_wait();
+    grid_launch_dependents();  // the next launch may start; it waits for this grid to finish
+
+    // ---- q, RoPE(q, t), token t's k, v, log_alpha (the leaving token too when w = 0)
+    for (int e = tid; e < D; e += kDecThreads) {
+        const Tin ke = k[e], ve = v[e];
+        tk[e] = ke;
+        tv[e] = ve;
+        if (absorb && w == 0) {
+            skj[e] = to_f(ke);
+            svj[e] = to_f(ve);
+        }
+    }
+    for (int i = tid; i < M; i += kDecThreads) {
+        const float l = la[i];
+        tla[i] = l;
+        if (absorb && w == 0) slj[i] = l;
+    }
+    for (int i = tid; i < H2; i += kDecThreads) {
+        const float x = to_f(q[i]), y = to_f(q[i + H2]);
+        const float2 cs = cst[i];  // written by this thread above
+        sq[i] = x;
+        sq[i + H2] = y;
+        sqr[i] = x * cs.x - y * cs.y;
+        sqr[i + H2] = y * cs.x + x * cs.y;
     }
     __syncthreads();
 
@@ -370,9 +393,9 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
         float vl[4], vh[4], d0 = 0.0f;
 #pragma unroll
         for (int f = 0; f < 4; f++) {
-            const float x = to_f(k[4 * j + f]), y = to_f(k[H2 + 4 * j + f]);
-            vl[f] = to_f(v[4 * j + f]);
-            vh[f] = to_f(v[H2 + 4 * j + f]);
+            const float x = to_f(tk[4 * j + f]), y = to_f(tk[H2 + 4 * j + f]);
+            vl[f] = to_f(tv[4 * j + f]);
+            vh[f] = to_f(tv[H2 + 4 * j + f]);
             const float2 cs = cst[4 * j + f];
             d0 += sqr[4 * j + f] * (x * cs.x - y * cs.y) + sqr[H2 + 4 * j + f] * (y * cs.x + x * cs.y);
         }
@@ -417,17 +440,17 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_step_kernel(const Decod
         Tin* wk = (Tin*)a.ring_k + ((size_t)bh * wst + en) * D;
         Tin* wv = (Tin*)a.ring_v + ((size_t)bh * wst + en) * D;
         for (int e = tid; e < D; e += kDecThreads) {
-            wk[e] = k[e];
-            wv[e] = v[e];
+            wk[e] = tk[e];
+            wv[e] = tv[e];
         }
-        for (int i = tid; i < M; i += kDecThreads) a.ring_la[((size_t)bh * wst + en) * M + i] = la[i];
+        for (int i = tid; i < M; i += kDecThreads) a.ring_la[((size_t)bh * wst + en) * M + i] = tla[i];
     }
     // ---- merge the cluster: CTA `rank` writes o[e] for e in its share of d.
     // Every remote read is issued at once: threads 0..ks-1 fetch the ranks'
     // (max, sum); thread (e, r) of the first D threads fetches rank r's
     // accumulator entry e, and the ks lanes of an e sum by shuffles.
     {
-        __shared__ float rm[8], rs[8];
+        __shared__ float rm[16], rs[16];
         if (tid < ks) {
             rm[tid] = *cl.map_shared_rank(&bm, tid);
             rs[tid] = *cl.map_shared_rank(&bs, tid);
@@ -482,11 +505,13 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
         return n;
     }();
     int ks = decode_cluster(a, M, D, resident);
-    // tuning override of the cluster size (1, 2, 4 or 8 CTAs per head)
+    // tuning override of the cluster size (1, 2, 4, 8 or 16 CTAs per head; 16 is a non-portable cluster size)
     if (const char* env = getenv("NHA_DECODE_CLUSTER")) {
         const int v = atoi(env);
-        if (v == 1 || v == 2 || v == 4 || v == 8) ks = v;
+        if (v == 1 || v == 2 || v == 4 || v == 8 || v == 16) ks = v;
     }
+    if (ks > 8 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+        return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.BH * ks));
     cfg.blockDim = dim3(kDecThreads);
