@@ -95,10 +95,9 @@ def work_model(wl):
         # (K, V in; log_alpha in by the K and the V CTA; the bf16 states
         # entering each chunk out)
         "state_scan": (BH * 4 * m * d * R, BH * R * (2 * d * e + 8 * m) + BH * ((R + 63) // 64) * 4 * m * d),
-        # reverse adjoint scan: fp32 contributions in, bf16 adjoints out, K and V
-        "adj_scan": (0, BH * ((R + 63) // 64) * m * d * 12),
-        # chunk carries of dlog_alpha: bf16 adjoints and states in, K and V
-        "adj_carry": (BH * ((R + 63) // 64) * m * d * 4, BH * ((R + 63) // 64) * m * d * 8),
+        # reverse adjoint scan with the dlog_alpha carries: fp32 contributions
+        # and bf16 states in, bf16 adjoints out, K and V
+        "adj_scan": (BH * ((R + 63) // 64) * m * d * 4, BH * ((R + 63) // 64) * m * d * 16),
         "bwd_wdq_tc": wdq, "bwd_window_dq": wdq,
         "bwd_wkv_tc": wkv, "bwd_window_dkdv": wkv,
         "bwd_sq_tc": sq, "bwd_slot_query": sq,

@@ -257,138 +257,166 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
     if (warp == 0) tmem_dealloc(tm, 128);
 }
 
-constexpr int kAdjSlots = 4, kAdjDepth = 4;
+constexpr int kAdjDepth = 8, kAdjWarps = 2;
 
-// Reverse chunk scan of the slot adjoints.  R_c, the adjoint carried into
-// chunk c from the later chunks, follows R_{c - 1} = exp(G_c) R_c + dR_c
-// (dR_c: the chunk's own contribution, from the query-side kernel); it is
-// written in bf16 for the key-side kernel and the carry kernel below.  One
-// CTA per (head, 4 slots): D threads for K and D for V (thread = column d),
-// each with the loads of kAdjDepth chunks in flight and nothing else on its
-// path (no block barrier).  At most 64 registers a thread: a CTA then fits
-// beside a key-major window CTA on one SM, so the scan runs in that kernel's
-// shadow on the side stream.
+// Reverse chunk scan of the slot adjoints, fused with the dlog_alpha carry.
+// R_c, the adjoint carried into chunk c from the later chunks, follows
+// R_{c - 1} = exp(G_c) R_c + dR_c (dR_c: the chunk's own contribution, from the
+// query-side kernel); it is written in bf16 for the key-side kernel.  The carry
+// of chunk c, sum_d R_c[i][d] S_prev(c + 1)[i][d] over K and V (the bf16
+// states; for the last chunk the final state, present only with its
+// gradient), is the total over all later rows of the gate gradient that every
+// row of chunk c receives; it is added to db1 of the chunk's last state row,
+// whose in-chunk suffix sum in the key-side kernel hands it to every row.
+//
+// One warp per (head, slot): lane l holds elements d in [PL l, PL l + PL) of
+// the K and the V adjoint, so the carry is a warp sum and no barrier is
+// needed.  Each lane streams its own pieces of the next kAdjDepth chunks
+// (contributions, states, the decay and the db1 entry) into its own shared
+// memory stages with cp.async; a CTA of two warps needs about 25 KB and 64
+// threads, so it fits beside a key-major window CTA on one SM and the scan
+// runs in that kernel's shadow on the side stream.
 template <int D>
-__global__ void __launch_bounds__(2 * D, 4)
-adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, const float* __restrict__ G,
-                __nv_bfloat16* __restrict__ RKb, __nv_bfloat16* __restrict__ RVb, const float* __restrict__ dhTk,
-                const float* __restrict__ dhTv, float* __restrict__ rend, Shape call, int M) {
-    constexpr int SG = kAdjSlots, NP = kAdjDepth;
-    const int lane = threadIdx.x & 31;
-    const int tz = threadIdx.x / D, d = threadIdx.x % D;  // tz 0: K, 1: V
-    const int bh = blockIdx.x, i0 = SG * blockIdx.y;
+struct AdjStage {
+    static constexpr int PL = D / 32;
+    float xk[32 * PL], xv[32 * PL];            // dR_c, K and V
+    __nv_bfloat16 sk[32 * PL], sv[32 * PL];    // S_prev(c + 1), K and V
+    float g, db;                               // exp(G_c) of the slot, db1 entry of the chunk's last row
+    float pad[2];
+};
+
+template <int D>
+__global__ void __launch_bounds__(32 * kAdjWarps)
+adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, const __nv_bfloat16* __restrict__ SK,
+                const __nv_bfloat16* __restrict__ SV, const float* __restrict__ G, __nv_bfloat16* __restrict__ RKb,
+                __nv_bfloat16* __restrict__ RVb, float* __restrict__ db1, const float* __restrict__ dhTk,
+                const float* __restrict__ dhTv, const __nv_bfloat16* __restrict__ htb, float* __restrict__ rend,
+                Shape call, int M) {
+    constexpr int PL = D / 32, NP = kAdjDepth;
+    using Stage = AdjStage<D>;
+    extern __shared__ __align__(16) unsigned char adj_smem[];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const long wid = (long)blockIdx.x * kAdjWarps + wib;
+    if (wid >= (long)call.BH * M) return;  // whole warp
+    const int bh = (int)(wid / M), i = (int)(wid % M);
+    Stage* stages = reinterpret_cast<Stage*>(adj_smem) + (size_t)wib * NP;
     const Shape sh = head_shape(call, bh);
     const int NC = sh.NC, NCS = sh.NCS;  // this head's chunks; chunks per head in the arrays
-    const float* X = tz == 0 ? RK : RV;
-    __nv_bfloat16* Xb = tz == 0 ? RKb : RVb;
-    auto at = [&](int c) { return (((size_t)bh * NCS + c) * M + i0) * D + d; };
-    const float* dh = tz == 0 ? dhTk : dhTv;
-    auto load = [&](int c, float (&x)[SG], float (&g)[SG]) {
-        const size_t o = at(c);
-        const float* gc = G + ((size_t)bh * NCS + c) * M + i0;
-#pragma unroll
-        for (int i = 0; i < SG; i++) {
-            x[i] = X[o + (size_t)i * D];
-            g[i] = __ldg(gc + i);
+    const bool has_dhT = dhTk != nullptr;
+    const int e0 = lane * PL;
+    auto row = [&](int c) { return (((size_t)bh * NCS + c) * M + i) * D + e0; };  // [BH][NCS][M][D]
+    auto db_at = [&](int c) {
+        const int last = min(c * kChunk + kChunk, sh.R) - 1;
+        return ((size_t)bh * NCS * kChunk + last) * M + i;
+    };
+    // one commit group per chunk and lane (empty past the first chunk)
+    auto issue = [&](int c) {
+        if (c >= 0) {
+            Stage& st = stages[c % NP];
+            const size_t o = row(c);
+            const __nv_bfloat16 *sk, *sv;
+            bool sval = true;
+            if (c + 1 < NC) {
+                sk = SK + row(c + 1);
+                sv = SV + row(c + 1);
+            } else {  // the final state (bf16 copy), with its gradient only
+                sk = htb + (((size_t)bh * 2 + 0) * M + i) * D + e0;
+                sv = htb + (((size_t)bh * 2 + 1) * M + i) * D + e0;
+                sval = has_dhT;
+            }
+            if constexpr (PL == 4) {
+                cp_async16(st.xk + e0, RK + o, true);
+                cp_async16(st.xv + e0, RV + o, true);
+                cp_async8(st.sk + e0, sk, sval);
+                cp_async8(st.sv + e0, sv, sval);
+            } else {
+                cp_async8(st.xk + e0, RK + o, true);
+                cp_async8(st.xv + e0, RV + o, true);
+                cp_async4(st.sk + e0, sk, sval);
+                cp_async4(st.sv + e0, sv, sval);
+            }
+            if (lane == 0) {
+                cp_async4(&st.g, G + ((size_t)bh * NCS + c) * M + i, true);
+                cp_async4(&st.db, db1 + db_at(c), true);
+            }
         }
+        cp_async_commit();
     };
     // R enters the last chunk as the gradient of the final state (zero without one)
-    float R[SG];
+    float rk[PL], rv[PL];
 #pragma unroll
-    for (int i = 0; i < SG; i++) R[i] = dh != nullptr ? dh[((size_t)bh * M + i0 + i) * D + d] : 0.0f;
-    float x[NP][SG], g[NP][SG];
-#pragma unroll
-    for (int p = 0; p < NP; p++)
-        if (NC - 1 - p >= 0) load(NC - 1 - p, x[p], g[p]);
-    const bool odd = lane & 1;  // packed bf16 pairs, as in the state scan
-    for (int base = NC - 1; base >= 0; base -= NP) {
-#pragma unroll
-        for (int p = 0; p < NP; p++) {
-            const int c = base - p;
-            if (c < 0) break;  // uniform over the CTA
-            const size_t o = at(c);
-#pragma unroll
-            for (int i = 0; i < SG; i += 2) {
-                const float recv = __shfl_xor_sync(0xffffffffu, odd ? R[i] : R[i + 1], 1);
-                const uint32_t pk = odd ? pack_bf16(recv, R[i + 1]) : pack_bf16(R[i], recv);
-                *reinterpret_cast<uint32_t*>(Xb + o + (size_t)(i + (odd ? 1 : 0)) * D - (odd ? 1 : 0)) = pk;
-            }
-#pragma unroll
-            for (int i = 0; i < SG; i++) R[i] = g[p][i] * R[i] + x[p][i];  // g = exp(G_c)
-            if (c - NP >= 0) load(c - NP, x[p], g[p]);
-        }
+    for (int e = 0; e < PL; e++) {
+        rk[e] = has_dhT ? dhTk[((size_t)bh * M + i) * D + e0 + e] : 0.0f;
+        rv[e] = has_dhT ? dhTv[((size_t)bh * M + i) * D + e0 + e] : 0.0f;
     }
+#pragma unroll
+    for (int p = 0; p < NP; p++) issue(NC - 1 - p);
+    for (int c = NC - 1; c >= 0; c--) {
+        cp_async_wait<NP - 1>();  // this lane's pieces of chunk c
+        const Stage& st = stages[c % NP];
+        const size_t o = row(c);
+        uint32_t pk[PL / 2], pv[PL / 2];
+#pragma unroll
+        for (int e = 0; e < PL; e += 2) {
+            pk[e / 2] = pack_bf16(rk[e], rk[e + 1]);
+            pv[e / 2] = pack_bf16(rv[e], rv[e + 1]);
+        }
+        if constexpr (PL == 4) {
+            *reinterpret_cast<uint2*>(RKb + o) = make_uint2(pk[0], pk[1]);
+            *reinterpret_cast<uint2*>(RVb + o) = make_uint2(pv[0], pv[1]);
+        } else {
+            *reinterpret_cast<uint32_t*>(RKb + o) = pk[0];
+            *reinterpret_cast<uint32_t*>(RVb + o) = pv[0];
+        }
+        float t = 0.0f;
+#pragma unroll
+        for (int e = 0; e < PL; e++)
+            t += rk[e] * __bfloat162float(st.sk[e0 + e]) + rv[e] * __bfloat162float(st.sv[e0 + e]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+        const float g = __shfl_sync(0xffffffffu, lane == 0 ? st.g : 0.0f, 0);  // exp(G_c), landed in lane 0's stage
+        if (lane == 0 && (c + 1 < NC || has_dhT)) db1[db_at(c)] = st.db + t;
+#pragma unroll
+        for (int e = 0; e < PL; e++) {
+            rk[e] = g * rk[e] + st.xk[e0 + e];
+            rv[e] = g * rv[e] + st.xv[e0 + e];
+        }
+        issue(c - NP);  // into the stage just read (this lane's own pieces)
+    }
+    cp_async_wait<0>();
     if (rend != nullptr)  // the adjoint of the state before chunk 0 (part of dh0)
 #pragma unroll
-        for (int i = 0; i < SG; i++) rend[(((size_t)bh * 2 + tz) * M + i0 + i) * D + d] = R[i];
-    // per-head windows: zeros after this head's last chunk (read as the pair's
-    // second half by the key-side kernel)
+        for (int e = 0; e < PL; e++) {
+            rend[(((size_t)bh * 2 + 0) * M + i) * D + e0 + e] = rk[e];
+            rend[(((size_t)bh * 2 + 1) * M + i) * D + e0 + e] = rv[e];
+        }
+    // per-head windows and sequence lengths: zeros after this head's last
+    // chunk (read as the pair's second half by the key-side kernel)
     if (NC < NCS)
 #pragma unroll
-        for (int i = 0; i < SG; i++) Xb[at(NC) + (size_t)i * D] = __float2bfloat16_rn(0.0f);
-}
-
-// The dlog_alpha carry of every chunk, in parallel: chunk c receives from all
-// later rows the gate gradient sum_d R_c[i][d] S_prev(c + 1)[i][d] over K and
-// V (the bf16 adjoints and states; for the last chunk S_prev(c + 1) is the
-// final state, present only with its gradient), added to db1 of the chunk's
-// last state row, whose in-chunk suffix sum in the key-side kernel then hands
-// it to every row.  One warp per (head, chunk, slot); lanes split d.
-template <int D>
-__global__ void __launch_bounds__(256)
-adj_carry_kernel(const __nv_bfloat16* __restrict__ RKb, const __nv_bfloat16* __restrict__ RVb,
-                 const __nv_bfloat16* __restrict__ SKb, const __nv_bfloat16* __restrict__ SVb,
-                 const __nv_bfloat16* __restrict__ htb, float* __restrict__ db1, Shape call, int M, int has_dhT) {
-    constexpr int PL = D / 32;  // elements per lane
-    const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    const int i = (int)(wid % M), c = (int)((wid / M) % call.NCS), bh = (int)(wid / ((long)M * call.NCS));
-    if (bh >= call.BH) return;
-    const Shape sh = head_shape(call, bh);
-    if (c >= sh.NC || (c + 1 >= sh.NC && !has_dhT)) return;  // whole warp
-    const size_t ro = (((size_t)bh * sh.NCS + c) * M + i) * D + lane * PL;
-    const __nv_bfloat16 *sk, *sv;
-    if (c + 1 < sh.NC) {
-        const size_t so = (((size_t)bh * sh.NCS + c + 1) * M + i) * D + lane * PL;
-        sk = SKb + so;
-        sv = SVb + so;
-    } else {
-        sk = htb + (((size_t)bh * 2 + 0) * M + i) * D + lane * PL;
-        sv = htb + (((size_t)bh * 2 + 1) * M + i) * D + lane * PL;
-    }
-    float t = 0.0f;
-#pragma unroll
-    for (int e = 0; e < PL; e++)
-        t += __bfloat162float(RKb[ro + e]) * __bfloat162float(sk[e]) + __bfloat162float(RVb[ro + e]) * __bfloat162float(sv[e]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-    if (lane == 0) {
-        const int last = min(c * kChunk + kChunk, sh.R) - 1;
-        db1[((size_t)bh * sh.NCS * kChunk + last) * M + i] += t;
-    }
+        for (int e = 0; e < PL; e++) {
+            RKb[row(NC) + e] = __float2bfloat16_rn(0.0f);
+            RVb[row(NC) + e] = __float2bfloat16_rn(0.0f);
+        }
 }
 
 cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st) {
     const Shape& sh = a.sh;
     if (sh.NCS == 0) return cudaSuccess;
-    const dim3 grid(sh.BH, M / kAdjSlots);
-    const long warps = (long)sh.BH * sh.NCS * M;
-    const unsigned cgrid = (unsigned)((warps + 7) / 8);
-    const int has_dhT = a.dhTk != nullptr ? 1 : 0;
+    const long warps = (long)sh.BH * M;
+    const unsigned grid = (unsigned)((warps + kAdjWarps - 1) / kAdjWarps);
     if (D == 128) {
+        const size_t sm = sizeof(AdjStage<128>) * kAdjDepth * kAdjWarps;
         NHA_LAUNCH("adj_scan", st,
-                   adj_scan_kernel<128><<<grid, 256, 0, st>>>(a.RK, a.RV, a.G, a.RKb, a.RVb, a.dhTk, a.dhTv, a.rend,
-                                                              sh, M));
-        NHA_LAUNCH("adj_carry", st,
-                   adj_carry_kernel<128><<<cgrid, 256, 0, st>>>(a.RKb, a.RVb, a.SKb, a.SVb, a.io.htb, a.wsDB1, sh, M,
-                                                                has_dhT));
+                   adj_scan_kernel<128><<<grid, 32 * kAdjWarps, sm, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb,
+                                                                          a.wsDB1, a.dhTk, a.dhTv, a.io.htb, a.rend,
+                                                                          sh, M));
     } else {
+        const size_t sm = sizeof(AdjStage<64>) * kAdjDepth * kAdjWarps;
         NHA_LAUNCH("adj_scan", st,
-                   adj_scan_kernel<64><<<grid, 128, 0, st>>>(a.RK, a.RV, a.G, a.RKb, a.RVb, a.dhTk, a.dhTv, a.rend,
-                                                             sh, M));
-        NHA_LAUNCH("adj_carry", st,
-                   adj_carry_kernel<64><<<cgrid, 256, 0, st>>>(a.RKb, a.RVb, a.SKb, a.SVb, a.io.htb, a.wsDB1, sh, M,
-                                                               has_dhT));
+                   adj_scan_kernel<64><<<grid, 32 * kAdjWarps, sm, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb,
+                                                                         a.wsDB1, a.dhTk, a.dhTv, a.io.htb, a.rend,
+                                                                         sh, M));
     }
     return cudaGetLastError();
 }

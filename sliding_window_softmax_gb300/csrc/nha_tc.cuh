@@ -371,6 +371,11 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool va
                  "r"(valid ? 16 : 0)
                  : "memory");
 }
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
+                 "r"(valid ? 8 : 0)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async4(void* smem, const void* gmem, bool valid) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
                  "r"(valid ? 4 : 0)
