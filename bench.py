@@ -98,6 +98,8 @@ def work_model(wl):
         # reverse adjoint scan with the dlog_alpha carries: fp32 contributions
         # and bf16 states in, bf16 adjoints out, K and V
         "adj_scan": (BH * ((R + 63) // 64) * m * d * 4, BH * ((R + 63) // 64) * m * d * 16),
+        # RoPE(q), RoPE(k) in bf16 and the (cos, sin) table: q, k in, copies out
+        "rope_qk": (0, BH * T * 4 * d * e + T * d * 4),
         "bwd_wdq_tc": wdq, "bwd_window_dq": wdq,
         "bwd_wkv_tc": wkv, "bwd_window_dkdv": wkv,
         "bwd_sq_tc": sq, "bwd_slot_query": sq,

@@ -40,7 +40,7 @@ def test_work_model_conventions():
     assert mdl["step_bytes"] == mdl["fwd_bytes"] + 10 * (8 * 64 * 2 + 8 * 16 + 4)
     # every kernel the bench can name as dominant has a model
     big = bench.work_model(LAYER_1P3B)["kernels"]
-    for k in ("fwd_tc", "bwd_sk_tc", "bwd_sq_tc", "bwd_wkv_tc", "bwd_wdq_tc", "state_scan", "adj_scan"):
+    for k in ("fwd_tc", "bwd_sk_tc", "bwd_sq_tc", "bwd_wkv_tc", "bwd_wdq_tc", "state_scan", "adj_scan", "rope_qk"):
         assert big[k][1] > 0
 
 
