@@ -47,7 +47,7 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
                      int* __restrict__ status) {
     constexpr int NS = kScanStages;
     constexpr int NSL = M;
-    constexpr int TPS = 256 / M, RPT = kChunk / TPS;  // gate threads per slot, rows per gate thread
+    constexpr int NPART = 256 / M, RPT = kChunk / NPART;  // gate threads per slot, rows per gate thread
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     // stage s: X_c [64 tokens][128 d] (d >= D zero), U_c [64 tokens][64], log_alpha [64][M], exp(G_c) [M]
@@ -55,7 +55,8 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
     auto UT = [&](int st) { return base + NS * 16384 + st * 8192; };
     auto LA = [&](int st) { return reinterpret_cast<float*>(base + NS * 24576 + st * 16384); };
     auto GS = [&](int st) { return reinterpret_cast<float*>(base + NS * 40960 + st * 256); };
-    __shared__ uint64_t full[NS], ufull[NS], empty[NS], sfull[2], tfree[2], drain;
+    __shared__ uint64_t full[NS], ufull[NS], empty[NS], sfull[2], tfree[2], pbar[2], drain;
+    __shared__ float PT[2][NPART][M];  // the gate threads' row-part totals, by chunk parity
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -73,6 +74,7 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
         for (int q = 0; q < 2; q++) {
             mbar_init(&sfull[q], 1);
             mbar_init(&tfree[q], 4);
+            mbar_init(&pbar[q], 8);
         }
         mbar_init(&drain, 1);
         s_abort = 0;
@@ -127,41 +129,48 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
             }
         }
     } else if (warp >= 4) {
-        // ---------------- gate warps: thread = (slot i, RPT rows) ----------------
-        // the TPS parts of a slot sit in consecutive lanes, so the chunk's
-        // cumsum is finished with shuffles inside the warp
-        const int g = tid - 128, i = g / TPS, part = g % TPS, r0 = part * RPT;
+        // ---------------- gate warps: thread = (slot, RPT consecutive rows) ----------------
+        // A warp reads consecutive slots of a row (no shared-memory bank
+        // conflicts).  Each thread sums its rows; the NPART parts of a slot lie
+        // in different warps and exchange their totals through shared memory
+        // and the pbar barrier (bounded wait, double-buffered by chunk parity).
+        // With E_s = exp(G - b_s) (E_{-1} = exp(G)), U[s] = E_s u_s = E_s - E_{s-1}:
+        // one exp per element, and rows past the chunk's tokens (log_alpha 0)
+        // give U = 0 by themselves.
+        const int g = tid - 128, slot = g % M, part = g / M, r0 = part * RPT;
         for (int c = 0; c < NC; c++) {
-            const int st = c % NS, nr = rows_of(c);
+            const int st = c % NS, nr = rows_of(c), pb = c & 1;
             if (!mbar_wait_ab(&full[st], (c / NS) & 1, kWaitCycles, abort)) break;
             const float* lr = LA(st);
-            float l[RPT], b[RPT], acc = 0.0f;
+            float b[RPT], acc = 0.0f;
 #pragma unroll
             for (int r = 0; r < RPT; r++) {
-                l[r] = (r0 + r < nr) ? lr[(r0 + r) * M + i] : 0.0f;
-                acc += l[r];
+                acc += (r0 + r < nr) ? lr[(r0 + r) * M + slot] : 0.0f;
                 b[r] = acc;
             }
-            // exclusive prefix of the parts' sums (offset) and the chunk total
-            float off = 0.0f, Gt = acc;
+            PT[pb][part][slot] = acc;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pbar[pb]);
+            if (!mbar_wait_ab(&pbar[pb], (c >> 1) & 1, kWaitCycles, abort)) break;
+            float off = 0.0f, Gt = 0.0f;  // parts before this one; the chunk total
 #pragma unroll
-            for (int sft = 1; sft < TPS; sft <<= 1) {
-                const float up = __shfl_up_sync(0xffffffffu, Gt, sft);
-                if (part >= sft) Gt += up;
+            for (int p2 = 0; p2 < NPART; p2++) {
+                const float t = PT[pb][p2][slot];
+                if (p2 < part) off += t;
+                Gt += t;
             }
-            off = Gt - acc;                                                // parts before this one
-            Gt = __shfl_sync(0xffffffffu, Gt, (lane / TPS) * TPS + TPS - 1);  // the last part's inclusive sum
+            float ep = fexp(Gt - off);  // E of the row before this part's first row
             unsigned char* ut = UT(st);
 #pragma unroll
             for (int r = 0; r < RPT; r++) {
-                const int row = r0 + r;
-                const float u = row < nr ? fexp(Gt - (b[r] + off)) * one_minus_exp(l[r]) : 0.0f;
-                *reinterpret_cast<__nv_bfloat16*>(ut + sw_off(row, i, 64)) = __float2bfloat16_rn(u);
+                const float e = fexp(Gt - (b[r] + off));
+                *reinterpret_cast<__nv_bfloat16*>(ut + sw_off(r0 + r, slot, 64)) = __float2bfloat16_rn(e - ep);
+                ep = e;
             }
-            if (part == 0) {
+            if (part == 0) {  // E_{-1} = exp(G): the chunk's decay
                 const float eg = fexp(Gt);
-                GS(st)[i] = eg;
-                if (tz == 0) G[((size_t)bh * NCS + c) * M + i] = eg;  // for the backward's adjoint scan
+                GS(st)[slot] = eg;
+                if (tz == 0) G[((size_t)bh * NCS + c) * M + slot] = eg;  // for the backward's adjoint scan
                 if (Gt < kGateRange) atomicOr(status, kStatusGateRangeBit);
             }
             fence_async_smem();  // U is an MMA operand: generic writes -> async proxy
@@ -207,14 +216,20 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
             }
             // S_prev(c + 1) = exp(G_c) S_prev(c) + dS_c, dS_c read from TMEM in
             // groups of at most 32 columns (fewer registers live at once)
-            const float* g = GS(st) + i0;  // exp(G_c)
+            const float4* g4 = reinterpret_cast<const float4*>(GS(st) + i0);  // exp(G_c)
             constexpr int GRP = NSL < 32 ? NSL : 32;
 #pragma unroll
             for (int h = 0; h < NSL; h += GRP) {
                 float dS[GRP];
                 tmem_ld(tl + 64 * b + h, dS, GRP);
 #pragma unroll
-                for (int i = 0; i < GRP; i++) S[h + i] = g[h + i] * S[h + i] + dS[i];
+                for (int i = 0; i < GRP; i += 4) {
+                    const float4 gv = g4[(h + i) / 4];
+                    S[h + i] = gv.x * S[h + i] + dS[i];
+                    S[h + i + 1] = gv.y * S[h + i + 1] + dS[i + 1];
+                    S[h + i + 2] = gv.z * S[h + i + 2] + dS[i + 2];
+                    S[h + i + 3] = gv.w * S[h + i + 3] + dS[i + 3];
+                }
             }
             fence_before_sync();
             __syncwarp();
