@@ -54,7 +54,8 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
     float* sG = s_tot + 4 * M;                             // [2][M]
     float* redm = sG + 2 * M;                              // [2][128]
     float* reds = redm + 256;                              // [2][128]
-    __shared__ uint64_t bar, gbar, sbar, qbar, full[NS], sfull[2], pready, bdone[2], drain[2];
+    __shared__ uint64_t bar, gbar, sbar, qbar, full[NS], sfull[2], pready, bdone[2], drain[2], s1done;
+    __shared__ int s_sv_issued;  // the producer issued the [S^V] pair copy (sbar phase 1)
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -83,6 +84,8 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
         mbar_init(&bar, 1);
         mbar_init(&gbar, 1);
         mbar_init(&sbar, 1);
+        mbar_init(&s1done, 1);
+        s_sv_issued = 0;
         mbar_init(&qbar, 1);
         for (int q = 0; q < NS; q++) mbar_init(&full[q], 1);
         for (int q = 0; q < 2; q++) {
@@ -104,13 +107,36 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
     // keys of every window block) at 256, O_1 (the other 64 keys) at 256 + D
     const uint32_t tA = 0, tO = 256, tO1 = 256 + D;
 
-    int s_issued = 0;  // thread 0: slot-branch operand copies issued (phases of sbar)
     int last_ph[NS];  // producer: phase of the last load issued into each stage
 #pragma unroll
     for (int q = 0; q < NS; q++) last_ph[q] = -1;
 
     if (warp == 8) {
         // ---------------- producer ----------------
+        if (slot && lane == 0) {
+            // The slot phase's first products (Q K_c^T and Q [S^K]^T) as soon as
+            // their operands land, while the tile warps form the gates; then the
+            // [S^V] pair into the [S^K] buffer they consumed, so its copy runs
+            // during the gates and the slot logits.
+            if (mbar_wait_ab(&sbar, 0, kWaitCycles, abort)) {
+                fence_after_sync();
+                const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[0]), s3 = smem_u32(KB[1]);
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_bf16(tm + tA, desc_k(s0, 128, kk), desc_k(s1, 128, kk), idesc_bf16(128, 128, false), kk > 0);
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_bf16(tm + tO, desc_k(s0, 128, kk), desc_k(s3, 2 * M, kk), idesc_bf16(128, 2 * M, false), kk > 0);
+                mma_commit(&bar);
+                mma_commit(&s1done);
+                if (mbar_wait_ab(&s1done, 0, kWaitCycles, abort)) {
+                    s_sv_issued = 1;
+                    mbar_arrive_expect_tx(&sbar, 2 * M * D * 2);
+#pragma unroll
+                    for (int xx = 0; xx < D; xx += 64)
+                        tma_load_3d(KB[1] + xx * 4 * M, &maps.sv, xx, (j0 / kChunk) * M, bh, &sbar);
+                }
+            }
+        }
+        __syncwarp();
         named_sync(2, kFwdThreads);  // the slot phase is done with the stage buffers
         if (lane == 0 && nb > 0 && !s_abort) {
             const bool o0 = slot;  // O_0 already holds the slot branch
@@ -181,7 +207,6 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
             // Rows past the tile's states are other rows or zeros; the masks and
             // zero gates keep them out of every product.
             if (tid == 0) {
-                s_issued = 1;
                 mbar_arrive_expect_tx(&sbar, 3 * TB + 2 * M * D * 2);
 #pragma unroll
                 for (int xx = 0; xx < D; xx += 64) {
@@ -204,31 +229,15 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
 #pragma unroll
                 for (int jj = 0; jj < HM; jj++) {
                     rho[jj] = 0.5f * sG[cr * M + h * HM + jj];
-                    ek[jj] = row_ok ? fexp(rho[jj] - b[jj]) * (-expm1f(lg[jj])) : 0.0f;
+                    ek[jj] = row_ok ? fexp(rho[jj] - b[jj]) * one_minus_exp(lg[jj]) : 0.0f;
                 }
                 store_row(VB[1], r, h * HM, ek, HM);
             }
             sync_for_mma<true>();
-            if (tid == 0) {
-                if (!mbar_wait(&sbar, 0, kWaitCycles)) *abort = 1;
-                fence_after_sync();
-                const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[0]), s3 = smem_u32(KB[1]);
-                for (int kk = 0; kk < D / 16; kk++)
-                    mma_bf16(tm + tA, desc_k(s0, 128, kk), desc_k(s1, 128, kk), idesc_bf16(128, 128, false), kk > 0);
-                for (int kk = 0; kk < D / 16; kk++)
-                    mma_bf16(tm + tO, desc_k(s0, 128, kk), desc_k(s3, 2 * M, kk), idesc_bf16(128, 2 * M, false), kk > 0);
-                mma_commit(&bar);
-            }
-            ok = ctl.wait();
+            ok = ctl.wait();  // Q K_c^T and Q [S^K]^T, issued by the producer warp
             if (ok) {
-                // A = Q K_c^T masked to the row's own chunk and s <= r; [S^V] replaces [S^K]
+                // A = Q K_c^T masked to the row's own chunk and s <= r ([S^V] is on its way)
                 mask_to_tile(tl + tA, KB[0], r, h, cr, row_ok, false);
-                if (tid == 0) {  // [S^K] consumed: the [S^V] pair in flight
-                    s_issued = 2;
-                    mbar_arrive_expect_tx(&sbar, 2 * M * D * 2);
-#pragma unroll
-                    for (int xx = 0; xx < D; xx += 64) tma_load_3d(KB[1] + xx * 4 * M, &maps.sv, xx, c1 * M, bh, &sbar);
-                }
                 sync_for_mma<true>();
                 if (tid == 0) {
                     const uint32_t s1 = smem_u32(KB[0]), s2 = smem_u32(VB[1]);
@@ -440,11 +449,11 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
             mma_commit(&drain[0]);
             mbar_wait(&drain[0], 0, kWaitCycles);
             if (slot) mbar_wait(&gbar, 0, kWaitCycles);
-            for (int q = 0; q < s_issued; q++) mbar_wait(&sbar, (uint32_t)q, kWaitCycles);
         }
-        if (warp == 8 && lane == 0) {  // window MMAs and copies
+        if (warp == 8 && lane == 0) {  // its MMAs, the slot operand copies (sbar phases 0, 1), window copies
             mma_commit(&drain[1]);
             mbar_wait(&drain[1], 0, kWaitCycles);
+            if (slot) mbar_wait(&sbar, s_sv_issued ? 1u : 0u, kWaitCycles);  // phase 1 completes after phase 0
             if (nb > 0) mbar_wait(&qbar, 0, kWaitCycles);
             for (int q = 0; q < NS; q++)
                 if (last_ph[q] >= 0) mbar_wait(&full[q], (uint32_t)last_ph[q], kWaitCycles);

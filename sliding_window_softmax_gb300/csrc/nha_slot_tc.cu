@@ -155,7 +155,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
     {  // Ek tile
         float ek[HM];
 #pragma unroll
-        for (int jj = 0; jj < HM; jj++) ek[jj] = row_ok ? fexp(rho[jj] - b[jj]) * (-expm1f(l[jj])) : 0.0f;
+        for (int jj = 0; jj < HM; jj++) ek[jj] = row_ok ? fexp(rho[jj] - b[jj]) * one_minus_exp(l[jj]) : 0.0f;
         store_row(XE, r, h * HM, ek, HM);
     }
     const float lse_r = row_ok ? a.lse[hoff + t] : 0.0f;
@@ -529,7 +529,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         float ek[HM], eke[HM], z[HM];
 #pragma unroll
         for (int jj = 0; jj < HM; jj++) {
-            ek[jj] = slot_ok ? fexp(-b[jj]) * (-expm1f(l[jj])) : 0.0f;
+            ek[jj] = slot_ok ? fexp(-b[jj]) * one_minus_exp(l[jj]) : 0.0f;
             eke[jj] = ek[jj] * fexp(0.5f * Grow[jj]);
             z[jj] = 0.0f;
         }
@@ -668,7 +668,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
             const float4 d4 = slot_ok ? *reinterpret_cast<const float4*>(db1 + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
             const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-            for (int q = 0; q < 4; q++) db[jj + q] = slot_ok ? dd[q] - (-expm1f(l[jj + q])) * du[jj + q] : 0.0f;
+            for (int q = 0; q < 4; q++) db[jj + q] = slot_ok ? dd[q] - one_minus_exp(l[jj + q]) * du[jj + q] : 0.0f;
         }
         chunk_suffix<M>(db, s_tot, warp, lane, h);
         // staged in XB (16-byte chunk q of the half row at q ^ (r & 7)), copied out coalesced
