@@ -185,3 +185,49 @@ def test_segments_chained_through_final_states(dtype):
     torch.cuda.synchronize()
     _cmp("final hTk", state[0], rhk, dtype, "state")
     _cmp("final hTv", state[1], rhv, dtype, "state")
+
+
+@pytest.mark.parametrize("windows", [None, [100, 0]])
+def test_long_chunk_scan_with_slot_states(windows):
+    """Few heads over many chunks (127 and 128 chunks of 64 tokens), h0 in
+    and hT out, compared with the oracle, forward and backward, with per-head
+    windows (so the heads have different chunk counts)."""
+    import sliding_window_softmax_gb300 as nha
+
+    wl = Workload("long scan", 1, 2, 8192, 64, 16, 100, dtype="bf16", seed=2201)
+    x = make_inputs(wl)
+    g = torch.Generator().manual_seed(2202)
+    h0 = (torch.randn(1, 2, 16, 64, generator=g) * 0.3 * 64 ** -0.25, torch.randn(1, 2, 16, 64, generator=g))
+    dhT = (torch.randn(1, 2, 16, 64, generator=g) * 0.1, torch.randn(1, 2, 16, 64, generator=g) * 0.1)
+    d = {n: t.cuda() for n, t in x.items()}
+    hd = tuple(t.cuda() for t in h0)
+    gd = tuple(t.cuda() for t in dhT)
+    wv = None if windows is None else torch.tensor(windows, dtype=torch.int32, device="cuda")
+    o, lse, hT = nha.nha_forward(d["q"], d["k"], d["v"], d["log_alpha"], w=wl.w, h0=hd, return_state=True,
+                                 windows=wv)
+    gr = nha.nha_backward(d["q"], d["k"], d["v"], d["log_alpha"], o, lse, d["dout"], w=wl.w, h0=hd, dhT=gd,
+                          windows=wv)
+    torch.cuda.synchronize()
+    got = dict(o=o, lse=lse, hTk=hT[0], hTv=hT[1], dq=gr[0], dk=gr[1], dv=gr[2], dlog_alpha=gr[3], dh0k=gr[4],
+               dh0v=gr[5])
+    got = {n: t.double().cpu().numpy() for n, t in got.items()}
+    for h in range(2):
+        wh = wl.w if windows is None else windows[h]
+        sel = {n: t[:, h:h + 1] for n, t in x.items()}
+        hs = (h0[0][:, h:h + 1], h0[1][:, h:h + 1])
+        gs = (dhT[0][:, h:h + 1], dhT[1][:, h:h + 1])
+        fo = oracle.forward(sel["q"], sel["k"], sel["v"], sel["log_alpha"], wh, h0=hs, return_state=True)
+        rg = oracle.backward(sel["q"], sel["k"], sel["v"], sel["log_alpha"], sel["dout"], wh, h0=hs, dhT=gs)
+        ref = dict(o=fo[0], lse=fo[1], hTk=fo[2], hTv=fo[3], dq=rg[0], dk=rg[1], dv=rg[2], dlog_alpha=rg[3],
+                   dh0k=rg[4], dh0v=rg[5])
+        for n, r in ref.items():
+            gv = got[n][:, h:h + 1]
+            err = np.abs(gv - r)
+            rel = np.linalg.norm(gv - r) / max(np.linalg.norm(r), 1e-30)
+            assert np.all(np.isfinite(gv)), f"head {h} {n}: non-finite"
+            if n == "lse":
+                assert err.max() <= 2e-2, f"head {h} {n}: max {err.max():.3e}"
+            elif n in ("o", "hTk", "hTv"):
+                assert rel <= 5e-3 and err.max() <= 2e-2, f"head {h} {n}: rel {rel:.3e} max {err.max():.3e}"
+            else:
+                assert rel <= 1e-2, f"head {h} {n}: rel {rel:.3e}"
