@@ -206,6 +206,11 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
             // operand tiles by TMA (thread 0): q, k_c, v_c rows and the [S^K] pair.
             // Rows past the tile's states are other rows or zeros; the masks and
             // zero gates keep them out of every product.
+            if (tid == 0) {  // log_alpha rows first (the gates wait for them), into the last stage's K~ buffer
+                mbar_arrive_expect_tx(&gbar, (uint32_t)(((M + 31) / 32) * 16384));
+#pragma unroll
+                for (int xx = 0; xx < M; xx += 32) tma_load_3d(KB[NS - 1] + xx * 512, &maps.la, xx, j0, bh, &gbar);
+            }
             if (tid == 0) {
                 mbar_arrive_expect_tx(&sbar, 3 * TB + 2 * M * D * 2);
 #pragma unroll
@@ -215,11 +220,6 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
                     tma_load_3d(VB[0] + xx * 256, &maps.v, xx, j0, bh, &sbar);
                     tma_load_3d(KB[1] + xx * 4 * M, &maps.sk, xx, c1 * M, bh, &sbar);
                 }
-            }
-            if (tid == 0) {  // log_alpha rows by TMA into the last stage's K~ buffer (idle here)
-                mbar_arrive_expect_tx(&gbar, (uint32_t)(((M + 31) / 32) * 16384));
-#pragma unroll
-                for (int xx = 0; xx < M; xx += 32) tma_load_3d(KB[NS - 1] + xx * 512, &maps.la, xx, j0, bh, &gbar);
             }
             if (!mbar_wait(&gbar, 0, kWaitCycles)) *abort = 1;
             float lg[HM], b[HM], rho[HM];
