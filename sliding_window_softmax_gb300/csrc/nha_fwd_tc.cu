@@ -54,7 +54,7 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
     float* sG = s_tot + 4 * M;                             // [2][M]
     float* redm = sG + 2 * M;                              // [2][128]
     float* reds = redm + 256;                              // [2][128]
-    __shared__ uint64_t bar, gbar, sbar, qbar, full[NS], sfull[2], pready, bdone[2], drain[2], s1done;
+    __shared__ uint64_t bar, gbar, sbar, qbar, full[NS], sfull[2], pready, bdone[2], drain[2], s1done, s2free;
     __shared__ int s_sv_issued;  // the producer issued the [S^V] pair copy (sbar phase 1)
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -85,6 +85,7 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
         mbar_init(&gbar, 1);
         mbar_init(&sbar, 1);
         mbar_init(&s1done, 1);
+        mbar_init(&s2free, 8);
         s_sv_issued = 0;
         mbar_init(&qbar, 1);
         for (int q = 0; q < NS; q++) mbar_init(&full[q], 1);
@@ -111,8 +112,23 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
 #pragma unroll
     for (int q = 0; q < NS; q++) last_ph[q] = -1;
 
+    // Window block j goes through stage (j + 2) % NS: block 0 through the last
+    // stage, whose K~ buffer held the slot phase's log_alpha rows and whose V
+    // buffer its scratch, so it can be loaded before the slot phase ends.
+    auto stage_of = [](int j) { return (j + 2) % NS; };
     if (warp == 8) {
         // ---------------- producer ----------------
+        auto load_block = [&](int j) {
+            const int stg = stage_of(j), kb = klo + j * 128;
+            mbar_arrive_expect_tx(&full[stg], 2 * TB);
+#pragma unroll
+            for (int xx = 0; xx < D; xx += 64) {
+                tma_load_3d(KB[stg] + xx * 256, &maps.k, xx, kb, bh, &full[stg]);
+                tma_load_3d(VB[stg] + xx * 256, &maps.v, xx, kb, bh, &full[stg]);
+            }
+            last_ph[stg] = (j / NS) & 1;
+        };
+        bool q_early = false, b0_early = false;
         if (slot && lane == 0) {
             // The slot phase's first products (Q K_c^T and Q [S^K]^T) as soon as
             // their operands land, while the tile warps form the gates; then the
@@ -133,45 +149,50 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
 #pragma unroll
                     for (int xx = 0; xx < D; xx += 64)
                         tma_load_3d(KB[1] + xx * 4 * M, &maps.sv, xx, (j0 / kChunk) * M, bh, &sbar);
+                    // q is read by the first products only: RoPE(q) for the window may replace it
+                    if (nb > 0) {
+                        q_early = true;
+                        mbar_arrive_expect_tx(&qbar, TB);
+#pragma unroll
+                        for (int xx = 0; xx < D; xx += 64) tma_load_3d(X0 + xx * 256, &maps.q, xx, tbase, bh, &qbar);
+                    }
                 }
+            }
+            // the window's first block once the tile warps are done with the last stage
+            if (nb > 0 && !s_abort && mbar_wait_ab(&s2free, 0, kWaitCycles, abort)) {
+                b0_early = true;
+                load_block(0);
             }
         }
         __syncwarp();
         named_sync(2, kFwdThreads);  // the slot phase is done with the stage buffers
         if (lane == 0 && nb > 0 && !s_abort) {
             const bool o0 = slot;  // O_0 already holds the slot branch
-            auto load_block = [&](int j) {
-                const int stg = j % NS, kb = klo + j * 128;
-                mbar_arrive_expect_tx(&full[stg], 2 * TB);
-#pragma unroll
-                for (int xx = 0; xx < D; xx += 64) {
-                    tma_load_3d(KB[stg] + xx * 256, &maps.k, xx, kb, bh, &full[stg]);
-                    tma_load_3d(VB[stg] + xx * 256, &maps.v, xx, kb, bh, &full[stg]);
-                }
-                last_ph[stg] = (j / NS) & 1;
-            };
             auto issue_s = [&](int j) {
-                const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[j % NS]);
+                const uint32_t s0 = smem_u32(X0), s1 = smem_u32(KB[stage_of(j)]);
                 for (int kk = 0; kk < D / 16; kk++)
                     mma_bf16(tm + 128 * (j & 1), desc_k(s0, 128, kk), desc_k(s1, 128, kk),
                              idesc_bf16(128, 128, false), kk > 0);
                 mma_commit(&sfull[j & 1]);
             };
-            mbar_arrive_expect_tx(&qbar, TB);
+            if (!q_early) {
+                mbar_arrive_expect_tx(&qbar, TB);
 #pragma unroll
-            for (int xx = 0; xx < D; xx += 64) tma_load_3d(X0 + xx * 256, &maps.q, xx, tbase, bh, &qbar);
-            for (int j = 0; j < min(NS, nb); j++) load_block(j);
-            bool ok = mbar_wait_ab(&qbar, 0, kWaitCycles, abort) && mbar_wait_ab(&full[0], 0, kWaitCycles, abort);
+                for (int xx = 0; xx < D; xx += 64) tma_load_3d(X0 + xx * 256, &maps.q, xx, tbase, bh, &qbar);
+            }
+            for (int j = b0_early ? 1 : 0; j < min(NS, nb); j++) load_block(j);
+            bool ok = mbar_wait_ab(&qbar, 0, kWaitCycles, abort) &&
+                      mbar_wait_ab(&full[stage_of(0)], 0, kWaitCycles, abort);
             if (ok) issue_s(0);
             for (int i = 0; i < nb && ok; i++) {
                 if (i + 1 < nb) {  // S buffer (i + 1) & 1 was read by block i - 1 (before its pready)
-                    if (!(ok = mbar_wait_ab(&full[(i + 1) % NS], ((i + 1) / NS) & 1, kWaitCycles, abort))) break;
+                    if (!(ok = mbar_wait_ab(&full[stage_of(i + 1)], ((i + 1) / NS) & 1, kWaitCycles, abort))) break;
                     issue_s(i + 1);
                 }
                 if (!(ok = mbar_wait_ab(&pready, i & 1, kWaitCycles, abort))) break;
                 fence_after_sync();
                 {
-                    const uint32_t sp = smem_u32(KB[i % NS]), sv = smem_u32(VB[i % NS]);
+                    const uint32_t sp = smem_u32(KB[stage_of(i)]), sv = smem_u32(VB[stage_of(i)]);
                     for (int kk = 0; kk < 4; kk++)
                         mma_bf16(tm + tO, desc_k(sp, 128, kk), desc_mn(sv, 128, kk), idesc_bf16(128, D, true),
                                  (o0 || i > 0 || kk > 0) ? 1u : 0u);
@@ -276,6 +297,9 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
                 store_row(VB[1] + 16384, r, h * HM, pq, HM);  // pEq, after Ek
                 named_sync(1, kTcThreads);
                 l = reds[r] + reds[128 + r];
+                // the last stage (log_alpha rows, scratch) is free: the producer loads window block 0
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s2free);
                 sync_for_mma<true>();
                 if (tid == 0) {
                     if (!mbar_wait(&sbar, 1, kWaitCycles)) *abort = 1;  // the [S^V] pair
@@ -315,7 +339,7 @@ fwd_tc_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps, int* __rest
         // ---- window branch: 128-key blocks of the band [tbase - w + 1, tbase + nq - 1]
         const int t = tbase + r;
         for (int i = 0; i < nb && ok; i++) {
-            const int kb = klo + i * 128, nk = min(128, khi - kb + 1), b = i & 1, stg = i % NS;
+            const int kb = klo + i * 128, nk = min(128, khi - kb + 1), b = i & 1, stg = stage_of(i);
             if (!(ok = mbar_wait_ab(&sfull[b], (i >> 1) & 1, kWaitCycles, abort))) break;
             fence_after_sync();
             float sv[64];
