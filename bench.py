@@ -78,10 +78,10 @@ def work_model(wl):
     # q~, dout, k~, v, lse, D in; dk, dv partials out
     wkv = (BH * 8 * d * n_sum, BH * T * (6 * d * e + 8))
     # q, k, v, dout, dq partials, log_alpha, lse, D_win, D^ in; state pairs in;
-    # dq, sigma dL, P_L (bf16), db1, D out; fp32 chunk adjoint contributions out
+    # dq, sigma dL, P_L (bf16), db1, D out; bf16 chunk adjoint contributions out
     sq = (BH * 12 * m * d * R,
           BH * T * (7 * d * e + 4 * m + 16) + BH * R * (2 * 2 * m + 4 * m) + BH * tiles * 2 * pair
-          + BH * ((R + 63) // 64) * 2 * m * d * 4)
+          + BH * ((R + 63) // 64) * 2 * m * d * 2)
     # q, dout, k, v, dk / dv partials in; dk, dv out; log_alpha, sigma dL, P_L,
     # db1 in; dlog_alpha out; adjoint pairs in
     sk = (BH * 12 * m * d * R,
@@ -95,9 +95,9 @@ def work_model(wl):
         # (K, V in; log_alpha in by the K and the V CTA; the bf16 states
         # entering each chunk out)
         "state_scan": (BH * 4 * m * d * R, BH * R * (2 * d * e + 8 * m) + BH * ((R + 63) // 64) * 4 * m * d),
-        # reverse adjoint scan with the dlog_alpha carries: fp32 contributions
+        # reverse adjoint scan with the dlog_alpha carries: bf16 contributions
         # and bf16 states in, bf16 adjoints out, K and V
-        "adj_scan": (BH * ((R + 63) // 64) * m * d * 4, BH * ((R + 63) // 64) * m * d * 16),
+        "adj_scan": (BH * ((R + 63) // 64) * m * d * 4, BH * ((R + 63) // 64) * m * d * 12),
         # RoPE(q), RoPE(k) in bf16 and the (cos, sin) table: q, k in, copies out
         "rope_qk": (0, BH * T * 4 * d * e + T * d * 4),
         "bwd_wdq_tc": wdq, "bwd_window_dq": wdq,

@@ -413,6 +413,7 @@ nha_status_t nha_backward_ex(const void* q, const void* k, const void* v, const 
     a.hdqw = (__nv_bfloat16*)a.dqw; a.hdqwV = (__nv_bfloat16*)a.dqwV;
     a.hdkw = (__nv_bfloat16*)a.dkw; a.hdvw = (__nv_bfloat16*)a.dvw;
     a.hDL = (__nv_bfloat16*)a.wsDL; a.hPL = (__nv_bfloat16*)a.wsPL;
+    a.hRK = (__nv_bfloat16*)a.RK; a.hRV = (__nv_bfloat16*)a.RV;
     a.reuse = reuse;
     a.io = state_io(ex, false);
     a.io.htb = (__nv_bfloat16*)(fws + fp.HTB);

@@ -100,6 +100,10 @@ struct BwdArgs {
     __nv_bfloat16* hdvw;
     __nv_bfloat16* hDL;
     __nv_bfloat16* hPL;
+    // bf16 path: the chunks' adjoint contributions dR_c in bf16 (aliasing RK,
+    // RV); the reverse scan carries their sum in fp32
+    __nv_bfloat16* hRK;
+    __nv_bfloat16* hRV;
     // the chunk states, gate totals, RoPE table and RoPE(q), RoPE(k) above are
     // the forward's, left in its workspace: the backward does not recompute them
     bool reuse;

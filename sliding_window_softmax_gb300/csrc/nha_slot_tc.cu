@@ -61,7 +61,9 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
-    const int x = blockIdx.x, bh = blockIdx.y;
+    // heads fastest, tiles in decreasing order: the window-only leading tiles
+    // (a copy each) start last
+    const int bh = blockIdx.x, x = gridDim.y - 1 - blockIdx.y;
     const Shape sh = head_shape(a.sh, bh);
     const int W0 = sh.T - sh.R, NLT = (W0 + 127) / 128;
     if (x >= NLT + (sh.R + 127) / 128) return;  // past this head's tiles (per-head windows)
@@ -314,14 +316,17 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
                 }
             }
             __syncthreads();
-            for (int e = tid; e < 2 * 2 * M * 8; e += kTcThreads) {  // (array, row n < 2M, 16-byte chunk)
-                const int arr = e / (2 * M * 8), n = (e / 8) % (2 * M), ch = e % 8;
+            for (int e = tid; e < 2 * 2 * M * 4; e += kTcThreads) {  // (array, row n < 2M, 8 columns)
+                const int arr = e / (2 * M * 4), n = (e / 4) % (2 * M), ch = e % 4;
                 const int cc = n / M, i = n % M;
                 if (cc == 0 || has2) {
-                    const int sw = (4 * ch + 4 * (n & 7)) & 31;
-                    const float4 val = *reinterpret_cast<const float4*>(slab + arr * 4096 + n * 32 + sw);
-                    float* dst = (arr == 0 ? a.RK : a.RV) + (((size_t)bh * sh.NCS + c1 + cc) * M + i) * D + c0 + 4 * ch;
-                    *reinterpret_cast<float4*>(dst) = val;
+                    const float* src = slab + arr * 4096 + n * 32;
+                    const float4 lo = *reinterpret_cast<const float4*>(src + ((8 * ch + 4 * (n & 7)) & 31));
+                    const float4 hi = *reinterpret_cast<const float4*>(src + ((8 * ch + 4 + 4 * (n & 7)) & 31));
+                    __nv_bfloat16* dst =
+                        (arr == 0 ? a.hRK : a.hRV) + (((size_t)bh * sh.NCS + c1 + cc) * M + i) * D + c0 + 8 * ch;
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16(lo.x, lo.y), pack_bf16(lo.z, lo.w),
+                                                                pack_bf16(hi.x, hi.y), pack_bf16(hi.z, hi.w));
                 }
             }
             __syncthreads();
@@ -431,7 +436,9 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = ((warp & 3) << 5) | lane, h = warp >> 2, cr = r >> 6;
-    const int x = blockIdx.x, bh = blockIdx.y;
+    // heads fastest, key tiles in increasing order: the tiles past the last
+    // state row (a copy each) start last
+    const int bh = blockIdx.x, x = blockIdx.y;
     const Shape sh = head_shape(a.sh, bh);
     const size_t hoff = (size_t)bh * sh.TS;
     const int sbase = x * 128, nk = min(128, sh.T - sbase);
@@ -745,7 +752,7 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sq_smem<D, M>())) != cudaSuccess)
             return e;
         if (qtiles > 0)
-            NHA_LAUNCH("bwd_sq_tc", st, kern<<<dim3(qtiles, sh.BH), kTcThreads, sq_smem<D, M>(), st>>>(a, maps, status));
+            NHA_LAUNCH("bwd_sq_tc", st, kern<<<dim3(sh.BH, qtiles), kTcThreads, sq_smem<D, M>(), st>>>(a, maps, status));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // queries t < w reading initial states: their slot part of D and dq
         if ((e = launch_h0_bwd_lead<__nv_bfloat16, D, M>(a, true, st)) != cudaSuccess) return e;
@@ -776,7 +783,7 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk_smem<D, M>())) != cudaSuccess)
             return e;
         NHA_LAUNCH("bwd_sk_tc", st,
-                   kern<<<dim3((sh.T + 127) / 128, sh.BH), kTcThreads, sk_smem<D, M>(), st>>>(a, maps, status));
+                   kern<<<dim3(sh.BH, (sh.T + 127) / 128), kTcThreads, sk_smem<D, M>(), st>>>(a, maps, status));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return launch_dh0<__nv_bfloat16, D, M>(a, st);

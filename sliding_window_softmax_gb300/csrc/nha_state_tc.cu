@@ -272,12 +272,13 @@ state_scan_tc_kernel(const __grid_constant__ StateMaps maps, const float* __rest
     if (warp == 0) tmem_dealloc(tm, 128);
 }
 
-constexpr int kAdjDepth = 8, kAdjWarps = 2;
+constexpr int kAdjDepth = 7, kAdjWarps = 2;
 
 // Reverse chunk scan of the slot adjoints, fused with the dlog_alpha carry.
 // R_c, the adjoint carried into chunk c from the later chunks, follows
 // R_{c - 1} = exp(G_c) R_c + dR_c (dR_c: the chunk's own contribution, from the
-// query-side kernel); it is written in bf16 for the key-side kernel.  The carry
+// query-side kernel in bf16; the sum is carried in fp32); it is written in
+// bf16 for the key-side kernel.  The carry
 // of chunk c, sum_d R_c[i][d] S_prev(c + 1)[i][d] over K and V (the bf16
 // states; for the last chunk the final state, present only with its
 // gradient), is the total over all later rows of the gate gradient that every
@@ -288,13 +289,13 @@ constexpr int kAdjDepth = 8, kAdjWarps = 2;
 // the K and the V adjoint, so the carry is a warp sum and no barrier is
 // needed.  Each lane streams its own pieces of the next kAdjDepth chunks
 // (contributions, states, the decay and the db1 entry) into its own shared
-// memory stages with cp.async; a CTA of two warps needs about 25 KB and 64
-// threads, so it fits beside a key-major window CTA on one SM and the scan
-// runs in that kernel's shadow on the side stream.
+// memory stages with cp.async; a CTA of two warps needs about 15 KB and 64
+// threads, so two fit beside a key-major window CTA (d = 128) on one SM and
+// the scan runs in that kernel's shadow on the side stream.
 template <int D>
 struct AdjStage {
     static constexpr int PL = D / 32;
-    float xk[32 * PL], xv[32 * PL];            // dR_c, K and V
+    __nv_bfloat16 xk[32 * PL], xv[32 * PL];    // dR_c, K and V
     __nv_bfloat16 sk[32 * PL], sv[32 * PL];    // S_prev(c + 1), K and V
     float g, db;                               // exp(G_c) of the slot, db1 entry of the chunk's last row
     float pad[2];
@@ -302,7 +303,8 @@ struct AdjStage {
 
 template <int D>
 __global__ void __launch_bounds__(32 * kAdjWarps)
-adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, const __nv_bfloat16* __restrict__ SK,
+adj_scan_kernel(const __nv_bfloat16* __restrict__ RK, const __nv_bfloat16* __restrict__ RV,
+                const __nv_bfloat16* __restrict__ SK,
                 const __nv_bfloat16* __restrict__ SV, const float* __restrict__ G, __nv_bfloat16* __restrict__ RKb,
                 __nv_bfloat16* __restrict__ RVb, float* __restrict__ db1, const float* __restrict__ dhTk,
                 const float* __restrict__ dhTv, const __nv_bfloat16* __restrict__ htb, float* __restrict__ rend,
@@ -340,13 +342,13 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
                 sval = has_dhT;
             }
             if constexpr (PL == 4) {
-                cp_async16(st.xk + e0, RK + o, true);
-                cp_async16(st.xv + e0, RV + o, true);
+                cp_async8(st.xk + e0, RK + o, true);
+                cp_async8(st.xv + e0, RV + o, true);
                 cp_async8(st.sk + e0, sk, sval);
                 cp_async8(st.sv + e0, sv, sval);
             } else {
-                cp_async8(st.xk + e0, RK + o, true);
-                cp_async8(st.xv + e0, RV + o, true);
+                cp_async4(st.xk + e0, RK + o, true);
+                cp_async4(st.xv + e0, RV + o, true);
                 cp_async4(st.sk + e0, sk, sval);
                 cp_async4(st.sv + e0, sv, sval);
             }
@@ -393,8 +395,8 @@ adj_scan_kernel(const float* __restrict__ RK, const float* __restrict__ RV, cons
         if (lane == 0 && (c + 1 < NC || has_dhT)) db1[db_at(c)] = st.db + t;
 #pragma unroll
         for (int e = 0; e < PL; e++) {
-            rk[e] = g * rk[e] + st.xk[e0 + e];
-            rv[e] = g * rv[e] + st.xv[e0 + e];
+            rk[e] = g * rk[e] + __bfloat162float(st.xk[e0 + e]);
+            rv[e] = g * rv[e] + __bfloat162float(st.xv[e0 + e]);
         }
         issue(c - NP);  // into the stage just read (this lane's own pieces)
     }
@@ -422,14 +424,19 @@ cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st) {
     const unsigned grid = (unsigned)((warps + kAdjWarps - 1) / kAdjWarps);
     if (D == 128) {
         const size_t sm = sizeof(AdjStage<128>) * kAdjDepth * kAdjWarps;
+        // all of the SM's memory as shared memory, the configuration of the
+        // key-major kernel its CTAs run beside
+        cudaError_t e = cudaFuncSetAttribute(adj_scan_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
         NHA_LAUNCH("adj_scan", st,
-                   adj_scan_kernel<128><<<grid, 32 * kAdjWarps, sm, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb,
+                   adj_scan_kernel<128><<<grid, 32 * kAdjWarps, sm, st>>>(a.hRK, a.hRV, a.SKb, a.SVb, a.G, a.RKb, a.RVb,
                                                                           a.wsDB1, a.dhTk, a.dhTv, a.io.htb, a.rend,
                                                                           sh, M));
     } else {
         const size_t sm = sizeof(AdjStage<64>) * kAdjDepth * kAdjWarps;
         NHA_LAUNCH("adj_scan", st,
-                   adj_scan_kernel<64><<<grid, 32 * kAdjWarps, sm, st>>>(a.RK, a.RV, a.SKb, a.SVb, a.G, a.RKb, a.RVb,
+                   adj_scan_kernel<64><<<grid, 32 * kAdjWarps, sm, st>>>(a.hRK, a.hRV, a.SKb, a.SVb, a.G, a.RKb, a.RVb,
                                                                          a.wsDB1, a.dhTk, a.dhTv, a.io.htb, a.rend,
                                                                          sh, M));
     }
