@@ -355,10 +355,9 @@ nha_status_t nha_decode_prefill(const void* k, const void* v, const float* log_a
 
 /* ---- Forward without device allocation (the pages have no counterpart) ----
  *
- * Some callers cannot allocate device memory: code that runs while a CUDA
- * graph is being captured, plugins that receive only their input and output
- * buffers from a host framework, or processes whose device memory belongs to
- * an allocator they may not call.  nha_forward_noalloc is nha_forward with
+ * Some callers cannot allocate device memory: plugins that receive only
+ * their input and output buffers from a host framework, or processes whose
+ * device memory belongs to an allocator they may not call.  nha_forward_noalloc is nha_forward with
  * its workspace taken from a fixed scratch array of NHA_NOALLOC_SCRATCH_BYTES
  * compiled into the library (every GPU that loads the library keeps that
  * array until the process exits).  It allocates and frees nothing.
@@ -370,8 +369,7 @@ nha_status_t nha_decode_prefill(const void* k, const void* v, const float* log_a
  * hand against NHA_NOALLOC_SCRATCH_BYTES.
  * Set-up: the first call on a device (and the first call after that device's
  * context was replaced, e.g. by cudaDeviceReset) looks up the scratch's
- * device address in the current context (cudaGetSymbolAddress); make that
- * call before any stream capture.
+ * device address in the current context (cudaGetSymbolAddress).
  * Sharing: all calls use the same scratch, which keeps the last call's
  * contents (the forward overwrites every part it reads, so nothing has to
  * start at zero).  Calls whose execution overlaps on the GPU (different

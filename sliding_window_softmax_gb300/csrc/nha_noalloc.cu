@@ -1,8 +1,7 @@
 // nha_forward_noalloc: the forward with its scratch in a fixed device array
 // compiled into the library, for callers that must not allocate device memory
-// (code running inside a CUDA-graph capture or under an allocator that is
-// owned by someone else, or plugins that receive only input and output
-// buffers from their host).  The operation itself is nha_forward's.
+// (code under an allocator that is owned by someone else, or plugins that
+// receive only input and output buffers from their host).  The operation itself is nha_forward's.
 #include <cudaTypedefs.h>
 
 #include <mutex>

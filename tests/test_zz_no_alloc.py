@@ -1,8 +1,8 @@
 """The forward entry point that allocates nothing (nha_forward_noalloc).
 
-It serves callers that cannot allocate device memory -- code running while a
-CUDA graph is captured, plugins that are handed only their input and output
-buffers, processes whose device memory belongs to another allocator.  It
+It serves callers that cannot allocate device memory -- plugins that are
+handed only their input and output buffers, processes whose device memory
+belongs to another allocator.  It
 takes its workspace from a fixed scratch array compiled into the library.
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.
