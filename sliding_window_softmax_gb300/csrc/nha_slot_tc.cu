@@ -428,8 +428,12 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
     unsigned char* XR = XB + TB;      // [Rc pair]  (2M rows)
     unsigned char* XM1 = XR + SSZ;
     unsigned char* XM2 = XM1 + 32768;
-    float* s_tot = reinterpret_cast<float*>(XM2 + 32768);  // [4][M]
+    float* s_tot = reinterpret_cast<float*>(XM2 + 32768);  // [4][M]; exp(G / 2) [2][M] during the passes
     float* sG = s_tot + 4 * M;                              // [2][M]
+    // d = 64 leaves room for both window partials (dk, dv rows of the tile)
+    // from the start; d = 128 brings each into XM1 once its masks are consumed
+    constexpr bool kPreP = D == 64;
+    unsigned char* XP = reinterpret_cast<unsigned char*>(((uintptr_t)(sG + 2 * M) + 1023) & ~(uintptr_t)1023);
     __shared__ uint64_t bar, lbar, ebar, dbar, gbar;  // MMAs; pass operands; window partials; db1; log_alpha + dL
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -512,6 +516,15 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         for (int xx = 0; xx < D; xx += 64)
             tma_load_3d(XM1 + xx * 256, pass == 0 ? &maps.dkw : &maps.dvw, xx, sbase, bh, &ebar);
     };
+    if (kPreP && tid == 0) {  // both partials at once, into XP (one phase of ebar)
+        e_issued++;
+        mbar_arrive_expect_tx(&ebar, 2 * TB);
+#pragma unroll
+        for (int xx = 0; xx < D; xx += 64) {
+            tma_load_3d(XP + xx * 256, &maps.dkw, xx, sbase, bh, &ebar);
+            tma_load_3d(XP + TB + xx * 256, &maps.dvw, xx, sbase, bh, &ebar);
+        }
+    }
     if (tid == 0) {  // log_alpha rows into XM1 (free until the first masks), sigma dL into XW
         g_issued = true;
         mbar_arrive_expect_tx(&gbar, (uint32_t)(((M + 31) / 32) * 16384 + 16384));
@@ -527,17 +540,21 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
     }
     float l[HM], b[HM];
     row_gates_tile<M>(XM1, slot_ok, l, b, s_tot, sG, warp, lane, h, r, nc);
-    // bq = b - rho (rho = G / 2) is all the passes need of b; exp(G - rho) = exp(rho)
-    // comes back from the chunk totals in shared memory when it is used
+    // bq = b - rho (rho = G / 2) is all the passes need of b; exp(G - rho) =
+    // exp(rho), one value per chunk and slot, is formed once into s_tot (free
+    // until the closing suffix sum)
+    if (tid < 2 * M) s_tot[tid] = fexp(0.5f * sG[tid]);
     const float* Grow = sG + cr * M + h * HM;
+    const float* EGrow = s_tot + cr * M + h * HM;
 #pragma unroll
     for (int jj = 0; jj < HM; jj++) b[jj] -= 0.5f * Grow[jj];
+    __syncthreads();
     {
         float ek[HM], eke[HM], z[HM];
 #pragma unroll
         for (int jj = 0; jj < HM; jj++) {
             ek[jj] = slot_ok ? fexp(-b[jj]) * one_minus_exp(l[jj]) : 0.0f;
-            eke[jj] = ek[jj] * fexp(0.5f * Grow[jj]);
+            eke[jj] = ek[jj] * EGrow[jj];
             z[jj] = 0.0f;
         }
         store_row(XE, r, h * HM, ek, HM);
@@ -613,7 +630,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
             ok = false;
             break;
         }
-        issue_partial(pass);
+        if (!kPreP) issue_partial(pass);
         if (pass == 0) issue_loads(1);  // the operand tiles are free: next pass in flight
         if (pass == 1 && tid == 0) {    // db1 rows of the tile for the gate gradient, into XA
             const int nrows = min(128, sh.NC * kChunk - sbase);
@@ -626,14 +643,17 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
             tmem_ld(tl + R0 + h * HM, intra, HM);
 #pragma unroll
             for (int jj = 0; jj < HM; jj++)
-                du[jj] += fexp(-b[jj]) * (intra[jj] + fexp(0.5f * Grow[jj]) * inter[jj]);
+                du[jj] += fexp(-b[jj]) * (intra[jj] + EGrow[jj] * inter[jj]);
         }
-        // dk (dv) = window partial + slot part, staged in XM2, written by TMA
-        if (mbar_wait(&ebar, (uint32_t)pass, kWaitCycles)) {
-            if (tid == 0) e_waited++;
-        } else {
-            atomicExch(&s_abort, 1);
+        // dk (dv) = window partial + slot part, staged in XM2 and copied out
+        if (!kPreP || pass == 0) {
+            if (mbar_wait(&ebar, kPreP ? 0u : (uint32_t)pass, kWaitCycles)) {
+                if (tid == 0) e_waited++;
+            } else {
+                atomicExch(&s_abort, 1);
+            }
         }
+        const unsigned char* part = kPreP ? XP + pass * TB : XM1;
 #pragma unroll
         for (int c0 = 0; c0 < HD; c0 += 32) {
             float g[32];
@@ -642,7 +662,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
             for (int e = 0; e < 32; e += 8) {
                 const uint32_t off = sw_chunk(r, (h * HD + c0 + e) >> 3, 128);
                 float f[8];
-                unpack8(*reinterpret_cast<const uint4*>(XM1 + off), f);
+                unpack8(*reinterpret_cast<const uint4*>(part + off), f);
 #pragma unroll
                 for (int q = 0; q < 8; q++) f[q] += g[e + q];
                 *reinterpret_cast<uint4*>(XM2 + off) = pack8(f);
@@ -723,8 +743,9 @@ size_t sq_smem() {
 }
 template <int D, int M>
 size_t sk_smem() {
-    return 1024 + 2 * 16384 + 32768 + 2 * 128 * D * 2 + ((2 * M * D * 2) + 1023) / 1024 * 1024 + 2 * 32768 +
-           6 * M * 4;
+    const size_t base = 1024 + 2 * 16384 + 32768 + 2 * 128 * D * 2 + ((2 * M * D * 2) + 1023) / 1024 * 1024 +
+                        2 * 32768 + 6 * M * 4;
+    return D == 64 ? (base + 1023) / 1024 * 1024 + 2 * 128 * D * 2 : base;  // + the two window partials
 }
 
 template <int D, int M>
