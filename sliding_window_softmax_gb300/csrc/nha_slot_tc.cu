@@ -411,7 +411,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
 
 // ---------------------------------------------------------------------------------------
 struct SkMaps {
-    CUtensorMap q, dout, k, v, rk, rv, dkw, dvw, la, dl, pl;
+    CUtensorMap q, dout, k, v, rk, rv, dkw, dvw, la, dl, pl, db1;
 };
 
 template <int D, int M>
@@ -467,7 +467,6 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         return;
     }
     const int c1 = sbase / kChunk;
-    const size_t jrow = (size_t)bh * sh.NCS * kChunk + s;
 
     if (tid < 2 * M) sG[tid] = 0.0f;
     if (tid == 0) {
@@ -633,10 +632,10 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         if (!kPreP) issue_partial(pass);
         if (pass == 0) issue_loads(1);  // the operand tiles are free: next pass in flight
         if (pass == 1 && tid == 0) {    // db1 rows of the tile for the gate gradient, into XA
-            const int nrows = min(128, sh.NC * kChunk - sbase);
-            d_issued = true;
-            mbar_arrive_expect_tx(&dbar, (uint32_t)(nrows * M * 4));
-            bulk_load(XA, a.wsDB1 + (jrow - r) * M, (uint32_t)(nrows * M * 4), &dbar);
+            d_issued = true;             // (32-column boxes, 128-byte swizzle, like log_alpha)
+            mbar_arrive_expect_tx(&dbar, (uint32_t)(((M + 31) / 32) * 16384));
+#pragma unroll
+            for (int xx = 0; xx < M; xx += 32) tma_load_3d(XA + xx * 512, &maps.db1, xx, sbase, bh, &dbar);
         }
         {
             float intra[HM];
@@ -689,10 +688,12 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         // (added by the adjoint scan), so the suffix sum hands it to every row.
         if (!mbar_wait(&dbar, 0, kWaitCycles)) atomicExch(&s_abort, 1);
         float db[HM];
-        const float* db1 = reinterpret_cast<const float*>(XA) + r * M + h * HM;
 #pragma unroll
         for (int jj = 0; jj < HM; jj += 4) {
-            const float4 d4 = slot_ok ? *reinterpret_cast<const float4*>(db1 + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int col = h * HM + jj, c = (col & 31) >> 2;
+            const float4 d4 = slot_ok ? *reinterpret_cast<const float4*>(XA + (col >> 5) * 16384 + r * 128 +
+                                                                          ((c ^ (r & 7)) << 4))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
             const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
             for (int q = 0; q < 4; q++) db[jj + q] = slot_ok ? dd[q] - one_minus_exp(l[jj + q]) * du[jj + q] : 0.0f;
@@ -798,7 +799,8 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
             (e = tmap_rows_bf16(&maps.dvw, a.hdvw, D, sh.T, sh.BH, 128)) != cudaSuccess ||
             (e = tmap_rows_f32(&maps.la, a.la, M, sh.T, sh.BH)) != cudaSuccess ||
             (e = tmap_rows_bf16(&maps.dl, a.hDL, M, ncm / M * kChunk, sh.BH, 128)) != cudaSuccess ||
-            (e = tmap_rows_bf16(&maps.pl, a.hPL, M, ncm / M * kChunk, sh.BH, 128)) != cudaSuccess)
+            (e = tmap_rows_bf16(&maps.pl, a.hPL, M, ncm / M * kChunk, sh.BH, 128)) != cudaSuccess ||
+            (e = tmap_rows_f32(&maps.db1, a.wsDB1, M, ncm / M * kChunk, sh.BH)) != cudaSuccess)
             return e;
         auto kern = bwd_sk_tc_kernel<D, M>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk_smem<D, M>())) != cudaSuccess)
