@@ -60,7 +60,8 @@ struct FwdArgs {
 
 // Backward arguments.  Workspace beyond the forward's: Dv [BH, T];
 // dqw, dkw, dvw [BH, T, D] (window-branch partial gradients, fp32);
-// wsDL, wsPL, wsDB1 [BH, NC * C, M]; RK, RV [BH, NC, M, D].
+// wsDL, wsPL, wsDB1 [BH, NC * C, M]; RK, RV [BH, NC, M, D] (the chunks' adjoint
+// contributions; the bf16 path keeps them in bf16 through hRK, hRV).
 struct BwdArgs {
     const void* q;
     const void* k;
@@ -88,7 +89,7 @@ struct BwdArgs {
     float* wsDB1;
     float* RK;
     float* RV;
-    __nv_bfloat16* SKb;  // bf16 copies of SK, SV, RK, RV (bf16 path)
+    __nv_bfloat16* SKb;  // bf16 chunk states (SKb, SVb) and carried adjoints (RKb, RVb), bf16 path
     __nv_bfloat16* SVb;
     __nv_bfloat16* RKb;
     __nv_bfloat16* RVb;
@@ -187,7 +188,7 @@ cudaError_t tc_bwd_slot(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bf
 template <int D>
 cudaError_t launch_wkv(const BwdArgs& a, const __nv_bfloat16* qr, const __nv_bfloat16* kr, const float2* tab,
                        int* status, cudaStream_t st);
-// bf16 path: reverse adjoint scan (RK, RV contributions in; RKb, RVb out) and
+// bf16 path: reverse adjoint scan (hRK, hRV contributions in; RKb, RVb out) and
 // the per-chunk dlog_alpha carry, added to wsDB1 of each chunk's last state row.
 cudaError_t launch_adj_scan(const BwdArgs& a, int M, int D, cudaStream_t st);
 // bf16 path: the chunk decays exp(G) (into G) and the states entering every
