@@ -431,10 +431,13 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
     float* s_tot = reinterpret_cast<float*>(XM2 + 32768);  // [4][M]; exp(G / 2) [2][M] during the passes
     float* sG = s_tot + 4 * M;                              // [2][M]
     // d = 64 leaves room for both window partials (dk, dv rows of the tile)
-    // from the start; d = 128 brings each into XM1 once its masks are consumed
+    // from the start; d = 128 brings each into XB as soon as the pass's first
+    // products have consumed its k (v) rows, and the second pass's v rows
+    // follow the first pass's dk
     constexpr bool kPreP = D == 64;
     unsigned char* XP = reinterpret_cast<unsigned char*>(((uintptr_t)(sG + 2 * M) + 1023) & ~(uintptr_t)1023);
-    __shared__ uint64_t bar, lbar, ebar, dbar, gbar;  // MMAs; pass operands; window partials; db1; log_alpha + dL
+    __shared__ uint64_t bar, lbar, ebar, dbar, gbar, vbar;  // MMAs; pass operands; window partials; db1;
+                                                            // log_alpha + dL; the second pass's v rows (d = 128)
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -475,6 +478,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         mbar_init(&ebar, 1);
         mbar_init(&dbar, 1);
         mbar_init(&gbar, 1);
+        mbar_init(&vbar, 1);
         mbar_fence_init();
         s_abort = 0;
     }
@@ -492,28 +496,38 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
     // pass.  Rows past the tile's states hold other tokens or zeros; every
     // product they enter is multiplied by a zero gate or masked away.
     int l_issued = 0, l_waited = 0, e_issued = 0, e_waited = 0;  // thread 0's copy bookkeeping
-    bool d_issued = false, g_issued = false, g_waited = false;
+    bool d_issued = false, g_issued = false, g_waited = false, v_issued = false, v_waited = false;
     // the second pass also brings P_L into XW (W o Eq is formed in place)
     auto issue_loads = [&](int pass) {
         if (tid != 0) return;
+        const bool with_b = kPreP || pass == 0;  // XB holds the first pass's dk at d = 128
         l_issued++;
-        mbar_arrive_expect_tx(&lbar, 2 * TB + 2 * M * D * 2 + (pass == 1 ? 16384 : 0));
+        mbar_arrive_expect_tx(&lbar, (with_b ? 2 : 1) * TB + 2 * M * D * 2 + (pass == 1 ? 16384 : 0));
 #pragma unroll
         for (int xx = 0; xx < D; xx += 64) {
             tma_load_3d(XA + xx * 256, pass == 0 ? &maps.q : &maps.dout, xx, sbase + sh.w, bh, &lbar);
-            tma_load_3d(XB + xx * 256, pass == 0 ? &maps.k : &maps.v, xx, sbase, bh, &lbar);
+            if (with_b) tma_load_3d(XB + xx * 256, pass == 0 ? &maps.k : &maps.v, xx, sbase, bh, &lbar);
             tma_load_3d(XR + xx * 4 * M, pass == 0 ? &maps.rk : &maps.rv, xx, c1 * M, bh, &lbar);
         }
         if (pass == 1) tma_load_3d(XW, &maps.pl, 0, sbase, bh, &lbar);
     };
-    // window partial dk or dv of the tile's rows into XM1 (its masks are consumed)
+    auto issue_v = [&]() {  // d = 128: the second pass's v rows into XB, once dk is out
+        if (tid != 0) return;
+        fence_async_smem();
+        v_issued = true;
+        mbar_arrive_expect_tx(&vbar, TB);
+#pragma unroll
+        for (int xx = 0; xx < D; xx += 64) tma_load_3d(XB + xx * 256, &maps.v, xx, sbase, bh, &vbar);
+    };
+    // d = 128: window partial dk or dv of the tile's rows into XB (its k or v
+    // rows are consumed by the pass's first products)
     auto issue_partial = [&](int pass) {
         if (tid != 0) return;
         e_issued++;
         mbar_arrive_expect_tx(&ebar, TB);
 #pragma unroll
         for (int xx = 0; xx < D; xx += 64)
-            tma_load_3d(XM1 + xx * 256, pass == 0 ? &maps.dkw : &maps.dvw, xx, sbase, bh, &ebar);
+            tma_load_3d(XB + xx * 256, pass == 0 ? &maps.dkw : &maps.dvw, xx, sbase, bh, &ebar);
     };
     if (kPreP && tid == 0) {  // both partials at once, into XP (one phase of ebar)
         e_issued++;
@@ -571,6 +585,13 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
             } else {
                 atomicExch(&s_abort, 1);
             }
+            if (!kPreP) {
+                if (mbar_wait(&vbar, 0, kWaitCycles)) {
+                    if (tid == 0) v_waited = true;
+                } else {
+                    atomicExch(&s_abort, 1);
+                }
+            }
         }
         {
             float weq[HM];
@@ -609,6 +630,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
             mma_commit(&bar);
         }
         if (!(ok = ctl.wait())) break;
+        if (!kPreP) issue_partial(pass);  // k (v) rows consumed
         mask_to_tile(tl + R0, XM1, r, h, cr, slot_ok, true);
         mask_to_tile(tl + R1, XM2, r, h, cr, slot_ok, true);
         float inter[HM];
@@ -629,7 +651,6 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
             ok = false;
             break;
         }
-        if (!kPreP) issue_partial(pass);
         if (pass == 0) issue_loads(1);  // the operand tiles are free: next pass in flight
         if (pass == 1 && tid == 0) {    // db1 rows of the tile for the gate gradient, into XA
             d_issued = true;             // (32-column boxes, 128-byte swizzle, like log_alpha)
@@ -652,7 +673,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
                 atomicExch(&s_abort, 1);
             }
         }
-        const unsigned char* part = kPreP ? XP + pass * TB : XM1;
+        const unsigned char* part = kPreP ? XP + pass * TB : XB;
 #pragma unroll
         for (int c0 = 0; c0 < HD; c0 += 32) {
             float g[32];
@@ -672,6 +693,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
             ok = false;
             break;
         }
+        if (!kPreP && pass == 0) issue_v();  // dk read out of XB
         {  // rows [0, nk) of the staged tile, 16-byte chunks, coalesced
             constexpr int CH = D / 8;
             __nv_bfloat16* ob = (__nv_bfloat16*)(pass == 0 ? a.dk : a.dv) + (hoff + sbase) * D;
@@ -729,6 +751,7 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
         for (int q = l_waited; q < l_issued; q++) mbar_wait(&lbar, (uint32_t)(q & 1), kWaitCycles);
         for (int q = e_waited; q < e_issued; q++) mbar_wait(&ebar, (uint32_t)(q & 1), kWaitCycles);
         if (d_issued) mbar_wait(&dbar, 0, kWaitCycles);
+        if (v_issued && !v_waited) mbar_wait(&vbar, 0, kWaitCycles);
         if (g_issued && !g_waited) mbar_wait(&gbar, 0, kWaitCycles);
         atomicOr(status, kStatusTimeoutBit);
     }
