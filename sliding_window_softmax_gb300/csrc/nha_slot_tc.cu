@@ -55,6 +55,11 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
     float* s_tot = reinterpret_cast<float*>(XG + 32768);  // [4][M]
     float* sG = s_tot + 4 * M;                             // [2][M]
     float* red = sG + 2 * M;                               // [2][128]
+    // d = 64 leaves room for both window partials of dq, fetched once the
+    // tile's first operand tiles have landed; d = 128 brings each into a tile
+    // its products have consumed
+    constexpr bool kPreP = D == 64;
+    unsigned char* XP = reinterpret_cast<unsigned char*>(((uintptr_t)(red + 256) + 1023) & ~(uintptr_t)1023);
     __shared__ uint64_t bar, lbar, ebar[2], gbar;  // MMAs; operand tiles; the two window partials; log_alpha
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -207,6 +212,15 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
         sync_for_mma();
         if (tid == 0) {
             wait_copies(&lbar, l_waited);
+            if (kPreP) {  // both dq partials at once, into XP (one phase of ebar[0])
+                e_issued++;
+                mbar_arrive_expect_tx(&ebar[0], 2 * TB);
+#pragma unroll
+                for (int xx = 0; xx < D; xx += 64) {
+                    tma_load_3d(XP + xx * 256, &maps.dqw, xx, tbase, bh, &ebar[0]);
+                    tma_load_3d(XP + TB + xx * 256, &maps.dqwv, xx, tbase, bh, &ebar[0]);
+                }
+            }
             fence_after_sync();
             const uint32_t sq = smem_u32(XQ), sk = smem_u32(XKV), ss = smem_u32(XS);
             for (int kk = 0; kk < D / 16; kk++)
@@ -293,7 +307,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
         ok = ctl.wait() && !s_abort;
     }
     if (ok) {
-        if (tid == 0) {  // dout consumed: the window partial dq goes in flight into its tile
+        if (!kPreP && tid == 0) {  // dout consumed: the window partial dq goes in flight into its tile
             e_issued++;
             mbar_arrive_expect_tx(&ebar[0], TB);
 #pragma unroll
@@ -345,7 +359,7 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
         ok = ctl.wait();
     }
     if (ok) {
-        if (tid == 0) {  // G1 consumed: the dq correction partial goes in flight into its tile
+        if (!kPreP && tid == 0) {  // G1 consumed: the dq correction partial goes in flight into its tile
             e_issued++;
             mbar_arrive_expect_tx(&ebar[1], TB);
 #pragma unroll
@@ -367,8 +381,10 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
         const float corr = Dhat_r - D_r;
         if (tid == 0) {
             wait_partial(0);
-            wait_partial(1);
+            if (!kPreP) wait_partial(1);
         }
+        const unsigned char* pq = kPreP ? XP : XdO;      // window partial dq
+        const unsigned char* pc = kPreP ? XP + TB : XG;  // its D correction partial
         ok = !__syncthreads_or(s_abort);
         if (ok) {
 #pragma unroll
@@ -379,8 +395,8 @@ bwd_sq_tc_kernel(const BwdArgs a, const __grid_constant__ SqMaps maps, int* __re
                 for (int e = 0; e < 32; e += 8) {
                     const uint32_t off = sw_chunk(r, (h * HD + c0 + e) >> 3, 128);
                     float f[8], c8[8];
-                    unpack8(*reinterpret_cast<const uint4*>(XdO + off), f);
-                    unpack8(*reinterpret_cast<const uint4*>(XG + off), c8);
+                    unpack8(*reinterpret_cast<const uint4*>(pq + off), f);
+                    unpack8(*reinterpret_cast<const uint4*>(pc + off), c8);
 #pragma unroll
                     for (int q = 0; q < 8; q++) f[q] += g[e + q] + corr * c8[q];
                     *reinterpret_cast<uint4*>(XM + off) = pack8(f);
@@ -762,8 +778,9 @@ bwd_sk_tc_kernel(const BwdArgs a, const __grid_constant__ SkMaps maps, int* __re
 
 template <int D, int M>
 size_t sq_smem() {
-    return 1024 + 16384 + 3 * 128 * D * 2 + ((2 * M * D * 2) + 1023) / 1024 * 1024 + 2 * 32768 + 6 * M * 4 +
-           256 * 4;
+    const size_t base = 1024 + 16384 + 3 * 128 * D * 2 + ((2 * M * D * 2) + 1023) / 1024 * 1024 + 2 * 32768 +
+                        6 * M * 4 + 256 * 4;
+    return D == 64 ? (base + 1023) / 1024 * 1024 + 2 * 128 * D * 2 : base;  // + the two dq partials
 }
 template <int D, int M>
 size_t sk_smem() {
